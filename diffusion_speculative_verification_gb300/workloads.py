@@ -1,0 +1,315 @@
+"""Seeded synthetic inputs for the verification pass and the acceptance step.
+
+This module only *draws* inputs; it holds none of the method's arithmetic
+(no mask, no RoPE, no attention, no acceptance rule).  Both the CUDA path
+(through the bindings) and the CPU oracle consume exactly the arrays made
+here, so a parity test compares the two on identical bytes.
+
+Shapes follow the five named workloads of the verification problem:
+
+* ``tiny``     1 sequence, 1 head, head_dim 64, fp32, 16 cached prompt keys,
+               block width B=4; acceptance over a 256-token vocabulary with
+               logits ~ N(0, 2) (variance 2), T=0 and T=1 Gumbel.
+* ``gqa1p7b``  8 sequences, 16 q / 8 kv heads, head_dim 128, bf16, 1024
+               cached keys, B=8; greedy acceptance over 151936 tokens, gamma=8.
+* ``gqa8b``    16 sequences, 32 q / 8 kv heads, 4096 cached keys, B=32;
+               rejection sampling at T=1 with gamma=16, draft logits =
+               target logits + N(0, 0.5^2).
+* ``prefill``  4 sequences, 32 q / 8 kv heads, 8192 fresh prompt rows under
+               a causal mask plus a B=16 paired tail, no cache.
+* ``sweep``    64 sequences, 32 q / 8 kv heads, cache length ~ U[256, 8192],
+               B drawn from {4, 8, 16, 32} per sequence; coupled-noise
+               acceptance over 151936 tokens at T in {0, 1, 1.5}.
+
+Generator: numpy PCG64 seeded per workload; normals by numpy's fp32
+standard normal (scaled in fp32); bf16 values are fp32 draws rounded to nearest-even.  Uniforms that
+the acceptance rule consumes (u for accept tests, u' for the emitted sample)
+and the Gumbel table G = -log(-log U), U in the open interval (0, 1), are
+drawn here and passed to both sides as inputs.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List, Optional
+
+import numpy as np
+
+F32 = "f32"
+BF16 = "bf16"
+
+MODE_ARGMAX = 0
+MODE_GUMBEL = 1
+MODE_REJECT = 2
+MODE_NAMES = {"argmax": MODE_ARGMAX, "gumbel": MODE_GUMBEL, "reject": MODE_REJECT}
+
+#: Per-sequence record, same field order as ``ssv_seq`` in include/ssv.h.
+SEQ_FIELDS = ("cache_len", "new_len", "block", "q_off", "kv_off", "tau_off")
+
+
+# --------------------------------------------------------------------------
+# bf16 helpers (storage format only)
+# --------------------------------------------------------------------------
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (nearest-even); returns the uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def values_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 values of a stored array (bf16 bits or fp32)."""
+    if dtype == BF16:
+        return bf16_bits_to_f32(arr).astype(np.float64)
+    return np.asarray(arr, dtype=np.float32).astype(np.float64)
+
+
+def _store(x32: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_bf16_bits(x32) if dtype == BF16 else np.ascontiguousarray(x32, dtype=np.float32)
+
+
+def _normal(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def open_uniform(rng: np.random.Generator, shape) -> np.ndarray:
+    """fp64 uniforms strictly inside (0, 1): (k + 0.5) / 2^53."""
+    k = rng.integers(0, 1 << 53, size=shape, dtype=np.uint64)
+    return (k.astype(np.float64) + 0.5) * (1.0 / float(1 << 53))
+
+
+def gumbel_table(rng: np.random.Generator, rows: int, V: int) -> np.ndarray:
+    """Gumbel(0,1) noise table, fp64 transform rounded to fp32, row by row."""
+    out = np.empty((rows, V), dtype=np.float32)
+    for r in range(rows):
+        u = open_uniform(rng, V)
+        out[r] = (-np.log(-np.log(u))).astype(np.float32)
+    return out
+
+
+def uniform01_f32(rng: np.random.Generator, shape) -> np.ndarray:
+    """fp32 uniforms in [0, 1) on a 2^-24 grid (exactly representable)."""
+    return (rng.integers(0, 1 << 24, size=shape, dtype=np.int64).astype(np.float64) / float(1 << 24)).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# layout
+# --------------------------------------------------------------------------
+def seq_table(cache_lens, new_lens, blocks) -> np.ndarray:
+    """int32 [batch, 6] table of ``ssv_seq`` records with packed offsets."""
+    cache_lens = np.asarray(cache_lens, np.int64)
+    new_lens = np.asarray(new_lens, np.int64)
+    blocks = np.asarray(blocks, np.int64)
+    batch = len(blocks)
+    rows = new_lens + 2 * blocks
+    t = np.zeros((batch, 6), np.int32)
+    t[:, 0] = cache_lens
+    t[:, 1] = new_lens
+    t[:, 2] = blocks
+    t[:, 3] = np.concatenate([[0], np.cumsum(rows)[:-1]]) if batch else []
+    t[:, 4] = np.concatenate([[0], np.cumsum(cache_lens)[:-1]]) if batch else []
+    t[:, 5] = np.concatenate([[0], np.cumsum(blocks)[:-1]]) if batch else []
+    return t
+
+
+def random_tau(rng: np.random.Generator, B: int) -> np.ndarray:
+    """Stage map: a uniformly random permutation of 1..B (slot k -> stage tau[k])."""
+    return (rng.permutation(B) + 1).astype(np.int32)
+
+
+@dataclasses.dataclass
+class AttnInputs:
+    name: str
+    dtype: str
+    Hq: int
+    Hkv: int
+    d: int
+    rope_base: float
+    seqs: np.ndarray          # int32 [batch, 6]
+    tau: np.ndarray           # int32 [sum B], 1..B per sequence
+    q_raw: np.ndarray         # [rows, Hq, d]  (pre-RoPE), bf16 bits or fp32
+    k_new_raw: np.ndarray     # [rows, Hkv, d] (pre-RoPE)
+    v_new: np.ndarray         # [rows, Hkv, d]
+    k_cache: np.ndarray       # [sum C, Hkv, d] (already rotated by the caller)
+    v_cache: np.ndarray       # [sum C, Hkv, d]
+
+    @property
+    def batch(self) -> int:
+        return int(self.seqs.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.q_raw.shape[0])
+
+    @property
+    def total_cache(self) -> int:
+        return int(self.k_cache.shape[0])
+
+
+@dataclasses.dataclass
+class AcceptInputs:
+    name: str
+    mode: int
+    T: float
+    V: int
+    logits_dtype: str
+    blocks: np.ndarray        # int32 [batch]
+    gammas: np.ndarray        # int32 [batch], 0 <= gamma <= B
+    slot_off: np.ndarray      # int32 [batch], first slot of each sequence
+    tau: np.ndarray           # int32 [sum B]
+    logits: np.ndarray        # [sum B, V] target logits of the mask slots, slot order
+    draft_logits: Optional[np.ndarray]   # [sum B, V] fp32 (reject mode)
+    draft_tokens: np.ndarray  # int32 [sum B], draft token of each slot
+    noise: Optional[np.ndarray]          # [n_noise, V] fp32 Gumbel table (gumbel mode)
+    noise_row: np.ndarray     # int32 [sum B], table row per slot
+    u_accept: np.ndarray      # fp32 [sum B], uniforms for the accept tests
+    u_sample: np.ndarray      # fp32 [batch], uniform for the emitted sample
+
+    @property
+    def batch(self) -> int:
+        return int(self.blocks.shape[0])
+
+
+# --------------------------------------------------------------------------
+# generators
+# --------------------------------------------------------------------------
+def make_attn_inputs(name: str, cache_lens, new_lens, blocks, Hq: int, Hkv: int, d: int,
+                     dtype: str, seed: int, rope_base: float = 10000.0) -> AttnInputs:
+    rng = np.random.default_rng(seed)
+    seqs = seq_table(cache_lens, new_lens, blocks)
+    rows = int(np.sum(np.asarray(new_lens) + 2 * np.asarray(blocks)))
+    total_c = int(np.sum(cache_lens))
+    tau = np.concatenate([random_tau(rng, int(b)) for b in blocks]).astype(np.int32) \
+        if len(blocks) else np.zeros(0, np.int32)
+    q = _store(_normal(rng, (rows, Hq, d)), dtype)
+    kn = _store(_normal(rng, (rows, Hkv, d)), dtype)
+    vn = _store(_normal(rng, (rows, Hkv, d)), dtype)
+    kc = _store(_normal(rng, (total_c, Hkv, d)), dtype)
+    vc = _store(_normal(rng, (total_c, Hkv, d)), dtype)
+    return AttnInputs(name, dtype, Hq, Hkv, d, rope_base, seqs, tau, q, kn, vn, kc, vc)
+
+
+PLANT_LOGIT = 40.0
+
+
+def make_accept_inputs(name: str, mode: int, T: float, V: int, blocks, gammas, seed: int,
+                       logits_dtype: str = F32, logit_std: float = 2.0 ** 0.5,
+                       draft_noise_std: float = 0.5, tau: Optional[np.ndarray] = None) -> AcceptInputs:
+    """Acceptance inputs with planted agreement.
+
+    For each sequence a cut stage c is drawn uniformly in 1..gamma+1.  Greedy
+    and coupled-noise modes: at stages before c the draft token's target
+    logit is raised to PLANT_LOGIT, which makes it the winner with
+    overwhelming probability; other stages carry uniform random draft tokens.
+    Reject mode: at stages before c the draft row is an exact copy of the
+    target row (ratio exactly 1), later stages use target + N(0, 0.5^2).
+    Planting only shapes the distribution of accepted lengths; both sides
+    compute the outcome from the same bytes.
+    """
+    rng = np.random.default_rng(seed)
+    blocks = np.asarray(blocks, np.int32)
+    gammas = np.asarray(gammas, np.int32)
+    batch = len(blocks)
+    S = int(blocks.sum())
+    slot_off = np.concatenate([[0], np.cumsum(blocks)[:-1]]).astype(np.int32) if batch else np.zeros(0, np.int32)
+    if tau is None:
+        tau = np.concatenate([random_tau(rng, int(b)) for b in blocks]).astype(np.int32) if batch else np.zeros(0, np.int32)
+    logits32 = np.empty((S, V), np.float32)
+    for r in range(S):
+        logits32[r] = _normal(rng, V, logit_std)
+    draft_tokens = rng.integers(0, V, size=S).astype(np.int32)
+    draft32 = None
+    if mode == MODE_REJECT:
+        draft32 = np.empty((S, V), np.float32)
+    for b in range(batch):
+        B, g, off = int(blocks[b]), int(gammas[b]), int(slot_off[b])
+        cut = int(rng.integers(1, g + 2))
+        slot_of_stage = np.empty(B, np.int64)
+        slot_of_stage[tau[off:off + B] - 1] = np.arange(B)
+        for s in range(1, B + 1):
+            k = off + int(slot_of_stage[s - 1])
+            if mode == MODE_REJECT:
+                if s < cut:
+                    draft32[k] = logits32[k]
+                else:
+                    draft32[k] = logits32[k] + _normal(rng, V, draft_noise_std)
+            elif s < cut:
+                logits32[k, draft_tokens[k]] = PLANT_LOGIT
+    logits = _store(logits32, logits_dtype)
+    noise = None
+    noise_row = np.zeros(S, np.int32)
+    if mode == MODE_GUMBEL:
+        noise_row = rng.permutation(S).astype(np.int32)
+        noise = gumbel_table(rng, S, V)
+    u_accept = uniform01_f32(rng, S)
+    u_sample = uniform01_f32(rng, batch)
+    return AcceptInputs(name, mode, float(T), V, logits_dtype, blocks, gammas, slot_off, tau,
+                        logits, draft32, draft_tokens, noise, noise_row, u_accept, u_sample)
+
+
+# --------------------------------------------------------------------------
+# named workloads
+# --------------------------------------------------------------------------
+VOCAB = 151936
+
+WORKLOADS: Dict[str, dict] = {
+    "tiny": dict(batch=1, Hq=1, Hkv=1, d=64, dtype=F32, seed=1001,
+                 accept=[("argmax", 0.0), ("gumbel", 1.0)], V=256, gamma="B"),
+    "gqa1p7b": dict(batch=8, Hq=16, Hkv=8, d=128, dtype=BF16, seed=1002,
+                    accept=[("argmax", 0.0)], V=VOCAB, gamma="B"),
+    "gqa8b": dict(batch=16, Hq=32, Hkv=8, d=128, dtype=BF16, seed=1003,
+                  accept=[("reject", 1.0)], V=VOCAB, gamma=16),
+    "prefill": dict(batch=4, Hq=32, Hkv=8, d=128, dtype=BF16, seed=1004,
+                    accept=[], V=VOCAB, gamma="B"),
+    "sweep": dict(batch=64, Hq=32, Hkv=8, d=128, dtype=BF16, seed=1005,
+                  accept=[("gumbel", 0.0), ("gumbel", 1.0), ("gumbel", 1.5)], V=VOCAB, gamma="B"),
+}
+
+
+def workload_lengths(name: str, seed: Optional[int] = None):
+    """(cache_lens, new_lens, blocks) of a named workload."""
+    w = WORKLOADS[name]
+    seed = w["seed"] if seed is None else seed
+    b = w["batch"]
+    if name == "tiny":
+        return [16], [0], [4]
+    if name == "gqa1p7b":
+        return [1024] * b, [0] * b, [8] * b
+    if name == "gqa8b":
+        return [4096] * b, [0] * b, [32] * b
+    if name == "prefill":
+        return [0] * b, [8192] * b, [16] * b
+    if name == "sweep":
+        rng = np.random.default_rng(seed + 7919)
+        cache = rng.integers(256, 8192 + 1, size=b).tolist()
+        blocks = rng.choice([4, 8, 16, 32], size=b).tolist()
+        return cache, [0] * b, blocks
+    raise KeyError(name)
+
+
+def workload_attn(name: str, seed: Optional[int] = None) -> AttnInputs:
+    w = WORKLOADS[name]
+    seed = w["seed"] if seed is None else seed
+    c, n, b = workload_lengths(name, seed)
+    return make_attn_inputs(name, c, n, b, w["Hq"], w["Hkv"], w["d"], w["dtype"], seed)
+
+
+def workload_gammas(name: str, blocks) -> List[int]:
+    g = WORKLOADS[name]["gamma"]
+    return [int(x) if g == "B" else min(int(g), int(x)) for x in blocks]
+
+
+def workload_accept(name: str, which: int = 0, seed: Optional[int] = None,
+                    tau: Optional[np.ndarray] = None) -> AcceptInputs:
+    w = WORKLOADS[name]
+    seed = w["seed"] if seed is None else seed
+    mode_name, T = w["accept"][which]
+    _, _, blocks = workload_lengths(name, seed)
+    return make_accept_inputs(f"{name}/{mode_name}/T={T}", MODE_NAMES[mode_name], T, w["V"], blocks,
+                              workload_gammas(name, blocks), seed + 100 * (which + 1), tau=tau)
