@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the verification pass on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch of the named workload:
+ssv_rope_copy (paired RoPE index) -> ssv_verify_attn (temporal-mask
+attention over prompt cache + 2B tail) -> ssv_accept (longest accepted
+prefix).  Inputs are seeded and synthetic (shapes of the named workload),
+resident in HBM before timing; every step is preceded by a 256 MB memset
+so that no input starts in the 129 MB L2, and each step is bracketed by
+CUDA events on the launching stream (the memset is outside the events).
+
+Prints one JSON line (rank 0).  `value` = algorithmic HBM bytes of one step
+(rope read+write, KV cache once per kv head + Q + K/V_new + O, every
+logits / noise / draft row the acceptance needs) / device step time.
+`e2e` repeats the measurement through the same public calls with the
+inputs copied from pinned host memory every step and the accepted tokens
+read back.  `roofline` is for the dominant op (largest device time).
+
+--impl reference times the CPU oracle (plain numpy fp64) on the machine's host
+cores, one sequence of the workload per step, same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from diffusion_speculative_verification_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verify-attn TFLOP/s or HBM GB/s (% of roofline); accept sequences/s"
+ACCEPT_INDEX = {"tiny": 1, "gqa1p7b": 0, "gqa8b": 0, "prefill": None, "sweep": 1}
+FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work
+# ---------------------------------------------------------------------------
+def attn_work(a: W.AttnInputs, out_bytes: int):
+    es = 2 if a.dtype == W.BF16 else 4
+    rows, Hq, Hkv, d = a.total_rows, a.Hq, a.Hkv, a.d
+    pairs = 0.0
+    for C, N, B, *_ in a.seqs:
+        C, N, B = float(C), float(N), float(B)
+        P = C + N
+        pairs += N * (N + 1) / 2 + N * C + 2 * B * P + B * (B + 1) / 2 + B * B
+    flops = pairs * Hq * 4.0 * d
+    bytes_ = (a.total_cache * Hkv * d * 2 * es + rows * Hq * d * es + rows * Hkv * d * 2 * es
+              + rows * Hq * d * out_bytes)
+    return float(bytes_), float(flops)
+
+
+def rope_bytes(a: W.AttnInputs) -> float:
+    es = 2 if a.dtype == W.BF16 else 4
+    return 2.0 * a.total_rows * (a.Hq + a.Hkv) * a.d * es
+
+
+def accept_bytes(x) -> float:
+    if x is None:
+        return 0.0
+    les = 2 if x.logits_dtype == W.BF16 else 4
+    tot = 0.0
+    for B, g in zip(x.blocks, x.gammas):
+        need = min(int(g) + 1, int(B))
+        tot += need * x.V * les
+        if x.mode == W.MODE_REJECT:
+            tot += int(g) * x.V * les
+        if x.mode == W.MODE_GUMBEL and x.T != 0.0:
+            tot += need * x.V * 4
+    return tot
+
+
+def kernel_launches(x) -> int:
+    n = 1 + 1  # rope, verify attention
+    if x is not None:
+        n += 2 if x.mode == W.MODE_REJECT else 1
+    return n
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._th = threading.Thread(target=self._read, daemon=True)
+        self._th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._th.join(timeout=2)
+        sel = [l for (t, l) in self.lines if self.t0 - 0.1 <= t <= self.t1 + 0.1] or [l for _, l in self.lines[-3:]]
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in sel:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle, one sequence per step
+# ---------------------------------------------------------------------------
+def _subset(a: W.AttnInputs, x, b: int):
+    """Sequence b of the workload as a 1-sequence batch (attention and acceptance inputs)."""
+    C, N, B, q_off, kv_off, t_off = (int(v) for v in a.seqs[b])
+    rows = N + 2 * B
+    sa = W.AttnInputs(a.name, a.dtype, a.Hq, a.Hkv, a.d, a.rope_base, W.seq_table([C], [N], [B]),
+                      a.tau[t_off:t_off + B].copy(), a.q_raw[q_off:q_off + rows], a.k_new_raw[q_off:q_off + rows],
+                      a.v_new[q_off:q_off + rows], a.k_cache[kv_off:kv_off + C], a.v_cache[kv_off:kv_off + C])
+    sx = None
+    if x is not None:
+        so = int(x.slot_off[b])
+        sl = slice(so, so + B)
+        nrow = x.noise_row[sl]
+        sx = W.AcceptInputs(x.name, x.mode, x.T, x.V, x.logits_dtype, x.blocks[b:b + 1], x.gammas[b:b + 1],
+                            np.zeros(1, np.int32), x.tau[sl], x.logits[sl],
+                            None if x.draft_logits is None else x.draft_logits[sl], x.draft_tokens[sl],
+                            None if x.noise is None else x.noise[np.sort(nrow)],
+                            np.argsort(np.argsort(nrow)).astype(np.int32), x.u_accept[sl], x.u_sample[b:b + 1])
+    return sa, sx
+
+
+def oracle_step(sa: W.AttnInputs, sx):
+    import oracle.rope as orope
+    import oracle.attention as oattn
+    import oracle.accept as oacc
+    q, k = orope.rope_copy_batch(sa.seqs, W.values_f64(sa.q_raw, sa.dtype), W.values_f64(sa.k_new_raw, sa.dtype),
+                                 sa.rope_base)
+    oattn.verify_attention(sa.seqs, sa.tau, q, W.values_f64(sa.k_cache, sa.dtype), W.values_f64(sa.v_cache, sa.dtype),
+                           k, W.values_f64(sa.v_new, sa.dtype))
+    if sx is not None:
+        oacc.accept_batch(sx)
+
+
+def seq_bytes(sa, sx, out_bytes):
+    return rope_bytes(sa) + attn_work(sa, out_bytes)[0] + accept_bytes(sx)
+
+
+def _cpu_baseline_child(config, seconds, q):
+    a = W.workload_attn(config)
+    xi = ACCEPT_INDEX[config]
+    x = None if xi is None else W.workload_accept(config, xi)
+    out_b = 2 if a.dtype == W.BF16 else 4
+    done_bytes, n, t0 = 0.0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        sa, sx = _subset(a, x, n % a.batch)
+        oracle_step(sa, sx)
+        done_bytes += seq_bytes(sa, sx, out_b)
+        n += 1
+    dt = time.perf_counter() - t0
+    q.put((done_bytes / dt / 1e9, n, dt))
+
+
+def cpu_baseline(config: str, seconds: float = 12.0):
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = str(cores)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_cpu_baseline_child, args=(config, seconds, q))
+    p.start()
+    gbs, n, dt = q.get()
+    p.join()
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} sequences of the {config} workload (rope + attention + acceptance, numpy fp64), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    a = W.workload_attn(args.config)
+    xi = ACCEPT_INDEX[args.config]
+    x = None if xi is None else W.workload_accept(args.config, xi)
+    out_b = 2 if a.dtype == W.BF16 else 4
+    for i in range(args.warmup):
+        oracle_step(*_subset(a, x, i % a.batch))
+    tot_t, tot_b = 0.0, 0.0
+    for i in range(args.steps):
+        sa, sx = _subset(a, x, i % a.batch)
+        t0 = time.perf_counter()
+        oracle_step(sa, sx)
+        tot_t += time.perf_counter() - t0
+        tot_b += seq_bytes(sa, sx, out_b)
+    gbs = tot_b / tot_t / 1e9
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": args.config, "unit_per_step": "one sequence"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one {args.config} sequence per step, {args.steps} steps"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from diffusion_speculative_verification_gb300 import build, ssv, io as sio
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    ssv.lib()
+
+    a = W.workload_attn(args.config)
+    xi = ACCEPT_INDEX[args.config]
+    x = None if xi is None else W.workload_accept(args.config, xi)
+    t = sio.attn_to_device(a, dev)
+    acc = None if x is None else sio.accept_to_device(x, dev)
+    out_dtype = torch.bfloat16 if a.dtype == W.BF16 else torch.float32
+    out_b = 2 if a.dtype == W.BF16 else 4
+    qo = torch.empty_like(t["q"])
+    ko = torch.empty_like(t["k_new"])
+    o = torch.empty(t["q"].shape, dtype=out_dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    batch = t["batch"]
+    aargs = ssv.attn_args(qo, t["k_cache"], t["v_cache"], ko, t["v_new"], o, batch, t["tau"], 0.0, status)
+    ws_attn = torch.zeros(max(256, ssv.verify_attn_workspace_bytes(aargs)), dtype=torch.uint8, device=dev)
+    outs = None
+    if acc is not None:
+        outs = (torch.empty(x.batch, dtype=torch.int32, device=dev), torch.empty(x.batch, dtype=torch.int32, device=dev),
+                torch.empty(len(x.tau), dtype=torch.int32, device=dev))
+        cargs = ssv.accept_args(acc["mode"], acc["T"], acc["logits"], acc["draft_tokens"], acc["tau"], acc["block"],
+                                acc["gamma"], acc["slot_off"], *outs, acc["draft_logits"], acc["noise"],
+                                acc["noise_row"], acc["u_accept"], acc["u_sample"], acc["max_block"], status)
+        ws_acc = torch.zeros(ssv.accept_workspace_bytes(cargs), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    L = ssv.lib()
+    import ctypes as C
+    sp = stream.cuda_stream
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        ssv.rope_copy(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko, stream=stream)
+        if evs:
+            evs[1].record(stream)
+        r = L.ssv_verify_attn(C.byref(aargs), ws_attn.data_ptr(), ws_attn.numel(), sp)
+        if r:
+            raise ssv.SsvError(r, "ssv_verify_attn")
+        if evs:
+            evs[2].record(stream)
+        if acc is not None:
+            r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), sp)
+            if r:
+                raise ssv.SsvError(r, "ssv_accept")
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert ssv.get_status(status) == ssv.SSV_OK
+
+    props = torch.cuda.get_device_properties(dev)
+    clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    assert ssv.get_status(status) == ssv.SSV_OK
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
+    step_ms = per.sum(axis=1)
+    tot_ms = float(step_ms.sum())
+    if world > 1:
+        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tot_ms = float(tt.item())
+
+    rb = rope_bytes(a)
+    ab, af = attn_work(a, out_b)
+    cb = accept_bytes(x)
+    step_bytes = rb + ab + cb
+    ms_step = tot_ms / args.steps
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    op_ms = per.mean(axis=0)
+    hbm_peak, tf_peak, peak_kind = load_peaks()
+    ops = {"rope": (op_ms[0], rb), "verify_attn": (op_ms[1], ab), "accept": (op_ms[2], cb)}
+    dom = max(ops, key=lambda k: ops[k][0])
+    ach = ops[dom][1] / (ops[dom][0] * 1e-3) / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind}
+    if dom == "verify_attn" and args.config == "prefill":
+        tfs = af / (op_ms[1] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(tfs / tf_peak, 4), "traffic": None, "peak_kind": peak_kind}
+
+    # ---- end to end: host inputs -> device, run, tokens back -------------------
+    e2e = run_e2e(args, a, x, t, acc, outs if acc is not None else None, o, dev, stream, step, out_b)
+
+    line = None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": a.dtype, "data": "synthetic (seeded)",
+            "config": {"workload": args.config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d,
+                       "l2": "256 MB memset before every step", "parallelism": f"replicas x{world}"},
+            "verify_attn": {"us": round(op_ms[1] * 1e3, 2), "gbs": round(ab / (op_ms[1] * 1e-3) / 1e9, 1),
+                            "tflops": round(af / (op_ms[1] * 1e-3) / 1e12, 2), "bytes": ab, "flops": af},
+            "rope": {"us": round(op_ms[0] * 1e3, 2), "gbs": round(rb / (op_ms[0] * 1e-3) / 1e9, 1), "bytes": rb},
+            "accept": None if x is None else {"us": round(op_ms[2] * 1e3, 2),
+                                              "gbs": round(cb / (op_ms[2] * 1e-3) / 1e9, 1), "bytes": cb,
+                                              "seq_per_s": round(world * x.batch / (op_ms[2] * 1e-3), 1)},
+            "seq_per_s": round(world * a.batch / (ms_step * 1e-3), 1),
+            "roofline": roof,
+            "gpu_launches": kernel_launches(x) * args.steps,
+            "clocks": clk,
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(args.config)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):
+    """Same calls, inputs copied from pinned host memory every step, results read back."""
+    import torch
+    names = ["q", "k_new", "v_new", "k_cache", "v_cache", "tau"]
+    host = {k: t[k].cpu().pin_memory() for k in names}
+    dev_bufs = {k: t[k] for k in names}
+    host["seqs"] = t["batch"].dev.cpu().pin_memory()
+    dev_bufs["seqs"] = t["batch"].dev
+    if acc is not None:
+        for k in ("logits", "draft_tokens", "tau", "block", "gamma", "slot_off", "noise_row", "u_accept", "u_sample",
+                  "draft_logits", "noise"):
+            if acc[k] is not None:
+                host["acc_" + k] = acc[k].cpu().pin_memory()
+                dev_bufs["acc_" + k] = acc[k]
+        results = list(outs)
+    else:
+        results = [o]
+    results_host = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in results_host)
+    steps = max(1, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for i in range(steps + 2):
+        if i == 2:
+            torch.cuda.synchronize()
+            e0.record(stream)
+        for k, h in host.items():
+            dev_bufs[k].copy_(h, non_blocking=True)
+        step()
+        for r, rh in zip(results, results_host):
+            rh.copy_(r, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    step_bytes = rope_bytes(a) + attn_work(a, out_b)[0] + accept_bytes(x)
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=list(W.WORKLOADS), default="gqa1p7b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,29 @@
+// Verify-attention launch parameters shared by the SIMT and tensor-core
+// schedules, and the host entry points of each schedule.
+#pragma once
+
+#include "ssv_internal.cuh"
+
+namespace ssv {
+
+struct AttnParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  void* o;
+  ssv_dtype in_dtype, out_dtype;
+  int Hq, Hkv, d;
+  float scale;  // softmax scale (1/sqrt(d) unless given)
+  const ssv_seq* seqs;
+  int batch;
+  const int32_t* tau;
+  int total_rows, total_cache, total_slots;
+  int max_cache, max_new, max_block;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);
+
+}  // namespace ssv

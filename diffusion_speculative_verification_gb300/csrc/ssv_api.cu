@@ -1,0 +1,111 @@
+// Host side of libssv: argument validation, schedule selection for the
+// verification attention, status handling.
+#include "ssv_internal.cuh"
+#include "attn.cuh"
+
+#include <math.h>
+#include <string.h>
+
+using namespace ssv;
+
+namespace {
+
+ssv_status attn_check(const ssv_attn_args* a) {
+  if (!a) return SSV_ERR_INVALID;
+  if (a->batch < 0 || a->total_rows < 0 || a->total_cache < 0 || a->total_slots < 0) return SSV_ERR_INVALID;
+  if (a->Hq <= 0 || a->Hkv <= 0 || a->Hq % a->Hkv != 0) return SSV_ERR_INVALID;
+  if (a->d != 64 && a->d != 128) return SSV_ERR_UNSUPPORTED;
+  if (a->in_dtype != SSV_F32 && a->in_dtype != SSV_BF16) return SSV_ERR_INVALID;
+  if (a->out_dtype != SSV_F32 && a->out_dtype != SSV_BF16) return SSV_ERR_INVALID;
+  if (a->in_dtype == SSV_F32 && a->out_dtype != SSV_F32) return SSV_ERR_UNSUPPORTED;
+  if (a->max_block < 1 || a->max_block > 64 || a->max_cache < 0 || a->max_new < 0) return SSV_ERR_INVALID;
+  if (!isfinite(a->scale) || a->scale < 0.f) return SSV_ERR_INVALID;
+  if (a->batch == 0 || a->total_rows == 0) return SSV_OK;
+  if (!a->q || !a->k_new || !a->v_new || !a->o || !a->seqs || !a->tau) return SSV_ERR_INVALID;
+  if (a->total_cache > 0 && (!a->k_cache || !a->v_cache)) return SSV_ERR_INVALID;
+  const uintptr_t al = (uintptr_t)a->q | (uintptr_t)a->k_cache | (uintptr_t)a->v_cache | (uintptr_t)a->k_new |
+                       (uintptr_t)a->v_new | (uintptr_t)a->o;
+  if (al & 15u) return SSV_ERR_INVALID;
+  return SSV_OK;
+}
+
+AttnParams to_params(const ssv_attn_args* a) {
+  AttnParams p;
+  p.q = a->q;
+  p.k_cache = a->k_cache;
+  p.v_cache = a->v_cache;
+  p.k_new = a->k_new;
+  p.v_new = a->v_new;
+  p.o = a->o;
+  p.in_dtype = a->in_dtype;
+  p.out_dtype = a->out_dtype;
+  p.Hq = a->Hq;
+  p.Hkv = a->Hkv;
+  p.d = a->d;
+  p.scale = a->scale > 0.f ? a->scale : (float)(1.0 / sqrt((double)a->d));
+  p.seqs = a->seqs;
+  p.batch = a->batch;
+  p.tau = a->tau;
+  p.total_rows = a->total_rows;
+  p.total_cache = a->total_cache;
+  p.total_slots = a->total_slots;
+  p.max_cache = a->max_cache;
+  p.max_new = a->max_new;
+  p.max_block = a->max_block;
+  p.dev_status = a->dev_status;
+  return p;
+}
+
+}  // namespace
+
+extern "C" ssv_status ssv_verify_attn_workspace(const ssv_attn_args* a, size_t* bytes) {
+  if (!bytes) return SSV_ERR_INVALID;
+  const ssv_status st = attn_check(a);
+  if (st != SSV_OK) return st;
+  *bytes = 256;
+  return SSV_OK;
+}
+
+extern "C" ssv_status ssv_verify_attn(const ssv_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const ssv_status st = attn_check(a);
+  if (st != SSV_OK) return st;
+  if (a->batch == 0 || a->total_rows == 0) return SSV_OK;
+  size_t need = 0;
+  ssv_verify_attn_workspace(a, &need);
+  if (need > 0 && (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need)) return SSV_ERR_WORKSPACE;
+  const AttnParams p = to_params(a);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_attn_simt(p, s);
+  return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
+}
+
+extern "C" ssv_status ssv_get_status(int32_t* dev_status, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!dev_status) {
+    return cudaStreamSynchronize(s) == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
+  }
+  int32_t h = 0;
+  if (cudaMemcpyAsync(&h, dev_status, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SSV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SSV_ERR_CUDA;
+  if (h != 0) {
+    if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), s) != cudaSuccess) return SSV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSV_ERR_CUDA;
+  }
+  return static_cast<ssv_status>(h);
+}
+
+extern "C" const char* ssv_status_string(ssv_status s) {
+  switch (s) {
+    case SSV_OK: return "ok";
+    case SSV_ERR_INVALID: return "invalid argument";
+    case SSV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SSV_ERR_CUDA: return "CUDA error";
+    case SSV_ERR_TIMEOUT: return "bounded device wait ran out";
+    case SSV_ERR_BAD_TAU: return "stage map is not a permutation of 1..B";
+    case SSV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SSV_ERR_NOT_FINITE: return "temperature not finite or negative";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* ssv_version(void) { return "ssv 0.1 sm_103a"; }

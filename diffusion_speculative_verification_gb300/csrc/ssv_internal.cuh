@@ -1,0 +1,93 @@
+// Internal helpers shared by the libssv translation units (device + host).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/ssv.h"
+
+namespace ssv {
+
+// ---------------------------------------------------------------------------
+// status
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* dev_status, int32_t code) {
+  if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// element conversion
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ float to_f32(float x) { return x; }
+  static __device__ __forceinline__ float from_f32(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+// ---------------------------------------------------------------------------
+// sequence lookup: sequences are packed in increasing q_off order
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int find_seq_by_row(const ssv_seq* seqs, int batch, int row) {
+  int lo = 0, hi = batch - 1, ans = -1;
+  while (lo <= hi) {
+    int mid = (lo + hi) >> 1;
+    if (seqs[mid].q_off <= row) { ans = mid; lo = mid + 1; } else { hi = mid - 1; }
+  }
+  return ans;
+}
+
+__device__ __forceinline__ int find_seq_by_slot(const int32_t* slot_off, int batch, int slot) {
+  int lo = 0, hi = batch - 1, ans = -1;
+  while (lo <= hi) {
+    int mid = (lo + hi) >> 1;
+    if (slot_off[mid] <= slot) { ans = mid; lo = mid + 1; } else { hi = mid - 1; }
+  }
+  return ans;
+}
+
+// ---------------------------------------------------------------------------
+// temporal attention rule on the 2B tail keys (SimSD summary, section 2).
+// r, t in [0, 2B): rows/keys D_1..D_B then D~_1..D~_B; tau_r / tau_t are the
+// stages of their slots.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool tail_allowed(int r, int t, int B, int tau_r, int tau_t) {
+  const bool row_mask = r >= B;
+  const bool key_mask = t >= B;
+  if (!row_mask) return !key_mask && tau_t <= tau_r;      // data row: revealed data only
+  return key_mask ? (tau_t >= tau_r) : (tau_t < tau_r);   // mask row
+}
+
+// Checks that tau[0..B) is a permutation of 1..B.  Executed by one warp
+// (all 32 lanes must call); returns the same answer on every lane.
+__device__ __forceinline__ bool warp_tau_is_permutation(const int32_t* tau, int B) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long seen = 0ull;
+  bool ok = true;
+  for (int j = lane; j < B; j += 32) {
+    int t = tau[j];
+    if (t < 1 || t > B) ok = false; else seen |= 1ull << (t - 1);
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    seen |= __shfl_xor_sync(0xffffffffu, seen, o);
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  const unsigned long long full = (B >= 64) ? ~0ull : ((1ull << B) - 1ull);
+  return ok && seen == full;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace ssv
+
+#define SSV_CUDA_CHECK(expr)                                   \
+  do {                                                         \
+    cudaError_t e_ = (expr);                                   \
+    if (e_ != cudaSuccess) return SSV_ERR_CUDA;                \
+  } while (0)

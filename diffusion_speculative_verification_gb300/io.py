@@ -1,0 +1,74 @@
+"""Moves seeded workload arrays (numpy) into torch tensors and back."""
+from __future__ import annotations
+
+import numpy as np
+
+from . import workloads as W
+from .ssv import Batch
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def tensor(arr: np.ndarray, dtype: str, device, pin: bool = False):
+    """numpy storage (bf16 bit patterns or fp32) -> torch tensor of that dtype."""
+    torch = _torch()
+    if dtype == W.BF16:
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    if pin:
+        return t.pin_memory()
+    return t.to(device)
+
+
+def to_numpy_storage(t) -> np.ndarray:
+    """torch tensor -> numpy storage (bf16 as uint16 bit patterns)."""
+    torch = _torch()
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def int_tensor(arr, device):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.int32)).to(device)
+
+
+def f32_tensor(arr, device):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+def attn_to_device(a: W.AttnInputs, device="cuda") -> dict:
+    return dict(
+        batch=Batch(a.seqs, device),
+        tau=int_tensor(a.tau, device),
+        q=tensor(a.q_raw, a.dtype, device),
+        k_new=tensor(a.k_new_raw, a.dtype, device),
+        v_new=tensor(a.v_new, a.dtype, device),
+        k_cache=tensor(a.k_cache, a.dtype, device),
+        v_cache=tensor(a.v_cache, a.dtype, device),
+    )
+
+
+def accept_to_device(x: W.AcceptInputs, device="cuda") -> dict:
+    d = dict(
+        mode=x.mode, T=x.T,
+        logits=tensor(x.logits, x.logits_dtype, device),
+        draft_tokens=int_tensor(x.draft_tokens, device),
+        tau=int_tensor(x.tau, device),
+        block=int_tensor(x.blocks, device),
+        gamma=int_tensor(x.gammas, device),
+        slot_off=int_tensor(x.slot_off, device),
+        noise_row=int_tensor(x.noise_row, device),
+        u_accept=f32_tensor(x.u_accept, device),
+        u_sample=f32_tensor(x.u_sample, device),
+        max_block=int(np.max(x.blocks)) if len(x.blocks) else 1,
+    )
+    d["draft_logits"] = None if x.draft_logits is None else tensor(x.draft_logits, x.logits_dtype, device)
+    d["noise"] = None if x.noise is None else f32_tensor(x.noise, device)
+    return d

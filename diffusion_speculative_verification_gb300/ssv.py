@@ -1,0 +1,246 @@
+"""ctypes binding of libssv (include/ssv.h).  Argument marshalling only:
+every step of the verification pass runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.
+
+The library is loaded from this package's ``lib/libssv.so`` (built in-tree
+by ``build.build()``).  If it is missing every call raises ``SsvError``;
+there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import numpy as np
+
+from .build import LIB
+
+SSV_OK, SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_CUDA = 0, 1, 2, 3
+SSV_ERR_TIMEOUT, SSV_ERR_BAD_TAU, SSV_ERR_WORKSPACE, SSV_ERR_NOT_FINITE = 4, 5, 6, 7
+SSV_F32, SSV_BF16 = 0, 1
+ARGMAX, GUMBEL, REJECT = 0, 1, 2
+
+#: every symbol include/ssv.h declares
+EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
+           "ssv_accept", "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
+
+
+class SsvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} (code {code})")
+
+
+class SeqC(C.Structure):
+    _fields_ = [("cache_len", C.c_int32), ("new_len", C.c_int32), ("block", C.c_int32),
+                ("q_off", C.c_int32), ("kv_off", C.c_int32), ("tau_off", C.c_int32)]
+
+
+class RopeArgs(C.Structure):
+    _fields_ = [("q_in", C.c_void_p), ("k_in", C.c_void_p), ("q_out", C.c_void_p), ("k_out", C.c_void_p),
+                ("dtype", C.c_int), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32),
+                ("base", C.c_double), ("seqs", C.c_void_p), ("batch", C.c_int32), ("total_rows", C.c_int32)]
+
+
+class AttnArgs(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("k_new", C.c_void_p),
+                ("v_new", C.c_void_p), ("o", C.c_void_p), ("in_dtype", C.c_int), ("out_dtype", C.c_int),
+                ("Hq", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float),
+                ("seqs", C.c_void_p), ("batch", C.c_int32), ("tau", C.c_void_p), ("total_rows", C.c_int32),
+                ("total_cache", C.c_int32), ("total_slots", C.c_int32), ("max_cache", C.c_int32),
+                ("max_new", C.c_int32), ("max_block", C.c_int32), ("dev_status", C.c_void_p)]
+
+
+class AcceptArgs(C.Structure):
+    _fields_ = [("mode", C.c_int), ("T", C.c_float), ("V", C.c_int32), ("batch", C.c_int32),
+                ("total_slots", C.c_int32), ("max_block", C.c_int32), ("logits_dtype", C.c_int),
+                ("logits", C.c_void_p), ("draft_logits", C.c_void_p), ("draft_tokens", C.c_void_p),
+                ("tau", C.c_void_p), ("block", C.c_void_p), ("gamma", C.c_void_p), ("slot_off", C.c_void_p),
+                ("noise", C.c_void_p), ("n_noise_rows", C.c_int32), ("noise_row", C.c_void_p),
+                ("u_accept", C.c_void_p), ("u_sample", C.c_void_p), ("n_acc", C.c_void_p),
+                ("n_out", C.c_void_p), ("tokens", C.c_void_p), ("dev_status", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libssv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise SsvError(SSV_ERR_UNSUPPORTED, f"libssv not built ({LIB} missing; run __graft_entry__.build())")
+        L = C.CDLL(LIB)
+        vp, sz = C.c_void_p, C.c_size_t
+        L.ssv_rope_copy.argtypes = [C.POINTER(RopeArgs), vp]
+        L.ssv_verify_attn_workspace.argtypes = [C.POINTER(AttnArgs), C.POINTER(sz)]
+        L.ssv_verify_attn.argtypes = [C.POINTER(AttnArgs), vp, sz, vp]
+        L.ssv_accept_workspace.argtypes = [C.POINTER(AcceptArgs), C.POINTER(sz)]
+        L.ssv_accept.argtypes = [C.POINTER(AcceptArgs), vp, sz, vp]
+        L.ssv_get_status.argtypes = [vp, vp]
+        L.ssv_status_string.argtypes = [C.c_int]
+        L.ssv_status_string.restype = C.c_char_p
+        L.ssv_version.restype = C.c_char_p
+        L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
+        for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
+                     "ssv_accept", "ssv_get_status", "ssv_bench"):
+            getattr(L, name).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().ssv_status_string(int(code)).decode()
+    except SsvError:
+        return "libssv unavailable"
+
+
+def version() -> str:
+    return lib().ssv_version().decode()
+
+
+def _check(code: int, what: str):
+    if code != SSV_OK:
+        raise SsvError(code, what)
+
+
+# ---------------------------------------------------------------------------
+# torch plumbing
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SSV_F32
+    if t.dtype == torch.bfloat16:
+        return SSV_BF16
+    raise SsvError(SSV_ERR_INVALID, f"unsupported dtype {t.dtype}")
+
+
+class Batch:
+    """A packed batch: host ssv_seq table + device copy + the bounds the library needs."""
+
+    def __init__(self, seqs: np.ndarray, device="cuda"):
+        torch = _torch()
+        self.host = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32).reshape(-1, 6))
+        self.dev = torch.from_numpy(self.host.copy()).to(device)
+        h = self.host
+        self.batch = int(h.shape[0])
+        self.total_rows = int(np.sum(h[:, 1] + 2 * h[:, 2])) if self.batch else 0
+        self.total_cache = int(np.sum(h[:, 0])) if self.batch else 0
+        self.total_slots = int(np.sum(h[:, 2])) if self.batch else 0
+        self.max_cache = int(h[:, 0].max()) if self.batch else 0
+        self.max_new = int(h[:, 1].max()) if self.batch else 0
+        self.max_block = int(h[:, 2].max()) if self.batch else 1
+
+
+def _workspace(nbytes: int, device, ws=None):
+    torch = _torch()
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise SsvError(SSV_ERR_WORKSPACE, "workspace")
+        return ws
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+def rope_copy(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, stream=None):
+    """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d]; returns (q_out, k_out)."""
+    q_out = q if q_out is None else q_out
+    k_out = k if k_out is None else k_out
+    a = RopeArgs(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _dtype_code(q), q.shape[1], k.shape[1], q.shape[2],
+                 float(base), _ptr(batch.dev), batch.batch, q.shape[0])
+    _check(lib().ssv_rope_copy(C.byref(a), _stream_ptr(stream)), "ssv_rope_copy")
+    return q_out, k_out
+
+
+def attn_args(q, k_cache, v_cache, k_new, v_new, out, batch: Batch, tau, scale: float = 0.0, dev_status=None):
+    return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(out),
+                    _dtype_code(q), _dtype_code(out), q.shape[1], k_new.shape[1], q.shape[2], float(scale),
+                    _ptr(batch.dev), batch.batch, _ptr(tau), batch.total_rows, batch.total_cache,
+                    batch.total_slots, batch.max_cache, batch.max_new, batch.max_block, _ptr(dev_status))
+
+
+def verify_attn_workspace_bytes(args: AttnArgs) -> int:
+    n = C.c_size_t(0)
+    _check(lib().ssv_verify_attn_workspace(C.byref(args), C.byref(n)), "ssv_verify_attn_workspace")
+    return int(n.value)
+
+
+def verify_attn(q, k_cache, v_cache, k_new, v_new, batch: Batch, tau, out=None, out_dtype=None,
+                scale: float = 0.0, workspace=None, dev_status=None, stream=None):
+    """Verification attention; returns O [rows, Hq, d]."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or q.dtype, device=q.device)
+    a = attn_args(q, k_cache, v_cache, k_new, v_new, out, batch, tau, scale, dev_status)
+    ws = _workspace(verify_attn_workspace_bytes(a), q.device, workspace)
+    _check(lib().ssv_verify_attn(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "ssv_verify_attn")
+    return out
+
+
+def accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
+                draft_logits=None, noise=None, noise_row=None, u_accept=None, u_sample=None, max_block=64,
+                dev_status=None):
+    return AcceptArgs(int(mode), float(T), logits.shape[1], block.shape[0], draft_tokens.shape[0], int(max_block),
+                      _dtype_code(logits), _ptr(logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(tau),
+                      _ptr(block), _ptr(gamma), _ptr(slot_off), _ptr(noise),
+                      0 if noise is None else noise.shape[0], _ptr(noise_row), _ptr(u_accept), _ptr(u_sample),
+                      _ptr(n_acc), _ptr(n_out), _ptr(tokens), _ptr(dev_status))
+
+
+def accept_workspace_bytes(args: AcceptArgs) -> int:
+    n = C.c_size_t(0)
+    _check(lib().ssv_accept_workspace(C.byref(args), C.byref(n)), "ssv_accept_workspace")
+    return int(n.value)
+
+
+def accept(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_logits=None, noise=None,
+           noise_row=None, u_accept=None, u_sample=None, max_block=64, workspace=None, dev_status=None,
+           stream=None, out=None):
+    """Acceptance; returns (n_acc [batch], n_out [batch], tokens [slots]) int32 device tensors."""
+    torch = _torch()
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(draft_tokens.shape[0], dtype=torch.int32, device=dev))
+    n_acc, n_out, tokens = out
+    a = accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
+                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status)
+    ws = _workspace(accept_workspace_bytes(a), dev, workspace)
+    _check(lib().ssv_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "ssv_accept")
+    return n_acc, n_out, tokens
+
+
+def get_status(dev_status, stream=None) -> int:
+    """Waits for the stream and returns (and clears) the device status word."""
+    return int(lib().ssv_get_status(_ptr(dev_status), _stream_ptr(stream)))
+
+
+def bench(config: str, iters: int = 20) -> str:
+    buf = C.create_string_buffer(4096)
+    _check(lib().ssv_bench(config.encode(), int(iters), buf, 4096), "ssv_bench")
+    return buf.value.decode()

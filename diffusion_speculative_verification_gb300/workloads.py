@@ -164,7 +164,7 @@ class AcceptInputs:
     slot_off: np.ndarray      # int32 [batch], first slot of each sequence
     tau: np.ndarray           # int32 [sum B]
     logits: np.ndarray        # [sum B, V] target logits of the mask slots, slot order
-    draft_logits: Optional[np.ndarray]   # [sum B, V] fp32 (reject mode)
+    draft_logits: Optional[np.ndarray]   # [sum B, V] same storage as logits (reject mode)
     draft_tokens: np.ndarray  # int32 [sum B], draft token of each slot
     noise: Optional[np.ndarray]          # [n_noise, V] fp32 Gumbel table (gumbel mode)
     noise_row: np.ndarray     # int32 [sum B], table row per slot
@@ -242,6 +242,7 @@ def make_accept_inputs(name: str, mode: int, T: float, V: int, blocks, gammas, s
             elif s < cut:
                 logits32[k, draft_tokens[k]] = PLANT_LOGIT
     logits = _store(logits32, logits_dtype)
+    draft = None if draft32 is None else _store(draft32, logits_dtype)
     noise = None
     noise_row = np.zeros(S, np.int32)
     if mode == MODE_GUMBEL:
@@ -250,7 +251,7 @@ def make_accept_inputs(name: str, mode: int, T: float, V: int, blocks, gammas, s
     u_accept = uniform01_f32(rng, S)
     u_sample = uniform01_f32(rng, batch)
     return AcceptInputs(name, mode, float(T), V, logits_dtype, blocks, gammas, slot_off, tau,
-                        logits, draft32, draft_tokens, noise, noise_row, u_accept, u_sample)
+                        logits, draft, draft_tokens, noise, noise_row, u_accept, u_sample)
 
 
 # --------------------------------------------------------------------------

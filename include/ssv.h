@@ -1,0 +1,261 @@
+/*
+ * ssv.h -- C ABI of libssv: the target-model verification pass of
+ * speculative decoding for block-diffusion language models, on one GB300
+ * (sm_103a).
+ *
+ * The pass (SimSD, "Simple Speculative Decoding in Diffusion Language
+ * Models", summary sections 1-4): after the prompt the target sees a data
+ * section D (B reference tokens) and a mask section D~ (B [MASK] slots);
+ * the pair (D_k, D~_k) occupies one response position.  A stage map tau,
+ * a permutation of 1..B, orders the positions in time and gates attention.
+ * One forward pass under that mask yields logits for every drafted
+ * position; acceptance then keeps the longest accepted prefix in stage
+ * order (SimSD section 4; state equality and the coupled Gumbel-noise match
+ * of the SPOT review, section "How it is used").
+ *
+ * Conventions for every entry point
+ *  - All pointers named "device" are CUDA device (or managed) addresses on
+ *    the current device; "host" pointers are ordinary CPU memory.  The
+ *    caller owns every buffer; the library allocates nothing on these
+ *    paths.  Scratch space is caller-provided ("workspace"), sized by the
+ *    matching *_workspace query, 256-byte aligned, and must be all-zero
+ *    when first used: each call leaves the zero-initialised counter area
+ *    zero again on exit.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on it.  Host-side validation errors return synchronously
+ *    and launch nothing.
+ *  - Errors found on the device (a stage map that is not a permutation, a
+ *    bounded wait that ran out, a non-finite temperature) are written to
+ *    `dev_status` (device int32, may be NULL; first error wins) and read
+ *    back with ssv_get_status().  Affected outputs are then unspecified.
+ *  - Nothing is thread-local; calls from several host threads on different
+ *    streams are safe.  Two calls whose workspaces overlap must not run
+ *    concurrently.
+ */
+#ifndef SSV_H_
+#define SSV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSV_API __attribute__((visibility("default")))
+#else
+#define SSV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSV_OK = 0,
+  SSV_ERR_INVALID = 1,      /* bad argument (null pointer, shape, alignment) */
+  SSV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim 96) */
+  SSV_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  SSV_ERR_TIMEOUT = 4,      /* a bounded on-device wait ran out */
+  SSV_ERR_BAD_TAU = 5,      /* stage map of some sequence is not a permutation of 1..B */
+  SSV_ERR_WORKSPACE = 6,    /* workspace null, misaligned or smaller than the query */
+  SSV_ERR_NOT_FINITE = 7    /* temperature not finite / negative */
+} ssv_status;
+
+typedef enum { SSV_F32 = 0, SSV_BF16 = 1 } ssv_dtype;
+
+typedef enum {
+  SSV_ACCEPT_ARGMAX = 0,    /* T = 0 state equality: accept iff draft == argmax(l) */
+  SSV_ACCEPT_GUMBEL = 1,    /* coupled noise: accept iff draft == argmax(fl(l/T) + G[row]) */
+  SSV_ACCEPT_REJECT = 2     /* standard rejection sampling, accept iff u < p(d)/q(d) */
+} ssv_accept_mode;
+
+/*
+ * One sequence of a packed batch.  Query rows of a sequence are its N fresh
+ * prompt rows followed by 2B tail rows (D_1..D_B, then D~_1..D~_B); they sit
+ * at rows [q_off, q_off + N + 2B) of Q, K_new, V_new and O.  Its C cached
+ * prompt keys sit at rows [kv_off, kv_off + C) of K_cache / V_cache.  Its
+ * stage map occupies tau[tau_off .. tau_off + B).
+ */
+typedef struct {
+  int32_t cache_len;  /* C >= 0 */
+  int32_t new_len;    /* N >= 0 */
+  int32_t block;      /* B, 1 <= B <= 64 */
+  int32_t q_off;
+  int32_t kv_off;
+  int32_t tau_off;
+} ssv_seq;
+
+/* ------------------------------------------------------------------------
+ * ssv_rope_copy -- rotary embedding with the RoPE-copy index.
+ * SimSD summary, section 3 "Position Encoding Alignment": each mask slot
+ * D~_k reuses the RoPE index of its data token D_k.
+ *
+ * Position of fresh prompt row i is C + i; of tail row r (0 <= r < 2B) it is
+ * P + (r mod B), P = C + N.  Rotate-half pairing (x_i, x_{i+d/2}) with
+ * theta_i = base^(-2i/d); angles are formed and reduced in fp64, the
+ * rotation is done in fp32 and stored in `dtype`.
+ *
+ * q_in  [total_rows, Hq, d]  device, dtype     q_out same shape (may equal q_in)
+ * k_in  [total_rows, Hkv, d] device, dtype     k_out same shape (may equal k_in)
+ * seqs  [batch] device ssv_seq.  Every row of [0, total_rows) must belong to
+ *       exactly one sequence (rows outside all sequences are left untouched).
+ * d in {64, 128}; pointers 16-byte aligned.
+ * Errors: SSV_ERR_INVALID (null, non-positive sizes, misalignment),
+ *         SSV_ERR_UNSUPPORTED (d), SSV_ERR_CUDA (launch).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* q_in;
+  const void* k_in;
+  void* q_out;
+  void* k_out;
+  ssv_dtype dtype;
+  int32_t Hq, Hkv, d;
+  double base;                 /* RoPE base, e.g. 10000 */
+  const ssv_seq* seqs;         /* device */
+  int32_t batch;
+  int32_t total_rows;
+} ssv_rope_args;
+
+SSV_API ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
+ * ssv_verify_attn -- attention of the verification pass.
+ * SimSD summary, section 2 "Temporal Attention Mask" and section 4
+ * "Verification".  For every query row and query head h (kv head h / G,
+ * G = Hq / Hkv):  O = softmax(scale * q K^T restricted to allowed keys) V.
+ * Keys of a sequence, in order: cache (C), fresh prompt (N), D_1..D_B,
+ * D~_1..D~_B.  Allowed keys:
+ *   fresh prompt row i : cache and fresh prompt keys 0 .. C+i (causal)
+ *   data row D_j       : whole prompt, D_k with tau(k) <= tau(j)  (reading;
+ *                        the pages fix only the mask-slot rule)
+ *   mask row D~_i      : whole prompt, D_j with tau(j) < tau(i),
+ *                        D~_j with tau(j) >= tau(i)
+ * The mask is derived on the device from tau; it is never stored.
+ *
+ * q       [total_rows, Hq, d]   device, in_dtype, post-RoPE
+ * k_cache [total_cache, Hkv, d] device, in_dtype, already rotated
+ * v_cache [total_cache, Hkv, d] device
+ * k_new   [total_rows, Hkv, d]  device, post-RoPE
+ * v_new   [total_rows, Hkv, d]  device
+ * o       [total_rows, Hq, d]   device, out_dtype (written for every row of
+ *                               every sequence)
+ * tau     [sum B] int32 device
+ * in_dtype: SSV_F32 (exact fp32 SIMT path) or SSV_BF16 (tensor-core path,
+ * fp32 accumulation).  out_dtype: SSV_F32 or SSV_BF16 (bf16 input only).
+ * d in {64, 128}; Hq % Hkv == 0; 1 <= B <= 64; pointers 16-byte aligned.
+ * max_cache / max_new / max_block bound every sequence's C / N / B (used to
+ * size grids and workspace).  scale 0 means 1/sqrt(d).
+ * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_WORKSPACE,
+ *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU, SSV_ERR_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  void* o;
+  ssv_dtype in_dtype;
+  ssv_dtype out_dtype;
+  int32_t Hq, Hkv, d;
+  float scale;
+  const ssv_seq* seqs;         /* device [batch] */
+  int32_t batch;
+  const int32_t* tau;          /* device [total_slots] */
+  int32_t total_rows;          /* sum of N + 2B */
+  int32_t total_cache;         /* sum of C */
+  int32_t total_slots;         /* sum of B */
+  int32_t max_cache, max_new, max_block;
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_attn_args;
+
+SSV_API ssv_status ssv_verify_attn_workspace(const ssv_attn_args* a, size_t* bytes);
+SSV_API ssv_status ssv_verify_attn(const ssv_attn_args* a, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * ssv_accept -- acceptance in temporal order, longest accepted prefix.
+ * SimSD summary section 4 "Acceptance" (rejection sampling in the draft's
+ * temporal order); SPOT review "How it is used" (state equality, exact at
+ * T = 0; coupled-noise match with one Gumbel table per absolute output
+ * position, which recovers the target distribution, Proposition 2).
+ *
+ * Per sequence b with block B, verified stages 1..gamma (0 <= gamma <= B):
+ * stage s is slot k = tau^{-1}(s).  Walk s = 1..gamma and accept while
+ *   ARGMAX : draft_tokens[k] == argmax_v l_k[v]            (ties: lowest v)
+ *   GUMBEL : draft_tokens[k] == argmax_v fl32(fl32(l_k[v]/T) + noise[noise_row[k]][v])
+ *            (IEEE fp32, no contraction; T = 0 means ARGMAX)
+ *   REJECT : u_accept[k] < p(d)/q(d), p = softmax(l_k/T), q = softmax(draft_logits_k/T)
+ * n_acc = leading accepted stages.  If c = n_acc + 1 <= B one target token
+ * is emitted at stage c: the ARGMAX/GUMBEL decision; for REJECT a sample of
+ * (p - q)_+ if c <= gamma, else of p, by inverse CDF with u_sample[b]
+ * (smallest v whose cumulative mass exceeds u_sample * total).
+ *
+ * logits       [total_slots, V] device, logits_dtype, row = slot (slot order);
+ *              only rows of stages <= min(gamma + 1, B) are read.
+ * draft_logits [total_slots, V] device, logits_dtype (REJECT only, else NULL)
+ * draft_tokens, tau, noise_row, u_accept: [total_slots] device
+ * block, gamma, slot_off, u_sample: [batch] device; slot_off[b] = first slot
+ * noise [n_noise_rows, V] fp32 device (GUMBEL with T > 0 only)
+ * Outputs: n_acc[batch], n_out[batch] (= n_acc + 1 if a token is emitted),
+ *          tokens[total_slots]: per sequence, the accepted drafts in stage
+ *          order then the emitted token, rest -1.
+ * V >= 1; T >= 0 (REJECT needs T > 0); 1 <= block <= 64.
+ * Errors: SSV_ERR_INVALID, SSV_ERR_WORKSPACE, SSV_ERR_NOT_FINITE,
+ *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  ssv_accept_mode mode;
+  float T;
+  int32_t V;
+  int32_t batch;
+  int32_t total_slots;
+  int32_t max_block;
+  ssv_dtype logits_dtype;
+  const void* logits;
+  const void* draft_logits;
+  const int32_t* draft_tokens;
+  const int32_t* tau;
+  const int32_t* block;
+  const int32_t* gamma;
+  const int32_t* slot_off;
+  const float* noise;
+  int32_t n_noise_rows;
+  const int32_t* noise_row;
+  const float* u_accept;
+  const float* u_sample;
+  int32_t* n_acc;
+  int32_t* n_out;
+  int32_t* tokens;
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_accept_args;
+
+SSV_API ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes);
+SSV_API ssv_status ssv_accept(const ssv_accept_args* a, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Status and utilities
+ * ---------------------------------------------------------------------- */
+/* Waits for `stream`, reads the device status word, resets it to 0 and
+ * returns it (SSV_OK if dev_status is NULL). */
+SSV_API ssv_status ssv_get_status(int32_t* dev_status, void* stream);
+
+SSV_API const char* ssv_status_string(ssv_status s);
+
+/* Library build identification, e.g. "ssv 0.1 sm_103a". */
+SSV_API const char* ssv_version(void);
+
+/* ------------------------------------------------------------------------
+ * ssv_bench -- native timing of the library on a named synthetic workload
+ * ("tiny", "gqa1p7b", "gqa8b", "prefill", "sweep").  Allocates its own
+ * device buffers (this is not a hot-path call), fills them with a
+ * counter-hash generator, runs `iters` timed iterations per op with an L2
+ * flush between them and writes one JSON object (median/p10/p90 times,
+ * algorithmic bytes and FLOPs) into json_out.  The DFlash review's latency
+ * model L = (T_draft + T_verify) / tau needs T_verify; this reports it.
+ * Errors: SSV_ERR_INVALID (unknown config, short buffer), SSV_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+SSV_API ssv_status ssv_bench(const char* config, int32_t iters, char* json_out, size_t json_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSV_H_ */

@@ -158,7 +158,8 @@ def accept_batch(inp) -> dict:
     Returns dict with int32 arrays n_acc [batch], n_out [batch],
     tokens [sum B] (stage order, -1 padded) and the per-sequence results.
     """
-    from_values = _logit_values(inp)
+    from_values = _logit_values(inp, inp.logits)
+    draft_values = None if inp.draft_logits is None else _logit_values(inp, inp.draft_logits)
     batch = len(inp.blocks)
     S = int(np.sum(inp.blocks))
     n_acc = np.zeros(batch, np.int32)
@@ -171,7 +172,7 @@ def accept_batch(inp) -> dict:
         noise_rows = None
         if inp.mode == MODE_GUMBEL and inp.T != 0.0:
             noise_rows = [inp.noise[int(inp.noise_row[off + k])] for k in range(B)]
-        draft_rows = None if inp.draft_logits is None else inp.draft_logits[sl]
+        draft_rows = None if draft_values is None else draft_values[sl]
         r = accept_sequence(inp.mode, inp.T, inp.tau[sl], g, inp.draft_tokens[sl], from_values[sl],
                             draft_rows, noise_rows, inp.u_accept[sl], float(inp.u_sample[b]))
         n_acc[b] = r.n_acc
@@ -181,11 +182,11 @@ def accept_batch(inp) -> dict:
     return dict(n_acc=n_acc, n_out=n_out, tokens=tokens, results=results)
 
 
-def _logit_values(inp) -> np.ndarray:
-    """Target logits as fp32 values (bf16 storage is widened exactly)."""
+def _logit_values(inp, arr) -> np.ndarray:
+    """Logits as fp32 values (bf16 storage is widened exactly)."""
     if getattr(inp, "logits_dtype", "f32") == "bf16":
-        return (np.asarray(inp.logits, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
-    return np.asarray(inp.logits, dtype=np.float32)
+        return (np.asarray(arr, np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.asarray(arr, dtype=np.float32)
 
 
 def emission_valid(res: SeqResult, v: int, rel_tol: float) -> bool:

@@ -64,7 +64,7 @@ def verify_attention(seqs: np.ndarray, tau: np.ndarray, q: np.ndarray, k_cache: 
             continue
         if local.size == 0:
             continue
-        A = verify_mask(C, N, B, tau[t_off:t_off + B])[local]
+        A = verify_mask(C, N, B, tau[t_off:t_off + B], rows=local)
         for h in range(Hq):
             kv = h // G
             keys, vals = sequence_keys(seq, k_cache, v_cache, k_new, v_new, kv)

@@ -29,32 +29,35 @@ from __future__ import annotations
 import numpy as np
 
 
-def verify_mask(C: int, N: int, B: int, tau) -> np.ndarray:
-    """uint8 [N + 2B, C + N + 2B]; 1 where query row may attend key."""
+def verify_mask(C: int, N: int, B: int, tau, rows=None) -> np.ndarray:
+    """uint8 [N + 2B, C + N + 2B]; 1 where query row may attend key.
+
+    ``rows`` optionally selects local query rows (the result then has one
+    line per selected row, in the given order).
+    """
     tau = [int(t) for t in tau]
     assert len(tau) == B and sorted(tau) == list(range(1, B + 1)), "tau must permute 1..B"
     P = C + N
-    A = np.zeros((N + 2 * B, P + 2 * B), dtype=np.uint8)
-    # fresh prompt rows: causal over cache + fresh prompt, never the tail
-    for i in range(N):
-        for key in range(C + i + 1):
-            A[i, key] = 1
-    # data rows D_j (slot j, 0-based here)
-    for j in range(B):
-        row = N + j
-        for key in range(P):
-            A[row, key] = 1
-        for k in range(B):
-            if tau[k] <= tau[j]:
-                A[row, P + k] = 1
-    # mask rows D~_i
-    for i in range(B):
-        row = N + B + i
-        for key in range(P):
-            A[row, key] = 1
-        for j in range(B):
-            if tau[j] < tau[i]:
-                A[row, P + j] = 1          # data token of an earlier stage
-            if tau[j] >= tau[i]:
-                A[row, P + B + j] = 1      # undecided mask slot
+    rows = list(range(N + 2 * B)) if rows is None else [int(r) for r in rows]
+    A = np.zeros((len(rows), P + 2 * B), dtype=np.uint8)
+    for out, row in enumerate(rows):
+        if row < N:
+            # fresh prompt row i = row: causal over cache + fresh prompt, never the tail
+            A[out, :C + row + 1] = 1
+        elif row < N + B:
+            # data row D_j (slot j, 0-based): whole prompt, earlier-or-same-stage data
+            j = row - N
+            A[out, :P] = 1
+            for k in range(B):
+                if tau[k] <= tau[j]:
+                    A[out, P + k] = 1
+        else:
+            # mask row D~_i
+            i = row - N - B
+            A[out, :P] = 1
+            for j in range(B):
+                if tau[j] < tau[i]:
+                    A[out, P + j] = 1          # data token of an earlier stage
+                if tau[j] >= tau[i]:
+                    A[out, P + B + j] = 1      # undecided mask slot
     return A

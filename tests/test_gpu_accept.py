@@ -1,0 +1,94 @@
+"""GPU parity of ssv_accept against the oracle (SimSD summary section 4;
+SPOT review, "How it is used").  Greedy and coupled-noise acceptance are
+bit-exact: both sides compare identical fp32 scores.  Rejection sampling:
+accepted lengths and accepted tokens bit-exact (every decision's margin
+exceeds the fp32 rounding band); the emitted sample equals the oracle's
+unless u'Z lies within 1e-5 Z of a CDF boundary, where the neighbour is
+also correct within rounding."""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_speculative_verification_gb300 import workloads as W, ssv
+from gpu_common import ensure_built, gpu_accept, compare_accept
+
+pytestmark = pytest.mark.gpu
+
+
+def setup_module():
+    ensure_built()
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_tiny(which):
+    x = W.workload_accept("tiny", which)
+    assert compare_accept(x, gpu_accept(x)) == 0
+
+
+def test_gqa1p7b_argmax():
+    x = W.workload_accept("gqa1p7b")
+    assert compare_accept(x, gpu_accept(x)) == 0
+
+
+def test_gqa8b_reject():
+    x = W.workload_accept("gqa8b")
+    differ = compare_accept(x, gpu_accept(x))
+    assert differ <= 2
+
+
+@pytest.fixture(scope="module")
+def sweep_inputs():
+    return W.workload_accept("sweep", 1)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0, 1.5])
+def test_sweep_gumbel(sweep_inputs, T):
+    x = sweep_inputs
+    x.T = T
+    assert compare_accept(x, gpu_accept(x)) == 0
+
+
+EDGE = {
+    "gamma0": dict(mode=W.MODE_ARGMAX, T=0.0, V=5000, blocks=[4, 1], gammas=[0, 0]),
+    "B1": dict(mode=W.MODE_GUMBEL, T=1.0, V=4097, blocks=[1, 1, 1], gammas=[1, 0, 1]),
+    "V1": dict(mode=W.MODE_ARGMAX, T=0.0, V=1, blocks=[3], gammas=[3]),
+    "B64": dict(mode=W.MODE_GUMBEL, T=0.7, V=12345, blocks=[64, 2], gammas=[64, 1]),
+    "reject_bonus": dict(mode=W.MODE_REJECT, T=1.0, V=9000, blocks=[8, 8, 4], gammas=[3, 8, 1]),
+    "reject_T07": dict(mode=W.MODE_REJECT, T=0.7, V=20000, blocks=[16] * 6, gammas=[16] * 6),
+    "bf16_logits": dict(mode=W.MODE_GUMBEL, T=1.5, V=30000, blocks=[8, 4], gammas=[8, 2], logits_dtype=W.BF16),
+    "bf16_reject": dict(mode=W.MODE_REJECT, T=1.0, V=30000, blocks=[8, 4], gammas=[5, 2], logits_dtype=W.BF16),
+}
+
+
+@pytest.mark.parametrize("name", list(EDGE))
+def test_edge_cases(name):
+    kw = dict(EDGE[name])
+    x = W.make_accept_inputs(name, kw.pop("mode"), kw.pop("T"), kw.pop("V"), kw.pop("blocks"), kw.pop("gammas"),
+                             seed=sum(map(ord, name)), **kw)
+    compare_accept(x, gpu_accept(x))
+
+
+def test_ties_resolve_to_lowest_index():
+    x = W.make_accept_inputs("ties", W.MODE_ARGMAX, 0.0, 10000, [4], [4], seed=5)
+    x.logits[:] = 0.0
+    x.logits[:, [17, 4000, 9999]] = 3.0
+    n_acc, n_out, tokens = gpu_accept(x)
+    compare_accept(x, (n_acc, n_out, tokens))
+    assert tokens[0] in (17, x.draft_tokens[np.argmin(x.tau)])
+
+
+def test_bad_tau_reports_status():
+    x = W.make_accept_inputs("bad", W.MODE_ARGMAX, 0.0, 100, [4], [4], seed=6)
+    x.tau[:] = [1, 2, 2, 4]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_accept(x, dev_status=st)
+    assert ssv.get_status(st) == ssv.SSV_ERR_BAD_TAU
+
+
+def test_repeated_calls_share_workspace():
+    """The arrival counters return to zero, so one workspace serves many calls."""
+    x = W.workload_accept("tiny", 1)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        assert compare_accept(x, gpu_accept(x, workspace=ws)) == 0
+    assert int(ws[:256].sum()) == 0
