@@ -597,3 +597,103 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
   }
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// ssv_accept_noalloc: ssv_accept with its scratch in a fixed device array.
+//
+// For callers that cannot allocate device memory themselves.  The scratch
+// lives in one file-scope array per device (kNoAllocScratchBytes, reserved
+// by every GPU that loads this library until the process exits).  Host code
+// cannot use the array's name as a device address, so the first call on each
+// device looks the address up with cudaGetSymbolAddress while that device is
+// current and caches it.  Every call shares the array: calls that overlap on
+// the GPU (other streams, other host threads) race and must be serialised by
+// the caller.  The arrival counters are cleared with a memset at each call.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kNoAllocMaxDevices] = {};
+
+ssv_status noalloc_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return SSV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return SSV_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return SSV_OK;
+}
+
+}  // namespace
+
+extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream) {
+  int nchunks = 0;
+  ssv_status st = accept_check(a, &nchunks);
+  if (st != SSV_OK) return st;
+  if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
+  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
+  if (L.total > kNoAllocScratchBytes) return SSV_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  st = noalloc_scratch_address(&scratch);
+  if (st != SSV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The counters [cnt_reduce, cnt_sample] must start at zero.
+  if (cudaMemsetAsync(scratch, 0, L.emit, s) != cudaSuccess) return SSV_ERR_CUDA;
+  char* w = static_cast<char*>(scratch);
+  AcceptParams p;
+  p.mode = a->mode;
+  p.T = a->T;
+  p.V = a->V;
+  p.batch = a->batch;
+  p.total_slots = a->total_slots;
+  p.nchunks = nchunks;
+  p.logits = a->logits;
+  p.draft_logits = a->draft_logits;
+  p.draft_tokens = a->draft_tokens;
+  p.tau = a->tau;
+  p.block = a->block;
+  p.gamma = a->gamma;
+  p.slot_off = a->slot_off;
+  p.noise = a->noise;
+  p.n_noise_rows = a->n_noise_rows;
+  p.noise_row = a->noise_row;
+  p.u_accept = a->u_accept;
+  p.u_sample = a->u_sample;
+  p.n_acc = a->n_acc;
+  p.n_out = a->n_out;
+  p.tokens = a->tokens;
+  p.dev_status = a->dev_status;
+  p.cnt_reduce = reinterpret_cast<int32_t*>(w + L.cnt_reduce);
+  p.cnt_sample = reinterpret_cast<int32_t*>(w + L.cnt_sample);
+  p.emit = reinterpret_cast<int32_t*>(w + L.emit);
+  p.part = reinterpret_cast<AccPartial*>(w + L.part);
+  p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
+  p.smass = reinterpret_cast<double*>(w + L.smass);
+  const bool bf = a->logits_dtype == SSV_BF16;
+  int mode = a->mode;
+  if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;
+  cudaError_t e;
+  switch (mode) {
+    case SSV_ACCEPT_ARGMAX:
+      e = bf ? launch_accept_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_ARGMAX, float>(p, s);
+      break;
+    case SSV_ACCEPT_GUMBEL:
+      e = bf ? launch_accept_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_GUMBEL, float>(p, s);
+      break;
+    default:
+      e = bf ? launch_accept_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_REJECT, float>(p, s);
+      break;
+  }
+  return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
+}

@@ -23,7 +23,7 @@ ARGMAX, GUMBEL, REJECT = 0, 1, 2
 
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
-           "ssv_accept", "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
+           "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
 
 
 class SsvError(RuntimeError):
@@ -78,13 +78,14 @@ def lib():
         L.ssv_verify_attn.argtypes = [C.POINTER(AttnArgs), vp, sz, vp]
         L.ssv_accept_workspace.argtypes = [C.POINTER(AcceptArgs), C.POINTER(sz)]
         L.ssv_accept.argtypes = [C.POINTER(AcceptArgs), vp, sz, vp]
+        L.ssv_accept_noalloc.argtypes = [C.POINTER(AcceptArgs), vp]
         L.ssv_get_status.argtypes = [vp, vp]
         L.ssv_status_string.argtypes = [C.c_int]
         L.ssv_status_string.restype = C.c_char_p
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
         for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
-                     "ssv_accept", "ssv_get_status", "ssv_bench"):
+                     "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_bench"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -232,6 +233,25 @@ def accept(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_log
     ws = _workspace(accept_workspace_bytes(a), dev, workspace)
     _check(lib().ssv_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
            "ssv_accept")
+    return n_acc, n_out, tokens
+
+
+def accept_noalloc(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_logits=None, noise=None,
+                   noise_row=None, u_accept=None, u_sample=None, max_block=64, dev_status=None, stream=None,
+                   out=None):
+    """ssv_accept without a workspace: scratch comes from the library's fixed
+    per-device array (for callers that cannot allocate).  Output tensors may
+    be passed in ``out``; otherwise they are allocated here by torch."""
+    torch = _torch()
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(draft_tokens.shape[0], dtype=torch.int32, device=dev))
+    n_acc, n_out, tokens = out
+    a = accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
+                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status)
+    _check(lib().ssv_accept_noalloc(C.byref(a), _stream_ptr(stream)), "ssv_accept_noalloc")
     return n_acc, n_out, tokens
 
 

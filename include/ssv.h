@@ -231,6 +231,32 @@ SSV_API ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes)
 SSV_API ssv_status ssv_accept(const ssv_accept_args* a, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ssv_accept_noalloc -- ssv_accept for callers that cannot allocate.
+ * The pages have no counterpart: this is an interface addition of the
+ * library.  Some callers have no way to obtain device memory of their own:
+ * a host runtime that owns every byte of the GPU and hands its plugins no
+ * allocator, or a latency-critical path where cudaMalloc (which can
+ * synchronise the device) and allocating library routines are not allowed.
+ * They pass inputs and outputs exactly as for ssv_accept but no workspace;
+ * the scratch lives in a fixed 4 MiB array inside the library, which every
+ * GPU that loads libssv holds until the process exits.
+ *  - Same arguments, semantics and results as ssv_accept.
+ *  - Calls whose scratch would exceed 4 MiB (roughly total_slots *
+ *    ceil(V / 4096) > 120000 chunk records, e.g. more than ~3000 slots at
+ *    V = 151936) return SSV_ERR_WORKSPACE and launch nothing.
+ *  - Calls nothing that allocates: no cudaMalloc/cudaFree, no allocating
+ *    library routine.  It clears its arrival counters with a memset on
+ *    `stream` at every call.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams or host threads)
+ *    race and must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+SSV_API ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
  * Status and utilities
  * ---------------------------------------------------------------------- */
 /* Waits for `stream`, reads the device status word, resets it to 0 and
