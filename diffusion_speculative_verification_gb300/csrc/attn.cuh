@@ -26,4 +26,9 @@ struct AttnParams {
 
 cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);
 
+namespace tc {
+bool attn_tc_supported(const AttnParams& p);
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t st);
+}  // namespace tc
+
 }  // namespace ssv

@@ -75,7 +75,7 @@ extern "C" ssv_status ssv_verify_attn(const ssv_attn_args* a, void* ws, size_t w
   if (need > 0 && (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need)) return SSV_ERR_WORKSPACE;
   const AttnParams p = to_params(a);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = launch_attn_simt(p, s);
+  const cudaError_t e = tc::attn_tc_supported(p) ? tc::launch_attn_tc(p, s) : launch_attn_simt(p, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }
 
