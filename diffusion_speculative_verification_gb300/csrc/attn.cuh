@@ -28,7 +28,9 @@ cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);
 
 namespace tc {
 bool attn_tc_supported(const AttnParams& p);
-cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t st);
+size_t attn_tc_workspace(const AttnParams& p);
+// ws: attn_tc_workspace(p) bytes, 256-byte aligned, counter area zero on entry (left zero on exit)
+cudaError_t launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t st);
 }  // namespace tc
 
 }  // namespace ssv

@@ -2,26 +2,40 @@
 //
 // SimSD summary, section 2 "Temporal Attention Mask" and section 4
 // "Verification": one pass of softmax(q K^T * scale) V under the temporal
-// mask, which is evaluated per (row, key) from tau on the fly.
+// mask, evaluated per (row, key) from tau on the fly (never stored).
 //
-// Tile = (sequence b, kv head g, R consecutive query rows of b) x all G query
-// heads of the group, M = R * G = 128 rows, so one K/V block feeds every
-// head that shares it (grouped-query packing).  Row m of the tile is
-// (query row row0 + m / G, head g * G + m % G); the Q box of the TMA tensor
-// map (64 x G x R elements) lands in exactly that order.
+// Work unit = (sequence b, kv head g, UR consecutive query rows of b) x all G
+// query heads of the group.  It is split into MT M-tiles of 128 packed rows
+// (R = 128 / G query rows x G heads each); tile row m is (query row
+// row0 + mt * R + m / G, head g * G + m % G), which is exactly the order in
+// which the 3-D TMA box (64 x G x R) lands in shared memory.  Every K/V block
+// loaded for a unit feeds all of its tiles (grouped-query packing).
 //
-// Per CTA (192 threads, one CTA per SM: 226 KB of shared memory):
-//   warp 0      TMA producer (Q once, then K/V blocks into a 2-stage ring)
-//               and TMEM allocator (512 columns: S double buffer + O)
-//   warp 1      MMA issuer: S_j = Q K_j^T (M=128, N=128, K=128) into TMEM,
-//               then O += P_{j-1} V_{j-1} (P from shared memory, V MN-major)
-//   warps 2..5  softmax: tcgen05.ld of S rows (thread = row = TMEM lane),
-//               mask, online max with lazy rescaling (only when the max
-//               grows by more than 2^8), exp2, bf16 P into swizzled shared
-//               memory; epilogue O / l from TMEM to global.
-// Key blocks: the sequence's cache keys (all visible to every row), then its
-// fresh keys (prompt rows causal, tail rows per tau).  Blocks whose 128 keys
-// are visible to every valid row of the tile skip the mask.
+// Keys of a unit: the sequence's cache keys (visible to every row), then its
+// fresh keys up to the last row that needs them (prompt rows are causal,
+// tail rows follow tau).  Blocks of 128 keys visible to every valid row skip
+// the mask.
+//
+// Scheduling is persistent stream-K: one CTA per SM; the concatenated key
+// blocks of all units are cut into equal contiguous ranges, one per CTA.  A
+// unit split across CTAs leaves fp32 partials (unnormalised O, running max,
+// sum) in the workspace; for each 32-row group the warp that arrives last
+// (per-group arrival counter, no waiting on other CTAs) merges the partials
+// and writes the output.  The plan is derived on the device from seqs.
+//
+// Roles per CTA (4 * MT + 2 warps):
+//   warp 0  TMA producer (Q tiles per segment, K/V blocks into a 2-stage
+//           ring) and TMEM owner (512 columns)
+//   warp 1  MMA issuer: S_mt = Q_mt K^T into TMEM, then O_mt += P_mt V with P
+//           read from TMEM (it overwrites S_mt's first 64 columns) and V as
+//           an MN-major shared-memory operand; tiles alternate so one
+//           softmax warpgroup computes while the tensor core serves the other
+//   warps 2.. softmax, 4 per tile (one TMEM lane quadrant each): S row from
+//           TMEM, mask, running max with lazy rescaling of O (only when the
+//           max grows by more than 2^8), exp2, bf16 P back into TMEM;
+//           epilogue O / l, or partial + merge.
+// Every wait is bounded; an expired wait raises a CTA abort flag, in-flight
+// copies and MMAs are drained, TMEM is freed and SSV_ERR_TIMEOUT reported.
 #include "ssv_internal.cuh"
 #include "attn.cuh"
 #include "tc_ptx.cuh"
@@ -37,87 +51,192 @@ namespace tc {
 using namespace ptx;
 
 constexpr int D = 128;
-constexpr int BM = 128;        // query rows per tile (M)
-constexpr int BN = 128;        // keys per block
-constexpr int NST = 2;         // K/V pipeline stages
-constexpr int kThreads = 192;
+constexpr int BN = 128;   // keys per block
+constexpr int NST = 2;    // K/V pipeline stages
 constexpr uint32_t TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 operand
-constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzle atom column (16 KB)
-constexpr uint32_t SM_Q = 0;
-constexpr uint32_t SM_K = SM_Q + TILE_BYTES;
-constexpr uint32_t SM_V = SM_K + NST * TILE_BYTES;
-constexpr uint32_t SM_P = SM_V + NST * TILE_BYTES;
-constexpr uint32_t SM_BAR = SM_P + 2 * TILE_BYTES;
-constexpr uint32_t SM_TOTAL = SM_BAR + 256;
-constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;  // base is rounded up to 1024 B
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzle atom column
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;    // S double buffer: columns [0, 256)
-constexpr uint32_t TM_O = 256;  // O: columns [256, 384)
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
+constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr int kMaxBatch = 1024;
 
-// barrier slots (8 bytes each) inside SM_BAR
 enum : uint32_t {
-  B_Q = 0,
-  B_KV_FULL = 1,   // +stage
-  B_KV_EMPTY = 3,  // +stage
-  B_S_FULL = 5,    // +buffer
-  B_S_FREE = 7,    // +buffer
-  B_P_FULL = 9,    // +buffer
-  B_PV_DONE = 11,  // +buffer
-  B_FINAL = 13,
-  B_COUNT = 14
+  B_Q_FULL = 0,
+  B_Q_EMPTY = 1,
+  B_KV_FULL = 2,                 // + stage
+  B_KV_EMPTY = B_KV_FULL + NST,  // + stage
+  B_S_FULL = B_KV_EMPTY + NST,   // + tile
+  B_P_FULL = B_S_FULL + 2,       // + tile
+  B_PV_DONE = B_P_FULL + 2,      // + tile
+  B_O_FREE = B_PV_DONE + 2,      // + tile
+  B_FINAL = B_O_FREE + 2,
+  B_COUNT = B_FINAL + 1
+};
+
+template <int MT>
+struct Cfg {
+  static constexpr int kSoftWarps = 4 * MT;
+  static constexpr int kThreads = 64 + 32 * kSoftWarps;
+  static constexpr uint32_t SM_Q = 0;
+  static constexpr uint32_t SM_K = SM_Q + MT * TILE_BYTES;
+  static constexpr uint32_t SM_V = SM_K + NST * TILE_BYTES;
+  static constexpr uint32_t SM_BAR = SM_V + NST * TILE_BYTES;
+  static constexpr uint32_t SM_PLAN = SM_BAR + 256;
+  static constexpr uint32_t SM_TOTAL = SM_PLAN + 16u * (kMaxBatch + 1);
+  static constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 };
 
 struct TcMaps {
   CUtensorMap q, kc, vc, kn, vn;
 };
 
-struct TileGeom {
-  int C, N, B, q_off, kv_off, tau_off;
-  int row0, rows;       // first local query row of the tile, rows of the sequence
-  int cache_blocks, nblocks;
-  int full_new;         // fresh keys [0, full_new) are visible to every valid row of the tile
+struct TcWork {
+  int32_t* cnt;    // [units][MT][4] arrival counters (zero between calls)
+  float* part_ml;  // [2 * grid][MT][128][2]  running max (log2 domain), sum
+  float* part_o;   // [2 * grid][MT][128][128] unnormalised O
 };
 
-__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + SM_BAR + 8u * i; }
+struct PlanHdr {
+  int W, U, Pe, begin, end, u0, k0;  // Pe = CTAs that own blocks (min(grid, W)): every owner is non-empty
+};
 
-template <typename OutT>
-__global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, int R, int G) {
+struct Unit {
+  int b, g;
+  int C, N, B, rows, q_off, kv_off, tau_off;
+  int row0, nvalid, mc, cache_blocks, nblocks, full_new;
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int unit_nblocks(int C, int N, int rows, int row0, int UR) {
+  const int kmax = (row0 + UR <= N) ? (row0 + UR) : rows;
+  return cdiv(C, BN) + cdiv(kmax, BN);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int w) {
+  return w == 0 ? a : (w == 1 ? b : (w == 2 ? c : (w == 3 ? d : 0u)));
+}
+
+// bits [0, n) set, n clamped to [0, 32]
+__device__ __forceinline__ uint32_t prefix32(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+
+// 32-bit window [t0, t0 + 32) of the 128-bit mask (w0 | w1 << 32 | ...), zero outside [0, 128)
+__device__ __forceinline__ uint32_t window32(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3, int t0) {
+  if (t0 <= -32 || t0 >= 128) return 0u;
+  const int w = t0 >> 5;  // floor division (arithmetic shift)
+  const int sh = t0 & 31;
+  const uint32_t lo = pick4(w0, w1, w2, w3, w);
+  const uint32_t hi = pick4(w0, w1, w2, w3, w + 1);
+  return sh == 0 ? lo : __funnelshift_r(lo, hi, sh);
+}
+
+template <int MT, typename OutT>
+__global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
+attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const TcWork work, int G) {
+  using C_ = Cfg<MT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + SM_BAR + 8 * B_COUNT + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_BAR + 8 * B_COUNT);
-  __shared__ int s_ok;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::SM_BAR + 8 * B_COUNT);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C_::SM_BAR + 8 * B_COUNT + 4);
+  PlanHdr* plan = reinterpret_cast<PlanHdr*>(smem + C_::SM_BAR + 8 * B_COUNT + 8);
+  int* s_prefU = reinterpret_cast<int*>(smem + C_::SM_PLAN);
+  int* s_prefB = s_prefU + (kMaxBatch + 1);
+  int* s_bgblk = s_prefB + (kMaxBatch + 1);
+  int* s_ntile = s_bgblk + kMaxBatch;
+  auto bar = [&](uint32_t i) -> uint32_t { return sbase + C_::SM_BAR + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
-  const ssv_seq sq = p.seqs[b];
-  TileGeom t;
-  t.C = sq.cache_len; t.N = sq.new_len; t.B = sq.block;
-  t.q_off = sq.q_off; t.kv_off = sq.kv_off; t.tau_off = sq.tau_off;
-  t.rows = t.N + 2 * t.B;
-  t.row0 = tile * R;
-  if (t.row0 >= t.rows) return;  // uniform: this sequence has fewer tiles
-  t.cache_blocks = (t.C + BN - 1) / BN;
-  const int kmax = (t.row0 + R <= t.N) ? (t.row0 + R) : t.rows;
-  t.nblocks = t.cache_blocks + (kmax + BN - 1) / BN;
-  t.full_new = (t.row0 < t.N) ? (t.row0 + 1) : t.N;
-  const int32_t* tau = p.tau + t.tau_off;
+  const int R = 128 / G;
+  const int UR = MT * R;
+  const int P = gridDim.x;   // CTAs launched; only the first Pe own key blocks
+  const int cta = blockIdx.x;
 
+  // ------------------------------------------------------------------ plan
   if (warp == 0) {
-    const bool ok = (t.B >= 1 && t.B <= 64) ? warp_tau_is_permutation(tau, t.B) : false;
+    int carryU = 0, carryB = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+      const int b = b0 + lane;
+      int units = 0, blocks = 0;
+      if (b < p.batch) {
+        const ssv_seq s = p.seqs[b];
+        const int rows = s.new_len + 2 * s.block;
+        const int nt = cdiv(rows, UR);
+        int bg = 0;
+        for (int t = 0; t < nt; ++t) bg += unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+        s_bgblk[b] = bg;
+        s_ntile[b] = nt;
+        units = p.Hkv * nt;
+        blocks = p.Hkv * bg;
+      }
+      int iu = units, ib = blocks;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int yu = __shfl_up_sync(0xffffffffu, iu, o), yb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) { iu += yu; ib += yb; }
+      }
+      if (b < p.batch) { s_prefU[b + 1] = carryU + iu; s_prefB[b + 1] = carryB + ib; }
+      carryU += __shfl_sync(0xffffffffu, iu, 31);
+      carryB += __shfl_sync(0xffffffffu, ib, 31);
+    }
+    if (cta == 0) {
+      // stage maps must permute 1..B (a bad map cannot index out of range: report only)
+      for (int b = 0; b < p.batch; ++b) {
+        const ssv_seq s = p.seqs[b];
+        const bool ok = (s.block >= 1 && s.block <= 64) && warp_tau_is_permutation(p.tau + s.tau_off, s.block);
+        if (!ok) {
+          if (lane == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
+          break;
+        }
+      }
+    }
     if (lane == 0) {
-      s_ok = ok;
+      s_prefU[0] = 0;
+      s_prefB[0] = 0;
+      PlanHdr h;
+      h.W = carryB;
+      h.U = carryU;
+      h.Pe = min(P, max(carryB, 1));
+      h.begin = cta < h.Pe ? (int)(((long long)cta * carryB) / h.Pe) : 0;
+      h.end = cta < h.Pe ? (int)(((long long)(cta + 1) * carryB) / h.Pe) : 0;
+      h.u0 = 0;
+      h.k0 = 0;
+      if (h.begin < h.end) {
+        int lo = 0, hi = p.batch - 1, b = 0;
+        while (lo <= hi) {  // last sequence whose first block is <= begin (every sequence has blocks)
+          const int mid = (lo + hi) >> 1;
+          if (s_prefB[mid] <= h.begin) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+        }
+        const int rem = h.begin - s_prefB[b];
+        const int gg = rem / s_bgblk[b];
+        int r2 = rem - gg * s_bgblk[b];
+        const ssv_seq s = p.seqs[b];
+        const int rows = s.new_len + 2 * s.block;
+        int t = 0;
+        for (; t < s_ntile[b] - 1; ++t) {
+          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+          if (r2 < nb) break;
+          r2 -= nb;
+        }
+        h.u0 = s_prefU[b] + gg * s_ntile[b] + t;
+        h.k0 = r2;
+      }
+      *plan = h;
       *abort = 0;
-      for (int i = 0; i < B_COUNT; ++i) {
+      for (uint32_t i = 0; i < B_COUNT; ++i) {
         uint32_t cnt = 1;
-        if (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL || i == B_P_FULL + 1) cnt = 4;
-        mbar_init(bar_addr(sbase, i), cnt);
+        if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_FREE || i == B_O_FREE + 1) cnt = 4;
+        mbar_init(bar(i), cnt);
       }
       fence_mbar_init();
-      if (!ok) report(p.dev_status, SSV_ERR_BAD_TAU);
     }
     __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -126,252 +245,462 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, int R, i
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const bool ok = s_ok != 0;
+  const int begin = plan->begin, end = plan->end, W = plan->W, Pe = plan->Pe;
 
-  if (ok && warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  // decode unit u from the shared plan tables
+  auto decode = [&](int u) -> Unit {
+    Unit x;
+    int lo = 0, hi = p.batch - 1, b = 0;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefU[mid] <= u) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    const int local = u - s_prefU[b];
+    x.b = b;
+    x.g = local / s_ntile[b];
+    const int tile = local - x.g * s_ntile[b];
+    const ssv_seq s = p.seqs[b];
+    x.C = s.cache_len; x.N = s.new_len; x.B = s.block;
+    x.q_off = s.q_off; x.kv_off = s.kv_off; x.tau_off = s.tau_off;
+    x.rows = x.N + 2 * x.B;
+    x.row0 = tile * UR;
+    x.nvalid = min(UR, x.rows - x.row0);
+    x.mc = (MT == 2 && x.nvalid > R) ? 2 : 1;
+    x.cache_blocks = cdiv(x.C, BN);
+    x.nblocks = unit_nblocks(x.C, x.N, x.rows, x.row0, UR);
+    x.full_new = (x.row0 < x.N) ? (x.row0 + 1) : x.N;
+    return x;
+  };
+  auto seg_start = [&](int c) -> int { return (int)(((long long)c * W) / Pe); };
+  auto owner = [&](int xb) -> int {  // CTA whose range holds global block xb
+    int c = (int)(((long long)xb * Pe) / (W > 0 ? W : 1));
+    c = min(max(c, 0), Pe - 1);
+    while (c + 1 < Pe && seg_start(c + 1) <= xb) ++c;
+    while (c > 0 && seg_start(c) > xb) --c;
+    return c;
+  };
+
+  if (warp == 0) {
+    // ============================================================ producer
+    if (lane == 0 && begin < end) {
       tma_prefetch(&maps.q); tma_prefetch(&maps.kc); tma_prefetch(&maps.vc);
       tma_prefetch(&maps.kn); tma_prefetch(&maps.vn);
-      const uint32_t bq = bar_addr(sbase, B_Q);
-      mbar_expect_tx(bq, TILE_BYTES);
-      tma_load_3d(sbase + SM_Q, &maps.q, 0, g * G, t.q_off + t.row0, bq);
-      tma_load_3d(sbase + SM_Q + HALF_BYTES, &maps.q, 64, g * G, t.q_off + t.row0, bq);
-      int issued = 0;
-      for (int j = 0; j < t.nblocks; ++j) {
-        const int st = j % NST;
-        if (j >= NST && !mbar_wait(bar_addr(sbase, B_KV_EMPTY + st), ((j - NST) / NST) & 1, abort)) break;
-        const uint32_t bf = bar_addr(sbase, B_KV_FULL + st);
-        mbar_expect_tx(bf, 2 * TILE_BYTES);
-        const uint32_t dk = sbase + SM_K + st * TILE_BYTES, dv = sbase + SM_V + st * TILE_BYTES;
-        if (j < t.cache_blocks) {
-          const int z = t.kv_off + j * BN;
-          tma_load_3d(dk, &maps.kc, 0, g, z, bf);
-          tma_load_3d(dk + HALF_BYTES, &maps.kc, 64, g, z, bf);
-          tma_load_3d(dv, &maps.vc, 0, g, z, bf);
-          tma_load_3d(dv + HALF_BYTES, &maps.vc, 64, g, z, bf);
-        } else {
-          const int z = t.q_off + (j - t.cache_blocks) * BN;
-          tma_load_3d(dk, &maps.kn, 0, g, z, bf);
-          tma_load_3d(dk + HALF_BYTES, &maps.kn, 64, g, z, bf);
-          tma_load_3d(dv, &maps.vn, 0, g, z, bf);
-          tma_load_3d(dv + HALF_BYTES, &maps.vn, 64, g, z, bf);
+      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kv_n = 0;
+      bool run = true;
+      while (run && remaining > 0) {
+        const Unit x = decode(u);
+        const int len = min(x.nblocks - k, remaining);
+        if (seg > 0 && !mbar_wait(bar(B_Q_EMPTY), (seg - 1) & 1, abort)) break;
+        mbar_expect_tx(bar(B_Q_FULL), x.mc * TILE_BYTES);
+        for (int mt = 0; mt < x.mc; ++mt) {
+          const int z = x.q_off + x.row0 + mt * R;
+          tma_load_3d(sbase + C_::SM_Q + mt * TILE_BYTES, &maps.q, 0, x.g * G, z, bar(B_Q_FULL));
+          tma_load_3d(sbase + C_::SM_Q + mt * TILE_BYTES + HALF_BYTES, &maps.q, 64, x.g * G, z, bar(B_Q_FULL));
         }
-        issued = j + 1;
+        ++seg;
+        for (int j = k; j < k + len; ++j) {
+          const int st = kv_n % NST;
+          if (kv_n >= NST && !mbar_wait(bar(B_KV_EMPTY + st), ((kv_n / NST) - 1) & 1, abort)) { run = false; break; }
+          mbar_expect_tx(bar(B_KV_FULL + st), 2 * TILE_BYTES);
+          const uint32_t dk = sbase + C_::SM_K + st * TILE_BYTES, dv = sbase + C_::SM_V + st * TILE_BYTES;
+          const bool cache = j < x.cache_blocks;
+          const CUtensorMap* mk = cache ? &maps.kc : &maps.kn;
+          const CUtensorMap* mv = cache ? &maps.vc : &maps.vn;
+          const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
+          tma_load_3d(dk, mk, 0, x.g, z, bar(B_KV_FULL + st));
+          tma_load_3d(dk + HALF_BYTES, mk, 64, x.g, z, bar(B_KV_FULL + st));
+          tma_load_3d(dv, mv, 0, x.g, z, bar(B_KV_FULL + st));
+          tma_load_3d(dv + HALF_BYTES, mv, 64, x.g, z, bar(B_KV_FULL + st));
+          ++kv_n;
+        }
+        remaining -= len;
+        ++u;
+        k = 0;
       }
-      // drain: every issued copy must land before the CTA exits (bounded,
-      // and regardless of the abort flag)
-      {
+      // drain (bounded, regardless of abort): the last Q load and the last NST K/V loads
+      if (seg > 0) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar_addr(sbase, B_Q), 0) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_Q_FULL), (seg - 1) & 1) && clock64() - t0 < kWaitBudget) {
         }
       }
-      for (int j = (issued > NST ? issued - NST : 0); j < issued; ++j) {
-        const int st = j % NST;
+      for (int n = (kv_n > NST ? kv_n - NST : 0); n < kv_n; ++n) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar_addr(sbase, B_KV_FULL + st), (j / NST) & 1) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_KV_FULL + n % NST), (n / NST) & 1) && clock64() - t0 < kWaitBudget) {
         }
       }
     }
-  } else if (ok && warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    if (lane == 0 && begin < end) {
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_pv = idesc_bf16(128, 128, true);
-      bool run = mbar_wait(bar_addr(sbase, B_Q), 0, abort);
-      auto issue_pv = [&](int jj) -> bool {
-        const int sb = jj & 1, st = jj % NST;
-        if (!mbar_wait(bar_addr(sbase, B_P_FULL + sb), (jj >> 1) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + SM_P + sb * TILE_BYTES, va = sbase + SM_V + st * TILE_BYTES;
+      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kv_n = 0;
+      int nblk0 = 0, nblk1 = 0, nseg0 = 0, nseg1 = 0;
+      bool run = true;
+      auto issue_s = [&](int mt, int st) {
+        const uint32_t qa = sbase + C_::SM_Q + mt * TILE_BYTES, ka = sbase + C_::SM_K + st * TILE_BYTES;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t ad = smem_desc_sw128(pa + (k >> 2) * HALF_BYTES + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(va + k * 2048, HALF_BYTES, 1024);
-          mma_f16(tmem + TM_O, ad, bd, id_pv, (jj > 0 || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+          mma_f16(tmem + mt * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), id_s,
+                  kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_addr(sbase, B_PV_DONE + sb));
-        mma_commit(bar_addr(sbase, B_KV_EMPTY + st));
-        return true;
+        mma_commit(bar(B_S_FULL + mt));
       };
-      for (int j = 0; run && j < t.nblocks; ++j) {
-        const int st = j % NST, sb = j & 1;
-        if (!mbar_wait(bar_addr(sbase, B_KV_FULL + st), (j / NST) & 1, abort)) { run = false; break; }
-        if (j >= 2 && !mbar_wait(bar_addr(sbase, B_S_FREE + sb), ((j - 2) >> 1) & 1, abort)) { run = false; break; }
+      auto issue_pv = [&](int mt, int st, bool acc) {
+        const uint32_t va = sbase + C_::SM_V + st * TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_f16_tmem_a(tmem + TM_O + mt * 128, tmem + mt * 128 + kk * 8,
+                         smem_desc_sw128(va + kk * 2048, HALF_BYTES, 1024), id_pv, (acc || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_PV_DONE + mt));
+      };
+      while (run && remaining > 0) {
+        const Unit x = decode(u);
+        const int len = min(x.nblocks - k, remaining);
+        if (!mbar_wait(bar(B_Q_FULL), seg & 1, abort)) break;
+        if (!mbar_wait(bar(B_KV_FULL + kv_n % NST), (kv_n / NST) & 1, abort)) break;
         tc_fence_after();
-        const uint32_t ka = sbase + SM_K + st * TILE_BYTES;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * HALF_BYTES + (k & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(sbase + SM_Q + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(ka + off, 16, 1024);
-          mma_f16(tmem + TM_S + sb * 128, ad, bd, id_s, k > 0 ? 1u : 0u);
-        }
-        mma_commit(bar_addr(sbase, B_S_FULL + sb));
-        if (j >= 1 && !issue_pv(j - 1)) { run = false; break; }
-      }
-      if (run) issue_pv(t.nblocks - 1);
-      // all MMAs issued by this thread complete before TMEM is released
-      mma_commit(bar_addr(sbase, B_FINAL));
-      const long long t0 = clock64();
-      while (!mbar_try_wait(bar_addr(sbase, B_FINAL), 0) && clock64() - t0 < kWaitBudget) {
-      }
-    }
-  } else if (ok) {
-    // ------------------------------------------------------------ softmax
-    const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
-    const int m = q4 * 32 + lane;            // tile row = TMEM lane
-    const int r_local = m / G, hj = m % G;
-    const int i = t.row0 + r_local;          // local query row
-    const bool valid = i < t.rows;
-    const bool prompt = i < t.N;
-    const int r = i - t.N;                   // tail row index
-    // allowed tail keys of this row: bit tk of (tm0 | tm1 << 32 | ...), 2B <= 128
-    uint32_t tm0 = 0u, tm1 = 0u, tm2 = 0u, tm3 = 0u;
-    if (valid && !prompt) {
-      const int tr = tau[r % t.B];
-      for (int tk = 0; tk < 2 * t.B; ++tk) {
-        if (!tail_allowed(r, tk, t.B, tr, tau[tk % t.B])) continue;
-        const uint32_t bit = 1u << (tk & 31);
-        if (tk < 32) tm0 |= bit; else if (tk < 64) tm1 |= bit; else if (tk < 96) tm2 |= bit; else tm3 |= bit;
-      }
-    }
-    const float qk_scale = p.scale * 1.4426950408889634f;
-    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    float m_used = -INFINITY, l_sum = 0.f;
-    bool run = true;
-    // every thread waits (bounded); the warp proceeds only if all succeeded,
-    // so the warp-collective tcgen05.ld / st below are never split
-    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
-      const bool w = mbar_wait(bar, parity, abort);
-      return __all_sync(0xffffffffu, w);
-    };
-    for (int j = 0; j < t.nblocks; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(bar_addr(sbase, B_S_FULL + sb), (j >> 1) & 1)) { run = false; break; }
-      tc_fence_after();
-      float s[BN];
-      {
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tmem + lane_base + TM_S + sb * 128 + c * 32, sr + c * 32);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_S_FREE + sb));
-      // ---- mask + scale
-      const bool is_cache = j < t.cache_blocks;
-      const int kbase = is_cache ? j * BN : (j - t.cache_blocks) * BN;
-      const bool full = is_cache ? (kbase + BN <= t.C) : (kbase + BN <= t.full_new);
-      float mx = -INFINITY;
-      if (full && valid) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) { s[c] *= qk_scale; mx = fmaxf(mx, s[c]); }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int kk = kbase + c;
-          bool al;
-          if (!valid) al = false;
-          else if (is_cache) al = kk < t.C;
-          else if (kk >= t.rows) al = false;
-          else if (prompt) al = kk <= i;
-          else if (kk < t.N) al = true;
-          else {
-            const int tk = kk - t.N;
-            const uint32_t wsel = tk < 64 ? (tk < 32 ? tm0 : tm1) : (tk < 96 ? tm2 : tm3);
-            al = (wsel >> (tk & 31)) & 1u;
-          }
-          s[c] = al ? s[c] * qk_scale : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-      }
-      // ---- online max with lazy rescale of O (warp-uniform: tcgen05.ld/st are collective)
-      const bool need = mx > m_used + kRescaleThreshold || (m_used == -INFINITY && mx > -INFINITY);
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // O holds PV of blocks < j; it must be complete before rescaling
-        if (!warp_wait(bar_addr(sbase, B_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1)) { run = false; break; }
-        tc_fence_after();
-        const float f = need ? exp2f(m_used - mx) : 1.f;
-        uint32_t raw[32];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tmem + lane_base + TM_O + c * 32, raw);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
-          tmem_st32(tmem + lane_base + TM_O + c * 32, raw);
-        }
-        tmem_wait_st();
-        l_sum *= f;
-      }
-      if (need) m_used = mx;
-      // ---- P = exp2(s - m), bf16, into the swizzled P buffer
-      if (j >= 2 && !warp_wait(bar_addr(sbase, B_PV_DONE + sb), ((j - 2) >> 1) & 1)) { run = false; break; }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      uint8_t* pbuf = smem + SM_P + sb * TILE_BYTES;
-#pragma unroll
-      for (int c8 = 0; c8 < BN / 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float p0 = exp2f(s[c8 * 8 + 2 * h] - mref);
-          const float p1 = exp2f(s[c8 * 8 + 2 * h + 1] - mref);
-          const __nv_bfloat16 b0 = __float2bfloat16_rn(p0), b1 = __float2bfloat16_rn(p1);
-          l_sum += __bfloat162float(b0) + __bfloat162float(b1);
-          w[h] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
-        }
-        const int atom = c8 >> 3, chunk = c8 & 7;
-        uint8_t* dst = pbuf + atom * HALF_BYTES + (m >> 3) * 1024 + (m & 7) * 128 + ((chunk ^ (m & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(sbase, B_P_FULL + sb));
-    }
-    // ---- epilogue
-    if (run && warp_wait(bar_addr(sbase, B_PV_DONE + ((t.nblocks - 1) & 1)), ((t.nblocks - 1) >> 1) & 1)) {
-      tc_fence_after();
-      const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-      OutT* orow = static_cast<OutT*>(p.o) + ((size_t)(t.q_off + i) * p.Hq + g * G + hj) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld32(tmem + lane_base + TM_O + c * 32, raw);
-        tmem_wait_ld();
-        if (valid) {
-          if constexpr (sizeof(OutT) == 4) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(orow + c * 32 + e) =
-                  make_float4(__uint_as_float(raw[e]) * inv, __uint_as_float(raw[e + 1]) * inv,
-                              __uint_as_float(raw[e + 2]) * inv, __uint_as_float(raw[e + 3]) * inv);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint32_t w[4];
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                const __nv_bfloat16 b0 = __float2bfloat16_rn(__uint_as_float(raw[e + 2 * h]) * inv);
-                const __nv_bfloat16 b1 = __float2bfloat16_rn(__uint_as_float(raw[e + 2 * h + 1]) * inv);
-                w[h] = static_cast<uint32_t>(__bfloat16_as_ushort(b0)) |
-                       (static_cast<uint32_t>(__bfloat16_as_ushort(b1)) << 16);
+        for (int mt = 0; mt < x.mc; ++mt) issue_s(mt, kv_n % NST);
+        for (int i = 0; i < len && run; ++i) {
+          const int st = kv_n % NST;
+          for (int mt = 0; mt < x.mc; ++mt) {
+            int& nb = mt ? nblk1 : nblk0;
+            const int ns = mt ? nseg1 : nseg0;
+            if (!mbar_wait(bar(B_P_FULL + mt), nb & 1, abort)) { run = false; break; }
+            if (i == 0 && ns > 0 && !mbar_wait(bar(B_O_FREE + mt), (ns - 1) & 1, abort)) { run = false; break; }
+            tc_fence_after();
+            issue_pv(mt, st, i > 0);
+            ++nb;
+            if (i + 1 < len) {
+              if (mt == 0 && !mbar_wait(bar(B_KV_FULL + (kv_n + 1) % NST), ((kv_n + 1) / NST) & 1, abort)) {
+                run = false;
+                break;
               }
-              *reinterpret_cast<uint4*>(orow + c * 32 + e) = make_uint4(w[0], w[1], w[2], w[3]);
+              tc_fence_after();
+              issue_s(mt, (kv_n + 1) % NST);
             }
           }
+          if (!run) break;
+          mma_commit(bar(B_KV_EMPTY + st));
+          ++kv_n;
         }
+        if (!run) break;
+        mma_commit(bar(B_Q_EMPTY));
+        ++nseg0;
+        if (x.mc > 1) ++nseg1;
+        remaining -= len;
+        ++seg;
+        ++u;
+        k = 0;
       }
     }
+    if (lane == 0) {
+      // every MMA issued by this thread completes before TMEM is released
+      mma_commit(bar(B_FINAL));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar(B_FINAL), 0) && clock64() - t0 < kWaitBudget) {
+      }
+    }
+  } else {
+    // ============================================================ softmax
+    const int mt = (warp - 2) >> 2;   // tile served by this warp
+    const int q4 = warp & 3;          // TMEM lane quadrant
+    const int m = q4 * 32 + lane;     // tile row = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_base + mt * 128;
+    const uint32_t tO = tmem + lane_base + TM_O + mt * 128;
+    const float cexp = p.scale * 1.4426950408889634f;
+    int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, nblk = 0, pos = begin;
+    bool run = true;
+    auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
+      const bool w = mbar_wait(b, parity, abort);
+      return __all_sync(0xffffffffu, w);
+    };
+    while (run && remaining > 0) {
+      const Unit x = decode(u);
+      const int len = min(x.nblocks - k, remaining);
+      const bool complete = (k == 0 && len == x.nblocks);
+      const int ustart = pos - k;  // global index of the unit's first block
+      if (mt < x.mc) {
+        const int r_local = mt * R + m / G;
+        const int hj = m % G;
+        const int i = x.row0 + r_local;  // local query row in the sequence
+        const bool valid = r_local < x.nvalid;
+        const bool warp_active = (mt * R + (q4 * 32) / G) < x.nvalid;
+        const bool prompt = i < x.N;
+        const int r = i - x.N;
+        uint32_t tm0 = 0u, tm1 = 0u, tm2 = 0u, tm3 = 0u;  // allowed tail keys of this row
+        if (warp_active && x.row0 + x.nvalid > x.N) {   // warp-uniform: the unit holds tail rows
+          // stage map of the sequence in two registers per lane, broadcast by shuffles
+          const int32_t* tau = p.tau + x.tau_off;
+          const int ta = lane < x.B ? tau[lane] : 0;
+          const int tb = lane + 32 < x.B ? tau[lane + 32] : 0;
+          const bool tail_row = valid && !prompt;
+          const int slot_r = tail_row ? (r % x.B) : 0;
+          const int tr = __shfl_sync(0xffffffffu, slot_r < 32 ? ta : tb, slot_r & 31);
+          for (int tk = 0; tk < 2 * x.B; ++tk) {
+            const int sk = tk % x.B;
+            const int tt = __shfl_sync(0xffffffffu, sk < 32 ? ta : tb, sk & 31);
+            if (!tail_row || !tail_allowed(r, tk, x.B, tr, tt)) continue;
+            const uint32_t bit = 1u << (tk & 31);
+            if (tk < 32) tm0 |= bit; else if (tk < 64) tm1 |= bit; else if (tk < 96) tm2 |= bit; else tm3 |= bit;
+          }
+        }
+        float m_used = -INFINITY, l_sum = 0.f;
+        for (int jj = 0; jj < len; ++jj, ++nblk) {
+          const int j = k + jj;
+          if (!warp_wait(bar(B_S_FULL + mt), nblk & 1)) { run = false; break; }
+          if (!warp_active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + mt));
+            continue;
+          }
+          tc_fence_after();
+          // ---- visibility of this block's 128 keys for this row, as 32-column bitmasks
+          const bool is_cache = j < x.cache_blocks;
+          const int kbase = is_cache ? j * BN : (j - x.cache_blocks) * BN;
+          const bool full = is_cache ? (kbase + BN <= x.C) : (kbase + BN <= x.full_new);
+          const bool all_vis = __all_sync(0xffffffffu, full && valid);
+          int lim = BN, lim_rows = 0, toff = 0;  // prefix limit; tail bits for columns < lim_rows
+          if (!valid) {
+            lim = 0;
+          } else if (!full) {
+            if (is_cache) {
+              lim = x.C - kbase;
+            } else if (prompt) {
+              lim = min(i + 1, x.rows) - kbase;
+            } else {
+              lim = x.N - kbase;
+              lim_rows = x.rows - kbase;
+              toff = kbase - x.N;  // tail index of column 0
+            }
+          }
+          auto vis32 = [&](int q) -> uint32_t {  // visibility bits of columns [32q, 32q + 32)
+            uint32_t v = prefix32(lim - 32 * q);
+            if (lim_rows > 32 * q) v |= window32(tm0, tm1, tm2, tm3, toff + 32 * q) & prefix32(lim_rows - 32 * q);
+            return v;
+          };
+          // ---- pass 1: row max of the raw scores (the scale is positive)
+          float mx;
+          {
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] = -INFINITY;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint32_t sr[64];
+              tmem_ld32(tS + h * 64, sr);
+              tmem_ld32(tS + h * 64 + 32, sr + 32);
+              tmem_wait_ld();
+              if (all_vis) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) a[e & 7] = fmaxf(a[e & 7], __uint_as_float(sr[e]));
+              } else {
+                const uint32_t v0 = vis32(2 * h), v1 = vis32(2 * h + 1);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                  const uint32_t vw = e < 32 ? v0 : v1;
+                  const float f = ((vw >> (e & 31)) & 1u) ? __uint_as_float(sr[e]) : -INFINITY;
+                  a[e & 7] = fmaxf(a[e & 7], f);
+                }
+              }
+            }
+            mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+          }
+          const float mxs = mx * cexp;
+          const bool need = (mx > -INFINITY) && (m_used == -INFINITY || mxs > m_used + kRescaleThreshold);
+          if (jj > 0 && __any_sync(0xffffffffu, need)) {
+            // O holds PV of the earlier blocks: it must be complete before rescaling
+            if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
+            tc_fence_after();
+            const float f = need ? ex2(m_used - mxs) : 1.f;
+            uint32_t raw[32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              tmem_ld32(tO + c * 32, raw);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+              tmem_st32(tO + c * 32, raw);
+            }
+            tmem_wait_st();
+            l_sum *= f;
+          }
+          if (need) m_used = mxs;
+          const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+          // ---- pass 2: P = exp2(s * c - m) as bf16 pairs into TMEM over S columns [0, 64).
+          // Chunk q reads S columns [32q, 32q + 32) and writes P columns [16q, 16q + 16),
+          // which lie in S columns already read.
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll 1
+          for (int q = 0; q < BN / 32; ++q) {
+            uint32_t sr[32];
+            tmem_ld32(tS + q * 32, sr);
+            tmem_wait_ld();
+            uint32_t pw[16];
+            if (all_vis) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref));
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
+                if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
+              }
+            } else {
+              const uint32_t vw = vis32(q);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float p0 = ((vw >> (2 * e)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref)) : 0.f;
+                const float p1 =
+                    ((vw >> (2 * e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref)) : 0.f;
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
+                if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
+              }
+            }
+            tmem_st16(tS + q * 16, pw);
+          }
+          tmem_wait_st();
+          l_sum += (l0 + l1) + (l2 + l3);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_P_FULL + mt));
+        }
+        if (!run) break;
+        // ---- segment epilogue: O stays in TMEM until O_FREE is signalled
+        if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
+        if (warp_active) {
+          tc_fence_after();
+          OutT* orow = static_cast<OutT*>(p.o) + ((size_t)(x.q_off + i) * p.Hq + x.g * G + hj) * D;
+          auto store_chunk = [&](int q, const float* v, float inv) {
+            if (!valid) return;
+            if constexpr (sizeof(OutT) == 4) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(orow + q * 32 + c) =
+                    make_float4(v[c] * inv, v[c + 1] * inv, v[c + 2] * inv, v[c + 3] * inv);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const __nv_bfloat162 bv = __floats2bfloat162_rn(v[c + 2 * h] * inv, v[c + 2 * h + 1] * inv);
+                  w[h] = *reinterpret_cast<const uint32_t*>(&bv);
+                }
+                *reinterpret_cast<uint4*>(orow + q * 32 + c) = make_uint4(w[0], w[1], w[2], w[3]);
+              }
+            }
+          };
+          if (complete) {
+            const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t raw[32];
+              tmem_ld32(tO + q * 32, raw);
+              tmem_wait_ld();
+              float v[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(raw[e]);
+              store_chunk(q, v, inv);
+            }
+          } else {
+            // ---- publish this segment's partial; the 32-row group arriving last merges
+            const int c_a = owner(ustart), c_b = owner(ustart + x.nblocks - 1);
+            const int which = (seg == 0) ? 0 : 1;
+            const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
+            __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t raw[32];
+              tmem_ld32(tO + q * 32, raw);
+              tmem_wait_ld();
+              float* po = work.part_o + myslot * D + q * 32;
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                __stcg(reinterpret_cast<float4*>(po + c),
+                       make_float4(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1]), __uint_as_float(raw[c + 2]),
+                                   __uint_as_float(raw[c + 3])));
+            }
+            __threadfence();
+            __syncwarp();
+            int prev = 0;
+            int32_t* counter = work.cnt + ((size_t)u * MT + mt) * 4 + q4;
+            if (lane == 0) prev = atomicAdd(counter, 1);
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev == c_b - c_a) {
+              __threadfence();
+              auto slot_of = [&](int cc) -> size_t {
+                const int wh = (cc == c_a && seg_start(cc) < ustart) ? 1 : 0;
+                return ((size_t)(cc * 2 + wh) * MT + mt) * 128 + m;
+              };
+              // combine in CTA order (not arrival order) so the result is deterministic
+              float M = m_used;
+              for (int cc = c_a; cc <= c_b; ++cc)
+                if (cc != cta) M = fmaxf(M, __ldcg(work.part_ml + slot_of(cc) * 2));
+              float L = 0.f;
+              for (int cc = c_a; cc <= c_b; ++cc) {
+                float mo = m_used, lo = l_sum;
+                if (cc != cta) {
+                  const float2 ml = __ldcg(reinterpret_cast<const float2*>(work.part_ml + slot_of(cc) * 2));
+                  mo = ml.x;
+                  lo = ml.y;
+                }
+                if (M > -INFINITY) L += lo * ex2(mo - M);
+              }
+              const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll 1
+              for (int q = 0; q < D / 32; ++q) {
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                for (int cc = c_a; cc <= c_b; ++cc) {
+                  if (cc == cta) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + q * 32, raw);
+                    tmem_wait_ld();
+                    const float fo = (M == -INFINITY) ? 0.f : ex2(m_used - M);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] += __uint_as_float(raw[e]) * fo;
+                  } else {
+                    const size_t sl = slot_of(cc);
+                    const float mo = __ldcg(work.part_ml + sl * 2);
+                    const float fo = (M == -INFINITY) ? 0.f : ex2(mo - M);
+                    const float* po = work.part_o + sl * D + q * 32;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                      const float4 w4 = __ldcg(reinterpret_cast<const float4*>(po + c));
+                      v[c] += w4.x * fo; v[c + 1] += w4.y * fo; v[c + 2] += w4.z * fo; v[c + 3] += w4.w * fo;
+                    }
+                  }
+                }
+                store_chunk(q, v, inv);
+              }
+              if (lane == 0) *counter = 0;  // ready for the next call
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_O_FREE + mt));
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_O_FREE + mt));
+        }
+      }
+      pos += len;
+      remaining -= len;
+      ++seg;
+      ++u;
+      k = 0;
+    }
   }
-  // ---------------------------------------------------------------- teardown
+  // ------------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (ok && *abort && threadIdx.x == 0) report(p.dev_status, SSV_ERR_TIMEOUT);
+  if (*abort && threadIdx.x == 0) report(p.dev_status, SSV_ERR_TIMEOUT);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -396,7 +725,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a [rows, heads, 128] bf16 tensor: dims (128, heads, rows),
-// box (64, box_heads, box_rows), 128-byte swizzle.
+// box (64, box_heads, box_rows), 128-byte swizzle, zero fill out of bounds.
 static bool encode_3d(CUtensorMap* m, const void* base, int heads, long long rows, int box_heads, int box_rows) {
   auto fn = encode_fn();
   if (!fn || rows <= 0) return false;
@@ -409,29 +738,76 @@ static bool encode_3d(CUtensorMap* m, const void* base, int heads, long long row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static int choose_mt(const AttnParams& p) {
+  const int G = p.Hq / p.Hkv;
+  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  return (max_rows * G > 128) ? 2 : 1;
+}
+
+struct WsLayout {
+  size_t cnt, ml, o, total;
+  int grid, mt, units;
+};
+
+static WsLayout ws_layout(const AttnParams& p) {
+  WsLayout L;
+  const int G = p.Hq / p.Hkv;
+  L.mt = choose_mt(p);
+  const int UR = L.mt * (128 / G);
+  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  L.units = (int)((long long)p.batch * p.Hkv * ((max_rows + UR - 1) / UR));
+  L.grid = sm_count();
+  size_t off = 0;
+  L.cnt = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)L.units * L.mt * 4, 256);
+  L.ml = off;
+  off = align_up(off + sizeof(float) * 2 * (size_t)(2 * L.grid) * L.mt * 128, 256);
+  L.o = off;
+  off = align_up(off + sizeof(float) * (size_t)(2 * L.grid) * L.mt * 128 * D, 256);
+  L.total = off;
+  return L;
+}
+
 bool attn_tc_supported(const AttnParams& p) {
   if (p.in_dtype != SSV_BF16 || p.d != D) return false;
   const int G = p.Hq / p.Hkv;
   if (G < 1 || G > 128 || (128 % G) != 0) return false;
-  if (p.max_block > 64) return false;
-  return encode_fn() != nullptr;
+  if (p.max_block > 64 || p.batch > kMaxBatch) return false;
+  // total key blocks must fit comfortably in int32
+  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
+                           ((p.max_cache + BN - 1) / BN + (max_rows + BN - 1) / BN);
+  if (blocks > (1LL << 30)) return false;
+  return encode_fn() != nullptr && sm_count() > 0;
 }
 
-template <typename OutT>
-static cudaError_t launch_t(const AttnParams& p, const TcMaps& maps, int R, int G, dim3 grid, cudaStream_t st) {
+size_t attn_tc_workspace(const AttnParams& p) { return ws_layout(p).total; }
+
+template <int MT, typename OutT>
+static cudaError_t launch_t(const AttnParams& p, const TcMaps& maps, const TcWork& w, int G, int grid,
+                            cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_tc_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_ALLOC);
+    attr_err = cudaFuncSetAttribute(attn_tc_kernel<MT, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<MT>::SM_ALLOC);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_tc_kernel<OutT><<<grid, kThreads, SM_ALLOC, st>>>(maps, p, R, G);
+  attn_tc_kernel<MT, OutT><<<grid, Cfg<MT>::kThreads, Cfg<MT>::SM_ALLOC, st>>>(maps, p, w, G);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t st) {
   const int G = p.Hq / p.Hkv;
-  const int R = BM / G;
+  const int R = 128 / G;
+  const WsLayout L = ws_layout(p);
   TcMaps maps;
   if (!encode_3d(&maps.q, p.q, p.Hq, p.total_rows, G, R)) return cudaErrorInvalidValue;
   if (!encode_3d(&maps.kn, p.k_new, p.Hkv, p.total_rows, 1, BN)) return cudaErrorInvalidValue;
@@ -443,10 +819,17 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t st) {
     maps.kc = maps.kn;  // never read: every sequence has C = 0
     maps.vc = maps.vn;
   }
-  const int max_rows = p.max_new + 2 * p.max_block;
-  dim3 grid((max_rows + R - 1) / R, p.Hkv, p.batch);
-  if (p.out_dtype == SSV_F32) return launch_t<float>(p, maps, R, G, grid, st);
-  return launch_t<__nv_bfloat16>(p, maps, R, G, grid, st);
+  char* w = static_cast<char*>(ws);
+  TcWork work;
+  work.cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  work.part_ml = reinterpret_cast<float*>(w + L.ml);
+  work.part_o = reinterpret_cast<float*>(w + L.o);
+  if (L.mt == 2) {
+    if (p.out_dtype == SSV_F32) return launch_t<2, float>(p, maps, work, G, L.grid, st);
+    return launch_t<2, __nv_bfloat16>(p, maps, work, G, L.grid, st);
+  }
+  if (p.out_dtype == SSV_F32) return launch_t<1, float>(p, maps, work, G, L.grid, st);
+  return launch_t<1, __nv_bfloat16>(p, maps, work, G, L.grid, st);
 }
 
 }  // namespace tc

@@ -63,6 +63,10 @@ extern "C" ssv_status ssv_verify_attn_workspace(const ssv_attn_args* a, size_t* 
   const ssv_status st = attn_check(a);
   if (st != SSV_OK) return st;
   *bytes = 256;
+  if (a->batch > 0 && a->total_rows > 0) {
+    const AttnParams p = to_params(a);
+    if (tc::attn_tc_supported(p)) *bytes = tc::attn_tc_workspace(p);
+  }
   return SSV_OK;
 }
 
@@ -75,7 +79,7 @@ extern "C" ssv_status ssv_verify_attn(const ssv_attn_args* a, void* ws, size_t w
   if (need > 0 && (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need)) return SSV_ERR_WORKSPACE;
   const AttnParams p = to_params(a);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = tc::attn_tc_supported(p) ? tc::launch_attn_tc(p, s) : launch_attn_simt(p, s);
+  const cudaError_t e = tc::attn_tc_supported(p) ? tc::launch_attn_tc(p, ws, s) : launch_attn_simt(p, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }
 
