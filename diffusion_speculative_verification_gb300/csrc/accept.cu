@@ -28,14 +28,17 @@
 namespace ssv {
 
 constexpr int kAccThreads = 256;
-constexpr int kAccPerThread = 16;
-constexpr int kAccChunk = kAccThreads * kAccPerThread;  // 4096 vocab entries per CTA
+constexpr int kAccVec = 4;                                 // elements per vector access
+constexpr int kAccIters = 8;                               // vector accesses per thread per stream
+constexpr int kAccPerThread = kAccVec * kAccIters;         // 32
+constexpr int kAccChunk = kAccThreads * kAccPerThread;     // 8192 vocab entries per CTA
 
 struct AccPartial {
-  float m_a, m_b;    // chunk max of l/T and of draft/T          (reject)
-  double s_a, s_b;   // sum over the chunk of exp(x - chunk max)  (reject)
-  float val;         // best decision score                       (argmax / gumbel)
-  int idx;           // its first index
+  float m_a, m_b;          // chunk max of l/T and of draft/T                      (reject)
+  float sa_hi, sa_lo;      // compensated sum over the chunk of exp(l/T - m_a)     (reject)
+  float sb_hi, sb_lo;      // same for the draft row                              (reject)
+  float val;               // best decision score                                  (argmax / gumbel)
+  int idx;                 // its first index
 };
 
 struct SlotNorm {
@@ -46,7 +49,9 @@ struct SlotNorm {
 struct AcceptParams {
   int mode;
   float T;
+  float rT;                // 1 / T (rejection sampling scales logits by it)
   int V;
+  int vec;                 // rows allow 4-element vector accesses
   int batch;
   int total_slots;
   int nchunks;
@@ -72,7 +77,7 @@ struct AcceptParams {
   int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
   AccPartial* part;     // [total_slots][nchunks]
   SlotNorm* norm;       // [total_slots]
-  double* smass;        // [batch][nchunks][2] : residual mass, p mass
+  float* smass;         // [batch][nchunks][4] : residual mass (hi, lo), p mass (hi, lo)
 };
 
 struct AccWorkspaceLayout {
@@ -87,7 +92,7 @@ static AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks)
   L.emit = o;       o = align_up(o + sizeof(int32_t) * 2 * (size_t)batch, 256);
   L.part = o;       o = align_up(o + sizeof(AccPartial) * (size_t)total_slots * nchunks, 256);
   L.norm = o;       o = align_up(o + sizeof(SlotNorm) * (size_t)total_slots, 256);
-  L.smass = o;      o = align_up(o + sizeof(double) * 2 * (size_t)batch * nchunks, 256);
+  L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nchunks, 256);
   L.total = o;
   return L;
 }
@@ -97,6 +102,42 @@ __device__ __forceinline__ float ld_logit(const void* base, size_t i) {
   return Elem<T>::to_f32(static_cast<const T*>(base)[i]);
 }
 
+// 4 consecutive elements starting at i (i % 4 == 0, row base suitably aligned), streaming load
+template <typename T>
+__device__ __forceinline__ void ld_vec4(const void* base, size_t i, float* out) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(base) + i));
+    out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+  } else {
+    const uint2 v = __ldcs(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + i));
+    out[0] = __uint_as_float(v.x << 16); out[1] = __uint_as_float(v.x & 0xffff0000u);
+    out[2] = __uint_as_float(v.y << 16); out[3] = __uint_as_float(v.y & 0xffff0000u);
+  }
+}
+
+// Loads this thread's kAccPerThread entries of a chunk: entry (it, k) is vocab
+// index c0 + (it * kAccThreads + tid) * 4 + k, so a thread's indices increase
+// with (it, k).  Entries past V read as `fill`.
+template <typename T>
+__device__ __forceinline__ void ld_chunk(const void* base, size_t rbase, int c0, int V, bool vec, float fill,
+                                         float* x) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int it = 0; it < kAccIters; ++it) {
+    const int e = c0 + (it * kAccThreads + tid) * kAccVec;
+    if (vec && e + kAccVec <= V) {
+      ld_vec4<T>(base, rbase + e, x + it * kAccVec);
+    } else {
+#pragma unroll
+      for (int k = 0; k < kAccVec; ++k) x[it * kAccVec + k] = (e + k < V) ? ld_logit<T>(base, rbase + e + k) : fill;
+    }
+  }
+}
+
+__device__ __forceinline__ int chunk_index(int c0, int j) {  // vocab index of a thread's j-th entry
+  return c0 + ((j / kAccVec) * kAccThreads + (int)threadIdx.x) * kAccVec + (j % kAccVec);
+}
+
 __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
   const float y = x - c;
   const float t = s + y;
@@ -104,11 +145,21 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
   s = t;
 }
 
+// (h1, l1) += (h2, l2) with an error-free transformation of the leading terms
+__device__ __forceinline__ void two_sum_acc(float& h1, float& l1, float h2, float l2) {
+  const float s = h1 + h2;
+  const float bb = s - h1;
+  const float err = (h1 - (s - bb)) + (h2 - bb);
+  h1 = s;
+  l1 = l1 + l2 + err;
+}
+
 // ---- block reductions (256 threads) ---------------------------------------
 __device__ __forceinline__ void argmax_combine(float& v, int& i, float ov, int oi) {
   if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
 }
 
+// result valid in thread 0
 __device__ void block_argmax(float& v, int& i) {
   __shared__ float sv[kAccThreads / 32];
   __shared__ int si[kAccThreads / 32];
@@ -118,53 +169,47 @@ __device__ void block_argmax(float& v, int& i) {
     argmax_combine(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
   if (lane == 0) { sv[wid] = v; si[wid] = i; }
   __syncthreads();
-  if (wid == 0) {
-    v = lane < kAccThreads / 32 ? sv[lane] : -INFINITY;
-    i = lane < kAccThreads / 32 ? si[lane] : INT_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      argmax_combine(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kAccThreads / 32; ++w) argmax_combine(v, i, sv[w], si[w]);
   }
-  __syncthreads();
 }
 
-__device__ float block_max(float v) {
-  __shared__ float sv[kAccThreads / 32];
-  __shared__ float res;
+// all threads receive the maxima
+__device__ void block_max2(float& a, float& b) {
+  __shared__ float sa[kAccThreads / 32], sb[kAccThreads / 32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) sv[wid] = v;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = sv[0];
-    for (int w = 1; w < kAccThreads / 32; ++w) m = fmaxf(m, sv[w]);
-    res = m;
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
   }
+  if (lane == 0) { sa[wid] = a; sb[wid] = b; }
   __syncthreads();
-  const float r = res;
-  __syncthreads();
-  return r;
+  a = sa[0];
+  b = sb[0];
+#pragma unroll
+  for (int w = 1; w < kAccThreads / 32; ++w) { a = fmaxf(a, sa[w]); b = fmaxf(b, sb[w]); }
 }
 
-// Sum in a fixed order (lane tree, then warps in order): deterministic.
-__device__ double block_sum(double v) {
-  __shared__ double sv[kAccThreads / 32];
-  __shared__ double res;
+// compensated sums of two (hi, lo) pairs, fixed order; result valid in thread 0
+__device__ void block_sum2x2(float& h1, float& l1, float& h2, float& l2) {
+  __shared__ float s[4][kAccThreads / 32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) sv[wid] = v;
+  for (int o = 16; o > 0; o >>= 1) {
+    const float a = __shfl_xor_sync(0xffffffffu, h1, o), b = __shfl_xor_sync(0xffffffffu, l1, o);
+    const float c = __shfl_xor_sync(0xffffffffu, h2, o), d = __shfl_xor_sync(0xffffffffu, l2, o);
+    two_sum_acc(h1, l1, a, b);
+    two_sum_acc(h2, l2, c, d);
+  }
+  if (lane == 0) { s[0][wid] = h1; s[1][wid] = l1; s[2][wid] = h2; s[3][wid] = l2; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double s = 0.0;
-    for (int w = 0; w < kAccThreads / 32; ++w) s += sv[w];
-    res = s;
+    for (int w = 1; w < kAccThreads / 32; ++w) {
+      two_sum_acc(h1, l1, s[0][w], s[1][w]);
+      two_sum_acc(h2, l2, s[2][w], s[3][w]);
+    }
   }
-  __syncthreads();
-  const double r = res;
-  __syncthreads();
-  return r;
 }
 
 // Exclusive prefix sum over the block (thread order), fp64.
@@ -185,19 +230,11 @@ __device__ double block_exclusive_scan(double v) {
   return before + incl - v;
 }
 
-// ---- per-sequence validity (uniform over the block) ------------------------
-__device__ bool seq_valid(const AcceptParams& p, int b) {
-  __shared__ int s_ok;
-  if (threadIdx.x < 32) {
-    const int B = p.block[b], g = p.gamma[b];
-    bool ok = B >= 1 && B <= 64 && g >= 0 && g <= B && p.slot_off[b] + B <= p.total_slots;
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) ok = warp_tau_is_permutation(p.tau + p.slot_off[b], B);
-    if (threadIdx.x == 0) s_ok = ok;
-  }
-  __syncthreads();
-  const bool ok = s_ok;
-  __syncthreads();
+// ---- per-sequence validity, checked by warp 0 (all 32 lanes) -----------------
+__device__ bool warp_seq_valid(const AcceptParams& p, int b) {
+  const int B = p.block[b], g = p.gamma[b];
+  bool ok = B >= 1 && B <= 64 && g >= 0 && g <= B && p.slot_off[b] + B <= p.total_slots;
+  if (ok) ok = warp_tau_is_permutation(p.tau + p.slot_off[b], B);
   return ok;
 }
 
@@ -222,23 +259,30 @@ __device__ void accept_finalize(const AcceptParams& p, int b) {
       s_dec[tid] = i;
       s_ok[tid] = (tid < g) && (p.draft_tokens[k] == i);
     } else {
+      const bool with_draft = tid < g;  // the draft row is read only for tested stages
       float ma = -INFINITY, mb = -INFINITY;
-      for (int c = 0; c < p.nchunks; ++c) { ma = fmaxf(ma, __ldcg(&pp[c].m_a)); mb = fmaxf(mb, __ldcg(&pp[c].m_b)); }
+      for (int c = 0; c < p.nchunks; ++c) {
+        ma = fmaxf(ma, __ldcg(&pp[c].m_a));
+        if (with_draft) mb = fmaxf(mb, __ldcg(&pp[c].m_b));
+      }
       double sa = 0.0, sb = 0.0;
       for (int c = 0; c < p.nchunks; ++c) {
-        sa += __ldcg(&pp[c].s_a) * exp((double)__ldcg(&pp[c].m_a) - (double)ma);
-        sb += __ldcg(&pp[c].s_b) * exp((double)__ldcg(&pp[c].m_b) - (double)mb);
+        sa += ((double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo)) *
+              exp((double)__ldcg(&pp[c].m_a) - (double)ma);
+        if (with_draft)
+          sb += ((double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo)) *
+                exp((double)__ldcg(&pp[c].m_b) - (double)mb);
       }
       SlotNorm nm;
       nm.m_a = ma; nm.m_b = mb; nm.s_a = sa; nm.s_b = sb;
       p.norm[k] = nm;
       s_dec[tid] = -1;
       int ok = 0;
-      if (tid < g) {
+      if (with_draft) {
         const int d = p.draft_tokens[k];
         if (d >= 0 && d < p.V) {
-          const float ad = __fdiv_rn(ld_logit<T>(p.logits, (size_t)k * p.V + d), p.T);
-          const float bd = __fdiv_rn(ld_logit<T>(p.draft_logits, (size_t)k * p.V + d), p.T);
+          const float ad = ld_logit<T>(p.logits, (size_t)k * p.V + d) * p.rT;
+          const float bd = ld_logit<T>(p.draft_logits, (size_t)k * p.V + d) * p.rT;
           // p(d)/q(d) = exp((a_d - M_a) - (b_d - M_b)) * S_b / S_a
           const double ratio = exp(((double)ad - (double)ma) - ((double)bd - (double)mb)) * (sb / sa);
           ok = (double)p.u_accept[k] < ratio;
@@ -278,82 +322,85 @@ __device__ void accept_finalize(const AcceptParams& p, int b) {
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_reduce_kernel(const AcceptParams p) {
+  __shared__ int s_ok, s_last;
   const int slot = blockIdx.x / p.nchunks;
   const int chunk = blockIdx.x % p.nchunks;
   const int b = find_seq_by_slot(p.slot_off, p.batch, slot);
   if (b < 0) return;
   const int off = p.slot_off[b];
-  if (slot - off >= p.block[b]) return;
-  if (!seq_valid(p, b)) {
-    if (threadIdx.x == 0 && slot == off && chunk == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
-    return;
-  }
-  const int B = p.block[b];
-  const int need = min(p.gamma[b] + 1, B);
-  if (p.tau[slot] > need) return;
-
+  const int B = p.block[b], g = p.gamma[b];
+  if (B < 1 || slot - off >= B) return;
+  const int need = min(g + 1, B);
+  const int st = p.tau[slot];
+  if (st < 1 || st > need) return;  // not a verified row (a bad map is reported below)
   const int tid = threadIdx.x;
   const size_t rbase = (size_t)slot * p.V;
   const int c0 = chunk * kAccChunk;
+  const bool vec = p.vec != 0;
+
+  // ---- streaming loads first (all in flight), validation overlaps them
+  float xa[kAccPerThread], xb[kAccPerThread];
+  const bool draft = (MODE == SSV_ACCEPT_REJECT) && st <= g;
+  const float* nrow = nullptr;
+  bool nrow_ok = true;
+  if (MODE == SSV_ACCEPT_GUMBEL) {
+    const int nr = p.noise_row[slot];
+    nrow_ok = nr >= 0 && nr < p.n_noise_rows;
+    nrow = p.noise + (size_t)(nrow_ok ? nr : 0) * p.V;
+  }
+  ld_chunk<T>(p.logits, rbase, c0, p.V, vec, -INFINITY, xa);
+  if (MODE == SSV_ACCEPT_GUMBEL) ld_chunk<float>(nrow, 0, c0, p.V, vec, 0.f, xb);
+  if (draft) ld_chunk<T>(p.draft_logits, rbase, c0, p.V, vec, -INFINITY, xb);
+  if (tid < 32) {
+    const bool ok = warp_seq_valid(p, b);
+    if (tid == 0) {
+      s_ok = ok && nrow_ok;
+      if (!ok && slot == off + 0 && chunk == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
+      if (!nrow_ok && chunk == 0) report(p.dev_status, SSV_ERR_INVALID);
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;
+
   AccPartial out;
   if (MODE != SSV_ACCEPT_REJECT) {
-    const float* nrow = nullptr;
     if (MODE == SSV_ACCEPT_GUMBEL) {
-      const int nr = p.noise_row[slot];
-      if (nr < 0 || nr >= p.n_noise_rows) {
-        if (tid == 0) report(p.dev_status, SSV_ERR_INVALID);
-        return;
-      }
-      nrow = p.noise + (size_t)nr * p.V;
+      const bool unit_t = p.T == 1.0f;  // l / 1 is exact
+#pragma unroll
+      for (int j = 0; j < kAccPerThread; ++j)
+        xa[j] = __fadd_rn(unit_t ? xa[j] : __fdiv_rn(xa[j], p.T), xb[j]);
     }
     float best = -INFINITY;
     int bi = INT_MAX;
-    float x[kAccPerThread];
 #pragma unroll
-    for (int it = 0; it < kAccPerThread; ++it) {
-      const int e = c0 + it * kAccThreads + tid;
-      x[it] = e < p.V ? ld_logit<T>(p.logits, rbase + e) : -INFINITY;
-    }
-    if (MODE == SSV_ACCEPT_GUMBEL) {
-#pragma unroll
-      for (int it = 0; it < kAccPerThread; ++it) {
-        const int e = c0 + it * kAccThreads + tid;
-        if (e < p.V) x[it] = __fadd_rn(__fdiv_rn(x[it], p.T), nrow[e]);
-      }
-    }
-#pragma unroll
-    for (int it = 0; it < kAccPerThread; ++it) {
-      const int e = c0 + it * kAccThreads + tid;
-      if (e < p.V && x[it] > best) { best = x[it]; bi = e; }
+    for (int j = 0; j < kAccPerThread; ++j) {
+      const int e = chunk_index(c0, j);
+      if (e < p.V && (xa[j] > best || bi == INT_MAX)) { best = xa[j]; bi = e; }
     }
     block_argmax(best, bi);
     out.val = best; out.idx = bi;
-    out.m_a = out.m_b = 0.f; out.s_a = out.s_b = 0.0;
+    out.m_a = out.m_b = out.sa_hi = out.sa_lo = out.sb_hi = out.sb_lo = 0.f;
   } else {
-    float xa[kAccPerThread], xb[kAccPerThread];
-#pragma unroll
-    for (int it = 0; it < kAccPerThread; ++it) {
-      const int e = c0 + it * kAccThreads + tid;
-      xa[it] = e < p.V ? __fdiv_rn(ld_logit<T>(p.logits, rbase + e), p.T) : -INFINITY;
-      xb[it] = e < p.V ? __fdiv_rn(ld_logit<T>(p.draft_logits, rbase + e), p.T) : -INFINITY;
-    }
     float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-    for (int it = 0; it < kAccPerThread; ++it) { ma = fmaxf(ma, xa[it]); mb = fmaxf(mb, xb[it]); }
-    ma = block_max(ma);
-    mb = block_max(mb);
+    for (int j = 0; j < kAccPerThread; ++j) {
+      xa[j] *= p.rT;
+      ma = fmaxf(ma, xa[j]);
+      if (draft) { xb[j] *= p.rT; mb = fmaxf(mb, xb[j]); }
+    }
+    block_max2(ma, mb);
     float sa = 0.f, ca = 0.f, sb = 0.f, cb = 0.f;
 #pragma unroll
-    for (int it = 0; it < kAccPerThread; ++it) {
-      kahan_add(sa, ca, expf(xa[it] - ma));
-      kahan_add(sb, cb, expf(xb[it] - mb));
+    for (int j = 0; j < kAccPerThread; ++j) {
+      kahan_add(sa, ca, expf(xa[j] - ma));
+      if (draft) kahan_add(sb, cb, expf(xb[j] - mb));
     }
+    float la = -ca, lb = -cb;
+    block_sum2x2(sa, la, sb, lb);
     out.m_a = ma; out.m_b = mb;
-    out.s_a = block_sum((double)sa - (double)ca);
-    out.s_b = block_sum((double)sb - (double)cb);
+    out.sa_hi = sa; out.sa_lo = la; out.sb_hi = sb; out.sb_lo = lb;
     out.val = 0.f; out.idx = 0;
   }
-  __shared__ int s_last;
   if (tid == 0) {
     p.part[(size_t)slot * p.nchunks + chunk] = out;
     __threadfence();
@@ -369,12 +416,16 @@ accept_reduce_kernel(const AcceptParams p) {
 }
 
 // ---- rejection sampling: emitted token ------------------------------------
+// Weight of vocab entry e: p_e = exp(l_e / T - M_a) / S_a and, for a residual
+// sample, (p_e - q_e)_+ with q likewise.  The same expression serves the chunk
+// masses and the final in-chunk scan.
 template <typename T>
-__device__ __forceinline__ void sample_weights(const AcceptParams& p, const SlotNorm& nm, size_t rbase, int e,
-                                               float inv_sa, float inv_sb, bool residual, float& wr, float& wp) {
-  const float pv = expf(__fdiv_rn(ld_logit<T>(p.logits, rbase + e), p.T) - nm.m_a) * inv_sa;
-  float qv = 0.f;
-  if (residual) qv = expf(__fdiv_rn(ld_logit<T>(p.draft_logits, rbase + e), p.T) - nm.m_b) * inv_sb;
+__device__ __forceinline__ void sample_weight(const AcceptParams& p, const SlotNorm& nm, size_t rbase, float la,
+                                              float lb, float inv_sa, float inv_sb, bool residual, float& wr,
+                                              float& wp) {
+  (void)rbase;
+  const float pv = expf(la * p.rT - nm.m_a) * inv_sa;
+  const float qv = residual ? expf(lb * p.rT - nm.m_b) * inv_sb : 0.f;
   wp = pv;
   wr = residual ? fmaxf(pv - qv, 0.f) : 0.f;
 }
@@ -382,11 +433,18 @@ __device__ __forceinline__ void sample_weights(const AcceptParams& p, const Slot
 template <typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_sample_kernel(const AcceptParams p) {
+  __shared__ int s_ok, s_last;
   const int b = blockIdx.x / p.nchunks;
   const int chunk = blockIdx.x % p.nchunks;
+  const int tid = threadIdx.x;
   // A sequence whose stage map or sizes were rejected never ran its finalize
   // step, so its emission record may be stale: skip it.
-  if (!seq_valid(p, b)) return;
+  if (tid < 32) {
+    const bool ok = warp_seq_valid(p, b);
+    if (tid == 0) s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
   const int eslot = p.emit[2 * b];
   const int soff = p.slot_off[b];
   const int nacc = p.n_acc[b];
@@ -396,26 +454,24 @@ accept_sample_kernel(const AcceptParams p) {
   const float inv_sa = (float)(1.0 / nm.s_a);
   const float inv_sb = residual ? (float)(1.0 / nm.s_b) : 0.f;
   const size_t rbase = (size_t)eslot * p.V;
-  const int tid = threadIdx.x;
   const int c0 = chunk * kAccChunk;
+  const bool vec = p.vec != 0;
+  float xa[kAccPerThread], xb[kAccPerThread];
+  ld_chunk<T>(p.logits, rbase, c0, p.V, vec, -INFINITY, xa);
+  if (residual) ld_chunk<T>(p.draft_logits, rbase, c0, p.V, vec, -INFINITY, xb);
   float sr = 0.f, cr = 0.f, sp = 0.f, cp = 0.f;
-#pragma unroll 4
-  for (int it = 0; it < kAccPerThread; ++it) {
-    const int e = c0 + it * kAccThreads + tid;
-    if (e < p.V) {
-      float wr, wp;
-      sample_weights<T>(p, nm, rbase, e, inv_sa, inv_sb, residual, wr, wp);
-      kahan_add(sr, cr, wr);
-      kahan_add(sp, cp, wp);
-    }
+#pragma unroll
+  for (int j = 0; j < kAccPerThread; ++j) {
+    float wr, wp;
+    sample_weight<T>(p, nm, rbase, xa[j], residual ? xb[j] : 0.f, inv_sa, inv_sb, residual, wr, wp);
+    kahan_add(sr, cr, wr);
+    kahan_add(sp, cp, wp);
   }
-  const double mr = block_sum((double)sr - (double)cr);
-  const double mp = block_sum((double)sp - (double)cp);
-  __shared__ int s_last;
+  float lr = -cr, lp = -cp;
+  block_sum2x2(sr, lr, sp, lp);
   if (tid == 0) {
-    double* sm = p.smass + ((size_t)b * p.nchunks + chunk) * 2;
-    sm[0] = mr;
-    sm[1] = mp;
+    float* sm = p.smass + ((size_t)b * p.nchunks + chunk) * 4;
+    sm[0] = sr; sm[1] = lr; sm[2] = sp; sm[3] = lp;
     __threadfence();
     const int prev = atomicAdd(&p.cnt_sample[b], 1);
     s_last = (prev == p.nchunks - 1);
@@ -429,18 +485,20 @@ accept_sample_kernel(const AcceptParams p) {
   __shared__ double s_before, s_thresh;
   __shared__ int s_use_res;
   if (tid == 0) {
-    const double* sm = p.smass + (size_t)b * p.nchunks * 2;
+    const float* sm = p.smass + (size_t)b * p.nchunks * 4;
     double zr = 0.0, zp = 0.0;
-    for (int c = 0; c < p.nchunks; ++c) { zr += __ldcg(&sm[2 * c]); zp += __ldcg(&sm[2 * c + 1]); }
+    for (int c = 0; c < p.nchunks; ++c) {
+      zr += (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1]);
+      zp += (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
+    }
     const int use_res = residual && zr > 0.0;
-    const int w = use_res ? 0 : 1;
     const double Z = use_res ? zr : zp;
     const double t = (double)p.u_sample[b] * Z;
-    double cum = 0.0;
+    double cum = 0.0, before = 0.0, before_last = 0.0;
     int cs = -1, last_nz = 0;
-    double before = 0.0, before_last = 0.0;
     for (int c = 0; c < p.nchunks; ++c) {
-      const double m = __ldcg(&sm[2 * c + w]);
+      const double m = use_res ? (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1])
+                               : (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
       if (m > 0.0) { last_nz = c; before_last = cum; }
       if (cs < 0 && cum + m > t) { cs = c; before = cum; }
       cum += m;
@@ -461,8 +519,10 @@ accept_sample_kernel(const AcceptParams p) {
     const int e = e0 + j;
     double w = 0.0;
     if (e < p.V) {
+      const float la = ld_logit<T>(p.logits, rbase + e);
+      const float lb = residual ? ld_logit<T>(p.draft_logits, rbase + e) : 0.f;
       float wr, wp;
-      sample_weights<T>(p, nm, rbase, e, inv_sa, inv_sb, residual, wr, wp);
+      sample_weight<T>(p, nm, rbase, la, lb, inv_sa, inv_sb, residual, wr, wp);
       w = use_res ? (double)wr : (double)wp;
     }
     if (w > 0.0) last_pos = e;
@@ -553,7 +613,10 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
   AcceptParams p;
   p.mode = a->mode;
   p.T = a->T;
+  p.rT = a->T > 0.f ? 1.0f / a->T : 0.f;
   p.V = a->V;
+  p.vec = ((a->V % 4) == 0 && ((uintptr_t)a->logits & 15u) == 0 && ((uintptr_t)a->draft_logits & 15u) == 0 &&
+           ((uintptr_t)a->noise & 15u) == 0) ? 1 : 0;
   p.batch = a->batch;
   p.total_slots = a->total_slots;
   p.nchunks = nchunks;
@@ -578,7 +641,7 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
   p.emit = reinterpret_cast<int32_t*>(w + L.emit);
   p.part = reinterpret_cast<AccPartial*>(w + L.part);
   p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
-  p.smass = reinterpret_cast<double*>(w + L.smass);
+  p.smass = reinterpret_cast<float*>(w + L.smass);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool bf = a->logits_dtype == SSV_BF16;
   int mode = a->mode;
@@ -654,7 +717,10 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   AcceptParams p;
   p.mode = a->mode;
   p.T = a->T;
+  p.rT = a->T > 0.f ? 1.0f / a->T : 0.f;
   p.V = a->V;
+  p.vec = ((a->V % 4) == 0 && ((uintptr_t)a->logits & 15u) == 0 && ((uintptr_t)a->draft_logits & 15u) == 0 &&
+           ((uintptr_t)a->noise & 15u) == 0) ? 1 : 0;
   p.batch = a->batch;
   p.total_slots = a->total_slots;
   p.nchunks = nchunks;
@@ -679,7 +745,7 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   p.emit = reinterpret_cast<int32_t*>(w + L.emit);
   p.part = reinterpret_cast<AccPartial*>(w + L.part);
   p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
-  p.smass = reinterpret_cast<double*>(w + L.smass);
+  p.smass = reinterpret_cast<float*>(w + L.smass);
   const bool bf = a->logits_dtype == SSV_BF16;
   int mode = a->mode;
   if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;

@@ -242,7 +242,7 @@ SSV_API ssv_status ssv_accept(const ssv_accept_args* a, void* workspace, size_t 
  * GPU that loads libssv holds until the process exits.
  *  - Same arguments, semantics and results as ssv_accept.
  *  - Calls whose scratch would exceed 4 MiB (roughly total_slots *
- *    ceil(V / 4096) > 120000 chunk records, e.g. more than ~3000 slots at
+ *    ceil(V / 8192) > 120000 chunk records, e.g. more than ~6000 slots at
  *    V = 151936) return SSV_ERR_WORKSPACE and launch nothing.
  *  - Calls nothing that allocates: no cudaMalloc/cudaFree, no allocating
  *    library routine.  It clears its arrival counters with a memset on

@@ -82,8 +82,8 @@ def test_noalloc_matches_workspace_path_two_calls_in_a_row():
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
     ensure_built()
-    # 4000 slots x 38 vocab chunks of partial records exceed the 4 MiB array;
-    # the refusal happens on the host before any pointer is touched.
-    a = ssv.AcceptArgs(ssv.ARGMAX, 0.0, 151936, 4000, 4000, 1, ssv.SSV_F32, 16, None, 16, 16, 16, 16, 16,
+    # 8000 slots x 19 vocab chunks of 32-byte partial records exceed the 4 MiB
+    # array; the refusal happens on the host before any pointer is touched.
+    a = ssv.AcceptArgs(ssv.ARGMAX, 0.0, 151936, 8000, 8000, 1, ssv.SSV_F32, 16, None, 16, 16, 16, 16, 16,
                        None, 0, None, None, None, 16, 16, 16, None)
     assert ssv.lib().ssv_accept_noalloc(C.byref(a), None) == ssv.SSV_ERR_WORKSPACE
