@@ -34,22 +34,28 @@ constexpr int kAccPerThread = kAccVec * kAccIters;         // 32
 constexpr int kAccChunk = kAccThreads * kAccPerThread;     // 8192 vocab entries per CTA
 
 struct AccPartial {
-  float m_a, m_b;          // chunk max of l/T and of draft/T                      (reject)
-  float sa_hi, sa_lo;      // compensated sum over the chunk of exp(l/T - m_a)     (reject)
+  float m_a, m_b;          // chunk max of the raw logits and of the draft logits  (reject)
+  float sa_hi, sa_lo;      // compensated sum over the chunk of 2^((l - m_a) c2)   (reject)
   float sb_hi, sb_lo;      // same for the draft row                              (reject)
   float val;               // best decision score                                  (argmax / gumbel)
   int idx;                 // its first index
 };
 
-struct SlotNorm {
+struct SlotNorm {  // p_v = 2^((l_v - m_a) c2) / s_a, q likewise
   float m_a, m_b;
   double s_a, s_b;
 };
 
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct AcceptParams {
   int mode;
   float T;
-  float rT;                // 1 / T (rejection sampling scales logits by it)
+  float c2;                // log2(e) / T: rejection-sampling weights are 2^((l - max) * c2)
   int V;
   int vec;                 // rows allow 4-element vector accesses
   int batch;
@@ -265,13 +271,14 @@ __device__ void accept_finalize(const AcceptParams& p, int b) {
         ma = fmaxf(ma, __ldcg(&pp[c].m_a));
         if (with_draft) mb = fmaxf(mb, __ldcg(&pp[c].m_b));
       }
+      const double c2 = (double)p.c2;
       double sa = 0.0, sb = 0.0;
       for (int c = 0; c < p.nchunks; ++c) {
         sa += ((double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo)) *
-              exp((double)__ldcg(&pp[c].m_a) - (double)ma);
+              exp2(((double)__ldcg(&pp[c].m_a) - (double)ma) * c2);
         if (with_draft)
           sb += ((double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo)) *
-                exp((double)__ldcg(&pp[c].m_b) - (double)mb);
+                exp2(((double)__ldcg(&pp[c].m_b) - (double)mb) * c2);
       }
       SlotNorm nm;
       nm.m_a = ma; nm.m_b = mb; nm.s_a = sa; nm.s_b = sb;
@@ -281,10 +288,10 @@ __device__ void accept_finalize(const AcceptParams& p, int b) {
       if (with_draft) {
         const int d = p.draft_tokens[k];
         if (d >= 0 && d < p.V) {
-          const float ad = ld_logit<T>(p.logits, (size_t)k * p.V + d) * p.rT;
-          const float bd = ld_logit<T>(p.draft_logits, (size_t)k * p.V + d) * p.rT;
-          // p(d)/q(d) = exp((a_d - M_a) - (b_d - M_b)) * S_b / S_a
-          const double ratio = exp(((double)ad - (double)ma) - ((double)bd - (double)mb)) * (sb / sa);
+          const double ld = ld_logit<T>(p.logits, (size_t)k * p.V + d);
+          const double qd = ld_logit<T>(p.draft_logits, (size_t)k * p.V + d);
+          // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
+          const double ratio = exp2(((ld - (double)ma) - (qd - (double)mb)) * c2) * (sb / sa);
           ok = (double)p.u_accept[k] < ratio;
         } else {
           report(p.dev_status, SSV_ERR_INVALID);
@@ -384,16 +391,16 @@ accept_reduce_kernel(const AcceptParams p) {
     float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kAccPerThread; ++j) {
-      xa[j] *= p.rT;
       ma = fmaxf(ma, xa[j]);
-      if (draft) { xb[j] *= p.rT; mb = fmaxf(mb, xb[j]); }
+      if (draft) mb = fmaxf(mb, xb[j]);
     }
     block_max2(ma, mb);
+    const float nma = -ma * p.c2, nmb = -mb * p.c2;
     float sa = 0.f, ca = 0.f, sb = 0.f, cb = 0.f;
 #pragma unroll
     for (int j = 0; j < kAccPerThread; ++j) {
-      kahan_add(sa, ca, expf(xa[j] - ma));
-      if (draft) kahan_add(sb, cb, expf(xb[j] - mb));
+      kahan_add(sa, ca, ex2f(fmaf(xa[j], p.c2, nma)));
+      if (draft) kahan_add(sb, cb, ex2f(fmaf(xb[j], p.c2, nmb)));
     }
     float la = -ca, lb = -cb;
     block_sum2x2(sa, la, sb, lb);
@@ -419,13 +426,10 @@ accept_reduce_kernel(const AcceptParams p) {
 // Weight of vocab entry e: p_e = exp(l_e / T - M_a) / S_a and, for a residual
 // sample, (p_e - q_e)_+ with q likewise.  The same expression serves the chunk
 // masses and the final in-chunk scan.
-template <typename T>
-__device__ __forceinline__ void sample_weight(const AcceptParams& p, const SlotNorm& nm, size_t rbase, float la,
-                                              float lb, float inv_sa, float inv_sb, bool residual, float& wr,
-                                              float& wp) {
-  (void)rbase;
-  const float pv = expf(la * p.rT - nm.m_a) * inv_sa;
-  const float qv = residual ? expf(lb * p.rT - nm.m_b) * inv_sb : 0.f;
+__device__ __forceinline__ void sample_weight(float c2, float nma, float nmb, float la, float lb, float inv_sa,
+                                              float inv_sb, bool residual, float& wr, float& wp) {
+  const float pv = ex2f(fmaf(la, c2, nma)) * inv_sa;
+  const float qv = residual ? ex2f(fmaf(lb, c2, nmb)) * inv_sb : 0.f;
   wp = pv;
   wr = residual ? fmaxf(pv - qv, 0.f) : 0.f;
 }
@@ -453,19 +457,20 @@ accept_sample_kernel(const AcceptParams p) {
   const SlotNorm nm = p.norm[eslot];
   const float inv_sa = (float)(1.0 / nm.s_a);
   const float inv_sb = residual ? (float)(1.0 / nm.s_b) : 0.f;
+  const float nma = -nm.m_a * p.c2, nmb = -nm.m_b * p.c2;
   const size_t rbase = (size_t)eslot * p.V;
   const int c0 = chunk * kAccChunk;
   const bool vec = p.vec != 0;
   float xa[kAccPerThread], xb[kAccPerThread];
   ld_chunk<T>(p.logits, rbase, c0, p.V, vec, -INFINITY, xa);
   if (residual) ld_chunk<T>(p.draft_logits, rbase, c0, p.V, vec, -INFINITY, xb);
+  float wr[kAccPerThread], wp[kAccPerThread];
   float sr = 0.f, cr = 0.f, sp = 0.f, cp = 0.f;
 #pragma unroll
   for (int j = 0; j < kAccPerThread; ++j) {
-    float wr, wp;
-    sample_weight<T>(p, nm, rbase, xa[j], residual ? xb[j] : 0.f, inv_sa, inv_sb, residual, wr, wp);
-    kahan_add(sr, cr, wr);
-    kahan_add(sp, cp, wp);
+    sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr[j], wp[j]);
+    kahan_add(sr, cr, wr[j]);
+    kahan_add(sp, cp, wp[j]);
   }
   float lr = -cr, lp = -cp;
   block_sum2x2(sr, lr, sp, lp);
@@ -509,36 +514,49 @@ accept_sample_kernel(const AcceptParams p) {
   __syncthreads();
   const int cs = s_chunk;
   const bool use_res = s_use_res != 0;
-  // contiguous run of kAccPerThread entries per thread, vocabulary order
-  const int e0 = cs * kAccChunk + tid * kAccPerThread;
-  double run[kAccPerThread];
-  double local = 0.0;
+  // Weights of the crossing chunk in vocabulary order, through shared memory
+  // (index i stored at i + i / 32 so that the contiguous runs read below are
+  // free of bank conflicts).
+  __shared__ float s_w[kAccChunk + kAccChunk / 32];
+  {
+    const int cc0 = cs * kAccChunk;
+    if (cs != chunk) {
+      ld_chunk<T>(p.logits, rbase, cc0, p.V, vec, -INFINITY, xa);
+      if (residual) ld_chunk<T>(p.draft_logits, rbase, cc0, p.V, vec, -INFINITY, xb);
+#pragma unroll
+      for (int j = 0; j < kAccPerThread; ++j)
+        sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr[j], wp[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kAccPerThread; ++j) {
+      const int li = chunk_index(0, j);  // index within the chunk
+      s_w[li + li / 32] = (cc0 + li < p.V) ? (use_res ? wr[j] : wp[j]) : 0.f;
+    }
+  }
+  __syncthreads();
+  // each thread: a contiguous run of kAccPerThread entries
+  const int r0 = tid * kAccPerThread;
+  float local = 0.f;
   int last_pos = -1;
 #pragma unroll
   for (int j = 0; j < kAccPerThread; ++j) {
-    const int e = e0 + j;
-    double w = 0.0;
-    if (e < p.V) {
-      const float la = ld_logit<T>(p.logits, rbase + e);
-      const float lb = residual ? ld_logit<T>(p.draft_logits, rbase + e) : 0.f;
-      float wr, wp;
-      sample_weight<T>(p, nm, rbase, la, lb, inv_sa, inv_sb, residual, wr, wp);
-      w = use_res ? (double)wr : (double)wp;
-    }
-    if (w > 0.0) last_pos = e;
-    run[j] = w;
+    const float w = s_w[(r0 + j) + (r0 + j) / 32];
     local += w;
+    if (w > 0.f) last_pos = cs * kAccChunk + r0 + j;
   }
-  const double excl = block_exclusive_scan(local);
+  const double excl = block_exclusive_scan((double)local);
   __shared__ int s_pick, s_last_nz;
   if (tid == 0) { s_pick = INT_MAX; s_last_nz = -1; }
   __syncthreads();
-  double acc = s_before + excl;
+  // remaining mass to cross inside this run, then an fp32 scan of the run
+  const float rel = (float)(s_thresh - (s_before + excl));
+  float acc = 0.f;
   int pick = INT_MAX;
 #pragma unroll
   for (int j = 0; j < kAccPerThread; ++j) {
-    acc += run[j];
-    if (pick == INT_MAX && run[j] > 0.0 && acc > s_thresh) pick = e0 + j;
+    const float w = s_w[(r0 + j) + (r0 + j) / 32];
+    acc += w;
+    if (pick == INT_MAX && w > 0.f && acc > rel) pick = cs * kAccChunk + r0 + j;
   }
   if (pick != INT_MAX) atomicMin(&s_pick, pick);
   if (last_pos >= 0) atomicMax(&s_last_nz, last_pos);
@@ -613,7 +631,7 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
   AcceptParams p;
   p.mode = a->mode;
   p.T = a->T;
-  p.rT = a->T > 0.f ? 1.0f / a->T : 0.f;
+  p.c2 = a->T > 0.f ? (float)(1.4426950408889634 / (double)a->T) : 0.f;
   p.V = a->V;
   p.vec = ((a->V % 4) == 0 && ((uintptr_t)a->logits & 15u) == 0 && ((uintptr_t)a->draft_logits & 15u) == 0 &&
            ((uintptr_t)a->noise & 15u) == 0) ? 1 : 0;
@@ -717,7 +735,7 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   AcceptParams p;
   p.mode = a->mode;
   p.T = a->T;
-  p.rT = a->T > 0.f ? 1.0f / a->T : 0.f;
+  p.c2 = a->T > 0.f ? (float)(1.4426950408889634 / (double)a->T) : 0.f;
   p.V = a->V;
   p.vec = ((a->V % 4) == 0 && ((uintptr_t)a->logits & 15u) == 0 && ((uintptr_t)a->draft_logits & 15u) == 0 &&
            ((uintptr_t)a->noise & 15u) == 0) ? 1 : 0;

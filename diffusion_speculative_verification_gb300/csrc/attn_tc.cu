@@ -52,20 +52,22 @@ using namespace ptx;
 
 constexpr int D = 128;
 constexpr int BN = 128;   // keys per block
-constexpr int NST = 2;    // K/V pipeline stages
+constexpr int NSK = 3;    // K pipeline stages (keys are needed first, so they run further ahead)
+constexpr int NSV = 2;    // V pipeline stages
 constexpr uint32_t TILE_BYTES = 128 * 128 * 2;  // one 128 x 128 bf16 operand
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzle atom column
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
-constexpr int kMaxBatch = 1024;
 
 enum : uint32_t {
   B_Q_FULL = 0,
   B_Q_EMPTY = 1,
-  B_KV_FULL = 2,                 // + stage
-  B_KV_EMPTY = B_KV_FULL + NST,  // + stage
-  B_S_FULL = B_KV_EMPTY + NST,   // + tile
+  B_K_FULL = 2,                  // + stage
+  B_K_EMPTY = B_K_FULL + NSK,    // + stage
+  B_V_FULL = B_K_EMPTY + NSK,    // + stage
+  B_V_EMPTY = B_V_FULL + NSV,    // + stage
+  B_S_FULL = B_V_EMPTY + NSV,    // + tile
   B_P_FULL = B_S_FULL + 2,       // + tile
   B_PV_DONE = B_P_FULL + 2,      // + tile
   B_O_FREE = B_PV_DONE + 2,      // + tile
@@ -79,18 +81,19 @@ struct Cfg {
   static constexpr int kThreads = 64 + 32 * kSoftWarps;
   static constexpr uint32_t SM_Q = 0;
   static constexpr uint32_t SM_K = SM_Q + MT * TILE_BYTES;
-  static constexpr uint32_t SM_V = SM_K + NST * TILE_BYTES;
-  static constexpr uint32_t SM_BAR = SM_V + NST * TILE_BYTES;
-  static constexpr uint32_t SM_PLAN = SM_BAR + 256;
-  static constexpr uint32_t SM_TOTAL = SM_PLAN + 16u * (kMaxBatch + 1);
+  static constexpr uint32_t SM_V = SM_K + NSK * TILE_BYTES;
+  static constexpr uint32_t SM_BAR = SM_V + NSV * TILE_BYTES;
+  static constexpr uint32_t SM_TOTAL = SM_BAR + 256;
   static constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 };
+static_assert(8 * B_COUNT + 8 + 7 * 4 <= 256, "barrier area overflow");
 
 struct TcMaps {
   CUtensorMap q, kc, vc, kn, vn;
 };
 
 struct TcWork {
+  int32_t* plan;   // [grid][4][batch + 1] per-CTA planning tables
   int32_t* cnt;    // [units][MT][4] arrival counters (zero between calls)
   float* part_ml;  // [2 * grid][MT][128][2]  running max (log2 domain), sum
   float* part_o;   // [2 * grid][MT][128][128] unnormalised O
@@ -117,6 +120,31 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// packed fp32x2 helpers (Blackwell f32x2 FMA / add) and a 3-input max
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int w) {
@@ -148,10 +176,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::SM_BAR + 8 * B_COUNT);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C_::SM_BAR + 8 * B_COUNT + 4);
   PlanHdr* plan = reinterpret_cast<PlanHdr*>(smem + C_::SM_BAR + 8 * B_COUNT + 8);
-  int* s_prefU = reinterpret_cast<int*>(smem + C_::SM_PLAN);
-  int* s_prefB = s_prefU + (kMaxBatch + 1);
-  int* s_bgblk = s_prefB + (kMaxBatch + 1);
-  int* s_ntile = s_bgblk + kMaxBatch;
+  // planning tables of this CTA (global workspace, visible to the CTA after __syncthreads)
+  int* s_prefU = work.plan + (size_t)blockIdx.x * 4 * (p.batch + 1);
+  int* s_prefB = s_prefU + (p.batch + 1);
+  int* s_bgblk = s_prefB + (p.batch + 1);
+  int* s_ntile = s_bgblk + (p.batch + 1);
   auto bar = [&](uint32_t i) -> uint32_t { return sbase + C_::SM_BAR + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,6 +227,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         }
       }
     }
+    __syncwarp();  // table entries written by every lane are read by lane 0 below
     if (lane == 0) {
       s_prefU[0] = 0;
       s_prefB[0] = 0;
@@ -285,11 +315,39 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     if (lane == 0 && begin < end) {
       tma_prefetch(&maps.q); tma_prefetch(&maps.kc); tma_prefetch(&maps.vc);
       tma_prefetch(&maps.kn); tma_prefetch(&maps.vn);
-      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kv_n = 0;
+      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kn = 0, vn = 0;
       bool run = true;
+      auto load_k = [&](const Unit& x, int j) -> bool {
+        const int st = kn % NSK;
+        if (kn >= NSK && !mbar_wait(bar(B_K_EMPTY + st), ((kn / NSK) - 1) & 1, abort)) return false;
+        mbar_expect_tx(bar(B_K_FULL + st), TILE_BYTES);
+        const bool cache = j < x.cache_blocks;
+        const CUtensorMap* mk = cache ? &maps.kc : &maps.kn;
+        const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
+        const uint32_t dk = sbase + C_::SM_K + st * TILE_BYTES;
+        tma_load_3d(dk, mk, 0, x.g, z, bar(B_K_FULL + st));
+        tma_load_3d(dk + HALF_BYTES, mk, 64, x.g, z, bar(B_K_FULL + st));
+        ++kn;
+        return true;
+      };
+      auto load_v = [&](const Unit& x, int j) -> bool {
+        const int st = vn % NSV;
+        if (vn >= NSV && !mbar_wait(bar(B_V_EMPTY + st), ((vn / NSV) - 1) & 1, abort)) return false;
+        mbar_expect_tx(bar(B_V_FULL + st), TILE_BYTES);
+        const bool cache = j < x.cache_blocks;
+        const CUtensorMap* mv = cache ? &maps.vc : &maps.vn;
+        const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
+        const uint32_t dv = sbase + C_::SM_V + st * TILE_BYTES;
+        tma_load_3d(dv, mv, 0, x.g, z, bar(B_V_FULL + st));
+        tma_load_3d(dv + HALF_BYTES, mv, 64, x.g, z, bar(B_V_FULL + st));
+        ++vn;
+        return true;
+      };
       while (run && remaining > 0) {
         const Unit x = decode(u);
         const int len = min(x.nblocks - k, remaining);
+        // the first key block does not depend on Q: start it before waiting for the Q buffer
+        if (!load_k(x, k)) break;
         if (seg > 0 && !mbar_wait(bar(B_Q_EMPTY), (seg - 1) & 1, abort)) break;
         mbar_expect_tx(bar(B_Q_FULL), x.mc * TILE_BYTES);
         for (int mt = 0; mt < x.mc; ++mt) {
@@ -298,34 +356,29 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           tma_load_3d(sbase + C_::SM_Q + mt * TILE_BYTES + HALF_BYTES, &maps.q, 64, x.g * G, z, bar(B_Q_FULL));
         }
         ++seg;
-        for (int j = k; j < k + len; ++j) {
-          const int st = kv_n % NST;
-          if (kv_n >= NST && !mbar_wait(bar(B_KV_EMPTY + st), ((kv_n / NST) - 1) & 1, abort)) { run = false; break; }
-          mbar_expect_tx(bar(B_KV_FULL + st), 2 * TILE_BYTES);
-          const uint32_t dk = sbase + C_::SM_K + st * TILE_BYTES, dv = sbase + C_::SM_V + st * TILE_BYTES;
-          const bool cache = j < x.cache_blocks;
-          const CUtensorMap* mk = cache ? &maps.kc : &maps.kn;
-          const CUtensorMap* mv = cache ? &maps.vc : &maps.vn;
-          const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
-          tma_load_3d(dk, mk, 0, x.g, z, bar(B_KV_FULL + st));
-          tma_load_3d(dk + HALF_BYTES, mk, 64, x.g, z, bar(B_KV_FULL + st));
-          tma_load_3d(dv, mv, 0, x.g, z, bar(B_KV_FULL + st));
-          tma_load_3d(dv + HALF_BYTES, mv, 64, x.g, z, bar(B_KV_FULL + st));
-          ++kv_n;
+        // keys run one block ahead of values
+        for (int j = k + 1; j < k + len; ++j) {
+          if (!load_k(x, j) || !load_v(x, j - 1)) { run = false; break; }
         }
+        if (!run || !load_v(x, k + len - 1)) break;
         remaining -= len;
         ++u;
         k = 0;
       }
-      // drain (bounded, regardless of abort): the last Q load and the last NST K/V loads
+      // drain (bounded, regardless of abort): the last Q load and the last K / V loads
       if (seg > 0) {
         const long long t0 = clock64();
         while (!mbar_try_wait(bar(B_Q_FULL), (seg - 1) & 1) && clock64() - t0 < kWaitBudget) {
         }
       }
-      for (int n = (kv_n > NST ? kv_n - NST : 0); n < kv_n; ++n) {
+      for (int n = (kn > NSK ? kn - NSK : 0); n < kn; ++n) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_KV_FULL + n % NST), (n / NST) & 1) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_K_FULL + n % NSK), (n / NSK) & 1) && clock64() - t0 < kWaitBudget) {
+        }
+      }
+      for (int n = (vn > NSV ? vn - NSV : 0); n < vn; ++n) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar(B_V_FULL + n % NSV), (n / NSV) & 1) && clock64() - t0 < kWaitBudget) {
         }
       }
     }
@@ -334,57 +387,58 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     if (lane == 0 && begin < end) {
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_pv = idesc_bf16(128, 128, true);
-      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kv_n = 0;
+      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kn = 0, vn = 0;
       int nblk0 = 0, nblk1 = 0, nseg0 = 0, nseg1 = 0;
       bool run = true;
+      static_assert(NSK == 3 && NSV == 2, "descriptor selection below assumes 3 K and 2 V stages");
+      const uint64_t dq0 = smem_desc_sw128(sbase + C_::SM_Q, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sbase + C_::SM_Q + (MT > 1 ? TILE_BYTES : 0), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sbase + C_::SM_K, 16, 1024);
+      const uint64_t dk1 = smem_desc_sw128(sbase + C_::SM_K + TILE_BYTES, 16, 1024);
+      const uint64_t dk2 = smem_desc_sw128(sbase + C_::SM_K + 2 * TILE_BYTES, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sbase + C_::SM_V, HALF_BYTES, 1024);
+      const uint64_t dv1 = smem_desc_sw128(sbase + C_::SM_V + TILE_BYTES, HALF_BYTES, 1024);
       auto issue_s = [&](int mt, int st) {
-        const uint32_t qa = sbase + C_::SM_Q + mt * TILE_BYTES, ka = sbase + C_::SM_K + st * TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-          mma_f16(tmem + mt * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024), id_s,
-                  kk > 0 ? 1u : 0u);
-        }
+        gemm_ss_k128(tmem + mt * 128, mt ? dq1 : dq0, st == 0 ? dk0 : (st == 1 ? dk1 : dk2), id_s, 0u);
         mma_commit(bar(B_S_FULL + mt));
       };
       auto issue_pv = [&](int mt, int st, bool acc) {
-        const uint32_t va = sbase + C_::SM_V + st * TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_f16_tmem_a(tmem + TM_O + mt * 128, tmem + mt * 128 + kk * 8,
-                         smem_desc_sw128(va + kk * 2048, HALF_BYTES, 1024), id_pv, (acc || kk > 0) ? 1u : 0u);
-        }
+        gemm_ts_k128(tmem + TM_O + mt * 128, tmem + mt * 128, st ? dv1 : dv0, id_pv, acc ? 1u : 0u);
         mma_commit(bar(B_PV_DONE + mt));
       };
+      auto wait_k = [&]() -> bool { return mbar_wait_poll(bar(B_K_FULL + kn % NSK), (kn / NSK) & 1, abort); };
       while (run && remaining > 0) {
         const Unit x = decode(u);
         const int len = min(x.nblocks - k, remaining);
-        if (!mbar_wait(bar(B_Q_FULL), seg & 1, abort)) break;
-        if (!mbar_wait(bar(B_KV_FULL + kv_n % NST), (kv_n / NST) & 1, abort)) break;
+        if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+        if (!wait_k()) break;
         tc_fence_after();
-        for (int mt = 0; mt < x.mc; ++mt) issue_s(mt, kv_n % NST);
+        for (int mt = 0; mt < x.mc; ++mt) issue_s(mt, kn % NSK);
+        mma_commit(bar(B_K_EMPTY + kn % NSK));
+        ++kn;
         for (int i = 0; i < len && run; ++i) {
-          const int st = kv_n % NST;
+          if (!mbar_wait_poll(bar(B_V_FULL + vn % NSV), (vn / NSV) & 1, abort)) { run = false; break; }
           for (int mt = 0; mt < x.mc; ++mt) {
             int& nb = mt ? nblk1 : nblk0;
             const int ns = mt ? nseg1 : nseg0;
-            if (!mbar_wait(bar(B_P_FULL + mt), nb & 1, abort)) { run = false; break; }
-            if (i == 0 && ns > 0 && !mbar_wait(bar(B_O_FREE + mt), (ns - 1) & 1, abort)) { run = false; break; }
+            if (!mbar_wait_poll(bar(B_P_FULL + mt), nb & 1, abort)) { run = false; break; }
+            if (i == 0 && ns > 0 && !mbar_wait_poll(bar(B_O_FREE + mt), (ns - 1) & 1, abort)) { run = false; break; }
             tc_fence_after();
-            issue_pv(mt, st, i > 0);
+            issue_pv(mt, vn % NSV, i > 0);
             ++nb;
             if (i + 1 < len) {
-              if (mt == 0 && !mbar_wait(bar(B_KV_FULL + (kv_n + 1) % NST), ((kv_n + 1) / NST) & 1, abort)) {
-                run = false;
-                break;
-              }
+              if (mt == 0 && !wait_k()) { run = false; break; }
               tc_fence_after();
-              issue_s(mt, (kv_n + 1) % NST);
+              issue_s(mt, kn % NSK);
             }
           }
           if (!run) break;
-          mma_commit(bar(B_KV_EMPTY + st));
-          ++kv_n;
+          if (i + 1 < len) {
+            mma_commit(bar(B_K_EMPTY + kn % NSK));
+            ++kn;
+          }
+          mma_commit(bar(B_V_EMPTY + vn % NSV));
+          ++vn;
         }
         if (!run) break;
         mma_commit(bar(B_Q_EMPTY));
@@ -482,86 +536,129 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             if (lim_rows > 32 * q) v |= window32(tm0, tm1, tm2, tm3, toff + 32 * q) & prefix32(lim_rows - 32 * q);
             return v;
           };
-          // ---- pass 1: row max of the raw scores (the scale is positive)
-          float mx;
-          {
-            float a[8];
+          // ---- steady state (not the segment's first block, no mask): one pass with the
+          // running max, P kept in registers until no row's max has grown past the
+          // rescale threshold; otherwise fall through to the two-pass path (S intact).
+          bool done = false;
+          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+          if (all_vis && jj > 0 && __all_sync(0xffffffffu, m_used > -INFINITY)) {
+            uint32_t b0[32], b1[32], pw[64];
+            float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+            uint64_t lp0 = 0ull, lp1 = 0ull;  // packed (even, odd) partial sums of P
+            const uint64_t cc2 = pack2(cexp, cexp), nm2 = pack2(-m_used, -m_used);
+            tmem_ld32(tS, b0);
+            tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) a[e] = -INFINITY;
+            for (int q = 0; q < BN / 32; ++q) {
+              uint32_t* cur = (q & 1) ? b1 : b0;
+              uint32_t* nxt = (q & 1) ? b0 : b1;
+              if (q + 1 < BN / 32) tmem_ld32(tS + (q + 1) * 32, nxt);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
+                if ((e & 3) == 0) a0 = max3(a0, s0, s1);
+                else if ((e & 3) == 1) a1 = max3(a1, s0, s1);
+                else if ((e & 3) == 2) a2 = max3(a2, s0, s1);
+                else a3 = max3(a3, s0, s1);
+                float x0, x1;
+                unpack2(ffma2(pack2(s0, s1), cc2, nm2), x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                pw[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&pb);
+                if (e & 1) lp1 = fadd2(lp1, pack2(p0, p1)); else lp0 = fadd2(lp0, pack2(p0, p1));
+              }
+              if (q + 1 < BN / 32) tmem_wait_ld();
+            }
+            const float mx1 = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+            if (!__any_sync(0xffffffffu, mx1 * cexp > m_used + kRescaleThreshold)) {
+#pragma unroll
+              for (int q = 0; q < BN / 32; ++q) tmem_st16(tS + q * 16, pw + q * 16);
+              unpack2(lp0, l0, l1);
+              unpack2(lp1, l2, l3);
+              done = true;
+            }
+          }
+          if (!done) {
+            // ---- pass 1: row max of the raw scores (the scale is positive)
+            float mx;
+            {
+              float a[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a[e] = -INFINITY;
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-              uint32_t sr[64];
-              tmem_ld32(tS + h * 64, sr);
-              tmem_ld32(tS + h * 64 + 32, sr + 32);
-              tmem_wait_ld();
-              if (all_vis) {
+              for (int h = 0; h < 2; ++h) {
+                uint32_t sr[64];
+                tmem_ld32(tS + h * 64, sr);
+                tmem_ld32(tS + h * 64 + 32, sr + 32);
+                tmem_wait_ld();
+                if (all_vis) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) a[e & 7] = fmaxf(a[e & 7], __uint_as_float(sr[e]));
-              } else {
-                const uint32_t v0 = vis32(2 * h), v1 = vis32(2 * h + 1);
+                  for (int e = 0; e < 64; ++e) a[e & 7] = fmaxf(a[e & 7], __uint_as_float(sr[e]));
+                } else {
+                  const uint32_t v0 = vis32(2 * h), v1 = vis32(2 * h + 1);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
-                  const uint32_t vw = e < 32 ? v0 : v1;
-                  const float f = ((vw >> (e & 31)) & 1u) ? __uint_as_float(sr[e]) : -INFINITY;
-                  a[e & 7] = fmaxf(a[e & 7], f);
+                  for (int e = 0; e < 64; ++e) {
+                    const uint32_t vw = e < 32 ? v0 : v1;
+                    const float f = ((vw >> (e & 31)) & 1u) ? __uint_as_float(sr[e]) : -INFINITY;
+                    a[e & 7] = fmaxf(a[e & 7], f);
+                  }
                 }
               }
+              mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
             }
-            mx = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
-          }
-          const float mxs = mx * cexp;
-          const bool need = (mx > -INFINITY) && (m_used == -INFINITY || mxs > m_used + kRescaleThreshold);
-          if (jj > 0 && __any_sync(0xffffffffu, need)) {
-            // O holds PV of the earlier blocks: it must be complete before rescaling
-            if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
-            tc_fence_after();
-            const float f = need ? ex2(m_used - mxs) : 1.f;
-            uint32_t raw[32];
+            const float mxs = mx * cexp;
+            const bool need = (mx > -INFINITY) && (m_used == -INFINITY || mxs > m_used + kRescaleThreshold);
+            if (jj > 0 && __any_sync(0xffffffffu, need)) {
+              // O holds PV of the earlier blocks: it must be complete before rescaling
+              if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
+              tc_fence_after();
+              const float f = need ? ex2(m_used - mxs) : 1.f;
+              uint32_t raw[32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              tmem_ld32(tO + c * 32, raw);
-              tmem_wait_ld();
+              for (int c = 0; c < D / 32; ++c) {
+                tmem_ld32(tO + c * 32, raw);
+                tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
-              tmem_st32(tO + c * 32, raw);
+                for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+                tmem_st32(tO + c * 32, raw);
+              }
+              tmem_wait_st();
+              l_sum *= f;
             }
-            tmem_wait_st();
-            l_sum *= f;
-          }
-          if (need) m_used = mxs;
-          const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-          // ---- pass 2: P = exp2(s * c - m) as bf16 pairs into TMEM over S columns [0, 64).
-          // Chunk q reads S columns [32q, 32q + 32) and writes P columns [16q, 16q + 16),
-          // which lie in S columns already read.
-          float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+            if (need) m_used = mxs;
+            const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+            // ---- pass 2: P = exp2(s * c - m) as bf16 pairs into TMEM over S columns [0, 64).
+            // Chunk q reads S columns [32q, 32q + 32) and writes P columns [16q, 16q + 16),
+            // which lie in S columns already read.
 #pragma unroll 1
-          for (int q = 0; q < BN / 32; ++q) {
-            uint32_t sr[32];
-            tmem_ld32(tS + q * 32, sr);
-            tmem_wait_ld();
-            uint32_t pw[16];
-            if (all_vis) {
+            for (int q = 0; q < BN / 32; ++q) {
+              uint32_t sr[32];
+              tmem_ld32(tS + q * 32, sr);
+              tmem_wait_ld();
+              uint32_t pw[16];
+              if (all_vis) {
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref));
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
-                if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
-              }
-            } else {
-              const uint32_t vw = vis32(q);
+                for (int e = 0; e < 16; ++e) {
+                  const float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref));
+                  const float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref));
+                  const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                  pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
+                  if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
+                }
+              } else {
+                const uint32_t vw = vis32(q);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const float p0 = ((vw >> (2 * e)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref)) : 0.f;
-                const float p1 =
-                    ((vw >> (2 * e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref)) : 0.f;
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
-                if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
+                for (int e = 0; e < 16; ++e) {
+                  const float p0 = ((vw >> (2 * e)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e]), cexp, -mref)) : 0.f;
+                  const float p1 =
+                      ((vw >> (2 * e + 1)) & 1u) ? ex2(fmaf(__uint_as_float(sr[2 * e + 1]), cexp, -mref)) : 0.f;
+                  const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                  pw[e] = *reinterpret_cast<const uint32_t*>(&pb);
+                  if (e & 1) { l2 += p0; l3 += p1; } else { l0 += p0; l1 += p1; }
+                }
               }
+              tmem_st16(tS + q * 16, pw);
             }
-            tmem_st16(tS + q * 16, pw);
           }
           tmem_wait_st();
           l_sum += (l0 + l1) + (l2 + l3);
@@ -752,7 +849,7 @@ static int choose_mt(const AttnParams& p) {
 }
 
 struct WsLayout {
-  size_t cnt, ml, o, total;
+  size_t plan, cnt, ml, o, total;
   int grid, mt, units;
 };
 
@@ -765,6 +862,8 @@ static WsLayout ws_layout(const AttnParams& p) {
   L.units = (int)((long long)p.batch * p.Hkv * ((max_rows + UR - 1) / UR));
   L.grid = sm_count();
   size_t off = 0;
+  L.plan = off;
+  off = align_up(off + sizeof(int32_t) * (size_t)L.grid * 4 * (p.batch + 1), 256);
   L.cnt = off;
   off = align_up(off + sizeof(int32_t) * (size_t)L.units * L.mt * 4, 256);
   L.ml = off;
@@ -779,7 +878,7 @@ bool attn_tc_supported(const AttnParams& p) {
   if (p.in_dtype != SSV_BF16 || p.d != D) return false;
   const int G = p.Hq / p.Hkv;
   if (G < 1 || G > 128 || (128 % G) != 0) return false;
-  if (p.max_block > 64 || p.batch > kMaxBatch) return false;
+  if (p.max_block > 64) return false;
   // total key blocks must fit comfortably in int32
   const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
   const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
@@ -821,6 +920,7 @@ cudaError_t launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t st) {
   }
   char* w = static_cast<char*>(ws);
   TcWork work;
+  work.plan = reinterpret_cast<int32_t*>(w + L.plan);
   work.cnt = reinterpret_cast<int32_t*>(w + L.cnt);
   work.part_ml = reinterpret_cast<float*>(w + L.ml);
   work.part_o = reinterpret_cast<float*>(w + L.o);
