@@ -78,6 +78,18 @@ def accept_bytes(x) -> float:
     return tot
 
 
+def aggregate_ms(local_ms: float, dist_mod=None, device=None) -> float:
+    """Max over ranks of a per-rank time (identity on one rank)."""
+    if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
+        return float(local_ms)
+    if dist_mod.get_world_size() == 1:
+        return float(local_ms)
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
 def kernel_launches(x) -> int:
     n = 1 + 1  # rope, verify attention
     if x is not None:
@@ -350,11 +362,7 @@ def run_ours(args):
     assert ssv.get_status(status) == ssv.SSV_OK
     per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
     step_ms = per.sum(axis=1)
-    tot_ms = float(step_ms.sum())
-    if world > 1:
-        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        tot_ms = float(tt.item())
+    tot_ms = aggregate_ms(float(step_ms.sum()), dist if world > 1 else None, dev)
 
     rb = rope_bytes(a)
     ab, af = attn_work(a, out_b)
