@@ -17,7 +17,9 @@
 // the mask.
 //
 // Scheduling is persistent stream-K: one CTA per SM; the concatenated key
-// blocks of all units are cut into equal contiguous ranges, one per CTA.  A
+// blocks of all units are cut into equal contiguous ranges, one per CTA (when
+// there are no more units than SMs, each unit gets the same whole number of
+// CTAs, so the kv heads of a sequence are read in lockstep).  A
 // unit split across CTAs leaves fp32 partials (unnormalised O, running max,
 // sum) in the workspace; for each 32-row group the warp that arrives last
 // (per-group arrival counter, no waiting on other CTAs) merges the partials
@@ -234,7 +236,12 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       PlanHdr h;
       h.W = carryB;
       h.U = carryU;
-      h.Pe = min(P, max(carryB, 1));
+      // With at most one unit per SM, give every unit the same number of CTAs so that the
+      // CTAs serving the kv heads of a sequence stream the same tokens at the same time
+      // (the heads of a token are adjacent in memory: DRAM pages are shared).  Otherwise
+      // split the concatenated blocks evenly (stream-K).
+      h.Pe = (carryU > 0 && carryU <= P) ? carryU * (P / carryU) : P;
+      h.Pe = min(h.Pe, max(carryB, 1));
       h.begin = cta < h.Pe ? (int)(((long long)cta * carryB) / h.Pe) : 0;
       h.end = cta < h.Pe ? (int)(((long long)(cta + 1) * carryB) / h.Pe) : 0;
       h.u0 = 0;
