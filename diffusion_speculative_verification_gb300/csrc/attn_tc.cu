@@ -88,7 +88,7 @@ struct Cfg {
   static constexpr uint32_t SM_TOTAL = SM_BAR + 256;
   static constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 };
-static_assert(8 * B_COUNT + 8 + 7 * 4 <= 256, "barrier area overflow");
+static_assert(8 * B_COUNT + 8 + 8 * 4 <= 256, "barrier area overflow");
 
 struct TcMaps {
   CUtensorMap q, kc, vc, kn, vn;
@@ -102,7 +102,7 @@ struct TcWork {
 };
 
 struct PlanHdr {
-  int W, U, Pe, begin, end, u0, k0;  // Pe = CTAs that own blocks (min(grid, W)): every owner is non-empty
+  int W, U, Pe, g, begin, end, u0, k0;  // per head: W blocks, U units, Pe owning CTAs; this CTA's head g
 };
 
 struct Unit {
@@ -192,6 +192,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   const int cta = blockIdx.x;
 
   // ------------------------------------------------------------------ plan
+  // Work is partitioned per kv head: CTA c serves head g = c % Hkv as rank r = c / Hkv of
+  // the Ph CTAs of that head, over the head's units in (sequence, row tile) order.  Every
+  // head has identical work, so CTAs of different heads stay at the same token offsets and
+  // read the heads of a token (adjacent in memory) together.  Tables are per head.
   if (warp == 0) {
     int carryU = 0, carryB = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -205,8 +209,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         for (int t = 0; t < nt; ++t) bg += unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
         s_bgblk[b] = bg;
         s_ntile[b] = nt;
-        units = p.Hkv * nt;
-        blocks = p.Hkv * bg;
+        units = nt;
+        blocks = bg;
       }
       int iu = units, ib = blocks;
 #pragma unroll
@@ -234,16 +238,19 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       s_prefU[0] = 0;
       s_prefB[0] = 0;
       PlanHdr h;
-      h.W = carryB;
-      h.U = carryU;
-      // With at most one unit per SM, give every unit the same number of CTAs so that the
-      // CTAs serving the kv heads of a sequence stream the same tokens at the same time
-      // (the heads of a token are adjacent in memory: DRAM pages are shared).  Otherwise
-      // split the concatenated blocks evenly (stream-K).
-      h.Pe = (carryU > 0 && carryU <= P) ? carryU * (P / carryU) : P;
-      h.Pe = min(h.Pe, max(carryB, 1));
-      h.begin = cta < h.Pe ? (int)(((long long)cta * carryB) / h.Pe) : 0;
-      h.end = cta < h.Pe ? (int)(((long long)(cta + 1) * carryB) / h.Pe) : 0;
+      h.W = carryB;  // key blocks per head
+      h.U = carryU;  // units per head
+      // CTAs per head: with no more units than CTAs, the same whole number per unit (each
+      // CTA owns an equal piece of one unit); otherwise an even split of the head's blocks.
+      const int cap = max(P / p.Hkv, 1);
+      int ph = (carryU > 0 && carryU <= cap) ? carryU * (cap / carryU) : cap;
+      ph = min(ph, max(carryB, 1));
+      h.Pe = ph;
+      h.g = cta % p.Hkv;
+      const int r = cta / p.Hkv;
+      const bool mine = cta < ph * p.Hkv;
+      h.begin = mine ? (int)(((long long)r * carryB) / ph) : 0;
+      h.end = mine ? (int)(((long long)(r + 1) * carryB) / ph) : 0;
       h.u0 = 0;
       h.k0 = 0;
       if (h.begin < h.end) {
@@ -252,9 +259,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           const int mid = (lo + hi) >> 1;
           if (s_prefB[mid] <= h.begin) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
         }
-        const int rem = h.begin - s_prefB[b];
-        const int gg = rem / s_bgblk[b];
-        int r2 = rem - gg * s_bgblk[b];
+        int r2 = h.begin - s_prefB[b];
         const ssv_seq s = p.seqs[b];
         const int rows = s.new_len + 2 * s.block;
         int t = 0;
@@ -263,7 +268,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           if (r2 < nb) break;
           r2 -= nb;
         }
-        h.u0 = s_prefU[b] + gg * s_ntile[b] + t;
+        h.u0 = s_prefU[b] + t;
         h.k0 = r2;
       }
       *plan = h;
@@ -282,9 +287,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int begin = plan->begin, end = plan->end, W = plan->W, Pe = plan->Pe;
+  const int begin = plan->begin, end = plan->end, W = plan->W, Ph = plan->Pe, Uh = plan->U;
+  const int gh = plan->g;           // kv head served by this CTA
+  const int rank = cta / p.Hkv;     // rank among the CTAs of head gh
 
-  // decode unit u from the shared plan tables
+  // decode head-local unit u (sequence, row tile) from the plan tables
   auto decode = [&](int u) -> Unit {
     Unit x;
     int lo = 0, hi = p.batch - 1, b = 0;
@@ -292,10 +299,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       const int mid = (lo + hi) >> 1;
       if (s_prefU[mid] <= u) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
     }
-    const int local = u - s_prefU[b];
+    const int tile = u - s_prefU[b];
     x.b = b;
-    x.g = local / s_ntile[b];
-    const int tile = local - x.g * s_ntile[b];
+    x.g = gh;
     const ssv_seq s = p.seqs[b];
     x.C = s.cache_len; x.N = s.new_len; x.B = s.block;
     x.q_off = s.q_off; x.kv_off = s.kv_off; x.tau_off = s.tau_off;
@@ -308,13 +314,14 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     x.full_new = (x.row0 < x.N) ? (x.row0 + 1) : x.N;
     return x;
   };
-  auto seg_start = [&](int c) -> int { return (int)(((long long)c * W) / Pe); };
-  auto owner = [&](int xb) -> int {  // CTA whose range holds global block xb
-    int c = (int)(((long long)xb * Pe) / (W > 0 ? W : 1));
-    c = min(max(c, 0), Pe - 1);
-    while (c + 1 < Pe && seg_start(c + 1) <= xb) ++c;
-    while (c > 0 && seg_start(c) > xb) --c;
-    return c;
+  // head-local block ranges: rank r owns [seg_start(r), seg_start(r + 1))
+  auto seg_start = [&](int r) -> int { return (int)(((long long)r * W) / Ph); };
+  auto owner = [&](int xb) -> int {  // rank whose range holds head-local block xb
+    int r = (int)(((long long)xb * Ph) / (W > 0 ? W : 1));
+    r = min(max(r, 0), Ph - 1);
+    while (r + 1 < Ph && seg_start(r + 1) <= xb) ++r;
+    while (r > 0 && seg_start(r) > xb) --r;
+    return r;
   };
 
   if (warp == 0) {
@@ -713,7 +720,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             }
           } else {
             // ---- publish this segment's partial; the 32-row group arriving last merges
-            const int c_a = owner(ustart), c_b = owner(ustart + x.nblocks - 1);
+            const int c_a = owner(ustart), c_b = owner(ustart + x.nblocks - 1);  // ranks of head gh
             const int which = (seg == 0) ? 0 : 1;
             const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
             __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
@@ -732,23 +739,23 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             __threadfence();
             __syncwarp();
             int prev = 0;
-            int32_t* counter = work.cnt + ((size_t)u * MT + mt) * 4 + q4;
+            int32_t* counter = work.cnt + (((size_t)gh * Uh + u) * MT + mt) * 4 + q4;
             if (lane == 0) prev = atomicAdd(counter, 1);
             prev = __shfl_sync(0xffffffffu, prev, 0);
             if (prev == c_b - c_a) {
               __threadfence();
-              auto slot_of = [&](int cc) -> size_t {
-                const int wh = (cc == c_a && seg_start(cc) < ustart) ? 1 : 0;
-                return ((size_t)(cc * 2 + wh) * MT + mt) * 128 + m;
+              auto slot_of = [&](int rr) -> size_t {  // partial slot of rank rr of head gh
+                const int wh = (rr == c_a && seg_start(rr) < ustart) ? 1 : 0;
+                return ((size_t)((rr * p.Hkv + gh) * 2 + wh) * MT + mt) * 128 + m;
               };
               // combine in CTA order (not arrival order) so the result is deterministic
               float M = m_used;
               for (int cc = c_a; cc <= c_b; ++cc)
-                if (cc != cta) M = fmaxf(M, __ldcg(work.part_ml + slot_of(cc) * 2));
+                if (cc != rank) M = fmaxf(M, __ldcg(work.part_ml + slot_of(cc) * 2));
               float L = 0.f;
               for (int cc = c_a; cc <= c_b; ++cc) {
                 float mo = m_used, lo = l_sum;
-                if (cc != cta) {
+                if (cc != rank) {
                   const float2 ml = __ldcg(reinterpret_cast<const float2*>(work.part_ml + slot_of(cc) * 2));
                   mo = ml.x;
                   lo = ml.y;
@@ -762,7 +769,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = 0.f;
                 for (int cc = c_a; cc <= c_b; ++cc) {
-                  if (cc == cta) {
+                  if (cc == rank) {
                     uint32_t raw[32];
                     tmem_ld32(tO + q * 32, raw);
                     tmem_wait_ld();
@@ -885,7 +892,7 @@ bool attn_tc_supported(const AttnParams& p) {
   if (p.in_dtype != SSV_BF16 || p.d != D) return false;
   const int G = p.Hq / p.Hkv;
   if (G < 1 || G > 128 || (128 % G) != 0) return false;
-  if (p.max_block > 64) return false;
+  if (p.max_block > 64 || p.Hkv > sm_count()) return false;  // every kv head needs a CTA
   // total key blocks must fit comfortably in int32
   const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
   const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
