@@ -97,6 +97,32 @@ def kernel_launches(x) -> int:
     return n
 
 
+KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_reduce_kernel", "rope": "rope_copy_kernel"}
+KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"], "accept_reduce_kernel": ["accept.cu"],
+                  "accept_sample_kernel": ["accept.cu"], "rope_copy_kernel": ["rope.cu"]}
+
+
+def measured_traffic(op: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
+    or None when there is none or the kernel source changed since it was taken."""
+    import hashlib
+    kern = KERNEL_OF_OP.get(op)
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if kern is None or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"{kern}_{workload}")
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kern]:
+        with open(os.path.join(ROOT, "diffusion_speculative_verification_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec.get("source_sha256_16"):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -376,11 +402,13 @@ def run_ours(args):
     dom = max(ops, key=lambda k: ops[k][0])
     ach = ops[dom][1] / (ops[dom][0] * 1e-3) / 1e9
     roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(ach / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind}
+            "frac": round(ach / hbm_peak, 4), "traffic": measured_traffic(dom, args.config), "peak_kind": peak_kind,
+            "algorithmic_bytes": ops[dom][1]}
     if dom == "verify_attn" and args.config == "prefill":
         tfs = af / (op_ms[1] * 1e-3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": round(tfs / tf_peak, 4), "traffic": None, "peak_kind": peak_kind}
+                "frac": round(tfs / tf_peak, 4), "traffic": measured_traffic(dom, args.config), "peak_kind": peak_kind,
+                "algorithmic_flops": af}
 
     # ---- end to end: host inputs -> device, run, tokens back -------------------
     e2e = run_e2e(args, a, x, t, acc, outs if acc is not None else None, o, dev, stream, step, out_b)
