@@ -97,9 +97,11 @@ def kernel_launches(x) -> int:
     return n
 
 
-KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_reduce_kernel", "rope": "rope_copy_kernel"}
-KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"], "accept_reduce_kernel": ["accept.cu"],
-                  "accept_sample_kernel": ["accept.cu"], "rope_copy_kernel": ["rope.cu"]}
+KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel"}
+KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"],
+                  "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh"],
+                  "accept_reduce_kernel": ["accept.cu", "accept.cuh"],
+                  "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"]}
 
 
 def measured_traffic(op: str, workload: str):

@@ -1,29 +1,21 @@
-// ssv_accept: acceptance in temporal order with the longest accepted prefix.
+// ssv_accept: acceptance in temporal order with the longest accepted prefix
+// (the shared records, arithmetic and completion steps are in accept.cuh).
 //
-// SimSD summary, section 4 "Acceptance": standard rejection sampling in the
-// temporal order the draft induces; the longest accepted prefix is kept.
-// SPOT review, section "How it is used": state equality (exact at T = 0) and
-// the coupled-noise match argmax(l/T + G[position]) with a Gumbel table
-// shared by drafter and target (Proposition 2).
-//
-// Two kernels, each finishing with a "last CTA of the sequence" step (a
-// per-sequence arrival counter in the workspace, no spinning):
-//   accept_reduce   grid = verified rows x vocab chunks.  One streaming pass
-//                   over each needed logits row (plus noise or draft row):
-//                   per chunk the (max, first argmax) of the decision score,
-//                   or for rejection sampling the chunk max and the
-//                   compensated sum of exp of l/T and of draft/T.  The last
-//                   CTA of a sequence merges the chunks, walks the stages in
-//                   tau order, writes n_acc / n_out / tokens and, for
-//                   rejection sampling, which row to sample from.
+// Reduce kernels:
+//   accept_stream   (accept_stream.cu) the default: persistent, one CTA per
+//                   SM, rows streamed through a shared-memory ring by bulk
+//                   copies.  Needs 16-byte aligned rows and at most
+//                   kStrMaxRows slots.
+//   accept_reduce   (below) any shape: grid = slots x vocab chunks, one
+//                   streaming pass of register loads per (row, chunk).
+// Both write one AccPartial per (verified row, chunk) and finish through the
+// row-merge / sequence-walk steps.
 //   accept_sample   (rejection sampling only) grid = vocab chunks x batch.
 //                   Chunk masses of (p - q)_+ and of p for the emission
-//                   row; the last CTA finds the chunk holding u' * Z and
-//                   scans it in vocabulary order (fp64 prefix sums).
-#include "ssv_internal.cuh"
-
-#include <limits.h>
-#include <math.h>
+//                   row; the last CTA finds the chunk holding u' * Z with a
+//                   warp scan and scans that chunk in vocabulary order
+//                   (fp64 prefix sums).
+#include "accept.cuh"
 
 namespace ssv {
 
@@ -31,82 +23,7 @@ constexpr int kAccThreads = 256;
 constexpr int kAccVec = 4;                                 // elements per vector access
 constexpr int kAccIters = 8;                               // vector accesses per thread per stream
 constexpr int kAccPerThread = kAccVec * kAccIters;         // 32
-constexpr int kAccChunk = kAccThreads * kAccPerThread;     // 8192 vocab entries per CTA
-
-struct AccPartial {
-  float m_a, m_b;          // chunk max of the raw logits and of the draft logits  (reject)
-  float sa_hi, sa_lo;      // compensated sum over the chunk of 2^((l - m_a) c2)   (reject)
-  float sb_hi, sb_lo;      // same for the draft row                              (reject)
-  float val;               // best decision score                                  (argmax / gumbel)
-  int idx;                 // its first index
-};
-
-struct SlotNorm {  // p_v = 2^((l_v - m_a) c2) / s_a, q likewise
-  float m_a, m_b;
-  double s_a, s_b;
-};
-
-__device__ __forceinline__ float ex2f(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-struct AcceptParams {
-  int mode;
-  float T;
-  float c2;                // log2(e) / T: rejection-sampling weights are 2^((l - max) * c2)
-  int V;
-  int vec;                 // rows allow 4-element vector accesses
-  int batch;
-  int total_slots;
-  int nchunks;
-  const void* logits;
-  const void* draft_logits;
-  const int32_t* draft_tokens;
-  const int32_t* tau;
-  const int32_t* block;
-  const int32_t* gamma;
-  const int32_t* slot_off;
-  const float* noise;
-  int n_noise_rows;
-  const int32_t* noise_row;
-  const float* u_accept;
-  const float* u_sample;
-  int32_t* n_acc;
-  int32_t* n_out;
-  int32_t* tokens;
-  int32_t* dev_status;
-  // workspace carve-up
-  int32_t* cnt_reduce;  // [batch]
-  int32_t* cnt_sample;  // [batch]
-  int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
-  AccPartial* part;     // [total_slots][nchunks]
-  SlotNorm* norm;       // [total_slots]
-  float* smass;         // [batch][nchunks][4] : residual mass (hi, lo), p mass (hi, lo)
-};
-
-struct AccWorkspaceLayout {
-  size_t cnt_reduce, cnt_sample, emit, part, norm, smass, total;
-};
-
-static AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks) {
-  AccWorkspaceLayout L;
-  size_t o = 0;
-  L.cnt_reduce = o; o = align_up(o + sizeof(int32_t) * (size_t)batch, 256);
-  L.cnt_sample = o; o = align_up(o + sizeof(int32_t) * (size_t)batch, 256);
-  L.emit = o;       o = align_up(o + sizeof(int32_t) * 2 * (size_t)batch, 256);
-  L.part = o;       o = align_up(o + sizeof(AccPartial) * (size_t)total_slots * nchunks, 256);
-  L.norm = o;       o = align_up(o + sizeof(SlotNorm) * (size_t)total_slots, 256);
-  L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nchunks, 256);
-  L.total = o;
-  return L;
-}
-
-template <typename T>
-__device__ __forceinline__ float ld_logit(const void* base, size_t i) {
-  return Elem<T>::to_f32(static_cast<const T*>(base)[i]);
-}
+static_assert(kAccThreads * kAccPerThread == kAccChunk, "one chunk per CTA");
 
 // 4 consecutive elements starting at i (i % 4 == 0, row base suitably aligned), streaming load
 template <typename T>
@@ -144,26 +61,7 @@ __device__ __forceinline__ int chunk_index(int c0, int j) {  // vocab index of a
   return c0 + ((j / kAccVec) * kAccThreads + (int)threadIdx.x) * kAccVec + (j % kAccVec);
 }
 
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-  const float y = x - c;
-  const float t = s + y;
-  c = (t - s) - y;
-  s = t;
-}
-
-// (h1, l1) += (h2, l2) with an error-free transformation of the leading terms
-__device__ __forceinline__ void two_sum_acc(float& h1, float& l1, float h2, float l2) {
-  const float s = h1 + h2;
-  const float bb = s - h1;
-  const float err = (h1 - (s - bb)) + (h2 - bb);
-  h1 = s;
-  l1 = l1 + l2 + err;
-}
-
 // ---- block reductions (256 threads) ---------------------------------------
-__device__ __forceinline__ void argmax_combine(float& v, int& i, float ov, int oi) {
-  if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
-}
 
 // result valid in thread 0
 __device__ void block_argmax(float& v, int& i) {
@@ -236,100 +134,11 @@ __device__ double block_exclusive_scan(double v) {
   return before + incl - v;
 }
 
-// ---- per-sequence validity, checked by warp 0 (all 32 lanes) -----------------
-__device__ bool warp_seq_valid(const AcceptParams& p, int b) {
-  const int B = p.block[b], g = p.gamma[b];
-  bool ok = B >= 1 && B <= 64 && g >= 0 && g <= B && p.slot_off[b] + B <= p.total_slots;
-  if (ok) ok = warp_tau_is_permutation(p.tau + p.slot_off[b], B);
-  return ok;
-}
-
-// ---- finalize: merge chunks, walk stages, write outputs --------------------
-template <int MODE, typename T>
-__device__ void accept_finalize(const AcceptParams& p, int b) {
-  __shared__ int s_slot[64];
-  __shared__ int s_dec[64];
-  __shared__ int s_ok[64];
-  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
-  const int need = min(g + 1, B);
-  const int tid = threadIdx.x;
-  if (tid < B) s_slot[p.tau[off + tid] - 1] = tid;
-  __syncthreads();
-  if (tid < need) {
-    const int k = off + s_slot[tid];
-    const AccPartial* pp = p.part + (size_t)k * p.nchunks;
-    if (MODE != SSV_ACCEPT_REJECT) {
-      float v = -INFINITY;
-      int i = INT_MAX;
-      for (int c = 0; c < p.nchunks; ++c) argmax_combine(v, i, __ldcg(&pp[c].val), __ldcg(&pp[c].idx));
-      s_dec[tid] = i;
-      s_ok[tid] = (tid < g) && (p.draft_tokens[k] == i);
-    } else {
-      const bool with_draft = tid < g;  // the draft row is read only for tested stages
-      float ma = -INFINITY, mb = -INFINITY;
-      for (int c = 0; c < p.nchunks; ++c) {
-        ma = fmaxf(ma, __ldcg(&pp[c].m_a));
-        if (with_draft) mb = fmaxf(mb, __ldcg(&pp[c].m_b));
-      }
-      const double c2 = (double)p.c2;
-      double sa = 0.0, sb = 0.0;
-      for (int c = 0; c < p.nchunks; ++c) {
-        sa += ((double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo)) *
-              exp2(((double)__ldcg(&pp[c].m_a) - (double)ma) * c2);
-        if (with_draft)
-          sb += ((double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo)) *
-                exp2(((double)__ldcg(&pp[c].m_b) - (double)mb) * c2);
-      }
-      SlotNorm nm;
-      nm.m_a = ma; nm.m_b = mb; nm.s_a = sa; nm.s_b = sb;
-      p.norm[k] = nm;
-      s_dec[tid] = -1;
-      int ok = 0;
-      if (with_draft) {
-        const int d = p.draft_tokens[k];
-        if (d >= 0 && d < p.V) {
-          const double ld = ld_logit<T>(p.logits, (size_t)k * p.V + d);
-          const double qd = ld_logit<T>(p.draft_logits, (size_t)k * p.V + d);
-          // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
-          const double ratio = exp2(((ld - (double)ma) - (qd - (double)mb)) * c2) * (sb / sa);
-          ok = (double)p.u_accept[k] < ratio;
-        } else {
-          report(p.dev_status, SSV_ERR_INVALID);
-        }
-      }
-      s_ok[tid] = ok;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int n = 0;
-    while (n < g && s_ok[n]) ++n;
-    for (int i = 0; i < n; ++i) p.tokens[off + i] = p.draft_tokens[off + s_slot[i]];
-    for (int i = n; i < B; ++i) p.tokens[off + i] = -1;
-    int nout = n;
-    int eslot = -1, ekind = 0;
-    if (n + 1 <= B) {
-      nout = n + 1;
-      if (MODE != SSV_ACCEPT_REJECT) {
-        p.tokens[off + n] = s_dec[n];
-      } else {
-        eslot = off + s_slot[n];
-        ekind = (n + 1 <= g) ? 1 : 0;
-      }
-    }
-    p.n_acc[b] = n;
-    p.n_out[b] = nout;
-    if (MODE == SSV_ACCEPT_REJECT) {
-      p.emit[2 * b] = eslot;
-      p.emit[2 * b + 1] = ekind;
-    }
-  }
-}
-
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_reduce_kernel(const AcceptParams p) {
-  __shared__ int s_ok, s_last;
+  __shared__ int s_ok;
+  __shared__ int s_slot[64];
   const int slot = blockIdx.x / p.nchunks;
   const int chunk = blockIdx.x % p.nchunks;
   const int b = find_seq_by_slot(p.slot_off, p.batch, slot);
@@ -408,18 +217,8 @@ accept_reduce_kernel(const AcceptParams p) {
     out.sa_hi = sa; out.sa_lo = la; out.sb_hi = sb; out.sb_lo = lb;
     out.val = 0.f; out.idx = 0;
   }
-  if (tid == 0) {
-    p.part[(size_t)slot * p.nchunks + chunk] = out;
-    __threadfence();
-    const int prev = atomicAdd(&p.cnt_reduce[b], 1);
-    s_last = (prev == need * p.nchunks - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  accept_finalize<MODE, T>(p, b);
-  __syncthreads();
-  if (tid == 0) p.cnt_reduce[b] = 0;
+  if (tid == 0) p.part[(size_t)slot * p.nchunks + chunk] = out;
+  if (tid < 32) warp_rows_done<MODE, T>(p, b, slot, 1, s_slot);
 }
 
 // ---- rejection sampling: emitted token ------------------------------------
@@ -464,13 +263,13 @@ accept_sample_kernel(const AcceptParams p) {
   float xa[kAccPerThread], xb[kAccPerThread];
   ld_chunk<T>(p.logits, rbase, c0, p.V, vec, -INFINITY, xa);
   if (residual) ld_chunk<T>(p.draft_logits, rbase, c0, p.V, vec, -INFINITY, xb);
-  float wr[kAccPerThread], wp[kAccPerThread];
   float sr = 0.f, cr = 0.f, sp = 0.f, cp = 0.f;
 #pragma unroll
   for (int j = 0; j < kAccPerThread; ++j) {
-    sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr[j], wp[j]);
-    kahan_add(sr, cr, wr[j]);
-    kahan_add(sp, cp, wp[j]);
+    float wr, wp;
+    sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr, wp);
+    kahan_add(sr, cr, wr);
+    kahan_add(sp, cp, wp);
   }
   float lr = -cr, lp = -cp;
   block_sum2x2(sr, lr, sp, lp);
@@ -485,31 +284,57 @@ accept_sample_kernel(const AcceptParams p) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of sequence b: locate u' * Z --------------------------------
+  // ---- last CTA of sequence b: locate u' * Z (warp 0, lanes over chunks) ----
   __shared__ int s_chunk;
   __shared__ double s_before, s_thresh;
   __shared__ int s_use_res;
-  if (tid == 0) {
+  if (tid < 32) {
+    const int lane = tid;
     const float* sm = p.smass + (size_t)b * p.nchunks * 4;
     double zr = 0.0, zp = 0.0;
-    for (int c = 0; c < p.nchunks; ++c) {
+    for (int c = lane; c < p.nchunks; c += 32) {
       zr += (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1]);
       zp += (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
     }
-    const int use_res = residual && zr > 0.0;
-    const double Z = use_res ? zr : zp;
-    const double t = (double)p.u_sample[b] * Z;
-    double cum = 0.0, before = 0.0, before_last = 0.0;
-    int cs = -1, last_nz = 0;
-    for (int c = 0; c < p.nchunks; ++c) {
-      const double m = use_res ? (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1])
-                               : (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
-      if (m > 0.0) { last_nz = c; before_last = cum; }
-      if (cs < 0 && cum + m > t) { cs = c; before = cum; }
-      cum += m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zr += __shfl_xor_sync(0xffffffffu, zr, o);
+      zp += __shfl_xor_sync(0xffffffffu, zp, o);
     }
-    if (cs < 0) { cs = last_nz; before = before_last; }
-    s_chunk = cs; s_before = before; s_thresh = t; s_use_res = use_res;
+    const bool use_res = residual && zr > 0.0;
+    const double t = (double)p.u_sample[b] * (use_res ? zr : zp);
+    // first chunk whose running mass passes t, in vocabulary order
+    double base = 0.0, before = 0.0, before_last = 0.0;
+    int cs = -1, last_nz = 0;
+    for (int r0 = 0; r0 < p.nchunks; r0 += 32) {
+      const int c = r0 + lane;
+      double m = 0.0;
+      if (c < p.nchunks)
+        m = use_res ? (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1])
+                    : (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
+      double incl = m;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const double excl = incl - m;
+      const unsigned cross = __ballot_sync(0xffffffffu, c < p.nchunks && base + incl > t);
+      const unsigned nz = __ballot_sync(0xffffffffu, c < p.nchunks && m > 0.0);
+      if (cs < 0 && cross) {
+        const int f = __ffs(cross) - 1;
+        cs = r0 + f;
+        before = base + __shfl_sync(0xffffffffu, excl, f);
+      }
+      if (nz) {
+        const int l = 31 - __clz(nz);
+        last_nz = r0 + l;
+        before_last = base + __shfl_sync(0xffffffffu, excl, l);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (cs < 0) { cs = last_nz; before = before_last; }  // rounding left t at the very end
+    if (lane == 0) { s_chunk = cs; s_before = before; s_thresh = t; s_use_res = use_res; }
   }
   __syncthreads();
   const int cs = s_chunk;
@@ -519,18 +344,16 @@ accept_sample_kernel(const AcceptParams p) {
   // free of bank conflicts).
   __shared__ float s_w[kAccChunk + kAccChunk / 32];
   {
+    // the crossing chunk is reloaded (it was just streamed, so from L2)
     const int cc0 = cs * kAccChunk;
-    if (cs != chunk) {
-      ld_chunk<T>(p.logits, rbase, cc0, p.V, vec, -INFINITY, xa);
-      if (residual) ld_chunk<T>(p.draft_logits, rbase, cc0, p.V, vec, -INFINITY, xb);
-#pragma unroll
-      for (int j = 0; j < kAccPerThread; ++j)
-        sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr[j], wp[j]);
-    }
+    ld_chunk<T>(p.logits, rbase, cc0, p.V, vec, -INFINITY, xa);
+    if (residual) ld_chunk<T>(p.draft_logits, rbase, cc0, p.V, vec, -INFINITY, xb);
 #pragma unroll
     for (int j = 0; j < kAccPerThread; ++j) {
+      float wr, wp;
+      sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr, wp);
       const int li = chunk_index(0, j);  // index within the chunk
-      s_w[li + li / 32] = (cc0 + li < p.V) ? (use_res ? wr[j] : wp[j]) : 0.f;
+      s_w[li + li / 32] = (cc0 + li < p.V) ? (use_res ? wr : wp) : 0.f;
     }
   }
   __syncthreads();
@@ -570,18 +393,38 @@ accept_sample_kernel(const AcceptParams p) {
 }
 
 template <int MODE, typename T>
-static cudaError_t launch_accept_t(const AcceptParams& p, cudaStream_t st) {
+static cudaError_t launch_reduce_t(const AcceptParams& p, cudaStream_t st) {
   const long long g1 = (long long)p.total_slots * p.nchunks;
   if (g1 > 0x7fffffffLL) return cudaErrorInvalidValue;
   accept_reduce_kernel<MODE, T><<<(unsigned)g1, kAccThreads, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (MODE == SSV_ACCEPT_REJECT) {
-    const long long g2 = (long long)p.batch * p.nchunks;
-    accept_sample_kernel<T><<<(unsigned)g2, kAccThreads, 0, st>>>(p);
-    e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+// Reduce (streaming kernel where the rows allow it) then, for rejection
+// sampling, the emitted-token pass.
+static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaStream_t st) {
+  cudaError_t e;
+  if (accept_stream_supported(p, mode, bf)) {
+    e = launch_accept_stream(p, mode, bf, st);
+  } else {
+    switch (mode) {
+      case SSV_ACCEPT_ARGMAX:
+        e = bf ? launch_reduce_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_ARGMAX, float>(p, st);
+        break;
+      case SSV_ACCEPT_GUMBEL:
+        e = bf ? launch_reduce_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_GUMBEL, float>(p, st);
+        break;
+      default:
+        e = bf ? launch_reduce_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_REJECT, float>(p, st);
+        break;
+    }
   }
-  return e;
+  if (e != cudaSuccess || mode != SSV_ACCEPT_REJECT) return e;
+  const long long g2 = (long long)p.batch * p.nchunks;
+  if (g2 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (bf) accept_sample_kernel<__nv_bfloat16><<<(unsigned)g2, kAccThreads, 0, st>>>(p);
+  else accept_sample_kernel<float><<<(unsigned)g2, kAccThreads, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace ssv
@@ -611,24 +454,11 @@ static ssv_status accept_check(const ssv_accept_args* a, int* nchunks) {
   return SSV_OK;
 }
 
-extern "C" ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes) {
-  if (!bytes) return SSV_ERR_INVALID;
-  int nchunks = 0;
-  const ssv_status st = accept_check(a, &nchunks);
-  if (st != SSV_OK) return st;
-  *bytes = accept_layout(a->batch, a->total_slots, nchunks).total;
-  return SSV_OK;
-}
-
-extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_bytes, void* stream) {
-  int nchunks = 0;
-  const ssv_status st = accept_check(a, &nchunks);
-  if (st != SSV_OK) return st;
-  if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
-  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
-  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
-  char* w = static_cast<char*>(ws);
-  AcceptParams p;
+// Parameter block over a workspace laid out by accept_layout.  Returns the
+// effective mode: coupled noise at T = 0 is the plain argmax.
+static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayout& L, int nchunks,
+                       AcceptParams* out) {
+  AcceptParams& p = *out;
   p.mode = a->mode;
   p.T = a->T;
   p.c2 = a->T > 0.f ? (float)(1.4426950408889634 / (double)a->T) : 0.f;
@@ -654,28 +484,39 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
   p.n_out = a->n_out;
   p.tokens = a->tokens;
   p.dev_status = a->dev_status;
-  p.cnt_reduce = reinterpret_cast<int32_t*>(w + L.cnt_reduce);
+  p.cnt_seq = reinterpret_cast<int32_t*>(w + L.cnt_seq);
   p.cnt_sample = reinterpret_cast<int32_t*>(w + L.cnt_sample);
+  p.cnt_row = reinterpret_cast<int32_t*>(w + L.cnt_row);
   p.emit = reinterpret_cast<int32_t*>(w + L.emit);
   p.part = reinterpret_cast<AccPartial*>(w + L.part);
   p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
+  p.rowres = reinterpret_cast<RowResult*>(w + L.rowres);
   p.smass = reinterpret_cast<float*>(w + L.smass);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool bf = a->logits_dtype == SSV_BF16;
   int mode = a->mode;
-  if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;   // T = 0 ignores the noise
-  cudaError_t e;
-  switch (mode) {
-    case SSV_ACCEPT_ARGMAX:
-      e = bf ? launch_accept_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_ARGMAX, float>(p, s);
-      break;
-    case SSV_ACCEPT_GUMBEL:
-      e = bf ? launch_accept_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_GUMBEL, float>(p, s);
-      break;
-    default:
-      e = bf ? launch_accept_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_REJECT, float>(p, s);
-      break;
-  }
+  if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;  // T = 0 ignores the noise
+  p.mode = mode;
+  return mode;
+}
+
+extern "C" ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes) {
+  if (!bytes) return SSV_ERR_INVALID;
+  int nchunks = 0;
+  const ssv_status st = accept_check(a, &nchunks);
+  if (st != SSV_OK) return st;
+  *bytes = accept_layout(a->batch, a->total_slots, nchunks).total;
+  return SSV_OK;
+}
+
+extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_bytes, void* stream) {
+  int nchunks = 0;
+  const ssv_status st = accept_check(a, &nchunks);
+  if (st != SSV_OK) return st;
+  if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
+  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
+  AcceptParams p;
+  const int mode = fill_params(a, static_cast<char*>(ws), L, nchunks, &p);
+  const cudaError_t e = launch_accept(p, mode, a->logits_dtype == SSV_BF16, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }
 
@@ -729,55 +570,11 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   st = noalloc_scratch_address(&scratch);
   if (st != SSV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The counters [cnt_reduce, cnt_sample] must start at zero.
+  // The arrival counters (cnt_seq, cnt_sample, cnt_row: the front of the
+  // layout, up to emit) must start at zero.
   if (cudaMemsetAsync(scratch, 0, L.emit, s) != cudaSuccess) return SSV_ERR_CUDA;
-  char* w = static_cast<char*>(scratch);
   AcceptParams p;
-  p.mode = a->mode;
-  p.T = a->T;
-  p.c2 = a->T > 0.f ? (float)(1.4426950408889634 / (double)a->T) : 0.f;
-  p.V = a->V;
-  p.vec = ((a->V % 4) == 0 && ((uintptr_t)a->logits & 15u) == 0 && ((uintptr_t)a->draft_logits & 15u) == 0 &&
-           ((uintptr_t)a->noise & 15u) == 0) ? 1 : 0;
-  p.batch = a->batch;
-  p.total_slots = a->total_slots;
-  p.nchunks = nchunks;
-  p.logits = a->logits;
-  p.draft_logits = a->draft_logits;
-  p.draft_tokens = a->draft_tokens;
-  p.tau = a->tau;
-  p.block = a->block;
-  p.gamma = a->gamma;
-  p.slot_off = a->slot_off;
-  p.noise = a->noise;
-  p.n_noise_rows = a->n_noise_rows;
-  p.noise_row = a->noise_row;
-  p.u_accept = a->u_accept;
-  p.u_sample = a->u_sample;
-  p.n_acc = a->n_acc;
-  p.n_out = a->n_out;
-  p.tokens = a->tokens;
-  p.dev_status = a->dev_status;
-  p.cnt_reduce = reinterpret_cast<int32_t*>(w + L.cnt_reduce);
-  p.cnt_sample = reinterpret_cast<int32_t*>(w + L.cnt_sample);
-  p.emit = reinterpret_cast<int32_t*>(w + L.emit);
-  p.part = reinterpret_cast<AccPartial*>(w + L.part);
-  p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
-  p.smass = reinterpret_cast<float*>(w + L.smass);
-  const bool bf = a->logits_dtype == SSV_BF16;
-  int mode = a->mode;
-  if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;
-  cudaError_t e;
-  switch (mode) {
-    case SSV_ACCEPT_ARGMAX:
-      e = bf ? launch_accept_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_ARGMAX, float>(p, s);
-      break;
-    case SSV_ACCEPT_GUMBEL:
-      e = bf ? launch_accept_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_GUMBEL, float>(p, s);
-      break;
-    default:
-      e = bf ? launch_accept_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, s) : launch_accept_t<SSV_ACCEPT_REJECT, float>(p, s);
-      break;
-  }
+  const int mode = fill_params(a, static_cast<char*>(scratch), L, nchunks, &p);
+  const cudaError_t e = launch_accept(p, mode, a->logits_dtype == SSV_BF16, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }

@@ -1,0 +1,305 @@
+// Shared pieces of the acceptance kernels (ssv_accept).
+//
+// SimSD summary, section 4 "Acceptance": standard rejection sampling in the
+// temporal order the draft induces; the longest accepted prefix is kept.
+// SPOT review, section "How it is used": state equality (exact at T = 0) and
+// the coupled-noise match argmax(l/T + G[position]) (Proposition 2).
+//
+// Every verified row (a slot whose stage is <= min(gamma + 1, B)) is cut
+// into vocabulary chunks of kAccChunk entries; a reduce kernel writes one
+// AccPartial per (row, chunk).  Completion is two-level and lock-free (an
+// arrival counter per row and per sequence, no spinning):
+//   row merge  the CTA that lands the last chunk of a row merges its chunk
+//              records with one warp (lanes over chunks): the decision token
+//              (argmax of the score) or, for rejection sampling, the row
+//              normalisers and the accept test u < p(d) / q(d);
+//   seq walk   the CTA that merges the last row of a sequence walks the
+//              stages in tau order with one warp and writes n_acc, n_out,
+//              tokens and, for rejection sampling, which row the emitted
+//              token is drawn from.
+#pragma once
+
+#include "ssv_internal.cuh"
+
+#include <limits.h>
+#include <math.h>
+
+namespace ssv {
+
+constexpr int kAccChunk = 8192;  // vocabulary entries per (row, chunk) record
+
+struct AccPartial {
+  float m_a, m_b;          // chunk max of the raw logits and of the draft logits  (reject)
+  float sa_hi, sa_lo;      // compensated sum over the chunk of 2^((l - m_a) c2)   (reject)
+  float sb_hi, sb_lo;      // same for the draft row                              (reject)
+  float val;               // best decision score                                  (argmax / gumbel)
+  int idx;                 // its first index
+};
+
+struct SlotNorm {  // p_v = 2^((l_v - m_a) c2) / s_a, q likewise
+  float m_a, m_b;
+  double s_a, s_b;
+};
+
+struct RowResult {
+  int ok;   // stage tested and accepted
+  int dec;  // decision token of the row (argmax / gumbel)
+};
+
+struct AcceptParams {
+  int mode;
+  float T;
+  float c2;                // log2(e) / T: rejection-sampling weights are 2^((l - max) * c2)
+  int V;
+  int vec;                 // rows allow 4-element vector accesses
+  int batch;
+  int total_slots;
+  int nchunks;
+  const void* logits;
+  const void* draft_logits;
+  const int32_t* draft_tokens;
+  const int32_t* tau;
+  const int32_t* block;
+  const int32_t* gamma;
+  const int32_t* slot_off;
+  const float* noise;
+  int n_noise_rows;
+  const int32_t* noise_row;
+  const float* u_accept;
+  const float* u_sample;
+  int32_t* n_acc;
+  int32_t* n_out;
+  int32_t* tokens;
+  int32_t* dev_status;
+  // workspace carve-up (the three counter arrays come first and are contiguous)
+  int32_t* cnt_seq;     // [batch]        merged rows of the sequence
+  int32_t* cnt_sample;  // [batch]        emission-row chunks done
+  int32_t* cnt_row;     // [total_slots]  chunks of the row done
+  int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
+  AccPartial* part;     // [total_slots][nchunks]
+  SlotNorm* norm;       // [total_slots]
+  RowResult* rowres;    // [total_slots]
+  float* smass;         // [batch][nchunks][4] : residual mass (hi, lo), p mass (hi, lo)
+};
+
+struct AccWorkspaceLayout {
+  size_t cnt_seq, cnt_sample, cnt_row, emit, part, norm, rowres, smass, total;
+};
+
+inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks) {
+  AccWorkspaceLayout L;
+  size_t o = 0;
+  L.cnt_seq = o;    o += sizeof(int32_t) * (size_t)batch;
+  L.cnt_sample = o; o += sizeof(int32_t) * (size_t)batch;
+  L.cnt_row = o;    o = align_up(o + sizeof(int32_t) * (size_t)total_slots, 256);
+  L.emit = o;       o = align_up(o + sizeof(int32_t) * 2 * (size_t)batch, 256);
+  L.part = o;       o = align_up(o + sizeof(AccPartial) * (size_t)total_slots * nchunks, 256);
+  L.norm = o;       o = align_up(o + sizeof(SlotNorm) * (size_t)total_slots, 256);
+  L.rowres = o;     o = align_up(o + sizeof(RowResult) * (size_t)total_slots, 256);
+  L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nchunks, 256);
+  L.total = o;
+  return L;
+}
+
+// ---- arithmetic -------------------------------------------------------------
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_logit(const void* base, size_t i) {
+  return Elem<T>::to_f32(static_cast<const T*>(base)[i]);
+}
+
+__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
+  const float y = x - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
+// (h1, l1) += (h2, l2) with an error-free transformation of the leading terms
+__device__ __forceinline__ void two_sum_acc(float& h1, float& l1, float h2, float l2) {
+  const float s = h1 + h2;
+  const float bb = s - h1;
+  const float err = (h1 - (s - bb)) + (h2 - bb);
+  h1 = s;
+  l1 = l1 + l2 + err;
+}
+
+// larger score wins; equal scores go to the smaller vocabulary index
+__device__ __forceinline__ void argmax_combine(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    argmax_combine(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void warp_sum2(float& h, float& l) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float a = __shfl_xor_sync(0xffffffffu, h, o), b = __shfl_xor_sync(0xffffffffu, l, o);
+    two_sum_acc(h, l, a, b);
+  }
+}
+
+// ---- per-sequence validity, checked by one warp (all 32 lanes) --------------
+__device__ __forceinline__ bool warp_seq_valid(const AcceptParams& p, int b) {
+  const int B = p.block[b], g = p.gamma[b];
+  bool ok = B >= 1 && B <= 64 && g >= 0 && g <= B && p.slot_off[b] + B <= p.total_slots;
+  if (ok) ok = warp_tau_is_permutation(p.tau + p.slot_off[b], B);
+  return ok;
+}
+
+// ---- completion steps (one warp, all 32 lanes) ------------------------------
+
+// Lane 0 publishes `add` arrivals on a counter (after its own prior writes);
+// returns on every lane whether this call completed the count.
+__device__ __forceinline__ bool warp_arrive(int32_t* counter, int add, int target) {
+  int last = 0;
+  if ((threadIdx.x & 31) == 0) {
+    __threadfence();
+    last = (atomicAdd(counter, add) + add) == target;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// Merge of verified row `slot` (1-based stage st, draft length g): lanes
+// over chunks.  Writes rowres[slot] and, for rejection sampling, norm[slot].
+template <int MODE, typename T>
+__device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
+  const int lane = threadIdx.x & 31;
+  const AccPartial* pp = p.part + (size_t)slot * p.nchunks;
+  const bool tested = st <= g;  // stages past gamma carry no draft token
+  RowResult rr;
+  rr.ok = 0;
+  rr.dec = -1;
+  if (MODE != SSV_ACCEPT_REJECT) {
+    float v = -INFINITY;
+    int i = INT_MAX;
+    for (int c = lane; c < p.nchunks; c += 32) argmax_combine(v, i, __ldcg(&pp[c].val), __ldcg(&pp[c].idx));
+    warp_argmax(v, i);
+    rr.dec = i;
+    rr.ok = tested && p.draft_tokens[slot] == i;
+    if (lane == 0) p.rowres[slot] = rr;
+    return;
+  }
+  // Rejection sampling: per lane a running (max, sum) over its chunks in
+  // fp64, then a max / rescaled-sum butterfly across the warp.
+  const double c2 = (double)p.c2;
+  double ma = -INFINITY, mb = -INFINITY, sa = 0.0, sb = 0.0;
+  for (int c = lane; c < p.nchunks; c += 32) {
+    const double cma = __ldcg(&pp[c].m_a);
+    const double csa = (double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo);
+    if (cma > ma) { sa = (ma == -INFINITY) ? 0.0 : sa * exp2((ma - cma) * c2); ma = cma; }
+    if (cma > -INFINITY) sa += csa * exp2((cma - ma) * c2);
+    if (tested) {
+      const double cmb = __ldcg(&pp[c].m_b);
+      const double csb = (double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo);
+      if (cmb > mb) { sb = (mb == -INFINITY) ? 0.0 : sb * exp2((mb - cmb) * c2); mb = cmb; }
+      if (cmb > -INFINITY) sb += csb * exp2((cmb - mb) * c2);
+    }
+  }
+  double Ma = ma, Mb = mb;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Ma = fmax(Ma, __shfl_xor_sync(0xffffffffu, Ma, o));
+    Mb = fmax(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
+  }
+  sa = (ma == -INFINITY) ? 0.0 : sa * exp2((ma - Ma) * c2);
+  sb = (mb == -INFINITY) ? 0.0 : sb * exp2((mb - Mb) * c2);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+  }
+  if (lane == 0) {
+    SlotNorm nm;
+    nm.m_a = (float)Ma;
+    nm.m_b = (float)Mb;
+    nm.s_a = sa;
+    nm.s_b = sb;
+    p.norm[slot] = nm;
+    if (tested) {
+      const int d = p.draft_tokens[slot];
+      if (d >= 0 && d < p.V) {
+        const double ld = ld_logit<T>(p.logits, (size_t)slot * p.V + d);
+        const double qd = ld_logit<T>(p.draft_logits, (size_t)slot * p.V + d);
+        // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
+        const double ratio = exp2(((ld - Ma) - (qd - Mb)) * c2) * (sb / sa);
+        rr.ok = (double)p.u_accept[slot] < ratio;
+      } else {
+        report(p.dev_status, SSV_ERR_INVALID);
+      }
+    }
+    p.rowres[slot] = rr;
+  }
+}
+
+// Walk of sequence b once every verified row is merged.  s_slot: 64 ints of
+// shared memory private to the calling warp (inverse stage map).
+template <int MODE>
+__device__ void warp_seq_walk(const AcceptParams& p, int b, int* s_slot) {
+  const int lane = threadIdx.x & 31;
+  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
+  for (int j = lane; j < B; j += 32) s_slot[__ldcg(&p.tau[off + j]) - 1] = j;
+  __syncwarp();
+  unsigned long long okmask = 0ull;
+  for (int base = 0; base < g; base += 32) {
+    const int st = base + lane;  // 0-based stage
+    const int ok = (st < g) ? __ldcg(&p.rowres[off + s_slot[st]].ok) : 0;
+    okmask |= (unsigned long long)__ballot_sync(0xffffffffu, ok) << base;
+  }
+  const unsigned long long rej = ~okmask;
+  int n = rej ? __ffsll((long long)rej) - 1 : 64;
+  n = min(n, g);  // longest accepted prefix in stage order
+  for (int i = lane; i < B; i += 32) {
+    int tok = -1;
+    if (i < n) tok = p.draft_tokens[off + s_slot[i]];
+    else if (i == n && MODE != SSV_ACCEPT_REJECT) tok = __ldcg(&p.rowres[off + s_slot[n]].dec);
+    p.tokens[off + i] = tok;
+  }
+  if (lane == 0) {
+    p.n_acc[b] = n;
+    p.n_out[b] = (n + 1 <= B) ? n + 1 : n;
+    if (MODE == SSV_ACCEPT_REJECT) {
+      p.emit[2 * b] = (n < B) ? off + s_slot[n] : -1;
+      p.emit[2 * b + 1] = (n + 1 <= g) ? 1 : 0;  // a rejected draft: residual (p - q)_+
+    }
+  }
+  __syncwarp();
+}
+
+// `add` more chunk records of row `slot` (sequence b) are written by lane 0:
+// run the row merge and the sequence walk when they complete the counts.
+template <int MODE, typename T>
+__device__ void warp_rows_done(const AcceptParams& p, int b, int slot, int add, int* s_slot) {
+  if (!warp_arrive(&p.cnt_row[slot], add, p.nchunks)) return;
+  const int B = p.block[b], g = p.gamma[b];
+  const int st = __ldcg(&p.tau[slot]);
+  warp_row_merge<MODE, T>(p, slot, st, g);
+  if ((threadIdx.x & 31) == 0) p.cnt_row[slot] = 0;
+  if (!warp_arrive(&p.cnt_seq[b], 1, min(g + 1, B))) return;
+  warp_seq_walk<MODE>(p, b, s_slot);
+  if ((threadIdx.x & 31) == 0) p.cnt_seq[b] = 0;
+}
+
+// ---- launchers ----------------------------------------------------------------
+// Streaming reduce (accept_stream.cu): one CTA per SM, bulk-copy ring.
+bool accept_stream_supported(const AcceptParams& p, int mode, bool bf16);
+cudaError_t launch_accept_stream(const AcceptParams& p, int mode, bool bf16, cudaStream_t st);
+
+}  // namespace ssv

@@ -1,0 +1,402 @@
+// accept_stream: the acceptance reduce as one persistent CTA per SM.
+//
+// Each CTA lists the verified rows of the batch in slot order (the same list
+// in every CTA), then takes a contiguous range of the list's (row, chunk)
+// units; a unit is kAccChunk vocabulary entries of the target logits row
+// plus, where the rule needs one, the same entries of the draft logits
+// (rejection sampling, tested stages) or of the noise row (coupled noise).
+// Warp roles:
+//   warps 0..15  consumers: wait for a stage of the ring, reduce it with
+//                warp shuffles (chunk max and compensated sums of
+//                2^((x - max) log2(e) / T), or the first argmax of the
+//                decision score), post one record per warp, release the
+//                stage;
+//   warp 16      producer (one lane): bulk-copies each unit's rows into the
+//                next free stage (cp.async.bulk, completion on an mbarrier);
+//   warp 17      publisher: merges the 16 warp records of a unit into its
+//                AccPartial and runs the row-merge / sequence-walk steps.
+// The ring keeps 128 to 192 KB of loads in flight per SM; no CTA-wide
+// barrier is taken once the list is built.  Every mbarrier wait is bounded:
+// on timeout the CTA raises SSV_ERR_TIMEOUT, the producer still waits
+// (bounded) for its own copies, and all roles return.
+#include "accept.cuh"
+#include "tc_ptx.cuh"
+
+#include <mutex>
+#include <type_traits>
+
+namespace ssv {
+namespace {
+
+using namespace ptx;
+
+constexpr int kStrConsumerWarps = 16;
+constexpr int kStrConsumers = kStrConsumerWarps * 32;        // 512
+constexpr int kStrThreads = kStrConsumers + 64;              // + producer warp + publisher warp
+constexpr int kStrWarps = kStrThreads / 32;
+constexpr int kStrProducerWarp = kStrConsumerWarps;
+constexpr int kStrGroups = kAccChunk / (4 * kStrConsumers);  // 4-entry groups per consumer thread
+constexpr int kStrRecRing = 8;
+constexpr int kStrMaxStages = 8;
+constexpr int kStrRingBytes = 192 * 1024;
+constexpr int kStrMaxRows = 2048;
+static_assert(kStrGroups * 4 * kStrConsumers == kAccChunk, "chunk split");
+
+template <int MODE, typename T>
+struct StrCfg {
+  using TB = typename std::conditional<MODE == SSV_ACCEPT_GUMBEL, float, T>::type;  // second stream
+  static constexpr uint32_t kRowB = kAccChunk * sizeof(T);                           // offset of the second row
+  static constexpr uint32_t kStage = kAccChunk * (sizeof(T) + (MODE == SSV_ACCEPT_ARGMAX ? 0 : sizeof(TB)));
+  static constexpr int kStages = (kStrRingBytes / kStage) < kStrMaxStages ? (kStrRingBytes / kStage) : kStrMaxStages;
+  static constexpr int kSmem = kStages * kStage;
+  static_assert(kStages >= 2, "ring depth");
+};
+
+struct StrShared {
+  uint64_t full[kStrMaxStages];
+  uint64_t empty[kStrMaxStages];
+  uint64_t rec_full[kStrRecRing];
+  uint64_t rec_empty[kStrRecRing];
+  AccPartial rec[kStrRecRing][kStrConsumerWarps];
+  int2 list[kStrMaxRows];              // x: slot | tested << 31, y: sequence
+  unsigned char seq_ok[kStrMaxRows];
+  int walk_slot[64];
+  int wcount[kStrWarps];
+  int abort;
+};
+
+// four consecutive entries of a staged row (e % 4 == 0)
+template <typename T>
+__device__ __forceinline__ void lds4(const unsigned char* row, int e, float* x) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + (size_t)e * 4);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(row + (size_t)e * 2);
+    x[0] = __uint_as_float(v.x << 16); x[1] = __uint_as_float(v.x & 0xffff0000u);
+    x[2] = __uint_as_float(v.y << 16); x[3] = __uint_as_float(v.y & 0xffff0000u);
+  }
+}
+
+// Is `slot` a verified row of a valid sequence?  (b: its sequence; tested:
+// its stage carries a draft token.)
+__device__ __forceinline__ bool verified_slot(const AcceptParams& p, const unsigned char* seq_ok, int slot, int& b,
+                                              int& tested) {
+  b = find_seq_by_slot(p.slot_off, p.batch, slot);
+  if (b < 0 || !seq_ok[b]) return false;
+  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
+  if (slot - off >= B) return false;
+  const int st = p.tau[slot];
+  tested = st <= g;
+  return st >= 1 && st <= min(g + 1, B);
+}
+
+// Bounded wait that ignores the abort flag (used to drain copies in flight).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* dev_status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudget) {
+      report(dev_status, SSV_ERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int MODE, typename T>
+__global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const AcceptParams p) {
+  using C = StrCfg<MODE, T>;
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ StrShared sh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), kStrConsumerWarps);
+    }
+    for (int r = 0; r < kStrRecRing; ++r) {
+      mbar_init(smem_u32(&sh.rec_full[r]), kStrConsumerWarps);
+      mbar_init(smem_u32(&sh.rec_empty[r]), 1);
+    }
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+
+  // ---- sequence validity: one warp per sequence
+  for (int b = warp; b < p.batch; b += kStrWarps) {
+    const bool ok = warp_seq_valid(p, b);
+    if (lane == 0) {
+      sh.seq_ok[b] = ok;
+      if (!ok && blockIdx.x == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
+    }
+  }
+  __syncthreads();
+  if (MODE == SSV_ACCEPT_GUMBEL) {  // a verified row needs a noise row in range
+    for (int slot = tid; slot < p.total_slots; slot += kStrThreads) {
+      int b, tested;
+      if (verified_slot(p, sh.seq_ok, slot, b, tested)) {
+        const int nr = p.noise_row[slot];
+        if (nr < 0 || nr >= p.n_noise_rows) {
+          sh.seq_ok[b] = 0;
+          if (blockIdx.x == 0) report(p.dev_status, SSV_ERR_INVALID);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- verified rows in slot order (ballot + warp counts per pass)
+  int total = 0;
+  for (int base = 0; base < p.total_slots; base += kStrThreads) {
+    const int slot = base + tid;
+    int b = -1, tested = 0;
+    const bool v = slot < p.total_slots && verified_slot(p, sh.seq_ok, slot, b, tested);
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) sh.wcount[warp] = __popc(bal);
+    __syncthreads();
+    int before = total, sum = 0;
+#pragma unroll
+    for (int w = 0; w < kStrWarps; ++w) {
+      const int c = sh.wcount[w];
+      before += (w < warp) ? c : 0;
+      sum += c;
+    }
+    if (v) {
+      const int pos = before + __popc(bal & ((1u << lane) - 1u));
+      sh.list[pos] = make_int2((int)((unsigned)slot | ((unsigned)tested << 31)), b);
+    }
+    total += sum;
+    __syncthreads();
+  }
+
+  // ---- this CTA's contiguous range of (row, chunk) units
+  const long long U = (long long)total * p.nchunks;
+  const long long u0 = U * blockIdx.x / gridDim.x;
+  const int n = (int)(U * (blockIdx.x + 1) / gridDim.x - u0);
+
+  if (warp == kStrProducerWarp) {
+    if (lane != 0) return;
+    int issued = 0;
+    for (int k = 0; k < n; ++k) {
+      const int s = k % C::kStages;
+      if (k >= C::kStages && !mbar_wait(smem_u32(&sh.empty[s]), ((k / C::kStages) - 1) & 1, &sh.abort)) break;
+      const long long u = u0 + k;
+      const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
+      const int2 e = sh.list[row];
+      const int slot = e.x & 0x7fffffff;
+      const int c0 = chunk * kAccChunk;
+      const int nvalid = min(kAccChunk, p.V - c0);
+      const uint32_t bytes_a = (uint32_t)nvalid * (uint32_t)sizeof(T);
+      uint32_t bytes_b = 0;
+      const void* src_b = nullptr;
+      if (MODE == SSV_ACCEPT_REJECT && e.x < 0) {
+        bytes_b = bytes_a;
+        src_b = static_cast<const T*>(p.draft_logits) + (size_t)slot * p.V + c0;
+      } else if (MODE == SSV_ACCEPT_GUMBEL) {
+        bytes_b = (uint32_t)nvalid * 4u;
+        src_b = p.noise + (size_t)p.noise_row[slot] * p.V + c0;
+      }
+      const uint32_t dst = smem_u32(ring + (size_t)s * C::kStage);
+      const uint32_t fb = smem_u32(&sh.full[s]);
+      mbar_expect_tx(fb, bytes_a + bytes_b);
+      bulk_load(dst, static_cast<const T*>(p.logits) + (size_t)slot * p.V + c0, bytes_a, fb);
+      if (bytes_b) bulk_load(dst + C::kRowB, src_b, bytes_b, fb);
+      issued = k + 1;
+    }
+    // leave no copy in flight: the last fill of every stage has landed
+    for (int s = 0; s < C::kStages && s < issued; ++s) {
+      const int k_last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+      drain_wait(smem_u32(&sh.full[s]), (k_last / C::kStages) & 1, p.dev_status);
+    }
+    if (sh.abort) report(p.dev_status, SSV_ERR_TIMEOUT);
+    return;
+  }
+
+  if (warp < kStrConsumerWarps) {
+    const bool unit_t = p.T == 1.0f;  // l / 1 is exact
+    for (int k = 0; k < n; ++k) {
+      const int s = k % C::kStages;
+      const bool got = mbar_wait(smem_u32(&sh.full[s]), (k / C::kStages) & 1, &sh.abort);
+      if (!__all_sync(0xffffffffu, got)) break;
+      const long long u = u0 + k;
+      const int chunk = (int)(u % p.nchunks);
+      const bool tested = sh.list[u / p.nchunks].x < 0;
+      const int c0 = chunk * kAccChunk;
+      const int nvalid = min(kAccChunk, p.V - c0);
+      const unsigned char* ra = ring + (size_t)s * C::kStage;
+      const unsigned char* rb = ra + C::kRowB;
+      AccPartial r;
+      if (MODE == SSV_ACCEPT_REJECT) {
+        float xa[4 * kStrGroups], xb[4 * kStrGroups];
+        float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kStrGroups; ++j) {
+          const int el = 4 * (j * kStrConsumers + tid);
+          if (el < nvalid) {
+            lds4<T>(ra, el, xa + 4 * j);
+            if (tested) lds4<T>(rb, el, xb + 4 * j);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xa[4 * j + q] = -INFINITY;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ma = fmaxf(ma, xa[4 * j + q]);
+            if (tested) {
+              if (el >= nvalid) xb[4 * j + q] = -INFINITY;
+              mb = fmaxf(mb, xb[4 * j + q]);
+            }
+          }
+        }
+        ma = warp_max(ma);
+        const float nma = (ma == -INFINITY) ? 0.f : -ma * p.c2;
+        float sa = 0.f, ca = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4 * kStrGroups; ++j) kahan_add(sa, ca, ex2f(fmaf(xa[j], p.c2, nma)));
+        float la = -ca;
+        warp_sum2(sa, la);
+        float sb = 0.f, lb = 0.f;
+        if (tested) {
+          mb = warp_max(mb);
+          const float nmb = (mb == -INFINITY) ? 0.f : -mb * p.c2;
+          float cb = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4 * kStrGroups; ++j) kahan_add(sb, cb, ex2f(fmaf(xb[j], p.c2, nmb)));
+          lb = -cb;
+          warp_sum2(sb, lb);
+        }
+        r.m_a = ma; r.m_b = tested ? mb : -INFINITY;
+        r.sa_hi = sa; r.sa_lo = la; r.sb_hi = sb; r.sb_lo = lb;
+        r.val = 0.f; r.idx = 0;
+      } else {
+        float best = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < kStrGroups; ++j) {
+          const int el = 4 * (j * kStrConsumers + tid);
+          if (el < nvalid) {
+            float x[4];
+            lds4<T>(ra, el, x);
+            if (MODE == SSV_ACCEPT_GUMBEL) {
+              float gn[4];
+              lds4<float>(rb, el, gn);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) x[q] = __fadd_rn(unit_t ? x[q] : __fdiv_rn(x[q], p.T), gn[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (x[q] > best || bi == INT_MAX) { best = x[q]; bi = c0 + el + q; }
+          }
+        }
+        warp_argmax(best, bi);
+        r.val = best; r.idx = bi;
+        r.m_a = r.m_b = r.sa_hi = r.sa_lo = r.sb_hi = r.sb_lo = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.empty[s]));
+      const int rs = k % kStrRecRing;
+      const bool room =
+          k < kStrRecRing || mbar_wait(smem_u32(&sh.rec_empty[rs]), ((k / kStrRecRing) - 1) & 1, &sh.abort);
+      if (!__all_sync(0xffffffffu, room)) break;
+      if (lane == 0) {
+        sh.rec[rs][warp] = r;
+        mbar_arrive(smem_u32(&sh.rec_full[rs]));
+      }
+    }
+    return;
+  }
+
+  // ---- publisher warp
+  int cur_row = -1, pend = 0;
+  int2 cur = make_int2(0, 0);
+  bool clean = true;
+  for (int k = 0; k < n; ++k) {
+    const int rs = k % kStrRecRing;
+    const bool got = mbar_wait(smem_u32(&sh.rec_full[rs]), (k / kStrRecRing) & 1, &sh.abort);
+    if (!__all_sync(0xffffffffu, got)) { clean = false; break; }
+    AccPartial x;
+    if (lane < kStrConsumerWarps) {
+      x = sh.rec[rs][lane];
+    } else {
+      x.m_a = x.m_b = -INFINITY;
+      x.sa_hi = x.sa_lo = x.sb_hi = x.sb_lo = 0.f;
+      x.val = -INFINITY;
+      x.idx = INT_MAX;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.rec_empty[rs]));
+    if (MODE == SSV_ACCEPT_REJECT) {
+      const float Ma = warp_max(x.m_a), Mb = warp_max(x.m_b);
+      const float fa = (x.m_a == -INFINITY) ? 0.f : ex2f((x.m_a - Ma) * p.c2);
+      const float fb = (x.m_b == -INFINITY) ? 0.f : ex2f((x.m_b - Mb) * p.c2);
+      float ha = x.sa_hi * fa, la = x.sa_lo * fa, hb = x.sb_hi * fb, lb = x.sb_lo * fb;
+      warp_sum2(ha, la);
+      warp_sum2(hb, lb);
+      x.m_a = Ma; x.m_b = Mb;
+      x.sa_hi = ha; x.sa_lo = la; x.sb_hi = hb; x.sb_lo = lb;
+    } else {
+      warp_argmax(x.val, x.idx);
+    }
+    const long long u = u0 + k;
+    const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
+    const int2 e = sh.list[row];
+    if (lane == 0) p.part[(size_t)(e.x & 0x7fffffff) * p.nchunks + chunk] = x;
+    if (row != cur_row) {
+      if (pend) warp_rows_done<MODE, T>(p, cur.y, cur.x & 0x7fffffff, pend, sh.walk_slot);
+      cur_row = row;
+      cur = e;
+      pend = 0;
+    }
+    ++pend;
+  }
+  if (clean && pend) warp_rows_done<MODE, T>(p, cur.y, cur.x & 0x7fffffff, pend, sh.walk_slot);
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int MODE, typename T>
+cudaError_t launch_t(const AcceptParams& p, cudaStream_t st) {
+  using C = StrCfg<MODE, T>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(accept_stream_kernel<MODE, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const long long units = (long long)p.total_slots * p.nchunks;
+  const int sms = device_sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = (int)(units < sms ? units : sms);
+  accept_stream_kernel<MODE, T><<<grid, kStrThreads, C::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool accept_stream_supported(const AcceptParams& p, int mode, bool bf16) {
+  const size_t es = bf16 ? 2 : 4;
+  if (p.total_slots > kStrMaxRows || p.batch > kStrMaxRows) return false;
+  if (((size_t)p.V * es) % 16 != 0 || ((uintptr_t)p.logits & 15u)) return false;
+  if (mode == SSV_ACCEPT_REJECT && ((uintptr_t)p.draft_logits & 15u)) return false;
+  if (mode == SSV_ACCEPT_GUMBEL && (((size_t)p.V * 4) % 16 != 0 || ((uintptr_t)p.noise & 15u))) return false;
+  return device_sm_count() > 0;
+}
+
+cudaError_t launch_accept_stream(const AcceptParams& p, int mode, bool bf16, cudaStream_t st) {
+  switch (mode) {
+    case SSV_ACCEPT_ARGMAX:
+      return bf16 ? launch_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_ARGMAX, float>(p, st);
+    case SSV_ACCEPT_GUMBEL:
+      return bf16 ? launch_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_GUMBEL, float>(p, st);
+    default:
+      return bf16 ? launch_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_REJECT, float>(p, st);
+  }
+}
+
+}  // namespace ssv

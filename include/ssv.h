@@ -27,7 +27,9 @@
  *  - Errors found on the device (a stage map that is not a permutation, a
  *    bounded wait that ran out, a non-finite temperature) are written to
  *    `dev_status` (device int32, may be NULL; first error wins) and read
- *    back with ssv_get_status().  Affected outputs are then unspecified.
+ *    back with ssv_get_status().  Affected outputs are then unspecified,
+ *    and after SSV_ERR_TIMEOUT the workspace's counter area may be left
+ *    non-zero: clear the workspace before its next use.
  *  - Nothing is thread-local; calls from several host threads on different
  *    streams are safe.  Two calls whose workspaces overlap must not run
  *    concurrently.
@@ -72,7 +74,9 @@ typedef enum {
  * prompt rows followed by 2B tail rows (D_1..D_B, then D~_1..D~_B); they sit
  * at rows [q_off, q_off + N + 2B) of Q, K_new, V_new and O.  Its C cached
  * prompt keys sit at rows [kv_off, kv_off + C) of K_cache / V_cache.  Its
- * stage map occupies tau[tau_off .. tau_off + B).
+ * stage map occupies tau[tau_off .. tau_off + B).  Sequences are packed in
+ * increasing q_off order without overlap (q_off[b] + N_b + 2B_b <=
+ * q_off[b+1]): kernels find a row's sequence by binary search on q_off.
  */
 typedef struct {
   int32_t cache_len;  /* C >= 0 */
@@ -192,7 +196,9 @@ SSV_API ssv_status ssv_verify_attn(const ssv_attn_args* a, void* workspace, size
  *              only rows of stages <= min(gamma + 1, B) are read.
  * draft_logits [total_slots, V] device, logits_dtype (REJECT only, else NULL)
  * draft_tokens, tau, noise_row, u_accept: [total_slots] device
- * block, gamma, slot_off, u_sample: [batch] device; slot_off[b] = first slot
+ * block, gamma, slot_off, u_sample: [batch] device; slot_off[b] = first slot;
+ *              sequences in increasing slot order without overlap
+ *              (slot_off[b] + block[b] <= slot_off[b+1])
  * noise [n_noise_rows, V] fp32 device (GUMBEL with T > 0 only)
  * Outputs: n_acc[batch], n_out[batch] (= n_acc + 1 if a token is emitted),
  *          tokens[total_slots]: per sequence, the accepted drafts in stage

@@ -92,3 +92,63 @@ def test_repeated_calls_share_workspace():
     for _ in range(3):
         assert compare_accept(x, gpu_accept(x, workspace=ws)) == 0
     assert int(ws[:256].sum()) == 0
+
+
+def _accept_with_logits_offset(x: W.AcceptInputs, elem_offset: int, dev_status=None):
+    """Runs ssv_accept with the logits (and draft logits) stored `elem_offset`
+    elements into a larger buffer, so that rows are not 16-byte aligned."""
+    from diffusion_speculative_verification_gb300 import io as sio
+    d = sio.accept_to_device(x)
+
+    def shifted(t):
+        if t is None:
+            return None
+        buf = torch.zeros(t.numel() + 16, dtype=t.dtype, device=t.device)
+        v = buf[elem_offset:elem_offset + t.numel()].view(t.shape)
+        v.copy_(t)
+        return v
+
+    n_acc, n_out, tokens = ssv.accept(d["mode"], d["T"], shifted(d["logits"]), d["draft_tokens"], d["tau"],
+                                      d["block"], d["gamma"], d["slot_off"], draft_logits=shifted(d["draft_logits"]),
+                                      noise=d["noise"], noise_row=d["noise_row"], u_accept=d["u_accept"],
+                                      u_sample=d["u_sample"], max_block=d["max_block"], dev_status=dev_status)
+    return n_acc.cpu().numpy(), n_out.cpu().numpy(), tokens.cpu().numpy()
+
+
+UNALIGNED = {
+    "argmax_f32": dict(mode=W.MODE_ARGMAX, T=0.0, V=20000, blocks=[8, 16, 4], gammas=[8, 12, 4]),
+    "gumbel_f32": dict(mode=W.MODE_GUMBEL, T=1.0, V=20000, blocks=[8, 16, 4], gammas=[8, 16, 2]),
+    "reject_bf16": dict(mode=W.MODE_REJECT, T=1.0, V=30000, blocks=[8, 4, 16], gammas=[5, 2, 16],
+                        logits_dtype=W.BF16),
+}
+
+
+@pytest.mark.parametrize("name", list(UNALIGNED))
+def test_rows_not_16b_aligned(name):
+    """Rows that bulk copies cannot address (offset by one element) go
+    through the general kernel; the results are the same."""
+    kw = dict(UNALIGNED[name])
+    x = W.make_accept_inputs(name, kw.pop("mode"), kw.pop("T"), kw.pop("V"), kw.pop("blocks"), kw.pop("gammas"),
+                             seed=sum(map(ord, name)) + 3, **kw)
+    aligned = gpu_accept(x)
+    shifted = _accept_with_logits_offset(x, 1)
+    compare_accept(x, aligned)
+    compare_accept(x, shifted)
+    assert np.array_equal(aligned[0], shifted[0]) and np.array_equal(aligned[1], shifted[1])
+
+
+def test_many_slots_general_kernel():
+    """More slots than the streaming kernel lists (2048) take the general kernel."""
+    blocks = [4] * 530  # 2120 slots
+    gammas = [int(g) for g in np.random.default_rng(11).integers(0, 5, size=len(blocks))]
+    x = W.make_accept_inputs("many", W.MODE_ARGMAX, 0.0, 640, blocks, gammas, seed=12)
+    assert compare_accept(x, gpu_accept(x)) == 0
+
+
+@pytest.mark.parametrize("V", [4096, 4097])
+def test_bad_noise_row_reports_status(V):
+    x = W.make_accept_inputs("badnoise", W.MODE_GUMBEL, 1.0, V, [4, 4], [4, 4], seed=13)
+    x.noise_row[1] = x.noise.shape[0] + 5
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_accept(x, dev_status=st)
+    assert ssv.get_status(st) == ssv.SSV_ERR_INVALID
