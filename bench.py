@@ -340,57 +340,122 @@ def run_ours(args):
                                 acc["gamma"], acc["slot_off"], *outs, acc["draft_logits"], acc["noise"],
                                 acc["noise_row"], acc["u_accept"], acc["u_sample"], acc["max_block"], status)
         ws_acc = torch.zeros(ssv.accept_workspace_bytes(cargs), dtype=torch.uint8, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # L2 flush between steps: a 256 MB read (twice the 129 MB L2) leaves only
+    # clean lines of an unrelated buffer, so no step inherits its inputs in L2
+    # and no write-back of dirty flush lines lands inside a measured step.
+    flush_buf = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def l2_flush():
+        torch.sum(flush_buf, dim=0, out=flush_out)
+
     L = ssv.lib()
     import ctypes as C
-    sp = stream.cuda_stream
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        ssv.rope_copy(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko, stream=stream)
-        if evs:
-            evs[1].record(stream)
-        r = L.ssv_verify_attn(C.byref(aargs), ws_attn.data_ptr(), ws_attn.numel(), sp)
+    def op_rope(s):
+        ssv.rope_copy(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko, stream=s)
+
+    def op_attn(s):
+        r = L.ssv_verify_attn(C.byref(aargs), ws_attn.data_ptr(), ws_attn.numel(), s.cuda_stream)
         if r:
             raise ssv.SsvError(r, "ssv_verify_attn")
-        if evs:
-            evs[2].record(stream)
+
+    def op_accept(s):
         if acc is not None:
-            r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), sp)
+            r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), s.cuda_stream)
             if r:
                 raise ssv.SsvError(r, "ssv_accept")
+
+    OPS = (op_rope, op_attn, op_accept)
+
+    def step(evs=None, s=None):
+        s = stream if s is None else s
+        for j, op in enumerate(OPS):
+            if evs:
+                evs[j].record(s)
+            op(s)
         if evs:
-            evs[3].record(stream)
+            evs[3].record(s)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        l2_flush()
         step()
     torch.cuda.synchronize()
     assert ssv.get_status(status) == ssv.SSV_OK
+
+    # Timed region.  Default: each sequence of K steps is captured once into a
+    # CUDA graph and replayed as one launch, timed by two events around the
+    # replay.  Graphs: K x [flush, rope, attn, accept] (the step), K x [flush],
+    # and K x [flush, op] per op; step and op times are the differences with
+    # the flush-only graph, divided by K.  No event sits between the kernels,
+    # and host launch latency never leaves the GPU idle inside a measurement.
+    # --eager: one call at a time with events between the ops.
+    launch = "eager" if args.eager else "cuda_graph"
+
+    def capture(bodies):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(args.steps):
+                l2_flush()
+                for body in bodies:
+                    body(cap)
+        stream.wait_stream(cap)
+        return g
+
+    graphs = None
+    if launch == "cuda_graph":
+        graphs = {"step": capture(OPS), "flush": capture(()), "rope": capture((op_rope,)),
+                  "verify_attn": capture((op_attn,))}
+        if acc is not None:
+            graphs["accept"] = capture((op_accept,))
+        torch.cuda.synchronize()
+        for g in graphs.values():  # first replay uploads the graph
+            g.replay()
+        torch.cuda.synchronize()
+
+    def timed_replay(g):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
 
     props = torch.cuda.get_device_properties(dev)
     clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
     if rank == 0:
         clocks.start()
         time.sleep(0.3)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark("t0")
-    for i in range(args.steps):
-        flush.zero_()
-        step(events[i])
-    torch.cuda.synchronize()
-    clocks.mark("t1")
+    if graphs is not None:
+        t_step = timed_replay(graphs["step"])
+        torch.cuda.synchronize()
+        clocks.mark("t1")
+        t_flush = timed_replay(graphs["flush"])
+        op_ms = np.array([(timed_replay(graphs[k]) - t_flush) / args.steps if k in graphs else 0.0
+                          for k in ("rope", "verify_attn", "accept")])
+        step_total = t_step - t_flush
+    else:
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            l2_flush()
+            step(events[i])
+        torch.cuda.synchronize()
+        clocks.mark("t1")
+        per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
+        op_ms = per.mean(axis=0)
+        step_total = float(per.sum())
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if rank == 0 else None
     assert ssv.get_status(status) == ssv.SSV_OK
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
-    step_ms = per.sum(axis=1)
-    tot_ms = aggregate_ms(float(step_ms.sum()), dist if world > 1 else None, dev)
+    tot_ms = aggregate_ms(float(step_total), dist if world > 1 else None, dev)
 
     rb = rope_bytes(a)
     ab, af = attn_work(a, out_b)
@@ -398,7 +463,6 @@ def run_ours(args):
     step_bytes = rb + ab + cb
     ms_step = tot_ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    op_ms = per.mean(axis=0)
     hbm_peak, tf_peak, peak_kind = load_peaks()
     ops = {"rope": (op_ms[0], rb), "verify_attn": (op_ms[1], ab), "accept": (op_ms[2], cb)}
     dom = max(ops, key=lambda k: ops[k][0])
@@ -422,7 +486,8 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": a.dtype, "data": "synthetic (seeded)",
             "config": {"workload": args.config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d,
-                       "l2": "256 MB memset before every step", "parallelism": f"replicas x{world}"},
+                       "l2": "256 MB read before every step", "launch": launch,
+                       "parallelism": f"replicas x{world}"},
             "verify_attn": {"us": round(op_ms[1] * 1e3, 2), "gbs": round(ab / (op_ms[1] * 1e-3) / 1e9, 1),
                             "tflops": round(af / (op_ms[1] * 1e-3) / 1e12, 2), "bytes": ab, "flops": af},
             "rope": {"us": round(op_ms[0] * 1e3, 2), "gbs": round(rb / (op_ms[0] * 1e-3) / 1e9, 1), "bytes": rb},
@@ -492,6 +557,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=list(W.WORKLOADS), default="gqa1p7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch the timed steps one call at a time")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -138,7 +138,7 @@ template <int MODE, typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_reduce_kernel(const AcceptParams p) {
   __shared__ int s_ok;
-  __shared__ int s_slot[64];
+  __shared__ WalkSmem s_walk;
   const int slot = blockIdx.x / p.nchunks;
   const int chunk = blockIdx.x % p.nchunks;
   const int b = find_seq_by_slot(p.slot_off, p.batch, slot);
@@ -218,7 +218,7 @@ accept_reduce_kernel(const AcceptParams p) {
     out.val = 0.f; out.idx = 0;
   }
   if (tid == 0) p.part[(size_t)slot * p.nchunks + chunk] = out;
-  if (tid < 32) warp_rows_done<MODE, T>(p, b, slot, 1, s_slot);
+  if (tid < 32) warp_rows_done<MODE, T>(p, b, slot, 1, s_walk);
 }
 
 // ---- rejection sampling: emitted token ------------------------------------

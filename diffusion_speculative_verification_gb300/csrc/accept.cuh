@@ -41,7 +41,7 @@ struct SlotNorm {  // p_v = 2^((l_v - m_a) c2) / s_a, q likewise
   double s_a, s_b;
 };
 
-struct RowResult {
+struct __align__(8) RowResult {
   int ok;   // stage tested and accepted
   int dec;  // decision token of the row (argmax / gumbel)
 };
@@ -164,16 +164,24 @@ __device__ __forceinline__ bool warp_seq_valid(const AcceptParams& p, int b) {
 
 // ---- completion steps (one warp, all 32 lanes) ------------------------------
 
-// Lane 0 publishes `add` arrivals on a counter (after its own prior writes);
-// returns on every lane whether this call completed the count.
+// Lane 0 publishes `add` arrivals on a counter, releasing its own earlier
+// writes; returns on every lane whether this call completed the count (then
+// every lane has acquire ordering for the other contributors' writes).  A
+// caller that brings the whole count at once needs no counter at all.
 __device__ __forceinline__ bool warp_arrive(int32_t* counter, int add, int target) {
+  if (add == target) {  // every record is this warp's own (lane 0 wrote them)
+    __syncwarp();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    return true;
+  }
   int last = 0;
   if ((threadIdx.x & 31) == 0) {
-    __threadfence();
-    last = (atomicAdd(counter, add) + add) == target;
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(prev) : "l"(counter), "r"(add) : "memory");
+    last = (prev + add) == target;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
-  if (last) __threadfence();
+  if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
   return last != 0;
 }
 
@@ -198,7 +206,19 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
     return;
   }
   // Rejection sampling: per lane a running (max, sum) over its chunks in
-  // fp64, then a max / rescaled-sum butterfly across the warp.
+  // fp64, then a max / rescaled-sum butterfly across the warp.  Lane 0 loads
+  // the draft token's two logits while the chunk records are in flight.
+  int d = -1;
+  double ld = 0.0, qd = 0.0;
+  float ua = 0.f;
+  if (tested && lane == 0) {
+    d = p.draft_tokens[slot];
+    ua = p.u_accept[slot];
+    if (d >= 0 && d < p.V) {
+      ld = ld_logit<T>(p.logits, (size_t)slot * p.V + d);
+      qd = ld_logit<T>(p.draft_logits, (size_t)slot * p.V + d);
+    }
+  }
   const double c2 = (double)p.c2;
   double ma = -INFINITY, mb = -INFINITY, sa = 0.0, sb = 0.0;
   for (int c = lane; c < p.nchunks; c += 32) {
@@ -234,13 +254,10 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
     nm.s_b = sb;
     p.norm[slot] = nm;
     if (tested) {
-      const int d = p.draft_tokens[slot];
       if (d >= 0 && d < p.V) {
-        const double ld = ld_logit<T>(p.logits, (size_t)slot * p.V + d);
-        const double qd = ld_logit<T>(p.draft_logits, (size_t)slot * p.V + d);
         // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
         const double ratio = exp2(((ld - Ma) - (qd - Mb)) * c2) * (sb / sa);
-        rr.ok = (double)p.u_accept[slot] < ratio;
+        rr.ok = (double)ua < ratio;
       } else {
         report(p.dev_status, SSV_ERR_INVALID);
       }
@@ -249,34 +266,63 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
   }
 }
 
-// Walk of sequence b once every verified row is merged.  s_slot: 64 ints of
-// shared memory private to the calling warp (inverse stage map).
+// Shared-memory scratch of the warp that walks a sequence.
+struct WalkSmem {
+  int slot[64];  // slot (offset in the sequence) of each stage
+  int ok[64];    // per stage: tested and accepted
+  int dec[64];   // per stage: decision token (argmax / gumbel)
+  int tok[64];   // per stage: draft token
+};
+
+// Walk of sequence b once every verified row is merged: one round of loads
+// (stage map, row results, draft tokens), rearranged into stage order.
 template <int MODE>
-__device__ void warp_seq_walk(const AcceptParams& p, int b, int* s_slot) {
+__device__ void warp_seq_walk(const AcceptParams& p, int b, WalkSmem& w) {
   const int lane = threadIdx.x & 31;
   const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
-  for (int j = lane; j < B; j += 32) s_slot[__ldcg(&p.tau[off + j]) - 1] = j;
+  const int need = min(g + 1, B);
+  int st[2], rok[2], rdec[2], dtok[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    st[h] = (j < B) ? __ldcg(&p.tau[off + j]) : 0;
+    dtok[h] = (j < B) ? p.draft_tokens[off + j] : -1;
+    const int2 r = (j < B) ? __ldcg(reinterpret_cast<const int2*>(p.rowres + off + j)) : make_int2(0, -1);
+    rok[h] = r.x;
+    rdec[h] = r.y;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    if (j < B) {
+      const int s0 = st[h] - 1;  // a valid sequence's map is a permutation of 1..B
+      const bool merged = s0 < need;  // only verified rows hold row results
+      w.slot[s0] = j;
+      w.ok[s0] = merged ? rok[h] : 0;
+      w.dec[s0] = merged ? rdec[h] : -1;
+      w.tok[s0] = dtok[h];
+    }
+  }
   __syncwarp();
   unsigned long long okmask = 0ull;
   for (int base = 0; base < g; base += 32) {
-    const int st = base + lane;  // 0-based stage
-    const int ok = (st < g) ? __ldcg(&p.rowres[off + s_slot[st]].ok) : 0;
-    okmask |= (unsigned long long)__ballot_sync(0xffffffffu, ok) << base;
+    const int s0 = base + lane;  // 0-based stage
+    okmask |= (unsigned long long)__ballot_sync(0xffffffffu, s0 < g && w.ok[s0]) << base;
   }
   const unsigned long long rej = ~okmask;
   int n = rej ? __ffsll((long long)rej) - 1 : 64;
   n = min(n, g);  // longest accepted prefix in stage order
   for (int i = lane; i < B; i += 32) {
     int tok = -1;
-    if (i < n) tok = p.draft_tokens[off + s_slot[i]];
-    else if (i == n && MODE != SSV_ACCEPT_REJECT) tok = __ldcg(&p.rowres[off + s_slot[n]].dec);
+    if (i < n) tok = w.tok[i];
+    else if (i == n && MODE != SSV_ACCEPT_REJECT) tok = w.dec[n];
     p.tokens[off + i] = tok;
   }
   if (lane == 0) {
     p.n_acc[b] = n;
     p.n_out[b] = (n + 1 <= B) ? n + 1 : n;
     if (MODE == SSV_ACCEPT_REJECT) {
-      p.emit[2 * b] = (n < B) ? off + s_slot[n] : -1;
+      p.emit[2 * b] = (n < B) ? off + w.slot[n] : -1;
       p.emit[2 * b + 1] = (n + 1 <= g) ? 1 : 0;  // a rejected draft: residual (p - q)_+
     }
   }
@@ -286,15 +332,15 @@ __device__ void warp_seq_walk(const AcceptParams& p, int b, int* s_slot) {
 // `add` more chunk records of row `slot` (sequence b) are written by lane 0:
 // run the row merge and the sequence walk when they complete the counts.
 template <int MODE, typename T>
-__device__ void warp_rows_done(const AcceptParams& p, int b, int slot, int add, int* s_slot) {
+__device__ void warp_rows_done(const AcceptParams& p, int b, int slot, int add, WalkSmem& w) {
   if (!warp_arrive(&p.cnt_row[slot], add, p.nchunks)) return;
   const int B = p.block[b], g = p.gamma[b];
   const int st = __ldcg(&p.tau[slot]);
   warp_row_merge<MODE, T>(p, slot, st, g);
-  if ((threadIdx.x & 31) == 0) p.cnt_row[slot] = 0;
+  if ((threadIdx.x & 31) == 0 && add != p.nchunks) p.cnt_row[slot] = 0;
   if (!warp_arrive(&p.cnt_seq[b], 1, min(g + 1, B))) return;
-  warp_seq_walk<MODE>(p, b, s_slot);
-  if ((threadIdx.x & 31) == 0) p.cnt_seq[b] = 0;
+  warp_seq_walk<MODE>(p, b, w);
+  if ((threadIdx.x & 31) == 0 && min(g + 1, B) != 1) p.cnt_seq[b] = 0;
 }
 
 // ---- launchers ----------------------------------------------------------------

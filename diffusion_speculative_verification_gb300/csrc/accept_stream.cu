@@ -52,15 +52,21 @@ struct StrCfg {
   static_assert(kStages >= 2, "ring depth");
 };
 
+constexpr int kStrPer = (kStrMaxRows + kStrThreads - 1) / kStrThreads;  // slots (sequences) per thread
+
 struct StrShared {
   uint64_t full[kStrMaxStages];
   uint64_t empty[kStrMaxStages];
   uint64_t rec_full[kStrRecRing];
   uint64_t rec_empty[kStrRecRing];
   AccPartial rec[kStrRecRing][kStrConsumerWarps];
-  int2 list[kStrMaxRows];              // x: slot | tested << 31, y: sequence
+  int32_t list[kStrMaxRows];           // verified slot | tested << 31
+  int32_t off[kStrMaxRows];            // slot_off per sequence
+  unsigned char blk[kStrMaxRows];      // block (0 when the sizes are invalid)
+  unsigned char gam[kStrMaxRows];      // gamma
+  unsigned char stage[kStrMaxRows];    // tau per slot (0 when outside 1..64)
   unsigned char seq_ok[kStrMaxRows];
-  int walk_slot[64];
+  WalkSmem walk;
   int wcount[kStrWarps];
   int abort;
 };
@@ -78,17 +84,25 @@ __device__ __forceinline__ void lds4(const unsigned char* row, int e, float* x) 
   }
 }
 
-// Is `slot` a verified row of a valid sequence?  (b: its sequence; tested:
-// its stage carries a draft token.)
-__device__ __forceinline__ bool verified_slot(const AcceptParams& p, const unsigned char* seq_ok, int slot, int& b,
-                                              int& tested) {
-  b = find_seq_by_slot(p.slot_off, p.batch, slot);
-  if (b < 0 || !seq_ok[b]) return false;
-  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
-  if (slot - off >= B) return false;
-  const int st = p.tau[slot];
+// Sequence holding `slot` (binary search over the shared slot offsets;
+// sequences are packed in increasing slot order), or -1.
+__device__ __forceinline__ int seq_of_slot(const StrShared& sh, int batch, int slot) {
+  int lo = 0, hi = batch - 1, ans = -1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (sh.off[mid] <= slot) { ans = mid; lo = mid + 1; } else { hi = mid - 1; }
+  }
+  return ans;
+}
+
+// Is `slot` a verified row (stage <= min(gamma + 1, B)) of a valid sequence?
+// b: its sequence; tested: its stage carries a draft token.
+__device__ __forceinline__ bool verified_slot(const StrShared& sh, int batch, int slot, int& b, int& tested) {
+  b = seq_of_slot(sh, batch, slot);
+  if (b < 0 || !sh.seq_ok[b] || slot - sh.off[b] >= sh.blk[b]) return false;
+  const int st = sh.stage[slot], g = sh.gam[b];
   tested = st <= g;
-  return st >= 1 && st <= min(g + 1, B);
+  return st >= 1 && st <= min(g + 1, (int)sh.blk[b]);
 }
 
 // Bounded wait that ignores the abort flag (used to drain copies in flight).
@@ -122,9 +136,40 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     fence_mbar_init();
   }
 
-  // ---- sequence validity: one warp per sequence
+  // ---- every metadata load at once (one round trip), kept in shared memory
+  int nrow[kStrPer];
+#pragma unroll
+  for (int i = 0; i < kStrPer; ++i) {
+    const int slot = tid + i * kStrThreads;
+    nrow[i] = 0;
+    if (slot < p.total_slots) {
+      const int t = p.tau[slot];
+      sh.stage[slot] = (t >= 1 && t <= 64) ? (unsigned char)t : 0;
+      if (MODE == SSV_ACCEPT_GUMBEL) nrow[i] = p.noise_row[slot];
+    }
+    if (slot < p.batch) {
+      const int off = p.slot_off[slot], B = p.block[slot], g = p.gamma[slot];
+      const bool sizes = off >= 0 && B >= 1 && B <= 64 && g >= 0 && g <= B && off + B <= p.total_slots;
+      sh.off[slot] = off;
+      sh.blk[slot] = sizes ? (unsigned char)B : 0;
+      sh.gam[slot] = sizes ? (unsigned char)g : 0;
+    }
+  }
+  __syncthreads();
+  // ---- sequence validity: sizes, and tau a permutation of 1..B (one warp per sequence)
   for (int b = warp; b < p.batch; b += kStrWarps) {
-    const bool ok = warp_seq_valid(p, b);
+    const int B = sh.blk[b], off = sh.off[b];
+    unsigned long long seen = 0ull;
+    bool ok = B >= 1;
+    if (ok) {
+      for (int j = lane; j < B; j += 32) {
+        const int t = sh.stage[off + j];
+        if (t < 1 || t > B) ok = false; else seen |= 1ull << (t - 1);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) seen |= __shfl_xor_sync(0xffffffffu, seen, o);
+    }
+    ok = __all_sync(0xffffffffu, ok) && seen == ((B >= 64) ? ~0ull : ((1ull << B) - 1ull));
     if (lane == 0) {
       sh.seq_ok[b] = ok;
       if (!ok && blockIdx.x == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
@@ -132,14 +177,14 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   }
   __syncthreads();
   if (MODE == SSV_ACCEPT_GUMBEL) {  // a verified row needs a noise row in range
-    for (int slot = tid; slot < p.total_slots; slot += kStrThreads) {
+#pragma unroll
+    for (int i = 0; i < kStrPer; ++i) {
+      const int slot = tid + i * kStrThreads;
       int b, tested;
-      if (verified_slot(p, sh.seq_ok, slot, b, tested)) {
-        const int nr = p.noise_row[slot];
-        if (nr < 0 || nr >= p.n_noise_rows) {
-          sh.seq_ok[b] = 0;
-          if (blockIdx.x == 0) report(p.dev_status, SSV_ERR_INVALID);
-        }
+      if (slot < p.total_slots && verified_slot(sh, p.batch, slot, b, tested) &&
+          (nrow[i] < 0 || nrow[i] >= p.n_noise_rows)) {
+        sh.seq_ok[b] = 0;
+        if (blockIdx.x == 0) report(p.dev_status, SSV_ERR_INVALID);
       }
     }
     __syncthreads();
@@ -150,7 +195,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   for (int base = 0; base < p.total_slots; base += kStrThreads) {
     const int slot = base + tid;
     int b = -1, tested = 0;
-    const bool v = slot < p.total_slots && verified_slot(p, sh.seq_ok, slot, b, tested);
+    const bool v = slot < p.total_slots && verified_slot(sh, p.batch, slot, b, tested);
     const unsigned bal = __ballot_sync(0xffffffffu, v);
     if (lane == 0) sh.wcount[warp] = __popc(bal);
     __syncthreads();
@@ -163,7 +208,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     }
     if (v) {
       const int pos = before + __popc(bal & ((1u << lane) - 1u));
-      sh.list[pos] = make_int2((int)((unsigned)slot | ((unsigned)tested << 31)), b);
+      sh.list[pos] = (int)((unsigned)slot | ((unsigned)tested << 31));
     }
     total += sum;
     __syncthreads();
@@ -182,14 +227,14 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
       if (k >= C::kStages && !mbar_wait(smem_u32(&sh.empty[s]), ((k / C::kStages) - 1) & 1, &sh.abort)) break;
       const long long u = u0 + k;
       const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
-      const int2 e = sh.list[row];
-      const int slot = e.x & 0x7fffffff;
+      const int e = sh.list[row];
+      const int slot = e & 0x7fffffff;
       const int c0 = chunk * kAccChunk;
       const int nvalid = min(kAccChunk, p.V - c0);
       const uint32_t bytes_a = (uint32_t)nvalid * (uint32_t)sizeof(T);
       uint32_t bytes_b = 0;
       const void* src_b = nullptr;
-      if (MODE == SSV_ACCEPT_REJECT && e.x < 0) {
+      if (MODE == SSV_ACCEPT_REJECT && e < 0) {
         bytes_b = bytes_a;
         src_b = static_cast<const T*>(p.draft_logits) + (size_t)slot * p.V + c0;
       } else if (MODE == SSV_ACCEPT_GUMBEL) {
@@ -220,15 +265,16 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
       if (!__all_sync(0xffffffffu, got)) break;
       const long long u = u0 + k;
       const int chunk = (int)(u % p.nchunks);
-      const bool tested = sh.list[u / p.nchunks].x < 0;
+      const bool tested = sh.list[u / p.nchunks] < 0;
       const int c0 = chunk * kAccChunk;
       const int nvalid = min(kAccChunk, p.V - c0);
       const unsigned char* ra = ring + (size_t)s * C::kStage;
       const unsigned char* rb = ra + C::kRowB;
       AccPartial r;
       if (MODE == SSV_ACCEPT_REJECT) {
+        // chunk max (3-input max), then sum of 2^((x - max) c2) with packed
+        // f32x2 FMA / add (two chains of 8 terms per thread), TwoSum across lanes
         float xa[4 * kStrGroups], xb[4 * kStrGroups];
-        float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
         for (int j = 0; j < kStrGroups; ++j) {
           const int el = 4 * (j * kStrConsumers + tid);
@@ -237,36 +283,38 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
             if (tested) lds4<T>(rb, el, xb + 4 * j);
           } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) xa[4 * j + q] = -INFINITY;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            ma = fmaxf(ma, xa[4 * j + q]);
-            if (tested) {
-              if (el >= nvalid) xb[4 * j + q] = -INFINITY;
-              mb = fmaxf(mb, xb[4 * j + q]);
-            }
+            for (int q = 0; q < 4; ++q) xa[4 * j + q] = xb[4 * j + q] = -INFINITY;
           }
         }
-        ma = warp_max(ma);
-        const float nma = (ma == -INFINITY) ? 0.f : -ma * p.c2;
-        float sa = 0.f, ca = 0.f;
+        const uint64_t c22 = pack2(p.c2, p.c2);
+        auto row_sum = [&](const float* x, float& m, float& hi, float& lo) {
+          m = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 4 * kStrGroups; ++j) kahan_add(sa, ca, ex2f(fmaf(xa[j], p.c2, nma)));
-        float la = -ca;
-        warp_sum2(sa, la);
-        float sb = 0.f, lb = 0.f;
+          for (int j = 0; j < 4 * kStrGroups; j += 2) m = max3(m, x[j], x[j + 1]);
+          m = warp_max(m);
+          const float nm = (m == -INFINITY) ? 0.f : -m * p.c2;
+          const uint64_t nm2 = pack2(nm, nm);
+          uint64_t acc = pack2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 4 * kStrGroups; j += 2) {
+            float y0, y1;
+            unpack2(ffma2(pack2(x[j], x[j + 1]), c22, nm2), y0, y1);
+            acc = fadd2(acc, pack2(ex2f(y0), ex2f(y1)));
+          }
+          float s0, s1;
+          unpack2(acc, s0, s1);
+          hi = s0;
+          lo = 0.f;
+          two_sum_acc(hi, lo, s1, 0.f);
+          warp_sum2(hi, lo);
+        };
+        row_sum(xa, r.m_a, r.sa_hi, r.sa_lo);
         if (tested) {
-          mb = warp_max(mb);
-          const float nmb = (mb == -INFINITY) ? 0.f : -mb * p.c2;
-          float cb = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4 * kStrGroups; ++j) kahan_add(sb, cb, ex2f(fmaf(xb[j], p.c2, nmb)));
-          lb = -cb;
-          warp_sum2(sb, lb);
+          row_sum(xb, r.m_b, r.sb_hi, r.sb_lo);
+        } else {
+          r.m_b = -INFINITY;
+          r.sb_hi = r.sb_lo = 0.f;
         }
-        r.m_a = ma; r.m_b = tested ? mb : -INFINITY;
-        r.sa_hi = sa; r.sa_lo = la; r.sb_hi = sb; r.sb_lo = lb;
         r.val = 0.f; r.idx = 0;
       } else {
         float best = -INFINITY;
@@ -307,8 +355,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   }
 
   // ---- publisher warp
-  int cur_row = -1, pend = 0;
-  int2 cur = make_int2(0, 0);
+  int cur_row = -1, cur_slot = 0, pend = 0;
   bool clean = true;
   for (int k = 0; k < n; ++k) {
     const int rs = k % kStrRecRing;
@@ -339,17 +386,17 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     }
     const long long u = u0 + k;
     const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
-    const int2 e = sh.list[row];
-    if (lane == 0) p.part[(size_t)(e.x & 0x7fffffff) * p.nchunks + chunk] = x;
+    const int slot = sh.list[row] & 0x7fffffff;
+    if (lane == 0) p.part[(size_t)slot * p.nchunks + chunk] = x;
     if (row != cur_row) {
-      if (pend) warp_rows_done<MODE, T>(p, cur.y, cur.x & 0x7fffffff, pend, sh.walk_slot);
+      if (pend) warp_rows_done<MODE, T>(p, seq_of_slot(sh, p.batch, cur_slot), cur_slot, pend, sh.walk);
       cur_row = row;
-      cur = e;
+      cur_slot = slot;
       pend = 0;
     }
     ++pend;
   }
-  if (clean && pend) warp_rows_done<MODE, T>(p, cur.y, cur.x & 0x7fffffff, pend, sh.walk_slot);
+  if (clean && pend) warp_rows_done<MODE, T>(p, seq_of_slot(sh, p.batch, cur_slot), cur_slot, pend, sh.walk);
 }
 
 int device_sm_count() {

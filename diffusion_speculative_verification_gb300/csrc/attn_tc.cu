@@ -124,31 +124,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// packed fp32x2 helpers (Blackwell f32x2 FMA / add) and a 3-input max
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t pick4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, int w) {
   return w == 0 ? a : (w == 1 ? b : (w == 2 ? c : (w == 3 ? d : 0u)));
 }
@@ -421,7 +396,56 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         mma_commit(bar(B_PV_DONE + mt));
       };
       auto wait_k = [&]() -> bool { return mbar_wait_poll(bar(B_K_FULL + kn % NSK), (kn / NSK) & 1, abort); };
-      while (run && remaining > 0) {
+      if constexpr (MT == 1) {
+        // One tile, S double-buffered: block n's S goes to TMEM buffer n & 1, so
+        // S(n + 1) runs while the softmax warps work on S(n).  Order per block:
+        // PV(n) (reads P(n) from buffer n & 1), then S(n + 2) into the same
+        // buffer (tensor-core operations of this thread complete in issue order).
+        int ns_issued = 0, np_issued = 0;  // blocks whose S / PV have been issued (CTA-wide)
+        auto issue_s_db = [&]() -> bool {
+          if (!wait_k()) return false;
+          tc_fence_after();
+          const int sbuf = ns_issued & 1;
+          const int st = kn % NSK;
+          gemm_ss_k128(tmem + sbuf * 128, dq0, st == 0 ? dk0 : (st == 1 ? dk1 : dk2), id_s, 0u);
+          mma_commit(bar(B_S_FULL + sbuf));
+          mma_commit(bar(B_K_EMPTY + st));
+          ++kn;
+          ++ns_issued;
+          return true;
+        };
+        while (run && remaining > 0) {
+          const Unit x = decode(u);
+          const int len = min(x.nblocks - k, remaining);
+          if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+          if (!issue_s_db()) break;
+          if (len > 1 && !issue_s_db()) break;
+          for (int i = 0; i < len; ++i) {
+            const int pbuf = np_issued & 1;
+            if (!mbar_wait_poll(bar(B_V_FULL + vn % NSV), (vn / NSV) & 1, abort) ||
+                !mbar_wait_poll(bar(B_P_FULL + pbuf), (np_issued >> 1) & 1, abort) ||
+                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
+              run = false;
+              break;
+            }
+            tc_fence_after();
+            gemm_ts_k128(tmem + TM_O, tmem + pbuf * 128, (vn % NSV) ? dv1 : dv0, id_pv, i > 0 ? 1u : 0u);
+            mma_commit(bar(B_PV_DONE));
+            mma_commit(bar(B_V_EMPTY + vn % NSV));
+            ++vn;
+            ++np_issued;
+            if (i + 2 < len && !issue_s_db()) { run = false; break; }
+          }
+          if (!run) break;
+          mma_commit(bar(B_Q_EMPTY));
+          ++nseg0;
+          remaining -= len;
+          ++seg;
+          ++u;
+          k = 0;
+        }
+      }
+      while (MT > 1 && run && remaining > 0) {
         const Unit x = decode(u);
         const int len = min(x.nblocks - k, remaining);
         if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
@@ -477,7 +501,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     const int q4 = warp & 3;          // TMEM lane quadrant
     const int m = q4 * 32 + lane;     // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS = tmem + lane_base + mt * 128;
+    const uint32_t tS0 = tmem + lane_base + mt * 128;
     const uint32_t tO = tmem + lane_base + TM_O + mt * 128;
     const float cexp = p.scale * 1.4426950408889634f;
     int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, nblk = 0, pos = begin;
@@ -519,10 +543,14 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         float m_used = -INFINITY, l_sum = 0.f;
         for (int jj = 0; jj < len; ++jj, ++nblk) {
           const int j = k + jj;
-          if (!warp_wait(bar(B_S_FULL + mt), nblk & 1)) { run = false; break; }
+          // one tile: S alternates between two TMEM buffers (block n in buffer n & 1)
+          const int sb = (MT == 1) ? (nblk & 1) : mt;
+          const uint32_t tS = (MT == 1) ? tS0 + sb * 128 : tS0;
+          const uint32_t sparity = (MT == 1) ? ((nblk >> 1) & 1) : (nblk & 1);
+          if (!warp_wait(bar(B_S_FULL + sb), sparity)) { run = false; break; }
           if (!warp_active) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + mt));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
             continue;
           }
           tc_fence_after();
@@ -678,7 +706,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           l_sum += (l0 + l1) + (l2 + l3);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_P_FULL + mt));
+          if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
         }
         if (!run) break;
         // ---- segment epilogue: O stays in TMEM until O_FREE is signalled
@@ -749,46 +777,106 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                 return ((size_t)((rr * p.Hkv + gh) * 2 + wh) * MT + mt) * 128 + m;
               };
               // combine in CTA order (not arrival order) so the result is deterministic
-              float M = m_used;
-              for (int cc = c_a; cc <= c_b; ++cc)
-                if (cc != rank) M = fmaxf(M, __ldcg(work.part_ml + slot_of(cc) * 2));
-              float L = 0.f;
-              for (int cc = c_a; cc <= c_b; ++cc) {
-                float mo = m_used, lo = l_sum;
-                if (cc != rank) {
-                  const float2 ml = __ldcg(reinterpret_cast<const float2*>(work.part_ml + slot_of(cc) * 2));
-                  mo = ml.x;
-                  lo = ml.y;
-                }
-                if (M > -INFINITY) L += lo * ex2(mo - M);
-              }
-              const float inv = (L > 0.f) ? 1.f / L : 0.f;
-#pragma unroll 1
-              for (int q = 0; q < D / 32; ++q) {
-                float v[32];
+              const int nparts = c_b - c_a + 1;
+              if (nparts <= 4) {
+                // (m, l) of every partial in one round of loads, then O 64 columns at a
+                // time with all of a partial's loads for those columns issued together
+                float2 ml[4];
+                const float* po[4];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0.f;
-                for (int cc = c_a; cc <= c_b; ++cc) {
-                  if (cc == rank) {
-                    uint32_t raw[32];
-                    tmem_ld32(tO + q * 32, raw);
-                    tmem_wait_ld();
-                    const float fo = (M == -INFINITY) ? 0.f : ex2(m_used - M);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] += __uint_as_float(raw[e]) * fo;
-                  } else {
-                    const size_t sl = slot_of(cc);
-                    const float mo = __ldcg(work.part_ml + sl * 2);
-                    const float fo = (M == -INFINITY) ? 0.f : ex2(mo - M);
-                    const float* po = work.part_o + sl * D + q * 32;
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                      const float4 w4 = __ldcg(reinterpret_cast<const float4*>(po + c));
-                      v[c] += w4.x * fo; v[c + 1] += w4.y * fo; v[c + 2] += w4.z * fo; v[c + 3] += w4.w * fo;
+                for (int k = 0; k < 4; ++k) {
+                  const int cc = c_a + k;
+                  po[k] = nullptr;
+                  ml[k] = make_float2(-INFINITY, 0.f);
+                  if (k < nparts) {
+                    if (cc == rank) {
+                      ml[k] = make_float2(m_used, l_sum);
+                    } else {
+                      const size_t sl = slot_of(cc);
+                      ml[k] = __ldcg(reinterpret_cast<const float2*>(work.part_ml + sl * 2));
+                      po[k] = work.part_o + sl * D;
                     }
                   }
                 }
-                store_chunk(q, v, inv);
+                float M = -INFINITY;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) M = fmaxf(M, ml[k].x);
+                float L = 0.f, fo[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  fo[k] = (M == -INFINITY || k >= nparts) ? 0.f : ex2(ml[k].x - M);
+                  L += ml[k].y * fo[k];
+                }
+                const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll 1
+                for (int q = 0; q < D / 32; ++q) {
+                  float v[32];
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) v[e] = 0.f;
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    if (k >= nparts) break;
+                    if (po[k] == nullptr) {
+                      uint32_t raw[32];
+                      tmem_ld32(tO + q * 32, raw);
+                      tmem_wait_ld();
+#pragma unroll
+                      for (int e = 0; e < 32; ++e) v[e] += __uint_as_float(raw[e]) * fo[k];
+                    } else {
+                      float4 w4[8];
+#pragma unroll
+                      for (int c = 0; c < 8; ++c) w4[c] = __ldcg(reinterpret_cast<const float4*>(po[k] + q * 32) + c);
+#pragma unroll
+                      for (int c = 0; c < 8; ++c) {
+                        v[4 * c] += w4[c].x * fo[k]; v[4 * c + 1] += w4[c].y * fo[k];
+                        v[4 * c + 2] += w4[c].z * fo[k]; v[4 * c + 3] += w4[c].w * fo[k];
+                      }
+                    }
+                  }
+                  store_chunk(q, v, inv);
+                }
+              } else {
+                float M = m_used;
+                for (int cc = c_a; cc <= c_b; ++cc)
+                  if (cc != rank) M = fmaxf(M, __ldcg(work.part_ml + slot_of(cc) * 2));
+                float L = 0.f;
+                for (int cc = c_a; cc <= c_b; ++cc) {
+                  float mo = m_used, lo = l_sum;
+                  if (cc != rank) {
+                    const float2 mlc = __ldcg(reinterpret_cast<const float2*>(work.part_ml + slot_of(cc) * 2));
+                    mo = mlc.x;
+                    lo = mlc.y;
+                  }
+                  if (M > -INFINITY) L += lo * ex2(mo - M);
+                }
+                const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll 1
+                for (int q = 0; q < D / 32; ++q) {
+                  float v[32];
+#pragma unroll
+                  for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                  for (int cc = c_a; cc <= c_b; ++cc) {
+                    if (cc == rank) {
+                      uint32_t raw[32];
+                      tmem_ld32(tO + q * 32, raw);
+                      tmem_wait_ld();
+                      const float f = (M == -INFINITY) ? 0.f : ex2(m_used - M);
+#pragma unroll
+                      for (int e = 0; e < 32; ++e) v[e] += __uint_as_float(raw[e]) * f;
+                    } else {
+                      const size_t sl = slot_of(cc);
+                      const float mo = __ldcg(work.part_ml + sl * 2);
+                      const float f = (M == -INFINITY) ? 0.f : ex2(mo - M);
+                      const float* pc = work.part_o + sl * D + q * 32;
+#pragma unroll
+                      for (int c = 0; c < 32; c += 4) {
+                        const float4 w4 = __ldcg(reinterpret_cast<const float4*>(pc + c));
+                        v[c] += w4.x * f; v[c + 1] += w4.y * f; v[c + 2] += w4.z * f; v[c + 3] += w4.w * f;
+                      }
+                    }
+                  }
+                  store_chunk(q, v, inv);
+                }
               }
               if (lane == 0) *counter = 0;  // ready for the next call
             }

@@ -4,12 +4,13 @@
 // reuses the RoPE index of data token D_k.  Fresh prompt row i sits at
 // position C + i, tail row r at P + (r mod B).
 //
-// One CTA handles ROWS consecutive rows.  The (cos, sin) pair of each
-// (row, frequency) is computed once into shared memory -- angle formed and
-// reduced modulo 2*pi in fp64, since positions reach 10^4 radians and fp32
-// would lose ~1e-3 rad -- then every head of Q and K of those rows is
-// rotated with 16-byte vector accesses.  HBM-bound: each element is read
-// and written once.
+// One CTA handles ROWS consecutive rows.  Their first elements are loaded
+// at entry, together with the sequence table, so that the one DRAM round
+// trip covers both.  The (cos, sin) pair of each (row, frequency) is then
+// computed once into shared memory -- angle formed and reduced modulo 2*pi
+// in fp64, since positions reach 10^4 radians and fp32 would lose ~1e-3
+// rad -- and every head of Q and K of those rows is rotated with 16-byte
+// vector accesses.  HBM-bound: each element is read and written once.
 #include "ssv_internal.cuh"
 
 #include <math.h>
@@ -28,8 +29,7 @@ template <> struct Vec16<float> { static constexpr int N = 4; };
 template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
 
 template <typename T>
-__device__ __forceinline__ void load16(const T* p, float* out) {
-  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ void unpack16(const uint4 raw, float* out) {
   if constexpr (sizeof(T) == 4) {
     out[0] = __uint_as_float(raw.x); out[1] = __uint_as_float(raw.y);
     out[2] = __uint_as_float(raw.z); out[3] = __uint_as_float(raw.w);
@@ -41,6 +41,11 @@ __device__ __forceinline__ void load16(const T* p, float* out) {
       out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
+}
+
+template <typename T>
+__device__ __forceinline__ void load16(const T* p, float* out) {
+  unpack16<T>(*reinterpret_cast<const uint4*>(p), out);
 }
 
 template <typename T>
@@ -70,21 +75,66 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   constexpr int HALF = D / 2;
   constexpr int VEC = Vec16<T>::N;
   constexpr int CHUNKS = HALF / VEC;
+  constexpr int PRE = 4;  // items per thread loaded before the positions are known
   __shared__ float s_cos[kRopeRows][HALF];
   __shared__ float s_sin[kRopeRows][HALF];
   __shared__ int s_pos[kRopeRows];
+  __shared__ ssv_seq s_seq[kRopeThreads];
 
   const int row0 = blockIdx.x * kRopeRows;
+  const int heads = Hq + Hkv;
+  const int items = kRopeRows * heads * CHUNKS;
+  auto item_ptrs = [&](int it, const T*& src, T*& dst, int& lr, int& ch) -> bool {
+    ch = it % CHUNKS;
+    const int hh = (it / CHUNKS) % heads;
+    lr = it / (CHUNKS * heads);
+    const int row = row0 + lr;
+    if (row >= total_rows) return false;
+    if (hh < Hq) {
+      src = q_in + ((size_t)row * Hq + hh) * D;
+      dst = q_out + ((size_t)row * Hq + hh) * D;
+    } else {
+      src = k_in + ((size_t)row * Hkv + (hh - Hq)) * D;
+      dst = k_out + ((size_t)row * Hkv + (hh - Hq)) * D;
+    }
+    return true;
+  };
+  // The rows' data does not depend on the positions: issue those loads first,
+  // together with the sequence table (one round trip for both).
+  uint4 pr1[PRE], pr2[PRE];  // kept packed until the angles are known
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int it = threadIdx.x + k * kRopeThreads;
+    const T* src;
+    T* dst;
+    int lr, ch;
+    if (it < items && item_ptrs(it, src, dst, lr, ch)) {
+      pr1[k] = *reinterpret_cast<const uint4*>(src + ch * VEC);
+      pr2[k] = *reinterpret_cast<const uint4*>(src + HALF + ch * VEC);
+    }
+  }
+  const bool table = batch <= kRopeThreads;
+  if (table && threadIdx.x < batch) s_seq[threadIdx.x] = seqs[threadIdx.x];
+  __syncthreads();
   if (threadIdx.x < kRopeRows) {
     const int row = row0 + threadIdx.x;
     int pos = -1;
     if (row < total_rows) {
-      const int b = find_seq_by_row(seqs, batch, row);
+      int b = -1;
+      if (table) {
+        int lo = 0, hi = batch - 1;
+        while (lo <= hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s_seq[mid].q_off <= row) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+        }
+      } else {
+        b = find_seq_by_row(seqs, batch, row);
+      }
       if (b >= 0) {
-        const ssv_seq s = seqs[b];
-        const int i = row - s.q_off;
-        if (i < s.new_len) pos = s.cache_len + i;
-        else if (i < s.new_len + 2 * s.block) pos = s.cache_len + s.new_len + (i - s.new_len) % s.block;
+        const ssv_seq sq = table ? s_seq[b] : seqs[b];
+        const int i = row - sq.q_off;
+        if (i < sq.new_len) pos = sq.cache_len + i;
+        else if (i < sq.new_len + 2 * sq.block) pos = sq.cache_len + sq.new_len + (i - sq.new_len) % sq.block;
       }
     }
     s_pos[threadIdx.x] = pos;
@@ -107,26 +157,8 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   }
   __syncthreads();
 
-  const int heads = Hq + Hkv;
-  const int items = kRopeRows * heads * CHUNKS;
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int ch = it % CHUNKS;
-    const int hh = (it / CHUNKS) % heads;
-    const int lr = it / (CHUNKS * heads);
-    const int row = row0 + lr;
-    if (s_pos[lr] < 0) continue;
-    const T* src;
-    T* dst;
-    if (hh < Hq) {
-      src = q_in + ((size_t)row * Hq + hh) * D;
-      dst = q_out + ((size_t)row * Hq + hh) * D;
-    } else {
-      src = k_in + ((size_t)row * Hkv + (hh - Hq)) * D;
-      dst = k_out + ((size_t)row * Hkv + (hh - Hq)) * D;
-    }
-    float x1[VEC], x2[VEC], y1[VEC], y2[VEC];
-    load16<T>(src + ch * VEC, x1);
-    load16<T>(src + HALF + ch * VEC, x2);
+  auto rotate = [&](int lr, int ch, const float* x1, const float* x2, T* dst) {
+    float y1[VEC], y2[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
       const float c = s_cos[lr][ch * VEC + v], s = s_sin[lr][ch * VEC + v];
@@ -135,6 +167,29 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
     }
     store16<T>(dst + ch * VEC, y1);
     store16<T>(dst + HALF + ch * VEC, y2);
+  };
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int it = threadIdx.x + k * kRopeThreads;
+    const T* src;
+    T* dst;
+    int lr, ch;
+    if (it < items && item_ptrs(it, src, dst, lr, ch) && s_pos[lr] >= 0) {
+      float x1[VEC], x2[VEC];
+      unpack16<T>(pr1[k], x1);
+      unpack16<T>(pr2[k], x2);
+      rotate(lr, ch, x1, x2, dst);
+    }
+  }
+  for (int it = threadIdx.x + PRE * kRopeThreads; it < items; it += blockDim.x) {
+    const T* src;
+    T* dst;
+    int lr, ch;
+    if (!item_ptrs(it, src, dst, lr, ch) || s_pos[lr] < 0) continue;
+    float x1[VEC], x2[VEC];
+    load16<T>(src + ch * VEC, x1);
+    load16<T>(src + HALF + ch * VEC, x2);
+    rotate(lr, ch, x1, x2, dst);
   }
 }
 
