@@ -367,15 +367,23 @@ def run_ours(args):
                 raise ssv.SsvError(r, "ssv_accept")
 
     OPS = (op_rope, op_attn, op_accept)
+    rargs = ssv.rope_args(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko)
+
+    def op_step(s):
+        """The whole step in one call (ssv_verify_step: the three kernels chained
+        with programmatic dependent launch)."""
+        ssv.verify_step(rargs, aargs, ws_attn, cargs if acc is not None else None,
+                        ws_acc if acc is not None else None, stream=s)
 
     def step(evs=None, s=None):
         s = stream if s is None else s
+        if not evs:
+            op_step(s)
+            return
         for j, op in enumerate(OPS):
-            if evs:
-                evs[j].record(s)
+            evs[j].record(s)
             op(s)
-        if evs:
-            evs[3].record(s)
+        evs[3].record(s)
 
     for _ in range(args.warmup):
         l2_flush()
@@ -385,11 +393,13 @@ def run_ours(args):
 
     # Timed region.  Default: each sequence of K steps is captured once into a
     # CUDA graph and replayed as one launch, timed by two events around the
-    # replay.  Graphs: K x [flush, rope, attn, accept] (the step), K x [flush],
-    # and K x [flush, op] per op; step and op times are the differences with
-    # the flush-only graph, divided by K.  No event sits between the kernels,
-    # and host launch latency never leaves the GPU idle inside a measurement.
-    # --eager: one call at a time with events between the ops.
+    # replay.  Graphs: K x [flush, ssv_verify_step] (the step: rotation,
+    # attention and acceptance chained by programmatic dependent launch),
+    # K x [flush], and K x [flush, op] per op (each op alone); step and op
+    # times are the differences with the flush-only graph, divided by K.  No
+    # event sits between the kernels, and host launch latency never leaves
+    # the GPU idle inside a measurement.  --eager: the three calls one at a
+    # time, with events between them.
     launch = "eager" if args.eager else "cuda_graph"
 
     def capture(bodies):
@@ -406,7 +416,7 @@ def run_ours(args):
 
     graphs = None
     if launch == "cuda_graph":
-        graphs = {"step": capture(OPS), "flush": capture(()), "rope": capture((op_rope,)),
+        graphs = {"step": capture((op_step,)), "flush": capture(()), "rope": capture((op_rope,)),
                   "verify_attn": capture((op_attn,))}
         if acc is not None:
             graphs["accept"] = capture((op_accept,))

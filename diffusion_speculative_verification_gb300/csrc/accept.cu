@@ -484,6 +484,7 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   p.n_out = a->n_out;
   p.tokens = a->tokens;
   p.dev_status = a->dev_status;
+  p.early = 0;
   p.cnt_seq = reinterpret_cast<int32_t*>(w + L.cnt_seq);
   p.cnt_sample = reinterpret_cast<int32_t*>(w + L.cnt_sample);
   p.cnt_row = reinterpret_cast<int32_t*>(w + L.cnt_row);
@@ -507,17 +508,36 @@ extern "C" ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* byt
   return SSV_OK;
 }
 
-extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_bytes, void* stream) {
+namespace ssv {
+
+ssv_status accept_validate(const ssv_accept_args* a, void* ws, size_t ws_bytes) {
   int nchunks = 0;
   const ssv_status st = accept_check(a, &nchunks);
   if (st != SSV_OK) return st;
   if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
   const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
+  return SSV_OK;
+}
+
+ssv_status accept_run(const ssv_accept_args* a, void* ws, size_t ws_bytes, cudaStream_t s, int early) {
+  const ssv_status st = accept_validate(a, ws, ws_bytes);
+  if (st != SSV_OK) return st;
+  if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
+  int nchunks = 0;
+  accept_check(a, &nchunks);
+  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
   AcceptParams p;
   const int mode = fill_params(a, static_cast<char*>(ws), L, nchunks, &p);
-  const cudaError_t e = launch_accept(p, mode, a->logits_dtype == SSV_BF16, static_cast<cudaStream_t>(stream));
+  p.early = early;
+  const cudaError_t e = launch_accept(p, mode, a->logits_dtype == SSV_BF16, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
+}
+
+}  // namespace ssv
+
+extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_bytes, void* stream) {
+  return ssv::accept_run(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -71,6 +71,10 @@ struct AcceptParams {
   int32_t* n_out;
   int32_t* tokens;
   int32_t* dev_status;
+  // 1: the kernel before this one on the stream is the step's attention
+  // kernel, whose outputs overlap none of the batch metadata; the metadata
+  // may then be read before it completes (programmatic dependent launch).
+  int early;
   // workspace carve-up (the three counter arrays come first and are contiguous)
   int32_t* cnt_seq;     // [batch]        merged rows of the sequence
   int32_t* cnt_sample;  // [batch]        emission-row chunks done

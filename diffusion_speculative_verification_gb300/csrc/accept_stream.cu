@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ StrShared sh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (!p.early) pdl_wait();  // any input may come from the preceding kernel
 
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -219,32 +220,44 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   const long long u0 = U * blockIdx.x / gridDim.x;
   const int n = (int)(U * (blockIdx.x + 1) / gridDim.x - u0);
 
+  // Rows of a unit: the logits chunk and, where the rule needs it, the draft
+  // logits or noise chunk (bytes multiples of 16 by construction).
+  auto unit_rows = [&](int k, const void*& a, uint32_t& bytes_a, const void*& b, uint32_t& bytes_b) {
+    const long long u = u0 + k;
+    const int e = sh.list[u / p.nchunks];
+    const int slot = e & 0x7fffffff;
+    const int c0 = (int)(u % p.nchunks) * kAccChunk;
+    const int nvalid = min(kAccChunk, p.V - c0);
+    a = static_cast<const T*>(p.logits) + (size_t)slot * p.V + c0;
+    bytes_a = (uint32_t)nvalid * (uint32_t)sizeof(T);
+    b = nullptr;
+    bytes_b = 0;
+    if (MODE == SSV_ACCEPT_REJECT && e < 0) {
+      b = static_cast<const T*>(p.draft_logits) + (size_t)slot * p.V + c0;
+      bytes_b = bytes_a;
+    } else if (MODE == SSV_ACCEPT_GUMBEL) {
+      b = p.noise + (size_t)p.noise_row[slot] * p.V + c0;
+      bytes_b = (uint32_t)nvalid * 4u;
+    }
+  };
+  // The list used only the batch metadata; logits, draft logits, noise and
+  // the workspace are read only once the preceding kernel has completed.
+  pdl_wait();
+  pdl_trigger();
+
   if (warp == kStrProducerWarp) {
     if (lane != 0) return;
     int issued = 0;
     for (int k = 0; k < n; ++k) {
       const int s = k % C::kStages;
       if (k >= C::kStages && !mbar_wait(smem_u32(&sh.empty[s]), ((k / C::kStages) - 1) & 1, &sh.abort)) break;
-      const long long u = u0 + k;
-      const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
-      const int e = sh.list[row];
-      const int slot = e & 0x7fffffff;
-      const int c0 = chunk * kAccChunk;
-      const int nvalid = min(kAccChunk, p.V - c0);
-      const uint32_t bytes_a = (uint32_t)nvalid * (uint32_t)sizeof(T);
-      uint32_t bytes_b = 0;
-      const void* src_b = nullptr;
-      if (MODE == SSV_ACCEPT_REJECT && e < 0) {
-        bytes_b = bytes_a;
-        src_b = static_cast<const T*>(p.draft_logits) + (size_t)slot * p.V + c0;
-      } else if (MODE == SSV_ACCEPT_GUMBEL) {
-        bytes_b = (uint32_t)nvalid * 4u;
-        src_b = p.noise + (size_t)p.noise_row[slot] * p.V + c0;
-      }
+      const void *src_a, *src_b;
+      uint32_t bytes_a, bytes_b;
+      unit_rows(k, src_a, bytes_a, src_b, bytes_b);
       const uint32_t dst = smem_u32(ring + (size_t)s * C::kStage);
       const uint32_t fb = smem_u32(&sh.full[s]);
       mbar_expect_tx(fb, bytes_a + bytes_b);
-      bulk_load(dst, static_cast<const T*>(p.logits) + (size_t)slot * p.V + c0, bytes_a, fb);
+      bulk_load(dst, src_a, bytes_a, fb);
       if (bytes_b) bulk_load(dst + C::kRowB, src_b, bytes_b, fb);
       issued = k + 1;
     }
@@ -420,8 +433,7 @@ cudaError_t launch_t(const AcceptParams& p, cudaStream_t st) {
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(units < sms ? units : sms);
-  accept_stream_kernel<MODE, T><<<grid, kStrThreads, C::kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(accept_stream_kernel<MODE, T>, dim3(grid), dim3(kStrThreads), C::kSmem, st, p);
 }
 
 }  // namespace

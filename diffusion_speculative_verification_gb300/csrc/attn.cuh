@@ -22,6 +22,10 @@ struct AttnParams {
   int total_rows, total_cache, total_slots;
   int max_cache, max_new, max_block;
   int32_t* dev_status;
+  // 1: the kernel before this one on the stream is the step's rotation kernel,
+  // whose outputs overlap none of seqs, tau and the KV cache; those may then
+  // be read before that kernel completes (programmatic dependent launch).
+  int early;
 };
 
 cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);

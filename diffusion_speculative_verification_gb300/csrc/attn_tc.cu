@@ -61,6 +61,7 @@ constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzle atom c
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr int kMergeBlocks = 8;                  // key blocks a partial merge costs, roughly
 
 enum : uint32_t {
   B_Q_FULL = 0,
@@ -89,6 +90,8 @@ struct Cfg {
   static constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 };
 static_assert(8 * B_COUNT + 8 + 8 * 4 <= 256, "barrier area overflow");
+constexpr size_t kMaxSmemPerCta = 227 * 1024;  // opt-in limit per CTA on sm_100-family parts
+static_assert(Cfg<2>::SM_ALLOC <= kMaxSmemPerCta, "pipeline buffers exceed shared memory");
 
 struct TcMaps {
   CUtensorMap q, kc, vc, kn, vn;
@@ -145,7 +148,7 @@ __device__ __forceinline__ uint32_t window32(uint32_t w0, uint32_t w1, uint32_t 
 
 template <int MT, typename OutT>
 __global__ void __launch_bounds__(Cfg<MT>::kThreads, 1)
-attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const TcWork work, int G) {
+attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const TcWork work, int G, int plan_smem) {
   using C_ = Cfg<MT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -153,8 +156,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::SM_BAR + 8 * B_COUNT);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C_::SM_BAR + 8 * B_COUNT + 4);
   PlanHdr* plan = reinterpret_cast<PlanHdr*>(smem + C_::SM_BAR + 8 * B_COUNT + 8);
-  // planning tables of this CTA (global workspace, visible to the CTA after __syncthreads)
-  int* s_prefU = work.plan + (size_t)blockIdx.x * 4 * (p.batch + 1);
+  // planning tables of this CTA: shared memory when they fit, else the global
+  // workspace (visible to the CTA after __syncthreads)
+  int* s_prefU = plan_smem ? reinterpret_cast<int*>(smem + C_::SM_TOTAL)
+                           : work.plan + (size_t)blockIdx.x * 4 * (p.batch + 1);
   int* s_prefB = s_prefU + (p.batch + 1);
   int* s_bgblk = s_prefB + (p.batch + 1);
   int* s_ntile = s_bgblk + (p.batch + 1);
@@ -172,6 +177,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   // head has identical work, so CTAs of different heads stay at the same token offsets and
   // read the heads of a token (adjacent in memory) together.  Tables are per head.
   if (warp == 0) {
+    // Before the preceding kernel completes, only an early launch (its outputs
+    // do not overlap seqs, tau or the KV cache) with the plan in shared memory
+    // may read inputs; otherwise wait here (the barrier below orders the rest).
+    if (!(p.early && plan_smem)) pdl_wait();
     int carryU = 0, carryB = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
       const int b = b0 + lane;
@@ -217,8 +226,15 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       h.U = carryU;  // units per head
       // CTAs per head: with no more units than CTAs, the same whole number per unit (each
       // CTA owns an equal piece of one unit); otherwise an even split of the head's blocks.
+      // A unit is split only when the blocks it saves outweigh the partial merge, which
+      // costs about kMergeBlocks key blocks of time.
       const int cap = max(P / p.Hkv, 1);
-      int ph = (carryU > 0 && carryU <= cap) ? carryU * (cap / carryU) : cap;
+      int ph = cap;
+      if (carryU > 0 && carryU <= cap) {
+        const int f = cap / carryU;  // CTAs per unit if split
+        const long long saved = (long long)carryB * (f - 1) / ((long long)f * carryU);  // blocks saved per unit
+        ph = (f > 1 && saved > kMergeBlocks) ? carryU * f : carryU;
+      }
       ph = min(ph, max(carryB, 1));
       h.Pe = ph;
       h.g = cta % p.Hkv;
@@ -261,6 +277,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Dependents may launch once every kernel before this one has completed,
+  // or (early launch) once the step's rotation kernel, which waited for its
+  // own predecessor before letting this one start, is the only one running.
+  pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   const int begin = plan->begin, end = plan->end, W = plan->W, Ph = plan->Pe, Uh = plan->U;
   const int gh = plan->g;           // kv head served by this CTA
@@ -332,11 +352,33 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         ++vn;
         return true;
       };
+      // Q, K_new and V_new may come from the preceding kernel (the rotation):
+      // they are loaded only after pdl_wait().  On an early launch KV-cache
+      // blocks are not.
+      bool waited = !(p.early && plan_smem);
+      auto dep_wait = [&]() {
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+        }
+      };
       while (run && remaining > 0) {
         const Unit x = decode(u);
         const int len = min(x.nblocks - k, remaining);
+        int jk = k, jv = k;  // next key / value block of the segment to load
+        if (!waited) {
+          // first segment: fill the rings with cache blocks while the preceding kernel runs
+          while (jk < k + len && jk < x.cache_blocks && jk - k < NSK) {
+            if (!load_k(x, jk++)) { run = false; break; }
+          }
+          while (run && jv + 1 < jk && jv - k < NSV) {
+            if (!load_v(x, jv++)) { run = false; break; }
+          }
+          if (!run) break;
+        }
+        dep_wait();
         // the first key block does not depend on Q: start it before waiting for the Q buffer
-        if (!load_k(x, k)) break;
+        if (jk == k && !load_k(x, jk++)) break;
         if (seg > 0 && !mbar_wait(bar(B_Q_EMPTY), (seg - 1) & 1, abort)) break;
         mbar_expect_tx(bar(B_Q_FULL), x.mc * TILE_BYTES);
         for (int mt = 0; mt < x.mc; ++mt) {
@@ -346,14 +388,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         }
         ++seg;
         // keys run one block ahead of values
-        for (int j = k + 1; j < k + len; ++j) {
-          if (!load_k(x, j) || !load_v(x, j - 1)) { run = false; break; }
+        while (jk < k + len || jv < k + len) {
+          if (jk < k + len && !load_k(x, jk++)) { run = false; break; }
+          if (jv < k + len && (jv + 1 < jk || jk == k + len) && !load_v(x, jv++)) { run = false; break; }
         }
-        if (!run || !load_v(x, k + len - 1)) break;
+        if (!run) break;
         remaining -= len;
         ++u;
         k = 0;
       }
+      if (!waited) pdl_wait();
       // drain (bounded, regardless of abort): the last Q load and the last K / V loads
       if (seg > 0) {
         const long long t0 = clock64();
@@ -709,7 +753,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
         }
         if (!run) break;
-        // ---- segment epilogue: O stays in TMEM until O_FREE is signalled
+        // ---- segment epilogue: O stays in TMEM until O_FREE is signalled.
+        // Every PV of the segment must be complete.  With S double-buffered the
+        // last two PVs can both be outstanding here, two barrier phases apart;
+        // a parity wait only tells adjacent phases apart, so wait for them in order.
+        if (MT == 1 && nblk >= 2 && !warp_wait(bar(B_PV_DONE + mt), (nblk - 2) & 1)) { run = false; break; }
         if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
         if (warp_active) {
           tc_fence_after();
@@ -734,9 +782,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               }
             }
           };
+          // (one-shot code: loops stay rolled, the instructions arrive cold)
           if (complete) {
             const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
               uint32_t raw[32];
               tmem_ld32(tO + q * 32, raw);
@@ -752,7 +801,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             const int which = (seg == 0) ? 0 : 1;
             const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
             __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
               uint32_t raw[32];
               tmem_ld32(tO + q * 32, raw);
@@ -900,6 +949,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   tc_fence_before();
   __syncthreads();
   if (*abort && threadIdx.x == 0) report(p.dev_status, SSV_ERR_TIMEOUT);
+  if (threadIdx.x == 32) pdl_wait();  // this grid never completes before the one it follows
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -991,6 +1041,15 @@ bool attn_tc_supported(const AttnParams& p) {
 
 size_t attn_tc_workspace(const AttnParams& p) { return ws_layout(p).total; }
 
+// Shared memory of a launch: the pipeline buffers, plus the planning tables
+// (4 x (batch + 1) ints) when they fit under the per-CTA limit.
+static size_t plan_table_bytes(const AttnParams& p) { return sizeof(int32_t) * 4 * (size_t)(p.batch + 1); }
+
+template <int MT>
+static bool plan_in_smem(const AttnParams& p) {
+  return Cfg<MT>::SM_ALLOC + plan_table_bytes(p) <= kMaxSmemPerCta;
+}
+
 template <int MT, typename OutT>
 static cudaError_t launch_t(const AttnParams& p, const TcMaps& maps, const TcWork& w, int G, int grid,
                             cudaStream_t st) {
@@ -998,11 +1057,12 @@ static cudaError_t launch_t(const AttnParams& p, const TcMaps& maps, const TcWor
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(attn_tc_kernel<MT, OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<MT>::SM_ALLOC);
+                                    (int)kMaxSmemPerCta);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  attn_tc_kernel<MT, OutT><<<grid, Cfg<MT>::kThreads, Cfg<MT>::SM_ALLOC, st>>>(maps, p, w, G);
-  return cudaGetLastError();
+  const int in_smem = plan_in_smem<MT>(p) ? 1 : 0;
+  const size_t smem = Cfg<MT>::SM_ALLOC + (in_smem ? plan_table_bytes(p) : 0);
+  return launch_pdl(attn_tc_kernel<MT, OutT>, dim3(grid), dim3(Cfg<MT>::kThreads), smem, st, maps, p, w, G, in_smem);
 }
 
 cudaError_t launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t st) {

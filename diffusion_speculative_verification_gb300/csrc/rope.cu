@@ -81,6 +81,8 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   __shared__ int s_pos[kRopeRows];
   __shared__ ssv_seq s_seq[kRopeThreads];
 
+  pdl_wait();  // Q and K come from the preceding kernel
+  pdl_trigger();  // dependents start only once every kernel before this one is complete
   const int row0 = blockIdx.x * kRopeRows;
   const int heads = Hq + Hkv;
   const int items = kRopeRows * heads * CHUNKS;
@@ -196,16 +198,15 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
 template <typename T, int D>
 static cudaError_t launch_rope(const ssv_rope_args* a, const RopeTheta& th, cudaStream_t st) {
   const int grid = (a->total_rows + kRopeRows - 1) / kRopeRows;
-  rope_copy_kernel<T, D><<<grid, kRopeThreads, 0, st>>>(
-      static_cast<const T*>(a->q_in), static_cast<const T*>(a->k_in), static_cast<T*>(a->q_out),
-      static_cast<T*>(a->k_out), a->Hq, a->Hkv, a->seqs, a->batch, a->total_rows, th);
-  return cudaGetLastError();
+  return launch_pdl(rope_copy_kernel<T, D>, dim3(grid), dim3(kRopeThreads), 0, st,
+                    static_cast<const T*>(a->q_in), static_cast<const T*>(a->k_in), static_cast<T*>(a->q_out),
+                    static_cast<T*>(a->k_out), a->Hq, a->Hkv, a->seqs, a->batch, a->total_rows, th);
 }
 
 }  // namespace ssv
 
-extern "C" ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream) {
-  using namespace ssv;
+namespace ssv {
+ssv_status rope_validate(const ssv_rope_args* a) {
   if (!a) return SSV_ERR_INVALID;
   if (a->total_rows < 0 || a->batch < 0 || a->Hq <= 0 || a->Hkv <= 0) return SSV_ERR_INVALID;
   if (a->total_rows == 0 || a->batch == 0) return SSV_OK;
@@ -215,6 +216,15 @@ extern "C" ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream) {
   if (!(a->base > 1.0) || !isfinite(a->base)) return SSV_ERR_INVALID;
   const uintptr_t al = (uintptr_t)a->q_in | (uintptr_t)a->k_in | (uintptr_t)a->q_out | (uintptr_t)a->k_out;
   if (al & 15u) return SSV_ERR_INVALID;
+  return SSV_OK;
+}
+}  // namespace ssv
+
+extern "C" ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream) {
+  using namespace ssv;
+  const ssv_status v = rope_validate(a);
+  if (v != SSV_OK) return v;
+  if (a->total_rows == 0 || a->batch == 0) return SSV_OK;
   RopeTheta th;
   for (int i = 0; i < 64; ++i) th.theta[i] = (i < a->d / 2) ? pow(a->base, -2.0 * i / a->d) : 0.0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

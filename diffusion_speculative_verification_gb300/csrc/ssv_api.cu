@@ -53,6 +53,7 @@ AttnParams to_params(const ssv_attn_args* a) {
   p.max_new = a->max_new;
   p.max_block = a->max_block;
   p.dev_status = a->dev_status;
+  p.early = 0;
   return p;
 }
 
@@ -70,17 +71,84 @@ extern "C" ssv_status ssv_verify_attn_workspace(const ssv_attn_args* a, size_t* 
   return SSV_OK;
 }
 
-extern "C" ssv_status ssv_verify_attn(const ssv_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+ssv_status attn_validate(const ssv_attn_args* a, void* ws, size_t ws_bytes) {
   const ssv_status st = attn_check(a);
   if (st != SSV_OK) return st;
   if (a->batch == 0 || a->total_rows == 0) return SSV_OK;
   size_t need = 0;
   ssv_verify_attn_workspace(a, &need);
   if (need > 0 && (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need)) return SSV_ERR_WORKSPACE;
-  const AttnParams p = to_params(a);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return SSV_OK;
+}
+
+ssv_status attn_run(const ssv_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t s, int early) {
+  const ssv_status st = attn_validate(a, ws, ws_bytes);
+  if (st != SSV_OK) return st;
+  if (a->batch == 0 || a->total_rows == 0) return SSV_OK;
+  AttnParams p = to_params(a);
+  p.early = early;
   const cudaError_t e = tc::attn_tc_supported(p) ? tc::launch_attn_tc(p, ws, s) : launch_attn_simt(p, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
+}
+
+// byte ranges [a, a + na) and [b, b + nb) intersect
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+size_t esize(ssv_dtype t) { return t == SSV_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" ssv_status ssv_verify_attn(const ssv_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+  return attn_run(a, ws, ws_bytes, static_cast<cudaStream_t>(stream), 0);
+}
+
+extern "C" ssv_status ssv_verify_step(const ssv_rope_args* rope, const ssv_attn_args* attn, void* attn_ws,
+                                      size_t attn_ws_bytes, const ssv_accept_args* acc, void* acc_ws,
+                                      size_t acc_ws_bytes, void* stream) {
+  if (!attn) return SSV_ERR_INVALID;
+  ssv_status st;
+  if (rope && (st = rope_validate(rope)) != SSV_OK) return st;
+  if ((st = attn_validate(attn, attn_ws, attn_ws_bytes)) != SSV_OK) return st;
+  if (acc && (st = accept_validate(acc, acc_ws, acc_ws_bytes)) != SSV_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // What each kernel may read before its predecessor completes, and what the
+  // predecessors write.
+  size_t rq = 0, rk = 0;
+  if (rope) {
+    const size_t e = rope->dtype == SSV_BF16 ? 2 : 4;
+    rq = (size_t)rope->total_rows * rope->Hq * rope->d * e;
+    rk = (size_t)rope->total_rows * rope->Hkv * rope->d * e;
+  }
+  auto written_by_rope = [&](const void* p, size_t n) {
+    return rope && (overlap(rope->q_out, rq, p, n) || overlap(rope->k_out, rk, p, n));
+  };
+  const size_t cache_bytes = (size_t)attn->total_cache * attn->Hkv * attn->d * esize(attn->in_dtype);
+  const int early_attn =
+      rope && !written_by_rope(attn->seqs, sizeof(ssv_seq) * (size_t)attn->batch) &&
+      !written_by_rope(attn->tau, sizeof(int32_t) * (size_t)attn->total_slots) &&
+      !written_by_rope(attn->k_cache, cache_bytes) && !written_by_rope(attn->v_cache, cache_bytes);
+  int early_acc = 0;
+  if (acc) {
+    const size_t ob = (size_t)attn->total_rows * attn->Hq * attn->d * esize(attn->out_dtype);
+    const void* meta[5] = {acc->tau, acc->block, acc->gamma, acc->slot_off, acc->noise_row};
+    const size_t mb[5] = {4 * (size_t)acc->total_slots, 4 * (size_t)acc->batch, 4 * (size_t)acc->batch,
+                          4 * (size_t)acc->batch, acc->noise_row ? 4 * (size_t)acc->total_slots : 0};
+    early_acc = 1;
+    for (int i = 0; i < 5; ++i)
+      if (written_by_rope(meta[i], mb[i]) || overlap(attn->o, ob, meta[i], mb[i]) ||
+          overlap(attn_ws, attn_ws_bytes, meta[i], mb[i]))
+        early_acc = 0;
+  }
+  if (rope && (st = ssv_rope_copy(rope, stream)) != SSV_OK) return st;
+  if ((st = attn_run(attn, attn_ws, attn_ws_bytes, s, early_attn)) != SSV_OK) return st;
+  if (acc && (st = accept_run(acc, acc_ws, acc_ws_bytes, s, early_acc)) != SSV_OK) return st;
+  return SSV_OK;
 }
 
 extern "C" ssv_status ssv_get_status(int32_t* dev_status, void* stream) {

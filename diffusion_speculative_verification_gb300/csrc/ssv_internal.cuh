@@ -84,6 +84,46 @@ __device__ __forceinline__ bool warp_tau_is_permutation(const int32_t* tau, int 
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// host-side pieces shared by the entry points (validation, launches with the
+// early-read flag of programmatic dependent launch)
+ssv_status rope_validate(const ssv_rope_args* a);
+ssv_status accept_validate(const ssv_accept_args* a, void* ws, size_t ws_bytes);
+ssv_status accept_run(const ssv_accept_args* a, void* ws, size_t ws_bytes, cudaStream_t s, int early);
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch (PDL)
+//
+// The kernels of the verification step are launched with programmatic
+// stream serialisation: a kernel may start while the kernel before it on
+// the stream is still running.  pdl_wait() waits for that kernel to
+// complete with its memory visible; a kernel reads no input and writes no
+// workspace before it, except on an "early" launch inside ssv_verify_step,
+// where the host has checked that the preceding kernel of the step writes
+// none of the inputs read early.  pdl_trigger() lets the next kernel launch;
+// each kernel triggers only once every kernel before it has completed, or on
+// an early launch once the step's own predecessor is the only one running,
+// so that early reads never overlap work from before the step.  Without the
+// launch attribute both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace ssv
 
 #define SSV_CUDA_CHECK(expr)                                   \

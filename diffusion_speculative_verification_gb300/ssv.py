@@ -22,7 +22,7 @@ SSV_F32, SSV_BF16 = 0, 1
 ARGMAX, GUMBEL, REJECT = 0, 1, 2
 
 #: every symbol include/ssv.h declares
-EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
+EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
            "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
 
 
@@ -79,13 +79,15 @@ def lib():
         L.ssv_accept_workspace.argtypes = [C.POINTER(AcceptArgs), C.POINTER(sz)]
         L.ssv_accept.argtypes = [C.POINTER(AcceptArgs), vp, sz, vp]
         L.ssv_accept_noalloc.argtypes = [C.POINTER(AcceptArgs), vp]
+        L.ssv_verify_step.argtypes = [C.POINTER(RopeArgs), C.POINTER(AttnArgs), vp, sz, C.POINTER(AcceptArgs), vp,
+                                      sz, vp]
         L.ssv_get_status.argtypes = [vp, vp]
         L.ssv_status_string.argtypes = [C.c_int]
         L.ssv_status_string.restype = C.c_char_p
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
-        for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_accept_workspace",
-                     "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_bench"):
+        for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step",
+                     "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_bench"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -165,14 +167,31 @@ def _workspace(nbytes: int, device, ws=None):
 # ---------------------------------------------------------------------------
 # entry points
 # ---------------------------------------------------------------------------
-def rope_copy(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, stream=None):
-    """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d]; returns (q_out, k_out)."""
+def rope_args(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None):
     q_out = q if q_out is None else q_out
     k_out = k if k_out is None else k_out
-    a = RopeArgs(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _dtype_code(q), q.shape[1], k.shape[1], q.shape[2],
-                 float(base), _ptr(batch.dev), batch.batch, q.shape[0])
+    return RopeArgs(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _dtype_code(q), q.shape[1], k.shape[1], q.shape[2],
+                    float(base), _ptr(batch.dev), batch.batch, q.shape[0])
+
+
+def rope_copy(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, stream=None):
+    """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d]; returns (q_out, k_out)."""
+    a = rope_args(q, k, batch, base, q_out, k_out)
     _check(lib().ssv_rope_copy(C.byref(a), _stream_ptr(stream)), "ssv_rope_copy")
-    return q_out, k_out
+    return (q if q_out is None else q_out), (k if k_out is None else k_out)
+
+
+def verify_step(rope: "RopeArgs | None", attn: AttnArgs, attn_workspace, accept: "AcceptArgs | None" = None,
+                accept_workspace=None, stream=None):
+    """ssv_verify_step on prepared argument blocks (see rope_args, attn_args,
+    accept_args): rotation, verification attention and acceptance as one call."""
+    aw = _ptr(attn_workspace)
+    awb = 0 if attn_workspace is None else attn_workspace.numel() * attn_workspace.element_size()
+    cw = _ptr(accept_workspace)
+    cwb = 0 if accept_workspace is None else accept_workspace.numel() * accept_workspace.element_size()
+    _check(lib().ssv_verify_step(None if rope is None else C.byref(rope), C.byref(attn), aw, awb,
+                                 None if accept is None else C.byref(accept), cw, cwb, _stream_ptr(stream)),
+           "ssv_verify_step")
 
 
 def attn_args(q, k_cache, v_cache, k_new, v_new, out, batch: Batch, tau, scale: float = 0.0, dev_status=None):

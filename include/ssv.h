@@ -237,6 +237,32 @@ SSV_API ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes)
 SSV_API ssv_status ssv_accept(const ssv_accept_args* a, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ssv_verify_step -- the whole verification step in one call: ssv_rope_copy
+ * (rope, may be NULL when Q and K_new are already rotated), ssv_verify_attn
+ * (attn), then ssv_accept (acc, may be NULL), in that order on `stream`, with
+ * the same arguments, results and workspaces as the three separate calls.
+ * SimSD summary sections 2-4 (one verification pass: rotation with the
+ * RoPE-copy index, temporal attention, acceptance in temporal order).
+ *
+ * The difference is overlap: each kernel is launched with programmatic
+ * dependent launch and may begin its input-independent set-up while the one
+ * before it finishes.  When the rotation's outputs (rope->q_out, k_out)
+ * overlap none of attn->seqs, tau, k_cache, v_cache, the attention kernel
+ * plans and starts streaming the KV cache before the rotation completes;
+ * when neither the rotation's outputs nor attn->o or the attention
+ * workspace overlap acc->tau, block, gamma, slot_off, noise_row, the
+ * acceptance kernel builds its row list before the attention completes.
+ * Everything else is read only after the preceding kernel has completed.
+ * Kernels that ran before the call must be complete or ordered by the stream
+ * as usual; nothing here relaxes that.
+ * All arguments are validated before anything is launched.
+ * Errors: those of the three calls.
+ * ---------------------------------------------------------------------- */
+SSV_API ssv_status ssv_verify_step(const ssv_rope_args* rope, const ssv_attn_args* attn, void* attn_workspace,
+                                   size_t attn_workspace_bytes, const ssv_accept_args* acc, void* acc_workspace,
+                                   size_t acc_workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * ssv_accept_noalloc -- ssv_accept for callers that cannot allocate.
  * The pages have no counterpart: this is an interface addition of the
  * library.  Some callers have no way to obtain device memory of their own:

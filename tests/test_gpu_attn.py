@@ -40,6 +40,24 @@ def test_attn_small(name, out):
     compare_attn(got, ref, out == "bf16", a.dtype == W.F32)
 
 
+# Units split across CTAs (partials merged by the last-arriving 32-row group):
+# in two (8 units per kv head over 19 CTAs), in three, and across every CTA
+# of a head (one long unit per head: more than four partials).
+SPLIT = {
+    "split2": lambda: W.make_attn_inputs("s", [4096] * 8, [0] * 8, [8] * 8, 16, 8, 128, W.BF16, 41),
+    "split3": lambda: W.make_attn_inputs("s", [3000, 3100, 2900, 3333, 3050], [0] * 5, [4, 8, 2, 16, 4], 8, 8, 128,
+                                         W.BF16, 42),
+    "split_many": lambda: W.make_attn_inputs("s", [8192], [0], [16], 32, 8, 128, W.BF16, 43),
+}
+
+
+@pytest.mark.parametrize("name", list(SPLIT))
+def test_attn_split_units(name):
+    a = SPLIT[name]()
+    got, ref, _ = gpu_verify(a, out_dtype="bf16")
+    compare_attn(got, ref, True, False)
+
+
 @pytest.mark.parametrize("name", ["gqa1p7b", "gqa8b", "sweep"])
 def test_attn_full_decode_shapes(name):
     a = W.workload_attn(name)
