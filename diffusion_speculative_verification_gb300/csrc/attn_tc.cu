@@ -74,7 +74,8 @@ enum : uint32_t {
   B_P_FULL = B_S_FULL + 2,       // + tile
   B_PV_DONE = B_P_FULL + 2,      // + tile
   B_O_FREE = B_PV_DONE + 2,      // + tile
-  B_FINAL = B_O_FREE + 2,
+  B_SEG_DONE = B_O_FREE + 2,     // one-tile path: every PV of a segment complete
+  B_FINAL = B_SEG_DONE + 1,
   B_COUNT = B_FINAL + 1
 };
 
@@ -475,6 +476,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             tc_fence_after();
             gemm_ts_k128(tmem + TM_O, tmem + pbuf * 128, (vn % NSV) ? dv1 : dv0, id_pv, i > 0 ? 1u : 0u);
             mma_commit(bar(B_PV_DONE));
+            if (i + 1 == len) mma_commit(bar(B_SEG_DONE));
             mma_commit(bar(B_V_EMPTY + vn % NSV));
             ++vn;
             ++np_issued;
@@ -754,11 +756,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         }
         if (!run) break;
         // ---- segment epilogue: O stays in TMEM until O_FREE is signalled.
-        // Every PV of the segment must be complete.  With S double-buffered the
-        // last two PVs can both be outstanding here, two barrier phases apart;
-        // a parity wait only tells adjacent phases apart, so wait for them in order.
-        if (MT == 1 && nblk >= 2 && !warp_wait(bar(B_PV_DONE + mt), (nblk - 2) & 1)) { run = false; break; }
-        if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
+        // Every PV of the segment must be complete.  Two tiles: S(j + 1) of a
+        // tile is issued after PV(j), so at most the last PV is pending here and
+        // the per-block barrier's parity is unambiguous.  One tile (S double-
+        // buffered): the last two PVs may be pending, or both done, i.e. two
+        // phases apart, which a parity wait cannot tell apart; the issuer
+        // signals the end of the segment on a barrier of its own instead.
+        if (MT == 1 ? !warp_wait(bar(B_SEG_DONE), seg & 1) : !warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) {
+          run = false;
+          break;
+        }
         if (warp_active) {
           tc_fence_after();
           OutT* orow = static_cast<OutT*>(p.o) + ((size_t)(x.q_off + i) * p.Hq + x.g * G + hj) * D;
