@@ -62,6 +62,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeBlocks = 8;                  // key blocks a partial merge costs, roughly
+constexpr int kSegBlocks = 2;                    // key blocks of time a segment's fixed work takes, roughly
 
 enum : uint32_t {
   B_Q_FULL = 0,
@@ -90,7 +91,6 @@ struct Cfg {
   static constexpr uint32_t SM_TOTAL = SM_BAR + 256;
   static constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 };
-static_assert(8 * B_COUNT + 8 + 8 * 4 <= 256, "barrier area overflow");
 constexpr size_t kMaxSmemPerCta = 227 * 1024;  // opt-in limit per CTA on sm_100-family parts
 static_assert(Cfg<2>::SM_ALLOC <= kMaxSmemPerCta, "pipeline buffers exceed shared memory");
 
@@ -105,9 +105,14 @@ struct TcWork {
   float* part_o;   // [2 * grid][MT][128][128] unnormalised O
 };
 
+// Per head: W key blocks, U units, Pe owning CTAs and Wc = W + kSegBlocks * U
+// cost units; this CTA's head g and its range [begin, end) of the head's
+// blocks, which starts at block k0 of unit u0.
 struct PlanHdr {
-  int W, U, Pe, g, begin, end, u0, k0;  // per head: W blocks, U units, Pe owning CTAs; this CTA's head g
+  long long Wc;
+  int W, U, Pe, g, begin, end, u0, k0;
 };
+static_assert(8 * B_COUNT + 8 + sizeof(PlanHdr) <= 256, "barrier area overflow");
 
 struct Unit {
   int b, g;
@@ -239,29 +244,41 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       ph = min(ph, max(carryB, 1));
       h.Pe = ph;
       h.g = cta % p.Hkv;
-      const int r = cta / p.Hkv;
-      const bool mine = cta < ph * p.Hkv;
-      h.begin = mine ? (int)(((long long)r * carryB) / ph) : 0;
-      h.end = mine ? (int)(((long long)(r + 1) * carryB) / ph) : 0;
-      h.u0 = 0;
-      h.k0 = 0;
-      if (h.begin < h.end) {
+      // The head's units are cut into Pe contiguous ranges of equal cost, where a
+      // unit costs its key blocks plus kSegBlocks for the fixed work of a segment
+      // (Q load, unmasked-max pass of its first block, epilogue).  Block xb of
+      // head-local unit u sits at cost coordinate xb + kSegBlocks * (u + 1); rank r
+      // owns the blocks whose coordinate lies in [r * Wc / Pe, (r + 1) * Wc / Pe).
+      const long long Wc = (long long)carryB + (long long)kSegBlocks * carryU;
+      h.Wc = Wc;
+      // first block at or after cost coordinate C, as (block, unit, offset in the unit)
+      auto locate = [&](long long C, int& u_out, int& k_out) -> int {
         int lo = 0, hi = p.batch - 1, b = 0;
-        while (lo <= hi) {  // last sequence whose first block is <= begin (every sequence has blocks)
+        while (lo <= hi) {  // last sequence whose cost range starts at or before C
           const int mid = (lo + hi) >> 1;
-          if (s_prefB[mid] <= h.begin) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+          if (s_prefB[mid] + (long long)kSegBlocks * s_prefU[mid] <= C) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
         }
-        int r2 = h.begin - s_prefB[b];
         const ssv_seq s = p.seqs[b];
         const int rows = s.new_len + 2 * s.block;
-        int t = 0;
-        for (; t < s_ntile[b] - 1; ++t) {
+        int xs = s_prefB[b], uu = s_prefU[b];
+        for (int t = 0;; ++t, ++uu) {
           const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
-          if (r2 < nb) break;
-          r2 -= nb;
+          // unit uu covers costs [xs + kSegBlocks * uu, xs + nb + kSegBlocks * (uu + 1))
+          if (t == s_ntile[b] - 1 || xs + nb + (long long)kSegBlocks * (uu + 1) > C) {
+            const long long i = min(max(C - xs - (long long)kSegBlocks * (uu + 1), 0ll), (long long)nb);
+            u_out = (i == nb) ? uu + 1 : uu;
+            k_out = (i == nb) ? 0 : (int)i;
+            return xs + (int)i;
+          }
+          xs += nb;
         }
-        h.u0 = s_prefU[b] + t;
-        h.k0 = r2;
+      };
+      const int r = cta / p.Hkv;
+      h.begin = h.end = h.u0 = h.k0 = 0;
+      if (cta < ph * p.Hkv && carryB > 0) {
+        int u1, k1;
+        h.begin = locate(((long long)r * Wc) / ph, h.u0, h.k0);
+        h.end = (r + 1 == ph) ? carryB : locate(((long long)(r + 1) * Wc) / ph, u1, k1);
       }
       *plan = h;
       *abort = 0;
@@ -283,7 +300,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   // own predecessor before letting this one start, is the only one running.
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
-  const int begin = plan->begin, end = plan->end, W = plan->W, Ph = plan->Pe, Uh = plan->U;
+  const int begin = plan->begin, end = plan->end, Ph = plan->Pe, Uh = plan->U;
+  const long long Wc = plan->Wc;
   const int gh = plan->g;           // kv head served by this CTA
   const int rank = cta / p.Hkv;     // rank among the CTAs of head gh
 
@@ -310,13 +328,14 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     x.full_new = (x.row0 < x.N) ? (x.row0 + 1) : x.N;
     return x;
   };
-  // head-local block ranges: rank r owns [seg_start(r), seg_start(r + 1))
-  auto seg_start = [&](int r) -> int { return (int)(((long long)r * W) / Ph); };
-  auto owner = [&](int xb) -> int {  // rank whose range holds head-local block xb
-    int r = (int)(((long long)xb * Ph) / (W > 0 ? W : 1));
+  // rank r owns the head's blocks with cost coordinate in [cost_start(r), cost_start(r + 1))
+  auto cost_start = [&](int r) -> long long { return ((long long)r * Wc) / Ph; };
+  auto owner = [&](int xb, int ub) -> int {  // rank owning head-local block xb of head-local unit ub
+    const long long c = xb + (long long)kSegBlocks * (ub + 1);
+    int r = (int)((c * Ph) / (Wc > 0 ? Wc : 1));
     r = min(max(r, 0), Ph - 1);
-    while (r + 1 < Ph && seg_start(r + 1) <= xb) ++r;
-    while (r > 0 && seg_start(r) > xb) --r;
+    while (r + 1 < Ph && cost_start(r + 1) <= c) ++r;
+    while (r > 0 && cost_start(r) > c) --r;
     return r;
   };
 
@@ -422,7 +441,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_pv = idesc_bf16(128, 128, true);
       int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kn = 0, vn = 0;
-      int nblk0 = 0, nblk1 = 0, nseg0 = 0, nseg1 = 0;
+      int nseg0 = 0, nseg1 = 0;
       bool run = true;
       static_assert(NSK == 3 && NSV == 2, "descriptor selection below assumes 3 K and 2 V stages");
       const uint64_t dq0 = smem_desc_sw128(sbase + C_::SM_Q, 16, 1024);
@@ -432,27 +451,42 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       const uint64_t dk2 = smem_desc_sw128(sbase + C_::SM_K + 2 * TILE_BYTES, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sbase + C_::SM_V, HALF_BYTES, 1024);
       const uint64_t dv1 = smem_desc_sw128(sbase + C_::SM_V + TILE_BYTES, HALF_BYTES, 1024);
-      auto issue_s = [&](int mt, int st) {
-        gemm_ss_k128(tmem + mt * 128, mt ? dq1 : dq0, st == 0 ? dk0 : (st == 1 ? dk1 : dk2), id_s, 0u);
-        mma_commit(bar(B_S_FULL + mt));
+      auto kdesc = [&](int st) { return st == 0 ? dk0 : (st == 1 ? dk1 : dk2); };
+      // The phases this thread waits on next (key block kn, value block vn,
+      // P of a tile) are tested ahead, inside the issue of the GEMM before
+      // (gemm_*_probe); `seen` holds one bit per phase already observed
+      // complete.  A probe only ever targets a phase that is the next one of
+      // its kind still to be consumed, so a set bit stays true until used.
+      enum : uint32_t { SEEN_K = 1, SEEN_V = 2, SEEN_P = 4 };  // P: SEEN_P << tile (two tiles)
+      struct Probe {
+        uint32_t bar, par, bit;
       };
-      auto issue_pv = [&](int mt, int st, bool acc) {
-        gemm_ts_k128(tmem + TM_O + mt * 128, tmem + mt * 128, st ? dv1 : dv0, id_pv, acc ? 1u : 0u);
-        mma_commit(bar(B_PV_DONE + mt));
+      uint32_t seen = 0;
+      auto pk = [&](int n) -> Probe { return {bar(B_K_FULL + n % NSK), (uint32_t)(n / NSK) & 1u, SEEN_K}; };
+      auto pv = [&](int n) -> Probe { return {bar(B_V_FULL + n % NSV), (uint32_t)(n / NSV) & 1u, SEEN_V}; };
+      auto absorb = [&](uint32_t r, const Probe& a, const Probe& b) {
+        seen |= ((r & 1u) ? a.bit : 0u) | ((r & 2u) ? b.bit : 0u);
       };
-      auto wait_k = [&]() -> bool { return mbar_wait_poll(bar(B_K_FULL + kn % NSK), (kn / NSK) & 1, abort); };
+      auto need = [&](const Probe& t) -> bool {  // wait for t unless already seen
+        if (seen & t.bit) {
+          seen &= ~t.bit;
+          return true;
+        }
+        return mbar_wait_poll(t.bar, t.par, abort);
+      };
       if constexpr (MT == 1) {
         // One tile, S double-buffered: block n's S goes to TMEM buffer n & 1, so
         // S(n + 1) runs while the softmax warps work on S(n).  Order per block:
         // PV(n) (reads P(n) from buffer n & 1), then S(n + 2) into the same
         // buffer (tensor-core operations of this thread complete in issue order).
         int ns_issued = 0, np_issued = 0;  // blocks whose S / PV have been issued (CTA-wide)
-        auto issue_s_db = [&]() -> bool {
-          if (!wait_k()) return false;
+        auto pp = [&](int n) -> Probe { return {bar(B_P_FULL + (n & 1)), (uint32_t)(n >> 1) & 1u, SEEN_P}; };
+        auto issue_s_db = [&](const Probe& a, const Probe& b) -> bool {
+          if (!need(pk(kn))) return false;
           tc_fence_after();
           const int sbuf = ns_issued & 1;
           const int st = kn % NSK;
-          gemm_ss_k128(tmem + sbuf * 128, dq0, st == 0 ? dk0 : (st == 1 ? dk1 : dk2), id_s, 0u);
+          absorb(gemm_ss_k128_probe(tmem + sbuf * 128, dq0, kdesc(st), id_s, 0u, a.bar, a.par, b.bar, b.par), a, b);
           mma_commit(bar(B_S_FULL + sbuf));
           mma_commit(bar(B_K_EMPTY + st));
           ++kn;
@@ -463,24 +497,26 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           const Unit x = decode(u);
           const int len = min(x.nblocks - k, remaining);
           if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
-          if (!issue_s_db()) break;
-          if (len > 1 && !issue_s_db()) break;
+          if (!issue_s_db(pv(vn), pk(kn + 1))) break;
+          if (len > 1 && !issue_s_db(pv(vn), pp(np_issued))) break;
           for (int i = 0; i < len; ++i) {
             const int pbuf = np_issued & 1;
-            if (!mbar_wait_poll(bar(B_V_FULL + vn % NSV), (vn / NSV) & 1, abort) ||
-                !mbar_wait_poll(bar(B_P_FULL + pbuf), (np_issued >> 1) & 1, abort) ||
+            if (!need(pv(vn)) || !need(pp(np_issued)) ||
                 (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
               run = false;
               break;
             }
             tc_fence_after();
-            gemm_ts_k128(tmem + TM_O, tmem + pbuf * 128, (vn % NSV) ? dv1 : dv0, id_pv, i > 0 ? 1u : 0u);
+            const Probe a = (i + 2 < len) ? pk(kn) : pp(np_issued + 1), b = pv(vn + 1);
+            absorb(gemm_ts_k128_probe(tmem + TM_O, tmem + pbuf * 128, (vn % NSV) ? dv1 : dv0, id_pv, i > 0 ? 1u : 0u,
+                                      a.bar, a.par, b.bar, b.par),
+                   a, b);
             mma_commit(bar(B_PV_DONE));
             if (i + 1 == len) mma_commit(bar(B_SEG_DONE));
             mma_commit(bar(B_V_EMPTY + vn % NSV));
             ++vn;
             ++np_issued;
-            if (i + 2 < len && !issue_s_db()) { run = false; break; }
+            if (i + 2 < len && !issue_s_db(pp(np_issued), pv(vn))) { run = false; break; }
           }
           if (!run) break;
           mma_commit(bar(B_Q_EMPTY));
@@ -491,47 +527,123 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           k = 0;
         }
       }
-      while (MT > 1 && run && remaining > 0) {
-        const Unit x = decode(u);
-        const int len = min(x.nblocks - k, remaining);
-        if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
-        if (!wait_k()) break;
-        tc_fence_after();
-        for (int mt = 0; mt < x.mc; ++mt) issue_s(mt, kn % NSK);
-        mma_commit(bar(B_K_EMPTY + kn % NSK));
-        ++kn;
-        for (int i = 0; i < len && run; ++i) {
-          if (!mbar_wait_poll(bar(B_V_FULL + vn % NSV), (vn / NSV) & 1, abort)) { run = false; break; }
-          for (int mt = 0; mt < x.mc; ++mt) {
-            int& nb = mt ? nblk1 : nblk0;
-            const int ns = mt ? nseg1 : nseg0;
-            if (!mbar_wait_poll(bar(B_P_FULL + mt), nb & 1, abort)) { run = false; break; }
-            if (i == 0 && ns > 0 && !mbar_wait_poll(bar(B_O_FREE + mt), (ns - 1) & 1, abort)) { run = false; break; }
-            tc_fence_after();
-            issue_pv(mt, vn % NSV, i > 0);
-            ++nb;
-            if (i + 1 < len) {
-              if (mt == 0 && !wait_k()) { run = false; break; }
-              tc_fence_after();
-              issue_s(mt, kn % NSK);
+      // Two tiles: per block, PV_0(j) S_0(j + 1) PV_1(j) S_1(j + 1).  The issue of
+      // a GEMM returns only once the tensor pipe's queue (about one MMA deep) has
+      // room, so whatever this thread does between GEMMs leaves the pipe idle:
+      // ring positions live in registers as barrier addresses, descriptors and
+      // parities, advanced by additions.
+      if constexpr (MT > 1) {
+        uint32_t kb = bar(B_K_FULL), kph = 0u;  // K ring: FULL barrier of the next key block's stage, parity
+        uint64_t kd = dk0;                      // and that stage's descriptor
+        int ks = 0;
+        uint32_t vb = bar(B_V_FULL), vph = 0u, vbn = bar(B_V_FULL + 1), vphn = 0u;  // V ring: next block, the one after
+        uint64_t vd = dv0, vdn = dv1;
+        const uint32_t pb0 = bar(B_P_FULL), pb1 = bar(B_P_FULL + 1);
+        uint32_t pph0 = 0u, pph1 = 0u;
+        constexpr uint32_t SEEN_P0 = SEEN_P, SEEN_P1 = SEEN_P << 1;
+        auto wait_seen = [&](uint32_t bit, uint32_t b, uint32_t par) -> bool {
+          if (seen & bit) {
+            seen &= ~bit;
+            return true;
+          }
+          return mbar_wait_poll(b, par, abort);
+        };
+        auto note = [&](uint32_t r, uint32_t bit_a, uint32_t bit_b) {
+          seen |= ((r & 1u) ? bit_a : 0u) | ((r & 2u) ? bit_b : 0u);
+        };
+        auto k_advance = [&]() {
+          if (ks == NSK - 1) {
+            ks = 0;
+            kb -= 8u * (NSK - 1);
+            kd -= (uint64_t)(NSK - 1) * (TILE_BYTES >> 4);
+            kph ^= 1u;
+          } else {
+            ++ks;
+            kb += 8u;
+            kd += TILE_BYTES >> 4;
+          }
+        };
+        auto v_advance = [&]() {  // two stages: the next becomes current; a stage's parity flips per use
+          const uint32_t tb = vb, tp = vph;
+          const uint64_t td = vd;
+          vb = vbn; vph = vphn; vd = vdn;
+          vbn = tb; vphn = tp ^ 1u; vdn = td;
+        };
+        while (run && remaining > 0) {
+          const Unit x = decode(u);
+          const int len = min(x.nblocks - k, remaining);
+          const bool two = x.mc > 1;
+          if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+          if (!wait_seen(SEEN_K, kb, kph)) break;
+          tc_fence_after();
+          note(gemm_ss_k128_probe(tmem, dq0, kd, id_s, 0u, vb, vph, vb, vph), SEEN_V, SEEN_V);
+          mma_commit(bar(B_S_FULL));
+          if (two) {
+            note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, vb, vph, vb, vph), SEEN_V, SEEN_V);
+            mma_commit(bar(B_S_FULL + 1));
+          }
+          mma_commit(kb + 8u * NSK);  // K_EMPTY of the stage
+          k_advance();
+          for (int i = 0; i < len; ++i) {
+            const bool more = i + 1 < len;
+            const uint32_t acc = i > 0 ? 1u : 0u;
+            if (!wait_seen(SEEN_V, vb, vph)) { run = false; break; }
+            // ---- tile 0
+            if (!wait_seen(SEEN_P0, pb0, pph0) ||
+                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
+              run = false;
+              break;
             }
+            tc_fence_after();
+            {
+              // needed next: the key block of S_0(j + 1) (else the next V), tile 1's P (else the next V)
+              const uint32_t b1 = more ? kb : vbn, p1 = more ? kph : vphn;
+              const uint32_t b2 = two ? pb1 : vbn, p2 = two ? pph1 : vphn;
+              note(gemm_ts_k128_probe(tmem + TM_O, tmem, vd, id_pv, acc, b1, p1, b2, p2), more ? SEEN_K : SEEN_V,
+                   two ? SEEN_P1 : SEEN_V);
+            }
+            mma_commit(bar(B_PV_DONE));
+            pph0 ^= 1u;
+            if (more) {
+              if (!wait_seen(SEEN_K, kb, kph)) { run = false; break; }
+              tc_fence_after();
+              const uint32_t b1 = two ? pb1 : pb0, p1 = two ? pph1 : pph0;
+              note(gemm_ss_k128_probe(tmem, dq0, kd, id_s, 0u, b1, p1, vbn, vphn), two ? SEEN_P1 : SEEN_P0, SEEN_V);
+              mma_commit(bar(B_S_FULL));
+            }
+            // ---- tile 1
+            if (two) {
+              if (!wait_seen(SEEN_P1, pb1, pph1) ||
+                  (i == 0 && nseg1 > 0 && !mbar_wait_poll(bar(B_O_FREE + 1), (nseg1 - 1) & 1, abort))) {
+                run = false;
+                break;
+              }
+              tc_fence_after();
+              note(gemm_ts_k128_probe(tmem + TM_O + 128, tmem + 128, vd, id_pv, acc, pb0, pph0, vbn, vphn), SEEN_P0,
+                   SEEN_V);
+              mma_commit(bar(B_PV_DONE + 1));
+              pph1 ^= 1u;
+              if (more) {
+                note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, pb0, pph0, vbn, vphn), SEEN_P0, SEEN_V);
+                mma_commit(bar(B_S_FULL + 1));
+              }
+            }
+            if (more) {
+              mma_commit(kb + 8u * NSK);
+              k_advance();
+            }
+            mma_commit(vb + 8u * NSV);  // V_EMPTY of the stage
+            v_advance();
           }
           if (!run) break;
-          if (i + 1 < len) {
-            mma_commit(bar(B_K_EMPTY + kn % NSK));
-            ++kn;
-          }
-          mma_commit(bar(B_V_EMPTY + vn % NSV));
-          ++vn;
+          mma_commit(bar(B_Q_EMPTY));
+          ++nseg0;
+          if (two) ++nseg1;
+          remaining -= len;
+          ++seg;
+          ++u;
+          k = 0;
         }
-        if (!run) break;
-        mma_commit(bar(B_Q_EMPTY));
-        ++nseg0;
-        if (x.mc > 1) ++nseg1;
-        remaining -= len;
-        ++seg;
-        ++u;
-        k = 0;
       }
     }
     if (lane == 0) {
@@ -804,7 +916,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             }
           } else {
             // ---- publish this segment's partial; the 32-row group arriving last merges
-            const int c_a = owner(ustart), c_b = owner(ustart + x.nblocks - 1);  // ranks of head gh
+            const int c_a = owner(ustart, u), c_b = owner(ustart + x.nblocks - 1, u);  // ranks of head gh
+            // rank c_a holds the unit's first block; this is not its first segment when it
+            // also owns the block before (which then belongs to unit u - 1)
+            const bool a_later = ustart > 0 && owner(ustart - 1, u - 1) == c_a;
             const int which = (seg == 0) ? 0 : 1;
             const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
             __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
@@ -829,7 +944,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             if (prev == c_b - c_a) {
               __threadfence();
               auto slot_of = [&](int rr) -> size_t {  // partial slot of rank rr of head gh
-                const int wh = (rr == c_a && seg_start(rr) < ustart) ? 1 : 0;
+                const int wh = (rr == c_a && a_later) ? 1 : 0;
                 return ((size_t)((rr * p.Hkv + gh) * 2 + wh) * MT + mt) * 128 + m;
               };
               // combine in CTA order (not arrival order) so the result is deterministic

@@ -217,6 +217,63 @@ __device__ __forceinline__ void gemm_ts_k128(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// The two GEMMs above with two barrier probes folded in: after the sixth MMA
+// they test, without waiting, whether the phase of parity par1 of barrier
+// bar1 and that of parity par2 of bar2 have completed (bits 0 and 1 of the
+// result).  An MMA issue stalls while the tensor pipe's queue (about one MMA
+// deep) is full, so the tests' latency overlaps the GEMM's last steps
+// instead of leaving the pipe idle after it.
+#define SSV_MMA_SS(OA, OB)                                                                   \
+  "add.s64 a, %3, " #OA ";\n\tadd.s64 b, %4, " #OB                                           \
+  ";\n\ttcgen05.mma.cta_group::1.kind::f16 [%2], a, b, %5, q;\n\t"
+#define SSV_MMA_TS(OA, OB)                                                                   \
+  "add.u32 a, %3, " #OA ";\n\tadd.s64 b, %4, " #OB                                           \
+  ";\n\ttcgen05.mma.cta_group::1.kind::f16 [%2], [a], b, %5, q;\n\t"
+#define SSV_PROBES                                                                           \
+  "mbarrier.test_wait.parity.shared::cta.b64 t1, [%7], %8;\n\t"                              \
+  "mbarrier.test_wait.parity.shared::cta.b64 t2, [%9], %10;\n\t"
+
+__device__ __forceinline__ uint32_t gemm_ss_k128_probe(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                       uint32_t idesc, uint32_t accumulate, uint32_t bar1,
+                                                       uint32_t par1, uint32_t bar2, uint32_t par2) {
+  uint32_t r1, r2;
+  asm volatile(
+      "{\n\t.reg .pred p, q, t1, t2;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], %3, %4, %5, p;\n\t"
+      SSV_MMA_SS(2, 2) SSV_MMA_SS(4, 4) SSV_MMA_SS(6, 6) SSV_MMA_SS(1024, 1024) SSV_MMA_SS(1026, 1026)
+      SSV_PROBES
+      SSV_MMA_SS(1028, 1028) SSV_MMA_SS(1030, 1030)
+      "selp.u32 %0, 1, 0, t1;\n\tselp.u32 %1, 1, 0, t2;\n\t}"
+      : "=r"(r1), "=r"(r2)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar1), "r"(par1), "r"(bar2),
+        "r"(par2)
+      : "memory");
+  return r1 | (r2 << 1);
+}
+
+__device__ __forceinline__ uint32_t gemm_ts_k128_probe(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                       uint32_t idesc, uint32_t accumulate, uint32_t bar1,
+                                                       uint32_t par1, uint32_t bar2, uint32_t par2) {
+  uint32_t r1, r2;
+  asm volatile(
+      "{\n\t.reg .pred p, q, t1, t2;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%2], [%3], %4, %5, p;\n\t"
+      SSV_MMA_TS(8, 128) SSV_MMA_TS(16, 256) SSV_MMA_TS(24, 384) SSV_MMA_TS(32, 512) SSV_MMA_TS(40, 640)
+      SSV_PROBES
+      SSV_MMA_TS(48, 768) SSV_MMA_TS(56, 896)
+      "selp.u32 %0, 1, 0, t1;\n\tselp.u32 %1, 1, 0, t2;\n\t}"
+      : "=r"(r1), "=r"(r2)
+      : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar1), "r"(par1), "r"(bar2),
+        "r"(par2)
+      : "memory");
+  return r1 | (r2 << 1);
+}
+#undef SSV_MMA_SS
+#undef SSV_MMA_TS
+#undef SSV_PROBES
+
 // mbarrier arrives once every MMA issued so far by this thread has completed
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
