@@ -62,7 +62,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeBlocks = 8;                  // key blocks a partial merge costs, roughly
-constexpr int kSegBlocks = 2;                    // key blocks of time a segment's fixed work takes, roughly
+// Work estimate of the plan, in cost units: a key block costs 1 + the tiles it
+// is multiplied into (the MMA work grows with the tiles, the K/V fetch does
+// not); a segment's fixed work (Q load, first block's unmasked-max pass,
+// epilogue) costs about two two-tile blocks.
+constexpr int kSegCost = 6;
 
 enum : uint32_t {
   B_Q_FULL = 0,
@@ -102,12 +106,19 @@ struct TcWork {
   int32_t* plan;   // [grid][4][batch + 1] per-CTA planning tables
   int32_t* cnt;    // [units][MT][4] arrival counters (zero between calls)
   float* part_ml;  // [2 * grid][MT][128][2]  running max (log2 domain), sum
-  float* part_o;   // [2 * grid][MT][128][128] unnormalised O
+  float* part_o;   // [2 * grid][MT][D / 4][128][4] unnormalised O (see part_o_at)
 };
 
-// Per head: W key blocks, U units, Pe owning CTAs and Wc = W + kSegBlocks * U
-// cost units; this CTA's head g and its range [begin, end) of the head's
-// blocks, which starts at block k0 of unit u0.
+// Float4 group c4 (columns 4 c4 .. 4 c4 + 3) of partial row `slot_row` (= tile
+// slot * 128 + row).  Column groups are outermost within a tile, so the 32
+// lanes of a warp (consecutive rows) touch 512 contiguous bytes per access.
+__device__ __forceinline__ float4* part_o_at(float* part_o, size_t slot_row, int c4) {
+  return reinterpret_cast<float4*>(part_o + (slot_row >> 7) * (128 * D)) + (size_t)c4 * 128 + (slot_row & 127);
+}
+
+// Per head: W key blocks, U units, Pe owning CTAs and Wc cost units; this
+// CTA's head g and its range [begin, end) of the head's blocks, which starts
+// at block k0 of unit u0.
 struct PlanHdr {
   long long Wc;
   int W, U, Pe, g, begin, end, u0, k0;
@@ -121,6 +132,10 @@ struct Unit {
 };
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int unit_weight(int rows, int row0, int UR, int R, int MT) {
+  return (MT == 2 && min(UR, rows - row0) > R) ? 3 : 2;  // 1 + tiles of the unit
+}
 
 __device__ __forceinline__ int unit_nblocks(int C, int N, int rows, int row0, int UR) {
   const int kmax = (row0 + UR <= N) ? (row0 + UR) : rows;
@@ -167,8 +182,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   int* s_prefU = plan_smem ? reinterpret_cast<int*>(smem + C_::SM_TOTAL)
                            : work.plan + (size_t)blockIdx.x * 4 * (p.batch + 1);
   int* s_prefB = s_prefU + (p.batch + 1);
-  int* s_bgblk = s_prefB + (p.batch + 1);
-  int* s_ntile = s_bgblk + (p.batch + 1);
+  int* s_prefC = s_prefB + (p.batch + 1);
+  int* s_ntile = s_prefC + (p.batch + 1);
   auto bar = [&](uint32_t i) -> uint32_t { return sbase + C_::SM_BAR + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,30 +202,33 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     // do not overlap seqs, tau or the KV cache) with the plan in shared memory
     // may read inputs; otherwise wait here (the barrier below orders the rest).
     if (!(p.early && plan_smem)) pdl_wait();
-    int carryU = 0, carryB = 0;
+    int carryU = 0, carryB = 0, carryC = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
       const int b = b0 + lane;
-      int units = 0, blocks = 0;
+      int units = 0, blocks = 0, cost = 0;
       if (b < p.batch) {
         const ssv_seq s = p.seqs[b];
         const int rows = s.new_len + 2 * s.block;
         const int nt = cdiv(rows, UR);
-        int bg = 0;
-        for (int t = 0; t < nt; ++t) bg += unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
-        s_bgblk[b] = bg;
+        for (int t = 0; t < nt; ++t) {
+          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+          blocks += nb;
+          cost += kSegCost + unit_weight(rows, t * UR, UR, R, MT) * nb;
+        }
         s_ntile[b] = nt;
         units = nt;
-        blocks = bg;
       }
-      int iu = units, ib = blocks;
+      int iu = units, ib = blocks, ic = cost;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int yu = __shfl_up_sync(0xffffffffu, iu, o), yb = __shfl_up_sync(0xffffffffu, ib, o);
-        if (lane >= o) { iu += yu; ib += yb; }
+        const int yc = __shfl_up_sync(0xffffffffu, ic, o);
+        if (lane >= o) { iu += yu; ib += yb; ic += yc; }
       }
-      if (b < p.batch) { s_prefU[b + 1] = carryU + iu; s_prefB[b + 1] = carryB + ib; }
+      if (b < p.batch) { s_prefU[b + 1] = carryU + iu; s_prefB[b + 1] = carryB + ib; s_prefC[b + 1] = carryC + ic; }
       carryU += __shfl_sync(0xffffffffu, iu, 31);
       carryB += __shfl_sync(0xffffffffu, ib, 31);
+      carryC += __shfl_sync(0xffffffffu, ic, 31);
     }
     if (cta == 0) {
       // stage maps must permute 1..B (a bad map cannot index out of range: report only)
@@ -227,6 +245,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     if (lane == 0) {
       s_prefU[0] = 0;
       s_prefB[0] = 0;
+      s_prefC[0] = 0;
       PlanHdr h;
       h.W = carryB;  // key blocks per head
       h.U = carryU;  // units per head
@@ -242,35 +261,40 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         ph = (f > 1 && saved > kMergeBlocks) ? carryU * f : carryU;
       }
       ph = min(ph, max(carryB, 1));
+      // every range at least one block's weight wide: no range falls between two
+      // block starts of a unit, so the ranks holding a unit's blocks are consecutive
+      ph = min(ph, max(carryC / (1 + MT), 1));
       h.Pe = ph;
       h.g = cta % p.Hkv;
-      // The head's units are cut into Pe contiguous ranges of equal cost, where a
-      // unit costs its key blocks plus kSegBlocks for the fixed work of a segment
-      // (Q load, unmasked-max pass of its first block, epilogue).  Block xb of
-      // head-local unit u sits at cost coordinate xb + kSegBlocks * (u + 1); rank r
-      // owns the blocks whose coordinate lies in [r * Wc / Pe, (r + 1) * Wc / Pe).
-      const long long Wc = (long long)carryB + (long long)kSegBlocks * carryU;
+      // The head's units are cut into Pe contiguous ranges of equal estimated cost.
+      // Unit u occupies the costs [c_u, c_u + kSegCost + w_u n_u) (its fixed work
+      // first), its i-th block sits at cost coordinate c_u + kSegCost + w_u i, and
+      // rank r owns the blocks whose coordinate lies in [r Wc / Pe, (r + 1) Wc / Pe).
+      const long long Wc = carryC;
       h.Wc = Wc;
       // first block at or after cost coordinate C, as (block, unit, offset in the unit)
       auto locate = [&](long long C, int& u_out, int& k_out) -> int {
         int lo = 0, hi = p.batch - 1, b = 0;
         while (lo <= hi) {  // last sequence whose cost range starts at or before C
           const int mid = (lo + hi) >> 1;
-          if (s_prefB[mid] + (long long)kSegBlocks * s_prefU[mid] <= C) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+          if (s_prefC[mid] <= C) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
         }
         const ssv_seq s = p.seqs[b];
         const int rows = s.new_len + 2 * s.block;
         int xs = s_prefB[b], uu = s_prefU[b];
+        long long cu = s_prefC[b];
         for (int t = 0;; ++t, ++uu) {
           const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
-          // unit uu covers costs [xs + kSegBlocks * uu, xs + nb + kSegBlocks * (uu + 1))
-          if (t == s_ntile[b] - 1 || xs + nb + (long long)kSegBlocks * (uu + 1) > C) {
-            const long long i = min(max(C - xs - (long long)kSegBlocks * (uu + 1), 0ll), (long long)nb);
+          const int w = unit_weight(rows, t * UR, UR, R, MT);
+          if (t == s_ntile[b] - 1 || cu + kSegCost + (long long)w * nb > C) {
+            const long long d = C - cu - kSegCost;
+            const int i = d <= 0 ? 0 : (int)min((d + w - 1) / w, (long long)nb);
             u_out = (i == nb) ? uu + 1 : uu;
-            k_out = (i == nb) ? 0 : (int)i;
-            return xs + (int)i;
+            k_out = (i == nb) ? 0 : i;
+            return xs + i;
           }
           xs += nb;
+          cu += kSegCost + (long long)w * nb;
         }
       };
       const int r = cta / p.Hkv;
@@ -330,13 +354,25 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   };
   // rank r owns the head's blocks with cost coordinate in [cost_start(r), cost_start(r + 1))
   auto cost_start = [&](int r) -> long long { return ((long long)r * Wc) / Ph; };
-  auto owner = [&](int xb, int ub) -> int {  // rank owning head-local block xb of head-local unit ub
-    const long long c = xb + (long long)kSegBlocks * (ub + 1);
+  auto owner_at = [&](long long c) -> int {  // rank owning the block at cost coordinate c
     int r = (int)((c * Ph) / (Wc > 0 ? Wc : 1));
     r = min(max(r, 0), Ph - 1);
     while (r + 1 < Ph && cost_start(r + 1) <= c) ++r;
     while (r > 0 && cost_start(r) > c) --r;
     return r;
+  };
+  auto unit_cost = [&](int u) -> long long {  // cost coordinate where head-local unit u starts
+    int lo = 0, hi = p.batch - 1, b = 0;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefU[mid] <= u) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    const ssv_seq s = p.seqs[b];
+    const int rows = s.new_len + 2 * s.block;
+    long long c = s_prefC[b];
+    for (int t = 0; t < u - s_prefU[b]; ++t)
+      c += kSegCost + (long long)unit_weight(rows, t * UR, UR, R, MT) * unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+    return c;
   };
 
   if (warp == 0) {
@@ -662,7 +698,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     const uint32_t tS0 = tmem + lane_base + mt * 128;
     const uint32_t tO = tmem + lane_base + TM_O + mt * 128;
     const float cexp = p.scale * 1.4426950408889634f;
-    int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, nblk = 0, pos = begin;
+    int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, nblk = 0;
     bool run = true;
     auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, abort);
@@ -672,7 +708,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       const Unit x = decode(u);
       const int len = min(x.nblocks - k, remaining);
       const bool complete = (k == 0 && len == x.nblocks);
-      const int ustart = pos - k;  // global index of the unit's first block
       if (mt < x.mc) {
         const int r_local = mt * R + m / G;
         const int hj = m % G;
@@ -916,10 +951,12 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             }
           } else {
             // ---- publish this segment's partial; the 32-row group arriving last merges
-            const int c_a = owner(ustart, u), c_b = owner(ustart + x.nblocks - 1, u);  // ranks of head gh
-            // rank c_a holds the unit's first block; this is not its first segment when it
-            // also owns the block before (which then belongs to unit u - 1)
-            const bool a_later = ustart > 0 && owner(ustart - 1, u - 1) == c_a;
+            const long long cu = unit_cost(u);
+            const int c_a = owner_at(cu + kSegCost);                                   // ranks of head gh holding
+            const int c_b = owner_at(cu + kSegCost + (long long)(1 + x.mc) * (x.nblocks - 1));  // the first, last block
+            // this is not rank c_a's first segment when it also owns the block before,
+            // the last of unit u - 1
+            const bool a_later = u > 0 && owner_at(cu - (1 + decode(u - 1).mc)) == c_a;
             const int which = (seg == 0) ? 0 : 1;
             const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
             __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
@@ -928,10 +965,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               uint32_t raw[32];
               tmem_ld32(tO + q * 32, raw);
               tmem_wait_ld();
-              float* po = work.part_o + myslot * D + q * 32;
 #pragma unroll
               for (int c = 0; c < 32; c += 4)
-                __stcg(reinterpret_cast<float4*>(po + c),
+                __stcg(part_o_at(work.part_o, myslot, q * 8 + c / 4),
                        make_float4(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1]), __uint_as_float(raw[c + 2]),
                                    __uint_as_float(raw[c + 3])));
             }
@@ -953,11 +989,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                 // (m, l) of every partial in one round of loads, then O 64 columns at a
                 // time with all of a partial's loads for those columns issued together
                 float2 ml[4];
-                const float* po[4];
+                size_t po[4];  // partial slot row of each part; ~0 for this CTA's own (in TMEM)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                   const int cc = c_a + k;
-                  po[k] = nullptr;
+                  po[k] = ~size_t(0);
                   ml[k] = make_float2(-INFINITY, 0.f);
                   if (k < nparts) {
                     if (cc == rank) {
@@ -965,7 +1001,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                     } else {
                       const size_t sl = slot_of(cc);
                       ml[k] = __ldcg(reinterpret_cast<const float2*>(work.part_ml + sl * 2));
-                      po[k] = work.part_o + sl * D;
+                      po[k] = sl;
                     }
                   }
                 }
@@ -987,7 +1023,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
 #pragma unroll
                   for (int k = 0; k < 4; ++k) {
                     if (k >= nparts) break;
-                    if (po[k] == nullptr) {
+                    if (po[k] == ~size_t(0)) {
                       uint32_t raw[32];
                       tmem_ld32(tO + q * 32, raw);
                       tmem_wait_ld();
@@ -996,7 +1032,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                     } else {
                       float4 w4[8];
 #pragma unroll
-                      for (int c = 0; c < 8; ++c) w4[c] = __ldcg(reinterpret_cast<const float4*>(po[k] + q * 32) + c);
+                      for (int c = 0; c < 8; ++c) w4[c] = __ldcg(part_o_at(work.part_o, po[k], q * 8 + c));
 #pragma unroll
                       for (int c = 0; c < 8; ++c) {
                         v[4 * c] += w4[c].x * fo[k]; v[4 * c + 1] += w4[c].y * fo[k];
@@ -1038,10 +1074,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                       const size_t sl = slot_of(cc);
                       const float mo = __ldcg(work.part_ml + sl * 2);
                       const float f = (M == -INFINITY) ? 0.f : ex2(mo - M);
-                      const float* pc = work.part_o + sl * D + q * 32;
 #pragma unroll
                       for (int c = 0; c < 32; c += 4) {
-                        const float4 w4 = __ldcg(reinterpret_cast<const float4*>(pc + c));
+                        const float4 w4 = __ldcg(part_o_at(work.part_o, sl, q * 8 + c / 4));
                         v[c] += w4.x * f; v[c + 1] += w4.y * f; v[c + 2] += w4.z * f; v[c + 3] += w4.w * f;
                       }
                     }
@@ -1060,7 +1095,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           if (lane == 0) mbar_arrive(bar(B_O_FREE + mt));
         }
       }
-      pos += len;
       remaining -= len;
       ++seg;
       ++u;
@@ -1157,7 +1191,7 @@ bool attn_tc_supported(const AttnParams& p) {
   const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
   const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
                            ((p.max_cache + BN - 1) / BN + (max_rows + BN - 1) / BN);
-  if (blocks > (1LL << 30)) return false;
+  if (blocks > (1LL << 27)) return false;  // plan costs (at most 9 units per block) stay in int32
   return encode_fn() != nullptr && sm_count() > 0;
 }
 
