@@ -30,8 +30,10 @@
 //           ring) and TMEM owner (512 columns)
 //   warp 1  MMA issuer: S_mt = Q_mt K^T into TMEM, then O_mt += P_mt V with P
 //           read from TMEM (it overwrites S_mt's first 64 columns) and V as
-//           an MN-major shared-memory operand; tiles alternate so one
-//           softmax warpgroup computes while the tensor core serves the other
+//           an MN-major shared-memory operand; with two active tiles they
+//           alternate so one softmax warpgroup computes while the tensor core
+//           serves the other; a unit with one active tile double-buffers its S
+//           over both tiles' S columns instead, so S(n + 1) overlaps softmax(n)
 //   warps 2.. softmax, 4 per tile (one TMEM lane quadrant each): S row from
 //           TMEM, mask, running max with lazy rescaling of O (only when the
 //           max grows by more than 2^8), exp2, bf16 P back into TMEM;
@@ -75,11 +77,13 @@ enum : uint32_t {
   B_K_EMPTY = B_K_FULL + NSK,    // + stage
   B_V_FULL = B_K_EMPTY + NSK,    // + stage
   B_V_EMPTY = B_V_FULL + NSV,    // + stage
-  B_S_FULL = B_V_EMPTY + NSV,    // + tile
+  B_S_FULL = B_V_EMPTY + NSV,    // + tile (units with two active tiles)
   B_P_FULL = B_S_FULL + 2,       // + tile
   B_PV_DONE = B_P_FULL + 2,      // + tile
   B_O_FREE = B_PV_DONE + 2,      // + tile
-  B_SEG_DONE = B_O_FREE + 2,     // one-tile path: every PV of a segment complete
+  B_SDB = B_O_FREE + 2,          // + S buffer (units with one active tile)
+  B_PDB = B_SDB + 2,             // + S buffer
+  B_SEG_DONE = B_PDB + 2,        // every PV of the segment complete (one phase per segment)
   B_FINAL = B_SEG_DONE + 1,
   B_COUNT = B_FINAL + 1
 };
@@ -308,7 +312,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       *abort = 0;
       for (uint32_t i = 0; i < B_COUNT; ++i) {
         uint32_t cnt = 1;
-        if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_FREE || i == B_O_FREE + 1) cnt = 4;
+        if (i == B_P_FULL || i == B_P_FULL + 1 || i == B_PDB || i == B_PDB + 1 || i == B_O_FREE || i == B_O_FREE + 1)
+          cnt = 4;
         mbar_init(bar(i), cnt);
       }
       fence_mbar_init();
@@ -476,155 +481,122 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     if (lane == 0 && begin < end) {
       const uint32_t id_s = idesc_bf16(128, 128, false);
       const uint32_t id_pv = idesc_bf16(128, 128, true);
-      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, kn = 0, vn = 0;
-      int nseg0 = 0, nseg1 = 0;
+      int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0;
+      int nseg0 = 0, nseg1 = 0;  // segments of tile 0 / tile 1 (their O_FREE phases)
       bool run = true;
-      static_assert(NSK == 3 && NSV == 2, "descriptor selection below assumes 3 K and 2 V stages");
       const uint64_t dq0 = smem_desc_sw128(sbase + C_::SM_Q, 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(sbase + C_::SM_Q + (MT > 1 ? TILE_BYTES : 0), 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(sbase + C_::SM_K, 16, 1024);
-      const uint64_t dk1 = smem_desc_sw128(sbase + C_::SM_K + TILE_BYTES, 16, 1024);
-      const uint64_t dk2 = smem_desc_sw128(sbase + C_::SM_K + 2 * TILE_BYTES, 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(sbase + C_::SM_V, HALF_BYTES, 1024);
-      const uint64_t dv1 = smem_desc_sw128(sbase + C_::SM_V + TILE_BYTES, HALF_BYTES, 1024);
-      auto kdesc = [&](int st) { return st == 0 ? dk0 : (st == 1 ? dk1 : dk2); };
-      // The phases this thread waits on next (key block kn, value block vn,
-      // P of a tile) are tested ahead, inside the issue of the GEMM before
-      // (gemm_*_probe); `seen` holds one bit per phase already observed
-      // complete.  A probe only ever targets a phase that is the next one of
-      // its kind still to be consumed, so a set bit stays true until used.
-      enum : uint32_t { SEEN_K = 1, SEEN_V = 2, SEEN_P = 4 };  // P: SEEN_P << tile (two tiles)
-      struct Probe {
-        uint32_t bar, par, bit;
-      };
+      // The issue of a GEMM returns only once the tensor pipe's queue (about one MMA
+      // deep) has room, so whatever this thread does between GEMMs leaves the pipe
+      // idle: ring positions live in registers as barrier addresses, descriptors and
+      // parities advanced by additions, and the phases waited on next are tested
+      // inside the issue of the GEMM before (gemm_*_probe).  `seen` holds one bit
+      // per such phase already observed complete; a probe only ever targets the next
+      // phase of its kind still to be consumed, so a set bit stays true until used.
+      enum : uint32_t { SEEN_K = 1, SEEN_V = 2, SEEN_P0 = 4, SEEN_P1 = 8, SEEN_PD = 16 };
       uint32_t seen = 0;
-      auto pk = [&](int n) -> Probe { return {bar(B_K_FULL + n % NSK), (uint32_t)(n / NSK) & 1u, SEEN_K}; };
-      auto pv = [&](int n) -> Probe { return {bar(B_V_FULL + n % NSV), (uint32_t)(n / NSV) & 1u, SEEN_V}; };
-      auto absorb = [&](uint32_t r, const Probe& a, const Probe& b) {
-        seen |= ((r & 1u) ? a.bit : 0u) | ((r & 2u) ? b.bit : 0u);
-      };
-      auto need = [&](const Probe& t) -> bool {  // wait for t unless already seen
-        if (seen & t.bit) {
-          seen &= ~t.bit;
+      uint32_t kb = bar(B_K_FULL), kph = 0u;  // K ring: FULL barrier of the next key block's stage, parity
+      uint64_t kd = smem_desc_sw128(sbase + C_::SM_K, 16, 1024);  // and that stage's descriptor
+      int ks = 0;
+      uint32_t vb = bar(B_V_FULL), vph = 0u, vbn = bar(B_V_FULL + 1), vphn = 0u;  // V ring: next block, the one after
+      uint64_t vd = smem_desc_sw128(sbase + C_::SM_V, HALF_BYTES, 1024);
+      uint64_t vdn = smem_desc_sw128(sbase + C_::SM_V + TILE_BYTES, HALF_BYTES, 1024);
+      const uint32_t pb0 = bar(B_P_FULL), pb1 = bar(B_P_FULL + 1);
+      uint32_t pph0 = 0u, pph1 = 0u;
+      int dbs = 0, dbp = 0;  // one-tile segments: blocks whose S / PV have been issued (S buffer = count & 1)
+      static_assert(NSV == 2, "the V ring below has two stages");
+      auto wait_seen = [&](uint32_t bit, uint32_t b, uint32_t par) -> bool {
+        if (seen & bit) {
+          seen &= ~bit;
           return true;
         }
-        return mbar_wait_poll(t.bar, t.par, abort);
+        return mbar_wait_poll(b, par, abort);
       };
-      if constexpr (MT == 1) {
-        // One tile, S double-buffered: block n's S goes to TMEM buffer n & 1, so
-        // S(n + 1) runs while the softmax warps work on S(n).  Order per block:
-        // PV(n) (reads P(n) from buffer n & 1), then S(n + 2) into the same
-        // buffer (tensor-core operations of this thread complete in issue order).
-        int ns_issued = 0, np_issued = 0;  // blocks whose S / PV have been issued (CTA-wide)
-        auto pp = [&](int n) -> Probe { return {bar(B_P_FULL + (n & 1)), (uint32_t)(n >> 1) & 1u, SEEN_P}; };
-        auto issue_s_db = [&](const Probe& a, const Probe& b) -> bool {
-          if (!need(pk(kn))) return false;
-          tc_fence_after();
-          const int sbuf = ns_issued & 1;
-          const int st = kn % NSK;
-          absorb(gemm_ss_k128_probe(tmem + sbuf * 128, dq0, kdesc(st), id_s, 0u, a.bar, a.par, b.bar, b.par), a, b);
-          mma_commit(bar(B_S_FULL + sbuf));
-          mma_commit(bar(B_K_EMPTY + st));
-          ++kn;
-          ++ns_issued;
-          return true;
-        };
-        while (run && remaining > 0) {
-          const Unit x = decode(u);
-          const int len = min(x.nblocks - k, remaining);
-          if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
-          if (!issue_s_db(pv(vn), pk(kn + 1))) break;
-          if (len > 1 && !issue_s_db(pv(vn), pp(np_issued))) break;
+      auto note = [&](uint32_t r, uint32_t bit_a, uint32_t bit_b) {
+        seen |= ((r & 1u) ? bit_a : 0u) | ((r & 2u) ? bit_b : 0u);
+      };
+      auto k_advance = [&]() {
+        if (ks == NSK - 1) {
+          ks = 0;
+          kb -= 8u * (NSK - 1);
+          kd -= (uint64_t)(NSK - 1) * (TILE_BYTES >> 4);
+          kph ^= 1u;
+        } else {
+          ++ks;
+          kb += 8u;
+          kd += TILE_BYTES >> 4;
+        }
+      };
+      auto v_advance = [&]() {  // two stages: the next becomes current; a stage's parity flips per use
+        const uint32_t tb = vb, tp = vph;
+        const uint64_t td = vd;
+        vb = vbn; vph = vphn; vd = vdn;
+        vbn = tb; vphn = tp ^ 1u; vdn = td;
+      };
+      auto pdb_bar = [&](int n) -> uint32_t { return bar(B_PDB + (n & 1)); };
+      auto pdb_par = [&](int n) -> uint32_t { return (uint32_t)(n >> 1) & 1u; };
+      // one-tile segment: S of the next key block into S buffer dbs & 1
+      auto issue_s_db = [&](uint32_t b1, uint32_t p1, uint32_t bit1, uint32_t b2, uint32_t p2, uint32_t bit2) -> bool {
+        if (!wait_seen(SEEN_K, kb, kph)) return false;
+        tc_fence_after();
+        const uint32_t sbuf = (uint32_t)dbs & 1u;
+        note(gemm_ss_k128_probe(tmem + sbuf * 128, dq0, kd, id_s, 0u, b1, p1, b2, p2), bit1, bit2);
+        mma_commit(bar(B_SDB + sbuf));
+        mma_commit(kb + 8u * NSK);  // K_EMPTY of the stage
+        k_advance();
+        ++dbs;
+        return true;
+      };
+      while (run && remaining > 0) {
+        const Unit x = decode(u);
+        const int len = min(x.nblocks - k, remaining);
+        if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+        if (x.mc == 1) {
+          // ---- one active tile: S double-buffered over both tiles' S columns, so
+          // S(n + 1) runs while the softmax warps work on S(n).  Per block: PV(n)
+          // (P(n) in buffer n & 1), then S(n + 2) into the same buffer (tensor-core
+          // operations of this thread complete in issue order).
+          if (!issue_s_db(vb, vph, SEEN_V, vb, vph, SEEN_V)) break;
+          if (len > 1 && !issue_s_db(vb, vph, SEEN_V, pdb_bar(dbp), pdb_par(dbp), SEEN_PD)) break;
           for (int i = 0; i < len; ++i) {
-            const int pbuf = np_issued & 1;
-            if (!need(pv(vn)) || !need(pp(np_issued)) ||
+            if (!wait_seen(SEEN_V, vb, vph) || !wait_seen(SEEN_PD, pdb_bar(dbp), pdb_par(dbp)) ||
                 (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
               run = false;
               break;
             }
             tc_fence_after();
-            const Probe a = (i + 2 < len) ? pk(kn) : pp(np_issued + 1), b = pv(vn + 1);
-            absorb(gemm_ts_k128_probe(tmem + TM_O, tmem + pbuf * 128, (vn % NSV) ? dv1 : dv0, id_pv, i > 0 ? 1u : 0u,
-                                      a.bar, a.par, b.bar, b.par),
-                   a, b);
+            {
+              const bool s_next = i + 2 < len;  // needed next: K for S(n + 2), else the next P
+              const uint32_t b1 = s_next ? kb : pdb_bar(dbp + 1), p1 = s_next ? kph : pdb_par(dbp + 1);
+              note(gemm_ts_k128_probe(tmem + TM_O, tmem + ((uint32_t)dbp & 1u) * 128, vd, id_pv, i > 0 ? 1u : 0u, b1,
+                                      p1, vbn, vphn),
+                   s_next ? SEEN_K : SEEN_PD, SEEN_V);
+            }
             mma_commit(bar(B_PV_DONE));
-            if (i + 1 == len) mma_commit(bar(B_SEG_DONE));
-            mma_commit(bar(B_V_EMPTY + vn % NSV));
-            ++vn;
-            ++np_issued;
-            if (i + 2 < len && !issue_s_db(pp(np_issued), pv(vn))) { run = false; break; }
+            mma_commit(vb + 8u * NSV);  // V_EMPTY of the stage
+            v_advance();
+            ++dbp;
+            if (i + 2 < len && !issue_s_db(pdb_bar(dbp), pdb_par(dbp), SEEN_PD, vb, vph, SEEN_V)) {
+              run = false;
+              break;
+            }
           }
           if (!run) break;
-          mma_commit(bar(B_Q_EMPTY));
-          ++nseg0;
-          remaining -= len;
-          ++seg;
-          ++u;
-          k = 0;
-        }
-      }
-      // Two tiles: per block, PV_0(j) S_0(j + 1) PV_1(j) S_1(j + 1).  The issue of
-      // a GEMM returns only once the tensor pipe's queue (about one MMA deep) has
-      // room, so whatever this thread does between GEMMs leaves the pipe idle:
-      // ring positions live in registers as barrier addresses, descriptors and
-      // parities, advanced by additions.
-      if constexpr (MT > 1) {
-        uint32_t kb = bar(B_K_FULL), kph = 0u;  // K ring: FULL barrier of the next key block's stage, parity
-        uint64_t kd = dk0;                      // and that stage's descriptor
-        int ks = 0;
-        uint32_t vb = bar(B_V_FULL), vph = 0u, vbn = bar(B_V_FULL + 1), vphn = 0u;  // V ring: next block, the one after
-        uint64_t vd = dv0, vdn = dv1;
-        const uint32_t pb0 = bar(B_P_FULL), pb1 = bar(B_P_FULL + 1);
-        uint32_t pph0 = 0u, pph1 = 0u;
-        constexpr uint32_t SEEN_P0 = SEEN_P, SEEN_P1 = SEEN_P << 1;
-        auto wait_seen = [&](uint32_t bit, uint32_t b, uint32_t par) -> bool {
-          if (seen & bit) {
-            seen &= ~bit;
-            return true;
-          }
-          return mbar_wait_poll(b, par, abort);
-        };
-        auto note = [&](uint32_t r, uint32_t bit_a, uint32_t bit_b) {
-          seen |= ((r & 1u) ? bit_a : 0u) | ((r & 2u) ? bit_b : 0u);
-        };
-        auto k_advance = [&]() {
-          if (ks == NSK - 1) {
-            ks = 0;
-            kb -= 8u * (NSK - 1);
-            kd -= (uint64_t)(NSK - 1) * (TILE_BYTES >> 4);
-            kph ^= 1u;
-          } else {
-            ++ks;
-            kb += 8u;
-            kd += TILE_BYTES >> 4;
-          }
-        };
-        auto v_advance = [&]() {  // two stages: the next becomes current; a stage's parity flips per use
-          const uint32_t tb = vb, tp = vph;
-          const uint64_t td = vd;
-          vb = vbn; vph = vphn; vd = vdn;
-          vbn = tb; vphn = tp ^ 1u; vdn = td;
-        };
-        while (run && remaining > 0) {
-          const Unit x = decode(u);
-          const int len = min(x.nblocks - k, remaining);
-          const bool two = x.mc > 1;
-          if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+        } else {
+          // ---- two tiles: per block, PV_0(j) S_0(j + 1) PV_1(j) S_1(j + 1)
           if (!wait_seen(SEEN_K, kb, kph)) break;
           tc_fence_after();
           note(gemm_ss_k128_probe(tmem, dq0, kd, id_s, 0u, vb, vph, vb, vph), SEEN_V, SEEN_V);
           mma_commit(bar(B_S_FULL));
-          if (two) {
-            note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, vb, vph, vb, vph), SEEN_V, SEEN_V);
-            mma_commit(bar(B_S_FULL + 1));
-          }
-          mma_commit(kb + 8u * NSK);  // K_EMPTY of the stage
+          note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, vb, vph, vb, vph), SEEN_V, SEEN_V);
+          mma_commit(bar(B_S_FULL + 1));
+          mma_commit(kb + 8u * NSK);
           k_advance();
           for (int i = 0; i < len; ++i) {
             const bool more = i + 1 < len;
             const uint32_t acc = i > 0 ? 1u : 0u;
             if (!wait_seen(SEEN_V, vb, vph)) { run = false; break; }
-            // ---- tile 0
+            // tile 0
             if (!wait_seen(SEEN_P0, pb0, pph0) ||
                 (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
               run = false;
@@ -632,54 +604,49 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             }
             tc_fence_after();
             {
-              // needed next: the key block of S_0(j + 1) (else the next V), tile 1's P (else the next V)
+              // needed next: the key block of S_0(j + 1) (else the next V), then tile 1's P
               const uint32_t b1 = more ? kb : vbn, p1 = more ? kph : vphn;
-              const uint32_t b2 = two ? pb1 : vbn, p2 = two ? pph1 : vphn;
-              note(gemm_ts_k128_probe(tmem + TM_O, tmem, vd, id_pv, acc, b1, p1, b2, p2), more ? SEEN_K : SEEN_V,
-                   two ? SEEN_P1 : SEEN_V);
+              note(gemm_ts_k128_probe(tmem + TM_O, tmem, vd, id_pv, acc, b1, p1, pb1, pph1), more ? SEEN_K : SEEN_V,
+                   SEEN_P1);
             }
             mma_commit(bar(B_PV_DONE));
             pph0 ^= 1u;
             if (more) {
               if (!wait_seen(SEEN_K, kb, kph)) { run = false; break; }
               tc_fence_after();
-              const uint32_t b1 = two ? pb1 : pb0, p1 = two ? pph1 : pph0;
-              note(gemm_ss_k128_probe(tmem, dq0, kd, id_s, 0u, b1, p1, vbn, vphn), two ? SEEN_P1 : SEEN_P0, SEEN_V);
+              note(gemm_ss_k128_probe(tmem, dq0, kd, id_s, 0u, pb1, pph1, vbn, vphn), SEEN_P1, SEEN_V);
               mma_commit(bar(B_S_FULL));
             }
-            // ---- tile 1
-            if (two) {
-              if (!wait_seen(SEEN_P1, pb1, pph1) ||
-                  (i == 0 && nseg1 > 0 && !mbar_wait_poll(bar(B_O_FREE + 1), (nseg1 - 1) & 1, abort))) {
-                run = false;
-                break;
-              }
-              tc_fence_after();
-              note(gemm_ts_k128_probe(tmem + TM_O + 128, tmem + 128, vd, id_pv, acc, pb0, pph0, vbn, vphn), SEEN_P0,
-                   SEEN_V);
-              mma_commit(bar(B_PV_DONE + 1));
-              pph1 ^= 1u;
-              if (more) {
-                note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, pb0, pph0, vbn, vphn), SEEN_P0, SEEN_V);
-                mma_commit(bar(B_S_FULL + 1));
-              }
+            // tile 1
+            if (!wait_seen(SEEN_P1, pb1, pph1) ||
+                (i == 0 && nseg1 > 0 && !mbar_wait_poll(bar(B_O_FREE + 1), (nseg1 - 1) & 1, abort))) {
+              run = false;
+              break;
             }
+            tc_fence_after();
+            note(gemm_ts_k128_probe(tmem + TM_O + 128, tmem + 128, vd, id_pv, acc, pb0, pph0, vbn, vphn), SEEN_P0,
+                 SEEN_V);
+            mma_commit(bar(B_PV_DONE + 1));
+            pph1 ^= 1u;
             if (more) {
+              note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, pb0, pph0, vbn, vphn), SEEN_P0, SEEN_V);
+              mma_commit(bar(B_S_FULL + 1));
               mma_commit(kb + 8u * NSK);
               k_advance();
             }
-            mma_commit(vb + 8u * NSV);  // V_EMPTY of the stage
+            mma_commit(vb + 8u * NSV);
             v_advance();
           }
           if (!run) break;
-          mma_commit(bar(B_Q_EMPTY));
-          ++nseg0;
-          if (two) ++nseg1;
-          remaining -= len;
-          ++seg;
-          ++u;
-          k = 0;
+          ++nseg1;
         }
+        mma_commit(bar(B_SEG_DONE));
+        mma_commit(bar(B_Q_EMPTY));
+        ++nseg0;
+        remaining -= len;
+        ++seg;
+        ++u;
+        k = 0;
       }
     }
     if (lane == 0) {
@@ -695,10 +662,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     const int q4 = warp & 3;          // TMEM lane quadrant
     const int m = q4 * 32 + lane;     // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t tS0 = tmem + lane_base + mt * 128;
     const uint32_t tO = tmem + lane_base + TM_O + mt * 128;
     const float cexp = p.scale * 1.4426950408889634f;
-    int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0, nblk = 0;
+    int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0;
+    int n2 = 0, ndb = 0;     // blocks in two-tile / one-tile units (their S / P barrier phases;
+                             // n2 + ndb = blocks of this tile = its PV_DONE phases)
     bool run = true;
     auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, abort);
@@ -714,6 +682,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         const int i = x.row0 + r_local;  // local query row in the sequence
         const bool valid = r_local < x.nvalid;
         const bool warp_active = (mt * R + (q4 * 32) / G) < x.nvalid;
+        const bool db = x.mc == 1;  // one active tile: its S is double-buffered
         const bool prompt = i < x.N;
         const int r = i - x.N;
         uint32_t tm0 = 0u, tm1 = 0u, tm2 = 0u, tm3 = 0u;  // allowed tail keys of this row
@@ -734,16 +703,18 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           }
         }
         float m_used = -INFINITY, l_sum = 0.f;
-        for (int jj = 0; jj < len; ++jj, ++nblk) {
+        for (int jj = 0; jj < len; ++jj) {
           const int j = k + jj;
-          // one tile: S alternates between two TMEM buffers (block n in buffer n & 1)
-          const int sb = (MT == 1) ? (nblk & 1) : mt;
-          const uint32_t tS = (MT == 1) ? tS0 + sb * 128 : tS0;
-          const uint32_t sparity = (MT == 1) ? ((nblk >> 1) & 1) : (nblk & 1);
-          if (!warp_wait(bar(B_S_FULL + sb), sparity)) { run = false; break; }
+          // one active tile: S alternates between two TMEM buffers (its n-th block in buffer n & 1)
+          const int sb = db ? (ndb & 1) : mt;
+          const uint32_t tS = tmem + lane_base + sb * 128;
+          const uint32_t sparity = db ? ((ndb >> 1) & 1) : (n2 & 1);
+          const int nblk = n2 + ndb;  // this tile's blocks before this one (= its PVs issued before)
+          if (db) ++ndb; else ++n2;
+          if (!warp_wait(db ? bar(B_SDB + sb) : bar(B_S_FULL + mt), sparity)) { run = false; break; }
           if (!warp_active) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+            if (lane == 0) mbar_arrive(db ? bar(B_PDB + sb) : bar(B_P_FULL + mt));
             continue;
           }
           tc_fence_after();
@@ -777,19 +748,19 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           bool done = false;
           float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
           if (all_vis && jj > 0 && __all_sync(0xffffffffu, m_used > -INFINITY)) {
-            uint32_t b0[32], b1[32], pw[64];
+            uint32_t b0[16], b1[16], pw[64];
             float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
             uint64_t lp0 = 0ull, lp1 = 0ull;  // packed (even, odd) partial sums of P
             const uint64_t cc2 = pack2(cexp, cexp), nm2 = pack2(-m_used, -m_used);
-            tmem_ld32(tS, b0);
+            tmem_ld16(tS, b0);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < BN / 32; ++q) {
+            for (int q = 0; q < BN / 16; ++q) {
               uint32_t* cur = (q & 1) ? b1 : b0;
               uint32_t* nxt = (q & 1) ? b0 : b1;
-              if (q + 1 < BN / 32) tmem_ld32(tS + (q + 1) * 32, nxt);
+              if (q + 1 < BN / 16) tmem_ld16(tS + (q + 1) * 16, nxt);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
+              for (int e = 0; e < 8; ++e) {
                 const float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
                 if ((e & 3) == 0) a0 = max3(a0, s0, s1);
                 else if ((e & 3) == 1) a1 = max3(a1, s0, s1);
@@ -799,10 +770,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                 unpack2(ffma2(pack2(s0, s1), cc2, nm2), x0, x1);
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                pw[q * 16 + e] = *reinterpret_cast<const uint32_t*>(&pb);
+                pw[q * 8 + e] = *reinterpret_cast<const uint32_t*>(&pb);
                 if (e & 1) lp1 = fadd2(lp1, pack2(p0, p1)); else lp0 = fadd2(lp0, pack2(p0, p1));
               }
-              if (q + 1 < BN / 32) tmem_wait_ld();
+              if (q + 1 < BN / 16) tmem_wait_ld();
             }
             const float mx1 = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
             if (!__any_sync(0xffffffffu, mx1 * cexp > m_used + kRescaleThreshold)) {
@@ -899,17 +870,17 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           l_sum += (l0 + l1) + (l2 + l3);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
+          if (lane == 0) mbar_arrive(db ? bar(B_PDB + sb) : bar(B_P_FULL + mt));
         }
         if (!run) break;
         // ---- segment epilogue: O stays in TMEM until O_FREE is signalled.
-        // Every PV of the segment must be complete.  Two tiles: S(j + 1) of a
-        // tile is issued after PV(j), so at most the last PV is pending here and
-        // the per-block barrier's parity is unambiguous.  One tile (S double-
-        // buffered): the last two PVs may be pending, or both done, i.e. two
-        // phases apart, which a parity wait cannot tell apart; the issuer
-        // signals the end of the segment on a barrier of its own instead.
-        if (MT == 1 ? !warp_wait(bar(B_SEG_DONE), seg & 1) : !warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) {
+        // Every PV of the segment must be complete.  Two active tiles: S(j + 1) of
+        // a tile is issued after PV(j), so at most the last PV is pending here and
+        // the per-block barrier's parity is unambiguous.  One active tile (S
+        // double-buffered): the last two PVs may be pending, or both done, i.e. two
+        // phases apart, which a parity wait cannot tell apart; the issuer signals
+        // the end of such a segment on a barrier of its own instead.
+        if (db ? !warp_wait(bar(B_SEG_DONE), seg & 1) : !warp_wait(bar(B_PV_DONE + mt), (n2 + ndb - 1) & 1)) {
           run = false;
           break;
         }
