@@ -79,8 +79,8 @@ enum : uint32_t {
   B_V_EMPTY = B_V_FULL + NSV,    // + stage
   B_S_FULL = B_V_EMPTY + NSV,    // + tile (units with two active tiles)
   B_P_FULL = B_S_FULL + 2,       // + tile
-  B_PV_DONE = B_P_FULL + 2,      // + tile
-  B_O_FREE = B_PV_DONE + 2,      // + tile
+  B_PV_DONE = B_P_FULL + 2,      // one active tile: each PV complete
+  B_O_FREE = B_PV_DONE + 1,      // + tile
   B_SDB = B_O_FREE + 2,          // + S buffer (units with one active tile)
   B_PDB = B_SDB + 2,             // + S buffer
   B_SEG_DONE = B_PDB + 2,        // every PV of the segment complete (one phase per segment)
@@ -609,7 +609,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               note(gemm_ts_k128_probe(tmem + TM_O, tmem, vd, id_pv, acc, b1, p1, pb1, pph1), more ? SEEN_K : SEEN_V,
                    SEEN_P1);
             }
-            mma_commit(bar(B_PV_DONE));
             pph0 ^= 1u;
             if (more) {
               if (!wait_seen(SEEN_K, kb, kph)) { run = false; break; }
@@ -626,7 +625,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             tc_fence_after();
             note(gemm_ts_k128_probe(tmem + TM_O + 128, tmem + 128, vd, id_pv, acc, pb0, pph0, vbn, vphn), SEEN_P0,
                  SEEN_V);
-            mma_commit(bar(B_PV_DONE + 1));
             pph1 ^= 1u;
             if (more) {
               note(gemm_ss_k128_probe(tmem + 128, dq1, kd, id_s, 0u, pb0, pph0, vbn, vphn), SEEN_P0, SEEN_V);
@@ -665,8 +663,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     const uint32_t tO = tmem + lane_base + TM_O + mt * 128;
     const float cexp = p.scale * 1.4426950408889634f;
     int u = plan->u0, k = plan->k0, remaining = end - begin, seg = 0;
-    int n2 = 0, ndb = 0;     // blocks in two-tile / one-tile units (their S / P barrier phases;
-                             // n2 + ndb = blocks of this tile = its PV_DONE phases)
+    int n2 = 0, ndb = 0;     // blocks in two-tile / one-tile units (their S / P barrier phases)
     bool run = true;
     auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
       const bool w = mbar_wait(b, parity, abort);
@@ -709,7 +706,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           const int sb = db ? (ndb & 1) : mt;
           const uint32_t tS = tmem + lane_base + sb * 128;
           const uint32_t sparity = db ? ((ndb >> 1) & 1) : (n2 & 1);
-          const int nblk = n2 + ndb;  // this tile's blocks before this one (= its PVs issued before)
           if (db) ++ndb; else ++n2;
           if (!warp_wait(db ? bar(B_SDB + sb) : bar(B_S_FULL + mt), sparity)) { run = false; break; }
           if (!warp_active) {
@@ -815,8 +811,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             const float mxs = mx * cexp;
             const bool need = (mx > -INFINITY) && (m_used == -INFINITY || mxs > m_used + kRescaleThreshold);
             if (jj > 0 && __any_sync(0xffffffffu, need)) {
-              // O holds PV of the earlier blocks: it must be complete before rescaling
-              if (!warp_wait(bar(B_PV_DONE + mt), (nblk - 1) & 1)) { run = false; break; }
+              // O holds PV of the earlier blocks: it must be complete before rescaling.
+              // Two active tiles: S(j) of a tile was issued after its PV(j - 1), so S(j)
+              // being complete implies it.  One active tile: wait for the PV of the
+              // previous block (phase ndb - 2 of the per-PV barrier, ndb counting this one).
+              if (db && !warp_wait(bar(B_PV_DONE), ndb & 1)) { run = false; break; }
               tc_fence_after();
               const float f = need ? ex2(m_used - mxs) : 1.f;
               uint32_t raw[32];
@@ -874,13 +873,9 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         }
         if (!run) break;
         // ---- segment epilogue: O stays in TMEM until O_FREE is signalled.
-        // Every PV of the segment must be complete.  Two active tiles: S(j + 1) of
-        // a tile is issued after PV(j), so at most the last PV is pending here and
-        // the per-block barrier's parity is unambiguous.  One active tile (S
-        // double-buffered): the last two PVs may be pending, or both done, i.e. two
-        // phases apart, which a parity wait cannot tell apart; the issuer signals
-        // the end of such a segment on a barrier of its own instead.
-        if (db ? !warp_wait(bar(B_SEG_DONE), seg & 1) : !warp_wait(bar(B_PV_DONE + mt), (n2 + ndb - 1) & 1)) {
+        // Every PV of the segment must be complete: the issuer commits the
+        // segment-end barrier after the segment's last MMA.
+        if (!warp_wait(bar(B_SEG_DONE), seg & 1)) {
           run = false;
           break;
         }
