@@ -113,6 +113,30 @@ struct TcWork {
   float* part_o;   // [2 * grid][MT][D / 4][128][4] unnormalised O (see part_o_at)
 };
 
+// Release increment (no return value, so no round trip) and a bounded
+// acquire poll for the per-(unit, tile, row group) arrival counters.
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits (bounded) until *p reaches `target`; false on timeout (raising *abort)
+// or when another role has raised *abort.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort) {
+  const long long t0 = clock64();
+  while (ld_acquire(p) < target) {
+    if (*abort) return false;
+    if (clock64() - t0 > ptx::kWaitBudget) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 // Float4 group c4 (columns 4 c4 .. 4 c4 + 3) of partial row `slot_row` (= tile
 // slot * 128 + row).  Column groups are outermost within a tile, so the 32
 // lanes of a warp (consecutive rows) touch 512 contiguous bytes per access.
@@ -253,16 +277,15 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       PlanHdr h;
       h.W = carryB;  // key blocks per head
       h.U = carryU;  // units per head
-      // CTAs per head: with no more units than CTAs, the same whole number per unit (each
-      // CTA owns an equal piece of one unit); otherwise an even split of the head's blocks.
-      // A unit is split only when the blocks it saves outweigh the partial merge, which
-      // costs about kMergeBlocks key blocks of time.
+      // CTAs per head: all of them, unless there are no more units than CTAs and one CTA
+      // per unit finishes sooner than spreading the head's blocks over all of them, which
+      // splits units and costs a merge (about kMergeBlocks key blocks of time).
       const int cap = max(P / p.Hkv, 1);
       int ph = cap;
       if (carryU > 0 && carryU <= cap) {
-        const int f = cap / carryU;  // CTAs per unit if split
-        const long long saved = (long long)carryB * (f - 1) / ((long long)f * carryU);  // blocks saved per unit
-        ph = (f > 1 && saved > kMergeBlocks) ? carryU * f : carryU;
+        const long long per_unit = (long long)carryB * cap;             // (blocks per unit) * U * cap
+        const long long per_cta = ((long long)carryB + (long long)kMergeBlocks * cap) * carryU;  // (...) * U * cap
+        ph = per_cta < per_unit ? cap : carryU;
       }
       ph = min(ph, max(carryB, 1));
       // every range at least one block's weight wide: no range falls between two
@@ -916,39 +939,40 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               store_chunk(q, v, inv);
             }
           } else {
-            // ---- publish this segment's partial; the 32-row group arriving last merges
+            // ---- split unit: ranks c_a .. c_b of head gh hold its pieces.  Rank c_a holds
+            // the head, which ends its range while every other piece starts its rank's
+            // range, so as a rule c_a finishes last: it merges.  The others publish their
+            // partial with a release increment and move on without waiting.
             const long long cu = unit_cost(u);
             const int c_a = owner_at(cu + kSegCost);                                   // ranks of head gh holding
             const int c_b = owner_at(cu + kSegCost + (long long)(1 + x.mc) * (x.nblocks - 1));  // the first, last block
-            // this is not rank c_a's first segment when it also owns the block before,
-            // the last of unit u - 1
-            const bool a_later = u > 0 && owner_at(cu - (1 + decode(u - 1).mc)) == c_a;
-            const int which = (seg == 0) ? 0 : 1;
-            const size_t myslot = ((size_t)(cta * 2 + which) * MT + mt) * 128 + m;
-            __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
-#pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-              uint32_t raw[32];
-              tmem_ld32(tO + q * 32, raw);
-              tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 32; c += 4)
-                __stcg(part_o_at(work.part_o, myslot, q * 8 + c / 4),
-                       make_float4(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1]), __uint_as_float(raw[c + 2]),
-                                   __uint_as_float(raw[c + 3])));
-            }
-            __threadfence();
-            __syncwarp();
-            int prev = 0;
             int32_t* counter = work.cnt + (((size_t)gh * Uh + u) * MT + mt) * 4 + q4;
-            if (lane == 0) prev = atomicAdd(counter, 1);
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev == c_b - c_a) {
-              __threadfence();
-              auto slot_of = [&](int rr) -> size_t {  // partial slot of rank rr of head gh
-                const int wh = (rr == c_a && a_later) ? 1 : 0;
-                return ((size_t)((rr * p.Hkv + gh) * 2 + wh) * MT + mt) * 128 + m;
-              };
+            // partial slot of rank rr (> c_a): its piece is the first segment of its range
+            auto slot_of = [&](int rr) -> size_t { return ((size_t)((rr * p.Hkv + gh) * 2) * MT + mt) * 128 + m; };
+            if (rank != c_a) {
+              const size_t myslot = slot_of(rank);
+              __stcg(reinterpret_cast<float2*>(work.part_ml + myslot * 2), make_float2(m_used, l_sum));
+#pragma unroll 1
+              for (int q = 0; q < D / 32; ++q) {
+                uint32_t raw[32];
+                tmem_ld32(tO + q * 32, raw);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                  __stcg(part_o_at(work.part_o, myslot, q * 8 + c / 4),
+                         make_float4(__uint_as_float(raw[c]), __uint_as_float(raw[c + 1]),
+                                     __uint_as_float(raw[c + 2]), __uint_as_float(raw[c + 3])));
+              }
+              __syncwarp();  // every lane's stores precede lane 0's release
+              if (lane == 0) red_release_add(counter, 1);
+            } else {
+              int ok = 1;
+              if (lane == 0) ok = wait_count(counter, c_b - c_a, abort) ? 1 : 0;
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              __syncwarp();  // the other lanes' loads below follow lane 0's acquire
+              if (!ok) run = false;
+            }
+            if (rank == c_a && run) {
               // combine in CTA order (not arrival order) so the result is deterministic
               const int nparts = c_b - c_a + 1;
               if (nparts <= 4) {
