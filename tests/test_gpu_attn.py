@@ -40,14 +40,18 @@ def test_attn_small(name, out):
     compare_attn(got, ref, out == "bf16", a.dtype == W.F32)
 
 
-# Units split across CTAs (partials merged by the last-arriving 32-row group):
-# in two (8 units per kv head over 19 CTAs), in three, and across every CTA
-# of a head (one long unit per head: more than four partials).
+# Units split across CTAs (partials merged by the rank holding each unit's
+# head): in two and three pieces, across every CTA of a head (one long unit
+# per head, more than four partials) with one M-tile and with two, and a mix
+# of one-tile (S double-buffered) and two-tile units, split, in one launch.
 SPLIT = {
     "split2": lambda: W.make_attn_inputs("s", [4096] * 8, [0] * 8, [8] * 8, 16, 8, 128, W.BF16, 41),
     "split3": lambda: W.make_attn_inputs("s", [3000, 3100, 2900, 3333, 3050], [0] * 5, [4, 8, 2, 16, 4], 8, 8, 128,
                                          W.BF16, 42),
     "split_many": lambda: W.make_attn_inputs("s", [8192], [0], [16], 32, 8, 128, W.BF16, 43),
+    "split_many_two_tiles": lambda: W.make_attn_inputs("s", [16384], [0], [32], 32, 8, 128, W.BF16, 44),
+    "mixed_tiles_split": lambda: W.make_attn_inputs("s", [2500, 700, 4100, 1900, 3000, 130], [0, 0, 40, 0, 0, 0],
+                                                    [32, 4, 16, 32, 8, 24], 32, 8, 128, W.BF16, 45),
 }
 
 
