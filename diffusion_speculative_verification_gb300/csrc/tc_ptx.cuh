@@ -153,76 +153,20 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, fp32 accumulate)
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A (M x K, 16-bit) sits in
-// TMEM: row m in lane m, two elements per 32-bit column.
-__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// One 128 x N x 128 GEMM as 8 MMAs of K = 16, both operands K-major SW128 in
-// shared memory: step kk reads byte offset (kk / 4) * 16384 + (kk % 4) * 32 of
-// each operand (descriptor units of 16 B: 1024 per atom column, 2 per step).
-// The first step accumulates iff `accumulate`, the others always.
-__device__ __forceinline__ void gemm_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t.reg .b64 a, b;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-      "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, q;\n\t"
-      "}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// One 128 x N x 128 GEMM with A (16-bit, M x K) in TMEM and B MN-major SW128
-// in shared memory: step kk reads A columns a_tmem + 8 kk and B rows
-// [16 kk, 16 kk + 16), byte offset 2048 kk (128 descriptor units).
-__device__ __forceinline__ void gemm_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t.reg .b32 a;\n\t.reg .b64 b;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 q, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, q;\n\t"
-      "}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The two GEMMs above with two barrier probes folded in: after the sixth MMA
-// they test, without waiting, whether the phase of parity par1 of barrier
-// bar1 and that of parity par2 of bar2 have completed (bits 0 and 1 of the
-// result).  An MMA issue stalls while the tensor pipe's queue (about one MMA
-// deep) is full, so the tests' latency overlaps the GEMM's last steps
-// instead of leaving the pipe idle after it.
+// One 128 x N x 128 GEMM, D[tmem] (+)= A * B, kind::f16 (bf16 in, fp32
+// accumulate), as 8 MMAs of K = 16; the first step accumulates iff
+// `accumulate`, the others always.
+//   gemm_ss_k128_probe: A and B K-major SW128 in shared memory; step kk reads
+//     byte offset (kk / 4) * 16384 + (kk % 4) * 32 of each operand (descriptor
+//     units of 16 B: 1024 per atom column, 2 per step).
+//   gemm_ts_k128_probe: A (16-bit, M x K) in TMEM, row m in lane m, two
+//     elements per 32-bit column; B MN-major SW128 in shared memory; step kk
+//     reads A columns a_tmem + 8 kk and B rows [16 kk, 16 kk + 16), byte
+//     offset 2048 kk (128 descriptor units).
+// Both fold in two barrier probes: after the sixth MMA they test, without
+// waiting, whether the phase of parity par1 of barrier bar1 and that of
+// parity par2 of bar2 have completed (bits 0 and 1 of the result), so the
+// tests' latency overlaps the GEMM's last steps.
 #define SSV_MMA_SS(OA, OB)                                                                   \
   "add.s64 a, %3, " #OA ";\n\tadd.s64 b, %4, " #OB                                           \
   ";\n\ttcgen05.mma.cta_group::1.kind::f16 [%2], a, b, %5, q;\n\t"
