@@ -149,6 +149,11 @@ SSV_API ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream);
  * size grids and workspace).  scale 0 means 1/sqrt(d).
  * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_WORKSPACE,
  *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU, SSV_ERR_TIMEOUT.
+ * Scheduling: the bf16 path launches one CTA per SM; where a unit of work is
+ * split across CTAs, the CTA holding its first key block waits (bounded, about
+ * one second of SM clock) for the others' partial results.  Work on other
+ * streams that keeps SMs busy for longer than that while this kernel runs can
+ * therefore end the call with SSV_ERR_TIMEOUT (never a hang).
  * ---------------------------------------------------------------------- */
 typedef struct {
   const void* q;
