@@ -713,10 +713,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           const int tb = lane + 32 < x.B ? tau[lane + 32] : 0;
           const bool tail_row = valid && !prompt;
           const int slot_r = tail_row ? (r % x.B) : 0;
-          const int tr = __shfl_sync(0xffffffffu, slot_r < 32 ? ta : tb, slot_r & 31);
+          // the stage of this lane's own slot: fetch both halves from the holding lane and
+          // choose here (a choice made inside the shuffle would use the source lane's slot)
+          const int tra = __shfl_sync(0xffffffffu, ta, slot_r & 31), trb = __shfl_sync(0xffffffffu, tb, slot_r & 31);
+          const int tr = slot_r < 32 ? tra : trb;
           for (int tk = 0; tk < 2 * x.B; ++tk) {
             const int sk = tk % x.B;
-            const int tt = __shfl_sync(0xffffffffu, sk < 32 ? ta : tb, sk & 31);
+            const int tt = __shfl_sync(0xffffffffu, sk < 32 ? ta : tb, sk & 31);  // sk: the same on every lane
             if (!tail_row || !tail_allowed(r, tk, x.B, tr, tt)) continue;
             const uint32_t bit = 1u << (tk & 31);
             if (tk < 32) tm0 |= bit; else if (tk < 64) tm1 |= bit; else if (tk < 96) tm2 |= bit; else tm3 |= bit;

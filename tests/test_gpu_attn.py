@@ -23,6 +23,8 @@ SMALL = {
     "mha_prefill_small": lambda: W.make_attn_inputs("r", [0, 64], [300, 129], [16, 2], 4, 4, 128, W.BF16, 34),
     "f32_multi": lambda: W.make_attn_inputs("r", [33, 0, 200], [0, 20, 7], [4, 1, 9], 4, 2, 64, W.F32, 35),
     "empty_cache_B1": lambda: W.make_attn_inputs("r", [0], [0], [1], 2, 1, 128, W.BF16, 36),
+    # B > 32 with warps whose tail rows straddle stage slot 32 (G = 4: 8 rows a warp)
+    "tail_B33_B47": lambda: W.make_attn_inputs("r", [0, 100], [0, 0], [33, 47], 16, 4, 128, W.BF16, 46),
 }
 
 
@@ -60,6 +62,26 @@ def test_attn_split_units(name):
     a = SPLIT[name]()
     got, ref, _ = gpu_verify(a, out_dtype="bf16")
     compare_attn(got, ref, True, False)
+
+
+def _random_shape(seed):
+    """Seeded random batch: group size, tail widths, ragged caches and prompts,
+    so that the plan's ranges, one- and two-tile units and split units vary."""
+    rng = np.random.default_rng(seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    batch = int(rng.integers(1, 9))
+    cache = [int(rng.choice([0, rng.integers(1, 400), rng.integers(400, 3000)])) for _ in range(batch)]
+    new = [int(rng.choice([0, 0, rng.integers(1, 300)])) for _ in range(batch)]
+    blocks = [int(rng.integers(1, 65)) for _ in range(batch)]
+    return W.make_attn_inputs("r", cache, new, blocks, G * Hkv, Hkv, 128, W.BF16, 1000 + seed)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_attn_random_shapes(seed):
+    a = _random_shape(seed)
+    got, ref, _ = gpu_verify(a, out_dtype="f32")
+    compare_attn(got, ref, False, False)
 
 
 @pytest.mark.parametrize("name", ["gqa1p7b", "gqa8b", "sweep"])
