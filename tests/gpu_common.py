@@ -112,3 +112,20 @@ def compare_accept(x: W.AcceptInputs, got):
             else:
                 assert have == want, f"seq {b}: emitted {have} vs {want}"
     return differ
+
+
+def random_attn_shape(seed, dtype=None, d=128):
+    """Seeded random batch: group size, tail widths (1..64), ragged caches and
+    prompts, so that plans, one- and two-tile units, split units and warps whose
+    rows straddle stage slot 32 vary from seed to seed."""
+    import numpy as np
+    from diffusion_speculative_verification_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8]))
+    batch = int(rng.integers(1, 9))
+    cache = [int(rng.choice([0, rng.integers(1, 400), rng.integers(400, 3000)])) for _ in range(batch)]
+    new = [int(rng.choice([0, 0, rng.integers(1, 300)])) for _ in range(batch)]
+    blocks = [int(rng.integers(1, 65)) for _ in range(batch)]
+    return W.make_attn_inputs("r", cache, new, blocks, G * Hkv, Hkv, d, W.BF16 if dtype is None else dtype,
+                              1000 + seed)

@@ -10,7 +10,8 @@ import pytest
 import torch
 
 from diffusion_speculative_verification_gb300 import workloads as W, ssv
-from gpu_common import ensure_built, gpu_accept, compare_accept
+from gpu_common import ensure_built, gpu_accept, compare_accept, REJECT_MARGIN
+import oracle.accept as oacc
 
 pytestmark = pytest.mark.gpu
 
@@ -152,3 +153,29 @@ def test_bad_noise_row_reports_status(V):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     gpu_accept(x, dev_status=st)
     assert ssv.get_status(st) == ssv.SSV_ERR_INVALID
+
+
+def _random_accept(seed):
+    """Seeded random batch: mode and temperature, vocabulary size (rows 16-byte
+    aligned or not), 1..12 sequences with B in 1..64 and gamma in 0..B, fp32 or
+    bf16 logits."""
+    rng = np.random.default_rng(seed)
+    mode = int(rng.choice([W.MODE_ARGMAX, W.MODE_GUMBEL, W.MODE_REJECT]))
+    T = {W.MODE_ARGMAX: 0.0, W.MODE_GUMBEL: float(rng.choice([0.0, 0.7, 1.0, 1.5])),
+         W.MODE_REJECT: float(rng.choice([0.7, 1.0, 1.3]))}[mode]
+    V = int(rng.choice([int(rng.integers(1, 3000)), int(rng.integers(3000, 40000)), 8 * int(rng.integers(500, 5000))]))
+    batch = int(rng.integers(1, 13))
+    blocks = [int(rng.integers(1, 65)) for _ in range(batch)]
+    gammas = [int(rng.integers(0, b + 1)) for b in blocks]
+    dt = W.BF16 if rng.random() < 0.3 else W.F32
+    return W.make_accept_inputs(f"random{seed}", mode, T, V, blocks, gammas, seed=3000 + seed, logits_dtype=dt)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_accept_random(seed):
+    x = _random_accept(seed)
+    if x.mode == W.MODE_REJECT:
+        margins = [m for r in oacc.accept_batch(x)["results"] for m in r.accept_margins]
+        if margins and min(margins) <= REJECT_MARGIN:
+            pytest.skip("a decision lies inside the fp32 rounding band for this seed")
+    compare_accept(x, gpu_accept(x))

@@ -11,7 +11,7 @@ import torch
 
 from diffusion_speculative_verification_gb300 import workloads as W, ssv, io as sio
 import oracle.attention as oattn
-from gpu_common import ensure_built, gpu_verify, compare_attn
+from gpu_common import ensure_built, gpu_verify, compare_attn, random_attn_shape
 
 pytestmark = pytest.mark.gpu
 
@@ -64,24 +64,19 @@ def test_attn_split_units(name):
     compare_attn(got, ref, True, False)
 
 
-def _random_shape(seed):
-    """Seeded random batch: group size, tail widths, ragged caches and prompts,
-    so that the plan's ranges, one- and two-tile units and split units vary."""
-    rng = np.random.default_rng(seed)
-    Hkv = int(rng.choice([1, 2, 4, 8]))
-    G = int(rng.choice([1, 2, 4, 8]))
-    batch = int(rng.integers(1, 9))
-    cache = [int(rng.choice([0, rng.integers(1, 400), rng.integers(400, 3000)])) for _ in range(batch)]
-    new = [int(rng.choice([0, 0, rng.integers(1, 300)])) for _ in range(batch)]
-    blocks = [int(rng.integers(1, 65)) for _ in range(batch)]
-    return W.make_attn_inputs("r", cache, new, blocks, G * Hkv, Hkv, 128, W.BF16, 1000 + seed)
-
-
 @pytest.mark.parametrize("seed", range(8))
 def test_attn_random_shapes(seed):
-    a = _random_shape(seed)
+    a = random_attn_shape(seed)
     got, ref, _ = gpu_verify(a, out_dtype="f32")
     compare_attn(got, ref, False, False)
+
+
+# fp32 inputs (exact SIMT path), head dims 64 and 128
+@pytest.mark.parametrize("seed", range(4))
+def test_attn_random_shapes_f32(seed):
+    a = random_attn_shape(100 + seed, W.F32, 64 if seed % 2 else 128)
+    got, ref, _ = gpu_verify(a)
+    compare_attn(got, ref, False, True)
 
 
 @pytest.mark.parametrize("name", ["gqa1p7b", "gqa8b", "sweep"])

@@ -13,7 +13,7 @@ import pytest
 
 from diffusion_speculative_verification_gb300 import workloads as W, io as sio
 import oracle.rope as orope
-from gpu_common import ensure_built, gpu_rope, bf16_ulp
+from gpu_common import ensure_built, gpu_rope, bf16_ulp, random_attn_shape
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +24,9 @@ CASES = {
     "f32_d128": lambda: W.make_attn_inputs("r", [9000, 3], [3, 0], [64, 2], 4, 2, 128, W.F32, 23),
     "gqa1p7b": lambda: W.workload_attn("gqa1p7b"),
     "prefill": lambda: W.workload_attn("prefill"),
+    "random_bf16_a": lambda: random_attn_shape(200),
+    "random_bf16_b": lambda: random_attn_shape(201, W.BF16, 64),
+    "random_f32": lambda: random_attn_shape(202, W.F32, 128),
 }
 
 
