@@ -7,7 +7,7 @@ import torch
 
 from diffusion_speculative_verification_gb300 import workloads as W, ssv, io as sio
 import oracle.attention as oattn
-from gpu_common import ensure_built, compare_attn, compare_accept
+from gpu_common import ensure_built, compare_attn, compare_accept, random_attn_shape
 
 pytestmark = pytest.mark.gpu
 
@@ -90,3 +90,31 @@ def test_step_without_rotation_or_acceptance():
     assert ssv.lib().ssv_verify_attn(C.byref(aa2), wa.data_ptr(), wa.numel(), None) == 0
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
+
+
+def _prepare_random(seed):
+    """Random batch (shared generator) with coupled-noise acceptance over the
+    same sequences and stage maps."""
+    a = random_attn_shape(300 + seed)
+    blocks = [int(s[2]) for s in a.seqs]
+    rng = np.random.default_rng(seed)
+    gammas = [int(rng.integers(0, b + 1)) for b in blocks]
+    x = W.make_accept_inputs(f"step{seed}", W.MODE_GUMBEL, 1.0, 4000 + 8 * seed, blocks, gammas, seed=4000 + seed,
+                             tau=a.tau)
+    return a, x, sio.attn_to_device(a), sio.accept_to_device(x)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_step_random_against_separate_calls_and_oracle(seed):
+    a, x, t, acc = _prepare_random(seed)
+    o_f, r_f, (qo, ko) = _run(a, x, t, acc, True)
+    o_s, r_s, _ = _run(a, x, t, acc, False)
+    assert np.array_equal(o_f, o_s)
+    for u, v in zip(r_f, r_s):
+        assert np.array_equal(u, v)
+    q64 = W.values_f64(sio.to_numpy_storage(qo), a.dtype)
+    k64 = W.values_f64(sio.to_numpy_storage(ko), a.dtype)
+    ref = oattn.verify_attention(a.seqs, a.tau, q64, W.values_f64(a.k_cache, a.dtype),
+                                 W.values_f64(a.v_cache, a.dtype), k64, W.values_f64(a.v_new, a.dtype))
+    compare_attn(o_f.astype(np.float64), ref, False, False)
+    compare_accept(x, r_f)
