@@ -25,6 +25,9 @@ SMALL = {
     "empty_cache_B1": lambda: W.make_attn_inputs("r", [0], [0], [1], 2, 1, 128, W.BF16, 36),
     # B > 32 with warps whose tail rows straddle stage slot 32 (G = 4: 8 rows a warp)
     "tail_B33_B47": lambda: W.make_attn_inputs("r", [0, 100], [0, 0], [33, 47], 16, 4, 128, W.BF16, 46),
+    # large query groups: an M-tile holds 4 query rows x 32 heads, or 1 row x 128 heads
+    "group32": lambda: W.make_attn_inputs("r", [700, 0, 129], [0, 40, 3], [8, 5, 16], 64, 2, 128, W.BF16, 47),
+    "group128": lambda: W.make_attn_inputs("r", [300, 1], [7, 0], [3, 2], 128, 1, 128, W.BF16, 48),
 }
 
 
@@ -77,6 +80,18 @@ def test_attn_random_shapes_f32(seed):
     a = random_attn_shape(100 + seed, W.F32, 64 if seed % 2 else 128)
     got, ref, _ = gpu_verify(a)
     compare_attn(got, ref, False, True)
+
+
+def test_attn_plan_tables_in_workspace():
+    """130 sequences with two M-tiles: the per-sequence plan tables exceed the
+    shared memory left by the pipeline and live in the workspace."""
+    rng = np.random.default_rng(49)
+    n = 130
+    cache = [int(v) for v in rng.integers(0, 600, size=n)]
+    blocks = [32 if i % 7 == 0 else int(rng.integers(1, 17)) for i in range(n)]
+    a = W.make_attn_inputs("r", cache, [0] * n, blocks, 32, 8, 128, W.BF16, 49)
+    got, ref, _ = gpu_verify(a, out_dtype="bf16")
+    compare_attn(got, ref, True, False)
 
 
 @pytest.mark.parametrize("name", ["gqa1p7b", "gqa8b", "sweep"])
