@@ -218,7 +218,9 @@ accept_reduce_kernel(const AcceptParams p) {
     out.val = 0.f; out.idx = 0;
   }
   if (tid == 0) p.part[(size_t)slot * p.nchunks + chunk] = out;
-  if (tid < 32) warp_rows_done<MODE, T>(p, b, slot, 1, s_walk);
+  if (tid < 32)
+    warp_rows_done<MODE, T>(p, b, slot, 1, __ldcg(&p.tau[slot]), p.slot_off[b], p.block[b], p.gamma[b], s_walk,
+                            nullptr);
 }
 
 // ---- rejection sampling: emitted token ------------------------------------

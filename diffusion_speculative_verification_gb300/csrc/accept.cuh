@@ -278,18 +278,20 @@ struct WalkSmem {
   int tok[64];   // per stage: draft token
 };
 
-// Walk of sequence b once every verified row is merged: one round of loads
-// (stage map, row results, draft tokens), rearranged into stage order.
+// Walk of sequence b (slots off .. off + B - 1, draft length g) once every
+// verified row is merged: one round of loads (row results, draft tokens, and
+// the stage map unless the caller holds it in shared memory as stage_s, one
+// byte per slot), rearranged into stage order.
 template <int MODE>
-__device__ void warp_seq_walk(const AcceptParams& p, int b, WalkSmem& w) {
+__device__ void warp_seq_walk(const AcceptParams& p, int b, int off, int B, int g, WalkSmem& w,
+                              const unsigned char* stage_s) {
   const int lane = threadIdx.x & 31;
-  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
   const int need = min(g + 1, B);
   int st[2], rok[2], rdec[2], dtok[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int j = lane + 32 * h;
-    st[h] = (j < B) ? __ldcg(&p.tau[off + j]) : 0;
+    st[h] = (j < B) ? (stage_s ? (int)stage_s[off + j] : __ldcg(&p.tau[off + j])) : 0;
     dtok[h] = (j < B) ? p.draft_tokens[off + j] : -1;
     const int2 r = (j < B) ? __ldcg(reinterpret_cast<const int2*>(p.rowres + off + j)) : make_int2(0, -1);
     rok[h] = r.x;
@@ -333,17 +335,18 @@ __device__ void warp_seq_walk(const AcceptParams& p, int b, WalkSmem& w) {
   __syncwarp();
 }
 
-// `add` more chunk records of row `slot` (sequence b) are written by lane 0:
-// run the row merge and the sequence walk when they complete the counts.
+// `add` more chunk records of row `slot` (stage st of sequence b, whose slots
+// start at off; block B, draft length g) are written by lane 0: run the row
+// merge and the sequence walk when they complete the counts.  stage_s: the
+// stage map in shared memory (one byte per slot), or null.
 template <int MODE, typename T>
-__device__ void warp_rows_done(const AcceptParams& p, int b, int slot, int add, WalkSmem& w) {
+__device__ void warp_rows_done(const AcceptParams& p, int b, int slot, int add, int st, int off, int B, int g,
+                               WalkSmem& w, const unsigned char* stage_s) {
   if (!warp_arrive(&p.cnt_row[slot], add, p.nchunks)) return;
-  const int B = p.block[b], g = p.gamma[b];
-  const int st = __ldcg(&p.tau[slot]);
   warp_row_merge<MODE, T>(p, slot, st, g);
   if ((threadIdx.x & 31) == 0 && add != p.nchunks) p.cnt_row[slot] = 0;
   if (!warp_arrive(&p.cnt_seq[b], 1, min(g + 1, B))) return;
-  warp_seq_walk<MODE>(p, b, w);
+  warp_seq_walk<MODE>(p, b, off, B, g, w, stage_s);
   if ((threadIdx.x & 31) == 0 && min(g + 1, B) != 1) p.cnt_seq[b] = 0;
 }
 

@@ -368,6 +368,11 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   }
 
   // ---- publisher warp
+  // completion of `add` records of row `slot`, with the metadata from shared memory
+  auto rows_done = [&](int slot, int add) {
+    const int b = seq_of_slot(sh, p.batch, slot);
+    warp_rows_done<MODE, T>(p, b, slot, add, sh.stage[slot], sh.off[b], sh.blk[b], sh.gam[b], sh.walk, sh.stage);
+  };
   int cur_row = -1, cur_slot = 0, pend = 0;
   bool clean = true;
   for (int k = 0; k < n; ++k) {
@@ -402,14 +407,14 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     const int slot = sh.list[row] & 0x7fffffff;
     if (lane == 0) p.part[(size_t)slot * p.nchunks + chunk] = x;
     if (row != cur_row) {
-      if (pend) warp_rows_done<MODE, T>(p, seq_of_slot(sh, p.batch, cur_slot), cur_slot, pend, sh.walk);
+      if (pend) rows_done(cur_slot, pend);
       cur_row = row;
       cur_slot = slot;
       pend = 0;
     }
     ++pend;
   }
-  if (clean && pend) warp_rows_done<MODE, T>(p, seq_of_slot(sh, p.batch, cur_slot), cur_slot, pend, sh.walk);
+  if (clean && pend) rows_done(cur_slot, pend);
 }
 
 int device_sm_count() {
