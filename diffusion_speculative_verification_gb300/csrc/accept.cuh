@@ -212,6 +212,10 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
   // Rejection sampling: per lane a running (max, sum) over its chunks in
   // fp64, then a max / rescaled-sum butterfly across the warp.  Lane 0 loads
   // the draft token's two logits while the chunk records are in flight.
+  // Scale factors 2^((m - M) c2) are fp32 exp2 of an fp64-formed argument
+  // (about 5e-7 relative, the order of the chunk sums' own exp2 rounding):
+  // FP64 is a small fraction of FP32 on this part and a chain of fp64 exp2
+  // calls cost microseconds at the tail of the kernel.
   int d = -1;
   double ld = 0.0, qd = 0.0;
   float ua = 0.f;
@@ -225,16 +229,17 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
   }
   const double c2 = (double)p.c2;
   double ma = -INFINITY, mb = -INFINITY, sa = 0.0, sb = 0.0;
+  auto scale = [&](double x) -> double { return (double)exp2f((float)(x * c2)); };  // 2^(x c2), x <= 0
   for (int c = lane; c < p.nchunks; c += 32) {
     const double cma = __ldcg(&pp[c].m_a);
     const double csa = (double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo);
-    if (cma > ma) { sa = (ma == -INFINITY) ? 0.0 : sa * exp2((ma - cma) * c2); ma = cma; }
-    if (cma > -INFINITY) sa += csa * exp2((cma - ma) * c2);
+    if (cma > ma) { sa = (ma == -INFINITY) ? 0.0 : sa * scale(ma - cma); ma = cma; }
+    if (cma > -INFINITY) sa += (cma == ma) ? csa : csa * scale(cma - ma);
     if (tested) {
       const double cmb = __ldcg(&pp[c].m_b);
       const double csb = (double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo);
-      if (cmb > mb) { sb = (mb == -INFINITY) ? 0.0 : sb * exp2((mb - cmb) * c2); mb = cmb; }
-      if (cmb > -INFINITY) sb += csb * exp2((cmb - mb) * c2);
+      if (cmb > mb) { sb = (mb == -INFINITY) ? 0.0 : sb * scale(mb - cmb); mb = cmb; }
+      if (cmb > -INFINITY) sb += (cmb == mb) ? csb : csb * scale(cmb - mb);
     }
   }
   double Ma = ma, Mb = mb;
@@ -243,8 +248,8 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
     Ma = fmax(Ma, __shfl_xor_sync(0xffffffffu, Ma, o));
     Mb = fmax(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
   }
-  sa = (ma == -INFINITY) ? 0.0 : sa * exp2((ma - Ma) * c2);
-  sb = (mb == -INFINITY) ? 0.0 : sb * exp2((mb - Mb) * c2);
+  sa = (ma == -INFINITY) ? 0.0 : (ma == Ma ? sa : sa * scale(ma - Ma));
+  sb = (mb == -INFINITY) ? 0.0 : (mb == Mb ? sb : sb * scale(mb - Mb));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     sa += __shfl_xor_sync(0xffffffffu, sa, o);
@@ -260,7 +265,7 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
     if (tested) {
       if (d >= 0 && d < p.V) {
         // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
-        const double ratio = exp2(((ld - Ma) - (qd - Mb)) * c2) * (sb / sa);
+        const double ratio = (double)exp2f((float)(((ld - Ma) - (qd - Mb)) * c2)) * (sb / sa);
         rr.ok = (double)ua < ratio;
       } else {
         report(p.dev_status, SSV_ERR_INVALID);
