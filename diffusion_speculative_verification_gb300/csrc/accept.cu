@@ -243,12 +243,17 @@ accept_sample_kernel(const AcceptParams p) {
   const int chunk = blockIdx.x % p.nchunks;
   const int tid = threadIdx.x;
   // A sequence whose stage map or sizes were rejected never ran its finalize
-  // step, so its emission record may be stale: skip it.
+  // step, so its emission record may be stale: skip it.  The check reads only
+  // the call's inputs, so it runs while the reduce kernel finishes (this kernel
+  // is launched as its programmatic dependent; the reduce kernel lets it start
+  // only after every kernel before the acceptance has completed).
   if (tid < 32) {
     const bool ok = warp_seq_valid(p, b);
     if (tid == 0) s_ok = ok;
   }
   __syncthreads();
+  pdl_wait();  // emission records, accepted lengths and row normalisers
+  pdl_trigger();
   if (!s_ok) return;
   const int eslot = p.emit[2 * b];
   const int soff = p.slot_off[b];
@@ -256,8 +261,10 @@ accept_sample_kernel(const AcceptParams p) {
   if (eslot < soff || eslot >= soff + p.block[b] || nacc < 0 || nacc >= p.block[b]) return;
   const bool residual = p.emit[2 * b + 1] != 0;
   const SlotNorm nm = p.norm[eslot];
-  const float inv_sa = (float)(1.0 / nm.s_a);
-  const float inv_sb = residual ? (float)(1.0 / nm.s_b) : 0.f;
+  // fp32 reciprocals (an fp64 division is slow on this part; a relative error
+  // of 1e-7 in a row's normaliser moves the sampling threshold by as much)
+  const float inv_sa = 1.f / (float)nm.s_a;
+  const float inv_sb = residual ? 1.f / (float)nm.s_b : 0.f;
   const float nma = -nm.m_a * p.c2, nmb = -nm.m_b * p.c2;
   const size_t rbase = (size_t)eslot * p.V;
   const int c0 = chunk * kAccChunk;
@@ -424,9 +431,8 @@ static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaS
   if (e != cudaSuccess || mode != SSV_ACCEPT_REJECT) return e;
   const long long g2 = (long long)p.batch * p.nchunks;
   if (g2 > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (bf) accept_sample_kernel<__nv_bfloat16><<<(unsigned)g2, kAccThreads, 0, st>>>(p);
-  else accept_sample_kernel<float><<<(unsigned)g2, kAccThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  if (bf) return launch_pdl(accept_sample_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+  return launch_pdl(accept_sample_kernel<float>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
 }
 
 }  // namespace ssv
