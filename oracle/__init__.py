@@ -20,6 +20,10 @@ What it computes, plainly and slowly, in float64 (numpy):
                               rejection sampling, longest accepted prefix
                               (SimSD summary section 4 "Acceptance"; SPOT review,
                               section "How it is used").
+* ``commit.commit_batch``     the pass's commit into the KV cache: fresh prompt
+                              rows, then the accepted data rows in stage order
+                              (SimSD summary section 4 "Acceptance", the longest
+                              accepted prefix is committed; reading for the layout).
 
 Pins (``tests/test_oracle_*.py``, marked ``not gpu``) tie each function to
 something other than itself: a hand-worked mask from the rule's text, mask
