@@ -78,6 +78,14 @@ def accept_bytes(x) -> float:
     return tot
 
 
+def commit_bytes(a: W.AttnInputs, n_acc) -> float:
+    """K and V rows read and written by the commit step: per sequence its N
+    fresh prompt rows and n_acc accepted data rows."""
+    es = 2 if a.dtype == W.BF16 else 4
+    rows = float(np.sum(a.seqs[:, 1].astype(np.int64) + np.asarray(n_acc, np.int64)))
+    return 2.0 * 2.0 * rows * a.Hkv * a.d * es
+
+
 def aggregate_ms(local_ms: float, dist_mod=None, device=None) -> float:
     """Max over ranks of a per-rank time (identity on one rank)."""
     if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
@@ -97,11 +105,13 @@ def kernel_launches(x) -> int:
     return n
 
 
-KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel"}
+KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel",
+                "commit": "commit_kernel"}
 KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"],
                   "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh"],
                   "accept_reduce_kernel": ["accept.cu", "accept.cuh"],
-                  "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"]}
+                  "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"],
+                  "commit_kernel": ["commit.cu"]}
 
 
 def measured_traffic(op: str, workload: str):
@@ -340,6 +350,14 @@ def run_ours(args):
                                 acc["gamma"], acc["slot_off"], *outs, acc["draft_logits"], acc["noise"],
                                 acc["noise_row"], acc["u_accept"], acc["u_sample"], acc["max_block"], status)
         ws_acc = torch.zeros(ssv.accept_workspace_bytes(cargs), dtype=torch.uint8, device=dev)
+    # commit step (timed on its own, not part of the step): the rotated fresh
+    # rows into destination caches laid out with room, seeded accepted counts
+    n_acc_c, dst_off, dst_cap, dst_rows, _ = W.commit_layout(a, 2024)
+    k_dst = torch.zeros((dst_rows, a.Hkv, a.d), dtype=ko.dtype, device=dev)
+    v_dst = torch.zeros_like(k_dst)
+    commit_in = [sio.int_tensor(v, dev) for v in (n_acc_c, dst_off, dst_cap)]
+    new_len = torch.empty(a.batch, dtype=torch.int32, device=dev)
+    margs = ssv.commit_args(ko, t["v_new"], k_dst, v_dst, batch, t["tau"], *commit_in, new_len, status)
     # L2 flush between steps: a 256 MB read (twice the 129 MB L2) leaves only
     # clean lines of an unrelated buffer, so no step inherits its inputs in L2
     # and no write-back of dirty flush lines lands inside a measured step.
@@ -366,6 +384,11 @@ def run_ours(args):
             if r:
                 raise ssv.SsvError(r, "ssv_accept")
 
+    def op_commit(s):
+        r = L.ssv_commit(C.byref(margs), s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_commit")
+
     OPS = (op_rope, op_attn, op_accept)
     rargs = ssv.rope_args(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko)
 
@@ -388,6 +411,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         l2_flush()
         step()
+        op_commit(stream)
     torch.cuda.synchronize()
     assert ssv.get_status(status) == ssv.SSV_OK
 
@@ -417,7 +441,7 @@ def run_ours(args):
     graphs = None
     if launch == "cuda_graph":
         graphs = {"step": capture((op_step,)), "flush": capture(()), "rope": capture((op_rope,)),
-                  "verify_attn": capture((op_attn,))}
+                  "verify_attn": capture((op_attn,)), "commit": capture((op_commit,))}
         if acc is not None:
             graphs["accept"] = capture((op_accept,))
         torch.cuda.synchronize()
@@ -451,6 +475,7 @@ def run_ours(args):
         op_ms = np.array([(timed_replay(graphs[k]) - t_flush) / args.steps if k in graphs else 0.0
                           for k in ("rope", "verify_attn", "accept")])
         step_total = t_step - t_flush
+        commit_ms = (timed_replay(graphs["commit"]) - t_flush) / args.steps
     else:
         events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
@@ -461,6 +486,14 @@ def run_ours(args):
         per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
         op_ms = per.mean(axis=0)
         step_total = float(per.sum())
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+        for i in range(args.steps):
+            l2_flush()
+            ev[2 * i].record(stream)
+            op_commit(stream)
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        commit_ms = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]))
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if rank == 0 else None
@@ -470,6 +503,7 @@ def run_ours(args):
     rb = rope_bytes(a)
     ab, af = attn_work(a, out_b)
     cb = accept_bytes(x)
+    mb = commit_bytes(a, n_acc_c)
     step_bytes = rb + ab + cb
     ms_step = tot_ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
@@ -504,6 +538,10 @@ def run_ours(args):
             "accept": None if x is None else {"us": round(op_ms[2] * 1e3, 2),
                                               "gbs": round(cb / (op_ms[2] * 1e-3) / 1e9, 1), "bytes": cb,
                                               "seq_per_s": round(world * x.batch / (op_ms[2] * 1e-3), 1)},
+            "commit": {"us": round(commit_ms * 1e3, 2), "gbs": round(mb / (commit_ms * 1e-3) / 1e9, 1),
+                       "bytes": mb, "frac_hbm": round(mb / (commit_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                       "traffic": measured_traffic("commit", args.config),
+                       "note": "timed alone, not in the step; accepted counts seeded uniform on 0..B"},
             "seq_per_s": round(world * a.batch / (ms_step * 1e-3), 1),
             "roofline": roof,
             "gpu_launches": kernel_launches(x) * args.steps,

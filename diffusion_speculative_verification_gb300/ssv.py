@@ -23,7 +23,8 @@ ARGMAX, GUMBEL, REJECT = 0, 1, 2
 
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
-           "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
+           "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_get_status", "ssv_status_string", "ssv_version",
+           "ssv_bench")
 
 
 class SsvError(RuntimeError):
@@ -62,6 +63,14 @@ class AcceptArgs(C.Structure):
                 ("n_out", C.c_void_p), ("tokens", C.c_void_p), ("dev_status", C.c_void_p)]
 
 
+class CommitArgs(C.Structure):
+    _fields_ = [("k_new", C.c_void_p), ("v_new", C.c_void_p), ("k_dst", C.c_void_p), ("v_dst", C.c_void_p),
+                ("dtype", C.c_int), ("Hkv", C.c_int32), ("d", C.c_int32), ("seqs", C.c_void_p),
+                ("batch", C.c_int32), ("tau", C.c_void_p), ("n_acc", C.c_void_p), ("dst_off", C.c_void_p),
+                ("dst_cap", C.c_void_p), ("new_len", C.c_void_p), ("total_rows", C.c_int32),
+                ("total_slots", C.c_int32), ("dst_rows", C.c_int32), ("dev_status", C.c_void_p)]
+
+
 _lib = None
 
 
@@ -79,6 +88,7 @@ def lib():
         L.ssv_accept_workspace.argtypes = [C.POINTER(AcceptArgs), C.POINTER(sz)]
         L.ssv_accept.argtypes = [C.POINTER(AcceptArgs), vp, sz, vp]
         L.ssv_accept_noalloc.argtypes = [C.POINTER(AcceptArgs), vp]
+        L.ssv_commit.argtypes = [C.POINTER(CommitArgs), vp]
         L.ssv_verify_step.argtypes = [C.POINTER(RopeArgs), C.POINTER(AttnArgs), vp, sz, C.POINTER(AcceptArgs), vp,
                                       sz, vp]
         L.ssv_get_status.argtypes = [vp, vp]
@@ -87,7 +97,8 @@ def lib():
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
         for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step",
-                     "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_get_status", "ssv_bench"):
+                     "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_get_status",
+                     "ssv_bench"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -197,8 +208,8 @@ def verify_step(rope: "RopeArgs | None", attn: AttnArgs, attn_workspace, accept:
 def attn_args(q, k_cache, v_cache, k_new, v_new, out, batch: Batch, tau, scale: float = 0.0, dev_status=None):
     return AttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(out),
                     _dtype_code(q), _dtype_code(out), q.shape[1], k_new.shape[1], q.shape[2], float(scale),
-                    _ptr(batch.dev), batch.batch, _ptr(tau), batch.total_rows, batch.total_cache,
-                    batch.total_slots, batch.max_cache, batch.max_new, batch.max_block, _ptr(dev_status))
+                    _ptr(batch.dev), batch.batch, _ptr(tau), batch.total_rows,
+                    batch.total_cache if k_cache is None else k_cache.shape[0], batch.total_slots, batch.max_cache, batch.max_new, batch.max_block, _ptr(dev_status))
 
 
 def verify_attn_workspace_bytes(args: AttnArgs) -> int:
@@ -272,6 +283,31 @@ def accept_noalloc(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, d
                     draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status)
     _check(lib().ssv_accept_noalloc(C.byref(a), _stream_ptr(stream)), "ssv_accept_noalloc")
     return n_acc, n_out, tokens
+
+
+def commit_args(k_new, v_new, k_dst, v_dst, batch: Batch, tau, n_acc, dst_off, dst_cap, new_len,
+                dev_status=None):
+    return CommitArgs(_ptr(k_new), _ptr(v_new), _ptr(k_dst), _ptr(v_dst), _dtype_code(k_new), k_new.shape[1],
+                      k_new.shape[2], _ptr(batch.dev), batch.batch, _ptr(tau), _ptr(n_acc), _ptr(dst_off),
+                      _ptr(dst_cap), _ptr(new_len), k_new.shape[0], tau.shape[0], k_dst.shape[0],
+                      _ptr(dev_status))
+
+
+def commit(k_new, v_new, k_dst, v_dst, batch: Batch, tau, n_acc, dst_off, dst_cap, new_len=None, dev_status=None,
+           stream=None):
+    """Appends each sequence's fresh prompt rows and accepted data rows (stage
+    order) to its cache in k_dst / v_dst (in place); returns new_len [batch]
+    int32 device (-1 for a sequence rejected on the device)."""
+    torch = _torch()
+    if k_dst.dtype != k_new.dtype or v_dst.dtype != k_new.dtype or v_new.dtype != k_new.dtype:
+        raise SsvError(SSV_ERR_INVALID, "ssv_commit: k_new, v_new, k_dst and v_dst must share one dtype")
+    if tuple(k_dst.shape[1:]) != tuple(k_new.shape[1:]) or v_dst.shape != k_dst.shape or v_new.shape != k_new.shape:
+        raise SsvError(SSV_ERR_INVALID, "ssv_commit: row shapes differ")
+    if new_len is None:
+        new_len = torch.empty(batch.batch, dtype=torch.int32, device=k_new.device)
+    a = commit_args(k_new, v_new, k_dst, v_dst, batch, tau, n_acc, dst_off, dst_cap, new_len, dev_status)
+    _check(lib().ssv_commit(C.byref(a), _stream_ptr(stream)), "ssv_commit")
+    return new_len
 
 
 def get_status(dev_status, stream=None) -> int:

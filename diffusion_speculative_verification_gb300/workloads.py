@@ -314,3 +314,41 @@ def workload_accept(name: str, which: int = 0, seed: Optional[int] = None,
     _, _, blocks = workload_lengths(name, seed)
     return make_accept_inputs(f"{name}/{mode_name}/T={T}", MODE_NAMES[mode_name], T, w["V"], blocks,
                               workload_gammas(name, blocks), seed + 100 * (which + 1), tau=tau)
+
+
+@dataclasses.dataclass
+class CommitInputs:
+    """Inputs of the commit step: the pass's fresh rows (from an AttnInputs),
+    accepted-stage counts, and destination caches laid out with room."""
+    attn: AttnInputs
+    n_acc: np.ndarray         # int32 [batch], 0..B
+    dst_off: np.ndarray       # int32 [batch], first destination row of each sequence
+    dst_cap: np.ndarray       # int32 [batch], rows of room from dst_off
+    k_dst: np.ndarray         # [dst_rows, Hkv, d] prior contents (same storage as the fresh rows)
+    v_dst: np.ndarray
+
+
+def commit_layout(a: AttnInputs, seed: int, slack: int = 3):
+    """Destination layout of the commit step: each sequence gets C + N + B +
+    slack rows of room, with a gap of `slack` rows between sequences; accepted
+    counts are uniform on 0..B.  Returns (n_acc, dst_off, dst_cap, dst_rows)
+    and the generator, positioned for the destination contents."""
+    rng = np.random.default_rng(seed)
+    C = a.seqs[:, 0].astype(np.int64)
+    N = a.seqs[:, 1].astype(np.int64)
+    B = a.seqs[:, 2].astype(np.int64)
+    cap = C + N + B + slack
+    off = np.concatenate([[slack], slack + np.cumsum(cap + slack)[:-1]]) if len(cap) else np.zeros(0, np.int64)
+    rows = int(off[-1] + cap[-1] + slack) if len(cap) else 1
+    n_acc = np.array([rng.integers(0, int(b) + 1) for b in B], np.int32)
+    return n_acc, off.astype(np.int32), cap.astype(np.int32), rows, rng
+
+
+def make_commit_inputs(a: AttnInputs, seed: int, slack: int = 3) -> CommitInputs:
+    """commit_layout plus destination rows holding seeded random values (so
+    rows the commit must not touch can be checked)."""
+    n_acc, off, cap, rows, rng = commit_layout(a, seed, slack)
+    shape = (rows, a.Hkv, a.d)
+    k_dst = _store(_normal(rng, shape), a.dtype)
+    v_dst = _store(_normal(rng, shape), a.dtype)
+    return CommitInputs(a, n_acc, off, cap, k_dst, v_dst)

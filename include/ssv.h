@@ -294,6 +294,66 @@ SSV_API ssv_status ssv_verify_step(const ssv_rope_args* rope, const ssv_attn_arg
 SSV_API ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ssv_commit -- commit of a verification pass into the KV cache.
+ * SimSD summary, section 4 "Speculative decoding pipeline" (Acceptance: the
+ * longest accepted prefix, in the temporal order the draft induces, is
+ * committed and the loop repeats) and "Main contributions" 3 (composes with
+ * a KV cache).  The pages give no cache layout; the reading taken: after
+ * sequence b's pass (C cached rows, N fresh prompt rows, block B, stage map
+ * tau, n_acc[b] accepted stages) its cache gains, appended after row C,
+ *   - the keys / values of the N fresh prompt rows, in row order, then
+ *   - those of the data rows of stages 1..n_acc, in stage order (stage s is
+ *     slot k = tau^{-1}(s), fresh row N + k).
+ * Mask rows are never committed.  Rows are copied as they are (keys keep the
+ * rotation ssv_rope_copy gave them).  new_len[b] = C + N + n_acc[b].
+ *
+ * k_new, v_new [total_rows, Hkv, d]  device, dtype: the pass's fresh rows
+ *                                     (post-RoPE keys), packed per sequence at
+ *                                     seqs[b].q_off as for ssv_verify_attn
+ * k_dst, v_dst [dst_rows, Hkv, d]    device, dtype: destination caches;
+ *                                     sequence b's cache starts at row
+ *                                     dst_off[b] and has dst_cap[b] rows of
+ *                                     room (rows C .. C + N + n_acc - 1 of it
+ *                                     are written, nothing else).  May be the
+ *                                     k_cache / v_cache of ssv_verify_attn
+ *                                     when its sequences were laid out with
+ *                                     room (dst_off = kv_off).
+ * seqs, tau, batch, total_rows as for ssv_verify_attn; n_acc [batch] device
+ * (as written by ssv_accept); dst_off, dst_cap [batch] device; new_len
+ * [batch] device, written (-1 for a sequence rejected on the device).
+ * dtype SSV_F32 or SSV_BF16; d in {64, 128}; pointers 16-byte aligned.
+ * k_new / v_new must not overlap k_dst / v_dst (checked), and the
+ * destination ranges [dst_off[b], dst_off[b] + dst_cap[b]) of different
+ * sequences must not overlap (not checked: overlapping ones race).
+ * Errors: SSV_ERR_INVALID, SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU (stage
+ * map not a permutation of 1..B) and SSV_ERR_INVALID (B outside 1..64, a
+ * stage map outside tau[0, total_slots), n_acc outside 0..B, or the
+ * appended rows do not fit dst_cap / dst_rows): that sequence's rows are not
+ * written and its new_len is -1.  No workspace; asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void* k_new;
+  const void* v_new;
+  void* k_dst;
+  void* v_dst;
+  ssv_dtype dtype;
+  int32_t Hkv, d;
+  const ssv_seq* seqs;         /* device [batch] */
+  int32_t batch;
+  const int32_t* tau;          /* device [total_slots] */
+  const int32_t* n_acc;        /* device [batch] */
+  const int32_t* dst_off;      /* device [batch] */
+  const int32_t* dst_cap;      /* device [batch] */
+  int32_t* new_len;            /* device [batch], out */
+  int32_t total_rows;          /* rows of k_new / v_new */
+  int32_t total_slots;         /* entries of tau (sum of B) */
+  int32_t dst_rows;            /* rows of k_dst / v_dst */
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_commit_args;
+
+SSV_API ssv_status ssv_commit(const ssv_commit_args* a, void* stream);
+
+/* ------------------------------------------------------------------------
  * Status and utilities
  * ---------------------------------------------------------------------- */
 /* Waits for `stream`, reads the device status word, resets it to 0 and
