@@ -352,3 +352,98 @@ def make_commit_inputs(a: AttnInputs, seed: int, slack: int = 3) -> CommitInputs
     k_dst = _store(_normal(rng, shape), a.dtype)
     v_dst = _store(_normal(rng, shape), a.dtype)
     return CommitInputs(a, n_acc, off, cap, k_dst, v_dst)
+
+
+# --------------------------------------------------------------------------
+# fused LM head + acceptance
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class LmheadInputs:
+    """Inputs of the fused LM head + acceptance: the acceptance metadata (an
+    AcceptInputs whose logits are None) plus the final hidden states of the
+    mask slots and the LM head."""
+    acc: AcceptInputs
+    hidden: int
+    h: np.ndarray             # bf16 bits [total_slots, hidden], row = slot (slot order)
+    w: np.ndarray             # bf16 bits [V, hidden]
+
+
+#: hidden width, acceptance mode and temperature of the fused LM head per
+#: named workload (hidden = query heads x head_dim of the workload's layer)
+LMHEAD: Dict[str, tuple] = {
+    "tiny": (64, "gumbel", 1.0),
+    "gqa1p7b": (2048, "argmax", 0.0),
+    "gqa8b": (4096, "argmax", 0.0),
+    "sweep": (4096, "gumbel", 1.0),
+}
+
+
+def lm_head_matrix(rng: np.random.Generator, V: int, hidden: int) -> np.ndarray:
+    """LM head [V, hidden] with N(0, 1) entries, bf16 bits (row by row blocks
+    to bound the fp32 temporary)."""
+    w = np.empty((V, hidden), np.uint16)
+    step = max(1, (1 << 26) // max(hidden, 1))
+    for r0 in range(0, V, step):
+        r1 = min(V, r0 + step)
+        w[r0:r1] = f32_to_bf16_bits(_normal(rng, (r1 - r0, hidden)))
+    return w
+
+
+def make_lmhead_inputs(name: str, mode: int, T: float, V: int, hidden: int, blocks, gammas, seed: int,
+                       plant: float = 64.0, tau: Optional[np.ndarray] = None,
+                       w: Optional[np.ndarray] = None) -> LmheadInputs:
+    """Hidden states with planted agreement.
+
+    Rows are h = z + (plant / hidden) w_t with z ~ N(0, 1/hidden) per entry
+    and w_t row t of the stored LM head (N(0, 1) entries), so that the score
+    of token t sits near `plant` while the others are about N(0, 1).  Per
+    sequence a cut stage c is drawn uniformly in 1..gamma+1: stages before c
+    plant the slot's draft token; stage c (if c <= B) plants a different
+    random token; later stages are z alone.  Planting only shapes the accepted
+    lengths; both sides compute the outcome from the same bytes.  `w` reuses
+    an LM head drawn earlier (same V and hidden)."""
+    rng = np.random.default_rng(seed)
+    blocks = np.asarray(blocks, np.int32)
+    gammas = np.asarray(gammas, np.int32)
+    batch = len(blocks)
+    S = int(blocks.sum())
+    slot_off = np.concatenate([[0], np.cumsum(blocks)[:-1]]).astype(np.int32) if batch else np.zeros(0, np.int32)
+    if tau is None:
+        tau = np.concatenate([random_tau(rng, int(b)) for b in blocks]).astype(np.int32) if batch else np.zeros(0, np.int32)
+    if w is None:
+        w = lm_head_matrix(rng, V, hidden)
+    assert w.shape == (V, hidden)
+    h32 = _normal(rng, (S, hidden), 1.0 / np.sqrt(hidden))
+    draft_tokens = rng.integers(0, V, size=S).astype(np.int32)
+    scale = np.float32(plant / hidden)
+    for b in range(batch):
+        B, g, off = int(blocks[b]), int(gammas[b]), int(slot_off[b])
+        cut = int(rng.integers(1, g + 2))
+        slot_of_stage = np.empty(B, np.int64)
+        slot_of_stage[tau[off:off + B] - 1] = np.arange(B)
+        for s in range(1, min(cut, B) + 1):
+            k = off + int(slot_of_stage[s - 1])
+            t = int(draft_tokens[k])
+            if s == cut:
+                t = int((t + 1 + rng.integers(0, V - 1)) % V) if V > 1 else t
+            h32[k] += scale * bf16_bits_to_f32(w[t])
+    h = f32_to_bf16_bits(h32)
+    noise = None
+    noise_row = np.zeros(S, np.int32)
+    if mode == MODE_GUMBEL:
+        noise_row = rng.permutation(S).astype(np.int32)
+        noise = gumbel_table(rng, S, V)
+    acc = AcceptInputs(name, mode, float(T), V, F32, blocks, gammas, slot_off, tau, None, None, draft_tokens,
+                       noise, noise_row, uniform01_f32(rng, S), uniform01_f32(rng, batch))
+    return LmheadInputs(acc, hidden, h, w)
+
+
+def workload_lmhead(name: str, seed: Optional[int] = None, w: Optional[np.ndarray] = None) -> LmheadInputs:
+    """The named workload's verified slots under the fused LM head."""
+    wl = WORKLOADS[name]
+    seed = wl["seed"] if seed is None else seed
+    hidden, mode_name, T = LMHEAD[name]
+    _, _, blocks = workload_lengths(name, seed)
+    V = wl["V"]
+    return make_lmhead_inputs(f"{name}/lmhead/{mode_name}/T={T}", MODE_NAMES[mode_name], T, V, hidden, blocks,
+                              workload_gammas(name, blocks), seed + 500, w=w)

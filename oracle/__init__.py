@@ -24,6 +24,9 @@ What it computes, plainly and slowly, in float64 (numpy):
                               rows, then the accepted data rows in stage order
                               (SimSD summary section 4 "Acceptance", the longest
                               accepted prefix is committed; reading for the layout).
+* ``lmhead.accept_lmhead``    the LM head over the mask slots (l = W h, exact,
+                              rounded once to fp32) followed by the acceptance
+                              above (SimSD summary section 4; SPOT review).
 
 Pins (``tests/test_oracle_*.py``, marked ``not gpu``) tie each function to
 something other than itself: a hand-worked mask from the rule's text, mask
@@ -35,4 +38,4 @@ invariance, brute-force laws of the Gumbel-max and rejection samplers.
 The attention *values* at full size carry no printed example on the pages
 and rest on those reductions.
 """
-from . import mask, rope, attention, accept  # noqa: F401
+from . import mask, rope, attention, accept, commit, lmhead  # noqa: F401
