@@ -86,6 +86,22 @@ def commit_bytes(a: W.AttnInputs, n_acc) -> float:
     return 2.0 * 2.0 * rows * a.Hkv * a.d * es
 
 
+def lmhead_work(x: W.LmheadInputs):
+    """Useful work of the fused LM head + acceptance: (bytes, flops, verified
+    rows).  Bytes: the LM head and the hidden states read once, plus the noise
+    rows of the verified slots (coupled noise at T > 0); flops: 2 V hidden per
+    verified row (the kernel also multiplies the unverified and padding rows
+    of its M-tiles; that work is not counted)."""
+    a = x.acc
+    need = [min(int(g) + 1, int(B)) for g, B in zip(a.gammas, a.blocks)]
+    ver = int(sum(need))
+    S = int(np.sum(a.blocks))
+    b = a.V * x.hidden * 2.0 + S * x.hidden * 2.0
+    if a.mode == W.MODE_GUMBEL and a.T != 0.0:
+        b += ver * a.V * 4.0
+    return b, 2.0 * ver * a.V * x.hidden, ver
+
+
 def aggregate_ms(local_ms: float, dist_mod=None, device=None) -> float:
     """Max over ranks of a per-rank time (identity on one rank)."""
     if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
@@ -520,6 +536,10 @@ def run_ours(args):
                 "frac": round(tfs / tf_peak, 4), "traffic": measured_traffic(dom, args.config), "peak_kind": peak_kind,
                 "algorithmic_flops": af}
 
+    lmh = None
+    if args.config in W.LMHEAD and not args.no_lmhead:
+        lmh = run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak)
+
     # ---- end to end: host inputs -> device, run, tokens back -------------------
     e2e = run_e2e(args, a, x, t, acc, outs if acc is not None else None, o, dev, stream, step, out_b)
 
@@ -542,6 +562,7 @@ def run_ours(args):
                        "bytes": mb, "frac_hbm": round(mb / (commit_ms * 1e-3) / 1e9 / hbm_peak, 4),
                        "traffic": measured_traffic("commit", args.config),
                        "note": "timed alone, not in the step; accepted counts seeded uniform on 0..B"},
+            "lmhead_accept": lmh,
             "seq_per_s": round(world * a.batch / (ms_step * 1e-3), 1),
             "roofline": roof,
             "gpu_launches": kernel_launches(x) * args.steps,
@@ -555,6 +576,75 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
+    """The fused LM head + acceptance on the workload's verified slots (timed
+    alone, after the same L2 flush), beside the unfused path it replaces
+    (cuBLAS bf16 GEMM to bf16 logits, then ssv_accept)."""
+    import ctypes as C
+    import torch
+    from diffusion_speculative_verification_gb300 import ssv, io as sio
+    x = W.workload_lmhead(args.config)
+    d = sio.lmhead_to_device(x, dev)
+    a = x.acc
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    outs = (torch.empty(len(a.blocks), dtype=torch.int32, device=dev),
+            torch.empty(len(a.blocks), dtype=torch.int32, device=dev),
+            torch.empty(len(a.tau), dtype=torch.int32, device=dev))
+    largs = ssv.lmhead_args(d["mode"], d["T"], d["h"], d["w"], d["draft_tokens"], d["tau"], d["block"], d["gamma"],
+                            d["slot_off"], *outs, d["noise"], d["noise_row"], status)
+    ws = torch.zeros(max(256, ssv.lmhead_accept_workspace_bytes(largs)), dtype=torch.uint8, device=dev)
+    L = ssv.lib()
+
+    def fused():
+        r = L.ssv_lmhead_accept(C.byref(largs), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_lmhead_accept")
+
+    logits = torch.empty((d["h"].shape[0], a.V), dtype=torch.bfloat16, device=dev)
+    cargs = ssv.accept_args(d["mode"], d["T"], logits, d["draft_tokens"], d["tau"], d["block"], d["gamma"],
+                            d["slot_off"], *outs, None, d["noise"], d["noise_row"], None, None, 64, status)
+    ws_acc = torch.zeros(ssv.accept_workspace_bytes(cargs), dtype=torch.uint8, device=dev)
+
+    def unfused():
+        torch.mm(d["h"], d["w"].t(), out=logits)
+        r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), stream.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_accept")
+
+    def median_ms(fn):
+        for _ in range(max(3, args.warmup)):
+            l2_flush()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(min(args.steps, 50))]
+        for e0, e1 in ev:
+            l2_flush()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([e0.elapsed_time(e1) for e0, e1 in ev]))
+
+    with torch.cuda.stream(stream):
+        t_f = median_ms(fused)
+        fused_tokens = [o.clone() for o in outs]
+        t_u = median_ms(unfused)
+    assert ssv.get_status(status) == ssv.SSV_OK
+    same = all(bool(torch.equal(u, v)) for u, v in zip(fused_tokens, outs))
+    nbytes, flops, ver = lmhead_work(x)
+    t_hbm = nbytes / (hbm_peak * 1e9) * 1e3
+    t_tc = flops / (tf_peak * 1e12) * 1e3
+    lb = max(t_hbm, t_tc)
+    return {"us": round(t_f * 1e3, 1), "unfused_us": round(t_u * 1e3, 1),
+            "unfused": "cuBLAS bf16 GEMM to bf16 logits, then ssv_accept", "same_outputs": same,
+            "mode": {W.MODE_ARGMAX: "argmax", W.MODE_GUMBEL: "gumbel"}[a.mode], "T": a.T, "V": a.V,
+            "hidden": x.hidden, "slots": int(np.sum(a.blocks)), "verified_rows": ver,
+            "bound": "hbm" if t_hbm >= t_tc else "tensor", "lower_bound_us": round(lb * 1e3, 1),
+            "frac": round(lb / t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
+            "gbs": round(nbytes / (t_f * 1e-3) / 1e9, 1),
+            "note": "timed alone, not in the step; logits never written"}
 
 
 def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):
@@ -605,6 +695,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=list(W.WORKLOADS), default="gqa1p7b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM head + acceptance measurement")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one call at a time")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -72,3 +72,22 @@ def accept_to_device(x: W.AcceptInputs, device="cuda") -> dict:
     d["draft_logits"] = None if x.draft_logits is None else tensor(x.draft_logits, x.logits_dtype, device)
     d["noise"] = None if x.noise is None else f32_tensor(x.noise, device)
     return d
+
+
+def lmhead_to_device(x: W.LmheadInputs, device="cuda", w=None) -> dict:
+    """Device copies of a fused LM-head input set (`w`: an LM head already on
+    the device, reused)."""
+    a = x.acc
+    d = dict(
+        mode=a.mode, T=a.T,
+        h=tensor(x.h, W.BF16, device),
+        w=tensor(x.w, W.BF16, device) if w is None else w,
+        draft_tokens=int_tensor(a.draft_tokens, device),
+        tau=int_tensor(a.tau, device),
+        block=int_tensor(a.blocks, device),
+        gamma=int_tensor(a.gammas, device),
+        slot_off=int_tensor(a.slot_off, device),
+        noise_row=int_tensor(a.noise_row, device),
+    )
+    d["noise"] = None if a.noise is None else f32_tensor(a.noise, device)
+    return d

@@ -23,8 +23,8 @@ ARGMAX, GUMBEL, REJECT = 0, 1, 2
 
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
-           "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_get_status", "ssv_status_string", "ssv_version",
-           "ssv_bench")
+           "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_lmhead_accept_workspace", "ssv_lmhead_accept",
+           "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
 
 
 class SsvError(RuntimeError):
@@ -71,6 +71,15 @@ class CommitArgs(C.Structure):
                 ("total_slots", C.c_int32), ("dst_rows", C.c_int32), ("dev_status", C.c_void_p)]
 
 
+class LmheadArgs(C.Structure):
+    _fields_ = [("mode", C.c_int), ("T", C.c_float), ("V", C.c_int32), ("hidden", C.c_int32),
+                ("batch", C.c_int32), ("total_slots", C.c_int32), ("hidden_states", C.c_void_p),
+                ("lm_head", C.c_void_p), ("draft_tokens", C.c_void_p), ("tau", C.c_void_p), ("block", C.c_void_p),
+                ("gamma", C.c_void_p), ("slot_off", C.c_void_p), ("noise", C.c_void_p),
+                ("n_noise_rows", C.c_int32), ("noise_row", C.c_void_p), ("n_acc", C.c_void_p),
+                ("n_out", C.c_void_p), ("tokens", C.c_void_p), ("dev_status", C.c_void_p)]
+
+
 _lib = None
 
 
@@ -89,6 +98,8 @@ def lib():
         L.ssv_accept.argtypes = [C.POINTER(AcceptArgs), vp, sz, vp]
         L.ssv_accept_noalloc.argtypes = [C.POINTER(AcceptArgs), vp]
         L.ssv_commit.argtypes = [C.POINTER(CommitArgs), vp]
+        L.ssv_lmhead_accept_workspace.argtypes = [C.POINTER(LmheadArgs), C.POINTER(sz)]
+        L.ssv_lmhead_accept.argtypes = [C.POINTER(LmheadArgs), vp, sz, vp]
         L.ssv_verify_step.argtypes = [C.POINTER(RopeArgs), C.POINTER(AttnArgs), vp, sz, C.POINTER(AcceptArgs), vp,
                                       sz, vp]
         L.ssv_get_status.argtypes = [vp, vp]
@@ -97,8 +108,8 @@ def lib():
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
         for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step",
-                     "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_get_status",
-                     "ssv_bench"):
+                     "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit",
+                     "ssv_lmhead_accept_workspace", "ssv_lmhead_accept", "ssv_get_status", "ssv_bench"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -308,6 +319,43 @@ def commit(k_new, v_new, k_dst, v_dst, batch: Batch, tau, n_acc, dst_off, dst_ca
     a = commit_args(k_new, v_new, k_dst, v_dst, batch, tau, n_acc, dst_off, dst_cap, new_len, dev_status)
     _check(lib().ssv_commit(C.byref(a), _stream_ptr(stream)), "ssv_commit")
     return new_len
+
+
+def lmhead_args(mode, T, hidden_states, lm_head, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
+                noise=None, noise_row=None, dev_status=None):
+    return LmheadArgs(int(mode), float(T), lm_head.shape[0], lm_head.shape[1], block.shape[0],
+                      draft_tokens.shape[0], _ptr(hidden_states), _ptr(lm_head), _ptr(draft_tokens), _ptr(tau),
+                      _ptr(block), _ptr(gamma), _ptr(slot_off), _ptr(noise), 0 if noise is None else noise.shape[0],
+                      _ptr(noise_row), _ptr(n_acc), _ptr(n_out), _ptr(tokens), _ptr(dev_status))
+
+
+def lmhead_accept_workspace_bytes(args: LmheadArgs) -> int:
+    n = C.c_size_t(0)
+    _check(lib().ssv_lmhead_accept_workspace(C.byref(args), C.byref(n)), "ssv_lmhead_accept_workspace")
+    return int(n.value)
+
+
+def lmhead_accept(mode, T, hidden_states, lm_head, draft_tokens, tau, block, gamma, slot_off, noise=None,
+                  noise_row=None, workspace=None, dev_status=None, stream=None, out=None):
+    """LM head over the slots' hidden states fused with acceptance; returns
+    (n_acc [batch], n_out [batch], tokens [slots]) int32 device tensors."""
+    torch = _torch()
+    if hidden_states.dtype != torch.bfloat16 or lm_head.dtype != torch.bfloat16:
+        raise SsvError(SSV_ERR_INVALID, "ssv_lmhead_accept: hidden states and LM head must be bf16")
+    if hidden_states.shape[1] != lm_head.shape[1] or hidden_states.shape[0] != draft_tokens.shape[0]:
+        raise SsvError(SSV_ERR_INVALID, "ssv_lmhead_accept: shapes")
+    dev = hidden_states.device
+    if out is None:
+        out = (torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(block.shape[0], dtype=torch.int32, device=dev),
+               torch.empty(draft_tokens.shape[0], dtype=torch.int32, device=dev))
+    n_acc, n_out, tokens = out
+    a = lmhead_args(mode, T, hidden_states, lm_head, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out,
+                    tokens, noise, noise_row, dev_status)
+    ws = _workspace(lmhead_accept_workspace_bytes(a), dev, workspace)
+    _check(lib().ssv_lmhead_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "ssv_lmhead_accept")
+    return n_acc, n_out, tokens
 
 
 def get_status(dev_status, stream=None) -> int:

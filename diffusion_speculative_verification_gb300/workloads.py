@@ -379,13 +379,23 @@ LMHEAD: Dict[str, tuple] = {
 
 
 def lm_head_matrix(rng: np.random.Generator, V: int, hidden: int) -> np.ndarray:
-    """LM head [V, hidden] with N(0, 1) entries, bf16 bits (row by row blocks
-    to bound the fp32 temporary)."""
+    """Synthetic LM head [V, hidden] as bf16 bit patterns drawn directly: a
+    random sign, a random 7-bit mantissa and exponent 2^-1 or 2^0, i.e.
+    |x| uniform over the bf16 values in [0.5, 2) (mean 0, E x^2 about 1.46).
+    Drawn in row blocks to bound the temporaries."""
     w = np.empty((V, hidden), np.uint16)
     step = max(1, (1 << 26) // max(hidden, 1))
     for r0 in range(0, V, step):
         r1 = min(V, r0 + step)
-        w[r0:r1] = f32_to_bf16_bits(_normal(rng, (r1 - r0, hidden)))
+        n = (r1 - r0) * hidden
+        u = rng.integers(0, 1 << 32, size=(n + 1) // 2, dtype=np.uint32).view(np.uint16)[:n].reshape(r1 - r0, hidden)
+        # bit 15 sign, bit 8 picks exponent 126 or 127 (moved to bit 7), bits 0..6 mantissa
+        e = u & np.uint16(0x0100)
+        e >>= np.uint16(1)
+        u &= np.uint16(0x807F)
+        u |= np.uint16(0x3F00)
+        u |= e
+        w[r0:r1] = u
     return w
 
 
@@ -394,9 +404,9 @@ def make_lmhead_inputs(name: str, mode: int, T: float, V: int, hidden: int, bloc
                        w: Optional[np.ndarray] = None) -> LmheadInputs:
     """Hidden states with planted agreement.
 
-    Rows are h = z + (plant / hidden) w_t with z ~ N(0, 1/hidden) per entry
-    and w_t row t of the stored LM head (N(0, 1) entries), so that the score
-    of token t sits near `plant` while the others are about N(0, 1).  Per
+    Rows are h = z + (plant / |w_t|^2) w_t with z ~ N(0, 1/hidden) per entry
+    and w_t row t of the stored LM head (lm_head_matrix), so that the score
+    of token t sits near `plant` while the others are about N(0, 1.5).  Per
     sequence a cut stage c is drawn uniformly in 1..gamma+1: stages before c
     plant the slot's draft token; stage c (if c <= B) plants a different
     random token; later stages are z alone.  Planting only shapes the accepted
@@ -415,7 +425,6 @@ def make_lmhead_inputs(name: str, mode: int, T: float, V: int, hidden: int, bloc
     assert w.shape == (V, hidden)
     h32 = _normal(rng, (S, hidden), 1.0 / np.sqrt(hidden))
     draft_tokens = rng.integers(0, V, size=S).astype(np.int32)
-    scale = np.float32(plant / hidden)
     for b in range(batch):
         B, g, off = int(blocks[b]), int(gammas[b]), int(slot_off[b])
         cut = int(rng.integers(1, g + 2))
@@ -426,7 +435,8 @@ def make_lmhead_inputs(name: str, mode: int, T: float, V: int, hidden: int, bloc
             t = int(draft_tokens[k])
             if s == cut:
                 t = int((t + 1 + rng.integers(0, V - 1)) % V) if V > 1 else t
-            h32[k] += scale * bf16_bits_to_f32(w[t])
+            wt = bf16_bits_to_f32(w[t])
+            h32[k] += np.float32(plant / float(np.dot(wt.astype(np.float64), wt))) * wt
     h = f32_to_bf16_bits(h32)
     noise = None
     noise_row = np.zeros(S, np.int32)

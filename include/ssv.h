@@ -354,6 +354,72 @@ typedef struct {
 SSV_API ssv_status ssv_commit(const ssv_commit_args* a, void* stream);
 
 /* ------------------------------------------------------------------------
+ * ssv_lmhead_accept -- LM head over the mask slots fused with acceptance.
+ * SimSD summary section 4 (the target scores every drafted position in one
+ * pass; acceptance in the temporal order the draft induces); SPOT review
+ * "How it is used" (state equality; coupled-noise match).  The pages do not
+ * say how the logits are formed; the reading taken: the logits of mask slot
+ * k are l_k = W h_k for the LM head W [V, hidden] and the slot's final
+ * hidden state h_k.  This call computes, for every verified row (stage
+ * <= min(gamma + 1, B)), the decision score over the whole vocabulary
+ * without writing logits anywhere:
+ *   ARGMAX : argmax_v l_k[v]                                   (ties: lowest v)
+ *   GUMBEL : argmax_v fl32(fl32(l_k[v] / T) + noise[noise_row[k]][v])
+ *            (IEEE fp32, no contraction; T = 0 means ARGMAX)
+ * and then walks the stages exactly as ssv_accept (same n_acc, n_out,
+ * tokens).  l_k is accumulated in fp32 on the tensor cores from the bf16
+ * operands (exact products, fp32 sums in an unspecified order), so a
+ * decision between two tokens whose scores differ by less than that
+ * accumulation error may fall either way.  Rejection sampling is not
+ * offered here (it needs the draft model's logits as well).
+ *
+ * hidden_states [total_slots, hidden] bf16 device, row = slot (slot order);
+ *               every row is read (rows of unverified stages too).
+ * lm_head       [V, hidden] bf16 device, row-major.
+ * draft_tokens, tau, noise_row: [total_slots] int32 device
+ * block, gamma, slot_off: [batch] int32 device (as for ssv_accept)
+ * noise [n_noise_rows, V] fp32 device (GUMBEL with T > 0 only, else NULL)
+ * Outputs n_acc, n_out [batch], tokens [total_slots] as for ssv_accept.
+ * Sizes: hidden % 64 == 0 and >= 64; 1 <= V; 1 <= total_slots <= 2048;
+ *        batch <= 2048; pointers 16-byte aligned.
+ * Workspace: ssv_lmhead_accept_workspace bytes, zero before first use.
+ * Errors: SSV_ERR_INVALID (mode REJECT, sizes, null, alignment),
+ *         SSV_ERR_NOT_FINITE (T), SSV_ERR_UNSUPPORTED (total_slots or batch
+ *         above 2048), SSV_ERR_WORKSPACE, SSV_ERR_CUDA; on device
+ *         SSV_ERR_BAD_TAU (that sequence's outputs are not written),
+ *         SSV_ERR_INVALID (a verified slot's noise_row outside the table;
+ *         likewise), SSV_ERR_TIMEOUT (a bounded wait ran out).
+ * Scheduling: one CTA per SM; the CTA that finishes an M-tile last merges
+ * its rows; no CTA waits on another.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  ssv_accept_mode mode;        /* SSV_ACCEPT_ARGMAX or SSV_ACCEPT_GUMBEL */
+  float T;
+  int32_t V;
+  int32_t hidden;
+  int32_t batch;
+  int32_t total_slots;
+  const void* hidden_states;   /* bf16 [total_slots, hidden] */
+  const void* lm_head;         /* bf16 [V, hidden] */
+  const int32_t* draft_tokens;
+  const int32_t* tau;
+  const int32_t* block;
+  const int32_t* gamma;
+  const int32_t* slot_off;
+  const float* noise;
+  int32_t n_noise_rows;
+  const int32_t* noise_row;
+  int32_t* n_acc;
+  int32_t* n_out;
+  int32_t* tokens;
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_lmhead_accept_args;
+
+SSV_API ssv_status ssv_lmhead_accept_workspace(const ssv_lmhead_accept_args* a, size_t* bytes);
+SSV_API ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
  * Status and utilities
  * ---------------------------------------------------------------------- */
 /* Waits for `stream`, reads the device status word, resets it to 0 and

@@ -51,6 +51,22 @@ def error_bound(h: np.ndarray, w: np.ndarray, l_exact: np.ndarray) -> np.ndarray
     return K * u * absdot + u * np.abs(l_exact)
 
 
+def logits_from_bits(h_bits: np.ndarray, w_bits: np.ndarray, with_bound: bool = False, block: int = 8192):
+    """lm_head_logits (and error_bound) from bf16 bit patterns, one block of
+    vocabulary rows at a time (bounds the fp64 temporaries for a full LM head).
+    Returns (logits [rows, V], bound [rows, V] or None)."""
+    hv = bf16_values(h_bits)
+    rows, V = hv.shape[0], w_bits.shape[0]
+    logits = np.empty((rows, V), np.float64)
+    bound = np.empty((rows, V), np.float64) if with_bound else None
+    for v0 in range(0, V, block):
+        wv = bf16_values(w_bits[v0:v0 + block])
+        logits[:, v0:v0 + block] = lm_head_logits(hv, wv)
+        if with_bound:
+            bound[:, v0:v0 + block] = error_bound(hv, wv, logits[:, v0:v0 + block])
+    return logits, bound
+
+
 def verified_slots(inp) -> np.ndarray:
     """Slots whose rows the acceptance reads: stage <= min(gamma + 1, B)."""
     out = []
@@ -67,7 +83,7 @@ def slot_logits(x, slots=None) -> np.ndarray:
     """fp64 logits of the given slots (default: every verified slot) as a
     [len(slots), V] array, for an LmheadInputs-like x (fields acc, h, w)."""
     slots = verified_slots(x.acc) if slots is None else np.asarray(slots, np.int64)
-    return lm_head_logits(bf16_values(x.h[slots]), bf16_values(x.w))
+    return logits_from_bits(x.h[slots], x.w)[0]
 
 
 def accept_lmhead(x) -> dict:
