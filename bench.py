@@ -122,12 +122,13 @@ def kernel_launches(x) -> int:
 
 
 KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel",
-                "commit": "commit_kernel"}
+                "commit": "commit_kernel", "lmhead": "lmhead_accept_kernel"}
 KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"],
                   "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh"],
                   "accept_reduce_kernel": ["accept.cu", "accept.cuh"],
                   "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"],
-                  "commit_kernel": ["commit.cu"]}
+                  "commit_kernel": ["commit.cu"],
+                  "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"]}
 
 
 def measured_traffic(op: str, workload: str):
@@ -643,7 +644,8 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
             "hidden": x.hidden, "slots": int(np.sum(a.blocks)), "verified_rows": ver,
             "bound": "hbm" if t_hbm >= t_tc else "tensor", "lower_bound_us": round(lb * 1e3, 1),
             "frac": round(lb / t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
-            "gbs": round(nbytes / (t_f * 1e-3) / 1e9, 1),
+            "gbs": round(nbytes / (t_f * 1e-3) / 1e9, 1), "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "traffic": measured_traffic("lmhead", args.config),
             "note": "timed alone, not in the step; logits never written"}
 
 
