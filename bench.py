@@ -598,8 +598,8 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
     ws = torch.zeros(max(256, ssv.lmhead_accept_workspace_bytes(largs)), dtype=torch.uint8, device=dev)
     L = ssv.lib()
 
-    def fused():
-        r = L.ssv_lmhead_accept(C.byref(largs), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    def fused():  # on the current stream (the capture stream while a graph is captured)
+        r = L.ssv_lmhead_accept(C.byref(largs), ws.data_ptr(), ws.numel(), torch.cuda.current_stream(dev).cuda_stream)
         if r:
             raise ssv.SsvError(r, "ssv_lmhead_accept")
 
@@ -610,28 +610,51 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
 
     def unfused():
         torch.mm(d["h"], d["w"].t(), out=logits)
-        r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), stream.cuda_stream)
+        r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), torch.cuda.current_stream(dev).cuda_stream)
         if r:
             raise ssv.SsvError(r, "ssv_accept")
 
-    def median_ms(fn):
+    K = min(args.steps, 50)
+
+    def graph_of(fn):
+        """K x [L2 flush, fn] captured once (fn may be None: the flush alone)."""
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(K):
+                l2_flush()
+                if fn is not None:
+                    fn()
+        stream.wait_stream(cap)
+        return g
+
+    def replay_ms(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # each op runs inside a CUDA graph (as the step's ops do), minus a flush-only graph
+    with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
             l2_flush()
-            fn()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(min(args.steps, 50))]
-        for e0, e1 in ev:
-            l2_flush()
-            e0.record(stream)
-            fn()
-            e1.record(stream)
+            fused()
         torch.cuda.synchronize()
-        return float(np.median([e0.elapsed_time(e1) for e0, e1 in ev]))
-
-    with torch.cuda.stream(stream):
-        t_f = median_ms(fused)
         fused_tokens = [o.clone() for o in outs]
-        t_u = median_ms(unfused)
+        for _ in range(max(3, args.warmup)):
+            l2_flush()
+            unfused()
+        torch.cuda.synchronize()
+        graphs = {"fused": graph_of(fused), "unfused": graph_of(unfused), "flush": graph_of(None)}
+        for g in graphs.values():
+            g.replay()
+        torch.cuda.synchronize()
+        t_flush = replay_ms(graphs["flush"])
+        t_f = (replay_ms(graphs["fused"]) - t_flush) / K
+        t_u = (replay_ms(graphs["unfused"]) - t_flush) / K
     assert ssv.get_status(status) == ssv.SSV_OK
     same = all(bool(torch.equal(u, v)) for u, v in zip(fused_tokens, outs))
     nbytes, flops, ver = lmhead_work(x)
@@ -646,7 +669,7 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
             "frac": round(lb / t_f, 4), "tflops": round(flops / (t_f * 1e-3) / 1e12, 1),
             "gbs": round(nbytes / (t_f * 1e-3) / 1e9, 1), "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
             "traffic": measured_traffic("lmhead", args.config),
-            "note": "timed alone, not in the step; logits never written"}
+            "launch": "cuda_graph", "note": "timed alone, not in the step; logits never written"}
 
 
 def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):

@@ -8,7 +8,13 @@
 // kernel forms l = H W^T on the tensor cores and takes the decision of every
 // verified row in the epilogue, so no logits row ever reaches memory.
 //
-// Work split.  The slots form Mt = ceil(S / 128) M-tiles of 128 rows; the
+// Rows.  A gather kernel first lists the slots whose rows the acceptance
+// reads (stage <= min(gamma + 1, B)) in slot order and, unless that is every
+// slot, copies their hidden states into the workspace, so no tensor-core work
+// is spent on unverified stages.  The GEMM kernel counts the same rows
+// itself; it waits for the gather only when the rows were compacted.
+//
+// Work split.  The n verified rows form Mt = ceil(n / 128) M-tiles; the
 // vocabulary is cut into 256-column pieces (the last one narrower when 256
 // does not divide V) and the pieces into G contiguous ranges, G = min(SMs /
 // Mt, pieces).  CTA c = g * Mt + m computes tile m over range g.  The Mt CTAs
@@ -40,6 +46,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <algorithm>
 #include <mutex>
 
 namespace ssv {
@@ -50,6 +57,8 @@ using namespace ptx;
 constexpr int kLmThreads = 192;
 constexpr int kLmStages = 4;
 constexpr int kLmMaxSlots = 2048;
+constexpr int kGatherThreads = 256;
+constexpr int kGatherPer = kLmMaxSlots / kGatherThreads;  // slots per thread in the listing
 constexpr int kLmMaxBatch = 2048;
 constexpr uint32_t kLmABytes = 128u * 128u;  // 128 rows x 64 bf16
 constexpr uint32_t kLmBBytes = 256u * 128u;  // 256 rows x 64 bf16
@@ -69,12 +78,16 @@ constexpr uint32_t SM_B = SM_A + kLmStages * kLmABytes;
 constexpr uint32_t SM_BAR = SM_B + kLmStages * kLmBBytes;
 constexpr uint32_t SM_MISC = SM_BAR + 8u * LB_COUNT;  // tmem slot, abort flag, tile-complete flag
 constexpr uint32_t SM_WALK = (SM_MISC + 16u + 15u) & ~15u;
-constexpr uint32_t SM_TOTAL = SM_WALK + 4u * sizeof(WalkSmem);
+constexpr uint32_t SM_SEQOF = SM_WALK + 4u * sizeof(WalkSmem);  // u16 per slot: its sequence
+constexpr uint32_t SM_NEED = SM_SEQOF + 2u * kLmMaxSlots;         // u8 per sequence: rows it needs
+constexpr uint32_t SM_WCNT = SM_NEED + kLmMaxBatch;               // per-warp counts
+constexpr uint32_t SM_TOTAL = SM_WCNT + 64u;
 constexpr size_t kLmSmem = SM_TOTAL + 1024;  // + alignment slack of the dynamic base
 static_assert(kLmSmem <= 227u * 1024u, "shared memory");
 
 struct LmMaps {
-  CUtensorMap h;    // hidden states [S, hidden], box 64 x 128
+  CUtensorMap h;    // compacted hidden states of the verified rows [S, hidden], box 64 x 128
+  CUtensorMap h0;   // the caller's hidden states [S, hidden], box 64 x 128 (every slot verified)
   CUtensorMap w;    // LM head [V, hidden], box 64 x 256
   CUtensorMap w64;  // LM head, box 64 x 64 (narrower pieces)
   CUtensorMap w16;  // LM head, box 64 x 16
@@ -83,12 +96,16 @@ struct LmMaps {
 struct LmParams {
   AcceptParams acc;  // metadata, outputs, row results and sequence counters (walk)
   int hidden, nk;    // nk = hidden / 64
-  int Mt, G, V16, NP;  // NP = 256-column pieces of the vocabulary
+  int Mt, V16, NP;     // Mt: M-tiles of the slot count (an upper bound); NP: 256-column pieces
   int use_noise, vec;
   float T;
   const float* noise;
   int n_noise_rows;
   const int32_t* noise_row;
+  const __nv_bfloat16* h_src;   // hidden states [S, hidden] (gather input)
+  __nv_bfloat16* h_rows;        // [S, hidden]: hidden states of the verified rows, compacted
+  int32_t* n_rows;              // [2]: verified rows, 1 if they are every slot (written by the gather)
+  int32_t* row_slot;            // [S]: slot of each compacted row
   int32_t* cnt_tile;            // [Mt]
   unsigned long long* rowkey;   // [Mt * 128]: best (score, index) key of each row, 0 = none
 };
@@ -171,6 +188,92 @@ __device__ __forceinline__ void lm_columns(const LmParams& p, uint32_t taddr, in
   }
 }
 
+// Sequence of every slot (0xFFFF: none) and rows each sequence needs (0: sizes
+// rejected), for the listing below.  Called by every thread of the CTA.
+__device__ __forceinline__ void seq_tables(const AcceptParams& a, unsigned short* seq_of, unsigned char* need_s) {
+  for (int i = threadIdx.x; i < kLmMaxSlots; i += blockDim.x) seq_of[i] = 0xFFFFu;
+  __syncthreads();
+  for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+    const int off = a.slot_off[b], B = a.block[b], g = a.gamma[b];
+    const bool ok = off >= 0 && B >= 1 && B <= 64 && g >= 0 && g <= B && off + B <= a.total_slots;
+    need_s[b] = ok ? (unsigned char)min(g + 1, B) : 0;
+    if (ok)
+      for (int j = 0; j < B; ++j) seq_of[off + j] = (unsigned short)b;
+  }
+  __syncthreads();
+}
+
+// Whether slot is listed: inside its sequence's sane extent, stage in 1..need.
+__device__ __forceinline__ int listed(const AcceptParams& a, const unsigned short* seq_of,
+                                      const unsigned char* need_s, int slot) {
+  if (slot >= a.total_slots || seq_of[slot] == 0xFFFFu) return 0;
+  const int st = a.tau[slot];
+  return (st >= 1 && st <= need_s[seq_of[slot]]) ? 1 : 0;
+}
+
+// Lists the verified slots in slot order (every CTA builds the same list;
+// CTA 0 publishes it) and copies their hidden-state rows, one warp per row,
+// rows dealt to CTAs in turn.  A slot is listed when it lies inside its
+// sequence's sane extent and its stage is in 1..min(gamma + 1, B); the GEMM
+// epilogue still checks the whole sequence before using a row (and reports
+// the sequences it rejects).
+__global__ void __launch_bounds__(kGatherThreads) lmhead_gather_kernel(const LmParams p) {
+  __shared__ int32_t list[kLmMaxSlots];
+  __shared__ unsigned short seq_of[kLmMaxSlots];
+  __shared__ unsigned char need_s[kLmMaxBatch];
+  __shared__ int32_t wsum[kGatherThreads / 32];
+  pdl_wait();  // hidden states and metadata may come from the kernels before this one
+  pdl_trigger();  // the GEMM may set up; it reads nothing of ours before its own wait
+  const AcceptParams& a = p.acc;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  seq_tables(a, seq_of, need_s);
+  int flag[kGatherPer];
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kGatherPer; ++i) {
+    flag[i] = listed(a, seq_of, need_s, tid * kGatherPer + i);
+    cnt += flag[i];
+  }
+  // exclusive scan of the per-thread counts (slot order = thread order)
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kGatherThreads / 32; ++w) {
+    before += (w < warp) ? wsum[w] : 0;
+    total += wsum[w];
+  }
+  int pos = before + incl - cnt;
+#pragma unroll
+  for (int i = 0; i < kGatherPer; ++i)
+    if (flag[i]) list[pos++] = tid * kGatherPer + i;
+  __syncthreads();
+  const bool identity = total == a.total_slots;  // then list[i] == i
+  if (blockIdx.x == 0) {
+    if (!identity)
+      for (int i = tid; i < total; i += kGatherThreads) p.row_slot[i] = list[i];
+    if (tid == 0) {
+      p.n_rows[0] = total;
+      p.n_rows[1] = identity ? 1 : 0;
+    }
+  }
+  if (identity) return;  // the GEMM reads the caller's rows directly
+  // copy: row i by CTA i mod gridDim, warp (i / gridDim) mod 8, 16-byte vectors
+  const size_t row_vec = (size_t)p.hidden / 8;  // 16-byte vectors per row
+  const int nw = kGatherThreads / 32;
+  for (int i = blockIdx.x + gridDim.x * warp; i < total; i += gridDim.x * nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.h_src) + (size_t)list[i] * row_vec;
+    uint4* dst = reinterpret_cast<uint4*>(p.h_rows) + (size_t)i * row_vec;
+    for (size_t e = lane; e < row_vec; e += 32) dst[e] = __ldg(src + e);
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kLmThreads, 1)
 lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
@@ -184,9 +287,6 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
   WalkSmem* walk = reinterpret_cast<WalkSmem*>(smem + SM_WALK);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x % p.Mt, g = blockIdx.x / p.Mt;
-  const int j_begin = (int)(((long long)p.NP * g) / p.G);
-  const int npieces = (int)(((long long)p.NP * (g + 1)) / p.G) - j_begin;  // pieces of this range
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -194,6 +294,7 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
     for (int i = 0; i < LB_COUNT; ++i) mbar_init(bar(i), (i == LB_ACCE || i == LB_ACCE + 1) ? 4u : 1u);
     fence_mbar_init();
     tma_prefetch(&maps.h);
+    tma_prefetch(&maps.h0);
     tma_prefetch(&maps.w);
     tma_prefetch(&maps.w64);
     tma_prefetch(&maps.w16);
@@ -203,8 +304,40 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // hidden states, metadata and noise may come from the kernels before this one
-  pdl_trigger();
+  // Count the verified rows here (the gather kernel reaches the same count):
+  // as the second kernel of the call this one may read the call's inputs
+  // before its wait, since the gather lets it start only after its own wait.
+  // When every slot is verified the rows are read from the caller's hidden
+  // states and nothing of the gather's is needed: the wait moves to the end.
+  int n_rows;
+  {
+    unsigned short* seq_of = reinterpret_cast<unsigned short*>(smem + SM_SEQOF);
+    unsigned char* need_s = smem + SM_NEED;
+    int* wcnt = reinterpret_cast<int*>(smem + SM_WCNT);
+    seq_tables(p.acc, seq_of, need_s);
+    int c = 0;
+    for (int slot = threadIdx.x; slot < p.acc.total_slots; slot += blockDim.x) c += listed(p.acc, seq_of, need_s, slot);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (lane == 0) wcnt[warp] = c;
+    __syncthreads();
+    n_rows = 0;
+    for (int w = 0; w < kLmThreads / 32; ++w) n_rows += wcnt[w];
+  }
+  const bool identity = n_rows == p.acc.total_slots;
+  if (!identity) {
+    pdl_wait();  // the compacted rows (and, through the gather, every kernel before)
+    pdl_trigger();
+  }
+  // tiles of the verified rows and this CTA's (tile, range); CTAs past the
+  // last (tile, range) pair have no work
+  const CUtensorMap* hmap = identity ? &maps.h0 : &maps.h;
+  const int Mt = (n_rows + 127) / 128;
+  const int G = Mt > 0 ? min((int)gridDim.x / Mt, p.NP) : 0;
+  const bool active = (int)blockIdx.x < G * Mt;
+  const int m = active ? (int)blockIdx.x % Mt : 0, g = active ? (int)blockIdx.x / Mt : 0;
+  const int j_begin = active ? (int)(((long long)p.NP * g) / G) : 0;
+  const int npieces = active ? (int)(((long long)p.NP * (g + 1)) / G) - j_begin : 0;  // pieces of this range
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -222,7 +355,7 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
           }
           const uint32_t fb = bar(LB_FULL + s);
           mbar_expect_tx(fb, kLmABytes + (uint32_t)w * 128u);
-          tma_load_2d(sbase + SM_A + s * kLmABytes, &maps.h, kc * 64, m * 128, fb);
+          tma_load_2d(sbase + SM_A + s * kLmABytes, hmap, kc * 64, m * 128, fb);
           const uint32_t bdst = sbase + SM_B + s * kLmBBytes;
           if (w == 256) {
             tma_load_2d(bdst, &maps.w, kc * 64, v0, fb);
@@ -276,15 +409,9 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
     const int q = warp & 3;           // TMEM lane quarter of this warp
     const int r = 32 * q + lane;      // row of the tile
     const int et = threadIdx.x - 64;  // 0..127
-    const int slot = m * 128 + r;
     const AcceptParams& a = p.acc;
-    // sizes of every sequence are checked somewhere (a sequence with no slot
-    // is seen by no row): sequence b by CTA b mod gridDim, thread (b / gridDim) mod 128
-    for (int b = blockIdx.x + gridDim.x * et; b < a.batch; b += gridDim.x * 128) {
-      const int B = a.block[b], gm = a.gamma[b], off = a.slot_off[b];
-      if (!(off >= 0 && B >= 1 && B <= 64 && gm >= 0 && gm <= B && off + B <= a.total_slots))
-        report(a.dev_status, SSV_ERR_BAD_TAU);
-    }
+    const int ci = m * 128 + r;  // compacted row
+    const int slot = (active && ci < n_rows) ? (identity ? ci : p.row_slot[ci]) : a.total_slots;
     // this row: sequence, stage, and whether it is verified / tested.  A
     // sequence is usable when its sizes are sane, its stage map permutes
     // 1..B and (coupled noise) every verified slot has a table row; every row
@@ -315,16 +442,33 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
         }
         perm = perm && seen == ((B >= 64) ? ~0ull : ((1ull << B) - 1ull));
         const int st = a.tau[slot];
-        if (slot == off) {
-          if (!perm) report(a.dev_status, SSV_ERR_BAD_TAU);
-          else if (!noise_ok) report(a.dev_status, SSV_ERR_INVALID);
-        }
         verified = perm && noise_ok && st <= need;
         tested = st <= gm;
         if (verified && p.use_noise) nrow = p.noise + (size_t)p.noise_row[slot] * (size_t)a.V;
       } else {
         b = -1;
       }
+    }
+    // rejected sequences, reported once: sequence b by CTA b mod gridDim, epilogue
+    // warp (b / gridDim) mod 4 (runs while the first piece is multiplied)
+    for (int sb = blockIdx.x + gridDim.x * q; sb < a.batch; sb += gridDim.x * 4) {
+      const int soff = a.slot_off[sb], sB = a.block[sb], sg = a.gamma[sb];
+      if (!(soff >= 0 && sB >= 1 && sB <= 64 && sg >= 0 && sg <= sB && soff + sB <= a.total_slots)) {
+        if (lane == 0) report(a.dev_status, SSV_ERR_BAD_TAU);
+        continue;
+      }
+      if (!warp_tau_is_permutation(a.tau + soff, sB)) {
+        if (lane == 0) report(a.dev_status, SSV_ERR_BAD_TAU);
+        continue;
+      }
+      bool bad_row = false;
+      if (p.use_noise)
+        for (int j = lane; j < sB; j += 32)
+          if (a.tau[soff + j] <= min(sg + 1, sB)) {
+            const int nr = p.noise_row[soff + j];
+            bad_row = bad_row || nr < 0 || nr >= p.n_noise_rows;
+          }
+      if (__any_sync(0xffffffffu, bad_row) && lane == 0) report(a.dev_status, SSV_ERR_INVALID);
     }
     // running first-argmax over the pieces of this CTA's range
     float best = -INFINITY;
@@ -364,13 +508,13 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
     }
     // fold this range's best into the row's key; the CTA that completes the
     // tile reads the keys
-    if (ok && bi != INT_MAX) atomicMax(p.rowkey + (size_t)m * 128 + r, score_key(best, bi));
+    if (active && ok && bi != INT_MAX) atomicMax(p.rowkey + (size_t)m * 128 + r, score_key(best, bi));
     __threadfence();
     epi_sync();
-    if (et == 0 && ok && !*abort) {
+    if (et == 0 && active && ok && !*abort) {
       int prev;
       asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.cnt_tile + m) : "memory");
-      *tile_done = (prev + 1 == p.G) ? 1 : 0;
+      *tile_done = (prev + 1 == G) ? 1 : 0;
     }
     epi_sync();
     if (*tile_done) {
@@ -406,6 +550,10 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (identity && threadIdx.x == 0) {  // never complete before the gather
+    pdl_wait();
+    pdl_trigger();
+  }
   if (*abort && threadIdx.x == 0) report(p.acc.dev_status, SSV_ERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
@@ -452,8 +600,8 @@ int lm_sm_count() {
 }
 
 struct LmLayout {
-  size_t cnt_tile, cnt_seq, rowkey, rowres, total;
-  int Mt, G, V16, NP;
+  size_t cnt_tile, cnt_seq, n_rows, row_slot, h_rows, rowkey, rowres, total;
+  int Mt, V16, NP;
 };
 
 LmLayout lm_layout(const ssv_lmhead_accept_args* a, int nsm) {
@@ -461,12 +609,13 @@ LmLayout lm_layout(const ssv_lmhead_accept_args* a, int nsm) {
   L.Mt = (a->total_slots + 127) / 128;
   L.V16 = (a->V + 15) / 16;
   L.NP = (L.V16 + 15) / 16;
-  L.G = nsm / (L.Mt > 0 ? L.Mt : 1);
-  if (L.G > L.NP) L.G = L.NP;
-  if (L.G < 1) L.G = 1;
+  (void)nsm;
   size_t o = 0;
   L.cnt_tile = o;  o += sizeof(int32_t) * (size_t)L.Mt;  // counters first, contiguous
   L.cnt_seq = o;   o = align_up(o + sizeof(int32_t) * (size_t)a->batch, 256);
+  L.n_rows = o;    o = align_up(o + 2 * sizeof(int32_t), 256);                               // written every call
+  L.row_slot = o;  o = align_up(o + sizeof(int32_t) * (size_t)a->total_slots, 256);
+  L.h_rows = o;    o = align_up(o + 2u * (size_t)a->total_slots * (size_t)a->hidden, 256);
   L.rowkey = o;    o = align_up(o + sizeof(unsigned long long) * (size_t)L.Mt * 128, 256);  // zero between calls
   L.rowres = o;    o = align_up(o + sizeof(RowResult) * (size_t)a->total_slots, 256);
   L.total = o;
@@ -532,12 +681,13 @@ extern "C" ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* w
   const LmLayout L = lm_layout(a, nsm);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
   LmMaps maps;
-  if (!encode_rows(&maps.h, a->hidden_states, a->total_slots, a->hidden, 128) ||
+  char* w = static_cast<char*>(ws);
+  if (!encode_rows(&maps.h, w + L.h_rows, a->total_slots, a->hidden, 128) ||
+      !encode_rows(&maps.h0, a->hidden_states, a->total_slots, a->hidden, 128) ||
       !encode_rows(&maps.w, a->lm_head, a->V, a->hidden, 256) ||
       !encode_rows(&maps.w64, a->lm_head, a->V, a->hidden, 64) ||
       !encode_rows(&maps.w16, a->lm_head, a->V, a->hidden, 16))
     return SSV_ERR_INVALID;
-  char* w = static_cast<char*>(ws);
   LmParams p;
   memset(&p, 0, sizeof(p));
   const bool noise = a->mode == SSV_ACCEPT_GUMBEL && a->T > 0.f;
@@ -561,7 +711,6 @@ extern "C" ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* w
   p.hidden = a->hidden;
   p.nk = a->hidden / 64;
   p.Mt = L.Mt;
-  p.G = L.G;
   p.V16 = L.V16;
   p.NP = L.NP;
   p.use_noise = noise ? 1 : 0;
@@ -571,9 +720,15 @@ extern "C" ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* w
   p.n_noise_rows = a->n_noise_rows;
   p.noise_row = a->noise_row;
   p.cnt_tile = reinterpret_cast<int32_t*>(w + L.cnt_tile);
+  p.h_src = static_cast<const __nv_bfloat16*>(a->hidden_states);
+  p.h_rows = reinterpret_cast<__nv_bfloat16*>(w + L.h_rows);
+  p.n_rows = reinterpret_cast<int32_t*>(w + L.n_rows);
+  p.row_slot = reinterpret_cast<int32_t*>(w + L.row_slot);
   p.rowkey = reinterpret_cast<unsigned long long*>(w + L.rowkey);
-  const int grid = L.Mt * L.G;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = noise ? lm_launch<SSV_ACCEPT_GUMBEL>(maps, p, grid, s) : lm_launch<SSV_ACCEPT_ARGMAX>(maps, p, grid, s);
+  const int gather_grid = std::min(nsm, std::max(1, (a->total_slots + 15) / 16));
+  cudaError_t e = launch_pdl(lmhead_gather_kernel, dim3(gather_grid), dim3(kGatherThreads), 0, s, p);
+  if (e == cudaSuccess)
+    e = noise ? lm_launch<SSV_ACCEPT_GUMBEL>(maps, p, nsm, s) : lm_launch<SSV_ACCEPT_ARGMAX>(maps, p, nsm, s);
   return e == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }
