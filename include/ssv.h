@@ -374,7 +374,9 @@ SSV_API ssv_status ssv_commit(const ssv_commit_args* a, void* stream);
  * offered here (it needs the draft model's logits as well).
  *
  * hidden_states [total_slots, hidden] bf16 device, row = slot (slot order);
- *               every row is read (rows of unverified stages too).
+ *               only rows of verified stages are read (when some stages
+ *               are not verified, a first kernel copies the verified rows
+ *               into the workspace and the GEMM runs over those).
  * lm_head       [V, hidden] bf16 device, row-major.
  * draft_tokens, tau, noise_row: [total_slots] int32 device
  * block, gamma, slot_off: [batch] int32 device (as for ssv_accept)
@@ -389,8 +391,9 @@ SSV_API ssv_status ssv_commit(const ssv_commit_args* a, void* stream);
  *         SSV_ERR_BAD_TAU (that sequence's outputs are not written),
  *         SSV_ERR_INVALID (a verified slot's noise_row outside the table;
  *         likewise), SSV_ERR_TIMEOUT (a bounded wait ran out).
- * Scheduling: one CTA per SM; the CTA that finishes an M-tile last merges
- * its rows; no CTA waits on another.
+ * Scheduling: two kernels chained by programmatic dependent launch (a
+ * gather of the verified rows, then the GEMM with one CTA per SM); the CTA
+ * that finishes an M-tile last merges its rows; no CTA waits on another.
  * ---------------------------------------------------------------------- */
 typedef struct {
   ssv_accept_mode mode;        /* SSV_ACCEPT_ARGMAX or SSV_ACCEPT_GUMBEL */
