@@ -1,4 +1,8 @@
-// ssv_bench: native timing of the library on a named synthetic workload.
+// ssv_bench: native timing of the library on a named synthetic workload:
+// rotation, verify attention, acceptance, the commit (each sequence appends
+// its prompt rows and gamma / 2 accepted rows) and the fused LM head +
+// acceptance (hidden width Hq * head_dim; greedy unless the workload uses
+// coupled noise).
 //
 // Buffers are allocated here (this is a measurement utility, not a hot-path
 // call) and filled on the device by a counter-hash generator (splitmix64
@@ -156,7 +160,16 @@ extern "C" ssv_status ssv_bench(const char* config, int32_t iters, char* json_ou
   float *d_ua = nullptr, *d_us = nullptr;
   cudaStream_t st = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
-  std::vector<float> t_rope, t_attn, t_acc;
+  std::vector<float> t_rope, t_attn, t_acc, t_commit, t_lm;
+  void *k_dst = nullptr, *v_dst = nullptr, *lm_w = nullptr, *lm_h = nullptr, *ws_l = nullptr;
+  int32_t *d_cnacc = nullptr, *d_doff = nullptr, *d_dcap = nullptr, *d_newlen = nullptr;
+  double commit_bytes = 0, lm_bytes = 0, lm_flops = 0;
+  size_t ws_lm = 0;
+  const int hidden = Hq * d;
+  ssv_commit_args ma;
+  ssv_lmhead_accept_args la;
+  memset(&ma, 0, sizeof(ma));
+  memset(&la, 0, sizeof(la));
   const size_t flush_bytes = 256u << 20;
   const int V = cfg->V;
   double acc_bytes = 0;
@@ -260,6 +273,52 @@ extern "C" ssv_status ssv_bench(const char* config, int32_t iters, char* json_ou
       acc_bytes += rowsb * V * 4.0;
     }
   }
+  {  // commit: every sequence appends its N prompt rows and gamma / 2 accepted data rows
+    std::vector<int32_t> nacc(batch), doff(batch), dcap(batch);
+    int drows = 0;
+    for (int b = 0; b < batch; ++b) {
+      nacc[b] = gammas[b] / 2;
+      dcap[b] = seqs[b].cache_len + seqs[b].new_len + seqs[b].block;
+      doff[b] = drows;
+      drows += dcap[b];
+      commit_bytes += 2.0 * 2.0 * (seqs[b].new_len + nacc[b]) * Hkv * d * es;
+    }
+    BENCH_CHECK(cudaMalloc(&k_dst, (size_t)drows * Hkv * d * es));
+    BENCH_CHECK(cudaMalloc(&v_dst, (size_t)drows * Hkv * d * es));
+    BENCH_CHECK(cudaMalloc((void**)&d_cnacc, sizeof(int32_t) * batch));
+    BENCH_CHECK(cudaMalloc((void**)&d_doff, sizeof(int32_t) * batch));
+    BENCH_CHECK(cudaMalloc((void**)&d_dcap, sizeof(int32_t) * batch));
+    BENCH_CHECK(cudaMalloc((void**)&d_newlen, sizeof(int32_t) * batch));
+    BENCH_CHECK(cudaMemcpyAsync(d_cnacc, nacc.data(), sizeof(int32_t) * batch, cudaMemcpyHostToDevice, st));
+    BENCH_CHECK(cudaMemcpyAsync(d_doff, doff.data(), sizeof(int32_t) * batch, cudaMemcpyHostToDevice, st));
+    BENCH_CHECK(cudaMemcpyAsync(d_dcap, dcap.data(), sizeof(int32_t) * batch, cudaMemcpyHostToDevice, st));
+    BENCH_CHECK(cudaStreamSynchronize(st));
+    ma.k_new = kn; ma.v_new = vn; ma.k_dst = k_dst; ma.v_dst = v_dst; ma.dtype = cfg->dt; ma.Hkv = Hkv; ma.d = d;
+    ma.seqs = d_seqs; ma.batch = batch; ma.tau = d_tau; ma.n_acc = d_cnacc; ma.dst_off = d_doff; ma.dst_cap = d_dcap;
+    ma.new_len = d_newlen; ma.total_rows = rows; ma.total_slots = slots; ma.dst_rows = drows;
+    ma.dev_status = d_status;
+  }
+  if (cfg->mode >= 0 && slots <= 2048) {  // fused LM head over the mask slots
+    BENCH_CHECK(cudaMalloc(&lm_w, (size_t)V * hidden * 2));
+    BENCH_CHECK(cudaMalloc(&lm_h, (size_t)slots * hidden * 2));
+    fill_normal<__nv_bfloat16><<<2048, 256, 0, st>>>((__nv_bfloat16*)lm_w, (size_t)V * hidden, 12, 1.f);
+    fill_normal<__nv_bfloat16><<<256, 256, 0, st>>>((__nv_bfloat16*)lm_h, (size_t)slots * hidden, 13,
+                                                     1.f / sqrtf((float)hidden));
+    BENCH_CHECK(cudaGetLastError());
+    const bool gumbel = cfg->mode == SSV_ACCEPT_GUMBEL;
+    la.mode = gumbel ? SSV_ACCEPT_GUMBEL : SSV_ACCEPT_ARGMAX; la.T = gumbel ? cfg->T : 0.f; la.V = V;
+    la.hidden = hidden; la.batch = batch; la.total_slots = slots; la.hidden_states = lm_h; la.lm_head = lm_w;
+    la.draft_tokens = d_draft; la.tau = d_tau; la.block = d_blocks; la.gamma = d_gam; la.slot_off = d_soff;
+    la.noise = (const float*)noise; la.n_noise_rows = slots; la.noise_row = d_nrow; la.n_acc = d_nacc;
+    la.n_out = d_nout; la.tokens = d_tok; la.dev_status = d_status;
+    BENCH_SSV(ssv_lmhead_accept_workspace(&la, &ws_lm));
+    BENCH_CHECK(cudaMalloc(&ws_l, std::max<size_t>(ws_lm, 256)));
+    BENCH_CHECK(cudaMemsetAsync(ws_l, 0, std::max<size_t>(ws_lm, 256), st));
+    double ver = 0;
+    for (int b = 0; b < batch; ++b) ver += std::min(gammas[b] + 1, blocks[b]);
+    lm_bytes = (double)V * hidden * 2 + (double)slots * hidden * 2 + ((gumbel && cfg->T > 0.f) ? ver * V * 4.0 : 0.0);
+    lm_flops = 2.0 * ver * V * hidden;
+  }
   BENCH_CHECK(cudaStreamSynchronize(st));
 
   for (int it = -3; it < iters; ++it) {
@@ -287,28 +346,49 @@ extern "C" ssv_status ssv_bench(const char* config, int32_t iters, char* json_ou
       BENCH_CHECK(cudaEventElapsedTime(&ms, e0, e1));
       if (it >= 0) t_acc.push_back(ms);
     }
+    BENCH_CHECK(cudaMemsetAsync(flush, it & 0xff, flush_bytes, st));
+    BENCH_CHECK(cudaEventRecord(e0, st));
+    BENCH_SSV(ssv_commit(&ma, st));
+    BENCH_CHECK(cudaEventRecord(e1, st));
+    BENCH_CHECK(cudaEventSynchronize(e1));
+    BENCH_CHECK(cudaEventElapsedTime(&ms, e0, e1));
+    if (it >= 0) t_commit.push_back(ms);
+    if (lm_w) {
+      BENCH_CHECK(cudaMemsetAsync(flush, it & 0xff, flush_bytes, st));
+      BENCH_CHECK(cudaEventRecord(e0, st));
+      BENCH_SSV(ssv_lmhead_accept(&la, ws_l, std::max<size_t>(ws_lm, 256), st));
+      BENCH_CHECK(cudaEventRecord(e1, st));
+      BENCH_CHECK(cudaEventSynchronize(e1));
+      BENCH_CHECK(cudaEventElapsedTime(&ms, e0, e1));
+      if (it >= 0) t_lm.push_back(ms);
+    }
   }
   BENCH_SSV(ssv_get_status(d_status, st));
   {
     const Timing tr = summarize(t_rope), ta = summarize(t_attn);
-    Timing tc = {0, 0, 0};
+    Timing tc = {0, 0, 0}, tm = summarize(t_commit), tl = {0, 0, 0};
     if (!t_acc.empty()) tc = summarize(t_acc);
+    if (!t_lm.empty()) tl = summarize(t_lm);
     const int n = snprintf(
         json_out, json_len,
         "{\"config\": \"%s\", \"iters\": %d, \"rope_us\": [%.3f, %.3f, %.3f], \"rope_bytes\": %.0f, "
         "\"attn_us\": [%.3f, %.3f, %.3f], \"attn_bytes\": %.0f, \"attn_flops\": %.0f, "
         "\"attn_gbs\": %.1f, \"attn_tflops\": %.2f, \"accept_us\": [%.3f, %.3f, %.3f], \"accept_bytes\": %.0f, "
-        "\"accept_gbs\": %.1f, \"accept_seq_per_s\": %.1f, \"t_verify_us\": %.3f}",
+        "\"accept_gbs\": %.1f, \"accept_seq_per_s\": %.1f, \"t_verify_us\": %.3f, "
+        "\"commit_us\": [%.3f, %.3f, %.3f], \"commit_bytes\": %.0f, \"lmhead_hidden\": %d, "
+        "\"lmhead_us\": [%.3f, %.3f, %.3f], \"lmhead_bytes\": %.0f, \"lmhead_flops\": %.0f}",
         cfg->name, iters, tr.med, tr.p10, tr.p90, rope_bytes, ta.med, ta.p10, ta.p90, attn_bytes, attn_flops,
         attn_bytes / (ta.med * 1e3), attn_flops / (ta.med * 1e6), tc.med, tc.p10, tc.p90, acc_bytes,
         tc.med > 0 ? acc_bytes / (tc.med * 1e3) : 0.0, tc.med > 0 ? batch / (tc.med * 1e-6) : 0.0,
-        tr.med + ta.med + tc.med);
+        tr.med + ta.med + tc.med, tm.med, tm.p10, tm.p90, commit_bytes, hidden, tl.med, tl.p10, tl.p90, lm_bytes,
+        lm_flops);
     if (n < 0 || (size_t)n >= json_len) rc = SSV_ERR_INVALID;
   }
 done:
   cudaStreamSynchronize(st);
   void* bufs[] = {q, kn, vn, kc, vc, o, logits, dlogits, noise, flush, ws_a, ws_c, d_seqs, d_tau, d_blocks,
-                  d_gam, d_soff, d_draft, d_nrow, d_nacc, d_nout, d_tok, d_status, d_ua, d_us};
+                  d_gam, d_soff, d_draft, d_nrow, d_nacc, d_nout, d_tok, d_status, d_ua, d_us, k_dst, v_dst,
+                  lm_w, lm_h, ws_l, d_cnacc, d_doff, d_dcap, d_newlen};
   for (void* p : bufs)
     if (p) cudaFree(p);
   if (e0) cudaEventDestroy(e0);
