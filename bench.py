@@ -128,7 +128,8 @@ KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"],
                   "accept_reduce_kernel": ["accept.cu", "accept.cuh"],
                   "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"],
                   "commit_kernel": ["commit.cu"],
-                  "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"]}
+                  "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"],
+                  "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"]}
 
 
 def measured_traffic(op: str, workload: str):

@@ -264,13 +264,22 @@ __global__ void __launch_bounds__(kGatherThreads) lmhead_gather_kernel(const LmP
     }
   }
   if (identity) return;  // the GEMM reads the caller's rows directly
-  // copy: row i by CTA i mod gridDim, warp (i / gridDim) mod 8, 16-byte vectors
+  // copy: row i by CTA i mod gridDim, warp (i / gridDim) mod 8, 16-byte vectors,
+  // eight loads in flight per lane before their stores
   const size_t row_vec = (size_t)p.hidden / 8;  // 16-byte vectors per row
   const int nw = kGatherThreads / 32;
   for (int i = blockIdx.x + gridDim.x * warp; i < total; i += gridDim.x * nw) {
     const uint4* src = reinterpret_cast<const uint4*>(p.h_src) + (size_t)list[i] * row_vec;
     uint4* dst = reinterpret_cast<uint4*>(p.h_rows) + (size_t)i * row_vec;
-    for (size_t e = lane; e < row_vec; e += 32) dst[e] = __ldg(src + e);
+    for (size_t e0 = lane; e0 < row_vec; e0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (e0 + 32 * t < row_vec) v[t] = __ldg(src + e0 + 32 * t);
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+        if (e0 + 32 * t < row_vec) dst[e0 + 32 * t] = v[t];
+    }
   }
 }
 
