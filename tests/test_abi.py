@@ -105,3 +105,48 @@ def test_bench_rejects_unknown_config(L):
     buf = C.create_string_buffer(256)
     assert L.ssv_bench(b"nope", 1, buf, 256) == ssv.SSV_ERR_INVALID
     assert L.ssv_bench(b"tiny", 0, buf, 256) == ssv.SSV_ERR_INVALID
+
+
+def _commit(**kw):
+    base = dict(k_new=16, v_new=4096, k_dst=1 << 20, v_dst=1 << 21, dtype=ssv.SSV_BF16, Hkv=2, d=128, seqs=16,
+                batch=2, tau=16, n_acc=16, dst_off=16, dst_cap=16, new_len=16, total_rows=4, total_slots=4,
+                dst_rows=20, dev_status=None)
+    base.update(kw)
+    return ssv.CommitArgs(**base)
+
+
+def test_commit_validation(L):
+    cases = [(dict(dtype=7), ssv.SSV_ERR_INVALID), (dict(d=96), ssv.SSV_ERR_UNSUPPORTED),
+             (dict(batch=-1), ssv.SSV_ERR_INVALID), (dict(Hkv=0), ssv.SSV_ERR_INVALID),
+             (dict(total_slots=-1), ssv.SSV_ERR_INVALID), (dict(n_acc=None), ssv.SSV_ERR_INVALID),
+             (dict(new_len=None), ssv.SSV_ERR_INVALID), (dict(k_new=24), ssv.SSV_ERR_INVALID),   # misaligned
+             (dict(k_dst=16), ssv.SSV_ERR_INVALID),                                             # overlaps k_new
+             (dict(v_dst=4096 + 512), ssv.SSV_ERR_INVALID)]                                     # overlaps v_new
+    for kw, code in cases:
+        assert L.ssv_commit(C.byref(_commit(**kw)), None) == code, kw
+    assert L.ssv_commit(C.byref(_commit(batch=0)), None) == ssv.SSV_OK   # nothing to do
+    assert L.ssv_commit(None, None) == ssv.SSV_ERR_INVALID
+
+
+def _lmh(**kw):
+    base = dict(mode=ssv.ARGMAX, T=0.0, V=1000, hidden=128, batch=2, total_slots=8, hidden_states=256,
+                lm_head=512, draft_tokens=16, tau=16, block=16, gamma=16, slot_off=16, noise=None,
+                n_noise_rows=0, noise_row=None, n_acc=16, n_out=16, tokens=16, dev_status=None)
+    base.update(kw)
+    return ssv.LmheadArgs(**base)
+
+
+def test_lmhead_validation(L):
+    cases = [(dict(mode=ssv.REJECT, T=1.0), ssv.SSV_ERR_INVALID), (dict(T=float("nan")), ssv.SSV_ERR_NOT_FINITE),
+             (dict(T=-0.5), ssv.SSV_ERR_NOT_FINITE), (dict(hidden=96), ssv.SSV_ERR_INVALID),
+             (dict(hidden=0), ssv.SSV_ERR_INVALID), (dict(V=0), ssv.SSV_ERR_INVALID),
+             (dict(total_slots=4096), ssv.SSV_ERR_UNSUPPORTED), (dict(batch=3000), ssv.SSV_ERR_UNSUPPORTED),
+             (dict(lm_head=None), ssv.SSV_ERR_INVALID), (dict(hidden_states=520), ssv.SSV_ERR_INVALID),
+             (dict(mode=ssv.GUMBEL, T=1.0), ssv.SSV_ERR_INVALID),                 # no noise table
+             (dict(mode=ssv.GUMBEL, T=1.0, noise=18, noise_row=16, n_noise_rows=8), ssv.SSV_ERR_INVALID)]
+    n = C.c_size_t(0)
+    for kw, code in cases:
+        assert L.ssv_lmhead_accept(C.byref(_lmh(**kw)), None, 0, None) == code, kw
+        assert L.ssv_lmhead_accept_workspace(C.byref(_lmh(**kw)), C.byref(n)) == code, kw
+    assert L.ssv_lmhead_accept(C.byref(_lmh(batch=0)), None, 0, None) == ssv.SSV_OK
+    assert L.ssv_lmhead_accept_workspace(C.byref(_lmh(total_slots=0)), C.byref(n)) == ssv.SSV_OK and n.value == 0
