@@ -77,6 +77,8 @@ DECISION_CASES = {
     "argmax_full_vocab": (oacc.MODE_ARGMAX, 0.0, 151936, 2048, 64),
     "gumbel_full_vocab": (oacc.MODE_GUMBEL, 1.5, 151936, 1024, 96),
     "argmax_many_tiles": (oacc.MODE_ARGMAX, 0.0, 32768, 4096, 1030),  # 9 M-tiles, K = 4096
+    "argmax_tiny_vocab": (oacc.MODE_ARGMAX, 0.0, 100, 64, 3),          # one 112-column piece, one CTA
+    "gumbel_max_slots": (oacc.MODE_GUMBEL, 1.0, 512, 64, 2048),        # 2048 sequences: 16 M-tiles
 }
 
 
