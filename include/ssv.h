@@ -77,6 +77,12 @@ typedef enum {
  * stage map occupies tau[tau_off .. tau_off + B).  Sequences are packed in
  * increasing q_off order without overlap (q_off[b] + N_b + 2B_b <=
  * q_off[b+1]): kernels find a row's sequence by binary search on q_off.
+ * The table is a precondition of every call that takes it: each extent lies
+ * inside its buffer (q_off + N + 2B <= total_rows, kv_off + C <= the cache
+ * rows, tau_off + B <= total_slots, all offsets >= 0).  ssv_commit checks
+ * the stage-map extent and its destination room on the device; the rotation
+ * and attention kernels use the offsets as given, so a table outside its
+ * buffers makes them read (and the attention write) outside the buffers.
  */
 typedef struct {
   int32_t cache_len;  /* C >= 0 */
