@@ -191,12 +191,9 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def mark(self, which):
-        setattr(self, which, time.time())
-
     def stop(self):
         if self.proc is None:
-            return None
+            return
         time.sleep(0.12)
         self.proc.terminate()
         try:
@@ -204,7 +201,16 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self._th.join(timeout=2)
-        sel = [l for (t, l) in self.lines if self.t0 - 0.1 <= t <= self.t1 + 0.1] or [l for _, l in self.lines[-3:]]
+        self.proc = None
+
+    def window(self, t0, t1):
+        """Median SM clock, maximum clock and throttle reasons of the samples
+        taken between host times t0 and t1 (the last few if none fell in)."""
+        if self.proc is None and not self.lines:
+            return None
+        time.sleep(0.12)
+        lines = list(self.lines)
+        sel = [l for (t, l) in lines if t0 - 0.1 <= t <= t1 + 0.1] or [l for _, l in lines[-3:]]
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for l in sel:
@@ -329,11 +335,229 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+class ConfigRun:
+    """Device buffers, argument blocks and timed ops of one named workload:
+    ssv_rope_copy, ssv_verify_attn and ssv_accept, each alone, and the whole
+    step (ssv_verify_step) — plus the commit step for the headline workload."""
+
+    def __init__(self, config, dev, with_commit):
+        import torch
+        from diffusion_speculative_verification_gb300 import ssv, io as sio
+        self.config = config
+        self.dev = dev
+        a = self.a = W.workload_attn(config)
+        xi = ACCEPT_INDEX[config]
+        x = self.x = None if xi is None else W.workload_accept(config, xi)
+        t = self.t = sio.attn_to_device(a, dev)
+        acc = self.acc = None if x is None else sio.accept_to_device(x, dev)
+        out_dtype = torch.bfloat16 if a.dtype == W.BF16 else torch.float32
+        self.out_b = 2 if a.dtype == W.BF16 else 4
+        self.qo = torch.empty_like(t["q"])
+        self.ko = torch.empty_like(t["k_new"])
+        self.o = torch.empty(t["q"].shape, dtype=out_dtype, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.batch = t["batch"]
+        self.aargs = ssv.attn_args(self.qo, t["k_cache"], t["v_cache"], self.ko, t["v_new"], self.o, self.batch,
+                                   t["tau"], 0.0, self.status)
+        self.ws_attn = torch.zeros(max(256, ssv.verify_attn_workspace_bytes(self.aargs)), dtype=torch.uint8,
+                                   device=dev)
+        self.rargs = ssv.rope_args(t["q"], t["k_new"], self.batch, a.rope_base, q_out=self.qo, k_out=self.ko)
+        self.outs = self.cargs = self.ws_acc = None
+        if acc is not None:
+            self.outs = (torch.empty(x.batch, dtype=torch.int32, device=dev),
+                         torch.empty(x.batch, dtype=torch.int32, device=dev),
+                         torch.empty(len(x.tau), dtype=torch.int32, device=dev))
+            self.cargs = ssv.accept_args(acc["mode"], acc["T"], acc["logits"], acc["draft_tokens"], acc["tau"],
+                                         acc["block"], acc["gamma"], acc["slot_off"], *self.outs,
+                                         acc["draft_logits"], acc["noise"], acc["noise_row"], acc["u_accept"],
+                                         acc["u_sample"], acc["max_block"], self.status)
+            self.ws_acc = torch.zeros(ssv.accept_workspace_bytes(self.cargs), dtype=torch.uint8, device=dev)
+        self.margs = None
+        if with_commit:
+            # commit step (timed on its own, not part of the step): the rotated
+            # fresh rows into destination caches laid out with room, seeded
+            # accepted counts
+            self.n_acc_c, dst_off, dst_cap, dst_rows, _ = W.commit_layout(a, 2024)
+            self.k_dst = torch.zeros((dst_rows, a.Hkv, a.d), dtype=self.ko.dtype, device=dev)
+            self.v_dst = torch.zeros_like(self.k_dst)
+            self.commit_in = [sio.int_tensor(v, dev) for v in (self.n_acc_c, dst_off, dst_cap)]
+            self.new_len = torch.empty(a.batch, dtype=torch.int32, device=dev)
+            self.margs = ssv.commit_args(self.ko, t["v_new"], self.k_dst, self.v_dst, self.batch, t["tau"],
+                                         *self.commit_in, self.new_len, self.status)
+
+    # ---- ops (each on stream s) ----
+    def op_rope(self, s):
+        from diffusion_speculative_verification_gb300 import ssv
+        ssv.rope_copy(self.t["q"], self.t["k_new"], self.batch, self.a.rope_base, q_out=self.qo, k_out=self.ko,
+                      stream=s)
+
+    def op_attn(self, s):
+        import ctypes as C
+        from diffusion_speculative_verification_gb300 import ssv
+        r = ssv.lib().ssv_verify_attn(C.byref(self.aargs), self.ws_attn.data_ptr(), self.ws_attn.numel(),
+                                      s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_verify_attn")
+
+    def op_accept(self, s):
+        import ctypes as C
+        from diffusion_speculative_verification_gb300 import ssv
+        if self.acc is not None:
+            r = ssv.lib().ssv_accept(C.byref(self.cargs), self.ws_acc.data_ptr(), self.ws_acc.numel(), s.cuda_stream)
+            if r:
+                raise ssv.SsvError(r, "ssv_accept")
+
+    def op_commit(self, s):
+        import ctypes as C
+        from diffusion_speculative_verification_gb300 import ssv
+        r = ssv.lib().ssv_commit(C.byref(self.margs), s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_commit")
+
+    def op_step(self, s):
+        """The whole step in one call (ssv_verify_step: the three kernels
+        chained with programmatic dependent launch)."""
+        from diffusion_speculative_verification_gb300 import ssv
+        ssv.verify_step(self.rargs, self.aargs, self.ws_attn, self.cargs, self.ws_acc, stream=s)
+
+    def step_eager(self, evs, s):
+        for j, op in enumerate((self.op_rope, self.op_attn, self.op_accept)):
+            evs[j].record(s)
+            op(s)
+        evs[3].record(s)
+
+    def work(self):
+        rb = rope_bytes(self.a)
+        ab, af = attn_work(self.a, self.out_b)
+        return rb, ab, af, accept_bytes(self.x)
+
+    def check_status(self):
+        from diffusion_speculative_verification_gb300 import ssv
+        st = ssv.get_status(self.status)
+        assert st == ssv.SSV_OK, f"{self.config}: device status {ssv.status_string(st)}"
+
+
+class Timer:
+    """Graph-replay timing on one stream.  Each graph holds K x [L2 flush,
+    body]; a body's time per step is (replay - flush-only replay) / K."""
+
+    def __init__(self, dev, stream, steps, l2_flush):
+        self.dev, self.stream, self.steps, self.l2_flush = dev, stream, steps, l2_flush
+        self._flush = None
+
+    def capture(self, bodies):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(self.dev)
+        cap.wait_stream(self.stream)
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(self.steps):
+                self.l2_flush()
+                for body in bodies:
+                    body(cap)
+        self.stream.wait_stream(cap)
+        return g
+
+    def replay_ms(self, g):
+        import torch
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        g.replay()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def flush_ms(self):
+        if self._flush is None:
+            self._flush = self.capture(())
+            self._flush.replay()
+        return self.replay_ms(self._flush)
+
+
+def warm(run: ConfigRun, stream, l2_flush, n):
+    import torch
+    for _ in range(n):
+        l2_flush()
+        run.op_step(stream)
+        if run.margs is not None:
+            run.op_commit(stream)
+    torch.cuda.synchronize()
+    run.check_status()
+
+
+def roofline_of(run: ConfigRun, op_ms, hbm_peak, tf_peak, peak_kind):
+    """Roofline record of the dominant op (largest device time): HBM-bound
+    ops against the measured copy bandwidth; the attention of the prefill
+    workload against the measured bf16 tensor peak."""
+    rb, ab, af, cb = run.work()
+    ops = {"rope": (op_ms[0], rb), "verify_attn": (op_ms[1], ab), "accept": (op_ms[2], cb)}
+    dom = max(ops, key=lambda k: ops[k][0])
+    if dom == "verify_attn" and run.config == "prefill":
+        tfs = af / (op_ms[1] * 1e-3) / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(tfs / tf_peak, 4), "traffic": measured_traffic(dom, run.config), "peak_kind": peak_kind,
+                "algorithmic_flops": af}
+    ach = ops[dom][1] / (ops[dom][0] * 1e-3) / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4), "traffic": measured_traffic(dom, run.config), "peak_kind": peak_kind,
+            "algorithmic_bytes": ops[dom][1]}
+
+
+def op_records(run: ConfigRun, op_ms, world=1):
+    rb, ab, af, cb = run.work()
+    x = run.x
+    return {
+        "verify_attn": {"us": round(op_ms[1] * 1e3, 2), "gbs": round(ab / (op_ms[1] * 1e-3) / 1e9, 1),
+                        "tflops": round(af / (op_ms[1] * 1e-3) / 1e12, 2), "bytes": ab, "flops": af},
+        "rope": {"us": round(op_ms[0] * 1e3, 2), "gbs": round(rb / (op_ms[0] * 1e-3) / 1e9, 1), "bytes": rb},
+        "accept": None if x is None else {"us": round(op_ms[2] * 1e3, 2),
+                                          "gbs": round(cb / (op_ms[2] * 1e-3) / 1e9, 1), "bytes": cb,
+                                          "seq_per_s": round(world * x.batch / (op_ms[2] * 1e-3), 1),
+                                          "mode": {W.MODE_ARGMAX: "argmax", W.MODE_GUMBEL: "gumbel",
+                                                   W.MODE_REJECT: "reject"}[x.mode], "T": x.T},
+    }
+
+
+def sub_record(config, args, dev, stream, l2_flush, clocks, hbm_peak, tf_peak, peak_kind):
+    """One more workload of the verification pass, measured like the headline
+    (CUDA-graph replays, L2 flushed before every step) with its own roofline."""
+    import torch
+    run = ConfigRun(config, dev, with_commit=False)
+    warm(run, stream, l2_flush, max(3, args.warmup))
+    K = max(1, min(args.steps, 100))
+    tm = Timer(dev, stream, K, l2_flush)
+    graphs = {"step": tm.capture((run.op_step,)), "rope": tm.capture((run.op_rope,)),
+              "verify_attn": tm.capture((run.op_attn,))}
+    if run.acc is not None:
+        graphs["accept"] = tm.capture((run.op_accept,))
+    for g in graphs.values():
+        g.replay()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    t_flush = tm.flush_ms()
+    t_step = (tm.replay_ms(graphs["step"]) - t_flush) / K
+    op_ms = np.array([(tm.replay_ms(graphs[k]) - t_flush) / K if k in graphs else 0.0
+                      for k in ("rope", "verify_attn", "accept")])
+    t1 = time.time()
+    run.check_status()
+    rb, ab, af, cb = run.work()
+    a = run.a
+    rec = {"workload": config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d, "steps": K,
+           "step_us": round(t_step * 1e3, 2), "step_gbs": round((rb + ab + cb) / (t_step * 1e-3) / 1e9, 1),
+           **op_records(run, op_ms), "roofline": roofline_of(run, op_ms, hbm_peak, tf_peak, peak_kind),
+           "clocks": clocks.window(t0, t1) if clocks is not None else None}
+    del run, graphs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from diffusion_speculative_verification_gb300 import build, ssv, io as sio
+    from diffusion_speculative_verification_gb300 import build, ssv
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -345,37 +569,9 @@ def run_ours(args):
     build.build()
     ssv.lib()
 
-    a = W.workload_attn(args.config)
-    xi = ACCEPT_INDEX[args.config]
-    x = None if xi is None else W.workload_accept(args.config, xi)
-    t = sio.attn_to_device(a, dev)
-    acc = None if x is None else sio.accept_to_device(x, dev)
-    out_dtype = torch.bfloat16 if a.dtype == W.BF16 else torch.float32
-    out_b = 2 if a.dtype == W.BF16 else 4
-    qo = torch.empty_like(t["q"])
-    ko = torch.empty_like(t["k_new"])
-    o = torch.empty(t["q"].shape, dtype=out_dtype, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    run = ConfigRun(args.config, dev, with_commit=True)
+    a, x = run.a, run.x
     stream = torch.cuda.current_stream(dev)
-    batch = t["batch"]
-    aargs = ssv.attn_args(qo, t["k_cache"], t["v_cache"], ko, t["v_new"], o, batch, t["tau"], 0.0, status)
-    ws_attn = torch.zeros(max(256, ssv.verify_attn_workspace_bytes(aargs)), dtype=torch.uint8, device=dev)
-    outs = None
-    if acc is not None:
-        outs = (torch.empty(x.batch, dtype=torch.int32, device=dev), torch.empty(x.batch, dtype=torch.int32, device=dev),
-                torch.empty(len(x.tau), dtype=torch.int32, device=dev))
-        cargs = ssv.accept_args(acc["mode"], acc["T"], acc["logits"], acc["draft_tokens"], acc["tau"], acc["block"],
-                                acc["gamma"], acc["slot_off"], *outs, acc["draft_logits"], acc["noise"],
-                                acc["noise_row"], acc["u_accept"], acc["u_sample"], acc["max_block"], status)
-        ws_acc = torch.zeros(ssv.accept_workspace_bytes(cargs), dtype=torch.uint8, device=dev)
-    # commit step (timed on its own, not part of the step): the rotated fresh
-    # rows into destination caches laid out with room, seeded accepted counts
-    n_acc_c, dst_off, dst_cap, dst_rows, _ = W.commit_layout(a, 2024)
-    k_dst = torch.zeros((dst_rows, a.Hkv, a.d), dtype=ko.dtype, device=dev)
-    v_dst = torch.zeros_like(k_dst)
-    commit_in = [sio.int_tensor(v, dev) for v in (n_acc_c, dst_off, dst_cap)]
-    new_len = torch.empty(a.batch, dtype=torch.int32, device=dev)
-    margs = ssv.commit_args(ko, t["v_new"], k_dst, v_dst, batch, t["tau"], *commit_in, new_len, status)
     # L2 flush between steps: a 256 MB read (twice the 129 MB L2) leaves only
     # clean lines of an unrelated buffer, so no step inherits its inputs in L2
     # and no write-back of dirty flush lines lands inside a measured step.
@@ -385,53 +581,7 @@ def run_ours(args):
     def l2_flush():
         torch.sum(flush_buf, dim=0, out=flush_out)
 
-    L = ssv.lib()
-    import ctypes as C
-
-    def op_rope(s):
-        ssv.rope_copy(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko, stream=s)
-
-    def op_attn(s):
-        r = L.ssv_verify_attn(C.byref(aargs), ws_attn.data_ptr(), ws_attn.numel(), s.cuda_stream)
-        if r:
-            raise ssv.SsvError(r, "ssv_verify_attn")
-
-    def op_accept(s):
-        if acc is not None:
-            r = L.ssv_accept(C.byref(cargs), ws_acc.data_ptr(), ws_acc.numel(), s.cuda_stream)
-            if r:
-                raise ssv.SsvError(r, "ssv_accept")
-
-    def op_commit(s):
-        r = L.ssv_commit(C.byref(margs), s.cuda_stream)
-        if r:
-            raise ssv.SsvError(r, "ssv_commit")
-
-    OPS = (op_rope, op_attn, op_accept)
-    rargs = ssv.rope_args(t["q"], t["k_new"], batch, a.rope_base, q_out=qo, k_out=ko)
-
-    def op_step(s):
-        """The whole step in one call (ssv_verify_step: the three kernels chained
-        with programmatic dependent launch)."""
-        ssv.verify_step(rargs, aargs, ws_attn, cargs if acc is not None else None,
-                        ws_acc if acc is not None else None, stream=s)
-
-    def step(evs=None, s=None):
-        s = stream if s is None else s
-        if not evs:
-            op_step(s)
-            return
-        for j, op in enumerate(OPS):
-            evs[j].record(s)
-            op(s)
-        evs[3].record(s)
-
-    for _ in range(args.warmup):
-        l2_flush()
-        step()
-        op_commit(stream)
-    torch.cuda.synchronize()
-    assert ssv.get_status(status) == ssv.SSV_OK
+    warm(run, stream, l2_flush, args.warmup)
 
     # Timed region.  Default: each sequence of K steps is captured once into a
     # CUDA graph and replayed as one launch, timed by two events around the
@@ -443,38 +593,17 @@ def run_ours(args):
     # the GPU idle inside a measurement.  --eager: the three calls one at a
     # time, with events between them.
     launch = "eager" if args.eager else "cuda_graph"
-
-    def capture(bodies):
-        g = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g, stream=cap):
-            for _ in range(args.steps):
-                l2_flush()
-                for body in bodies:
-                    body(cap)
-        stream.wait_stream(cap)
-        return g
-
+    tm = Timer(dev, stream, args.steps, l2_flush)
     graphs = None
     if launch == "cuda_graph":
-        graphs = {"step": capture((op_step,)), "flush": capture(()), "rope": capture((op_rope,)),
-                  "verify_attn": capture((op_attn,)), "commit": capture((op_commit,))}
-        if acc is not None:
-            graphs["accept"] = capture((op_accept,))
+        graphs = {"step": tm.capture((run.op_step,)), "rope": tm.capture((run.op_rope,)),
+                  "verify_attn": tm.capture((run.op_attn,)), "commit": tm.capture((run.op_commit,))}
+        if run.acc is not None:
+            graphs["accept"] = tm.capture((run.op_accept,))
         torch.cuda.synchronize()
         for g in graphs.values():  # first replay uploads the graph
             g.replay()
         torch.cuda.synchronize()
-
-    def timed_replay(g):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1)
 
     props = torch.cuda.get_device_properties(dev)
     clocks = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
@@ -484,23 +613,23 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.mark("t0")
+    t0 = time.time()
     if graphs is not None:
-        t_step = timed_replay(graphs["step"])
+        t_step = tm.replay_ms(graphs["step"])
         torch.cuda.synchronize()
-        clocks.mark("t1")
-        t_flush = timed_replay(graphs["flush"])
-        op_ms = np.array([(timed_replay(graphs[k]) - t_flush) / args.steps if k in graphs else 0.0
+        t1 = time.time()
+        t_flush = tm.flush_ms()
+        op_ms = np.array([(tm.replay_ms(graphs[k]) - t_flush) / args.steps if k in graphs else 0.0
                           for k in ("rope", "verify_attn", "accept")])
         step_total = t_step - t_flush
-        commit_ms = (timed_replay(graphs["commit"]) - t_flush) / args.steps
+        commit_ms = (tm.replay_ms(graphs["commit"]) - t_flush) / args.steps
     else:
         events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
             l2_flush()
-            step(events[i])
+            run.step_eager(events[i], stream)
         torch.cuda.synchronize()
-        clocks.mark("t1")
+        t1 = time.time()
         per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in events])   # ms [steps, 3]
         op_ms = per.mean(axis=0)
         step_total = float(per.sum())
@@ -508,42 +637,38 @@ def run_ours(args):
         for i in range(args.steps):
             l2_flush()
             ev[2 * i].record(stream)
-            op_commit(stream)
+            run.op_commit(stream)
             ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
         commit_ms = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]))
     if world > 1:
         dist.barrier()
-    clk = clocks.stop() if rank == 0 else None
-    assert ssv.get_status(status) == ssv.SSV_OK
+    clk = clocks.window(t0, t1) if rank == 0 else None
+    run.check_status()
     tot_ms = aggregate_ms(float(step_total), dist if world > 1 else None, dev)
 
-    rb = rope_bytes(a)
-    ab, af = attn_work(a, out_b)
-    cb = accept_bytes(x)
-    mb = commit_bytes(a, n_acc_c)
+    rb, ab, af, cb = run.work()
+    mb = commit_bytes(a, run.n_acc_c)
     step_bytes = rb + ab + cb
     ms_step = tot_ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
     hbm_peak, tf_peak, peak_kind = load_peaks()
-    ops = {"rope": (op_ms[0], rb), "verify_attn": (op_ms[1], ab), "accept": (op_ms[2], cb)}
-    dom = max(ops, key=lambda k: ops[k][0])
-    ach = ops[dom][1] / (ops[dom][0] * 1e-3) / 1e9
-    roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(ach / hbm_peak, 4), "traffic": measured_traffic(dom, args.config), "peak_kind": peak_kind,
-            "algorithmic_bytes": ops[dom][1]}
-    if dom == "verify_attn" and args.config == "prefill":
-        tfs = af / (op_ms[1] * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(tfs, 1), "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": round(tfs / tf_peak, 4), "traffic": measured_traffic(dom, args.config), "peak_kind": peak_kind,
-                "algorithmic_flops": af}
+    roof = roofline_of(run, op_ms, hbm_peak, tf_peak, peak_kind)
 
     lmh = None
     if args.config in W.LMHEAD and not args.no_lmhead:
         lmh = run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak)
 
     # ---- end to end: host inputs -> device, run, tokens back -------------------
-    e2e = run_e2e(args, a, x, t, acc, outs if acc is not None else None, o, dev, stream, step, out_b)
+    e2e = run_e2e(args, run, stream)
+
+    subs = {}
+    if rank == 0 or world > 1:
+        for c in [c for c in args.sub_configs.split(",") if c and c != args.config]:
+            subs[c] = sub_record(c, args, dev, stream, l2_flush, clocks if rank == 0 else None, hbm_peak, tf_peak,
+                                 peak_kind)
+    if rank == 0:
+        clocks.stop()
 
     line = None
     if rank == 0:
@@ -554,12 +679,7 @@ def run_ours(args):
             "config": {"workload": args.config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d,
                        "l2": "256 MB read before every step", "launch": launch,
                        "parallelism": f"replicas x{world}"},
-            "verify_attn": {"us": round(op_ms[1] * 1e3, 2), "gbs": round(ab / (op_ms[1] * 1e-3) / 1e9, 1),
-                            "tflops": round(af / (op_ms[1] * 1e-3) / 1e12, 2), "bytes": ab, "flops": af},
-            "rope": {"us": round(op_ms[0] * 1e3, 2), "gbs": round(rb / (op_ms[0] * 1e-3) / 1e9, 1), "bytes": rb},
-            "accept": None if x is None else {"us": round(op_ms[2] * 1e3, 2),
-                                              "gbs": round(cb / (op_ms[2] * 1e-3) / 1e9, 1), "bytes": cb,
-                                              "seq_per_s": round(world * x.batch / (op_ms[2] * 1e-3), 1)},
+            **op_records(run, op_ms, world),
             "commit": {"us": round(commit_ms * 1e3, 2), "gbs": round(mb / (commit_ms * 1e-3) / 1e9, 1),
                        "bytes": mb, "frac_hbm": round(mb / (commit_ms * 1e-3) / 1e9 / hbm_peak, 4),
                        "traffic": measured_traffic("commit", args.config),
@@ -570,6 +690,7 @@ def run_ours(args):
             "gpu_launches": kernel_launches(x) * args.steps,
             "clocks": clk,
             "e2e": e2e,
+            "configs": subs,
         }
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(args.config)
@@ -673,9 +794,10 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
             "launch": "cuda_graph", "note": "timed alone, not in the step; logits never written"}
 
 
-def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):
+def run_e2e(args, run: ConfigRun, stream):
     """Same calls, inputs copied from pinned host memory every step, results read back."""
     import torch
+    t, acc = run.t, run.acc
     names = ["q", "k_new", "v_new", "k_cache", "v_cache", "tau"]
     host = {k: t[k].cpu().pin_memory() for k in names}
     dev_bufs = {k: t[k] for k in names}
@@ -687,9 +809,9 @@ def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):
             if acc[k] is not None:
                 host["acc_" + k] = acc[k].cpu().pin_memory()
                 dev_bufs["acc_" + k] = acc[k]
-        results = list(outs)
+        results = list(run.outs)
     else:
-        results = [o]
+        results = [run.o]
     results_host = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(v.numel() * v.element_size() for v in results_host)
@@ -702,24 +824,30 @@ def run_e2e(args, a, x, t, acc, outs, o, dev, stream, step, out_b):
             e0.record(stream)
         for k, h in host.items():
             dev_bufs[k].copy_(h, non_blocking=True)
-        step()
+        run.op_step(stream)
         for r, rh in zip(results, results_host):
             rh.copy_(r, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
+    run.check_status()
     ms = e0.elapsed_time(e1) / steps
-    step_bytes = rope_bytes(a) + attn_work(a, out_b)[0] + accept_bytes(x)
-    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+    rb, ab, af, cb = run.work()
+    del host, results_host
+    return {"value": round((rb + ab + cb) / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 4), "steps": steps}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=list(W.WORKLOADS), default="gqa1p7b")
+    ap.add_argument("--config", choices=list(W.WORKLOADS), default="sweep",
+                    help="headline workload (default: sweep, the largest by bytes)")
+    ap.add_argument("--sub-configs", default="prefill,gqa8b,gqa1p7b",
+                    help="comma-separated workloads measured after the headline, each as a sub-record "
+                         "with its own roofline ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM head + acceptance measurement")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one call at a time")

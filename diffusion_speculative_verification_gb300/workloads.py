@@ -22,7 +22,10 @@ Shapes follow the five named workloads of the verification problem:
                acceptance over 151936 tokens at T in {0, 1, 1.5}.
 
 Generator: numpy PCG64 seeded per workload; normals by numpy's fp32
-standard normal (scaled in fp32); bf16 values are fp32 draws rounded to nearest-even.  Uniforms that
+standard normal (scaled in fp32); bf16 values are fp32 draws rounded to
+nearest-even.  Large arrays and per-row tables are drawn in pieces on worker
+threads, each piece from a generator seeded by (one draw of the workload's
+generator, piece index), so the values never depend on the thread count.  Uniforms that
 the acceptance rule consumes (u for accept tests, u' for the emitted sample)
 and the Gumbel table G = -log(-log U), U in the open interval (0, 1), are
 drawn here and passed to both sides as inputs.
@@ -78,6 +81,44 @@ def _normal(rng: np.random.Generator, shape, std: float = 1.0) -> np.ndarray:
     return x
 
 
+#: arrays above this many elements are drawn in fixed-size pieces on worker
+#: threads, each piece from its own generator seeded by (a draw of the parent
+#: generator, piece index): the values depend only on the seed, never on the
+#: thread count.
+_PIECE = 1 << 22
+
+
+def _pool():
+    import concurrent.futures as cf
+    import os
+    return cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+
+
+def _normal_store(rng: np.random.Generator, shape, dtype: str, std: float = 1.0) -> np.ndarray:
+    """N(0, std^2) fp32 draws stored as `dtype` (bf16 bits or fp32)."""
+    n = int(np.prod(shape))
+    if n <= _PIECE:
+        return _store(_normal(rng, shape, std), dtype)
+    seed = int(rng.integers(0, 1 << 63))
+    out = np.empty(n, np.uint16 if dtype == BF16 else np.float32)
+
+    def piece(i):
+        lo, hi = i * _PIECE, min(n, (i + 1) * _PIECE)
+        out[lo:hi] = _store(_normal(np.random.default_rng([seed, i]), hi - lo, std), dtype)
+
+    with _pool() as ex:
+        list(ex.map(piece, range((n + _PIECE - 1) // _PIECE)))
+    return out.reshape(shape)
+
+
+def _rows_parallel(rng: np.random.Generator, rows: int, fn) -> None:
+    """fn(row, generator) for every row, each row with its own generator
+    seeded from one draw of `rng` (thread-count independent)."""
+    seed = int(rng.integers(0, 1 << 63))
+    with _pool() as ex:
+        list(ex.map(lambda r: fn(r, np.random.default_rng([seed, r])), range(rows)))
+
+
 def open_uniform(rng: np.random.Generator, shape) -> np.ndarray:
     """fp64 uniforms strictly inside (0, 1): (k + 0.5) / 2^53."""
     k = rng.integers(0, 1 << 53, size=shape, dtype=np.uint64)
@@ -87,9 +128,11 @@ def open_uniform(rng: np.random.Generator, shape) -> np.ndarray:
 def gumbel_table(rng: np.random.Generator, rows: int, V: int) -> np.ndarray:
     """Gumbel(0,1) noise table, fp64 transform rounded to fp32, row by row."""
     out = np.empty((rows, V), dtype=np.float32)
-    for r in range(rows):
-        u = open_uniform(rng, V)
-        out[r] = (-np.log(-np.log(u))).astype(np.float32)
+
+    def row(r, g):
+        out[r] = (-np.log(-np.log(open_uniform(g, V)))).astype(np.float32)
+
+    _rows_parallel(rng, rows, row)
     return out
 
 
@@ -187,11 +230,11 @@ def make_attn_inputs(name: str, cache_lens, new_lens, blocks, Hq: int, Hkv: int,
     total_c = int(np.sum(cache_lens))
     tau = np.concatenate([random_tau(rng, int(b)) for b in blocks]).astype(np.int32) \
         if len(blocks) else np.zeros(0, np.int32)
-    q = _store(_normal(rng, (rows, Hq, d)), dtype)
-    kn = _store(_normal(rng, (rows, Hkv, d)), dtype)
-    vn = _store(_normal(rng, (rows, Hkv, d)), dtype)
-    kc = _store(_normal(rng, (total_c, Hkv, d)), dtype)
-    vc = _store(_normal(rng, (total_c, Hkv, d)), dtype)
+    q = _normal_store(rng, (rows, Hq, d), dtype)
+    kn = _normal_store(rng, (rows, Hkv, d), dtype)
+    vn = _normal_store(rng, (rows, Hkv, d), dtype)
+    kc = _normal_store(rng, (total_c, Hkv, d), dtype)
+    vc = _normal_store(rng, (total_c, Hkv, d), dtype)
     return AttnInputs(name, dtype, Hq, Hkv, d, rope_base, seqs, tau, q, kn, vn, kc, vc)
 
 
@@ -221,8 +264,11 @@ def make_accept_inputs(name: str, mode: int, T: float, V: int, blocks, gammas, s
     if tau is None:
         tau = np.concatenate([random_tau(rng, int(b)) for b in blocks]).astype(np.int32) if batch else np.zeros(0, np.int32)
     logits32 = np.empty((S, V), np.float32)
-    for r in range(S):
-        logits32[r] = _normal(rng, V, logit_std)
+
+    def logit_row(r, g):
+        logits32[r] = _normal(g, V, logit_std)
+
+    _rows_parallel(rng, S, logit_row)
     draft_tokens = rng.integers(0, V, size=S).astype(np.int32)
     draft32 = None
     if mode == MODE_REJECT:
@@ -349,8 +395,8 @@ def make_commit_inputs(a: AttnInputs, seed: int, slack: int = 3) -> CommitInputs
     rows the commit must not touch can be checked)."""
     n_acc, off, cap, rows, rng = commit_layout(a, seed, slack)
     shape = (rows, a.Hkv, a.d)
-    k_dst = _store(_normal(rng, shape), a.dtype)
-    v_dst = _store(_normal(rng, shape), a.dtype)
+    k_dst = _normal_store(rng, shape, a.dtype)
+    v_dst = _normal_store(rng, shape, a.dtype)
     return CommitInputs(a, n_acc, off, cap, k_dst, v_dst)
 
 
