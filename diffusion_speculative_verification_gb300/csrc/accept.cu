@@ -10,12 +10,12 @@
 //                   streaming pass of register loads per (row, chunk).
 // Both write one AccPartial per (verified row, chunk) and finish through the
 // row-merge / sequence-walk steps.
-//   accept_sample   (rejection sampling only) grid = vocab chunks x batch.
-//                   Chunk masses of (p - q)_+ and of p for the emission
-//                   row; the last CTA finds the chunk holding u' * Z with a
-//                   warp scan and scans that chunk in vocabulary order
-//                   (fp64 prefix sums).
+//   accept_emit_norm, accept_sample   (rejection sampling only, below)
+//                   the emitted token in double-float arithmetic: the
+//                   emission row's normalisers, then its chunk masses and
+//                   the inverse-CDF search.
 #include "accept.cuh"
+#include "dfloat.cuh"
 
 namespace ssv {
 
@@ -116,24 +116,6 @@ __device__ void block_sum2x2(float& h1, float& l1, float& h2, float& l2) {
   }
 }
 
-// Exclusive prefix sum over the block (thread order), fp64.
-__device__ double block_exclusive_scan(double v) {
-  __shared__ double sw[kAccThreads / 32];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  double incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) sw[wid] = incl;
-  __syncthreads();
-  double before = 0.0;
-  for (int w = 0; w < wid; ++w) before += sw[w];
-  __syncthreads();
-  return before + incl - v;
-}
-
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_reduce_kernel(const AcceptParams p) {
@@ -224,177 +206,321 @@ accept_reduce_kernel(const AcceptParams p) {
 }
 
 // ---- rejection sampling: emitted token ------------------------------------
-// Weight of vocab entry e: p_e = exp(l_e / T - M_a) / S_a and, for a residual
-// sample, (p_e - q_e)_+ with q likewise.  The same expression serves the chunk
-// masses and the final in-chunk scan.
-__device__ __forceinline__ void sample_weight(float c2, float nma, float nmb, float la, float lb, float inv_sa,
-                                              float inv_sb, bool residual, float& wr, float& wp) {
-  const float pv = ex2f(fmaf(la, c2, nma)) * inv_sa;
-  const float qv = residual ? ex2f(fmaf(lb, c2, nmb)) * inv_sb : 0.f;
-  wp = pv;
-  wr = residual ? fmaxf(pv - qv, 0.f) : 0.f;
+// The emitted token is the smallest v whose cumulative weight exceeds u' Z
+// (inverse CDF).  It is computed in double-float arithmetic (dfloat.cuh):
+// every weight to about 5e-13 relative and every sum as a tree of depth
+// below 32 double-float additions, so the token can differ from the exact
+// one only when u' Z lies within about 1e-12 Z of a CDF boundary (for a
+// residual sample, that divided by the residual's total mass).  The row is
+// cut into sub-chunks of kEmitSub entries, one CTA each, 8 consecutive
+// entries per thread:
+//   accept_emit_norm   for a residual sample, each sub-chunk's sums of
+//                      e_a = 2^((l - m_a) c2) and e_b = 2^((ql - m_b) c2)
+//                      (unnormalised p and q).
+//   accept_sample      every CTA of sequence b adds the sub-chunk sums in the
+//                      same fixed order (S_a, S_b), forms the weights
+//                      w = (e_a S_b - e_b S_a)_+ (the residual (p - q)_+ scaled
+//                      by S_a S_b) and e_a (p scaled by S_a), and writes its
+//                      masses per warp and per sub-chunk; the last CTA finds
+//                      the sub-chunk, then the warp, then (one warp, one
+//                      thread's 8 entries per lane) the entry where the
+//                      cumulative mass passes u' Z (fp64 prefix sums of the
+//                      exact pair values; the residual unless it vanished,
+//                      then p).
+
+struct EmitCtx {
+  bool residual;
+  float ma, mb;  // row maxima of the logits and the draft logits
+  dfx c2;        // log2(e) / T
+  dfx sa, sb;    // S_a, S_b (residual only)
+};
+
+// residual weight (e_a S_b - e_b S_a)_+ and p weight e_a of one entry
+__device__ __forceinline__ void emit_weights(const EmitCtx& c, float la, float lb, const float2* tab, dfx& wr,
+                                             dfx& wp) {
+  const dfx ea = dfx_exp2_diff(la, c.ma, c.c2, tab);
+  wp = ea;
+  wr = dfx{0.f, 0.f};
+  if (c.residual) {
+    const dfx eb = dfx_exp2_diff(lb, c.mb, c.c2, tab);
+    const dfx d = dfx_add(dfx_mul(ea, c.sb), dfx_mul(dfx{-eb.hi, -eb.lo}, c.sa));
+    if (d.hi > 0.f) wr = d;
+  }
+}
+
+__device__ __forceinline__ dfx shfl_xor_dfx(dfx a, int o) {
+  return dfx{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+
+// The 8 consecutive entries [e0, e0 + 8) of a row (fill -inf past V).
+template <typename T>
+__device__ __forceinline__ void ld_run8(const void* base, size_t rbase, int e0, int V, bool vec, float* x) {
+  if (vec && e0 + 8 <= V) {
+    if constexpr (sizeof(T) == 4) {
+      const float4* p4 = reinterpret_cast<const float4*>(static_cast<const float*>(base) + rbase + e0);
+      const float4 a = __ldcg(p4), b = __ldcg(p4 + 1);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {  // rows are 8-byte aligned (V % 4 == 0): two 4-entry loads
+      const uint2* p2 = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + rbase + e0);
+      const uint2 u = __ldcg(p2), v = __ldcg(p2 + 1);
+      const uint32_t w[4] = {u.x, u.y, v.x, v.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = (e0 + i < V) ? ld_logit<T>(base, rbase + e0 + i) : -INFINITY;
+  }
+}
+
+// Common prologue of the two emission kernels: validity of sequence b (reads
+// only the call's inputs, so it runs before the wait), the 2^(j/256) table
+// into shared memory, then the wait for the reduce kernel's records.
+__device__ __forceinline__ bool emit_prologue(const AcceptParams& p, int b, float2* s_tab, int* s_ok) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    const bool ok = warp_seq_valid(p, b);
+    if (tid == 0) *s_ok = ok;
+  }
+  dfx_exp2_table(p.e2pow, s_tab, tid);  // kAccThreads == 256 entries
+  __syncthreads();
+  pdl_wait();  // emission records, accepted lengths and row normalisers
+  pdl_trigger();
+  return *s_ok != 0;
+}
+
+static_assert(kAccThreads == 256 && kEmitSub == 8 * kAccThreads, "one table entry and 8 row entries per thread");
+
+template <typename T>
+__global__ void __launch_bounds__(kAccThreads)
+accept_emit_norm_kernel(const AcceptParams p) {
+  __shared__ int s_ok;
+  __shared__ float2 s_tab[256];
+  __shared__ float4 s_w[kAccThreads / 32];
+  const int b = blockIdx.x / p.nsub;
+  const int sub = blockIdx.x % p.nsub;
+  // A sequence whose stage map or sizes were rejected never ran its walk,
+  // so its emission record may be stale: skip it.
+  if (!emit_prologue(p, b, s_tab, &s_ok)) return;
+  const int eslot = p.emit[2 * b];
+  const int soff = p.slot_off[b];
+  if (eslot < soff || eslot >= soff + p.block[b] || p.emit[2 * b + 1] == 0) return;  // bonus: no normaliser needed
+  const SlotNorm nm = p.norm[eslot];
+  const dfx c2{p.c2_hi, p.c2_lo};
+  const size_t rbase = (size_t)eslot * p.V;
+  const int e0 = sub * kEmitSub + threadIdx.x * 8;
+  float xa[8], xb[8];
+  ld_run8<T>(p.logits, rbase, e0, p.V, p.vec != 0, xa);
+  ld_run8<T>(p.draft_logits, rbase, e0, p.V, p.vec != 0, xb);
+  dfx sa{0.f, 0.f}, sb{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    sa = dfx_add(sa, dfx_exp2_diff(xa[j], nm.m_a, c2, s_tab));
+    sb = dfx_add(sb, dfx_exp2_diff(xb[j], nm.m_b, c2, s_tab));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sa = dfx_add(sa, shfl_xor_dfx(sa, o));
+    sb = dfx_add(sb, shfl_xor_dfx(sb, o));
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) s_w[wid] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kAccThreads / 32; ++w) {
+      sa = dfx_add(sa, dfx{s_w[w].x, s_w[w].y});
+      sb = dfx_add(sb, dfx{s_w[w].z, s_w[w].w});
+    }
+    p.enorm[(size_t)b * p.nsub + sub] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
+  }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_sample_kernel(const AcceptParams p) {
   __shared__ int s_ok, s_last;
-  const int b = blockIdx.x / p.nchunks;
-  const int chunk = blockIdx.x % p.nchunks;
-  const int tid = threadIdx.x;
-  // A sequence whose stage map or sizes were rejected never ran its finalize
-  // step, so its emission record may be stale: skip it.  The check reads only
-  // the call's inputs, so it runs while the reduce kernel finishes (this kernel
-  // is launched as its programmatic dependent; the reduce kernel lets it start
-  // only after every kernel before the acceptance has completed).
-  if (tid < 32) {
-    const bool ok = warp_seq_valid(p, b);
-    if (tid == 0) s_ok = ok;
-  }
-  __syncthreads();
-  pdl_wait();  // emission records, accepted lengths and row normalisers
-  pdl_trigger();
-  if (!s_ok) return;
+  __shared__ float2 s_tab[256];
+  __shared__ float4 s_w[kAccThreads / 32];
+  __shared__ float4 s_S;
+  const int b = blockIdx.x / p.nsub;
+  const int sub = blockIdx.x % p.nsub;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (!emit_prologue(p, b, s_tab, &s_ok)) return;
   const int eslot = p.emit[2 * b];
   const int soff = p.slot_off[b];
   const int nacc = p.n_acc[b];
   if (eslot < soff || eslot >= soff + p.block[b] || nacc < 0 || nacc >= p.block[b]) return;
-  const bool residual = p.emit[2 * b + 1] != 0;
   const SlotNorm nm = p.norm[eslot];
-  // fp32 reciprocals (an fp64 division is slow on this part; a relative error
-  // of 1e-7 in a row's normaliser moves the sampling threshold by as much)
-  const float inv_sa = 1.f / (float)nm.s_a;
-  const float inv_sb = residual ? 1.f / (float)nm.s_b : 0.f;
-  const float nma = -nm.m_a * p.c2, nmb = -nm.m_b * p.c2;
-  const size_t rbase = (size_t)eslot * p.V;
-  const int c0 = chunk * kAccChunk;
-  const bool vec = p.vec != 0;
-  float xa[kAccPerThread], xb[kAccPerThread];
-  ld_chunk<T>(p.logits, rbase, c0, p.V, vec, -INFINITY, xa);
-  if (residual) ld_chunk<T>(p.draft_logits, rbase, c0, p.V, vec, -INFINITY, xb);
-  float sr = 0.f, cr = 0.f, sp = 0.f, cp = 0.f;
+  EmitCtx c;
+  c.residual = p.emit[2 * b + 1] != 0;
+  c.ma = nm.m_a;
+  c.mb = nm.m_b;
+  c.c2 = dfx{p.c2_hi, p.c2_lo};
+  c.sa = c.sb = dfx{0.f, 0.f};
+  if (c.residual) {
+    // S_a, S_b: warp 0 adds the sub-chunk sums, lane l over sub-chunks l, l + 32, ...,
+    // then a butterfly; the same fixed order in every CTA of the sequence
+    if (wid == 0) {
+      const float4* en = p.enorm + (size_t)b * p.nsub;
+      dfx a{0.f, 0.f}, bb{0.f, 0.f};
+      for (int k = lane; k < p.nsub; k += 32) {
+        const float4 v = __ldcg(en + k);
+        a = dfx_add(a, dfx{v.x, v.y});
+        bb = dfx_add(bb, dfx{v.z, v.w});
+      }
 #pragma unroll
-  for (int j = 0; j < kAccPerThread; ++j) {
-    float wr, wp;
-    sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr, wp);
-    kahan_add(sr, cr, wr);
-    kahan_add(sp, cp, wp);
+      for (int o = 16; o > 0; o >>= 1) {
+        a = dfx_add(a, shfl_xor_dfx(a, o));
+        bb = dfx_add(bb, shfl_xor_dfx(bb, o));
+      }
+      if (lane == 0) s_S = make_float4(a.hi, a.lo, bb.hi, bb.lo);
+    }
+    __syncthreads();
+    c.sa = dfx{s_S.x, s_S.y};
+    c.sb = dfx{s_S.z, s_S.w};
   }
-  float lr = -cr, lp = -cp;
-  block_sum2x2(sr, lr, sp, lp);
-  if (tid == 0) {
-    float* sm = p.smass + ((size_t)b * p.nchunks + chunk) * 4;
-    sm[0] = sr; sm[1] = lr; sm[2] = sp; sm[3] = lp;
-    __threadfence();
-    const int prev = atomicAdd(&p.cnt_sample[b], 1);
-    s_last = (prev == p.nchunks - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- last CTA of sequence b: locate u' * Z (warp 0, lanes over chunks) ----
-  __shared__ int s_chunk;
-  __shared__ double s_before, s_thresh;
-  __shared__ int s_use_res;
-  if (tid < 32) {
-    const int lane = tid;
-    const float* sm = p.smass + (size_t)b * p.nchunks * 4;
-    double zr = 0.0, zp = 0.0;
-    for (int c = lane; c < p.nchunks; c += 32) {
-      zr += (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1]);
-      zp += (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
+  const size_t rbase = (size_t)eslot * p.V;
+  const bool vec = p.vec != 0;
+  {
+    const int e0 = sub * kEmitSub + tid * 8;
+    float xa[8], xb[8];
+    ld_run8<T>(p.logits, rbase, e0, p.V, vec, xa);
+    if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, xb);
+    dfx mr{0.f, 0.f}, mp{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      dfx wr, wp;
+      emit_weights(c, xa[j], c.residual ? xb[j] : -INFINITY, s_tab, wr, wp);
+      mr = dfx_add(mr, wr);
+      mp = dfx_add(mp, wp);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      zr += __shfl_xor_sync(0xffffffffu, zr, o);
-      zp += __shfl_xor_sync(0xffffffffu, zp, o);
+      mr = dfx_add(mr, shfl_xor_dfx(mr, o));
+      mp = dfx_add(mp, shfl_xor_dfx(mp, o));
     }
-    const bool use_res = residual && zr > 0.0;
-    const double t = (double)p.u_sample[b] * (use_res ? zr : zp);
-    // first chunk whose running mass passes t, in vocabulary order
-    double base = 0.0, before = 0.0, before_last = 0.0;
-    int cs = -1, last_nz = 0;
-    for (int r0 = 0; r0 < p.nchunks; r0 += 32) {
-      const int c = r0 + lane;
-      double m = 0.0;
-      if (c < p.nchunks)
-        m = use_res ? (double)__ldcg(&sm[4 * c]) + (double)__ldcg(&sm[4 * c + 1])
-                    : (double)__ldcg(&sm[4 * c + 2]) + (double)__ldcg(&sm[4 * c + 3]);
-      double incl = m;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const double excl = incl - m;
-      const unsigned cross = __ballot_sync(0xffffffffu, c < p.nchunks && base + incl > t);
-      const unsigned nz = __ballot_sync(0xffffffffu, c < p.nchunks && m > 0.0);
-      if (cs < 0 && cross) {
-        const int f = __ffs(cross) - 1;
-        cs = r0 + f;
-        before = base + __shfl_sync(0xffffffffu, excl, f);
-      }
-      if (nz) {
-        const int l = 31 - __clz(nz);
-        last_nz = r0 + l;
-        before_last = base + __shfl_sync(0xffffffffu, excl, l);
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      const float4 m4 = make_float4(mr.hi, mr.lo, mp.hi, mp.lo);
+      s_w[wid] = m4;
+      p.wmass[((size_t)b * p.nsub + sub) * 8 + wid] = m4;
     }
-    if (cs < 0) { cs = last_nz; before = before_last; }  // rounding left t at the very end
-    if (lane == 0) { s_chunk = cs; s_before = before; s_thresh = t; s_use_res = use_res; }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kAccThreads / 32; ++w) {
+        mr = dfx_add(mr, dfx{s_w[w].x, s_w[w].y});
+        mp = dfx_add(mp, dfx{s_w[w].z, s_w[w].w});
+      }
+      p.smass[(size_t)b * p.nsub + sub] = make_float4(mr.hi, mr.lo, mp.hi, mp.lo);
+      __threadfence();
+      const int prev = atomicAdd(&p.cnt_sample[b], 1);
+      s_last = (prev == p.nsub - 1);
+    }
   }
   __syncthreads();
-  const int cs = s_chunk;
-  const bool use_res = s_use_res != 0;
-  // Weights of the crossing chunk in vocabulary order, through shared memory
-  // (index i stored at i + i / 32 so that the contiguous runs read below are
-  // free of bank conflicts).
-  __shared__ float s_w[kAccChunk + kAccChunk / 32];
+  if (!s_last || wid != 0) return;
+  __threadfence();
+
+  // ---- last CTA of sequence b, warp 0: locate u' * Z ---------------------------
+  const float4* sm = p.smass + (size_t)b * p.nsub;
+  double zr = 0.0, zp = 0.0;
+  for (int k = lane; k < p.nsub; k += 32) {
+    const float4 v = __ldcg(sm + k);
+    zr += (double)v.x + (double)v.y;
+    zp += (double)v.z + (double)v.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    zr += __shfl_xor_sync(0xffffffffu, zr, o);
+    zp += __shfl_xor_sync(0xffffffffu, zp, o);
+  }
+  const bool use_res = c.residual && zr > 0.0;  // (p - q)_+ vanished: sample p
+  const double t = (double)p.u_sample[b] * (use_res ? zr : zp);
+  auto mass = [&](const float4& v) -> double { return use_res ? (double)v.x + (double)v.y : (double)v.z + (double)v.w; };
+  // level 1: the first sub-chunk whose running mass passes t (else the last non-empty one)
+  double before = 0.0, before_last = 0.0, base = 0.0;
+  int cs = -1, last_nz = 0;
+  for (int r0 = 0; r0 < p.nsub; r0 += 32) {
+    const int k = r0 + lane;
+    const double m = (k < p.nsub) ? mass(__ldcg(sm + k)) : 0.0;
+    double incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const double excl = incl - m;
+    const unsigned cross = __ballot_sync(0xffffffffu, k < p.nsub && base + incl > t);
+    const unsigned nz = __ballot_sync(0xffffffffu, k < p.nsub && m > 0.0);
+    if (cs < 0 && cross) {
+      const int f = __ffs(cross) - 1;
+      cs = r0 + f;
+      before = base + __shfl_sync(0xffffffffu, excl, f);
+    }
+    if (nz) {
+      const int l = 31 - __clz(nz);
+      last_nz = r0 + l;
+      before_last = base + __shfl_sync(0xffffffffu, excl, l);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (cs < 0) { cs = last_nz; before = before_last; }  // rounding left t at the very end
+  // level 2: the warp of that sub-chunk (lanes 0..7 hold the 8 warp masses)
+  int wsel;
   {
-    // the crossing chunk is reloaded (it was just streamed, so from L2)
-    const int cc0 = cs * kAccChunk;
-    ld_chunk<T>(p.logits, rbase, cc0, p.V, vec, -INFINITY, xa);
-    if (residual) ld_chunk<T>(p.draft_logits, rbase, cc0, p.V, vec, -INFINITY, xb);
+    const double m = (lane < 8) ? mass(__ldcg(p.wmass + ((size_t)b * p.nsub + cs) * 8 + lane)) : 0.0;
+    double incl = m;
 #pragma unroll
-    for (int j = 0; j < kAccPerThread; ++j) {
-      float wr, wp;
-      sample_weight(p.c2, nma, nmb, xa[j], residual ? xb[j] : -INFINITY, inv_sa, inv_sb, residual, wr, wp);
-      const int li = chunk_index(0, j);  // index within the chunk
-      s_w[li + li / 32] = (cc0 + li < p.V) ? (use_res ? wr : wp) : 0.f;
+    for (int o = 1; o < 8; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
     }
+    const double excl = incl - m;
+    const unsigned cross = __ballot_sync(0xffffffffu, lane < 8 && before + incl > t);
+    const unsigned nz = __ballot_sync(0xffffffffu, lane < 8 && m > 0.0);
+    wsel = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 7);
+    before += __shfl_sync(0xffffffffu, excl, wsel);
   }
-  __syncthreads();
-  // each thread: a contiguous run of kAccPerThread entries
-  const int r0 = tid * kAccPerThread;
-  float local = 0.f;
+  // level 3: that warp's 256 entries, 8 consecutive per lane
+  const int e0 = cs * kEmitSub + wsel * 256 + lane * 8;
+  float ya[8], yb[8];
+  ld_run8<T>(p.logits, rbase, e0, p.V, vec, ya);
+  if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, yb);
+  dfx w8[8];
+  dfx run{0.f, 0.f};
   int last_pos = -1;
 #pragma unroll
-  for (int j = 0; j < kAccPerThread; ++j) {
-    const float w = s_w[(r0 + j) + (r0 + j) / 32];
-    local += w;
-    if (w > 0.f) last_pos = cs * kAccChunk + r0 + j;
+  for (int k = 0; k < 8; ++k) {
+    dfx wr, wp;
+    emit_weights(c, ya[k], c.residual ? yb[k] : -INFINITY, s_tab, wr, wp);
+    w8[k] = use_res ? wr : wp;
+    run = dfx_add(run, w8[k]);
+    if (w8[k].hi > 0.f) last_pos = e0 + k;
   }
-  const double excl = block_exclusive_scan((double)local);
-  __shared__ int s_pick, s_last_nz;
-  if (tid == 0) { s_pick = INT_MAX; s_last_nz = -1; }
-  __syncthreads();
-  // remaining mass to cross inside this run, then an fp32 scan of the run
-  const float rel = (float)(s_thresh - (s_before + excl));
-  float acc = 0.f;
+  const double rm = dfx_to_double(run);
+  double incl = rm;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const double rel = t - (before + (incl - rm));  // mass still to cross at the start of this lane's run
+  dfx acc{0.f, 0.f};
   int pick = INT_MAX;
 #pragma unroll
-  for (int j = 0; j < kAccPerThread; ++j) {
-    const float w = s_w[(r0 + j) + (r0 + j) / 32];
-    acc += w;
-    if (pick == INT_MAX && w > 0.f && acc > rel) pick = cs * kAccChunk + r0 + j;
+  for (int k = 0; k < 8; ++k) {
+    acc = dfx_add(acc, w8[k]);
+    if (pick == INT_MAX && w8[k].hi > 0.f && dfx_to_double(acc) > rel) pick = e0 + k;
   }
-  if (pick != INT_MAX) atomicMin(&s_pick, pick);
-  if (last_pos >= 0) atomicMax(&s_last_nz, last_pos);
-  __syncthreads();
-  if (tid == 0) {
-    int v = s_pick != INT_MAX ? s_pick : s_last_nz;
+  // lanes are in vocabulary order: the first lane with a crossing holds the token
+  const unsigned has = __ballot_sync(0xffffffffu, pick != INT_MAX);
+  const int v_pick = has ? __shfl_sync(0xffffffffu, pick, __ffs(has) - 1) : INT_MAX;
+  const unsigned anyw = __ballot_sync(0xffffffffu, last_pos >= 0);
+  const int v_last = anyw ? __shfl_sync(0xffffffffu, last_pos, 31 - __clz(anyw)) : -1;
+  if (lane == 0) {
+    int v = v_pick != INT_MAX ? v_pick : v_last;
     if (v < 0) v = 0;
     p.tokens[soff + nacc] = v;
     p.cnt_sample[b] = 0;
@@ -429,9 +555,15 @@ static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaS
     }
   }
   if (e != cudaSuccess || mode != SSV_ACCEPT_REJECT) return e;
-  const long long g2 = (long long)p.batch * p.nchunks;
+  const long long g2 = (long long)p.batch * p.nsub;
   if (g2 > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (bf) return launch_pdl(accept_sample_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+  if (bf) {
+    e = launch_pdl(accept_emit_norm_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(accept_sample_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+  }
+  e = launch_pdl(accept_emit_norm_kernel<float>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+  if (e != cudaSuccess) return e;
   return launch_pdl(accept_sample_kernel<float>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
 }
 
@@ -500,7 +632,19 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   p.part = reinterpret_cast<AccPartial*>(w + L.part);
   p.norm = reinterpret_cast<SlotNorm*>(w + L.norm);
   p.rowres = reinterpret_cast<RowResult*>(w + L.rowres);
-  p.smass = reinterpret_cast<float*>(w + L.smass);
+  p.nsub = nchunks * (kAccChunk / kEmitSub);
+  p.enorm = reinterpret_cast<float4*>(w + L.enorm);
+  p.smass = reinterpret_cast<float4*>(w + L.smass);
+  p.wmass = reinterpret_cast<float4*>(w + L.wmass);
+  // double-float constants of the emitted sample: log2(e) / T and 2^(2^i / 256)
+  const double c2d = a->T > 0.f ? 1.4426950408889634074 / (double)a->T : 0.0;
+  p.c2_hi = (float)c2d;
+  p.c2_lo = (float)(c2d - (double)p.c2_hi);
+  for (int i = 0; i < 8; ++i) {
+    const double v = exp2((double)(1 << i) / 256.0);
+    p.e2pow[i].x = (float)v;
+    p.e2pow[i].y = (float)(v - (double)(float)v);
+  }
   int mode = a->mode;
   if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;  // T = 0 ignores the noise
   p.mode = mode;

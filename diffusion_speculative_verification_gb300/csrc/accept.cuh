@@ -77,20 +77,32 @@ struct AcceptParams {
   int early;
   // workspace carve-up (the three counter arrays come first and are contiguous)
   int32_t* cnt_seq;     // [batch]        merged rows of the sequence
-  int32_t* cnt_sample;  // [batch]        emission-row chunks done
+  int32_t* cnt_sample;  // [batch]        emission-row sub-chunks done
   int32_t* cnt_row;     // [total_slots]  chunks of the row done
   int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
   AccPartial* part;     // [total_slots][nchunks]
   SlotNorm* norm;       // [total_slots]
   RowResult* rowres;    // [total_slots]
-  float* smass;         // [batch][nchunks][4] : residual mass (hi, lo), p mass (hi, lo)
+  // rejection-sampling emission (double-float), per sequence over nsub
+  // sub-chunks of kEmitSub vocabulary entries:
+  int nsub;
+  float4* enorm;        // [batch][nsub]     sums of e_a = 2^((l - m_a) c2) and e_b = 2^((ql - m_b) c2)
+  float4* smass;        // [batch][nsub]     residual mass, p mass (each hi, lo)
+  float4* wmass;        // [batch][nsub][8]  the same per warp of the sub-chunk's CTA
+  // c2 = log2(e) / T split into an fp32 head and tail; 2^(2^i / 256),
+  // i = 0..7, likewise (host-computed)
+  float c2_hi, c2_lo;
+  float2 e2pow[8];
 };
 
+constexpr int kEmitSub = 2048;  // vocabulary entries per emission CTA (256 threads x 8)
+
 struct AccWorkspaceLayout {
-  size_t cnt_seq, cnt_sample, cnt_row, emit, part, norm, rowres, smass, total;
+  size_t cnt_seq, cnt_sample, cnt_row, emit, part, norm, rowres, enorm, smass, wmass, total;
 };
 
 inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks) {
+  const size_t nsub = (size_t)nchunks * (kAccChunk / kEmitSub);
   AccWorkspaceLayout L;
   size_t o = 0;
   L.cnt_seq = o;    o += sizeof(int32_t) * (size_t)batch;
@@ -100,7 +112,9 @@ inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks)
   L.part = o;       o = align_up(o + sizeof(AccPartial) * (size_t)total_slots * nchunks, 256);
   L.norm = o;       o = align_up(o + sizeof(SlotNorm) * (size_t)total_slots, 256);
   L.rowres = o;     o = align_up(o + sizeof(RowResult) * (size_t)total_slots, 256);
-  L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nchunks, 256);
+  L.enorm = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nsub, 256);
+  L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nsub, 256);
+  L.wmass = o;      o = align_up(o + sizeof(float) * 4 * 8 * (size_t)batch * nsub, 256);
   L.total = o;
   return L;
 }

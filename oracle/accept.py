@@ -189,17 +189,14 @@ def _logit_values(inp, arr) -> np.ndarray:
     return np.asarray(arr, dtype=np.float32)
 
 
-def emission_valid(res: SeqResult, v: int, rel_tol: float) -> bool:
-    """True if token v's CDF interval lies within rel_tol * Z of the threshold.
-
-    Used where fp32 rounding on the GPU can move the inverse-CDF crossing to a
-    neighbouring token: several answers are then correct within the bound.
-    """
+def sample_margin(res: SeqResult) -> float:
+    """Distance of the sampling threshold u' Z to the nearer end of the chosen
+    token's CDF interval, relative to Z: [cdf[v-1], cdf[v]) holds u' Z, so the
+    inverse-CDF choice is unchanged by any perturbation of the CDF smaller
+    than this."""
     cdf = res.sample_cdf
     Z = float(cdf[-1])
+    v = res.tokens[-1]
     lo = 0.0 if v == 0 else float(cdf[v - 1])
     hi = float(cdf[v])
-    if hi <= lo:                       # zero-mass token is never a valid sample
-        return False
-    tol = rel_tol * Z
-    return lo - tol <= res.sample_threshold < hi + tol
+    return min(res.sample_threshold - lo, hi - res.sample_threshold) / Z

@@ -1,17 +1,18 @@
 """GPU parity of ssv_accept against the oracle (SimSD summary section 4;
-SPOT review, "How it is used").  Greedy and coupled-noise acceptance are
-bit-exact: both sides compare identical fp32 scores.  Rejection sampling:
-accepted lengths and accepted tokens bit-exact (every decision's margin
-exceeds the fp32 rounding band); the emitted sample equals the oracle's
-unless u'Z lies within 1e-5 Z of a CDF boundary, where the neighbour is
-also correct within rounding."""
+SPOT review, "How it is used").  Every mode is bit-exact on n_acc, n_out
+and every token.  Greedy and coupled-noise acceptance compare identical fp32
+scores.  Rejection sampling: each accept test's log-ratio margin exceeds the
+fp32 rounding band of the device's ratio, and each emitted sample's threshold
+u'Z lies farther from a CDF boundary than the double-float band of the
+device's weights plus the oracle's fp64 summation bound (both derived in
+gpu_common); the seeded sets are asserted to contain no decision inside a
+band, so the emitted token is unique."""
 import numpy as np
 import pytest
 import torch
 
 from diffusion_speculative_verification_gb300 import workloads as W, ssv
-from gpu_common import ensure_built, gpu_accept, compare_accept, REJECT_MARGIN
-import oracle.accept as oacc
+from gpu_common import ensure_built, gpu_accept, compare_accept
 
 pytestmark = pytest.mark.gpu
 
@@ -23,18 +24,18 @@ def setup_module():
 @pytest.mark.parametrize("which", [0, 1])
 def test_tiny(which):
     x = W.workload_accept("tiny", which)
-    assert compare_accept(x, gpu_accept(x)) == 0
+    compare_accept(x, gpu_accept(x))
 
 
 def test_gqa1p7b_argmax():
     x = W.workload_accept("gqa1p7b")
-    assert compare_accept(x, gpu_accept(x)) == 0
+    compare_accept(x, gpu_accept(x))
 
 
 def test_gqa8b_reject():
     x = W.workload_accept("gqa8b")
-    differ = compare_accept(x, gpu_accept(x))
-    assert differ <= 2
+    worst = compare_accept(x, gpu_accept(x))
+    assert worst > 1.0
 
 
 @pytest.fixture(scope="module")
@@ -46,7 +47,7 @@ def sweep_inputs():
 def test_sweep_gumbel(sweep_inputs, T):
     x = sweep_inputs
     x.T = T
-    assert compare_accept(x, gpu_accept(x)) == 0
+    compare_accept(x, gpu_accept(x))
 
 
 EDGE = {
@@ -91,7 +92,7 @@ def test_repeated_calls_share_workspace():
     x = W.workload_accept("tiny", 1)
     ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     for _ in range(3):
-        assert compare_accept(x, gpu_accept(x, workspace=ws)) == 0
+        compare_accept(x, gpu_accept(x, workspace=ws))
     assert int(ws[:256].sum()) == 0
 
 
@@ -143,7 +144,7 @@ def test_many_slots_general_kernel():
     blocks = [4] * 530  # 2120 slots
     gammas = [int(g) for g in np.random.default_rng(11).integers(0, 5, size=len(blocks))]
     x = W.make_accept_inputs("many", W.MODE_ARGMAX, 0.0, 640, blocks, gammas, seed=12)
-    assert compare_accept(x, gpu_accept(x)) == 0
+    compare_accept(x, gpu_accept(x))
 
 
 @pytest.mark.parametrize("V", [4096, 4097])
@@ -173,9 +174,4 @@ def _random_accept(seed):
 
 @pytest.mark.parametrize("seed", range(10))
 def test_accept_random(seed):
-    x = _random_accept(seed)
-    if x.mode == W.MODE_REJECT:
-        margins = [m for r in oacc.accept_batch(x)["results"] for m in r.accept_margins]
-        if margins and min(margins) <= REJECT_MARGIN:
-            pytest.skip("a decision lies inside the fp32 rounding band for this seed")
-    compare_accept(x, gpu_accept(x))
+    compare_accept(_random_accept(seed), gpu_accept(_random_accept(seed)))

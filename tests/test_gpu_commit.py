@@ -67,7 +67,7 @@ def _oracle(c: W.CommitInputs, keep=None, seqs=None, tau=None, n_acc=None, k_new
 
 @pytest.mark.parametrize("name", list(CASES))
 def test_commit_parity(name):
-    c = W.make_commit_inputs(CASES[name](), seed=hash(name) % 1000 + 7)
+    c = W.make_commit_inputs(CASES[name](), seed=sum(map(ord, name)) + 7)  # fixed per case, replayable
     k, v, nl, st = _run(c)
     assert st == ssv.SSV_OK
     k_ref, v_ref, nl_ref = _oracle(c)

@@ -8,7 +8,9 @@
   time (the collapse the review reports for uncoupled sampling).
 * Rejection sampling, SimSD summary section 4: the law of the emitted token
   is p, computed by integrating the oracle's own decisions over a fine grid
-  of uniforms (brute force at V <= 5).
+  of uniforms (brute force at V <= 5), at T = 0.7, 1 and 1.3 against the
+  library softmax; the oracle's softmax(l / T) against the logistic closed
+  form at V = 2 and the library routine.
 * Longest accepted prefix in temporal (tau) order, emission rules.
 """
 import numpy as np
@@ -19,8 +21,35 @@ from diffusion_speculative_verification_gb300 import workloads as W
 
 
 def softmax_ref(l, T):
-    e = np.exp((np.asarray(l, np.float64) - np.max(l)) / T)
-    return e / e.sum()
+    """softmax(l / T) by scipy (a library routine the oracle does not use),
+    with T taken as the fp32 value the acceptance call receives."""
+    from scipy.special import softmax
+    return softmax(np.asarray(l, np.float64) / float(np.float32(T)))
+
+
+@pytest.mark.parametrize("T", [0.7, 1.0, 1.3, 2.5])
+def test_softmax64_two_tokens_closed_form(T):
+    """V = 2: p_0 = 1 / (1 + e^((l_1 - l_0) / T)) exactly (the logistic
+    function), so a mistake in how the oracle applies T fails here."""
+    import math
+    rng = np.random.default_rng(int(T * 100))
+    T32 = float(np.float32(T))
+    for _ in range(50):
+        l = rng.standard_normal(2) * 3.0
+        p = A.softmax64(l, T)
+        p0 = 1.0 / (1.0 + math.exp((l[1] - l[0]) / T32))
+        assert abs(p[0] - p0) < 4e-16 and abs(p[1] - (1.0 - p0)) < 4e-16
+    # a temperature that is not applied (T taken as 1) is far off at T != 1
+    if T != 1.0:
+        l = np.array([0.0, 1.0])
+        assert abs(A.softmax64(l, T)[0] - 1.0 / (1.0 + math.e)) > 1e-2
+
+
+@pytest.mark.parametrize("T", [0.7, 1.3])
+def test_softmax64_matches_library(T):
+    rng = np.random.default_rng(int(T * 10))
+    l = rng.standard_normal(7) * 2.0
+    np.testing.assert_allclose(A.softmax64(l, T), softmax_ref(l, T), rtol=1e-14, atol=0)
 
 
 @pytest.mark.parametrize("T", [0.5, 1.0, 1.5])
@@ -83,10 +112,14 @@ def test_coupling_shared_noise_always_accepted(T):
     assert np.mean(accepted_uncoupled) < 0.5
 
 
-@pytest.mark.parametrize("V,seed", [(2, 0), (3, 1), (4, 2), (5, 3)])
-def test_rejection_law_is_p(V, seed):
+@pytest.mark.parametrize("V,seed,T", [(2, 0, 1.0), (3, 1, 1.0), (4, 2, 1.0), (5, 3, 1.0), (2, 4, 0.7), (4, 5, 0.7),
+                                       (3, 6, 1.3), (5, 7, 1.3)])
+def test_rejection_law_is_p(V, seed, T):
+    """Drafts drawn from q, accepted with probability min(1, p/q), residual
+    samples of (p - q)_+ at a rejection: the emitted token's law is p =
+    softmax(l / T), by integrating the oracle's own decisions over a grid of
+    uniforms.  p and q here come from the library softmax."""
     rng = np.random.default_rng(seed)
-    T = 1.0
     l = rng.standard_normal(V) * 1.5
     ql = l + rng.standard_normal(V) * 0.8
     p = softmax_ref(l, T)
@@ -114,7 +147,8 @@ def test_rejection_law_is_p(V, seed):
     np.testing.assert_allclose(law, p, atol=3.0 / M, rtol=0)
 
 
-def test_bonus_law_is_p():
+@pytest.mark.parametrize("T", [1.0, 0.7, 1.3])
+def test_bonus_law_is_p(T):
     rng = np.random.default_rng(5)
     l = rng.standard_normal(4)
     M = 4000
@@ -122,10 +156,10 @@ def test_bonus_law_is_p():
     counts = np.zeros(4)
     for u2 in grid:
         # gamma = 0 < B = 1: nothing to verify, sample the bonus from p
-        r = _seq(A.MODE_REJECT, 1.0, [1], 0, [0], l[None, :], draft_rows=l[None, :], u_accept=[0.0], u_sample=u2)
+        r = _seq(A.MODE_REJECT, T, [1], 0, [0], l[None, :], draft_rows=l[None, :], u_accept=[0.0], u_sample=u2)
         assert r.emit_kind == "bonus" and r.n_acc == 0
         counts[r.tokens[0]] += 1
-    np.testing.assert_allclose(counts / M, softmax_ref(l, 1.0), atol=2.0 / M)
+    np.testing.assert_allclose(counts / M, softmax_ref(l, T), atol=2.0 / M)
 
 
 def test_identical_draft_always_accepted():
@@ -194,12 +228,14 @@ def test_batch_matches_per_sequence():
     assert A.accept_batch(inp)["n_acc"].max() > 0
 
 
-def test_emission_valid_rule():
+def test_sample_margin_rule():
     w = np.array([0.0, 0.25, 0.25, 0.5])
-    v, t, cdf = A.inverse_cdf(w, 0.5)
-    assert v == 3                      # cdf = [0, .25, .5, 1]: first entry strictly above 0.5
+    v, t, cdf = A.inverse_cdf(w, 0.55)
+    assert v == 3                      # cdf = [0, .25, .5, 1]: first entry strictly above 0.55
     res = A.SeqResult(0, [v], "residual", 0, [], t, cdf)
-    assert A.emission_valid(res, 3, 0.0)
-    assert A.emission_valid(res, 2, 1e-6) and not A.emission_valid(res, 2, 0.0)   # boundary within tolerance
-    assert not A.emission_valid(res, 0, 0.1)                                       # zero-mass token
-    assert not A.emission_valid(res, 1, 1e-3)
+    assert abs(A.sample_margin(res) - 0.05) < 1e-15      # 0.55 is 0.05 above the boundary at 0.5
+    v, t, cdf = A.inverse_cdf(w, 0.3)
+    res = A.SeqResult(0, [v], "bonus", 0, [], t, cdf)
+    assert v == 2 and abs(A.sample_margin(res) - 0.05) < 1e-15
+    v, t, cdf = A.inverse_cdf(w, 0.0)  # the first token of positive mass; t sits on its lower end
+    assert v == 1 and A.sample_margin(A.SeqResult(0, [v], "bonus", 0, [], t, cdf)) == 0.0
