@@ -49,6 +49,11 @@ attn_simt_kernel(const AttnParams p) {
   const ssv_seq s = p.seqs[b];
   const int i = row - s.q_off;
   const int B = s.block;
+  if (!seq_extents_ok(s, p.total_rows, p.total_cache, p.total_slots) || s.cache_len > p.max_cache ||
+      s.new_len > p.max_new || s.block > p.max_block) {
+    if (lane == 0) report(p.dev_status, SSV_ERR_INVALID);  // sequence outside the buffers: skipped
+    return;
+  }
   if (i >= s.new_len + 2 * B) return;
   const int kvh = h / (p.Hq / p.Hkv);
   const int32_t* tau = p.tau + s.tau_off;

@@ -237,7 +237,12 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       if (b < p.batch) {
         const ssv_seq s = p.seqs[b];
         const int rows = s.new_len + 2 * s.block;
-        const int nt = cdiv(rows, UR);
+        // a sequence outside the call's buffers (or above the stated maxima)
+        // gets no units: its rows are neither read nor written
+        const bool ok = seq_extents_ok(s, p.total_rows, p.total_cache, p.total_slots) &&
+                        s.cache_len <= p.max_cache && s.new_len <= p.max_new && s.block <= p.max_block;
+        if (!ok && cta == 0) report(p.dev_status, SSV_ERR_INVALID);
+        const int nt = ok ? cdiv(rows, UR) : 0;
         for (int t = 0; t < nt; ++t) {
           const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
           blocks += nb;
@@ -258,11 +263,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       carryB += __shfl_sync(0xffffffffu, ib, 31);
       carryC += __shfl_sync(0xffffffffu, ic, 31);
     }
+    __syncwarp();  // s_ntile entries written by every lane are read below
     if (cta == 0) {
       // stage maps must permute 1..B (a bad map cannot index out of range: report only)
       for (int b = 0; b < p.batch; ++b) {
         const ssv_seq s = p.seqs[b];
-        const bool ok = (s.block >= 1 && s.block <= 64) && warp_tau_is_permutation(p.tau + s.tau_off, s.block);
+        if (s_ntile[b] == 0) continue;  // skipped above (extents), or no rows
+        const bool ok = warp_tau_is_permutation(p.tau + s.tau_off, s.block);
         if (!ok) {
           if (lane == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
           break;

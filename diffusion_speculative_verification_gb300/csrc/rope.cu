@@ -2,7 +2,8 @@
 //
 // SimSD summary, section 3 "Position Encoding Alignment": mask slot D~_k
 // reuses the RoPE index of data token D_k.  Fresh prompt row i sits at
-// position C + i, tail row r at P + (r mod B).
+// position C + i, tail row r at P + (r mod B); or, with a position table,
+// each fresh row and each data row D_k at its table entry and D~_k at D_k's.
 //
 // One CTA handles ROWS consecutive rows.  Their first elements are loaded
 // at entry, together with the sequence table, so that the one DRAM round
@@ -71,6 +72,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kRopeThreads)
 rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_out, T* k_out,
                  int Hq, int Hkv, const ssv_seq* __restrict__ seqs, int batch, int total_rows,
+                 const int32_t* __restrict__ positions, int32_t* dev_status,
                  const __grid_constant__ RopeTheta th) {
   constexpr int HALF = D / 2;
   constexpr int VEC = Vec16<T>::N;
@@ -134,9 +136,27 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
       }
       if (b >= 0) {
         const ssv_seq sq = table ? s_seq[b] : seqs[b];
+        // a sequence outside the rows (or whose positions leave int range) is
+        // skipped: its rows are left as they are
+        const bool ok = sq.cache_len >= 0 && sq.new_len >= 0 && sq.block >= 1 && sq.block <= 64 &&
+                        sq.q_off >= 0 && (long long)sq.q_off + sq.new_len + 2LL * sq.block <= total_rows &&
+                        (long long)sq.cache_len + sq.new_len + sq.block <= 0x7fffffffLL;
         const int i = row - sq.q_off;
-        if (i < sq.new_len) pos = sq.cache_len + i;
-        else if (i < sq.new_len + 2 * sq.block) pos = sq.cache_len + sq.new_len + (i - sq.new_len) % sq.block;
+        if (!ok) {
+          report(dev_status, SSV_ERR_INVALID);
+        } else if (i < sq.new_len + 2 * sq.block) {
+          // the row whose position applies: itself, or for a tail row its data row
+          const int k = (i - sq.new_len) % sq.block;
+          const int src = (i < sq.new_len) ? row : sq.q_off + sq.new_len + k;
+          pos = (i < sq.new_len) ? sq.cache_len + i : sq.cache_len + sq.new_len + k;
+          if (positions) {
+            pos = positions[src];
+            if (pos < 0) {
+              report(dev_status, SSV_ERR_INVALID);
+              pos = -1;
+            }
+          }
+        }
       }
     }
     s_pos[threadIdx.x] = pos;
@@ -200,7 +220,8 @@ static cudaError_t launch_rope(const ssv_rope_args* a, const RopeTheta& th, cuda
   const int grid = (a->total_rows + kRopeRows - 1) / kRopeRows;
   return launch_pdl(rope_copy_kernel<T, D>, dim3(grid), dim3(kRopeThreads), 0, st,
                     static_cast<const T*>(a->q_in), static_cast<const T*>(a->k_in), static_cast<T*>(a->q_out),
-                    static_cast<T*>(a->k_out), a->Hq, a->Hkv, a->seqs, a->batch, a->total_rows, th);
+                    static_cast<T*>(a->k_out), a->Hq, a->Hkv, a->seqs, a->batch, a->total_rows, a->positions,
+                    a->dev_status, th);
 }
 
 }  // namespace ssv

@@ -180,4 +180,4 @@ extern "C" const char* ssv_status_string(ssv_status s) {
   return "unknown status";
 }
 
-extern "C" const char* ssv_version(void) { return "ssv 0.1 sm_103a"; }
+extern "C" const char* ssv_version(void) { return "ssv 0.2 sm_103a"; }

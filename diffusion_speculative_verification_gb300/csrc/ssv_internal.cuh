@@ -82,6 +82,19 @@ __device__ __forceinline__ bool warp_tau_is_permutation(const int32_t* tau, int 
   return ok && seen == full;
 }
 
+// The extents of sequence s lie inside the call's buffers: rows
+// [q_off, q_off + N + 2B) of the query-side arrays, cache rows
+// [kv_off, kv_off + C) and stage-map entries [tau_off, tau_off + B).  The
+// attention kernels check this on the device before touching a sequence and
+// skip (and report) one that fails.
+__host__ __device__ __forceinline__ bool seq_extents_ok(const ssv_seq& s, int total_rows, int total_cache,
+                                                        int total_slots) {
+  return s.cache_len >= 0 && s.new_len >= 0 && s.block >= 1 && s.block <= 64 && s.q_off >= 0 &&
+         (long long)s.q_off + s.new_len + 2LL * s.block <= (long long)total_rows && s.kv_off >= 0 &&
+         (long long)s.kv_off + s.cache_len <= (long long)total_cache && s.tau_off >= 0 &&
+         (long long)s.tau_off + s.block <= (long long)total_slots;
+}
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // host-side pieces shared by the entry points (validation, launches with the

@@ -41,7 +41,8 @@ class SeqC(C.Structure):
 class RopeArgs(C.Structure):
     _fields_ = [("q_in", C.c_void_p), ("k_in", C.c_void_p), ("q_out", C.c_void_p), ("k_out", C.c_void_p),
                 ("dtype", C.c_int), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32),
-                ("base", C.c_double), ("seqs", C.c_void_p), ("batch", C.c_int32), ("total_rows", C.c_int32)]
+                ("base", C.c_double), ("seqs", C.c_void_p), ("batch", C.c_int32), ("total_rows", C.c_int32),
+                ("positions", C.c_void_p), ("dev_status", C.c_void_p)]
 
 
 class AttnArgs(C.Structure):
@@ -189,16 +190,19 @@ def _workspace(nbytes: int, device, ws=None):
 # ---------------------------------------------------------------------------
 # entry points
 # ---------------------------------------------------------------------------
-def rope_args(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None):
+def rope_args(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, positions=None, dev_status=None):
+    """positions: optional int32 [rows] device table (fresh rows and data rows
+    at their entries, mask rows at their data row's)."""
     q_out = q if q_out is None else q_out
     k_out = k if k_out is None else k_out
     return RopeArgs(_ptr(q), _ptr(k), _ptr(q_out), _ptr(k_out), _dtype_code(q), q.shape[1], k.shape[1], q.shape[2],
-                    float(base), _ptr(batch.dev), batch.batch, q.shape[0])
+                    float(base), _ptr(batch.dev), batch.batch, q.shape[0], _ptr(positions), _ptr(dev_status))
 
 
-def rope_copy(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, stream=None):
+def rope_copy(q, k, batch: Batch, base: float = 10000.0, q_out=None, k_out=None, stream=None, positions=None,
+              dev_status=None):
     """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d]; returns (q_out, k_out)."""
-    a = rope_args(q, k, batch, base, q_out, k_out)
+    a = rope_args(q, k, batch, base, q_out, k_out, positions, dev_status)
     _check(lib().ssv_rope_copy(C.byref(a), _stream_ptr(stream)), "ssv_rope_copy")
     return (q if q_out is None else q_out), (k if k_out is None else k_out)
 

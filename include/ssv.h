@@ -77,12 +77,14 @@ typedef enum {
  * stage map occupies tau[tau_off .. tau_off + B).  Sequences are packed in
  * increasing q_off order without overlap (q_off[b] + N_b + 2B_b <=
  * q_off[b+1]): kernels find a row's sequence by binary search on q_off.
- * The table is a precondition of every call that takes it: each extent lies
- * inside its buffer (q_off + N + 2B <= total_rows, kv_off + C <= the cache
- * rows, tau_off + B <= total_slots, all offsets >= 0).  ssv_commit checks
- * the stage-map extent and its destination room on the device; the rotation
- * and attention kernels use the offsets as given, so a table outside its
- * buffers makes them read (and the attention write) outside the buffers.
+ * Every kernel checks each sequence's extents on the device before it
+ * touches the sequence's rows (q_off + N + 2B <= total_rows, kv_off + C <=
+ * the cache rows, tau_off + B <= total_slots, all offsets >= 0, 1 <= B <=
+ * 64, and for the attention C, N, B within max_cache, max_new, max_block):
+ * a sequence that fails is skipped -- nothing of it is read or written --
+ * and SSV_ERR_INVALID is reported through dev_status.  Overlapping or
+ * unsorted sequences are not detected (their rows may be processed twice or
+ * under the wrong sequence, still inside the buffers).
  */
 typedef struct {
   int32_t cache_len;  /* C >= 0 */
@@ -98,8 +100,17 @@ typedef struct {
  * SimSD summary, section 3 "Position Encoding Alignment": each mask slot
  * D~_k reuses the RoPE index of its data token D_k.
  *
- * Position of fresh prompt row i is C + i; of tail row r (0 <= r < 2B) it is
- * P + (r mod B), P = C + N.  Rotate-half pairing (x_i, x_{i+d/2}) with
+ * Positions, without a position table (positions == NULL): fresh prompt row
+ * i is at C + i; tail row r (0 <= r < 2B) at P + (r mod B), P = C + N.
+ * With a table (device int32 [total_rows], entries >= 0): fresh prompt row
+ * i of a sequence is at positions[q_off + i], data row D_k at
+ * positions[q_off + N + k - 1], and mask row D~_k at D_k's entry (entries
+ * at mask rows are not read).  The table serves passes whose positions are
+ * not contiguous: after a commit (ssv_commit) the accepted data rows keep
+ * the positions of their slots, so the next pass over the same block gives
+ * its remaining slots, and the emitted token entering as a fresh prompt
+ * row, the positions of their own slots (a reading: the pages do not
+ * describe the loop).  Rotate-half pairing (x_i, x_{i+d/2}) with
  * theta_i = base^(-2i/d); angles are formed and reduced in fp64, the
  * rotation is done in fp32 and stored in `dtype`.
  *
@@ -109,7 +120,11 @@ typedef struct {
  *       exactly one sequence (rows outside all sequences are left untouched).
  * d in {64, 128}; pointers 16-byte aligned.
  * Errors: SSV_ERR_INVALID (null, non-positive sizes, misalignment),
- *         SSV_ERR_UNSUPPORTED (d), SSV_ERR_CUDA (launch).
+ *         SSV_ERR_UNSUPPORTED (d), SSV_ERR_CUDA (launch); on device
+ *         SSV_ERR_INVALID for a sequence whose rows leave [0, total_rows)
+ *         (or B outside 1..64, or C + N + B beyond int range; its rows are
+ *         left untouched) and for a negative table entry (that row is left
+ *         untouched).
  * ---------------------------------------------------------------------- */
 typedef struct {
   const void* q_in;
@@ -122,6 +137,8 @@ typedef struct {
   const ssv_seq* seqs;         /* device */
   int32_t batch;
   int32_t total_rows;
+  const int32_t* positions;    /* device [total_rows] or NULL (see above) */
+  int32_t* dev_status;         /* device, may be NULL */
 } ssv_rope_args;
 
 SSV_API ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream);
@@ -154,7 +171,9 @@ SSV_API ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream);
  * max_cache / max_new / max_block bound every sequence's C / N / B (used to
  * size grids and workspace).  scale 0 means 1/sqrt(d).
  * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_WORKSPACE,
- *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU, SSV_ERR_TIMEOUT.
+ *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU, SSV_ERR_TIMEOUT, and
+ *         SSV_ERR_INVALID for a sequence outside the buffers (skipped: its
+ *         rows of o are not written).
  * Scheduling: the bf16 path launches one CTA per SM; where a unit of work is
  * split across CTAs, the CTA holding its first key block waits (bounded, about
  * one second of SM clock) for the others' partial results.  Work on other
@@ -437,7 +456,7 @@ SSV_API ssv_status ssv_get_status(int32_t* dev_status, void* stream);
 
 SSV_API const char* ssv_status_string(ssv_status s);
 
-/* Library build identification, e.g. "ssv 0.1 sm_103a". */
+/* Library build identification, e.g. "ssv 0.2 sm_103a". */
 SSV_API const char* ssv_version(void);
 
 /* ------------------------------------------------------------------------

@@ -9,15 +9,27 @@ absolute position 0 at the first cache key.
 Positions of one sequence's query rows (cache keys arrive already rotated):
   * fresh prompt row i        -> C + i
   * tail row r (0 <= r < 2B)  -> P + (r mod B), with P = C + N
-so D_k (r = k-1) and D~_k (r = B + k-1) share position P + k - 1.
+so D_k (r = k-1) and D~_k (r = B + k-1) share position P + k - 1; or, with
+explicit positions for the fresh rows and data rows, those, and D~_k again
+takes D_k's.
 """
 from __future__ import annotations
 
 import numpy as np
 
 
-def rope_positions(C: int, N: int, B: int) -> np.ndarray:
-    """int64 [N + 2B] absolute position of each query row of one sequence."""
+def rope_positions(C: int, N: int, B: int, given=None) -> np.ndarray:
+    """int64 [N + 2B] absolute position of each query row of one sequence.
+
+    `given` (optional, N + B entries): explicit positions of the N fresh
+    prompt rows and of the data rows D_1..D_B, for a pass whose positions are
+    not contiguous (the remaining slots of a block after a commit, which
+    keep their own slots' positions; a reading, the pages do not describe
+    the loop).  Mask row D~_k still takes D_k's position (RoPE copy)."""
+    if given is not None:
+        given = [int(x) for x in given]
+        assert len(given) == N + B
+        return np.asarray(given[:N] + [given[N + (r % B)] for r in range(2 * B)], dtype=np.int64)
     P = C + N
     pos = [C + i for i in range(N)]
     pos += [P + (r % B) for r in range(2 * B)]
@@ -50,13 +62,16 @@ def rotate(x: np.ndarray, pos: np.ndarray, base: float = 10000.0) -> np.ndarray:
     return out
 
 
-def rope_copy_batch(seqs: np.ndarray, q: np.ndarray, k: np.ndarray, base: float = 10000.0):
-    """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d] of a packed batch (float64)."""
+def rope_copy_batch(seqs: np.ndarray, q: np.ndarray, k: np.ndarray, base: float = 10000.0, positions=None):
+    """Rotate Q [rows, Hq, d] and K_new [rows, Hkv, d] of a packed batch
+    (float64).  positions: optional [rows] table, read at each sequence's
+    fresh rows and data rows (see rope_positions)."""
     qo = np.empty(q.shape, np.float64)
     ko = np.empty(k.shape, np.float64)
     for C, N, B, q_off, _kv_off, _t in np.asarray(seqs):
         rows = N + 2 * B
-        pos = rope_positions(int(C), int(N), int(B))
+        given = None if positions is None else np.asarray(positions)[q_off:q_off + N + B]
+        pos = rope_positions(int(C), int(N), int(B), given)
         qo[q_off:q_off + rows] = rotate(q[q_off:q_off + rows], pos, base)
         ko[q_off:q_off + rows] = rotate(k[q_off:q_off + rows], pos, base)
     return qo, ko

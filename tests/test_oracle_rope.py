@@ -18,6 +18,32 @@ def test_positions_fixture():
     assert pos.tolist() == meta["pos"]
 
 
+def test_given_positions_fixture():
+    meta, _ = read_fixture("rope_positions_given_C5_N1_B2.txt")
+    pos = rope_positions(meta["C"], meta["N"], meta["B"], meta["given"])
+    assert pos.tolist() == meta["pos"]
+    # the default positions are what a table holding them gives
+    C, N, B = 9, 2, 4
+    dflt = rope_positions(C, N, B)
+    assert rope_positions(C, N, B, list(dflt[:N + B])).tolist() == dflt.tolist()
+
+
+def test_given_positions_batch_reads_fresh_and_data_rows_only():
+    a = W.make_attn_inputs("t", [3, 0], [2, 1], [3, 2], 2, 1, 64, W.F32, seed=21)
+    q = W.values_f64(a.q_raw, a.dtype)
+    k = W.values_f64(a.k_new_raw, a.dtype)
+    rows = a.total_rows
+    table = np.full(rows, -99, np.int64)   # mask-row entries must never be read
+    per = [[11, 12, 40, 41, 42], [7, 30, 31]]
+    for (C, N, B, q_off, _kv, _t), given in zip(a.seqs, per):
+        table[q_off:q_off + N + B] = given
+    qo, ko = rope_copy_batch(a.seqs, q, k, positions=table)
+    for (C, N, B, q_off, _kv, _t), given in zip(a.seqs, per):
+        pos = given[:N] + given[N:] + given[N:]
+        np.testing.assert_array_equal(qo[q_off:q_off + N + 2 * B], rotate(q[q_off:q_off + N + 2 * B], np.array(pos)))
+        np.testing.assert_array_equal(ko[q_off:q_off + N + 2 * B], rotate(k[q_off:q_off + N + 2 * B], np.array(pos)))
+
+
 def test_pair_shares_position():
     for C, N, B in [(0, 0, 1), (16, 0, 4), (5, 9, 32)]:
         pos = rope_positions(C, N, B)
