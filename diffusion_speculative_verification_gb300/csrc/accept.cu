@@ -645,6 +645,9 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
     p.e2pow[i].x = (float)v;
     p.e2pow[i].y = (float)(v - (double)(float)v);
   }
+  const FaultSetting f = fault_for(SSV_FAULT_ACCEPT);
+  p.wait_budget = f.budget;
+  p.fault_skip = f.skip;
   int mode = a->mode;
   if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;  // T = 0 ignores the noise
   p.mode = mode;

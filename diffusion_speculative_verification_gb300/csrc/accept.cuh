@@ -93,6 +93,11 @@ struct AcceptParams {
   // i = 0..7, likewise (host-computed)
   float c2_hi, c2_lo;
   float2 e2pow[8];
+  // bounded waits of the streaming reduce give up after wait_budget SM
+  // cycles; fault_skip >= 0 makes its CTA 0 leave out that chunk's copy
+  // (test support, ssv_set_fault_injection)
+  long long wait_budget;
+  int fault_skip;
 };
 
 constexpr int kEmitSub = 2048;  // vocabulary entries per emission CTA (256 threads x 8)

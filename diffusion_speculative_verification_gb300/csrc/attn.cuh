@@ -26,6 +26,10 @@ struct AttnParams {
   // whose outputs overlap none of seqs, tau and the KV cache; those may then
   // be read before that kernel completes (programmatic dependent launch).
   int early;
+  // bounded waits give up after wait_budget SM cycles; fault_skip >= 0 makes
+  // CTA 0 leave out that key-block copy (test support, ssv_set_fault_injection)
+  long long wait_budget;
+  int fault_skip;
 };
 
 cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);

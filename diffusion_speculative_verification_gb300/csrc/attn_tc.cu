@@ -125,11 +125,11 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
 }
 // Waits (bounded) until *p reaches `target`; false on timeout (raising *abort)
 // or when another role has raised *abort.
-__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort) {
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort, long long budget) {
   const long long t0 = clock64();
   while (ld_acquire(p) < target) {
     if (*abort) return false;
-    if (clock64() - t0 > ptx::kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }
@@ -215,6 +215,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   auto bar = [&](uint32_t i) -> uint32_t { return sbase + C_::SM_BAR + 8u * i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long wb = p.wait_budget;  // cycles a bounded wait may take (kWaitBudget unless a test shortens it)
   const int R = 128 / G;
   const int UR = MT * R;
   const int P = gridDim.x;   // CTAs launched; only the first Pe own key blocks
@@ -419,7 +420,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       bool run = true;
       auto load_k = [&](const Unit& x, int j) -> bool {
         const int st = kn % NSK;
-        if (kn >= NSK && !mbar_wait(bar(B_K_EMPTY + st), ((kn / NSK) - 1) & 1, abort)) return false;
+        if (kn >= NSK && !mbar_wait(bar(B_K_EMPTY + st), ((kn / NSK) - 1) & 1, abort, wb)) return false;
+        if (cta == 0 && kn == p.fault_skip) {  // test support: this key block's copy is left out
+          ++kn;
+          return true;
+        }
         mbar_expect_tx(bar(B_K_FULL + st), TILE_BYTES);
         const bool cache = j < x.cache_blocks;
         const CUtensorMap* mk = cache ? &maps.kc : &maps.kn;
@@ -432,7 +437,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       };
       auto load_v = [&](const Unit& x, int j) -> bool {
         const int st = vn % NSV;
-        if (vn >= NSV && !mbar_wait(bar(B_V_EMPTY + st), ((vn / NSV) - 1) & 1, abort)) return false;
+        if (vn >= NSV && !mbar_wait(bar(B_V_EMPTY + st), ((vn / NSV) - 1) & 1, abort, wb)) return false;
         mbar_expect_tx(bar(B_V_FULL + st), TILE_BYTES);
         const bool cache = j < x.cache_blocks;
         const CUtensorMap* mv = cache ? &maps.vc : &maps.vn;
@@ -470,7 +475,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         dep_wait();
         // the first key block does not depend on Q: start it before waiting for the Q buffer
         if (jk == k && !load_k(x, jk++)) break;
-        if (seg > 0 && !mbar_wait(bar(B_Q_EMPTY), (seg - 1) & 1, abort)) break;
+        if (seg > 0 && !mbar_wait(bar(B_Q_EMPTY), (seg - 1) & 1, abort, wb)) break;
         mbar_expect_tx(bar(B_Q_FULL), x.mc * TILE_BYTES);
         for (int mt = 0; mt < x.mc; ++mt) {
           const int z = x.q_off + x.row0 + mt * R;
@@ -492,17 +497,17 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       // drain (bounded, regardless of abort): the last Q load and the last K / V loads
       if (seg > 0) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_Q_FULL), (seg - 1) & 1) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_Q_FULL), (seg - 1) & 1) && clock64() - t0 < wb) {
         }
       }
       for (int n = (kn > NSK ? kn - NSK : 0); n < kn; ++n) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_K_FULL + n % NSK), (n / NSK) & 1) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_K_FULL + n % NSK), (n / NSK) & 1) && clock64() - t0 < wb) {
         }
       }
       for (int n = (vn > NSV ? vn - NSV : 0); n < vn; ++n) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar(B_V_FULL + n % NSV), (n / NSV) & 1) && clock64() - t0 < kWaitBudget) {
+        while (!mbar_try_wait(bar(B_V_FULL + n % NSV), (n / NSV) & 1) && clock64() - t0 < wb) {
         }
       }
     }
@@ -540,7 +545,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           seen &= ~bit;
           return true;
         }
-        return mbar_wait_poll(b, par, abort);
+        return mbar_wait_poll(b, par, abort, wb);
       };
       auto note = [&](uint32_t r, uint32_t bit_a, uint32_t bit_b) {
         seen |= ((r & 1u) ? bit_a : 0u) | ((r & 2u) ? bit_b : 0u);
@@ -580,7 +585,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       while (run && remaining > 0) {
         const Unit x = decode(u);
         const int len = min(x.nblocks - k, remaining);
-        if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort)) break;
+        if (!mbar_wait_poll(bar(B_Q_FULL), seg & 1, abort, wb)) break;
         if (x.mc == 1) {
           // ---- one active tile: S double-buffered over both tiles' S columns, so
           // S(n + 1) runs while the softmax warps work on S(n).  Per block: PV(n)
@@ -590,7 +595,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           if (len > 1 && !issue_s_db(vb, vph, SEEN_V, pdb_bar(dbp), pdb_par(dbp), SEEN_PD)) break;
           for (int i = 0; i < len; ++i) {
             if (!wait_seen(SEEN_V, vb, vph) || !wait_seen(SEEN_PD, pdb_bar(dbp), pdb_par(dbp)) ||
-                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
+                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort, wb))) {
               run = false;
               break;
             }
@@ -628,7 +633,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             if (!wait_seen(SEEN_V, vb, vph)) { run = false; break; }
             // tile 0
             if (!wait_seen(SEEN_P0, pb0, pph0) ||
-                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort))) {
+                (i == 0 && nseg0 > 0 && !mbar_wait_poll(bar(B_O_FREE), (nseg0 - 1) & 1, abort, wb))) {
               run = false;
               break;
             }
@@ -648,7 +653,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             }
             // tile 1
             if (!wait_seen(SEEN_P1, pb1, pph1) ||
-                (i == 0 && nseg1 > 0 && !mbar_wait_poll(bar(B_O_FREE + 1), (nseg1 - 1) & 1, abort))) {
+                (i == 0 && nseg1 > 0 && !mbar_wait_poll(bar(B_O_FREE + 1), (nseg1 - 1) & 1, abort, wb))) {
               run = false;
               break;
             }
@@ -681,7 +686,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       // every MMA issued by this thread completes before TMEM is released
       mma_commit(bar(B_FINAL));
       const long long t0 = clock64();
-      while (!mbar_try_wait(bar(B_FINAL), 0) && clock64() - t0 < kWaitBudget) {
+      while (!mbar_try_wait(bar(B_FINAL), 0) && clock64() - t0 < wb) {
       }
     }
   } else {
@@ -696,7 +701,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     int n2 = 0, ndb = 0;     // blocks in two-tile / one-tile units (their S / P barrier phases)
     bool run = true;
     auto warp_wait = [&](uint32_t b, uint32_t parity) -> bool {
-      const bool w = mbar_wait(b, parity, abort);
+      const bool w = mbar_wait(b, parity, abort, wb);
       return __all_sync(0xffffffffu, w);
     };
     while (run && remaining > 0) {
@@ -977,7 +982,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               if (lane == 0) red_release_add(counter, 1);
             } else {
               int ok = 1;
-              if (lane == 0) ok = wait_count(counter, c_b - c_a, abort) ? 1 : 0;
+              if (lane == 0) ok = wait_count(counter, c_b - c_a, abort, wb) ? 1 : 0;
               ok = __shfl_sync(0xffffffffu, ok, 0);
               __syncwarp();  // the other lanes' loads below follow lane 0's acquire
               if (!ok) run = false;

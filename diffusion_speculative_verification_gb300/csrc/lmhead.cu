@@ -108,6 +108,11 @@ struct LmParams {
   int32_t* row_slot;            // [S]: slot of each compacted row
   int32_t* cnt_tile;            // [Mt]
   unsigned long long* rowkey;   // [Mt * 128]: best (score, index) key of each row, 0 = none
+  // bounded waits give up after wait_budget SM cycles; fault_skip >= 0 makes
+  // CTA 0 leave out that operand stage's copies (test support,
+  // ssv_set_fault_injection)
+  long long wait_budget;
+  int fault_skip;
 };
 
 // Order-preserving 32-bit image of a non-NaN float (-0 taken as +0), above
@@ -139,10 +144,10 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 
 // Bounded wait that ignores the abort flag: used to drain a role's own
 // asynchronous work before the CTA exits.
-__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, long long budget) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitBudget) return false;
+    if (clock64() - t0 > budget) return false;
   return true;
 }
 
@@ -358,11 +363,15 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
         piece_of(p.V16, j_begin + pc, v0, w);
         for (int kc = 0; kc < p.nk; ++kc) {
           const int s = it % kLmStages;
-          if (it >= kLmStages && !mbar_wait(bar(LB_EMPTY + s), ((it / kLmStages) - 1) & 1, abort)) {
+          if (it >= kLmStages && !mbar_wait(bar(LB_EMPTY + s), ((it / kLmStages) - 1) & 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }
           const uint32_t fb = bar(LB_FULL + s);
+          if (blockIdx.x == 0 && it == p.fault_skip) {  // test support: this stage's copies are left out
+            ++it;
+            continue;
+          }
           mbar_expect_tx(fb, kLmABytes + (uint32_t)w * 128u);
           tma_load_2d(sbase + SM_A + s * kLmABytes, hmap, kc * 64, m * 128, fb);
           const uint32_t bdst = sbase + SM_B + s * kLmBBytes;
@@ -378,7 +387,7 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
       }
       // every copy issued lands before the CTA exits (the older ones were
       // consumed before their stage was reused)
-      for (int j = max(0, it - kLmStages); j < it; ++j) drain_wait(bar(LB_FULL + j % kLmStages), (j / kLmStages) & 1);
+      for (int j = max(0, it - kLmStages); j < it; ++j) drain_wait(bar(LB_FULL + j % kLmStages), (j / kLmStages) & 1, p.wait_budget);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -389,13 +398,13 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
         int v0, w;
         piece_of(p.V16, j_begin + pc, v0, w);
         const int buf = pc & 1;
-        if (pc >= 2 && !mbar_wait_poll(bar(LB_ACCE + buf), ((pc >> 1) - 1) & 1, abort)) break;
+        if (pc >= 2 && !mbar_wait_poll(bar(LB_ACCE + buf), ((pc >> 1) - 1) & 1, abort, p.wait_budget)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)buf * 256u;
         const uint32_t idesc = idesc_bf16(128, (uint32_t)w, false);
         for (int kc = 0; kc < p.nk; ++kc) {
           const int s = it % kLmStages;
-          if (!mbar_wait_poll(bar(LB_FULL + s), (it / kLmStages) & 1, abort)) {
+          if (!mbar_wait_poll(bar(LB_FULL + s), (it / kLmStages) & 1, abort, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -411,7 +420,7 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
       }
       // every MMA issued completes before TMEM is released
       mma_commit(bar(LB_FIN));
-      drain_wait(bar(LB_FIN), 0);
+      drain_wait(bar(LB_FIN), 0, p.wait_budget);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -493,7 +502,9 @@ lmhead_accept_kernel(const __grid_constant__ LmMaps maps, const LmParams p) {
         if (nrow && pc + 1 < npieces) prefetch_noise_l2(nrow, v0 + 256, a.V);
         load_noise<32>(p, nrow, v0, gn[0]);
       }
-      if (!mbar_wait(bar(LB_ACCF + buf), (pc >> 1) & 1, abort)) {
+      // warp-uniform: a lane that saw the phase complete while another gave up
+      // must not go on to the warp-collective TMEM loads alone
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(LB_ACCF + buf), (pc >> 1) & 1, abort, p.wait_budget))) {
         ok = false;
         break;
       }
@@ -734,6 +745,11 @@ extern "C" ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* w
   p.n_rows = reinterpret_cast<int32_t*>(w + L.n_rows);
   p.row_slot = reinterpret_cast<int32_t*>(w + L.row_slot);
   p.rowkey = reinterpret_cast<unsigned long long*>(w + L.rowkey);
+  const FaultSetting f = fault_for(SSV_FAULT_LMHEAD);
+  p.wait_budget = f.budget;
+  p.fault_skip = f.skip;
+  c.wait_budget = f.budget;
+  c.fault_skip = -1;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int gather_grid = std::min(nsm, std::max(1, (a->total_slots + 15) / 16));
   cudaError_t e = launch_pdl(lmhead_gather_kernel, dim3(gather_grid), dim3(kGatherThreads), 0, s, p);

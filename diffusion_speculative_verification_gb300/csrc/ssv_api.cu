@@ -6,7 +6,41 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 using namespace ssv;
+
+// ---------------------------------------------------------------------------
+// test support: fault injection without a GPU fault (ssv_set_fault_injection)
+// ---------------------------------------------------------------------------
+namespace {
+std::atomic<int> g_fault_kernel{SSV_FAULT_NONE};
+std::atomic<int> g_fault_skip{-1};
+std::atomic<long long> g_fault_budget{kDefaultWaitBudget};
+}  // namespace
+
+namespace ssv {
+FaultSetting fault_for(int kernel) {
+  if (kernel == SSV_FAULT_NONE || g_fault_kernel.load() != kernel) return {kDefaultWaitBudget, -1};
+  return {g_fault_budget.load(), g_fault_skip.load()};
+}
+}  // namespace ssv
+
+extern "C" ssv_status ssv_set_fault_injection(const ssv_fault_injection* f) {
+  if (!f) {
+    g_fault_kernel = SSV_FAULT_NONE;
+    g_fault_skip = -1;
+    g_fault_budget = kDefaultWaitBudget;
+    return SSV_OK;
+  }
+  if (f->kernel < SSV_FAULT_NONE || f->kernel > SSV_FAULT_LMHEAD || f->skip < -1 || f->wait_budget_cycles < 1000 ||
+      f->wait_budget_cycles > kDefaultWaitBudget)
+    return SSV_ERR_INVALID;
+  g_fault_budget = f->wait_budget_cycles;
+  g_fault_skip = f->skip;
+  g_fault_kernel = f->kernel;
+  return SSV_OK;
+}
 
 namespace {
 
@@ -54,6 +88,9 @@ AttnParams to_params(const ssv_attn_args* a) {
   p.max_block = a->max_block;
   p.dev_status = a->dev_status;
   p.early = 0;
+  const FaultSetting f = fault_for(SSV_FAULT_ATTN);
+  p.wait_budget = f.budget;
+  p.fault_skip = f.skip;
   return p;
 }
 

@@ -97,6 +97,19 @@ __host__ __device__ __forceinline__ bool seq_extents_ok(const ssv_seq& s, int to
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Bounded waits give up after this many SM cycles (about one second).
+constexpr long long kDefaultWaitBudget = 1ll << 31;
+
+// Test support (ssv_set_fault_injection): the wait budget and the index of
+// the copy that CTA 0 leaves out, for a launch of `kernel` (an
+// ssv_fault_kernel); {kDefaultWaitBudget, -1} unless that kernel is the one
+// chosen.  Read on the host at launch time.
+struct FaultSetting {
+  long long budget;
+  int skip;
+};
+FaultSetting fault_for(int kernel);
+
 // host-side pieces shared by the entry points (validation, launches with the
 // early-read flag of programmatic dependent launch)
 ssv_status rope_validate(const ssv_rope_args* a);

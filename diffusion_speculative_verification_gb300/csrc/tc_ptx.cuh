@@ -1,16 +1,19 @@
 // Inline-PTX wrappers for the Blackwell (sm_100-family) asynchronous units
 // used by the tensor-core attention kernels: mbarrier, TMA tiled loads,
 // tcgen05 (TMEM allocation, MMA, commit, loads/stores).  Every wait is
-// bounded: it gives up after kWaitBudget SM cycles (about one second) or as
-// soon as another role of the CTA has raised the shared abort flag.
+// bounded: it gives up after a budget of SM cycles (kWaitBudget, about one
+// second, unless a test shortens it) or as soon as another role of the CTA
+// has raised the shared abort flag.
 #pragma once
 
 #include <stdint.h>
 
+#include "ssv_internal.cuh"
+
 namespace ssv {
 namespace ptx {
 
-constexpr long long kWaitBudget = 1ll << 31;
+constexpr long long kWaitBudget = kDefaultWaitBudget;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -73,12 +76,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase of parity `parity` to complete.  Returns false
 // (and raises *abort) when the budget runs out; returns false at once if
 // another role already raised *abort.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, long long budget) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }
@@ -97,13 +100,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Bounded wait by polling (never suspends): for a single latency-critical
 // thread such as the MMA issuer.  Same contract as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int* abort, long long budget) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort = 1;
       return false;
     }

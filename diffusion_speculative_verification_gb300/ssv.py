@@ -24,7 +24,8 @@ ARGMAX, GUMBEL, REJECT = 0, 1, 2
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
            "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_lmhead_accept_workspace", "ssv_lmhead_accept",
-           "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench")
+           "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench", "ssv_set_fault_injection")
+FAULT_NONE, FAULT_ATTN, FAULT_ACCEPT, FAULT_LMHEAD = 0, 1, 2, 3
 
 
 class SsvError(RuntimeError):
@@ -70,6 +71,10 @@ class CommitArgs(C.Structure):
                 ("batch", C.c_int32), ("tau", C.c_void_p), ("n_acc", C.c_void_p), ("dst_off", C.c_void_p),
                 ("dst_cap", C.c_void_p), ("new_len", C.c_void_p), ("total_rows", C.c_int32),
                 ("total_slots", C.c_int32), ("dst_rows", C.c_int32), ("dev_status", C.c_void_p)]
+
+
+class FaultInjection(C.Structure):
+    _fields_ = [("kernel", C.c_int), ("skip", C.c_int32), ("wait_budget_cycles", C.c_int64)]
 
 
 class LmheadArgs(C.Structure):
@@ -360,6 +365,17 @@ def lmhead_accept(mode, T, hidden_states, lm_head, draft_tokens, tau, block, gam
     _check(lib().ssv_lmhead_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
            "ssv_lmhead_accept")
     return n_acc, n_out, tokens
+
+
+def set_fault_injection(kernel=None, skip: int = -1, wait_budget_cycles: int = 1 << 31):
+    """Test support: shorten the bounded waits of one kernel and make its CTA 0
+    leave out one copy (see ssv_set_fault_injection); kernel None restores the
+    defaults."""
+    if kernel is None:
+        _check(lib().ssv_set_fault_injection(None), "ssv_set_fault_injection")
+        return
+    f = FaultInjection(int(kernel), int(skip), int(wait_budget_cycles))
+    _check(lib().ssv_set_fault_injection(C.byref(f)), "ssv_set_fault_injection")
 
 
 def get_status(dev_status, stream=None) -> int:

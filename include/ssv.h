@@ -448,6 +448,41 @@ SSV_API ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* work
                                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * ssv_set_fault_injection -- test support for failure detection.
+ * The pages have no counterpart: this lets a test make a bounded device wait
+ * run out without faulting, trapping or hanging the GPU.  For the chosen
+ * kernel -- the tensor-core attention (SSV_FAULT_ATTN), the streaming
+ * acceptance reduce (SSV_FAULT_ACCEPT) or the fused LM head's GEMM
+ * (SSV_FAULT_LMHEAD) -- every bounded wait gives up after
+ * wait_budget_cycles SM cycles instead of about one second, and, if
+ * skip >= 0, CTA 0 leaves out one asynchronous copy: its skip-th key block
+ * (attention), its skip-th vocabulary chunk (acceptance) or its skip-th
+ * operand stage (LM head), so that the wait for that copy runs out.  The
+ * kernel then drains every copy and MMA it issued (bounded), releases its
+ * tensor memory, writes SSV_ERR_TIMEOUT to dev_status and returns; its
+ * outputs are unspecified and its workspace counters must be cleared before
+ * the workspace is used again (as after any SSV_ERR_TIMEOUT).
+ * The setting is process-wide and applies to every later launch of that
+ * kernel from every host thread, until reset with NULL.  For tests only.
+ * f: kernel in SSV_FAULT_NONE..SSV_FAULT_LMHEAD, skip >= -1,
+ *    1000 <= wait_budget_cycles <= 2^31.  Errors: SSV_ERR_INVALID.
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  SSV_FAULT_NONE = 0,
+  SSV_FAULT_ATTN = 1,
+  SSV_FAULT_ACCEPT = 2,
+  SSV_FAULT_LMHEAD = 3
+} ssv_fault_kernel;
+
+typedef struct {
+  ssv_fault_kernel kernel;
+  int32_t skip;                /* index of the copy CTA 0 leaves out, or -1 */
+  int64_t wait_budget_cycles;  /* budget of every bounded wait of that kernel */
+} ssv_fault_injection;
+
+SSV_API ssv_status ssv_set_fault_injection(const ssv_fault_injection* f);
+
+/* ------------------------------------------------------------------------
  * Status and utilities
  * ---------------------------------------------------------------------- */
 /* Waits for `stream`, reads the device status word, resets it to 0 and
