@@ -701,12 +701,16 @@ extern "C" ssv_status ssv_accept(const ssv_accept_args* a, void* ws, size_t ws_b
 // For callers that cannot allocate device memory themselves.  The scratch
 // lives in one file-scope array per device (kNoAllocScratchBytes, reserved
 // by every GPU that loads this library until the process exits).  Host code
-// cannot use the array's name as a device address, so the first call on each
-// device looks the address up with cudaGetSymbolAddress while that device is
-// current and caches it.  Every call shares the array: calls that overlap on
-// the GPU (other streams, other host threads) race and must be serialised by
-// the caller.  The arrival counters are cleared with a memset at each call.
+// cannot use the array's name as a device address, so the first call in each
+// CUDA context looks the address up with cudaGetSymbolAddress while that
+// context is current and caches it per device, together with the context it
+// belongs to: a call from another context on the same device (after
+// cudaDeviceReset, or with a context the caller made current) looks it up
+// again.  Every call shares the array: calls that overlap on the GPU (other
+// streams, other host threads) race and must be serialised by the caller.
+// The arrival counters are cleared with a memset at each call.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
 #include <mutex>
 
 namespace {
@@ -716,19 +720,47 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_accept_scratch[kNoAllocScratchBytes];
 
+struct ScratchEntry {
+  CUcontext ctx;
+  void* addr;
+};
+
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kNoAllocMaxDevices] = {};
+ScratchEntry g_scratch[kNoAllocMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
 
 ssv_status noalloc_scratch_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return SSV_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return SSV_ERR_CUDA;
+  if (dev >= kNoAllocMaxDevices) return SSV_ERR_INVALID;
+  CUcontext ctx = nullptr;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS) return SSV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& e = g_scratch[dev];
+  if (!ctx || !e.addr || e.ctx != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return SSV_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    // with no context current, the lookup above made the device's primary one current
+    if (!ctx && (get(&ctx) != CUDA_SUCCESS || !ctx)) return SSV_ERR_CUDA;
+    e.ctx = ctx;
+    e.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return SSV_OK;
 }
 

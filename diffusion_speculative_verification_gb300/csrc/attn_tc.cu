@@ -1223,6 +1223,14 @@ static cudaError_t launch_t(const AttnParams& p, const TcMaps& maps, const TcWor
   if (attr_err != cudaSuccess) return attr_err;
   const int in_smem = plan_in_smem<MT>(p) ? 1 : 0;
   const size_t smem = Cfg<MT>::SM_ALLOC + (in_smem ? plan_table_bytes(p) : 0);
+  // The merge of a split unit waits (bounded) on partials from other CTAs of
+  // the grid, so every CTA must be able to be resident at once: one per SM,
+  // checked here rather than discovered as a timeout.
+  int per_sm = 0;
+  const cudaError_t oe =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_tc_kernel<MT, OutT>, Cfg<MT>::kThreads, smem);
+  if (oe != cudaSuccess) return oe;
+  if ((long long)per_sm * sm_count() < grid) return cudaErrorCooperativeLaunchTooLarge;
   return launch_pdl(attn_tc_kernel<MT, OutT>, dim3(grid), dim3(Cfg<MT>::kThreads), smem, st, maps, p, w, G, in_smem);
 }
 

@@ -176,9 +176,11 @@ SSV_API ssv_status ssv_rope_copy(const ssv_rope_args* a, void* stream);
  *         rows of o are not written).
  * Scheduling: the bf16 path launches one CTA per SM; where a unit of work is
  * split across CTAs, the CTA holding its first key block waits (bounded, about
- * one second of SM clock) for the others' partial results.  Work on other
- * streams that keeps SMs busy for longer than that while this kernel runs can
- * therefore end the call with SSV_ERR_TIMEOUT (never a hang).
+ * one second of SM clock) for the others' partial results.  Before launching,
+ * the host checks that the kernel's resources let one CTA reside on every SM
+ * at once (else SSV_ERR_CUDA, nothing launched).  Work on other streams that
+ * keeps SMs busy for longer than that second while this kernel runs can
+ * still end the call with SSV_ERR_TIMEOUT (never a hang).
  * ---------------------------------------------------------------------- */
 typedef struct {
   const void* q;
@@ -309,9 +311,13 @@ SSV_API ssv_status ssv_verify_step(const ssv_rope_args* rope, const ssv_attn_arg
  *  - Calls nothing that allocates: no cudaMalloc/cudaFree, no allocating
  *    library routine.  It clears its arrival counters with a memset on
  *    `stream` at every call.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress with that device current) and caches it; make
- *    that first call before any stream capture.
+ *  - The first call in each CUDA context looks up the array's device
+ *    address (cudaGetSymbolAddress with that context current) and caches it
+ *    per device together with the context; a later call from another
+ *    context on that device (after cudaDeviceReset, or a context the caller
+ *    made current) looks it up again.  Make the first call in a context
+ *    before any stream capture.  Device ordinals of 64 and above are refused
+ *    with SSV_ERR_INVALID.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that overlap on the GPU (different streams or host threads)
  *    race and must be serialised by the caller.

@@ -6,8 +6,9 @@ takes no workspace and uses the library's fixed 4 MiB per-device scratch
 array instead.  These tests call it through the C ABI and check that, on
 two calls in a row, it returns exactly what ssv_accept (caller workspace)
 returns on the same inputs -- the acceptance tests' tolerance, which is
-bit-exact for lengths and tokens -- and that a call too large for the
-array is refused before anything is launched.
+bit-exact for lengths and tokens -- that a call after one that timed out
+(leaving arrival counters non-zero in the shared array) is again exact, and
+that a call too large for the array is refused before anything is launched.
 
 Kept in a file of its own that sorts last, so a run that stops at the
 first failure has executed every other test before this one.
@@ -78,6 +79,30 @@ def test_noalloc_matches_workspace_path_two_calls_in_a_row():
         for w, f, s in zip(want, first, second):
             np.testing.assert_array_equal(f, w, err_msg=name)
             np.testing.assert_array_equal(s, w, err_msg=name)
+
+
+def test_noalloc_recovers_from_counters_left_non_zero():
+    """A call whose reduce times out (a left-out copy, ssv_set_fault_injection)
+    leaves arrival counters non-zero in the shared array; the next call clears
+    them itself and again returns what the workspace path returns."""
+    ensure_built()
+    x = W.make_accept_inputs("c", W.MODE_ARGMAX, 0.0, 65536, [8] * 6, [8, 8, 5, 8, 3, 8], seed=73)
+    d = sio.accept_to_device(x)
+    want = _run_workspace_path(d, x)
+    out = _outputs(x)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = _args(d, x, out, status)
+    stream = torch.cuda.current_stream().cuda_stream
+    try:
+        ssv.set_fault_injection(ssv.FAULT_ACCEPT, 0, 200_000)
+        assert ssv.lib().ssv_accept_noalloc(C.byref(a), stream) == ssv.SSV_OK
+        assert ssv.get_status(status) == ssv.SSV_ERR_TIMEOUT
+    finally:
+        ssv.set_fault_injection(None)
+    for _ in range(2):
+        got = _run_noalloc(d, x)
+        for w, g in zip(want, got):
+            np.testing.assert_array_equal(g, w)
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch():
