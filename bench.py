@@ -74,7 +74,7 @@ def accept_bytes(x) -> float:
         if x.mode == W.MODE_REJECT:
             tot += int(g) * x.V * les
         if x.mode == W.MODE_GUMBEL and x.T != 0.0:
-            tot += need * x.V * 4
+            tot += need * x.V * 4      # noise rows read (generated noise reads nothing more)
     return tot
 
 
@@ -372,6 +372,14 @@ class ConfigRun:
                                          acc["draft_logits"], acc["noise"], acc["noise_row"], acc["u_accept"],
                                          acc["u_sample"], acc["max_block"], self.status)
             self.ws_acc = torch.zeros(ssv.accept_workspace_bytes(self.cargs), dtype=torch.uint8, device=dev)
+        self.gargs = None
+        if acc is not None and x.mode == W.MODE_GUMBEL and x.T != 0.0:
+            # the same acceptance with the coupled noise generated on the device
+            # (each slot's position = its table row index; a fixed generator key)
+            self.gargs = ssv.accept_args(W.MODE_GUMBEL_GEN, acc["T"], acc["logits"], acc["draft_tokens"], acc["tau"],
+                                         acc["block"], acc["gamma"], acc["slot_off"], *self.outs, None, None,
+                                         acc["noise_row"], None, None, acc["max_block"], self.status,
+                                         noise_seed=0x5EED5EED5EED)
         self.margs = None
         if with_commit:
             # commit step (timed on its own, not part of the step): the rotated
@@ -406,6 +414,13 @@ class ConfigRun:
             r = ssv.lib().ssv_accept(C.byref(self.cargs), self.ws_acc.data_ptr(), self.ws_acc.numel(), s.cuda_stream)
             if r:
                 raise ssv.SsvError(r, "ssv_accept")
+
+    def op_accept_gen(self, s):
+        import ctypes as C
+        from diffusion_speculative_verification_gb300 import ssv
+        r = ssv.lib().ssv_accept(C.byref(self.gargs), self.ws_acc.data_ptr(), self.ws_acc.numel(), s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_accept (generated noise)")
 
     def op_commit(self, s):
         import ctypes as C
@@ -600,6 +615,9 @@ def run_ours(args):
                   "verify_attn": tm.capture((run.op_attn,)), "commit": tm.capture((run.op_commit,))}
         if run.acc is not None:
             graphs["accept"] = tm.capture((run.op_accept,))
+        if run.gargs is not None:
+            run.op_accept_gen(stream)
+            graphs["accept_gen"] = tm.capture((run.op_accept_gen,))
         torch.cuda.synchronize()
         for g in graphs.values():  # first replay uploads the graph
             g.replay()
@@ -623,6 +641,7 @@ def run_ours(args):
                           for k in ("rope", "verify_attn", "accept")])
         step_total = t_step - t_flush
         commit_ms = (tm.replay_ms(graphs["commit"]) - t_flush) / args.steps
+        gen_ms = (tm.replay_ms(graphs["accept_gen"]) - t_flush) / args.steps if "accept_gen" in graphs else None
     else:
         events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
         for i in range(args.steps):
@@ -641,6 +660,7 @@ def run_ours(args):
             ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
         commit_ms = float(np.mean([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]))
+        gen_ms = None
     if world > 1:
         dist.barrier()
     clk = clocks.window(t0, t1) if rank == 0 else None
@@ -685,6 +705,13 @@ def run_ours(args):
                        "traffic": measured_traffic("commit", args.config),
                        "note": "timed alone, not in the step; accepted counts seeded uniform on 0..B"},
             "lmhead_accept": lmh,
+            "accept_noise_generated": None if gen_ms is None else {
+                "us": round(gen_ms * 1e3, 2), "table_us": round(op_ms[2] * 1e3, 2),
+                "speedup_vs_table": round(op_ms[2] / gen_ms, 3),
+                "gbs": round(accept_bytes(run.x) / 2 / (gen_ms * 1e-3) / 1e9, 1),
+                "bytes": accept_bytes(run.x) / 2,
+                "note": "same acceptance, coupled noise generated on the device (Philox4x32-10 + fixed fp32 "
+                        "transform) instead of read from the table; bytes = logits rows only; timed alone"},
             "seq_per_s": round(world * a.batch / (ms_step * 1e-3), 1),
             "roofline": roof,
             "gpu_launches": kernel_launches(x) * args.steps,

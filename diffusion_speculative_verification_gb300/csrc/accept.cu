@@ -161,6 +161,21 @@ accept_reduce_kernel(const AcceptParams p) {
   if (!s_ok) return;
 
   AccPartial out;
+  if (MODE == SSV_ACCEPT_GUMBEL_GEN) {
+    // every entry's noise generated here: entries (it, 0..3) are 4 consecutive
+    // tokens, one generator call
+    const bool unit_t = p.T == 1.0f;
+    const uint32_t pos = (uint32_t)p.noise_row[slot];
+#pragma unroll
+    for (int it = 0; it < kAccIters; ++it) {
+      const int e = chunk_index(c0, it * kAccVec);
+      const uint4 w = noise::philox4x32_10(make_uint4((uint32_t)e >> 2, pos, 0u, 0u), (uint32_t)p.noise_seed,
+                                           (uint32_t)(p.noise_seed >> 32));
+      const uint32_t wq[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int k = 0; k < kAccVec; ++k) xa[it * kAccVec + k] = gen_score(xa[it * kAccVec + k], wq[k], p.T, unit_t);
+    }
+  }
   if (MODE != SSV_ACCEPT_REJECT) {
     if (MODE == SSV_ACCEPT_GUMBEL) {
       const bool unit_t = p.T == 1.0f;  // l / 1 is exact
@@ -549,6 +564,10 @@ static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaS
       case SSV_ACCEPT_GUMBEL:
         e = bf ? launch_reduce_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_GUMBEL, float>(p, st);
         break;
+      case SSV_ACCEPT_GUMBEL_GEN:
+        e = bf ? launch_reduce_t<SSV_ACCEPT_GUMBEL_GEN, __nv_bfloat16>(p, st)
+               : launch_reduce_t<SSV_ACCEPT_GUMBEL_GEN, float>(p, st);
+        break;
       default:
         e = bf ? launch_reduce_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_REJECT, float>(p, st);
         break;
@@ -573,7 +592,8 @@ using namespace ssv;
 
 static ssv_status accept_check(const ssv_accept_args* a, int* nchunks) {
   if (!a) return SSV_ERR_INVALID;
-  if (a->mode != SSV_ACCEPT_ARGMAX && a->mode != SSV_ACCEPT_GUMBEL && a->mode != SSV_ACCEPT_REJECT)
+  if (a->mode != SSV_ACCEPT_ARGMAX && a->mode != SSV_ACCEPT_GUMBEL && a->mode != SSV_ACCEPT_REJECT &&
+      a->mode != SSV_ACCEPT_GUMBEL_GEN)
     return SSV_ERR_INVALID;
   if (!isfinite(a->T) || a->T < 0.f) return SSV_ERR_NOT_FINITE;
   if (a->V < 1 || a->batch < 0 || a->total_slots < 0) return SSV_ERR_INVALID;
@@ -591,6 +611,7 @@ static ssv_status accept_check(const ssv_accept_args* a, int* nchunks) {
   if (a->mode == SSV_ACCEPT_GUMBEL && a->T > 0.f) {
     if (!a->noise || !a->noise_row || a->n_noise_rows < 1) return SSV_ERR_INVALID;
   }
+  if (a->mode == SSV_ACCEPT_GUMBEL_GEN && a->T > 0.f && !a->noise_row) return SSV_ERR_INVALID;
   return SSV_OK;
 }
 
@@ -648,8 +669,10 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   const FaultSetting f = fault_for(SSV_FAULT_ACCEPT);
   p.wait_budget = f.budget;
   p.fault_skip = f.skip;
+  p.noise_seed = a->noise_seed;
   int mode = a->mode;
-  if (mode == SSV_ACCEPT_GUMBEL && a->T == 0.f) mode = SSV_ACCEPT_ARGMAX;  // T = 0 ignores the noise
+  if ((mode == SSV_ACCEPT_GUMBEL || mode == SSV_ACCEPT_GUMBEL_GEN) && a->T == 0.f)
+    mode = SSV_ACCEPT_ARGMAX;  // T = 0 ignores the noise
   p.mode = mode;
   return mode;
 }

@@ -20,6 +20,7 @@
 #pragma once
 
 #include "ssv_internal.cuh"
+#include "noisegen.cuh"
 
 #include <limits.h>
 #include <math.h>
@@ -98,6 +99,7 @@ struct AcceptParams {
   // (test support, ssv_set_fault_injection)
   long long wait_budget;
   int fault_skip;
+  uint64_t noise_seed;  // SSV_ACCEPT_GUMBEL_GEN: key of the noise generator
 };
 
 constexpr int kEmitSub = 2048;  // vocabulary entries per emission CTA (256 threads x 8)
@@ -183,6 +185,12 @@ __device__ __forceinline__ bool warp_seq_valid(const AcceptParams& p, int b) {
   bool ok = B >= 1 && B <= 64 && g >= 0 && g <= B && p.slot_off[b] + B <= p.total_slots;
   if (ok) ok = warp_tau_is_permutation(p.tau + p.slot_off[b], B);
   return ok;
+}
+
+// Coupled-noise score fl32(fl32(l / T) + G) with G generated from the word x
+// (T == 1: l / 1 is exact and skipped).
+__device__ __forceinline__ float gen_score(float l, uint32_t x, float T, bool unit_t) {
+  return __fadd_rn(unit_t ? l : __fdiv_rn(l, T), noise::gumbel_from_bits(x));
 }
 
 // ---- completion steps (one warp, all 32 lanes) ------------------------------

@@ -4,7 +4,8 @@
 // in every CTA), then takes a contiguous range of the list's (row, chunk)
 // units; a unit is kAccChunk vocabulary entries of the target logits row
 // plus, where the rule needs one, the same entries of the draft logits
-// (rejection sampling, tested stages) or of the noise row (coupled noise).
+// (rejection sampling, tested stages) or of the noise row (coupled noise
+// from a table; generated noise needs the logits alone).
 // Warp roles:
 //   warps 0..15  consumers: wait for a stage of the ring, reduce it with
 //                warp shuffles (chunk max and compensated sums of
@@ -46,7 +47,8 @@ template <int MODE, typename T>
 struct StrCfg {
   using TB = typename std::conditional<MODE == SSV_ACCEPT_GUMBEL, float, T>::type;  // second stream
   static constexpr uint32_t kRowB = kAccChunk * sizeof(T);                           // offset of the second row
-  static constexpr uint32_t kStage = kAccChunk * (sizeof(T) + (MODE == SSV_ACCEPT_ARGMAX ? 0 : sizeof(TB)));
+  static constexpr bool kOneRow = MODE == SSV_ACCEPT_ARGMAX || MODE == SSV_ACCEPT_GUMBEL_GEN;  // logits only
+  static constexpr uint32_t kStage = kAccChunk * (sizeof(T) + (kOneRow ? 0 : sizeof(TB)));
   static constexpr int kStages = (kStrRingBytes / kStage) < kStrMaxStages ? (kStrRingBytes / kStage) : kStrMaxStages;
   static constexpr int kSmem = kStages * kStage;
   static_assert(kStages >= 2, "ring depth");
@@ -333,6 +335,62 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
           r.sb_hi = r.sb_lo = 0.f;
         }
         r.val = 0.f; r.idx = 0;
+      } else if (MODE == SSV_ACCEPT_GUMBEL_GEN) {
+        // Coupled noise generated here.  Every entry gets its generator word
+        // and a cheap upper bound of its score (noise::gumbel_upper); the entry
+        // with the largest bound in the warp is scored exactly, and only entries
+        // whose bound reaches that score can beat it, so only those are scored
+        // exactly (about 0.2% of entries): the warp's result is the exact first
+        // argmax of the exact scores.
+        const uint32_t pos = (uint32_t)p.noise_row[sh.list[u / p.nchunks] & 0x7fffffff];
+        const uint32_t key0 = (uint32_t)p.noise_seed, key1 = (uint32_t)(p.noise_seed >> 32);
+        const float inv_t = 1.f / p.T;
+        float xv[4 * kStrGroups], ub[4 * kStrGroups];
+        uint32_t wv[4 * kStrGroups];
+        float umax = -INFINITY, xsel = 0.f;  // this lane's largest bound, and its entry's logit and word
+        uint32_t wsel = 0u;
+#pragma unroll
+        for (int j = 0; j < kStrGroups; ++j) {
+          const int el = 4 * (j * kStrConsumers + tid);
+          if (el < nvalid) {
+            lds4<T>(ra, el, xv + 4 * j);
+            const uint4 w = noise::philox4x32_10(make_uint4((uint32_t)(c0 + el) >> 2, pos, 0u, 0u), key0, key1);
+            wv[4 * j] = w.x; wv[4 * j + 1] = w.y; wv[4 * j + 2] = w.z; wv[4 * j + 3] = w.w;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int jj = 4 * j + q;
+              const float sa = unit_t ? xv[jj] : xv[jj] * inv_t;
+              ub[jj] = (el + q < nvalid) ? __fmaf_rn(fabsf(sa), 1e-6f, sa + noise::gumbel_upper(wv[jj])) : -INFINITY;
+              const bool up = ub[jj] > umax;
+              umax = up ? ub[jj] : umax;
+              xsel = up ? xv[jj] : xsel;
+              wsel = up ? wv[jj] : wsel;
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) { ub[4 * j + q] = -INFINITY; xv[4 * j + q] = 0.f; wv[4 * j + q] = 0u; }
+          }
+        }
+        // the warp's largest bound: its entry, scored exactly, bounds the warp's best from below
+        const float wmax = warp_max(umax);
+        const unsigned who = __ballot_sync(0xffffffffu, umax > -INFINITY && umax == wmax);
+        const int src = who ? __ffs(who) - 1 : 0;
+        float lb = -INFINITY;
+        if (lane == src && who) lb = gen_score(xsel, wsel, p.T, unit_t);
+        lb = __shfl_sync(0xffffffffu, lb, src);
+        float best = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int jj = 0; jj < 4 * kStrGroups; ++jj) {
+          if (ub[jj] > -INFINITY && ub[jj] >= lb) {  // a token that can reach the warp's best: score it exactly
+            const float sc = gen_score(xv[jj], wv[jj], p.T, unit_t);
+            const int idx = c0 + 4 * ((jj >> 2) * kStrConsumers + tid) + (jj & 3);
+            if (sc > best || bi == INT_MAX) { best = sc; bi = idx; }
+          }
+        }
+        warp_argmax(best, bi);
+        r.val = best; r.idx = bi;
+        r.m_a = r.m_b = r.sa_hi = r.sa_lo = r.sb_hi = r.sb_lo = 0.f;
       } else {
         float best = -INFINITY;
         int bi = INT_MAX;
@@ -462,6 +520,9 @@ cudaError_t launch_accept_stream(const AcceptParams& p, int mode, bool bf16, cud
       return bf16 ? launch_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_ARGMAX, float>(p, st);
     case SSV_ACCEPT_GUMBEL:
       return bf16 ? launch_t<SSV_ACCEPT_GUMBEL, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_GUMBEL, float>(p, st);
+    case SSV_ACCEPT_GUMBEL_GEN:
+      return bf16 ? launch_t<SSV_ACCEPT_GUMBEL_GEN, __nv_bfloat16>(p, st)
+                  : launch_t<SSV_ACCEPT_GUMBEL_GEN, float>(p, st);
     default:
       return bf16 ? launch_t<SSV_ACCEPT_REJECT, __nv_bfloat16>(p, st) : launch_t<SSV_ACCEPT_REJECT, float>(p, st);
   }

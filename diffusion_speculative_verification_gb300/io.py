@@ -68,6 +68,7 @@ def accept_to_device(x: W.AcceptInputs, device="cuda") -> dict:
         u_accept=f32_tensor(x.u_accept, device),
         u_sample=f32_tensor(x.u_sample, device),
         max_block=int(np.max(x.blocks)) if len(x.blocks) else 1,
+        noise_seed=int(getattr(x, "noise_seed", 0)),
     )
     d["draft_logits"] = None if x.draft_logits is None else tensor(x.draft_logits, x.logits_dtype, device)
     d["noise"] = None if x.noise is None else f32_tensor(x.noise, device)

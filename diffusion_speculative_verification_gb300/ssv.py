@@ -19,7 +19,7 @@ from .build import LIB
 SSV_OK, SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_CUDA = 0, 1, 2, 3
 SSV_ERR_TIMEOUT, SSV_ERR_BAD_TAU, SSV_ERR_WORKSPACE, SSV_ERR_NOT_FINITE = 4, 5, 6, 7
 SSV_F32, SSV_BF16 = 0, 1
-ARGMAX, GUMBEL, REJECT = 0, 1, 2
+ARGMAX, GUMBEL, REJECT, GUMBEL_GEN = 0, 1, 2, 3
 
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
@@ -62,7 +62,8 @@ class AcceptArgs(C.Structure):
                 ("tau", C.c_void_p), ("block", C.c_void_p), ("gamma", C.c_void_p), ("slot_off", C.c_void_p),
                 ("noise", C.c_void_p), ("n_noise_rows", C.c_int32), ("noise_row", C.c_void_p),
                 ("u_accept", C.c_void_p), ("u_sample", C.c_void_p), ("n_acc", C.c_void_p),
-                ("n_out", C.c_void_p), ("tokens", C.c_void_p), ("dev_status", C.c_void_p)]
+                ("n_out", C.c_void_p), ("tokens", C.c_void_p), ("dev_status", C.c_void_p),
+                ("noise_seed", C.c_uint64)]
 
 
 class CommitArgs(C.Structure):
@@ -253,12 +254,12 @@ def verify_attn(q, k_cache, v_cache, k_new, v_new, batch: Batch, tau, out=None, 
 
 def accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
                 draft_logits=None, noise=None, noise_row=None, u_accept=None, u_sample=None, max_block=64,
-                dev_status=None):
+                dev_status=None, noise_seed=0):
     return AcceptArgs(int(mode), float(T), logits.shape[1], block.shape[0], draft_tokens.shape[0], int(max_block),
                       _dtype_code(logits), _ptr(logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(tau),
                       _ptr(block), _ptr(gamma), _ptr(slot_off), _ptr(noise),
                       0 if noise is None else noise.shape[0], _ptr(noise_row), _ptr(u_accept), _ptr(u_sample),
-                      _ptr(n_acc), _ptr(n_out), _ptr(tokens), _ptr(dev_status))
+                      _ptr(n_acc), _ptr(n_out), _ptr(tokens), _ptr(dev_status), int(noise_seed))
 
 
 def accept_workspace_bytes(args: AcceptArgs) -> int:
@@ -269,7 +270,7 @@ def accept_workspace_bytes(args: AcceptArgs) -> int:
 
 def accept(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_logits=None, noise=None,
            noise_row=None, u_accept=None, u_sample=None, max_block=64, workspace=None, dev_status=None,
-           stream=None, out=None):
+           stream=None, out=None, noise_seed=0):
     """Acceptance; returns (n_acc [batch], n_out [batch], tokens [slots]) int32 device tensors."""
     torch = _torch()
     dev = logits.device
@@ -279,7 +280,7 @@ def accept(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_log
                torch.empty(draft_tokens.shape[0], dtype=torch.int32, device=dev))
     n_acc, n_out, tokens = out
     a = accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
-                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status)
+                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status, noise_seed)
     ws = _workspace(accept_workspace_bytes(a), dev, workspace)
     _check(lib().ssv_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
            "ssv_accept")
@@ -288,7 +289,7 @@ def accept(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_log
 
 def accept_noalloc(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, draft_logits=None, noise=None,
                    noise_row=None, u_accept=None, u_sample=None, max_block=64, dev_status=None, stream=None,
-                   out=None):
+                   out=None, noise_seed=0):
     """ssv_accept without a workspace: scratch comes from the library's fixed
     per-device array (for callers that cannot allocate).  Output tensors may
     be passed in ``out``; otherwise they are allocated here by torch."""
@@ -300,7 +301,7 @@ def accept_noalloc(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, d
                torch.empty(draft_tokens.shape[0], dtype=torch.int32, device=dev))
     n_acc, n_out, tokens = out
     a = accept_args(mode, T, logits, draft_tokens, tau, block, gamma, slot_off, n_acc, n_out, tokens,
-                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status)
+                    draft_logits, noise, noise_row, u_accept, u_sample, max_block, dev_status, noise_seed)
     _check(lib().ssv_accept_noalloc(C.byref(a), _stream_ptr(stream)), "ssv_accept_noalloc")
     return n_acc, n_out, tokens
 

@@ -43,7 +43,8 @@ BF16 = "bf16"
 MODE_ARGMAX = 0
 MODE_GUMBEL = 1
 MODE_REJECT = 2
-MODE_NAMES = {"argmax": MODE_ARGMAX, "gumbel": MODE_GUMBEL, "reject": MODE_REJECT}
+MODE_GUMBEL_GEN = 3
+MODE_NAMES = {"argmax": MODE_ARGMAX, "gumbel": MODE_GUMBEL, "reject": MODE_REJECT, "gumbel_gen": MODE_GUMBEL_GEN}
 
 #: Per-sequence record, same field order as ``ssv_seq`` in include/ssv.h.
 SEQ_FIELDS = ("cache_len", "new_len", "block", "q_off", "kv_off", "tau_off")
@@ -213,6 +214,7 @@ class AcceptInputs:
     noise_row: np.ndarray     # int32 [sum B], table row per slot
     u_accept: np.ndarray      # fp32 [sum B], uniforms for the accept tests
     u_sample: np.ndarray      # fp32 [batch], uniform for the emitted sample
+    noise_seed: int = 0       # generated coupled noise: key of the generator (noise_row holds positions)
 
     @property
     def batch(self) -> int:
@@ -291,13 +293,18 @@ def make_accept_inputs(name: str, mode: int, T: float, V: int, blocks, gammas, s
     draft = None if draft32 is None else _store(draft32, logits_dtype)
     noise = None
     noise_row = np.zeros(S, np.int32)
+    noise_seed = 0
     if mode == MODE_GUMBEL:
         noise_row = rng.permutation(S).astype(np.int32)
         noise = gumbel_table(rng, S, V)
+    elif mode == MODE_GUMBEL_GEN:
+        # one position per slot (distinct, any 32-bit pattern), one generator key
+        noise_row = (int(rng.integers(0, 1 << 30)) + rng.permutation(S)).astype(np.int32)
+        noise_seed = int(rng.integers(0, 1 << 63))
     u_accept = uniform01_f32(rng, S)
     u_sample = uniform01_f32(rng, batch)
     return AcceptInputs(name, mode, float(T), V, logits_dtype, blocks, gammas, slot_off, tau,
-                        logits, draft, draft_tokens, noise, noise_row, u_accept, u_sample)
+                        logits, draft, draft_tokens, noise, noise_row, u_accept, u_sample, noise_seed)
 
 
 # --------------------------------------------------------------------------

@@ -66,7 +66,9 @@ typedef enum { SSV_F32 = 0, SSV_BF16 = 1 } ssv_dtype;
 typedef enum {
   SSV_ACCEPT_ARGMAX = 0,    /* T = 0 state equality: accept iff draft == argmax(l) */
   SSV_ACCEPT_GUMBEL = 1,    /* coupled noise: accept iff draft == argmax(fl(l/T) + G[row]) */
-  SSV_ACCEPT_REJECT = 2     /* standard rejection sampling, accept iff u < p(d)/q(d) */
+  SSV_ACCEPT_REJECT = 2,    /* standard rejection sampling, accept iff u < p(d)/q(d) */
+  SSV_ACCEPT_GUMBEL_GEN = 3 /* coupled noise generated on the device: accept iff
+                               draft == argmax(fl(l/T) + G(noise_seed, noise_row[k], v)) */
 } ssv_accept_mode;
 
 /*
@@ -219,6 +221,17 @@ SSV_API ssv_status ssv_verify_attn(const ssv_attn_args* a, void* workspace, size
  *   GUMBEL : draft_tokens[k] == argmax_v fl32(fl32(l_k[v]/T) + noise[noise_row[k]][v])
  *            (IEEE fp32, no contraction; T = 0 means ARGMAX)
  *   REJECT : u_accept[k] < p(d)/q(d), p = softmax(l_k/T), q = softmax(draft_logits_k/T)
+ *   GUMBEL_GEN : as GUMBEL with the table value replaced by one generated on
+ *            the device, G(seed, pos, v) = -L(-L(U)), U = (floor(x / 2^9) + 1/2)
+ *            2^-23, x = word (v mod 4) of Philox4x32-10 at counter
+ *            (floor(v / 4), pos, 0, 0) under key (low, high word of noise_seed),
+ *            pos = noise_row[k] (any 32-bit value the caller assigns to the
+ *            slot's absolute output position; drafter and target use the same),
+ *            L the natural logarithm by one fixed sequence of fp32 operations:
+ *            reduction to m in [sqrt(1/2), sqrt 2], s = (m - 1) / (m + 1),
+ *            ln m = 2 s + s z (2/3 + z (2/5 + z (2/7 + z 2/9))), z = s^2
+ *            (Horner from the inside, every operation rounded to nearest), plus
+ *            e ln 2.  Nothing but the logits is read; T = 0 means ARGMAX.
  * n_acc = leading accepted stages.  If c = n_acc + 1 <= B one target token
  * is emitted at stage c: the ARGMAX/GUMBEL decision; for REJECT a sample of
  * (p - q)_+ if c <= gamma, else of p, by inverse CDF with u_sample[b]
@@ -232,6 +245,7 @@ SSV_API ssv_status ssv_verify_attn(const ssv_attn_args* a, void* workspace, size
  *              sequences in increasing slot order without overlap
  *              (slot_off[b] + block[b] <= slot_off[b+1])
  * noise [n_noise_rows, V] fp32 device (GUMBEL with T > 0 only)
+ * noise_seed: GUMBEL_GEN only (noise_row then holds positions, not rows)
  * Outputs: n_acc[batch], n_out[batch] (= n_acc + 1 if a token is emitted),
  *          tokens[total_slots]: per sequence, the accepted drafts in stage
  *          order then the emitted token, rest -1.
@@ -263,6 +277,7 @@ typedef struct {
   int32_t* n_out;
   int32_t* tokens;
   int32_t* dev_status;         /* device, may be NULL */
+  uint64_t noise_seed;         /* GUMBEL_GEN: key of the noise generator */
 } ssv_accept_args;
 
 SSV_API ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* bytes);

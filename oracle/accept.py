@@ -25,6 +25,9 @@ Decisions (readings where the pages are silent are marked):
            one exact value per candidate); T = 0 ignores G.  Accept iff
            d_k == t_k.  row_k is the table row the caller assigns to the
            slot's absolute output position.
+  GUMBEL_GEN  as GUMBEL with G generated, not read (oracle.noise: Philox4x32-10
+           at the slot's 32-bit position noise_row[k] and the call's seed,
+           then -L(-L(U)) in fixed fp32 operations; a reading).
   REJECT   p = softmax(l_k / T), q = softmax(ql_k / T) (draft logits), in fp64.
            Accept iff u_k < p(d_k) / q(d_k)  (probability min(1, p/q)).
 n_acc = number of leading accepted stages.  Then one target token is emitted
@@ -45,6 +48,7 @@ import numpy as np
 MODE_ARGMAX = 0
 MODE_GUMBEL = 1
 MODE_REJECT = 2
+MODE_GUMBEL_GEN = 3   # GUMBEL with the noise generated (oracle.noise) instead of read from a table
 
 
 def stage_slots(tau) -> np.ndarray:
@@ -170,10 +174,17 @@ def accept_batch(inp) -> dict:
         B, g, off = int(inp.blocks[b]), int(inp.gammas[b]), int(inp.slot_off[b])
         sl = slice(off, off + B)
         noise_rows = None
-        if inp.mode == MODE_GUMBEL and inp.T != 0.0:
+        mode = inp.mode
+        if mode == MODE_GUMBEL and inp.T != 0.0:
             noise_rows = [inp.noise[int(inp.noise_row[off + k])] for k in range(B)]
+        elif mode == MODE_GUMBEL_GEN:
+            # each slot's noise generated at its position (the 32-bit pattern of noise_row)
+            from oracle.noise import gumbel_rows
+            pos = np.asarray(inp.noise_row[sl], np.int32).view(np.uint32)
+            noise_rows = list(gumbel_rows(int(inp.noise_seed), pos, inp.V)) if inp.T != 0.0 else None
+            mode = MODE_GUMBEL
         draft_rows = None if draft_values is None else draft_values[sl]
-        r = accept_sequence(inp.mode, inp.T, inp.tau[sl], g, inp.draft_tokens[sl], from_values[sl],
+        r = accept_sequence(mode, inp.T, inp.tau[sl], g, inp.draft_tokens[sl], from_values[sl],
                             draft_rows, noise_rows, inp.u_accept[sl], float(inp.u_sample[b]))
         n_acc[b] = r.n_acc
         n_out[b] = r.n_out

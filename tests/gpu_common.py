@@ -75,7 +75,8 @@ def gpu_accept(x: W.AcceptInputs, dev_status=None, workspace=None):
     n_acc, n_out, tokens = ssv.accept(d["mode"], d["T"], d["logits"], d["draft_tokens"], d["tau"], d["block"],
                                       d["gamma"], d["slot_off"], draft_logits=d["draft_logits"], noise=d["noise"],
                                       noise_row=d["noise_row"], u_accept=d["u_accept"], u_sample=d["u_sample"],
-                                      max_block=d["max_block"], dev_status=dev_status, workspace=workspace)
+                                      max_block=d["max_block"], dev_status=dev_status, workspace=workspace,
+                                      noise_seed=d["noise_seed"])
     return n_acc.cpu().numpy(), n_out.cpu().numpy(), tokens.cpu().numpy()
 
 

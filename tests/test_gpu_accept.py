@@ -113,7 +113,8 @@ def _accept_with_logits_offset(x: W.AcceptInputs, elem_offset: int, dev_status=N
     n_acc, n_out, tokens = ssv.accept(d["mode"], d["T"], shifted(d["logits"]), d["draft_tokens"], d["tau"],
                                       d["block"], d["gamma"], d["slot_off"], draft_logits=shifted(d["draft_logits"]),
                                       noise=d["noise"], noise_row=d["noise_row"], u_accept=d["u_accept"],
-                                      u_sample=d["u_sample"], max_block=d["max_block"], dev_status=dev_status)
+                                      u_sample=d["u_sample"], max_block=d["max_block"], dev_status=dev_status,
+                                      noise_seed=d["noise_seed"])
     return n_acc.cpu().numpy(), n_out.cpu().numpy(), tokens.cpu().numpy()
 
 

@@ -239,3 +239,24 @@ def test_sample_margin_rule():
     assert v == 2 and abs(A.sample_margin(res) - 0.05) < 1e-15
     v, t, cdf = A.inverse_cdf(w, 0.0)  # the first token of positive mass; t sits on its lower end
     assert v == 1 and A.sample_margin(A.SeqResult(0, [v], "bonus", 0, [], t, cdf)) == 0.0
+
+
+@pytest.mark.parametrize("T", [1.0, 1.5])
+def test_generated_noise_coupling(T):
+    """Generated coupled noise (SPOT review, "How it is used"): a drafter that
+    evaluates the same generator at the same positions, with the same model,
+    is always accepted; the batch oracle reads each slot's noise at its
+    position."""
+    from oracle.noise import gumbel_rows
+    inp = W.make_accept_inputs("gen", W.MODE_GUMBEL_GEN, T, 300, [6, 3], [6, 3], seed=21)
+    pos = inp.noise_row.view(np.uint32)
+    G = gumbel_rows(inp.noise_seed, pos, inp.V)
+    l = inp.logits.astype(np.float32)
+    inp.draft_tokens = np.array([int(np.argmax(A.gumbel_scores(l[k], G[k], T))) for k in range(len(pos))], np.int32)
+    out = A.accept_batch(inp)
+    assert out["n_acc"].tolist() == [6, 3] and out["n_out"].tolist() == [6, 3]
+    # one changed draft at the slot of stage 1 rejects everything from there
+    k0 = int(np.argmin(inp.tau[:6]))
+    inp.draft_tokens[k0] = (inp.draft_tokens[k0] + 1) % inp.V
+    out = A.accept_batch(inp)
+    assert out["n_acc"][0] == 0 and out["tokens"][0] == int(np.argmax(A.gumbel_scores(l[k0], G[k0], T)))
