@@ -679,6 +679,10 @@ def run_ours(args):
     if args.config in W.LMHEAD and not args.no_lmhead:
         lmh = run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak)
 
+    tree = None
+    if not args.no_tree and rank == 0:
+        tree = run_tree(args, dev, stream, l2_flush, hbm_peak)
+
     # ---- end to end: host inputs -> device, run, tokens back -------------------
     e2e = run_e2e(args, run, stream)
 
@@ -705,6 +709,7 @@ def run_ours(args):
                        "traffic": measured_traffic("commit", args.config),
                        "note": "timed alone, not in the step; accepted counts seeded uniform on 0..B"},
             "lmhead_accept": lmh,
+            "tree_verification": tree,
             "accept_noise_generated": None if gen_ms is None else {
                 "us": round(gen_ms * 1e3, 2), "table_us": round(op_ms[2] * 1e3, 2),
                 "speedup_vs_table": round(op_ms[2] / gen_ms, 3),
@@ -821,6 +826,99 @@ def run_lmhead(args, dev, stream, l2_flush, hbm_peak, tf_peak):
             "launch": "cuda_graph", "note": "timed alone, not in the step; logits never written"}
 
 
+def tree_work(t: W.TreeInputs, out_bytes: int):
+    """Useful work of the tree pass: (bytes, flops) of the attention -- KV cache
+    once per kv head, Q, new K/V and the defined output rows; 4 d flops per
+    (defined row, visible key, head) -- and the logits bytes the acceptance
+    reads (every (node, position) row)."""
+    import oracle.tree as otree  # counting only: the tree's per-node masks
+    es = 2 if t.dtype == W.BF16 else 4
+    flops = 0.0
+    out_rows = 0
+    for s in t.seqs:
+        C, N, B, E, q_off, k_off, kv_off, e_off, o_off = (int(x) for x in s)
+        committed, _ = otree.tree_nodes(B, t.parent[e_off:e_off + E], t.pos[e_off:e_off + E])
+        defined = sum(B - bin(c).count("1") for c in committed)
+        out_rows += N + defined
+        flops += (N * (N + 1) / 2 + N * C + defined * (C + N + B)) * t.Hq * 4.0 * t.d
+    nq = int(np.sum(t.seqs[:, 1] + t.seqs[:, 2]))
+    nk = int(np.sum(t.seqs[:, 1] + t.seqs[:, 3] + t.seqs[:, 2]))
+    nc = int(np.sum(t.seqs[:, 0]))
+    bytes_ = (nc * 2 + nk * 2) * t.Hkv * t.d * es + nq * t.Hq * t.d * es + out_rows * t.Hq * t.d * out_bytes
+    acc_bytes = float(t.total_out - int(np.sum(t.seqs[:, 1]))) * t.V * 4.0
+    return float(bytes_), float(flops), acc_bytes
+
+
+TREE_WORKLOAD = dict(cache=[4096] * 4, new=[0] * 4, blocks=[32] * 4, edges=[8] * 4, Hq=32, Hkv=8, d=128, seed=1006,
+                     V=W.VOCAB)
+
+
+def run_tree(args, dev, stream, l2_flush, hbm_peak):
+    """Tree (state-set) verification on a SPOT-like shape: block width 32, a
+    draft tree of 8 edges (budget D8), the 8B-class layer with a 4096-key
+    prompt cache; the attention pass over every (node, position) row, then the
+    acceptance by state equality over 151936-token logits (greedy).  Timed
+    alone after the same L2 flush, as CUDA-graph replays."""
+    import torch
+    from diffusion_speculative_verification_gb300 import ssv, io as sio
+    c = TREE_WORKLOAD
+    t = W.make_tree_inputs("tree", c["cache"], c["new"], c["blocks"], c["edges"], c["Hq"], c["Hkv"], c["d"], W.BF16,
+                           c["seed"], V=c["V"], mode=W.MODE_ARGMAX, T=0.0)
+    d = sio.tree_to_device(t, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.zeros((t.total_out, t.Hq, t.d), dtype=torch.bfloat16, device=dev)
+    aargs = ssv.tree_attn_args(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], o, d["seqs"], d["parent"],
+                               d["pos"], t.total_out, d["max_cache"], 0.0, status)
+    outs = [torch.empty(t.batch, dtype=torch.int32, device=dev), torch.empty((t.batch, 64), dtype=torch.int32, device=dev),
+            torch.empty(t.batch, dtype=torch.int32, device=dev), torch.empty(t.batch, dtype=torch.int32, device=dev)]
+    cargs = ssv.tree_accept_args(W.MODE_ARGMAX, 0.0, d["logits"], d["seqs"], d["parent"], d["pos"], d["token"], *outs,
+                                 dev_status=status)
+    import ctypes as C
+    L = ssv.lib()
+    n = C.c_size_t(0)
+    L.ssv_tree_accept_workspace(C.byref(cargs), C.byref(n))
+    ws = torch.zeros(max(256, int(n.value)), dtype=torch.uint8, device=dev)
+
+    def op_attn(s):
+        r = L.ssv_tree_verify_attn(C.byref(aargs), s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_tree_verify_attn")
+
+    def op_acc(s):
+        r = L.ssv_tree_accept(C.byref(cargs), ws.data_ptr(), ws.numel(), s.cuda_stream)
+        if r:
+            raise ssv.SsvError(r, "ssv_tree_accept")
+
+    for _ in range(3):
+        l2_flush()
+        op_attn(stream)
+        op_acc(stream)
+    torch.cuda.synchronize()
+    assert ssv.get_status(status) == ssv.SSV_OK
+    K = max(1, min(args.steps, 20))
+    tm = Timer(dev, stream, K, l2_flush)
+    ga, gc = tm.capture((op_attn,)), tm.capture((op_acc,))
+    ga.replay(); gc.replay()
+    torch.cuda.synchronize()
+    t_flush = tm.flush_ms()
+    t_a = (tm.replay_ms(ga) - t_flush) / K
+    t_c = (tm.replay_ms(gc) - t_flush) / K
+    assert ssv.get_status(status) == ssv.SSV_OK
+    ab, af, cb = tree_work(t, 2)
+    res = {"workload": "batch 4, 32 q / 8 kv heads, d 128, bf16, prompt cache 4096, block 32, 8-edge draft tree, "
+                       "V 151936 greedy",
+           "edges": c["edges"], "output_rows": t.total_out,
+           "attn_us": round(t_a * 1e3, 2), "attn_gbs": round(ab / (t_a * 1e-3) / 1e9, 1),
+           "attn_tflops": round(af / (t_a * 1e-3) / 1e12, 2), "attn_bytes": ab, "attn_flops": af,
+           "attn_frac_hbm": round(ab / (t_a * 1e-3) / 1e9 / hbm_peak, 4),
+           "accept_us": round(t_c * 1e3, 2), "accept_gbs": round(cb / (t_c * 1e-3) / 1e9, 1), "accept_bytes": cb,
+           "accept_frac_hbm": round(cb / (t_c * 1e-3) / 1e9 / hbm_peak, 4),
+           "n_acc": outs[0].cpu().tolist(), "launch": "cuda_graph", "note": "timed alone, not in the step"}
+    del d, o, ws, ga, gc
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_e2e(args, run: ConfigRun, stream):
     """Same calls, inputs copied from pinned host memory every step, results read back."""
     import torch
@@ -877,6 +975,7 @@ def main():
                          "with its own roofline ('' for none)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-lmhead", action="store_true", help="skip the fused LM head + acceptance measurement")
+    ap.add_argument("--no-tree", action="store_true", help="skip the tree verification measurement")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps one call at a time")
     args = ap.parse_args()
     if args.warmup < 3:

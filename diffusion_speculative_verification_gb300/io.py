@@ -92,3 +92,26 @@ def lmhead_to_device(x: W.LmheadInputs, device="cuda", w=None) -> dict:
     )
     d["noise"] = None if a.noise is None else f32_tensor(a.noise, device)
     return d
+
+
+def tree_to_device(t: W.TreeInputs, device="cuda") -> dict:
+    """Device copies of a tree input set (attention inputs, and acceptance
+    inputs when they were drawn)."""
+    d = dict(
+        seqs=int_tensor(t.seqs, device),
+        parent=int_tensor(t.parent, device),
+        pos=int_tensor(t.pos, device),
+        token=int_tensor(t.token, device),
+        q=tensor(t.q, t.dtype, device),
+        k_new=tensor(t.k_new, t.dtype, device),
+        v_new=tensor(t.v_new, t.dtype, device),
+        k_cache=tensor(t.k_cache, t.dtype, device),
+        v_cache=tensor(t.v_cache, t.dtype, device),
+        total_out=t.total_out,
+        max_cache=int(t.seqs[:, 0].max()) if t.batch else 0,
+    )
+    d["logits"] = None if t.logits is None else f32_tensor(t.logits, device)
+    d["noise"] = None if t.noise is None else f32_tensor(t.noise, device)
+    d["noise_row"] = None if t.noise_row is None else int_tensor(t.noise_row, device)
+    d["pos_off"] = None if t.pos_off is None else int_tensor(t.pos_off, device)
+    return d

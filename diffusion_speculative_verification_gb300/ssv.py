@@ -24,7 +24,8 @@ ARGMAX, GUMBEL, REJECT, GUMBEL_GEN = 0, 1, 2, 3
 #: every symbol include/ssv.h declares
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
            "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_lmhead_accept_workspace", "ssv_lmhead_accept",
-           "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench", "ssv_set_fault_injection")
+           "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench", "ssv_set_fault_injection",
+           "ssv_tree_verify_attn", "ssv_tree_accept_workspace", "ssv_tree_accept")
 FAULT_NONE, FAULT_ATTN, FAULT_ACCEPT, FAULT_LMHEAD = 0, 1, 2, 3
 
 
@@ -74,6 +75,24 @@ class CommitArgs(C.Structure):
                 ("total_slots", C.c_int32), ("dst_rows", C.c_int32), ("dev_status", C.c_void_p)]
 
 
+class TreeAttnArgs(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("k_new", C.c_void_p),
+                ("v_new", C.c_void_p), ("o", C.c_void_p), ("in_dtype", C.c_int), ("out_dtype", C.c_int),
+                ("Hq", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32), ("scale", C.c_float), ("seqs", C.c_void_p),
+                ("batch", C.c_int32), ("parent", C.c_void_p), ("pos", C.c_void_p), ("total_q", C.c_int32),
+                ("total_k", C.c_int32), ("total_cache", C.c_int32), ("total_edges", C.c_int32),
+                ("total_out", C.c_int32), ("max_cache", C.c_int32), ("dev_status", C.c_void_p)]
+
+
+class TreeAcceptArgs(C.Structure):
+    _fields_ = [("mode", C.c_int), ("T", C.c_float), ("V", C.c_int32), ("seqs", C.c_void_p), ("batch", C.c_int32),
+                ("logits_dtype", C.c_int), ("logits", C.c_void_p), ("parent", C.c_void_p), ("pos", C.c_void_p),
+                ("token", C.c_void_p), ("total_edges", C.c_int32), ("total_out", C.c_int32),
+                ("noise", C.c_void_p), ("n_noise_rows", C.c_int32), ("noise_row", C.c_void_p),
+                ("pos_off", C.c_void_p), ("total_positions", C.c_int32), ("n_acc", C.c_void_p), ("path", C.c_void_p),
+                ("emit_pos", C.c_void_p), ("emit_tok", C.c_void_p), ("dev_status", C.c_void_p)]
+
+
 class FaultInjection(C.Structure):
     _fields_ = [("kernel", C.c_int), ("skip", C.c_int32), ("wait_budget_cycles", C.c_int64)]
 
@@ -114,9 +133,15 @@ def lib():
         L.ssv_status_string.restype = C.c_char_p
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
+        L.ssv_set_fault_injection.argtypes = [C.POINTER(FaultInjection)]
+        L.ssv_tree_verify_attn.argtypes = [C.POINTER(TreeAttnArgs), vp]
+        L.ssv_tree_accept_workspace.argtypes = [C.POINTER(TreeAcceptArgs), C.POINTER(sz)]
+        L.ssv_tree_accept.argtypes = [C.POINTER(TreeAcceptArgs), vp, sz, vp]
         for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step",
                      "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit",
-                     "ssv_lmhead_accept_workspace", "ssv_lmhead_accept", "ssv_get_status", "ssv_bench"):
+                     "ssv_lmhead_accept_workspace", "ssv_lmhead_accept", "ssv_get_status", "ssv_bench",
+                     "ssv_set_fault_injection", "ssv_tree_verify_attn", "ssv_tree_accept_workspace",
+                     "ssv_tree_accept"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -377,6 +402,60 @@ def set_fault_injection(kernel=None, skip: int = -1, wait_budget_cycles: int = 1
         return
     f = FaultInjection(int(kernel), int(skip), int(wait_budget_cycles))
     _check(lib().ssv_set_fault_injection(C.byref(f)), "ssv_set_fault_injection")
+
+
+def tree_attn_args(q, k_cache, v_cache, k_new, v_new, out, seqs, parent, pos, total_out, max_cache,
+                   scale: float = 0.0, dev_status=None):
+    """seqs: int32 [batch, 9] device tensor of ssv_tree_seq records."""
+    return TreeAttnArgs(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(out), _dtype_code(q),
+                        _dtype_code(out), q.shape[1], k_new.shape[1], q.shape[2], float(scale), _ptr(seqs),
+                        seqs.shape[0], _ptr(parent), _ptr(pos), q.shape[0], k_new.shape[0],
+                        0 if k_cache is None else k_cache.shape[0], 0 if parent is None else parent.shape[0],
+                        int(total_out), int(max_cache), _ptr(dev_status))
+
+
+def tree_verify_attn(q, k_cache, v_cache, k_new, v_new, seqs, parent, pos, total_out, max_cache, out=None,
+                     out_dtype=None, scale: float = 0.0, dev_status=None, stream=None):
+    """Attention of the tree pass; returns O [total_out, Hq, d] (rows of
+    committed positions are left as they were in `out`)."""
+    torch = _torch()
+    if out is None:
+        out = torch.zeros((int(total_out), q.shape[1], q.shape[2]), dtype=out_dtype or q.dtype, device=q.device)
+    a = tree_attn_args(q, k_cache, v_cache, k_new, v_new, out, seqs, parent, pos, total_out, max_cache, scale,
+                       dev_status)
+    _check(lib().ssv_tree_verify_attn(C.byref(a), _stream_ptr(stream)), "ssv_tree_verify_attn")
+    return out
+
+
+def tree_accept_args(mode, T, logits, seqs, parent, pos, token, n_acc, path, emit_pos, emit_tok, noise=None,
+                     noise_row=None, pos_off=None, dev_status=None):
+    return TreeAcceptArgs(int(mode), float(T), logits.shape[1], _ptr(seqs), seqs.shape[0], _dtype_code(logits),
+                          _ptr(logits), _ptr(parent), _ptr(pos), _ptr(token),
+                          0 if parent is None else parent.shape[0], logits.shape[0], _ptr(noise),
+                          0 if noise is None else noise.shape[0], _ptr(noise_row), _ptr(pos_off),
+                          0 if noise_row is None else noise_row.shape[0], _ptr(n_acc), _ptr(path), _ptr(emit_pos),
+                          _ptr(emit_tok), _ptr(dev_status))
+
+
+def tree_accept(mode, T, logits, seqs, parent, pos, token, noise=None, noise_row=None, pos_off=None, workspace=None,
+                dev_status=None, stream=None):
+    """Acceptance of the tree by state equality; returns (n_acc [batch],
+    path [batch, 64], emit_pos [batch], emit_tok [batch]) int32 device tensors."""
+    torch = _torch()
+    dev = logits.device
+    b = seqs.shape[0]
+    n_acc = torch.empty(b, dtype=torch.int32, device=dev)
+    path = torch.empty((b, 64), dtype=torch.int32, device=dev)
+    ep = torch.empty(b, dtype=torch.int32, device=dev)
+    et = torch.empty(b, dtype=torch.int32, device=dev)
+    a = tree_accept_args(mode, T, logits, seqs, parent, pos, token, n_acc, path, ep, et, noise, noise_row, pos_off,
+                         dev_status)
+    n = C.c_size_t(0)
+    _check(lib().ssv_tree_accept_workspace(C.byref(a), C.byref(n)), "ssv_tree_accept_workspace")
+    ws = _workspace(int(n.value), dev, workspace)
+    _check(lib().ssv_tree_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "ssv_tree_accept")
+    return n_acc, path, ep, et
 
 
 def get_status(dev_status, stream=None) -> int:

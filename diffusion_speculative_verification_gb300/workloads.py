@@ -510,3 +510,158 @@ def workload_lmhead(name: str, seed: Optional[int] = None, w: Optional[np.ndarra
     V = wl["V"]
     return make_lmhead_inputs(f"{name}/lmhead/{mode_name}/T={T}", MODE_NAMES[mode_name], T, V, hidden, blocks,
                               workload_gammas(name, blocks), seed + 500, w=w)
+
+
+# --------------------------------------------------------------------------
+# tree (state-set) verification
+# --------------------------------------------------------------------------
+#: Per-sequence record of a tree batch, field order of ssv_tree_seq in include/ssv.h.
+TREE_FIELDS = ("cache_len", "new_len", "block", "n_edges", "q_off", "k_off", "kv_off", "edge_off", "o_off")
+
+
+@dataclasses.dataclass
+class TreeInputs:
+    """One draft tree per sequence over a block of B positions, with the
+    attention inputs of the tree pass and (optionally) planted acceptance
+    inputs.  Layout: query rows N + B per sequence (fresh prompt rows, then
+    one mask-slot row per position) at q_off; new key/value rows N + E + B
+    (fresh rows, one data row per edge, one mask row per position) at k_off;
+    output and logits rows N + (E + 1) B at o_off (fresh rows, then node-major
+    (node, position))."""
+    name: str
+    dtype: str
+    Hq: int
+    Hkv: int
+    d: int
+    seqs: np.ndarray          # int32 [batch, 9] (TREE_FIELDS)
+    parent: np.ndarray        # int32 [sum E], -1 = root
+    pos: np.ndarray           # int32 [sum E]
+    token: np.ndarray         # int32 [sum E]
+    q: np.ndarray             # [sum (N + B), Hq, d] (post-RoPE), bf16 bits or fp32
+    k_new: np.ndarray         # [sum (N + E + B), Hkv, d]
+    v_new: np.ndarray
+    k_cache: np.ndarray       # [sum C, Hkv, d]
+    v_cache: np.ndarray
+    # acceptance (None when not drawn)
+    mode: int = MODE_ARGMAX
+    T: float = 0.0
+    V: int = 0
+    logits: Optional[np.ndarray] = None   # fp32 [sum (N + (E+1) B), V]
+    noise: Optional[np.ndarray] = None    # fp32 [sum B, V] (coupled noise)
+    noise_row: Optional[np.ndarray] = None  # int32 [sum B]
+    pos_off: Optional[np.ndarray] = None  # int32 [batch]: first noise_row entry of each sequence
+    planted: Optional[list] = None        # per sequence: (edges of the planted path, planted emission (p, v) or None)
+
+    @property
+    def batch(self) -> int:
+        return int(self.seqs.shape[0])
+
+    @property
+    def total_out(self) -> int:
+        s = self.seqs
+        return int(np.sum(s[:, 1] + (s[:, 3] + 1) * s[:, 2])) if len(s) else 0
+
+
+def random_tree(rng: np.random.Generator, B: int, E: int):
+    """E edges over a block of B positions: each edge hangs under a random
+    earlier node (half the time the newest one, so paths grow deep) and commits
+    a random position still undecided there.  Returns (parent, pos) int32."""
+    committed = [0]
+    parent, pos = [], []
+    for e in range(E):
+        for _ in range(64):
+            par = e - 1 if (e > 0 and rng.random() < 0.5) else int(rng.integers(-1, e))
+            und = [p for p in range(B) if not (committed[par + 1] >> p) & 1]
+            if und:
+                break
+        else:
+            par, und = -1, list(range(B))
+        p = int(rng.choice(und))
+        parent.append(par)
+        pos.append(p)
+        committed.append(committed[par + 1] | (1 << p))
+    return np.asarray(parent, np.int32), np.asarray(pos, np.int32)
+
+
+def make_tree_inputs(name: str, cache_lens, new_lens, blocks, n_edges, Hq: int, Hkv: int, d: int, dtype: str,
+                     seed: int, V: int = 0, mode: int = MODE_ARGMAX, T: float = 0.0) -> TreeInputs:
+    """Seeded tree-pass inputs; with V > 0 also acceptance inputs with a
+    planted target path: per sequence a cut depth is drawn; along the tree
+    from the root, while above the cut, one existing child edge is made the
+    target's transition (its token's logit raised to 40 in the row of its
+    position, which makes it both the decision and the most confident
+    position); at the cut node a transition outside the tree is planted the
+    same way.  Planting only shapes the accepted lengths."""
+    rng = np.random.default_rng(seed)
+    C = np.asarray(cache_lens, np.int64)
+    N = np.asarray(new_lens, np.int64)
+    B = np.asarray(blocks, np.int64)
+    E = np.asarray(n_edges, np.int64)
+    batch = len(B)
+    cum = lambda x: np.concatenate([[0], np.cumsum(x)[:-1]]) if batch else np.zeros(0, np.int64)  # noqa: E731
+    seqs = np.zeros((batch, 9), np.int32)
+    seqs[:, 0], seqs[:, 1], seqs[:, 2], seqs[:, 3] = C, N, B, E
+    seqs[:, 4] = cum(N + B)
+    seqs[:, 5] = cum(N + E + B)
+    seqs[:, 6] = cum(C)
+    seqs[:, 7] = cum(E)
+    seqs[:, 8] = cum(N + (E + 1) * B)
+    parent, pos = [], []
+    for b in range(batch):
+        pa, po = random_tree(rng, int(B[b]), int(E[b]))
+        parent.append(pa)
+        pos.append(po)
+    parent = np.concatenate(parent).astype(np.int32) if batch else np.zeros(0, np.int32)
+    pos = np.concatenate(pos).astype(np.int32) if batch else np.zeros(0, np.int32)
+    token = rng.integers(0, max(V, 1), size=len(parent)).astype(np.int32)
+    q = _normal_store(rng, (int(np.sum(N + B)), Hq, d), dtype)
+    kn = _normal_store(rng, (int(np.sum(N + E + B)), Hkv, d), dtype)
+    vn = _normal_store(rng, (int(np.sum(N + E + B)), Hkv, d), dtype)
+    kc = _normal_store(rng, (int(np.sum(C)), Hkv, d), dtype)
+    vc = _normal_store(rng, (int(np.sum(C)), Hkv, d), dtype)
+    t = TreeInputs(name, dtype, Hq, Hkv, d, seqs, parent, pos, token, q, kn, vn, kc, vc)
+    if V <= 0:
+        return t
+    total_out = t.total_out
+    logits = np.empty((total_out, V), np.float32)
+
+    def row(r, g):
+        logits[r] = _normal(g, V, 2.0 ** 0.5)
+
+    _rows_parallel(rng, total_out, row)
+    planted = []
+    for b in range(batch):
+        Bb, Eb, e0, o0, Nb = int(B[b]), int(E[b]), int(seqs[b, 7]), int(seqs[b, 8]), int(N[b])
+        pa, po, tk = parent[e0:e0 + Eb], pos[e0:e0 + Eb], token[e0:e0 + Eb]
+        cut = int(rng.integers(0, Bb + 1))
+        n, committed, depth = 0, 0, 0
+        path, emit = [], None
+        while True:
+            und = [p for p in range(Bb) if not (committed >> p) & 1]
+            if not und:
+                break
+            kids = [e for e in range(Eb) if int(pa[e]) + 1 == n]
+            if depth < cut and kids:
+                e = int(rng.choice(kids))
+                logits[o0 + Nb + n * Bb + int(po[e]), int(tk[e])] = 40.0
+                committed |= 1 << int(po[e])
+                path.append(e)
+                n, depth = e + 1, depth + 1
+                continue
+            # a transition outside the tree: a position and token no child has
+            p = int(rng.choice(und))
+            bad = {int(tk[e]) for e in kids if int(po[e]) == p}
+            v = int(rng.integers(0, V))
+            if V > len(bad):
+                while v in bad:
+                    v = int(rng.integers(0, V))
+            logits[o0 + Nb + n * Bb + p, v] = 40.0
+            emit = (p, v)
+            break
+        planted.append((path, emit))
+    t.mode, t.T, t.V, t.logits, t.planted = mode, float(T), V, logits, planted
+    if mode == MODE_GUMBEL:
+        t.pos_off = cum(B).astype(np.int32)
+        t.noise_row = rng.permutation(int(np.sum(B))).astype(np.int32)
+        t.noise = gumbel_table(rng, int(np.sum(B)), V)
+    return t

@@ -469,6 +469,127 @@ SSV_API ssv_status ssv_lmhead_accept(const ssv_lmhead_accept_args* a, void* work
                                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Tree (state-set) verification -- the verification pass over a draft tree
+ * of block states and the acceptance by state equality.
+ * SPOT review, "How it works" (the drafter grows a tree of candidate block
+ * states, each edge committing one position with one token) and "How it is
+ * used" (an edge (y, z) is accepted only if z is the target's next state
+ * from y, so the accepted set is one path; coupled noise at T > 0); SimSD
+ * summary section 2 (in a block state, the mask slot of an undecided
+ * position sees the committed data tokens and the undecided mask slots).
+ * Readings (the pages give neither a layout nor the target's choice of
+ * position):
+ *  - Tree of a sequence: E edges (0 <= E <= 63) over B positions
+ *    (1 <= B <= 64); edge e hangs under node parent[e] + 1 (parent[e] = -1:
+ *    the root, the block state before the pass; parent[e] < e) and commits
+ *    position pos[e] (undecided there) with token token[e].  Node 0 is the
+ *    root, node e + 1 the child of edge e.
+ *  - Query rows at q_off: the N fresh prompt rows, then one mask-slot row per
+ *    position p (its query is the same in every state).  New key / value rows
+ *    at k_off: the N fresh rows, one data row per edge, one mask row per
+ *    position.  Output rows at o_off: the N fresh rows (causal over cache and
+ *    fresh prompt), then node-major rows (n, p), n = 0..E, p = 0..B-1: row
+ *    (n, p), for p undecided at node n, is mask slot p attending the whole
+ *    prompt, the data rows of the edges on the path root -> n and the mask
+ *    rows of the positions undecided at n.  Rows of committed positions are
+ *    not written.  A chain of edges in stage order gives SimSD's mask rows.
+ *  - Target transition from node n: for each undecided p the decision token
+ *    dec(n, p) of logits row (n, p) (argmax, or coupled-noise argmax with the
+ *    noise row of position p) and its confidence l[dec] - logsumexp(l)
+ *    (log-probability under softmax(l)); the most confident position wins
+ *    (ties: the lowest).  The walk from the root follows the child edge
+ *    carrying that (position, token) (the lowest such edge) while there is
+ *    one, and emits the transition where there is none; a node with no
+ *    undecided position ends the walk with nothing emitted.
+ * Every kernel checks each sequence's extents and tree on the device; a
+ * sequence that fails is skipped (its outputs are not written; the
+ * acceptance sets n_acc = -1) and SSV_ERR_INVALID is reported.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t cache_len;  /* C >= 0 */
+  int32_t new_len;    /* N >= 0 */
+  int32_t block;      /* B, 1 <= B <= 64 */
+  int32_t n_edges;    /* E, 0 <= E <= 63 */
+  int32_t q_off;      /* N + B query rows */
+  int32_t k_off;      /* N + E + B new key / value rows */
+  int32_t kv_off;     /* C cache rows */
+  int32_t edge_off;   /* E entries of parent / pos / token */
+  int32_t o_off;      /* N + (E + 1) B output rows (and logits rows) */
+} ssv_tree_seq;
+
+/* ssv_tree_verify_attn -- the attention of the tree pass.
+ * q [total_q, Hq, d], k_new / v_new [total_k, Hkv, d], k_cache / v_cache
+ * [total_cache, Hkv, d] device, in_dtype (post-RoPE); o [total_out, Hq, d]
+ * device, out_dtype.  parent, pos [total_edges] int32 device.  Sequences in
+ * increasing q_off order.  d in {64, 128}, Hq % Hkv == 0, pointers 16-byte
+ * aligned; max_cache bounds every C.  No workspace.  fp32 SIMT arithmetic.
+ * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_CUDA; on device
+ * SSV_ERR_INVALID (see above). */
+typedef struct {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  void* o;
+  ssv_dtype in_dtype;
+  ssv_dtype out_dtype;
+  int32_t Hq, Hkv, d;
+  float scale;                 /* 0 => 1/sqrt(d) */
+  const ssv_tree_seq* seqs;    /* device [batch] */
+  int32_t batch;
+  const int32_t* parent;       /* device [total_edges] */
+  const int32_t* pos;          /* device [total_edges] */
+  int32_t total_q, total_k, total_cache, total_edges, total_out;
+  int32_t max_cache;
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_tree_attn_args;
+
+SSV_API ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* stream);
+
+/* ssv_tree_accept -- acceptance of the tree by state equality.
+ * logits [total_out, V] device (row (n, p) of sequence b at o_off + N + n B + p,
+ * the numbering of the attention's output rows; fresh rows are not read).
+ * mode SSV_ACCEPT_ARGMAX or SSV_ACCEPT_GUMBEL (coupled noise: the table row of
+ * position p of sequence b is noise_row[pos_off[b] + p]; T = 0 means argmax).
+ * parent, pos, token [total_edges] int32 device.
+ * Outputs (device): n_acc [batch] (accepted edges, -1 for a rejected
+ * sequence); path [batch * 64] (the accepted edges' ids within the sequence,
+ * root first, -1 padded); emit_pos, emit_tok [batch] (the target's
+ * transition where the walk stopped, -1 if none).
+ * Workspace: ssv_tree_accept_workspace bytes, 256-byte aligned (no state is
+ * kept between calls).  Errors: SSV_ERR_INVALID, SSV_ERR_NOT_FINITE,
+ * SSV_ERR_WORKSPACE, SSV_ERR_CUDA; on device SSV_ERR_INVALID. */
+typedef struct {
+  ssv_accept_mode mode;
+  float T;
+  int32_t V;
+  const ssv_tree_seq* seqs;    /* device [batch] */
+  int32_t batch;
+  ssv_dtype logits_dtype;
+  const void* logits;
+  const int32_t* parent;
+  const int32_t* pos;
+  const int32_t* token;
+  int32_t total_edges;
+  int32_t total_out;
+  const float* noise;          /* [n_noise_rows, V] fp32 (GUMBEL, T > 0) */
+  int32_t n_noise_rows;
+  const int32_t* noise_row;    /* [total_positions] */
+  const int32_t* pos_off;      /* [batch] */
+  int32_t total_positions;
+  int32_t* n_acc;
+  int32_t* path;
+  int32_t* emit_pos;
+  int32_t* emit_tok;
+  int32_t* dev_status;         /* device, may be NULL */
+} ssv_tree_accept_args;
+
+SSV_API ssv_status ssv_tree_accept_workspace(const ssv_tree_accept_args* a, size_t* bytes);
+SSV_API ssv_status ssv_tree_accept(const ssv_tree_accept_args* a, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* ------------------------------------------------------------------------
  * ssv_set_fault_injection -- test support for failure detection.
  * The pages have no counterpart: this lets a test make a bounded device wait
  * run out without faulting, trapping or hanging the GPU.  For the chosen

@@ -33,6 +33,16 @@ def test_every_declared_symbol_exported(L):
     assert ssv.version().startswith("ssv ")
 
 
+def test_every_entry_point_has_a_declared_signature(L):
+    """Without argtypes ctypes passes a Python int as a 32-bit C int, which
+    truncates device addresses: every entry point that takes arguments must
+    declare them."""
+    for name in ssv.EXPORTS:
+        if name == "ssv_version":
+            continue
+        assert getattr(L, name).argtypes is not None, name
+
+
 def test_status_strings(L):
     for code in range(8):
         assert ssv.status_string(code) != "unknown status"
