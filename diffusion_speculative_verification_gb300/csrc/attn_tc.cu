@@ -264,19 +264,6 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       carryB += __shfl_sync(0xffffffffu, ib, 31);
       carryC += __shfl_sync(0xffffffffu, ic, 31);
     }
-    __syncwarp();  // s_ntile entries written by every lane are read below
-    if (cta == 0) {
-      // stage maps must permute 1..B (a bad map cannot index out of range: report only)
-      for (int b = 0; b < p.batch; ++b) {
-        const ssv_seq s = p.seqs[b];
-        if (s_ntile[b] == 0) continue;  // skipped above (extents), or no rows
-        const bool ok = warp_tau_is_permutation(p.tau + s.tau_off, s.block);
-        if (!ok) {
-          if (lane == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
-          break;
-        }
-      }
-    }
     __syncwarp();  // table entries written by every lane are read by lane 0 below
     if (lane == 0) {
       s_prefU[0] = 0;
@@ -719,23 +706,50 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         const int r = i - x.N;
         uint32_t tm0 = 0u, tm1 = 0u, tm2 = 0u, tm3 = 0u;  // allowed tail keys of this row
         if (warp_active && x.row0 + x.nvalid > x.N) {   // warp-uniform: the unit holds tail rows
-          // stage map of the sequence in two registers per lane, broadcast by shuffles
+          // stage map of the sequence in two registers per lane
           const int32_t* tau = p.tau + x.tau_off;
           const int ta = lane < x.B ? tau[lane] : 0;
           const int tb = lane + 32 < x.B ? tau[lane + 32] : 0;
-          const bool tail_row = valid && !prompt;
-          const int slot_r = tail_row ? (r % x.B) : 0;
+          // the stage map must permute 1..B; a bad map cannot index out of range
+          // (the shuffles below take lane indices mod 32): report only
+          {
+            unsigned long long seen = 0ull;
+            bool ok = true;
+            if (lane < x.B) { if (ta < 1 || ta > x.B) ok = false; else seen |= 1ull << (ta - 1); }
+            if (lane + 32 < x.B) { if (tb < 1 || tb > x.B) ok = false; else seen |= 1ull << (tb - 1); }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) seen |= __shfl_xor_sync(0xffffffffu, seen, o);
+            ok = __all_sync(0xffffffffu, ok);
+            const unsigned long long full = (x.B >= 64) ? ~0ull : ((1ull << x.B) - 1ull);
+            if (!(ok && seen == full) && lane == 0) report(p.dev_status, SSV_ERR_BAD_TAU);
+          }
+          const bool tail_row = valid && !prompt;  // other rows see no tail key (masks stay 0)
+          const int slot_r = tail_row ? (r % x.B) : 0;  // the unit holds tail rows, so B > 0
           // the stage of this lane's own slot: fetch both halves from the holding lane and
           // choose here (a choice made inside the shuffle would use the source lane's slot)
           const int tra = __shfl_sync(0xffffffffu, ta, slot_r & 31), trb = __shfl_sync(0xffffffffu, tb, slot_r & 31);
           const int tr = slot_r < 32 ? tra : trb;
-          for (int tk = 0; tk < 2 * x.B; ++tk) {
-            const int sk = tk % x.B;
-            const int tt = __shfl_sync(0xffffffffu, sk < 32 ? ta : tb, sk & 31);  // sk: the same on every lane
-            if (!tail_row || !tail_allowed(r, tk, x.B, tr, tt)) continue;
-            const uint32_t bit = 1u << (tk & 31);
-            if (tk < 32) tm0 |= bit; else if (tk < 64) tm1 |= bit; else if (tk < 96) tm2 |= bit; else tm3 |= bit;
+          // le / lt: the slots whose stage is <= tr / < tr, accumulated over the stages
+          // v = 1..B in order (one ballot pair per stage: the slot holding stage v)
+          unsigned long long acc = 0ull, le = 0ull, lt = 0ull;
+          for (int v = 1; v <= x.B; ++v) {
+            const uint32_t lo = __ballot_sync(0xffffffffu, ta == v), hi = __ballot_sync(0xffffffffu, tb == v);
+            acc |= ((unsigned long long)hi << 32) | lo;
+            if (v == tr - 1) lt = acc;
+            if (v == tr) le = acc;
           }
+          // tail key t < B is data slot t, t >= B mask slot t - B.  A data row sees the
+          // data slots of stages <= its own; a mask row sees the data slots of earlier
+          // stages and the mask slots of its own stage and later ones.
+          // (every lane took part in the ballots; only tail rows keep masks)
+          const unsigned long long bmask = (x.B >= 64) ? ~0ull : ((1ull << x.B) - 1ull);
+          const bool data_row = r < x.B;
+          const unsigned long long lo_part = !tail_row ? 0ull : (data_row ? le : lt);          // keys [0, B)
+          const unsigned long long hi_part = (!tail_row || data_row) ? 0ull : (~lt & bmask);  // keys [B, 2B)
+          const unsigned long long w01 = lo_part | (x.B < 64 ? (hi_part << x.B) : 0ull);
+          const unsigned long long w23 = x.B == 0 ? 0ull : (x.B < 64 ? (hi_part >> (64 - x.B)) : hi_part);
+          tm0 = (uint32_t)w01; tm1 = (uint32_t)(w01 >> 32);
+          tm2 = (uint32_t)w23; tm3 = (uint32_t)(w23 >> 32);
         }
         float m_used = -INFINITY, l_sum = 0.f;
         for (int jj = 0; jj < len; ++jj) {
@@ -1107,6 +1121,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     }
   }
   // ------------------------------------------------------------------ teardown
+  __syncwarp();  // the producer and issuer lanes rejoin their warps before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (*abort && threadIdx.x == 0) report(p.dev_status, SSV_ERR_TIMEOUT);
