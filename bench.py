@@ -490,6 +490,32 @@ class Timer:
         return self.replay_ms(self._flush)
 
 
+def read_floor_ms(tm: Timer, dev, nbytes: int) -> float:
+    """Achievable time of a plain streaming read of `nbytes` after the same L2
+    flush, in the same graph-replay measurement (ssv_stream_read: 16-byte
+    loads, two CTAs per SM).  It pays the launch and first-byte latency a
+    kernel of the path pays, so on small workloads it is the floor such a
+    kernel can approach, well above bytes / peak bandwidth."""
+    import torch
+    from diffusion_speculative_verification_gb300 import ssv
+    buf = torch.ones(max((nbytes + 15) // 16, 1) * 4, dtype=torch.int32, device=dev)
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    g = tm.capture((lambda st: ssv.stream_read(buf, out, st),))
+    g.replay()
+    torch.cuda.synchronize()
+    t = (tm.replay_ms(g) - tm.flush_ms()) / tm.steps
+    del g, buf
+    return t
+
+
+def floors_of(tm: Timer, dev, run: ConfigRun) -> dict:
+    rb, ab, af, cb = run.work()
+    f = {"verify_attn": read_floor_ms(tm, dev, int(ab)), "rope": read_floor_ms(tm, dev, int(rb))}
+    if run.x is not None:
+        f["accept"] = read_floor_ms(tm, dev, int(cb))
+    return f
+
+
 def warm(run: ConfigRun, stream, l2_flush, n):
     import torch
     for _ in range(n):
@@ -519,10 +545,10 @@ def roofline_of(run: ConfigRun, op_ms, hbm_peak, tf_peak, peak_kind):
             "algorithmic_bytes": ops[dom][1]}
 
 
-def op_records(run: ConfigRun, op_ms, world=1):
+def op_records(run: ConfigRun, op_ms, world=1, floors=None):
     rb, ab, af, cb = run.work()
     x = run.x
-    return {
+    recs = {
         "verify_attn": {"us": round(op_ms[1] * 1e3, 2), "gbs": round(ab / (op_ms[1] * 1e-3) / 1e9, 1),
                         "tflops": round(af / (op_ms[1] * 1e-3) / 1e12, 2), "bytes": ab, "flops": af},
         "rope": {"us": round(op_ms[0] * 1e3, 2), "gbs": round(rb / (op_ms[0] * 1e-3) / 1e9, 1), "bytes": rb},
@@ -532,6 +558,12 @@ def op_records(run: ConfigRun, op_ms, world=1):
                                           "mode": {W.MODE_ARGMAX: "argmax", W.MODE_GUMBEL: "gumbel",
                                                    W.MODE_REJECT: "reject"}[x.mode], "T": x.T},
     }
+    # the same bytes read by a plain streaming reduction after the same flush
+    for k, i in (("rope", 0), ("verify_attn", 1), ("accept", 2)):
+        if floors and recs.get(k) is not None and k in floors:
+            recs[k]["read_floor_us"] = round(floors[k] * 1e3, 2)
+            recs[k]["x_floor"] = round(op_ms[i] / floors[k], 2)
+    return recs
 
 
 def sub_record(config, args, dev, stream, l2_flush, clocks, hbm_peak, tf_peak, peak_kind):
@@ -555,12 +587,14 @@ def sub_record(config, args, dev, stream, l2_flush, clocks, hbm_peak, tf_peak, p
     op_ms = np.array([(tm.replay_ms(graphs[k]) - t_flush) / K if k in graphs else 0.0
                       for k in ("rope", "verify_attn", "accept")])
     t1 = time.time()
+    floors = floors_of(tm, dev, run)
     run.check_status()
     rb, ab, af, cb = run.work()
     a = run.a
     rec = {"workload": config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d, "steps": K,
            "step_us": round(t_step * 1e3, 2), "step_gbs": round((rb + ab + cb) / (t_step * 1e-3) / 1e9, 1),
-           **op_records(run, op_ms), "roofline": roofline_of(run, op_ms, hbm_peak, tf_peak, peak_kind),
+           **op_records(run, op_ms, floors=floors),
+           "roofline": roofline_of(run, op_ms, hbm_peak, tf_peak, peak_kind),
            "clocks": clocks.window(t0, t1) if clocks is not None else None}
     del run, graphs
     torch.cuda.synchronize()
@@ -664,6 +698,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clk = clocks.window(t0, t1) if rank == 0 else None
+    floors = floors_of(tm, dev, run) if graphs is not None else None
     run.check_status()
     tot_ms = aggregate_ms(float(step_total), dist if world > 1 else None, dev)
 
@@ -703,7 +738,7 @@ def run_ours(args):
             "config": {"workload": args.config, "batch": a.batch, "Hq": a.Hq, "Hkv": a.Hkv, "head_dim": a.d,
                        "l2": "256 MB read before every step", "launch": launch,
                        "parallelism": f"replicas x{world}"},
-            **op_records(run, op_ms, world),
+            **op_records(run, op_ms, world, floors),
             "commit": {"us": round(commit_ms * 1e3, 2), "gbs": round(mb / (commit_ms * 1e-3) / 1e9, 1),
                        "bytes": mb, "frac_hbm": round(mb / (commit_ms * 1e-3) / 1e9 / hbm_peak, 4),
                        "traffic": measured_traffic("commit", args.config),

@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <mutex>
+#include <type_traits>
 
 namespace ssv {
 namespace tc {
@@ -790,12 +791,14 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             if (lim_rows > 32 * q) v |= window32(tm0, tm1, tm2, tm3, toff + 32 * q) & prefix32(lim_rows - 32 * q);
             return v;
           };
-          // ---- steady state (not the segment's first block, no mask): one pass with the
-          // running max, P kept in registers until no row's max has grown past the
-          // rescale threshold; otherwise fall through to the two-pass path (S intact).
+          // ---- steady state (not the segment's first block): one pass with the running
+          // max, P kept in registers until no row's max has grown past the rescale
+          // threshold; otherwise fall through to the two-pass path (S intact).  Columns
+          // a row may not see enter as -inf (their P is exactly 0).
           bool done = false;
           float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-          if (all_vis && jj > 0 && __all_sync(0xffffffffu, m_used > -INFINITY)) {
+          auto one_pass = [&](auto masked_tag) {
+            constexpr bool kMasked = decltype(masked_tag)::value;
             uint32_t b0[16], b1[16], pw[64];
             float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
             uint64_t lp0 = 0ull, lp1 = 0ull;  // packed (even, odd) partial sums of P
@@ -807,9 +810,16 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               uint32_t* cur = (q & 1) ? b1 : b0;
               uint32_t* nxt = (q & 1) ? b0 : b1;
               if (q + 1 < BN / 16) tmem_ld16(tS + (q + 1) * 16, nxt);
+              uint32_t vq = ~0u;  // visibility of this chunk's 16 columns (bits 0..15)
+              if constexpr (kMasked) vq = vis32(q >> 1) >> ((q & 1) * 16);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
+                float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
+                if constexpr (kMasked) {
+                  const uint32_t bits = vq >> (2 * e);
+                  s0 = (bits & 1u) ? s0 : -INFINITY;
+                  s1 = (bits & 2u) ? s1 : -INFINITY;
+                }
                 if ((e & 3) == 0) a0 = max3(a0, s0, s1);
                 else if ((e & 3) == 1) a1 = max3(a1, s0, s1);
                 else if ((e & 3) == 2) a2 = max3(a2, s0, s1);
@@ -831,6 +841,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
               unpack2(lp1, l2, l3);
               done = true;
             }
+          };
+          if (jj > 0 && __all_sync(0xffffffffu, m_used > -INFINITY)) {
+            if (all_vis) one_pass(std::false_type{});
+            else one_pass(std::true_type{});
           }
           if (!done) {
             // ---- pass 1: row max of the raw scores (the scale is positive)

@@ -57,6 +57,29 @@ __global__ void fill_tokens(int32_t* p, size_t n, uint64_t seed, int V) {
     p[i] = (int32_t)(mix64(seed ^ i) % (uint64_t)V);
 }
 
+// Plain streaming read, the reference a kernel of the path that reads the same
+// bytes is measured against: 16-byte loads, eight independent ones in flight
+// per thread, two CTAs of 512 threads per SM, each CTA one contiguous range;
+// the XOR of everything read goes to *out so that no load can be dropped.
+__global__ void __launch_bounds__(512) stream_read_kernel(const uint4* __restrict__ buf, size_t n16, uint32_t* out) {
+  const size_t per = (n16 + gridDim.x - 1) / gridDim.x;
+  const size_t b = (size_t)blockIdx.x * per, e = (b + per < n16) ? b + per : n16;
+  uint32_t acc = 0u;
+  for (size_t i = b + threadIdx.x; i < e; i += (size_t)blockDim.x * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const size_t j = i + (size_t)u * blockDim.x;
+      v[u] = j < e ? __ldcs(buf + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc) atomicXor(out, acc);
+}
+
 uint64_t host_mix(uint64_t x) {
   x += 0x9E3779B97F4A7C15ull;
   x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -395,4 +418,18 @@ done:
   if (e1) cudaEventDestroy(e1);
   if (st) cudaStreamDestroy(st);
   return rc;
+}
+
+extern "C" ssv_status ssv_stream_read(const void* buf, size_t bytes, uint32_t* out, void* stream) {
+  if (!buf || !out || ((uintptr_t)buf & 15u) || (bytes & 15u)) return SSV_ERR_INVALID;
+  if (bytes == 0) return SSV_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return SSV_ERR_CUDA;
+  const size_t n16 = bytes / 16;
+  const size_t want = (n16 + 4095) / 4096;  // at least 64 KB per CTA
+  const int grid = (int)std::min<size_t>((size_t)2 * sms, std::max<size_t>(want, 1));
+  stream_read_kernel<<<grid, 512, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<const uint4*>(buf), n16, out);
+  return cudaGetLastError() == cudaSuccess ? SSV_OK : SSV_ERR_CUDA;
 }

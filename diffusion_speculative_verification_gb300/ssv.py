@@ -25,7 +25,7 @@ ARGMAX, GUMBEL, REJECT, GUMBEL_GEN = 0, 1, 2, 3
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
            "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_lmhead_accept_workspace", "ssv_lmhead_accept",
            "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench", "ssv_set_fault_injection",
-           "ssv_tree_verify_attn", "ssv_tree_accept_workspace", "ssv_tree_accept")
+           "ssv_tree_verify_attn", "ssv_tree_accept_workspace", "ssv_tree_accept", "ssv_stream_read")
 FAULT_NONE, FAULT_ATTN, FAULT_ACCEPT, FAULT_LMHEAD = 0, 1, 2, 3
 
 
@@ -133,6 +133,7 @@ def lib():
         L.ssv_status_string.restype = C.c_char_p
         L.ssv_version.restype = C.c_char_p
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
+        L.ssv_stream_read.argtypes = [vp, sz, vp, vp]
         L.ssv_set_fault_injection.argtypes = [C.POINTER(FaultInjection)]
         L.ssv_tree_verify_attn.argtypes = [C.POINTER(TreeAttnArgs), vp]
         L.ssv_tree_accept_workspace.argtypes = [C.POINTER(TreeAcceptArgs), C.POINTER(sz)]
@@ -141,7 +142,7 @@ def lib():
                      "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit",
                      "ssv_lmhead_accept_workspace", "ssv_lmhead_accept", "ssv_get_status", "ssv_bench",
                      "ssv_set_fault_injection", "ssv_tree_verify_attn", "ssv_tree_accept_workspace",
-                     "ssv_tree_accept"):
+                     "ssv_tree_accept", "ssv_stream_read"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -456,6 +457,13 @@ def tree_accept(mode, T, logits, seqs, parent, pos, token, noise=None, noise_row
     _check(lib().ssv_tree_accept(C.byref(a), _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream)),
            "ssv_tree_accept")
     return n_acc, path, ep, et
+
+
+def stream_read(buf, out, stream=None):
+    """Reads every byte of the device tensor `buf` once (measurement reference
+    for memory-bound kernels); XOR checksum into the int32 device tensor `out`."""
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().ssv_stream_read(_ptr(buf), nbytes, _ptr(out), _stream_ptr(stream)), "ssv_stream_read")
 
 
 def get_status(dev_status, stream=None) -> int:

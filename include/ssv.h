@@ -648,6 +648,20 @@ SSV_API const char* ssv_version(void);
  * ---------------------------------------------------------------------- */
 SSV_API ssv_status ssv_bench(const char* config, int32_t iters, char* json_out, size_t json_len);
 
+/* ------------------------------------------------------------------------
+ * ssv_stream_read -- the measurement reference for a memory-bound kernel
+ * of the path: reads `bytes` at device address `buf` once (16-byte loads,
+ * two CTAs per SM, each a contiguous range) and XORs every word read into
+ * *out (device address; a checksum that keeps the loads live, not a result
+ * of the method).  Timed like the kernel it is compared with (same L2
+ * flush, same launch mode), it gives the achievable time for reading those
+ * bytes, launch and first-byte latency included; on small workloads that is
+ * well above bytes / peak bandwidth.  Not a hot-path call.  buf must be
+ * 16-byte aligned and bytes a multiple of 16.  Asynchronous on `stream`.
+ * Errors: SSV_ERR_INVALID (null or misaligned arguments), SSV_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+SSV_API ssv_status ssv_stream_read(const void* buf, size_t bytes, uint32_t* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
