@@ -69,7 +69,7 @@ __device__ __forceinline__ void store16(T* p, const float* v) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kRopeThreads)
+__global__ void __launch_bounds__(kRopeThreads, 4)  // four CTAs per SM: a whole decode batch in one wave
 rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_out, T* k_out,
                  int Hq, int Hkv, const ssv_seq* __restrict__ seqs, int batch, int total_rows,
                  const int32_t* __restrict__ positions, int32_t* dev_status,
@@ -77,7 +77,7 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   constexpr int HALF = D / 2;
   constexpr int VEC = Vec16<T>::N;
   constexpr int CHUNKS = HALF / VEC;
-  constexpr int PRE = 4;  // items per thread loaded before the positions are known
+  constexpr int PRE = 5;  // items per thread loaded before the positions are known (all of them up to 40 heads)
   __shared__ float s_cos[kRopeRows][HALF];
   __shared__ float s_sin[kRopeRows][HALF];
   __shared__ int s_pos[kRopeRows];
