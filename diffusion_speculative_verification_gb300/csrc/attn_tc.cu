@@ -65,11 +65,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_O = 256;                   // O_mt at columns 256 + 128 mt; S_mt / P_mt at 128 mt
 constexpr float kRescaleThreshold = 8.0f;        // log2 units
 constexpr int kMergeBlocks = 8;                  // key blocks a partial merge costs, roughly
-// Work estimate of the plan, in cost units: a key block costs 1 + the tiles it
-// is multiplied into (the MMA work grows with the tiles, the K/V fetch does
-// not); a segment's fixed work (Q load, first block's unmasked-max pass,
-// epilogue) costs about two two-tile blocks.
-constexpr int kSegCost = 6;
+// Work estimate of the plan, in cost units of about 0.3 us, fitted to the
+// per-CTA times of a mixed decode batch (prompt lengths 256..8192, blocks of
+// 4..32 slots): a key block multiplied into one tile costs 4 (1.2 us: the
+// K/V fetch and one S / PV pair), into two tiles 7 (2.2 us: the tensor
+// work doubles, the fetch does not); a segment's fixed work (Q load, the
+// first block's two-pass softmax, the masked last block, the epilogue) 22.
+constexpr int kSegCost = 22;
+constexpr int kMaxBlockCost = 7;
 
 enum : uint32_t {
   B_Q_FULL = 0,
@@ -163,7 +166,7 @@ struct Unit {
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ int unit_weight(int rows, int row0, int UR, int R, int MT) {
-  return (MT == 2 && min(UR, rows - row0) > R) ? 3 : 2;  // 1 + tiles of the unit
+  return (MT == 2 && min(UR, rows - row0) > R) ? 7 : 4;  // cost of a key block of the unit
 }
 
 __device__ __forceinline__ int unit_nblocks(int C, int N, int rows, int row0, int UR) {
@@ -286,7 +289,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       ph = min(ph, max(carryB, 1));
       // every range at least one block's weight wide: no range falls between two
       // block starts of a unit, so the ranks holding a unit's blocks are consecutive
-      ph = min(ph, max(carryC / (1 + MT), 1));
+      ph = min(ph, max(carryC / kMaxBlockCost, 1));
       h.Pe = ph;
       h.g = cta % p.Hkv;
       // The head's units are cut into Pe contiguous ranges of equal estimated cost.
@@ -988,7 +991,8 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
             // partial with a release increment and move on without waiting.
             const long long cu = unit_cost(u);
             const int c_a = owner_at(cu + kSegCost);                                   // ranks of head gh holding
-            const int c_b = owner_at(cu + kSegCost + (long long)(1 + x.mc) * (x.nblocks - 1));  // the first, last block
+            const int c_b = owner_at(cu + kSegCost + (long long)unit_weight(x.rows, x.row0, UR, R, MT) *
+                                                          (x.nblocks - 1));                 // the first, last block
             int32_t* counter = work.cnt + (((size_t)gh * Uh + u) * MT + mt) * 4 + q4;
             // partial slot of rank rr (> c_a): its piece is the first segment of its range
             auto slot_of = [&](int rr) -> size_t { return ((size_t)((rr * p.Hkv + gh) * 2) * MT + mt) * 128 + m; };
@@ -1225,7 +1229,7 @@ bool attn_tc_supported(const AttnParams& p) {
   const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
   const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
                            ((p.max_cache + BN - 1) / BN + (max_rows + BN - 1) / BN);
-  if (blocks > (1LL << 27)) return false;  // plan costs (at most 9 units per block) stay in int32
+  if (blocks > (1LL << 26)) return false;  // plan costs (at most 29 units per block) stay in int32
   return encode_fn() != nullptr && sm_count() > 0;
 }
 
