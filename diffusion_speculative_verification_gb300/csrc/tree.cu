@@ -8,15 +8,17 @@
 // (in a block state, the mask slot of an undecided position sees the
 // committed data tokens and the undecided mask slots).
 //
-// ssv_tree_verify_attn: one warp per (query row, kv head, group of up to 8 of
-// its query heads), fp32 FMA; each key's K and V are loaded once for all the
-// warp's heads.  A fresh prompt row is causal over cache and fresh prompt.
-// A mask-slot row M_p runs once over the whole prompt (cache + fresh), then,
-// for every node n where p is undecided, continues a copy of that running
-// softmax over the node's tail keys -- the data rows of the edges on the
-// path to n and the mask rows of the positions undecided at n -- and writes
-// output row (n, p).  The tree is checked and its per-node bitmasks
-// (committed positions, path edges) built in shared memory by each warp.
+// ssv_tree_verify_attn: one CTA of 8 warps per (query row, kv head, group of
+// up to 8 of its query heads), fp32 FMA; each key's K and V are loaded once
+// for all the group's heads.  A fresh prompt row is causal over cache and
+// fresh prompt.  The prompt keys are cut into 8 contiguous ranges, one per
+// warp, and the warps' partial softmax states merged.  A mask-slot row M_p
+// runs once over the whole prompt (cache + fresh) that way, then, for every
+// node n where p is undecided (nodes dealt to the warps in turn), continues a
+// copy of the merged state over the node's tail keys -- the data rows of the
+// edges on the path to n and the mask rows of the positions undecided at n --
+// and writes output row (n, p).  The tree is checked and its per-node bitmasks
+// (committed positions, path edges) built in shared memory once per CTA.
 //
 // ssv_tree_accept: a reduce kernel over (row, vocabulary chunk) records each
 // chunk's decision (first argmax of l or of fl(fl(l/T) + G)) and its
@@ -36,7 +38,7 @@ namespace {
 
 constexpr int kTreeMaxB = 64;
 constexpr int kTreeMaxE = 63;   // nodes 0..63 fit one 64-bit path mask per node
-constexpr int kTreeWarps = 4;
+constexpr int kTreeWarps = 8;   // warps sharing one (row, kv head) task's prompt keys
 constexpr int kTreeHeads = 8;   // most query heads a warp serves together
 
 struct TreeAttnParams {
@@ -163,6 +165,49 @@ __device__ __forceinline__ void add_key(RunState<E, GH>& st, const float (*q)[E]
   }
 }
 
+// Four keys at once into the running state: the four dot products reduce
+// across the warp side by side, and the state is rescaled once per four keys.
+template <int E, int GH>
+__device__ __forceinline__ void add_keys4(RunState<E, GH>& st, const float (*q)[E], const float (*kk)[E],
+                                          const float (*vv)[E], int gh) {
+  float sc[4][GH];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      float part = 0.f;
+      if (h < gh) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) part = fmaf(q[h][e], kk[k][e], part);
+      }
+      sc[k][h] = part;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int h = 0; h < GH; ++h) sc[k][h] += __shfl_xor_sync(0xffffffffu, sc[k][h], o);
+#pragma unroll
+  for (int h = 0; h < GH; ++h) {
+    if (h >= gh) continue;
+    const float mx = fmaxf(fmaxf(st.m[h], fmaxf(sc[0][h], sc[1][h])), fmaxf(sc[2][h], sc[3][h]));
+    const float corr = exp2f(st.m[h] - mx);
+    float pk[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pk[k] = exp2f(sc[k][h] - mx);
+    st.l[h] = st.l[h] * corr + ((pk[0] + pk[1]) + (pk[2] + pk[3]));
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float a = st.acc[h][e] * corr;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) a = fmaf(pk[k], vv[k][e], a);
+      st.acc[h][e] = a;
+    }
+    st.m[h] = mx;
+  }
+}
+
 template <typename OutT, int E, int GH>
 __device__ __forceinline__ void store_row(const RunState<E, GH>& st, OutT* o, int h0, int gh, int lane) {
 #pragma unroll
@@ -178,11 +223,15 @@ __device__ __forceinline__ void store_row(const RunState<E, GH>& st, OutT* o, in
 template <typename T, typename OutT, int D, int GH>
 __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAttnParams p) {
   constexpr int E = D / 32;
-  __shared__ unsigned long long s_cm[kTreeWarps][kTreeMaxE + 1], s_pm[kTreeWarps][kTreeMaxE + 1];
+  __shared__ unsigned long long s_cm[kTreeMaxE + 1], s_pm[kTreeMaxE + 1];
+  __shared__ float s_ml[kTreeWarps][2][GH];       // each warp's running max and sum per head
+  __shared__ float s_acc[kTreeWarps][GH][D];      // and its unnormalised output
+  __shared__ int s_ok;
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int G = p.Hq / p.Hkv;
   const int nhc = (G + GH - 1) / GH;
-  const long long w = (long long)blockIdx.x * kTreeWarps + wl;
+  // one CTA per (query row, kv head, group of heads): every early return below is CTA-uniform
+  const long long w = blockIdx.x;
   if (w >= (long long)p.total_q * p.Hkv * nhc) return;
   const int qr = (int)(w / ((long long)p.Hkv * nhc));
   const int g = (int)((w / nhc) % p.Hkv), hc = (int)(w % nhc);
@@ -190,17 +239,22 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
   if (b < 0) return;
   const ssv_tree_seq s = p.seqs[b];
   if (!tree_seq_ok(s, p.total_q, p.total_k, p.total_cache, p.total_edges, p.total_out) || s.cache_len > p.max_cache) {
-    if (lane == 0) report(p.dev_status, SSV_ERR_INVALID);
+    if (threadIdx.x == 0) report(p.dev_status, SSV_ERR_INVALID);
     return;
   }
   const int i = qr - s.q_off;
   if (i >= s.new_len + s.block) return;
-  unsigned long long* cm = s_cm[wl];
-  unsigned long long* pm = s_pm[wl];
-  if (!build_tree_masks(s, p.parent, p.pos, cm, pm)) {
-    if (lane == 0) report(p.dev_status, SSV_ERR_INVALID);
-    return;
+  if (wl == 0) {
+    const bool ok = build_tree_masks(s, p.parent, p.pos, s_cm, s_pm);
+    if (lane == 0) {
+      s_ok = ok ? 1 : 0;
+      if (!ok) report(p.dev_status, SSV_ERR_INVALID);
+    }
   }
+  __syncthreads();
+  if (!s_ok) return;
+  const unsigned long long* cm = s_cm;
+  const unsigned long long* pm = s_pm;
   const int h0 = g * G + hc * GH;
   const int gh = min(GH, G - hc * GH);
   const T* Q = static_cast<const T*>(p.q);
@@ -239,25 +293,72 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
   };
   const bool fresh = i < s.new_len;
   // prompt keys: the cache, then the fresh prompt rows (all of them for a mask
-  // slot; up to the row itself for a fresh row)
+  // slot; up to the row itself for a fresh row), cut into kTreeWarps
+  // contiguous ranges, one per warp; the partial softmax states are then merged
   const int n_fresh = fresh ? i + 1 : s.new_len;
-  for (int j = 0; j < s.cache_len; ++j) {
+  const int n_prompt = s.cache_len + n_fresh;
+  const int j_lo = (int)(((long long)n_prompt * wl) / kTreeWarps);
+  const int j_hi = (int)(((long long)n_prompt * (wl + 1)) / kTreeWarps);
+  auto key_prompt = [&](int j, float* kk, float* vv) {
+    if (j < s.cache_len) key_cache(j, kk, vv);
+    else key_new(j - s.cache_len, kk, vv);
+  };
+  int j = j_lo;
+  for (; j + 4 <= j_hi; j += 4) {
+    float kk[4][E], vv[4][E];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) key_prompt(j + k, kk[k], vv[k]);
+    add_keys4<E, GH>(st, q, kk, vv, gh);
+  }
+  for (; j < j_hi; ++j) {
     float kk[E], vv[E];
-    key_cache(j, kk, vv);
+    key_prompt(j, kk, vv);
     add_key<E, GH>(st, q, kk, vv, gh);
   }
-  for (int j = 0; j < n_fresh; ++j) {
-    float kk[E], vv[E];
-    key_new(j, kk, vv);
-    add_key<E, GH>(st, q, kk, vv, gh);
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      s_ml[wl][0][h] = st.m[h];
+      s_ml[wl][1][h] = st.l[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < GH; ++h)
+#pragma unroll
+    for (int e = 0; e < E; ++e) s_acc[wl][h][lane * E + e] = st.acc[h][e];
+  __syncthreads();
+  // every warp forms the merged state (the ranges in order; empty ones have max -inf)
+#pragma unroll
+  for (int h = 0; h < GH; ++h) {
+    float M = -INFINITY;
+    for (int u = 0; u < kTreeWarps; ++u) M = fmaxf(M, s_ml[u][0][h]);
+    float l = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (M > -INFINITY) {
+      for (int u = 0; u < kTreeWarps; ++u) {
+        const float mu = s_ml[u][0][h];
+        if (!(mu > -INFINITY)) continue;
+        const float f = exp2f(mu - M);
+        l = fmaf(s_ml[u][1][h], f, l);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(s_acc[u][h][lane * E + e], f, acc[e]);
+      }
+    }
+    st.m[h] = M;
+    st.l[h] = l;
+#pragma unroll
+    for (int e = 0; e < E; ++e) st.acc[h][e] = acc[e];
   }
   if (fresh) {
-    store_row<OutT, E, GH>(st, O + (size_t)(s.o_off + i) * p.Hq * D, h0, gh, lane);
+    if (wl == 0) store_row<OutT, E, GH>(st, O + (size_t)(s.o_off + i) * p.Hq * D, h0, gh, lane);
     return;
   }
+  // a mask slot: each node where its position is undecided continues a copy of
+  // the prompt state over the node's tail keys; nodes dealt to the warps in turn
   const int pp = i - s.new_len;  // position of this mask slot
   const unsigned long long full = (s.block >= 64) ? ~0ull : ((1ull << s.block) - 1ull);
-  for (int n = 0; n <= s.n_edges; ++n) {
+  for (int n = wl; n <= s.n_edges; n += kTreeWarps) {
     if ((cm[n] >> pp) & 1ull) continue;  // committed at n: no row
     RunState<E, GH> t = st;
     for (unsigned long long m = pm[n]; m; m &= m - 1) {  // data rows of the path's edges
@@ -277,8 +378,7 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
 template <typename T, typename OutT, int D, int GH>
 cudaError_t launch_tree_attn_gh(const TreeAttnParams& p, cudaStream_t st) {
   const int G = p.Hq / p.Hkv;
-  const long long warps = (long long)p.total_q * p.Hkv * ((G + GH - 1) / GH);
-  const long long grid = (warps + kTreeWarps - 1) / kTreeWarps;
+  const long long grid = (long long)p.total_q * p.Hkv * ((G + GH - 1) / GH);  // one CTA per task
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   tree_attn_kernel<T, OutT, D, GH><<<(unsigned)grid, kTreeWarps * 32, 0, st>>>(p);
   return cudaGetLastError();
