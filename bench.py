@@ -913,9 +913,10 @@ def run_tree(args, dev, stream, l2_flush, hbm_peak):
     n = C.c_size_t(0)
     L.ssv_tree_accept_workspace(C.byref(cargs), C.byref(n))
     ws = torch.zeros(max(256, int(n.value)), dtype=torch.uint8, device=dev)
+    wsa = torch.zeros(max(256, ssv.tree_verify_attn_workspace_bytes(aargs)), dtype=torch.uint8, device=dev)
 
     def op_attn(s):
-        r = L.ssv_tree_verify_attn(C.byref(aargs), s.cuda_stream)
+        r = L.ssv_tree_verify_attn(C.byref(aargs), wsa.data_ptr(), wsa.numel(), s.cuda_stream)
         if r:
             raise ssv.SsvError(r, "ssv_tree_verify_attn")
 

@@ -30,6 +30,17 @@ struct AttnParams {
   // CTA 0 leave out that key-block copy (test support, ssv_set_fault_injection)
   long long wait_budget;
   int fault_skip;
+  // Prompt-only pass (the tree pass's shared prefix, tensor-core schedule
+  // only): a sequence has N prompt rows and `block` further query rows, each
+  // of which sees the whole prompt (cache + N fresh keys) and nothing else;
+  // no stage map is read.  Its fresh keys are rows [tau_off, tau_off + N) of
+  // k_new / v_new (total_krows rows), its query and output rows [q_off,
+  // q_off + N + block) of q / o (total_rows rows).  lse (when not null):
+  // [total_rows][Hq] log2-sum-exp2 of the scaled scores (scale * log2 e) of
+  // each output row, -inf for a row that saw no key.
+  int prompt_only;
+  int total_krows;
+  float* lse;
 };
 
 cudaError_t launch_attn_simt(const AttnParams& p, cudaStream_t st);

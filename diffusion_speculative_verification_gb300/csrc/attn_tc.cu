@@ -159,7 +159,7 @@ static_assert(8 * B_COUNT + 8 + sizeof(PlanHdr) <= 256, "barrier area overflow")
 
 struct Unit {
   int b, g;
-  int C, N, B, rows, q_off, kv_off, tau_off;
+  int C, N, B, rows, q_off, k_off, kv_off, tau_off;  // k_off: first fresh key row
   int row0, nvalid, mc, cache_blocks, nblocks, full_new;
 };
 
@@ -169,9 +169,18 @@ __device__ __forceinline__ int unit_weight(int rows, int row0, int UR, int R, in
   return (MT == 2 && min(UR, rows - row0) > R) ? 7 : 4;  // cost of a key block of the unit
 }
 
-__device__ __forceinline__ int unit_nblocks(int C, int N, int rows, int row0, int UR) {
-  const int kmax = (row0 + UR <= N) ? (row0 + UR) : rows;
+// Key blocks of the unit whose rows start at row0: the cache, then the fresh
+// keys up to its last prompt row (causal), or through the tail rows' keys when
+// it holds tail rows (in a prompt-only pass tail rows see the prompt alone).
+__device__ __forceinline__ int unit_nblocks(int C, int N, int rows, int row0, int UR, bool tail_keys) {
+  const int kmax = (row0 + UR <= N) ? (row0 + UR) : (tail_keys ? rows : N);
   return cdiv(C, BN) + cdiv(kmax, BN);
+}
+
+// Query rows of a sequence: N prompt rows, then 2B tail rows (B data, B mask)
+// or, in a prompt-only pass, B rows.
+__device__ __forceinline__ int seq_rows(const ssv_seq& s, bool prompt_only) {
+  return s.new_len + (prompt_only ? 1 : 2) * s.block;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -224,6 +233,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
   const int UR = MT * R;
   const int P = gridDim.x;   // CTAs launched; only the first Pe own key blocks
   const int cta = blockIdx.x;
+  const bool po = p.prompt_only != 0;
 
   // ------------------------------------------------------------------ plan
   // Work is partitioned per kv head: CTA c serves head g = c % Hkv as rank r = c / Hkv of
@@ -241,15 +251,20 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       int units = 0, blocks = 0, cost = 0;
       if (b < p.batch) {
         const ssv_seq s = p.seqs[b];
-        const int rows = s.new_len + 2 * s.block;
+        const int rows = seq_rows(s, po);
         // a sequence outside the call's buffers (or above the stated maxima)
         // gets no units: its rows are neither read nor written
-        const bool ok = seq_extents_ok(s, p.total_rows, p.total_cache, p.total_slots) &&
-                        s.cache_len <= p.max_cache && s.new_len <= p.max_new && s.block <= p.max_block;
+        const bool ext = po ? (s.cache_len >= 0 && s.new_len >= 0 && s.block >= 1 && s.block <= 64 && s.q_off >= 0 &&
+                               (long long)s.q_off + rows <= p.total_rows && s.tau_off >= 0 &&
+                               (long long)s.tau_off + s.new_len <= p.total_krows && s.kv_off >= 0 &&
+                               (long long)s.kv_off + s.cache_len <= p.total_cache)
+                            : seq_extents_ok(s, p.total_rows, p.total_cache, p.total_slots);
+        const bool ok = ext && s.cache_len <= p.max_cache && s.new_len <= p.max_new && s.block <= p.max_block;
         if (!ok && cta == 0) report(p.dev_status, SSV_ERR_INVALID);
-        const int nt = ok ? cdiv(rows, UR) : 0;
+        // (a prompt-only sequence without prompt keys has nothing to attend to: no units)
+        const int nt = (ok && (!po || s.cache_len + s.new_len > 0)) ? cdiv(rows, UR) : 0;
         for (int t = 0; t < nt; ++t) {
-          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR, !po);
           blocks += nb;
           cost += kSegCost + unit_weight(rows, t * UR, UR, R, MT) * nb;
         }
@@ -306,11 +321,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           if (s_prefC[mid] <= C) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
         }
         const ssv_seq s = p.seqs[b];
-        const int rows = s.new_len + 2 * s.block;
+        const int rows = seq_rows(s, po);
         int xs = s_prefB[b], uu = s_prefU[b];
         long long cu = s_prefC[b];
         for (int t = 0;; ++t, ++uu) {
-          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+          const int nb = unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR, !po);
           const int w = unit_weight(rows, t * UR, UR, R, MT);
           if (t == s_ntile[b] - 1 || cu + kSegCost + (long long)w * nb > C) {
             const long long d = C - cu - kSegCost;
@@ -370,12 +385,13 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
     const ssv_seq s = p.seqs[b];
     x.C = s.cache_len; x.N = s.new_len; x.B = s.block;
     x.q_off = s.q_off; x.kv_off = s.kv_off; x.tau_off = s.tau_off;
-    x.rows = x.N + 2 * x.B;
+    x.k_off = po ? s.tau_off : s.q_off;
+    x.rows = seq_rows(s, po);
     x.row0 = tile * UR;
     x.nvalid = min(UR, x.rows - x.row0);
     x.mc = (MT == 2 && x.nvalid > R) ? 2 : 1;
     x.cache_blocks = cdiv(x.C, BN);
-    x.nblocks = unit_nblocks(x.C, x.N, x.rows, x.row0, UR);
+    x.nblocks = unit_nblocks(x.C, x.N, x.rows, x.row0, UR, !po);
     x.full_new = (x.row0 < x.N) ? (x.row0 + 1) : x.N;
     return x;
   };
@@ -395,10 +411,11 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
       if (s_prefU[mid] <= u) { b = mid; lo = mid + 1; } else { hi = mid - 1; }
     }
     const ssv_seq s = p.seqs[b];
-    const int rows = s.new_len + 2 * s.block;
+    const int rows = seq_rows(s, po);
     long long c = s_prefC[b];
     for (int t = 0; t < u - s_prefU[b]; ++t)
-      c += kSegCost + (long long)unit_weight(rows, t * UR, UR, R, MT) * unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR);
+      c += kSegCost + (long long)unit_weight(rows, t * UR, UR, R, MT) *
+                          unit_nblocks(s.cache_len, s.new_len, rows, t * UR, UR, !po);
     return c;
   };
 
@@ -419,7 +436,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         mbar_expect_tx(bar(B_K_FULL + st), TILE_BYTES);
         const bool cache = j < x.cache_blocks;
         const CUtensorMap* mk = cache ? &maps.kc : &maps.kn;
-        const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
+        const int z = cache ? (x.kv_off + j * BN) : (x.k_off + (j - x.cache_blocks) * BN);
         const uint32_t dk = sbase + C_::SM_K + st * TILE_BYTES;
         tma_load_3d(dk, mk, 0, x.g, z, bar(B_K_FULL + st));
         tma_load_3d(dk + HALF_BYTES, mk, 64, x.g, z, bar(B_K_FULL + st));
@@ -432,7 +449,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         mbar_expect_tx(bar(B_V_FULL + st), TILE_BYTES);
         const bool cache = j < x.cache_blocks;
         const CUtensorMap* mv = cache ? &maps.vc : &maps.vn;
-        const int z = cache ? (x.kv_off + j * BN) : (x.q_off + (j - x.cache_blocks) * BN);
+        const int z = cache ? (x.kv_off + j * BN) : (x.k_off + (j - x.cache_blocks) * BN);
         const uint32_t dv = sbase + C_::SM_V + st * TILE_BYTES;
         tma_load_3d(dv, mv, 0, x.g, z, bar(B_V_FULL + st));
         tma_load_3d(dv + HALF_BYTES, mv, 64, x.g, z, bar(B_V_FULL + st));
@@ -709,7 +726,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         const bool prompt = i < x.N;
         const int r = i - x.N;
         uint32_t tm0 = 0u, tm1 = 0u, tm2 = 0u, tm3 = 0u;  // allowed tail keys of this row
-        if (warp_active && x.row0 + x.nvalid > x.N) {   // warp-uniform: the unit holds tail rows
+        if (!po && warp_active && x.row0 + x.nvalid > x.N) {   // warp-uniform: the unit holds tail rows
           // stage map of the sequence in two registers per lane
           const int32_t* tau = p.tau + x.tau_off;
           const int ta = lane < x.B ? tau[lane] : 0;
@@ -951,6 +968,10 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
         if (warp_active) {
           tc_fence_after();
           OutT* orow = static_cast<OutT*>(p.o) + ((size_t)(x.q_off + i) * p.Hq + x.g * G + hj) * D;
+          // log2-sum-exp2 of the row's scaled scores (m is that of the scores behind l)
+          auto store_lse = [&](float m, float l) {
+            if (p.lse && valid) p.lse[(size_t)(x.q_off + i) * p.Hq + x.g * G + hj] = l > 0.f ? m + log2f(l) : -INFINITY;
+          };
           auto store_chunk = [&](int q, const float* v, float inv) {
             if (!valid) return;
             if constexpr (sizeof(OutT) == 4) {
@@ -974,6 +995,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
           // (one-shot code: loops stay rolled, the instructions arrive cold)
           if (complete) {
             const float inv = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+            store_lse(m_used, l_sum);
 #pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
               uint32_t raw[32];
@@ -1052,6 +1074,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                   L += ml[k].y * fo[k];
                 }
                 const float inv = (L > 0.f) ? 1.f / L : 0.f;
+                store_lse(M, L);
 #pragma unroll 1
                 for (int q = 0; q < D / 32; ++q) {
                   float v[32];
@@ -1094,6 +1117,7 @@ attn_tc_kernel(const __grid_constant__ TcMaps maps, const AttnParams p, const Tc
                   if (M > -INFINITY) L += lo * ex2(mo - M);
                 }
                 const float inv = (L > 0.f) ? 1.f / L : 0.f;
+                store_lse(M, L);
 #pragma unroll 1
                 for (int q = 0; q < D / 32; ++q) {
                   float v[32];
@@ -1190,7 +1214,7 @@ static int sm_count() {
 
 static int choose_mt(const AttnParams& p) {
   const int G = p.Hq / p.Hkv;
-  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  const long long max_rows = (long long)p.max_new + (p.prompt_only ? 1LL : 2LL) * p.max_block;
   return (max_rows * G > 128) ? 2 : 1;
 }
 
@@ -1204,7 +1228,7 @@ static WsLayout ws_layout(const AttnParams& p) {
   const int G = p.Hq / p.Hkv;
   L.mt = choose_mt(p);
   const int UR = L.mt * (128 / G);
-  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  const long long max_rows = (long long)p.max_new + (p.prompt_only ? 1LL : 2LL) * p.max_block;
   L.units = (int)((long long)p.batch * p.Hkv * ((max_rows + UR - 1) / UR));
   L.grid = sm_count();
   size_t off = 0;
@@ -1226,7 +1250,7 @@ bool attn_tc_supported(const AttnParams& p) {
   if (G < 1 || G > 128 || (128 % G) != 0) return false;
   if (p.max_block > 64 || p.Hkv > sm_count()) return false;  // every kv head needs a CTA
   // total key blocks must fit comfortably in int32
-  const long long max_rows = (long long)p.max_new + 2LL * p.max_block;
+  const long long max_rows = (long long)p.max_new + (p.prompt_only ? 1LL : 2LL) * p.max_block;
   const long long blocks = (long long)p.batch * p.Hkv * (max_rows / (128 / G) + 1) *
                            ((p.max_cache + BN - 1) / BN + (max_rows + BN - 1) / BN);
   if (blocks > (1LL << 26)) return false;  // plan costs (at most 29 units per block) stay in int32
@@ -1273,8 +1297,14 @@ cudaError_t launch_attn_tc(const AttnParams& p, void* ws, cudaStream_t st) {
   const WsLayout L = ws_layout(p);
   TcMaps maps;
   if (!encode_3d(&maps.q, p.q, p.Hq, p.total_rows, G, R)) return cudaErrorInvalidValue;
-  if (!encode_3d(&maps.kn, p.k_new, p.Hkv, p.total_rows, 1, BN)) return cudaErrorInvalidValue;
-  if (!encode_3d(&maps.vn, p.v_new, p.Hkv, p.total_rows, 1, BN)) return cudaErrorInvalidValue;
+  const int krows = p.prompt_only ? p.total_krows : p.total_rows;
+  if (krows > 0) {
+    if (!encode_3d(&maps.kn, p.k_new, p.Hkv, krows, 1, BN)) return cudaErrorInvalidValue;
+    if (!encode_3d(&maps.vn, p.v_new, p.Hkv, krows, 1, BN)) return cudaErrorInvalidValue;
+  } else {
+    maps.kn = maps.q;  // never read: every sequence has N = 0
+    maps.vn = maps.q;
+  }
   if (p.total_cache > 0) {
     if (!encode_3d(&maps.kc, p.k_cache, p.Hkv, p.total_cache, 1, BN)) return cudaErrorInvalidValue;
     if (!encode_3d(&maps.vc, p.v_cache, p.Hkv, p.total_cache, 1, BN)) return cudaErrorInvalidValue;

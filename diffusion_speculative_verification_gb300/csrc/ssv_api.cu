@@ -91,6 +91,9 @@ AttnParams to_params(const ssv_attn_args* a) {
   const FaultSetting f = fault_for(SSV_FAULT_ATTN);
   p.wait_budget = f.budget;
   p.fault_skip = f.skip;
+  p.prompt_only = 0;
+  p.total_krows = a->total_rows;
+  p.lse = nullptr;
   return p;
 }
 

@@ -29,9 +29,11 @@
 // that (position, token) (lowest such edge), or emits the transition.
 #include "ssv_internal.cuh"
 #include "accept.cuh"
+#include "attn.cuh"
 
 #include <limits.h>
 #include <math.h>
+#include <string.h>
 
 namespace ssv {
 namespace {
@@ -57,6 +59,11 @@ struct TreeAttnParams {
   int total_q, total_k, total_cache, total_edges, total_out;
   int max_cache;
   int32_t* dev_status;
+  // when set: the prompt part of every query row already done (tensor-core
+  // prompt pass): normalised output [total_q][Hq][d] and its log2-sum-exp2
+  // [total_q][Hq] (scores scaled by scale * log2 e)
+  const float* pre_o;
+  const float* pre_lse;
 };
 
 // sequence whose rows [key(s), key(s) + span) hold `row` (sequences in increasing order)
@@ -292,63 +299,78 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
     load_lane<T, E>(Vn + off, vv);
   };
   const bool fresh = i < s.new_len;
-  // prompt keys: the cache, then the fresh prompt rows (all of them for a mask
-  // slot; up to the row itself for a fresh row), cut into kTreeWarps
-  // contiguous ranges, one per warp; the partial softmax states are then merged
   const int n_fresh = fresh ? i + 1 : s.new_len;
-  const int n_prompt = s.cache_len + n_fresh;
-  const int j_lo = (int)(((long long)n_prompt * wl) / kTreeWarps);
-  const int j_hi = (int)(((long long)n_prompt * (wl + 1)) / kTreeWarps);
-  auto key_prompt = [&](int j, float* kk, float* vv) {
-    if (j < s.cache_len) key_cache(j, kk, vv);
-    else key_new(j - s.cache_len, kk, vv);
-  };
-  int j = j_lo;
-  for (; j + 4 <= j_hi; j += 4) {
-    float kk[4][E], vv[4][E];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) key_prompt(j + k, kk[k], vv[k]);
-    add_keys4<E, GH>(st, q, kk, vv, gh);
-  }
-  for (; j < j_hi; ++j) {
-    float kk[E], vv[E];
-    key_prompt(j, kk, vv);
-    add_key<E, GH>(st, q, kk, vv, gh);
-  }
-  if (lane == 0) {
+  if (p.pre_o) {
+    // the prompt part from the prompt pass: the state (m = lse, l = 1, acc = O)
+    // continues the softmax exactly where that pass left it
+    const bool any = s.cache_len + n_fresh > 0;
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
-      s_ml[wl][0][h] = st.m[h];
-      s_ml[wl][1][h] = st.l[h];
+      if (h >= gh || !any) continue;
+      const size_t r = (size_t)qr * p.Hq + h0 + h;
+      st.m[h] = p.pre_lse[r];
+      st.l[h] = 1.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) st.acc[h][e] = p.pre_o[r * D + lane * E + e];
     }
-  }
+  } else {
+    // prompt keys: the cache, then the fresh prompt rows (all of them for a mask
+    // slot; up to the row itself for a fresh row), cut into kTreeWarps
+    // contiguous ranges, one per warp; the partial softmax states are then merged
+    const int n_prompt = s.cache_len + n_fresh;
+    const int j_lo = (int)(((long long)n_prompt * wl) / kTreeWarps);
+    const int j_hi = (int)(((long long)n_prompt * (wl + 1)) / kTreeWarps);
+    auto key_prompt = [&](int j, float* kk, float* vv) {
+      if (j < s.cache_len) key_cache(j, kk, vv);
+      else key_new(j - s.cache_len, kk, vv);
+    };
+    int j = j_lo;
+    for (; j + 4 <= j_hi; j += 4) {
+      float kk[4][E], vv[4][E];
 #pragma unroll
-  for (int h = 0; h < GH; ++h)
+      for (int k = 0; k < 4; ++k) key_prompt(j + k, kk[k], vv[k]);
+      add_keys4<E, GH>(st, q, kk, vv, gh);
+    }
+    for (; j < j_hi; ++j) {
+      float kk[E], vv[E];
+      key_prompt(j, kk, vv);
+      add_key<E, GH>(st, q, kk, vv, gh);
+    }
+    if (lane == 0) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) s_acc[wl][h][lane * E + e] = st.acc[h][e];
-  __syncthreads();
-  // every warp forms the merged state (the ranges in order; empty ones have max -inf)
-#pragma unroll
-  for (int h = 0; h < GH; ++h) {
-    float M = -INFINITY;
-    for (int u = 0; u < kTreeWarps; ++u) M = fmaxf(M, s_ml[u][0][h]);
-    float l = 0.f, acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    if (M > -INFINITY) {
-      for (int u = 0; u < kTreeWarps; ++u) {
-        const float mu = s_ml[u][0][h];
-        if (!(mu > -INFINITY)) continue;
-        const float f = exp2f(mu - M);
-        l = fmaf(s_ml[u][1][h], f, l);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(s_acc[u][h][lane * E + e], f, acc[e]);
+      for (int h = 0; h < GH; ++h) {
+        s_ml[wl][0][h] = st.m[h];
+        s_ml[wl][1][h] = st.l[h];
       }
     }
-    st.m[h] = M;
-    st.l[h] = l;
 #pragma unroll
-    for (int e = 0; e < E; ++e) st.acc[h][e] = acc[e];
+    for (int h = 0; h < GH; ++h)
+#pragma unroll
+      for (int e = 0; e < E; ++e) s_acc[wl][h][lane * E + e] = st.acc[h][e];
+    __syncthreads();
+    // every warp forms the merged state (the ranges in order; empty ones have max -inf)
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      float M = -INFINITY;
+      for (int u = 0; u < kTreeWarps; ++u) M = fmaxf(M, s_ml[u][0][h]);
+      float l = 0.f, acc[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = 0.f;
+      if (M > -INFINITY) {
+        for (int u = 0; u < kTreeWarps; ++u) {
+          const float mu = s_ml[u][0][h];
+          if (!(mu > -INFINITY)) continue;
+          const float f = exp2f(mu - M);
+          l = fmaf(s_ml[u][1][h], f, l);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = fmaf(s_acc[u][h][lane * E + e], f, acc[e]);
+        }
+      }
+      st.m[h] = M;
+      st.l[h] = l;
+#pragma unroll
+      for (int e = 0; e < E; ++e) st.acc[h][e] = acc[e];
+    }
   }
   if (fresh) {
     if (wl == 0) store_row<OutT, E, GH>(st, O + (size_t)(s.o_off + i) * p.Hq * D, h0, gh, lane);
@@ -373,6 +395,23 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
     }
     store_row<OutT, E, GH>(t, O + (size_t)(s.o_off + s.new_len + n * s.block + pp) * p.Hq * D, h0, gh, lane);
   }
+}
+
+// The prompt pass's sequence table: the tree sequence's cache, fresh prompt
+// rows and its B mask-slot query rows; its fresh keys start at k_off (carried
+// in tau_off, which a prompt-only pass reads in place of a stage map).
+__global__ void tree_prompt_seqs_kernel(const ssv_tree_seq* ts, ssv_seq* out, int batch) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const ssv_tree_seq t = ts[b];
+  ssv_seq o;
+  o.cache_len = t.cache_len;
+  o.new_len = t.new_len;
+  o.block = t.block;
+  o.q_off = t.q_off;
+  o.kv_off = t.kv_off;
+  o.tau_off = t.k_off;
+  out[b] = o;
 }
 
 template <typename T, typename OutT, int D, int GH>
@@ -585,7 +624,9 @@ __global__ void __launch_bounds__(32) tree_walk_kernel(const TreeAccParams p) {
 
 using namespace ssv;
 
-extern "C" ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* stream) {
+namespace {
+
+ssv_status tree_attn_check(const ssv_tree_attn_args* a) {
   if (!a) return SSV_ERR_INVALID;
   if (a->batch < 0 || a->total_q < 0 || a->total_k < 0 || a->total_cache < 0 || a->total_edges < 0 ||
       a->total_out < 0)
@@ -603,16 +644,111 @@ extern "C" ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* st
   const uintptr_t al = (uintptr_t)a->q | (uintptr_t)a->k_cache | (uintptr_t)a->v_cache | (uintptr_t)a->k_new |
                        (uintptr_t)a->v_new | (uintptr_t)a->o;
   if (al & 15u) return SSV_ERR_INVALID;
+  return SSV_OK;
+}
+
+float tree_scale(const ssv_tree_attn_args* a) {
+  return a->scale > 0.f ? a->scale : (float)(1.0 / sqrt((double)a->d));
+}
+
+// The prompt pass as a prompt-only verify-attention pass on the tensor cores:
+// its parameters (workspace pointers left for the caller), or false when the
+// shapes are outside that schedule (fp32 inputs, d = 64, ...).
+bool tree_prompt_params(const ssv_tree_attn_args* a, AttnParams& ap) {
+  if (a->in_dtype != SSV_BF16 || a->d != 128) return false;
+  memset(&ap, 0, sizeof(ap));
+  ap.q = a->q;
+  ap.k_cache = a->k_cache;
+  ap.v_cache = a->v_cache;
+  ap.k_new = a->k_new;
+  ap.v_new = a->v_new;
+  ap.in_dtype = SSV_BF16;
+  ap.out_dtype = SSV_F32;
+  ap.Hq = a->Hq;
+  ap.Hkv = a->Hkv;
+  ap.d = a->d;
+  ap.scale = tree_scale(a);
+  ap.batch = a->batch;
+  ap.tau = nullptr;
+  ap.total_rows = a->total_q;
+  ap.total_cache = a->total_cache;
+  ap.total_slots = 0;
+  ap.max_cache = a->max_cache;
+  ap.max_new = a->total_q;  // every N is below the query rows
+  ap.max_block = kTreeMaxB;
+  ap.dev_status = a->dev_status;
+  ap.early = 0;
+  ap.wait_budget = kDefaultWaitBudget;
+  ap.fault_skip = -1;
+  ap.prompt_only = 1;
+  ap.total_krows = a->total_k;
+  return tc::attn_tc_supported(ap);
+}
+
+struct TreeWs {
+  size_t attn, o, lse, seqs, total;
+};
+
+TreeWs tree_ws_layout(const ssv_tree_attn_args* a, const AttnParams& ap) {
+  TreeWs L;
+  size_t off = 0;
+  L.attn = off;
+  off = align_up(off + tc::attn_tc_workspace(ap), 256);
+  L.o = off;
+  off = align_up(off + sizeof(float) * (size_t)a->total_q * a->Hq * a->d, 256);
+  L.lse = off;
+  off = align_up(off + sizeof(float) * (size_t)a->total_q * a->Hq, 256);
+  L.seqs = off;
+  off = align_up(off + sizeof(ssv_seq) * (size_t)a->batch, 256);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" ssv_status ssv_tree_verify_attn_workspace(const ssv_tree_attn_args* a, size_t* bytes) {
+  if (!bytes) return SSV_ERR_INVALID;
+  const ssv_status v = tree_attn_check(a);
+  if (v != SSV_OK) return v;
+  *bytes = 0;
+  AttnParams ap;
+  if (a->batch > 0 && a->total_q > 0 && tree_prompt_params(a, ap)) *bytes = tree_ws_layout(a, ap).total;
+  return SSV_OK;
+}
+
+extern "C" ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const ssv_status v = tree_attn_check(a);
+  if (v != SSV_OK) return v;
+  if (a->batch == 0 || a->total_q == 0) return SSV_OK;
   TreeAttnParams p;
   p.q = a->q; p.k_cache = a->k_cache; p.v_cache = a->v_cache; p.k_new = a->k_new; p.v_new = a->v_new; p.o = a->o;
   p.Hq = a->Hq; p.Hkv = a->Hkv; p.d = a->d;
-  p.scale = a->scale > 0.f ? a->scale : (float)(1.0 / sqrt((double)a->d));
+  p.scale = tree_scale(a);
   p.seqs = a->seqs; p.batch = a->batch; p.parent = a->parent; p.pos = a->pos;
   p.total_q = a->total_q; p.total_k = a->total_k; p.total_cache = a->total_cache;
   p.total_edges = a->total_edges; p.total_out = a->total_out; p.max_cache = a->max_cache;
   p.dev_status = a->dev_status;
+  p.pre_o = nullptr;
+  p.pre_lse = nullptr;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
+  cudaError_t e = cudaSuccess;
+  AttnParams ap;
+  if (tree_prompt_params(a, ap)) {
+    // the prompt part of every query row on the tensor cores, then the nodes
+    const TreeWs L = tree_ws_layout(a, ap);
+    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
+    char* w = static_cast<char*>(ws);
+    ssv_seq* pseqs = reinterpret_cast<ssv_seq*>(w + L.seqs);
+    tree_prompt_seqs_kernel<<<(a->batch + 127) / 128, 128, 0, st>>>(a->seqs, pseqs, a->batch);
+    e = cudaGetLastError();
+    ap.seqs = pseqs;
+    ap.o = w + L.o;
+    ap.lse = reinterpret_cast<float*>(w + L.lse);
+    if (e == cudaSuccess) e = tc::launch_attn_tc(ap, w + L.attn, st);
+    p.pre_o = reinterpret_cast<const float*>(w + L.o);
+    p.pre_lse = reinterpret_cast<const float*>(w + L.lse);
+  }
+  if (e != cudaSuccess) return SSV_ERR_CUDA;
   const bool bf = a->in_dtype == SSV_BF16, obf = a->out_dtype == SSV_BF16;
   if (a->d == 128) {
     e = !bf ? launch_tree_attn_t<float, float, 128>(p, st)

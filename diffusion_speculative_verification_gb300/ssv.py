@@ -25,7 +25,8 @@ ARGMAX, GUMBEL, REJECT, GUMBEL_GEN = 0, 1, 2, 3
 EXPORTS = ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step", "ssv_accept_workspace",
            "ssv_accept", "ssv_accept_noalloc", "ssv_commit", "ssv_lmhead_accept_workspace", "ssv_lmhead_accept",
            "ssv_get_status", "ssv_status_string", "ssv_version", "ssv_bench", "ssv_set_fault_injection",
-           "ssv_tree_verify_attn", "ssv_tree_accept_workspace", "ssv_tree_accept", "ssv_stream_read")
+           "ssv_tree_verify_attn_workspace", "ssv_tree_verify_attn", "ssv_tree_accept_workspace", "ssv_tree_accept",
+           "ssv_stream_read")
 FAULT_NONE, FAULT_ATTN, FAULT_ACCEPT, FAULT_LMHEAD = 0, 1, 2, 3
 
 
@@ -135,14 +136,15 @@ def lib():
         L.ssv_bench.argtypes = [C.c_char_p, C.c_int32, C.c_char_p, sz]
         L.ssv_stream_read.argtypes = [vp, sz, vp, vp]
         L.ssv_set_fault_injection.argtypes = [C.POINTER(FaultInjection)]
-        L.ssv_tree_verify_attn.argtypes = [C.POINTER(TreeAttnArgs), vp]
+        L.ssv_tree_verify_attn_workspace.argtypes = [C.POINTER(TreeAttnArgs), C.POINTER(sz)]
+        L.ssv_tree_verify_attn.argtypes = [C.POINTER(TreeAttnArgs), vp, sz, vp]
         L.ssv_tree_accept_workspace.argtypes = [C.POINTER(TreeAcceptArgs), C.POINTER(sz)]
         L.ssv_tree_accept.argtypes = [C.POINTER(TreeAcceptArgs), vp, sz, vp]
         for name in ("ssv_rope_copy", "ssv_verify_attn_workspace", "ssv_verify_attn", "ssv_verify_step",
                      "ssv_accept_workspace", "ssv_accept", "ssv_accept_noalloc", "ssv_commit",
                      "ssv_lmhead_accept_workspace", "ssv_lmhead_accept", "ssv_get_status", "ssv_bench",
-                     "ssv_set_fault_injection", "ssv_tree_verify_attn", "ssv_tree_accept_workspace",
-                     "ssv_tree_accept", "ssv_stream_read"):
+                     "ssv_set_fault_injection", "ssv_tree_verify_attn_workspace", "ssv_tree_verify_attn",
+                     "ssv_tree_accept_workspace", "ssv_tree_accept", "ssv_stream_read"):
             getattr(L, name).restype = C.c_int
         _lib = L
     return _lib
@@ -415,16 +417,26 @@ def tree_attn_args(q, k_cache, v_cache, k_new, v_new, out, seqs, parent, pos, to
                         int(total_out), int(max_cache), _ptr(dev_status))
 
 
+def tree_verify_attn_workspace_bytes(args: TreeAttnArgs) -> int:
+    n = C.c_size_t(0)
+    _check(lib().ssv_tree_verify_attn_workspace(C.byref(args), C.byref(n)), "ssv_tree_verify_attn_workspace")
+    return n.value
+
+
 def tree_verify_attn(q, k_cache, v_cache, k_new, v_new, seqs, parent, pos, total_out, max_cache, out=None,
-                     out_dtype=None, scale: float = 0.0, dev_status=None, stream=None):
+                     out_dtype=None, scale: float = 0.0, dev_status=None, stream=None, workspace=None):
     """Attention of the tree pass; returns O [total_out, Hq, d] (rows of
-    committed positions are left as they were in `out`)."""
+    committed positions are left as they were in `out`).  workspace: a zeroed
+    uint8 device tensor of tree_verify_attn_workspace_bytes (allocated here
+    when not given)."""
     torch = _torch()
     if out is None:
         out = torch.zeros((int(total_out), q.shape[1], q.shape[2]), dtype=out_dtype or q.dtype, device=q.device)
     a = tree_attn_args(q, k_cache, v_cache, k_new, v_new, out, seqs, parent, pos, total_out, max_cache, scale,
                        dev_status)
-    _check(lib().ssv_tree_verify_attn(C.byref(a), _stream_ptr(stream)), "ssv_tree_verify_attn")
+    ws = _workspace(tree_verify_attn_workspace_bytes(a), q.device, workspace)
+    _check(lib().ssv_tree_verify_attn(C.byref(a), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+                                      _stream_ptr(stream)), "ssv_tree_verify_attn")
     return out
 
 

@@ -522,9 +522,19 @@ typedef struct {
  * [total_cache, Hkv, d] device, in_dtype (post-RoPE); o [total_out, Hq, d]
  * device, out_dtype.  parent, pos [total_edges] int32 device.  Sequences in
  * increasing q_off order.  d in {64, 128}, Hq % Hkv == 0, pointers 16-byte
- * aligned; max_cache bounds every C.  No workspace.  fp32 SIMT arithmetic.
- * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_CUDA; on device
- * SSV_ERR_INVALID (see above). */
+ * aligned; max_cache bounds every C.
+ * The part every row shares -- the prompt (cache + fresh rows), the same keys
+ * for a mask slot at every node -- is computed once per query row: for bf16
+ * inputs with d = 128 on the tensor cores (the verify attention's schedule
+ * in a prompt-only form, bf16 P and fp32 accumulation as there), which then
+ * leaves each row's normalised output and log-sum-exp in the workspace; a
+ * node kernel (fp32) continues that softmax over each node's tail keys.
+ * Other inputs run the prompt part in the node kernel itself (fp32 SIMT).
+ * Workspace: ssv_tree_verify_attn_workspace bytes (0 when the prompt part
+ * runs in fp32), 256-byte aligned, all-zero before its first use and left
+ * reusable (as for ssv_verify_attn).
+ * Errors: SSV_ERR_INVALID, SSV_ERR_UNSUPPORTED, SSV_ERR_WORKSPACE,
+ * SSV_ERR_CUDA; on device SSV_ERR_INVALID (see above). */
 typedef struct {
   const void* q;
   const void* k_cache;
@@ -545,7 +555,9 @@ typedef struct {
   int32_t* dev_status;         /* device, may be NULL */
 } ssv_tree_attn_args;
 
-SSV_API ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* stream);
+SSV_API ssv_status ssv_tree_verify_attn_workspace(const ssv_tree_attn_args* a, size_t* bytes);
+SSV_API ssv_status ssv_tree_verify_attn(const ssv_tree_attn_args* a, void* workspace, size_t workspace_bytes,
+                                        void* stream);
 
 /* ssv_tree_accept -- acceptance of the tree by state equality.
  * logits [total_out, V] device (row (n, p) of sequence b at o_off + N + n B + p,

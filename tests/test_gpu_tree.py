@@ -132,3 +132,23 @@ def test_tree_accept_rejects_bad_tree():
     good = W.make_tree_inputs("badacc", [5, 5], [0, 0], [4, 4], [3, 3], 2, 1, 64, W.F32, seed=920, V=100)
     r0 = otree.tree_accept_batch(good.mode, good.T, good.seqs, good.parent, good.pos, good.token, good.logits)[0]
     assert n_acc[0] == r0.n_acc and (ep[0], et[0]) == (r0.emit_pos, r0.emit_tok)
+
+
+def test_tree_attention_workspace_reuse():
+    """The tensor-core prompt pass leaves its workspace reusable: a second call
+    on the same workspace gives identical outputs."""
+    t = CASES["bf16_d128_g4"]()
+    d = sio.tree_to_device(t)
+    a = ssv.tree_attn_args(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"],
+                           torch.zeros((t.total_out, t.Hq, t.d), dtype=torch.bfloat16, device="cuda"), d["seqs"],
+                           d["parent"], d["pos"], t.total_out, d["max_cache"])
+    nbytes = ssv.tree_verify_attn_workspace_bytes(a)
+    assert nbytes > 0  # bf16, d = 128: the prompt pass runs on the tensor cores
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        o = torch.full((t.total_out, t.Hq, t.d), 7.0, dtype=torch.bfloat16, device="cuda")
+        ssv.tree_verify_attn(d["q"], d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], d["seqs"], d["parent"],
+                             d["pos"], t.total_out, d["max_cache"], out=o, workspace=ws)
+        outs.append(o.float().cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
