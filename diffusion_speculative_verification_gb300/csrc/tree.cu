@@ -93,21 +93,32 @@ __device__ __forceinline__ bool tree_seq_ok(const ssv_tree_seq& s, int total_q, 
 // commit a position in 0..B-1 still undecided there.
 __device__ __forceinline__ bool build_tree_masks(const ssv_tree_seq& s, const int32_t* parent, const int32_t* pos,
                                                  unsigned long long* cm, unsigned long long* pm) {
+  // every edge's (parent, position) loaded at once, two per lane (E <= 63)
+  const int lane = threadIdx.x & 31;
+  const int pa0 = lane < s.n_edges ? parent[s.edge_off + lane] : 0;
+  const int po0 = lane < s.n_edges ? pos[s.edge_off + lane] : 0;
+  const int pa1 = lane + 32 < s.n_edges ? parent[s.edge_off + lane + 32] : 0;
+  const int po1 = lane + 32 < s.n_edges ? pos[s.edge_off + lane + 32] : 0;
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
+  if (lane == 0) {
     cm[0] = 0ull;
     pm[0] = 0ull;
-    for (int e = 0; e < s.n_edges; ++e) {
-      const int par = parent[s.edge_off + e], p = pos[s.edge_off + e];
-      if (par < -1 || par >= e || p < 0 || p >= s.block || ((cm[par + 1] >> p) & 1ull)) {
-        ok = 0;
-        break;
-      }
-      cm[e + 1] = cm[par + 1] | (1ull << p);
+  }
+  __syncwarp();
+  for (int e = 0; e < s.n_edges; ++e) {  // warp-uniform walk; lane 0 writes
+    const int a0 = __shfl_sync(0xffffffffu, pa0, e & 31), a1 = __shfl_sync(0xffffffffu, pa1, e & 31);
+    const int b0 = __shfl_sync(0xffffffffu, po0, e & 31), b1 = __shfl_sync(0xffffffffu, po1, e & 31);
+    const int par = e < 32 ? a0 : a1, p = e < 32 ? b0 : b1;
+    if (par < -1 || par >= e || p < 0 || p >= s.block) { ok = 0; break; }
+    const unsigned long long c = cm[par + 1];
+    if ((c >> p) & 1ull) { ok = 0; break; }
+    __syncwarp();
+    if (lane == 0) {
+      cm[e + 1] = c | (1ull << p);
       pm[e + 1] = pm[par + 1] | (1ull << e);
     }
+    __syncwarp();
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
 }
@@ -172,14 +183,14 @@ __device__ __forceinline__ void add_key(RunState<E, GH>& st, const float (*q)[E]
   }
 }
 
-// Four keys at once into the running state: the four dot products reduce
-// across the warp side by side, and the state is rescaled once per four keys.
-template <int E, int GH>
+// NK keys at once into the running state: the NK dot products reduce across
+// the warp side by side, and the state is rescaled once per NK keys.
+template <int E, int GH, int NK = 4>
 __device__ __forceinline__ void add_keys4(RunState<E, GH>& st, const float (*q)[E], const float (*kk)[E],
                                           const float (*vv)[E], int gh) {
-  float sc[4][GH];
+  float sc[NK][GH];
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
+  for (int k = 0; k < NK; ++k)
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
       float part = 0.f;
@@ -192,23 +203,28 @@ __device__ __forceinline__ void add_keys4(RunState<E, GH>& st, const float (*q)[
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < NK; ++k)
 #pragma unroll
       for (int h = 0; h < GH; ++h) sc[k][h] += __shfl_xor_sync(0xffffffffu, sc[k][h], o);
 #pragma unroll
   for (int h = 0; h < GH; ++h) {
     if (h >= gh) continue;
-    const float mx = fmaxf(fmaxf(st.m[h], fmaxf(sc[0][h], sc[1][h])), fmaxf(sc[2][h], sc[3][h]));
-    const float corr = exp2f(st.m[h] - mx);
-    float pk[4];
+    float mx = st.m[h];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) pk[k] = exp2f(sc[k][h] - mx);
-    st.l[h] = st.l[h] * corr + ((pk[0] + pk[1]) + (pk[2] + pk[3]));
+    for (int k = 0; k < NK; ++k) mx = fmaxf(mx, sc[k][h]);
+    const float corr = exp2f(st.m[h] - mx);
+    float pk[NK], ps = 0.f;
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+      pk[k] = exp2f(sc[k][h] - mx);
+      ps += pk[k];
+    }
+    st.l[h] = st.l[h] * corr + ps;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       float a = st.acc[h][e] * corr;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) a = fmaf(pk[k], vv[k][e], a);
+      for (int k = 0; k < NK; ++k) a = fmaf(pk[k], vv[k][e], a);
       st.acc[h][e] = a;
     }
     st.m[h] = mx;
@@ -234,6 +250,7 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
   __shared__ float s_ml[kTreeWarps][2][GH];       // each warp's running max and sum per head
   __shared__ float s_acc[kTreeWarps][GH][D];      // and its unnormalised output
   __shared__ int s_ok;
+  __shared__ int s_keys[kTreeWarps][kTreeMaxE + kTreeMaxB];  // a node's tail-key rows, per warp
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int G = p.Hq / p.Hkv;
   const int nhc = (G + GH - 1) / GH;
@@ -380,19 +397,33 @@ __global__ void __launch_bounds__(kTreeWarps * 32) tree_attn_kernel(const TreeAt
   // the prompt state over the node's tail keys; nodes dealt to the warps in turn
   const int pp = i - s.new_len;  // position of this mask slot
   const unsigned long long full = (s.block >= 64) ? ~0ull : ((1ull << s.block) - 1ull);
+  int* klist = s_keys[wl];
   for (int n = wl; n <= s.n_edges; n += kTreeWarps) {
     if ((cm[n] >> pp) & 1ull) continue;  // committed at n: no row
+    // the node's tail keys (rows of the sequence's new keys): the data rows of
+    // the path's edges, then the mask rows of the positions undecided at n
+    int cnt = 0;
+    if (lane == 0) {
+      for (unsigned long long m = pm[n]; m; m &= m - 1) klist[cnt++] = s.new_len + __ffsll((long long)m) - 1;
+      for (unsigned long long m = full & ~cm[n]; m; m &= m - 1)
+        klist[cnt++] = s.new_len + s.n_edges + __ffsll((long long)m) - 1;
+    }
+    cnt = __shfl_sync(0xffffffffu, cnt, 0);
+    __syncwarp();
     RunState<E, GH> t = st;
-    for (unsigned long long m = pm[n]; m; m &= m - 1) {  // data rows of the path's edges
+    int k = 0;
+    for (; k + 4 <= cnt; k += 4) {  // four keys' loads in flight at once
+      float kk[4][E], vv[4][E];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) key_new(klist[k + u], kk[u], vv[u]);
+      add_keys4<E, GH>(t, q, kk, vv, gh);
+    }
+    for (; k < cnt; ++k) {
       float kk[E], vv[E];
-      key_new(s.new_len + __ffsll((long long)m) - 1, kk, vv);
+      key_new(klist[k], kk, vv);
       add_key<E, GH>(t, q, kk, vv, gh);
     }
-    for (unsigned long long m = full & ~cm[n]; m; m &= m - 1) {  // mask rows of undecided positions
-      float kk[E], vv[E];
-      key_new(s.new_len + s.n_edges + __ffsll((long long)m) - 1, kk, vv);
-      add_key<E, GH>(t, q, kk, vv, gh);
-    }
+    __syncwarp();  // the list is rewritten for the warp's next node
     store_row<OutT, E, GH>(t, O + (size_t)(s.o_off + s.new_len + n * s.block + pp) * p.Hq * D, h0, gh, lane);
   }
 }
