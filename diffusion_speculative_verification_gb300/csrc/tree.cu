@@ -489,6 +489,12 @@ struct TreeAccParams {
   int32_t* emit_tok;
   int32_t* dev_status;
   AccPartial* part;  // [total_out][nchunks]
+  int vec;           // rows (logits and noise) allow 16-byte loads of 8-entry runs
+  struct RowConf {
+    double conf;     // log-probability of the decision under softmax(l)
+    int dec;         // the decision token, -1 if none
+    int pad;
+  }* rowconf;        // [total_out]
 };
 
 constexpr int kTrThreads = 256;
@@ -518,19 +524,47 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
   const int c0 = chunk * kAccChunk;
   float best = -INFINITY, mx = -INFINITY;
   int bi = INT_MAX;
-  float xs[kAccChunk / kTrThreads];
+  constexpr int kRuns = kAccChunk / kTrThreads / 8;  // runs of 8 consecutive entries per thread
+  float xs[kRuns * 8];
 #pragma unroll
-  for (int k = 0; k < kAccChunk / kTrThreads; ++k) {
-    const int e = c0 + k * kTrThreads + threadIdx.x;
-    float x = -INFINITY;
-    if (e < p.V) {
-      x = Elem<T>::to_f32(lrow[e]);
-      float sc = x;
-      if (MODE == SSV_ACCEPT_GUMBEL) sc = __fadd_rn(__fdiv_rn(x, p.T), nrow[e]);
-      if (sc > best || bi == INT_MAX) { best = sc; bi = e; }
+  for (int g = 0; g < kRuns; ++g) {
+    const int e0 = c0 + 8 * (g * kTrThreads + (int)threadIdx.x);
+    float x8[8], n8[8];
+    if (p.vec && e0 + 8 <= p.V) {  // 16-byte loads
+      if constexpr (sizeof(T) == 2) {
+        const uint4 u = *reinterpret_cast<const uint4*>(lrow + e0);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x8[2 * j] = __uint_as_float(w[j] << 16);
+          x8[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        }
+      } else {
+        const float4 a = *reinterpret_cast<const float4*>(lrow + e0), c = *reinterpret_cast<const float4*>(lrow + e0 + 4);
+        x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w; x8[4] = c.x; x8[5] = c.y; x8[6] = c.z; x8[7] = c.w;
+      }
+      if (MODE == SSV_ACCEPT_GUMBEL) {
+        const float4 a = *reinterpret_cast<const float4*>(nrow + e0), c = *reinterpret_cast<const float4*>(nrow + e0 + 4);
+        n8[0] = a.x; n8[1] = a.y; n8[2] = a.z; n8[3] = a.w; n8[4] = c.x; n8[5] = c.y; n8[6] = c.z; n8[7] = c.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        x8[j] = (e0 + j < p.V) ? Elem<T>::to_f32(lrow[e0 + j]) : -INFINITY;
+        n8[j] = (MODE == SSV_ACCEPT_GUMBEL && e0 + j < p.V) ? nrow[e0 + j] : 0.f;
+      }
     }
-    xs[k] = x;
-    mx = fmaxf(mx, x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x = x8[j];
+      if (e0 + j < p.V) {
+        float sc = x;
+        if (MODE == SSV_ACCEPT_GUMBEL) sc = __fadd_rn(__fdiv_rn(x, p.T), n8[j]);
+        if (sc > best || bi == INT_MAX) { best = sc; bi = e0 + j; }
+      }
+      xs[g * 8 + j] = x;
+      mx = fmaxf(mx, x);
+    }
   }
   // chunk max, then the compensated sum of 2^((x - max) c2)
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -543,7 +577,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
   const float nm = (cm == -INFINITY) ? 0.f : -cm * p.c2;
   float sh = 0.f, sl = 0.f;
 #pragma unroll
-  for (int k = 0; k < kAccChunk / kTrThreads; ++k) kahan_add(sh, sl, ex2f(fmaf(xs[k], p.c2, nm)));
+  for (int k = 0; k < kRuns * 8; ++k) kahan_add(sh, sl, ex2f(fmaf(xs[k], p.c2, nm)));
   sl = -sl;
   warp_sum2(sh, sl);
   warp_argmax(best, bi);
@@ -560,6 +594,48 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
     r.val = best; r.idx = bi;
     p.part[(size_t)row * p.nchunks + chunk] = r;
   }
+}
+
+// Every output row's decision and confidence from its chunk records, one
+// thread per row, all rows at once (the walk then only compares them).
+template <int MODE, typename T>
+__global__ void __launch_bounds__(128) tree_rowconf_kernel(const TreeAccParams p) {
+  pdl_wait();  // the chunk records
+  pdl_trigger();
+  const int row = blockIdx.x * 128 + threadIdx.x;
+  if (row >= p.total_out) return;
+  const int b = find_tree_seq(p.seqs, p.batch, row, [](const ssv_tree_seq& s) { return s.o_off; });
+  if (b < 0) return;
+  const ssv_tree_seq s = p.seqs[b];
+  const int li = row - s.o_off - s.new_len;
+  if (s.block < 1 || s.block > kTreeMaxB || li < 0 || li >= (s.n_edges + 1) * s.block) return;
+  const AccPartial* pr = p.part + (size_t)row * p.nchunks;
+  float v = -INFINITY;
+  int idx = INT_MAX;
+  double M = -INFINITY;
+  for (int c = 0; c < p.nchunks; ++c) {
+    argmax_combine(v, idx, __ldcg(&pr[c].val), __ldcg(&pr[c].idx));
+    M = fmax(M, (double)__ldcg(&pr[c].m_a));
+  }
+  const double c2 = (double)p.c2;
+  double S = 0.0;
+  for (int c = 0; c < p.nchunks; ++c) {
+    const double cmx = __ldcg(&pr[c].m_a);
+    if (cmx == -INFINITY) continue;
+    const double cs = (double)__ldcg(&pr[c].sa_hi) + (double)__ldcg(&pr[c].sa_lo);
+    S += cs * (double)exp2f((float)((cmx - M) * c2));
+  }
+  TreeAccParams::RowConf rc;
+  rc.dec = -1;
+  rc.conf = -INFINITY;
+  rc.pad = 0;
+  if (idx != INT_MAX) {
+    const double ld = (MODE == SSV_ACCEPT_GUMBEL) ? (double)Elem<T>::to_f32(static_cast<const T*>(p.logits)[(size_t)row * p.V + idx])
+                                                  : (double)v;
+    rc.conf = (ld - M) - log(S);  // S = sum e^(l - M)
+    rc.dec = idx;
+  }
+  p.rowconf[row] = rc;
 }
 
 template <int MODE, typename T>
@@ -585,7 +661,6 @@ __global__ void __launch_bounds__(32) tree_walk_kernel(const TreeAccParams p) {
     return;
   }
   const unsigned long long full = (s.block >= 64) ? ~0ull : ((1ull << s.block) - 1ull);
-  const double c2 = (double)p.c2;
   int n = 0, acc = 0, epos = -1, etok = -1;
   while (true) {
     const unsigned long long und = full & ~s_cm[n];
@@ -598,27 +673,10 @@ __global__ void __launch_bounds__(32) tree_walk_kernel(const TreeAccParams p) {
       const int pp = lane + 32 * hpos;
       if (pp >= s.block || !((und >> pp) & 1ull)) continue;
       const size_t row = (size_t)s.o_off + s.new_len + (size_t)n * s.block + pp;
-      const AccPartial* pr = p.part + row * p.nchunks;
-      float v = -INFINITY;
-      int idx = INT_MAX;
-      double M = -INFINITY;
-      for (int c = 0; c < p.nchunks; ++c) {
-        argmax_combine(v, idx, __ldcg(&pr[c].val), __ldcg(&pr[c].idx));
-        M = fmax(M, (double)__ldcg(&pr[c].m_a));
-      }
-      double S = 0.0;
-      for (int c = 0; c < p.nchunks; ++c) {
-        const double cmx = __ldcg(&pr[c].m_a);
-        if (cmx == -INFINITY) continue;
-        const double cs = (double)__ldcg(&pr[c].sa_hi) + (double)__ldcg(&pr[c].sa_lo);
-        S += cs * (double)exp2f((float)((cmx - M) * c2));
-      }
-      if (idx == INT_MAX) continue;
-      const double ld = (MODE == SSV_ACCEPT_GUMBEL) ? (double)Elem<T>::to_f32(static_cast<const T*>(p.logits)[row * p.V + idx])
-                                                    : (double)v;
-      // confidence: log-probability of the decision under softmax(l) (S = sum e^(l - M))
-      const double conf = (ld - M) - log(S);
-      if (conf > best_c || (conf == best_c && pp < best_p)) { best_c = conf; best_p = pp; best_t = idx; }
+      const int dec = __ldcg(&p.rowconf[row].dec);
+      if (dec < 0) continue;
+      const double conf = __ldcg(&p.rowconf[row].conf);  // log-probability of the decision under softmax(l)
+      if (conf > best_c || (conf == best_c && pp < best_p)) { best_c = conf; best_p = pp; best_t = dec; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -814,7 +872,8 @@ extern "C" ssv_status ssv_tree_accept_workspace(const ssv_tree_accept_args* a, s
   int nchunks = 0;
   const ssv_status st = tree_accept_check(a, &nchunks);
   if (st != SSV_OK) return st;
-  *bytes = align_up(sizeof(AccPartial) * (size_t)a->total_out * nchunks + 256, 256);
+  *bytes = align_up(sizeof(AccPartial) * (size_t)a->total_out * nchunks, 256) +
+           align_up(sizeof(TreeAccParams::RowConf) * (size_t)a->total_out + 256, 256);
   return SSV_OK;
 }
 
@@ -842,6 +901,14 @@ extern "C" ssv_status ssv_tree_accept(const ssv_tree_accept_args* a, void* ws, s
   p.n_acc = a->n_acc; p.path = a->path; p.emit_pos = a->emit_pos; p.emit_tok = a->emit_tok;
   p.dev_status = a->dev_status;
   p.part = static_cast<AccPartial*>(ws);
+  p.rowconf = reinterpret_cast<TreeAccParams::RowConf*>(static_cast<char*>(ws) +
+                                                        align_up(sizeof(AccPartial) * (size_t)a->total_out * nchunks, 256));
+  {
+    const size_t es = a->logits_dtype == SSV_BF16 ? 2 : 4;
+    bool v = ((size_t)a->V * es) % 16 == 0 && ((uintptr_t)a->logits & 15u) == 0;
+    if (mode == SSV_ACCEPT_GUMBEL) v = v && ((size_t)a->V * 4) % 16 == 0 && ((uintptr_t)a->noise & 15u) == 0;
+    p.vec = v ? 1 : 0;
+  }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long long g1 = (long long)a->total_out * nchunks;
   if (g1 > 0x7fffffffLL) return SSV_ERR_INVALID;
@@ -857,6 +924,15 @@ extern "C" ssv_status ssv_tree_accept(const ssv_tree_accept_args* a, void* ws, s
       else tree_reduce_kernel<SSV_ACCEPT_ARGMAX, float><<<(unsigned)g1, kTrThreads, 0, s>>>(pr);
     }
     e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && a->total_out > 0) {
+    const dim3 gr((unsigned)((a->total_out + 127) / 128));
+    if (mode == SSV_ACCEPT_GUMBEL)
+      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, __nv_bfloat16>, gr, dim3(128), 0, s, p)
+             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, float>, gr, dim3(128), 0, s, p);
+    else
+      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, __nv_bfloat16>, gr, dim3(128), 0, s, p)
+             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, float>, gr, dim3(128), 0, s, p);
   }
   if (e == cudaSuccess) {
     if (mode == SSV_ACCEPT_GUMBEL)
