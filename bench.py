@@ -123,13 +123,16 @@ def kernel_launches(x) -> int:
 
 KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel",
                 "commit": "commit_kernel", "lmhead": "lmhead_accept_kernel"}
-KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh"],
-                  "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh"],
-                  "accept_reduce_kernel": ["accept.cu", "accept.cuh"],
-                  "accept_sample_kernel": ["accept.cu", "accept.cuh"], "rope_copy_kernel": ["rope.cu"],
+KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh", "ssv_internal.cuh"],
+                  "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh", "noisegen.cuh"],
+                  "accept_reduce_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
+                  "accept_sample_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
+                  "accept_emit_norm_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
+                  "rope_copy_kernel": ["rope.cu"],
                   "commit_kernel": ["commit.cu"],
                   "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"],
-                  "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"]}
+                  "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"],
+                  "tree_attn_kernel": ["tree.cu", "accept.cuh"], "tree_reduce_kernel": ["tree.cu", "accept.cuh"]}
 
 
 def measured_traffic(op: str, workload: str):
