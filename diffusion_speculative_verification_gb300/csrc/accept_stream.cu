@@ -15,7 +15,10 @@
 //   warp 16      producer (one lane): bulk-copies each unit's rows into the
 //                next free stage (cp.async.bulk, completion on an mbarrier);
 //   warp 17      publisher: merges the 16 warp records of a unit into its
-//                AccPartial and runs the row-merge / sequence-walk steps.
+//                AccPartial; under rejection sampling it also runs the
+//                row-merge / sequence-walk steps (the decision modes leave
+//                them to accept_finish_kernel, one CTA per sequence after
+//                the stream).
 // The ring keeps 128 to 192 KB of loads in flight per SM; no CTA-wide
 // barrier is taken once the list is built.  Every mbarrier wait is bounded:
 // on timeout the CTA raises SSV_ERR_TIMEOUT, the producer still waits
@@ -429,8 +432,12 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     return;
   }
 
-  // ---- publisher warp
-  // completion of `add` records of row `slot`, with the metadata from shared memory
+  // ---- publisher warp: the unit's record.  Decisions (greedy, coupled noise):
+  // the rows are merged and the sequences walked by accept_finish_kernel once
+  // every record is written.  Rejection sampling: the CTA that brings a row's
+  // last record merges it and the one that merges a sequence's last row walks
+  // it, here (those merges, with their draft-logit reads, overlap the stream).
+  constexpr bool kInline = MODE == SSV_ACCEPT_REJECT;
   auto rows_done = [&](int slot, int add) {
     const int b = seq_of_slot(sh, p.batch, slot);
     warp_rows_done<MODE, T>(p, b, slot, add, sh.stage[slot], sh.off[b], sh.blk[b], sh.gam[b], sh.walk, sh.stage);
@@ -468,15 +475,62 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
     const int slot = sh.list[row] & 0x7fffffff;
     if (lane == 0) p.part[(size_t)slot * p.nchunks + chunk] = x;
-    if (row != cur_row) {
-      if (pend) rows_done(cur_slot, pend);
-      cur_row = row;
-      cur_slot = slot;
-      pend = 0;
+    if constexpr (kInline) {
+      if (row != cur_row) {
+        if (pend) rows_done(cur_slot, pend);
+        cur_row = row;
+        cur_slot = slot;
+        pend = 0;
+      }
+      ++pend;
     }
-    ++pend;
   }
-  if (clean && pend) rows_done(cur_slot, pend);
+  if constexpr (kInline) {
+    if (clean && pend) rows_done(cur_slot, pend);
+  }
+}
+
+// Completion of the streaming pass for the decision modes (greedy, coupled
+// noise), one CTA per sequence, launched as its programmatic dependent (every
+// chunk record is written once the streaming grid has completed): each warp
+// merges verified rows of the sequence (first argmax over the chunks), then
+// warp 0 walks the stages.  A sequence the streaming pass rejected (sizes, stage
+// map, coupled-noise rows) has no records: it is skipped here too.
+constexpr int kFinWarps = 16;
+
+template <int MODE, typename T>
+__global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const AcceptParams p) {
+  __shared__ WalkSmem walk;
+  __shared__ int s_ok;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (warp == 0) {
+    bool ok = warp_seq_valid(p, b);
+    if (ok && MODE == SSV_ACCEPT_GUMBEL) {
+      const int off = p.slot_off[b], B = p.block[b], need = min(p.gamma[b] + 1, B);
+      bool bad = false;
+      for (int j = lane; j < B; j += 32) {
+        const int st = p.tau[off + j];
+        if (st >= 1 && st <= need) {
+          const int nr = p.noise_row[off + j];
+          bad = bad || nr < 0 || nr >= p.n_noise_rows;
+        }
+      }
+      ok = !__any_sync(0xffffffffu, bad);
+    }
+    if (lane == 0) s_ok = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b], need = min(g + 1, B);
+  for (int j = warp; j < B; j += kFinWarps) {  // warp-uniform
+    const int st = p.tau[off + j];
+    if (st >= 1 && st <= need) warp_row_merge<MODE, T>(p, off + j, st, g);
+  }
+  __syncthreads();  // every row result of the sequence written
+  if (warp == 0) warp_seq_walk<MODE>(p, b, off, B, g, walk, nullptr);
 }
 
 int device_sm_count() {
@@ -500,7 +554,9 @@ cudaError_t launch_t(const AcceptParams& p, cudaStream_t st) {
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(units < sms ? units : sms);
-  return launch_pdl(accept_stream_kernel<MODE, T>, dim3(grid), dim3(kStrThreads), C::kSmem, st, p);
+  const cudaError_t e = launch_pdl(accept_stream_kernel<MODE, T>, dim3(grid), dim3(kStrThreads), C::kSmem, st, p);
+  if (e != cudaSuccess || p.batch == 0 || MODE == SSV_ACCEPT_REJECT) return e;
+  return launch_pdl(accept_finish_kernel<MODE, T>, dim3(p.batch), dim3(kFinWarps * 32), 0, st, p);
 }
 
 }  // namespace
