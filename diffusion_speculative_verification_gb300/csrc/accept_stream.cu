@@ -15,10 +15,11 @@
 //   warp 16      producer (one lane): bulk-copies each unit's rows into the
 //                next free stage (cp.async.bulk, completion on an mbarrier);
 //   warp 17      publisher: merges the 16 warp records of a unit into its
-//                AccPartial; under rejection sampling it also runs the
-//                row-merge / sequence-walk steps (the decision modes leave
-//                them to accept_finish_kernel, one CTA per sequence after
-//                the stream).
+//                AccPartial.  The row merges and sequence walks follow the
+//                stream as programmatic dependents: accept_finish_kernel (one
+//                CTA per sequence) for the decision modes; for rejection
+//                sampling accept_rowmerge_kernel (a warp per slot, all rows
+//                at once) and accept_walk_kernel (a warp per sequence).
 // The ring keeps 128 to 192 KB of loads in flight per SM; no CTA-wide
 // barrier is taken once the list is built.  Every mbarrier wait is bounded:
 // on timeout the CTA raises SSV_ERR_TIMEOUT, the producer still waits
@@ -71,7 +72,6 @@ struct StrShared {
   unsigned char gam[kStrMaxRows];      // gamma
   unsigned char stage[kStrMaxRows];    // tau per slot (0 when outside 1..64)
   unsigned char seq_ok[kStrMaxRows];
-  WalkSmem walk;
   int wcount[kStrWarps];
   int abort;
 };
@@ -432,22 +432,12 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     return;
   }
 
-  // ---- publisher warp: the unit's record.  Decisions (greedy, coupled noise):
-  // the rows are merged and the sequences walked by accept_finish_kernel once
-  // every record is written.  Rejection sampling: the CTA that brings a row's
-  // last record merges it and the one that merges a sequence's last row walks
-  // it, here (those merges, with their draft-logit reads, overlap the stream).
-  constexpr bool kInline = MODE == SSV_ACCEPT_REJECT;
-  auto rows_done = [&](int slot, int add) {
-    const int b = seq_of_slot(sh, p.batch, slot);
-    warp_rows_done<MODE, T>(p, b, slot, add, sh.stage[slot], sh.off[b], sh.blk[b], sh.gam[b], sh.walk, sh.stage);
-  };
-  int cur_row = -1, cur_slot = 0, pend = 0;
-  bool clean = true;
+  // ---- publisher warp: the unit's record; the rows are merged and the
+  // sequences walked by the completion kernels once every record is written.
   for (int k = 0; k < n; ++k) {
     const int rs = k % kStrRecRing;
     const bool got = mbar_wait(smem_u32(&sh.rec_full[rs]), (k / kStrRecRing) & 1, &sh.abort, p.wait_budget);
-    if (!__all_sync(0xffffffffu, got)) { clean = false; break; }
+    if (!__all_sync(0xffffffffu, got)) break;
     AccPartial x;
     if (lane < kStrConsumerWarps) {
       x = sh.rec[rs][lane];
@@ -475,18 +465,6 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
     const int slot = sh.list[row] & 0x7fffffff;
     if (lane == 0) p.part[(size_t)slot * p.nchunks + chunk] = x;
-    if constexpr (kInline) {
-      if (row != cur_row) {
-        if (pend) rows_done(cur_slot, pend);
-        cur_row = row;
-        cur_slot = slot;
-        pend = 0;
-      }
-      ++pend;
-    }
-  }
-  if constexpr (kInline) {
-    if (clean && pend) rows_done(cur_slot, pend);
   }
 }
 
@@ -533,6 +511,35 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const Acc
   if (warp == 0) warp_seq_walk<MODE>(p, b, off, B, g, walk, nullptr);
 }
 
+// Completion under rejection sampling, where a row merge also reads the
+// draft token's two logits and forms the normalisers: every verified row of
+// every sequence at once (one warp per slot), then one warp per sequence walks.
+constexpr int kMergeWarps = 16;
+
+template <int MODE, typename T>
+__global__ void __launch_bounds__(kMergeWarps * 32) accept_rowmerge_kernel(const AcceptParams p) {
+  pdl_wait();  // every chunk record of the streaming pass
+  pdl_trigger();
+  const int slot = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  if (slot >= p.total_slots) return;
+  const int b = find_seq_by_slot(p.slot_off, p.batch, slot);
+  if (b < 0 || !warp_seq_valid(p, b)) return;
+  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
+  if (slot >= off + B) return;
+  const int st = p.tau[slot];
+  if (st >= 1 && st <= min(g + 1, B)) warp_row_merge<MODE, T>(p, slot, st, g);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(32) accept_walk_kernel(const AcceptParams p) {
+  __shared__ WalkSmem walk;
+  pdl_wait();  // every row result
+  pdl_trigger();
+  const int b = blockIdx.x;
+  if (!warp_seq_valid(p, b)) return;
+  warp_seq_walk<MODE>(p, b, p.slot_off[b], p.block[b], p.gamma[b], walk, nullptr);
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -554,9 +561,14 @@ cudaError_t launch_t(const AcceptParams& p, cudaStream_t st) {
   const int sms = device_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(units < sms ? units : sms);
-  const cudaError_t e = launch_pdl(accept_stream_kernel<MODE, T>, dim3(grid), dim3(kStrThreads), C::kSmem, st, p);
-  if (e != cudaSuccess || p.batch == 0 || MODE == SSV_ACCEPT_REJECT) return e;
-  return launch_pdl(accept_finish_kernel<MODE, T>, dim3(p.batch), dim3(kFinWarps * 32), 0, st, p);
+  cudaError_t e = launch_pdl(accept_stream_kernel<MODE, T>, dim3(grid), dim3(kStrThreads), C::kSmem, st, p);
+  if (e != cudaSuccess || p.batch == 0) return e;
+  if (MODE != SSV_ACCEPT_REJECT)
+    return launch_pdl(accept_finish_kernel<MODE, T>, dim3(p.batch), dim3(kFinWarps * 32), 0, st, p);
+  e = launch_pdl(accept_rowmerge_kernel<MODE, T>, dim3((p.total_slots + kMergeWarps - 1) / kMergeWarps),
+                 dim3(kMergeWarps * 32), 0, st, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(accept_walk_kernel<MODE>, dim3(p.batch), dim3(32), 0, st, p);
 }
 
 }  // namespace
