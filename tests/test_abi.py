@@ -160,3 +160,23 @@ def test_lmhead_validation(L):
         assert L.ssv_lmhead_accept_workspace(C.byref(_lmh(**kw)), C.byref(n)) == code, kw
     assert L.ssv_lmhead_accept(C.byref(_lmh(batch=0)), None, 0, None) == ssv.SSV_OK
     assert L.ssv_lmhead_accept_workspace(C.byref(_lmh(total_slots=0)), C.byref(n)) == ssv.SSV_OK and n.value == 0
+
+
+def test_stream_read_rejects_bad_arguments(L):
+    """The read-floor reference validates its arguments on the host."""
+    out = 1 << 20
+    assert L.ssv_stream_read(None, 64, out, None) == ssv.SSV_ERR_INVALID
+    assert L.ssv_stream_read(1 << 20, 64, None, None) == ssv.SSV_ERR_INVALID
+    assert L.ssv_stream_read((1 << 20) + 8, 64, out, None) == ssv.SSV_ERR_INVALID  # misaligned
+    assert L.ssv_stream_read(1 << 20, 40, out, None) == ssv.SSV_ERR_INVALID        # not a multiple of 16
+    assert L.ssv_stream_read(1 << 20, 0, out, None) == ssv.SSV_OK                  # nothing to read
+
+
+def test_tree_attention_workspace_query(L):
+    """fp32 inputs run the prompt part in the node kernel: no workspace."""
+    a = ssv.TreeAttnArgs(1 << 20, 1 << 21, 1 << 22, 1 << 23, 1 << 24, 1 << 25, ssv.SSV_F32, ssv.SSV_F32, 4, 2, 64, 0.0,
+                         1 << 26, 1, 1 << 27, 1 << 28, 8, 12, 16, 2, 40, 16, None)
+    n = C.c_size_t(7)
+    assert L.ssv_tree_verify_attn_workspace(C.byref(a), C.byref(n)) == ssv.SSV_OK
+    assert n.value == 0
+    assert L.ssv_tree_verify_attn_workspace(C.byref(a), None) == ssv.SSV_ERR_INVALID
