@@ -22,7 +22,7 @@ struct RopeTheta {
   double theta[64];  // theta_i = base^(-2i/d), i < d/2
 };
 
-constexpr int kRopeRows = 4;
+constexpr int kRopeRows = 4;  // rows per CTA (one when that leaves most SMs idle)
 constexpr int kRopeThreads = 256;
 
 template <typename T> struct Vec16;
@@ -68,7 +68,7 @@ __device__ __forceinline__ void store16(T* p, const float* v) {
   *reinterpret_cast<uint4*>(p) = raw;
 }
 
-template <typename T, int D>
+template <typename T, int D, int ROWS>
 __global__ void __launch_bounds__(kRopeThreads, 4)  // four CTAs per SM: a whole decode batch in one wave
 rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_out, T* k_out,
                  int Hq, int Hkv, const ssv_seq* __restrict__ seqs, int batch, int total_rows,
@@ -78,16 +78,16 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   constexpr int VEC = Vec16<T>::N;
   constexpr int CHUNKS = HALF / VEC;
   constexpr int PRE = 5;  // items per thread loaded before the positions are known (all of them up to 40 heads)
-  __shared__ float s_cos[kRopeRows][HALF];
-  __shared__ float s_sin[kRopeRows][HALF];
-  __shared__ int s_pos[kRopeRows];
+  __shared__ float s_cos[ROWS][HALF];
+  __shared__ float s_sin[ROWS][HALF];
+  __shared__ int s_pos[ROWS];
   __shared__ ssv_seq s_seq[kRopeThreads];
 
   pdl_wait();  // Q and K come from the preceding kernel
   pdl_trigger();  // dependents start only once every kernel before this one is complete
-  const int row0 = blockIdx.x * kRopeRows;
+  const int row0 = blockIdx.x * ROWS;
   const int heads = Hq + Hkv;
-  const int items = kRopeRows * heads * CHUNKS;
+  const int items = ROWS * heads * CHUNKS;
   auto item_ptrs = [&](int it, const T*& src, T*& dst, int& lr, int& ch) -> bool {
     ch = it % CHUNKS;
     const int hh = (it / CHUNKS) % heads;
@@ -120,7 +120,7 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   const bool table = batch <= kRopeThreads;
   if (table && threadIdx.x < batch) s_seq[threadIdx.x] = seqs[threadIdx.x];
   __syncthreads();
-  if (threadIdx.x < kRopeRows) {
+  if (threadIdx.x < ROWS) {
     const int row = row0 + threadIdx.x;
     int pos = -1;
     if (row < total_rows) {
@@ -162,7 +162,7 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
     s_pos[threadIdx.x] = pos;
   }
   __syncthreads();
-  for (int t = threadIdx.x; t < kRopeRows * HALF; t += blockDim.x) {
+  for (int t = threadIdx.x; t < ROWS * HALF; t += blockDim.x) {
     const int lr = t / HALF, i = t % HALF;
     const int pos = s_pos[lr];
     float c = 1.f, s = 0.f;
@@ -215,13 +215,24 @@ rope_copy_kernel(const T* __restrict__ q_in, const T* __restrict__ k_in, T* q_ou
   }
 }
 
-template <typename T, int D>
-static cudaError_t launch_rope(const ssv_rope_args* a, const RopeTheta& th, cudaStream_t st) {
-  const int grid = (a->total_rows + kRopeRows - 1) / kRopeRows;
-  return launch_pdl(rope_copy_kernel<T, D>, dim3(grid), dim3(kRopeThreads), 0, st,
+template <typename T, int D, int ROWS>
+static cudaError_t launch_rope_rows(const ssv_rope_args* a, const RopeTheta& th, cudaStream_t st) {
+  const int grid = (a->total_rows + ROWS - 1) / ROWS;
+  return launch_pdl(rope_copy_kernel<T, D, ROWS>, dim3(grid), dim3(kRopeThreads), 0, st,
                     static_cast<const T*>(a->q_in), static_cast<const T*>(a->k_in), static_cast<T*>(a->q_out),
                     static_cast<T*>(a->k_out), a->Hq, a->Hkv, a->seqs, a->batch, a->total_rows, a->positions,
                     a->dev_status, th);
+}
+
+// A small batch (fewer than four rows per SM) gets one row per CTA, so that its
+// loads and angles spread over the SMs; a larger one four rows per CTA.
+template <typename T, int D>
+static cudaError_t launch_rope(const ssv_rope_args* a, const RopeTheta& th, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  if ((long long)a->total_rows < 4LL * sms) return launch_rope_rows<T, D, 1>(a, th, st);
+  return launch_rope_rows<T, D, kRopeRows>(a, th, st);
 }
 
 }  // namespace ssv
