@@ -482,16 +482,25 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const Acc
   __shared__ int s_ok;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x;
-  pdl_wait();
-  pdl_trigger();
+  // Before the wait: the call's inputs (the streaming kernel writes none of
+  // them, and it lets this kernel start only after its own wait) -- the
+  // sequence's validity and the stages of the rows each warp merges.
+  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
+  const bool sizes = off >= 0 && B >= 1 && B <= 64 && g >= 0 && g <= B && off + B <= p.total_slots;
+  const int need = sizes ? min(g + 1, B) : 0;
+  int st[64 / kFinWarps];
+#pragma unroll
+  for (int k = 0; k < 64 / kFinWarps; ++k) {
+    const int j = warp + k * kFinWarps;
+    st[k] = (sizes && j < B) ? p.tau[off + j] : 0;
+  }
   if (warp == 0) {
-    bool ok = warp_seq_valid(p, b);
+    bool ok = sizes && warp_seq_valid(p, b);
     if (ok && MODE == SSV_ACCEPT_GUMBEL) {
-      const int off = p.slot_off[b], B = p.block[b], need = min(p.gamma[b] + 1, B);
       bool bad = false;
       for (int j = lane; j < B; j += 32) {
-        const int st = p.tau[off + j];
-        if (st >= 1 && st <= need) {
+        const int t = p.tau[off + j];
+        if (t >= 1 && t <= need) {
           const int nr = p.noise_row[off + j];
           bad = bad || nr < 0 || nr >= p.n_noise_rows;
         }
@@ -501,11 +510,13 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const Acc
     if (lane == 0) s_ok = ok ? 1 : 0;
   }
   __syncthreads();
+  pdl_wait();  // every chunk record of the streaming pass
+  pdl_trigger();
   if (!s_ok) return;
-  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b], need = min(g + 1, B);
-  for (int j = warp; j < B; j += kFinWarps) {  // warp-uniform
-    const int st = p.tau[off + j];
-    if (st >= 1 && st <= need) warp_row_merge<MODE, T>(p, off + j, st, g);
+#pragma unroll
+  for (int k = 0; k < 64 / kFinWarps; ++k) {  // warp-uniform
+    const int j = warp + k * kFinWarps;
+    if (j < B && st[k] >= 1 && st[k] <= need) warp_row_merge<MODE, T>(p, off + j, st[k], g);
   }
   __syncthreads();  // every row result of the sequence written
   if (warp == 0) warp_seq_walk<MODE>(p, b, off, B, g, walk, nullptr);
