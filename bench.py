@@ -115,24 +115,31 @@ def aggregate_ms(local_ms: float, dist_mod=None, device=None) -> float:
 
 
 def kernel_launches(x) -> int:
-    n = 1 + 1  # rope, verify attention
+    """Kernels one step launches: the rotation and the verification
+    attention, then the acceptance -- the streaming reduce plus its
+    completion (one finish kernel for the decision rules; for rejection
+    sampling the row merge with the walk, then the three emission passes:
+    normalisers, masses, the token)."""
+    n = 1 + 1
     if x is not None:
-        n += 2 if x.mode == W.MODE_REJECT else 1
+        n += 5 if x.mode == W.MODE_REJECT else 2
     return n
 
 
 KERNEL_OF_OP = {"verify_attn": "attn_tc_kernel", "accept": "accept_stream_kernel", "rope": "rope_copy_kernel",
                 "commit": "commit_kernel", "lmhead": "lmhead_accept_kernel"}
 KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh", "ssv_internal.cuh"],
-                  "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh", "noisegen.cuh"],
+                  "accept_stream_kernel": ["accept_stream.cu", "accept.cuh", "tc_ptx.cuh", "noisegen.cuh", "dfloat.cuh"],
                   "accept_reduce_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
                   "accept_sample_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
                   "accept_emit_norm_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
+                  "accept_locate_kernel": ["accept.cu", "accept.cuh", "dfloat.cuh", "noisegen.cuh"],
                   "rope_copy_kernel": ["rope.cu"],
                   "commit_kernel": ["commit.cu"],
-                  "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"],
-                  "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh"],
-                  "tree_attn_kernel": ["tree.cu", "accept.cuh"], "tree_reduce_kernel": ["tree.cu", "accept.cuh"]}
+                  "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh", "dfloat.cuh"],
+                  "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh", "dfloat.cuh"],
+                  "tree_attn_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh"],
+                  "tree_reduce_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh"]}
 
 
 def measured_traffic(op: str, workload: str):

@@ -17,6 +17,8 @@
 #include "accept.cuh"
 #include "dfloat.cuh"
 
+#include <algorithm>
+
 namespace ssv {
 
 constexpr int kAccThreads = 256;
@@ -231,17 +233,21 @@ accept_reduce_kernel(const AcceptParams p) {
 // entries per thread:
 //   accept_emit_norm   for a residual sample, each sub-chunk's sums of
 //                      e_a = 2^((l - m_a) c2) and e_b = 2^((ql - m_b) c2)
-//                      (unnormalised p and q).
+//                      (unnormalised p and q); where the workspace holds
+//                      room for them (eexp), also every entry's e_a and e_b
+//                      and the p masses (sums of e_a) per warp and sub-chunk.
 //   accept_sample      every CTA of sequence b adds the sub-chunk sums in the
 //                      same fixed order (S_a, S_b), forms the weights
 //                      w = (e_a S_b - e_b S_a)_+ (the residual (p - q)_+ scaled
-//                      by S_a S_b) and e_a (p scaled by S_a), and writes its
-//                      masses per warp and per sub-chunk; the last CTA finds
-//                      the sub-chunk, then the warp, then (one warp, one
-//                      thread's 8 entries per lane) the entry where the
-//                      cumulative mass passes u' Z (fp64 prefix sums of the
-//                      exact pair values; the residual unless it vanished,
-//                      then p).
+//                      by S_a S_b) and e_a (p scaled by S_a) -- from the stored
+//                      exponentials when there are any, the same values --
+//                      and writes its masses per warp and per sub-chunk.
+//   accept_locate      one CTA per sequence finds the sub-chunk, then the
+//                      warp, then the entry where the cumulative mass passes
+//                      u' Z (double-float prefix sums; the residual unless it
+//                      vanished, then p).
+// fp64 is avoided throughout: it is a narrow pipe on this part (tens of
+// cycles per dependent operation).
 
 struct EmitCtx {
   bool residual;
@@ -250,22 +256,50 @@ struct EmitCtx {
   dfx sa, sb;    // S_a, S_b (residual only)
 };
 
-// residual weight (e_a S_b - e_b S_a)_+ and p weight e_a of one entry
+// residual weight (e_a S_b - e_b S_a)_+ of one entry
+__device__ __forceinline__ dfx residual_weight(const EmitCtx& c, dfx ea, dfx eb) {
+  const dfx d = dfx_add(dfx_mul(ea, c.sb), dfx_mul(dfx{-eb.hi, -eb.lo}, c.sa));
+  return d.hi > 0.f ? d : dfx{0.f, 0.f};
+}
+
+// residual weight and p weight e_a of one entry, from its two logits
 __device__ __forceinline__ void emit_weights(const EmitCtx& c, float la, float lb, const float2* tab, dfx& wr,
                                              dfx& wp) {
   const dfx ea = dfx_exp2_diff(la, c.ma, c.c2, tab);
   wp = ea;
   wr = dfx{0.f, 0.f};
-  if (c.residual) {
-    const dfx eb = dfx_exp2_diff(lb, c.mb, c.c2, tab);
-    const dfx d = dfx_add(dfx_mul(ea, c.sb), dfx_mul(dfx{-eb.hi, -eb.lo}, c.sa));
-    if (d.hi > 0.f) wr = d;
-  }
+  if (c.residual) wr = residual_weight(c, ea, dfx_exp2_diff(lb, c.mb, c.c2, tab));
 }
 
 __device__ __forceinline__ dfx shfl_xor_dfx(dfx a, int o) {
   return dfx{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
+__device__ __forceinline__ dfx shfl_up_dfx(dfx a, int o) {
+  return dfx{__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ dfx shfl_dfx(dfx a, int src) {
+  return dfx{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+__device__ __forceinline__ dfx dfx_neg(dfx a) { return dfx{-a.hi, -a.lo}; }
+// a > b, decided on the sign of the renormalised difference
+__device__ __forceinline__ bool dfx_gt(dfx a, dfx b) { return dfx_add(a, dfx_neg(b)).hi > 0.f; }
+// inclusive prefix sum over the lanes (Hillis-Steele, 5 double-float additions deep)
+__device__ __forceinline__ dfx warp_incl_scan(dfx x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const dfx y = shfl_up_dfx(x, o);
+    if (lane >= o) x = dfx_add(x, y);
+  }
+  return x;
+}
+
+// exclusive prefix from the inclusive one (every lane takes part in the shuffle)
+__device__ __forceinline__ dfx warp_excl_of(dfx incl, int lane) {
+  const dfx y = shfl_up_dfx(incl, 1);
+  return lane ? y : dfx{0.f, 0.f};
+}
+
+constexpr int kEmitLane = 4;  // sub-chunk masses per lane in the level-1 search
 
 // The 8 consecutive entries [e0, e0 + 8) of a row (fill -inf past V).
 template <typename T>
@@ -291,20 +325,58 @@ __device__ __forceinline__ void ld_run8(const void* base, size_t rbase, int e0, 
   }
 }
 
-// Common prologue of the two emission kernels: validity of sequence b (reads
-// only the call's inputs, so it runs before the wait), the 2^(j/256) table
-// into shared memory, then the wait for the reduce kernel's records.
-__device__ __forceinline__ bool emit_prologue(const AcceptParams& p, int b, float2* s_tab, int* s_ok) {
-  const int tid = threadIdx.x;
-  if (tid < 32) {
-    const bool ok = warp_seq_valid(p, b);
-    if (tid == 0) *s_ok = ok;
+// The normaliser pass takes its work as items (sequence, sub-chunk) of the
+// sequences that sample the residual this call, dealt round-robin over a
+// grid sized to be resident at once, so that no SM idles on a sequence
+// without work.  The emission records are authoritative: the pass before the
+// walks set every sequence's record to "none" (emit[2b] = -1), and the walk
+// of each valid sequence wrote its own.
+constexpr int kEmitList = 2048;  // sequences listed per round (8 KB of shared memory)
+
+// The emitting sequences among b in [b0, b0 + kEmitList), in increasing b,
+// into s_seq (emission slot | residual << 31 in s_rec); returns their count.
+// Called by every thread of the CTA (barriers inside).
+__device__ int emit_list(const AcceptParams& p, int b0, bool residual_only, int* s_seq, int* s_rec, int* s_wc) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int total = 0;
+  const int end = min(p.batch, b0 + kEmitList);
+  for (int base = b0; base < end; base += kAccThreads) {
+    const int b = base + tid;
+    int es = -1, res = 0;
+    if (b < end) {
+      es = __ldcg(p.emit + 2 * b);
+      res = __ldcg(p.emit + 2 * b + 1);
+    }
+    const bool v = es >= 0 && es < p.total_slots && (!residual_only || res != 0);
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) s_wc[wid] = __popc(bal);
+    __syncthreads();
+    int before = total, sum = 0;
+#pragma unroll
+    for (int w = 0; w < kAccThreads / 32; ++w) {
+      const int c = s_wc[w];
+      before += (w < wid) ? c : 0;
+      sum += c;
+    }
+    if (v) {
+      const int pos = before + __popc(bal & ((1u << lane) - 1u));
+      s_seq[pos] = b;
+      s_rec[pos] = (int)((unsigned)es | ((res != 0 ? 1u : 0u) << 31));
+    }
+    total += sum;
+    __syncthreads();
   }
-  dfx_exp2_table(p.e2pow, s_tab, tid);  // kAccThreads == 256 entries
+  return total;
+}
+
+// The 2^(j/256) table into shared memory (inputs only, before the wait),
+// then the wait for the walks' emission records, accepted lengths and row
+// maxima (normaliser pass).
+__device__ __forceinline__ void emit_prologue(const AcceptParams& p, float2* s_tab) {
+  dfx_exp2_table(p.e2pow, s_tab, threadIdx.x);  // kAccThreads == 256 entries
   __syncthreads();
-  pdl_wait();  // emission records, accepted lengths and row normalisers
+  pdl_wait();
   pdl_trigger();
-  return *s_ok != 0;
 }
 
 static_assert(kAccThreads == 256 && kEmitSub == 8 * kAccThreads, "one table entry and 8 row entries per thread");
@@ -312,86 +384,133 @@ static_assert(kAccThreads == 256 && kEmitSub == 8 * kAccThreads, "one table entr
 template <typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_emit_norm_kernel(const AcceptParams p) {
-  __shared__ int s_ok;
   __shared__ float2 s_tab[256];
   __shared__ float4 s_w[kAccThreads / 32];
-  const int b = blockIdx.x / p.nsub;
-  const int sub = blockIdx.x % p.nsub;
-  // A sequence whose stage map or sizes were rejected never ran its walk,
-  // so its emission record may be stale: skip it.
-  if (!emit_prologue(p, b, s_tab, &s_ok)) return;
-  const int eslot = p.emit[2 * b];
-  const int soff = p.slot_off[b];
-  if (eslot < soff || eslot >= soff + p.block[b] || p.emit[2 * b + 1] == 0) return;  // bonus: no normaliser needed
-  const SlotNorm nm = p.norm[eslot];
+  __shared__ int s_seq[kEmitList], s_rec[kEmitList], s_wc[kAccThreads / 32];
+  emit_prologue(p, s_tab);
   const dfx c2{p.c2_hi, p.c2_lo};
-  const size_t rbase = (size_t)eslot * p.V;
-  const int e0 = sub * kEmitSub + threadIdx.x * 8;
-  float xa[8], xb[8];
-  ld_run8<T>(p.logits, rbase, e0, p.V, p.vec != 0, xa);
-  ld_run8<T>(p.draft_logits, rbase, e0, p.V, p.vec != 0, xb);
-  dfx sa{0.f, 0.f}, sb{0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    sa = dfx_add(sa, dfx_exp2_diff(xa[j], nm.m_a, c2, s_tab));
-    sb = dfx_add(sb, dfx_exp2_diff(xb[j], nm.m_b, c2, s_tab));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sa = dfx_add(sa, shfl_xor_dfx(sa, o));
-    sb = dfx_add(sb, shfl_xor_dfx(sb, o));
-  }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) s_w[wid] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kAccThreads / 32; ++w) {
-      sa = dfx_add(sa, dfx{s_w[w].x, s_w[w].y});
-      sb = dfx_add(sb, dfx{s_w[w].z, s_w[w].w});
+  long long it0 = 0;  // items of earlier rounds
+  for (int b0 = 0; b0 < p.batch; b0 += kEmitList) {
+    const int n = emit_list(p, b0, true, s_seq, s_rec, s_wc);
+    const long long items = (long long)n * p.nsub;
+    // this CTA's items of the round: global item indices congruent to blockIdx.x
+    long long first = ((long long)blockIdx.x - it0 % gridDim.x + gridDim.x) % gridDim.x;
+    for (long long it = first; it < items; it += gridDim.x) {
+      const int b = s_seq[it / p.nsub];
+      const int sub = (int)(it % p.nsub);
+      const int eslot = s_rec[it / p.nsub] & 0x7fffffff;
+      const SlotNorm nm = p.norm[eslot];
+      const size_t rbase = (size_t)eslot * p.V;
+      const int e0 = sub * kEmitSub + threadIdx.x * 8;
+      float xa[8], xb[8];
+      ld_run8<T>(p.logits, rbase, e0, p.V, p.vec != 0, xa);
+      ld_run8<T>(p.draft_logits, rbase, e0, p.V, p.vec != 0, xb);
+      const size_t cta = (size_t)b * p.nsub + sub;
+      float4* ex = p.eexp ? p.eexp + cta * kEmitSub + threadIdx.x : nullptr;
+      dfx sa{0.f, 0.f}, sb{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const dfx ea = dfx_exp2_diff(xa[j], nm.m_a, c2, s_tab);
+        const dfx eb = dfx_exp2_diff(xb[j], nm.m_b, c2, s_tab);
+        if (ex) __stcg(ex + j * kAccThreads, make_float4(ea.hi, ea.lo, eb.hi, eb.lo));
+        sa = dfx_add(sa, ea);
+        sb = dfx_add(sb, eb);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sa = dfx_add(sa, shfl_xor_dfx(sa, o));
+        sb = dfx_add(sb, shfl_xor_dfx(sb, o));
+      }
+      // With the exponentials stored, the p masses (the fallback when the
+      // residual vanishes) are these sums of e_a, in the sampling pass's order.
+      if (lane == 0) {
+        s_w[wid] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
+        if (ex) __stcg(reinterpret_cast<float2*>(p.wmass + cta * 8 + wid) + 1, make_float2(sa.hi, sa.lo));
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kAccThreads / 32; ++w) {
+          sa = dfx_add(sa, dfx{s_w[w].x, s_w[w].y});
+          sb = dfx_add(sb, dfx{s_w[w].z, s_w[w].w});
+        }
+        p.enorm[cta] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
+        if (ex) __stcg(reinterpret_cast<float2*>(p.smass + cta) + 1, make_float2(sa.hi, sa.lo));
+      }
+      __syncthreads();  // s_w is reused by the next item
     }
-    p.enorm[(size_t)b * p.nsub + sub] = make_float4(sa.hi, sa.lo, sb.hi, sb.lo);
+    it0 += items;
   }
 }
 
+// S_a, S_b of sequence b from its sub-chunk sums (one warp): kEmitLane
+// consecutive sums per lane (one round of loads for nsub <= 128), then a
+// butterfly.  The same fixed order wherever it is formed (the sampling CTAs
+// and the locating CTA must agree to the last bit).
+__device__ __forceinline__ float4 warp_emit_norms(const AcceptParams& p, int b) {
+  const int lane = threadIdx.x & 31;
+  const float4* en = p.enorm + (size_t)b * p.nsub;
+  dfx a{0.f, 0.f}, bb{0.f, 0.f};
+  for (int k0 = 0; k0 < p.nsub; k0 += 32 * kEmitLane) {
+    float4 v[kEmitLane];
+#pragma unroll
+    for (int k = 0; k < kEmitLane; ++k) {
+      const int i = k0 + lane * kEmitLane + k;
+      v[k] = i < p.nsub ? __ldcg(en + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kEmitLane; ++k) {
+      a = dfx_add(a, dfx{v[k].x, v[k].y});
+      bb = dfx_add(bb, dfx{v[k].z, v[k].w});
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = dfx_add(a, shfl_xor_dfx(a, o));
+    bb = dfx_add(bb, shfl_xor_dfx(bb, o));
+  }
+  return make_float4(a.hi, a.lo, bb.hi, bb.lo);
+}
+
+// Emission context of sequence b from its records, or false when it emits
+// nothing this call.
+__device__ __forceinline__ bool emit_ctx(const AcceptParams& p, int b, int& eslot, EmitCtx& c) {
+  eslot = __ldcg(p.emit + 2 * b);
+  if (eslot < 0 || eslot >= p.total_slots) return false;
+  c.residual = __ldcg(p.emit + 2 * b + 1) != 0;
+  const float2 nm = __ldcg(reinterpret_cast<const float2*>(p.norm + eslot));  // m_a, m_b
+  c.ma = nm.x;
+  c.mb = nm.y;
+  c.c2 = dfx{p.c2_hi, p.c2_lo};
+  c.sa = c.sb = dfx{0.f, 0.f};
+  return true;
+}
+
+// Sampling pass: one CTA per (sequence, sub-chunk); the masses of the
+// sampled weights per warp and per sub-chunk.
 template <typename T>
 __global__ void __launch_bounds__(kAccThreads)
 accept_sample_kernel(const AcceptParams p) {
-  __shared__ int s_ok, s_last;
   __shared__ float2 s_tab[256];
   __shared__ float4 s_w[kAccThreads / 32];
   __shared__ float4 s_S;
   const int b = blockIdx.x / p.nsub;
   const int sub = blockIdx.x % p.nsub;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (!emit_prologue(p, b, s_tab, &s_ok)) return;
-  const int eslot = p.emit[2 * b];
-  const int soff = p.slot_off[b];
-  const int nacc = p.n_acc[b];
-  if (eslot < soff || eslot >= soff + p.block[b] || nacc < 0 || nacc >= p.block[b]) return;
-  const SlotNorm nm = p.norm[eslot];
+  // Before the wait: the emission record and row maxima (the row merges
+  // wrote them, and they completed before the normaliser pass let this
+  // kernel start) and the exponential table.
+  int eslot;
   EmitCtx c;
-  c.residual = p.emit[2 * b + 1] != 0;
-  c.ma = nm.m_a;
-  c.mb = nm.m_b;
-  c.c2 = dfx{p.c2_hi, p.c2_lo};
-  c.sa = c.sb = dfx{0.f, 0.f};
+  if (!emit_ctx(p, b, eslot, c)) return;
+  dfx_exp2_table(p.e2pow, s_tab, tid);  // kAccThreads == 256 entries
+  __syncthreads();
+  pdl_wait();  // the normalisers and stored exponentials
+  pdl_trigger();
   if (c.residual) {
-    // S_a, S_b: warp 0 adds the sub-chunk sums, lane l over sub-chunks l, l + 32, ...,
-    // then a butterfly; the same fixed order in every CTA of the sequence
     if (wid == 0) {
-      const float4* en = p.enorm + (size_t)b * p.nsub;
-      dfx a{0.f, 0.f}, bb{0.f, 0.f};
-      for (int k = lane; k < p.nsub; k += 32) {
-        const float4 v = __ldcg(en + k);
-        a = dfx_add(a, dfx{v.x, v.y});
-        bb = dfx_add(bb, dfx{v.z, v.w});
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        a = dfx_add(a, shfl_xor_dfx(a, o));
-        bb = dfx_add(bb, shfl_xor_dfx(bb, o));
-      }
-      if (lane == 0) s_S = make_float4(a.hi, a.lo, bb.hi, bb.lo);
+      const float4 S = warp_emit_norms(p, b);
+      if (lane == 0) s_S = S;
     }
     __syncthreads();
     c.sa = dfx{s_S.x, s_S.y};
@@ -399,146 +518,246 @@ accept_sample_kernel(const AcceptParams p) {
   }
   const size_t rbase = (size_t)eslot * p.V;
   const bool vec = p.vec != 0;
+  // stored exponentials of the residual's row (the normaliser pass wrote them
+  // and this sub-chunk's p masses): only the residual weights are formed here
+  const bool stored = c.residual && p.eexp != nullptr;
   {
-    const int e0 = sub * kEmitSub + tid * 8;
-    float xa[8], xb[8];
-    ld_run8<T>(p.logits, rbase, e0, p.V, vec, xa);
-    if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, xb);
+    const size_t cta = (size_t)b * p.nsub + sub;
     dfx mr{0.f, 0.f}, mp{0.f, 0.f};
+    if (stored) {
+      const float4* ex = p.eexp + cta * kEmitSub + tid;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      dfx wr, wp;
-      emit_weights(c, xa[j], c.residual ? xb[j] : -INFINITY, s_tab, wr, wp);
-      mr = dfx_add(mr, wr);
-      mp = dfx_add(mp, wp);
+      for (int j = 0; j < 8; ++j) {
+        const float4 v = __ldcg(ex + j * kAccThreads);
+        mr = dfx_add(mr, residual_weight(c, dfx{v.x, v.y}, dfx{v.z, v.w}));
+      }
+    } else {
+      const int e0 = sub * kEmitSub + tid * 8;
+      float xa[8], xb[8];
+      ld_run8<T>(p.logits, rbase, e0, p.V, vec, xa);
+      if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, xb);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        dfx wr, wp;
+        emit_weights(c, xa[j], c.residual ? xb[j] : -INFINITY, s_tab, wr, wp);
+        mr = dfx_add(mr, wr);
+        mp = dfx_add(mp, wp);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       mr = dfx_add(mr, shfl_xor_dfx(mr, o));
-      mp = dfx_add(mp, shfl_xor_dfx(mp, o));
+      if (!stored) mp = dfx_add(mp, shfl_xor_dfx(mp, o));
     }
     if (lane == 0) {
       const float4 m4 = make_float4(mr.hi, mr.lo, mp.hi, mp.lo);
       s_w[wid] = m4;
-      p.wmass[((size_t)b * p.nsub + sub) * 8 + wid] = m4;
+      if (stored) __stcg(reinterpret_cast<float2*>(p.wmass + cta * 8 + wid), make_float2(mr.hi, mr.lo));
+      else p.wmass[cta * 8 + wid] = m4;
     }
     __syncthreads();
     if (tid == 0) {
       for (int w = 1; w < kAccThreads / 32; ++w) {
         mr = dfx_add(mr, dfx{s_w[w].x, s_w[w].y});
-        mp = dfx_add(mp, dfx{s_w[w].z, s_w[w].w});
+        if (!stored) mp = dfx_add(mp, dfx{s_w[w].z, s_w[w].w});
       }
-      p.smass[(size_t)b * p.nsub + sub] = make_float4(mr.hi, mr.lo, mp.hi, mp.lo);
-      __threadfence();
-      const int prev = atomicAdd(&p.cnt_sample[b], 1);
-      s_last = (prev == p.nsub - 1);
+      if (stored) __stcg(reinterpret_cast<float2*>(p.smass + cta), make_float2(mr.hi, mr.lo));
+      else p.smass[cta] = make_float4(mr.hi, mr.lo, mp.hi, mp.lo);
+    }
+  }
+}
+
+// Locating pass: one CTA per sequence, once every mass is written: the
+// token where the cumulative mass passes t = u' Z.
+template <typename T>
+__global__ void __launch_bounds__(kAccThreads)
+accept_locate_kernel(const AcceptParams p) {
+  __shared__ float2 s_tab[256];
+  __shared__ int s_cs, s_use_res, s_wsel;
+  __shared__ float4 s_S;
+  __shared__ float2 s_t, s_before;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // Before the wait: everything but the masses -- the emission record, row
+  // maxima, normalisers and stored exponentials were complete before the
+  // sampling pass let this kernel start -- and the exponential table.
+  int eslot;
+  EmitCtx c;
+  if (!emit_ctx(p, b, eslot, c)) return;
+  const size_t rbase = (size_t)eslot * p.V;
+  const bool vec = p.vec != 0;
+  const bool stored = c.residual && p.eexp != nullptr;
+  if (wid == 1 && c.residual) {  // the normalisers (residual weights of level 3)
+    const float4 S = warp_emit_norms(p, b);
+    if (lane == 0) s_S = S;
+  }
+  dfx_exp2_table(p.e2pow, s_tab, tid);  // kAccThreads == 256 entries
+  __syncthreads();
+  pdl_wait();  // the masses
+  pdl_trigger();
+  // Level 1 (warp 0): the sub-chunk masses, kEmitLane consecutive per lane
+  // in registers (one round of loads for nsub <= 128), the total Z and
+  // t = u' Z, then the first sub-chunk whose cumulative mass passes t (else,
+  // rounding having left t at the very end, the last non-empty one).  All
+  // in double-float arithmetic.
+  const float4* sm = p.smass + (size_t)b * p.nsub;
+  if (wid == 0) {
+    constexpr int kBlk = 32 * kEmitLane;
+    const int nblk = (p.nsub + kBlk - 1) / kBlk;
+    float4 v[kEmitLane];
+    auto load_blk = [&](int blk) {
+#pragma unroll
+      for (int k = 0; k < kEmitLane; ++k) {
+        const int i = blk * kBlk + lane * kEmitLane + k;
+        v[k] = (i < p.nsub) ? __ldcg(sm + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+    dfx zr{0.f, 0.f}, zp{0.f, 0.f};
+    for (int blk = 0; blk < nblk; ++blk) {
+      load_blk(blk);
+#pragma unroll
+      for (int k = 0; k < kEmitLane; ++k) {
+        zr = dfx_add(zr, dfx{v[k].x, v[k].y});
+        zp = dfx_add(zp, dfx{v[k].z, v[k].w});
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zr = dfx_add(zr, shfl_xor_dfx(zr, o));
+      zp = dfx_add(zp, shfl_xor_dfx(zp, o));
+    }
+    const bool use_res = c.residual && zr.hi > 0.f;  // (p - q)_+ vanished: sample p
+    const dfx t = dfx_mul(use_res ? zr : zp, dfx{p.u_sample[b], 0.f});
+    dfx base{0.f, 0.f}, before{0.f, 0.f}, before_last{0.f, 0.f};
+    int cs = -1, last_nz = 0;
+    for (int blk = 0; blk < nblk; ++blk) {
+      if (nblk > 1) load_blk(blk);  // a single block is still in registers
+      dfx pre[kEmitLane];  // this lane's inclusive prefix over its sub-chunks
+      dfx run{0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kEmitLane; ++k) {
+        run = dfx_add(run, use_res ? dfx{v[k].x, v[k].y} : dfx{v[k].z, v[k].w});
+        pre[k] = run;
+      }
+      const dfx incl = warp_incl_scan(run, lane);
+      const dfx start = dfx_add(base, warp_excl_of(incl, lane));  // before this lane's first
+      int kc = -1, kz = -1;
+#pragma unroll
+      for (int k = 0; k < kEmitLane; ++k) {
+        const int i = blk * kBlk + lane * kEmitLane + k;
+        const bool nonzero = (use_res ? v[k].x : v[k].z) > 0.f;
+        if (i < p.nsub && nonzero) kz = k;
+        if (kc < 0 && i < p.nsub && dfx_gt(dfx_add(start, pre[k]), t)) kc = k;
+      }
+      const unsigned cross = __ballot_sync(0xffffffffu, kc >= 0);
+      const unsigned nz = __ballot_sync(0xffffffffu, kz >= 0);
+      // cumulative mass before sub-chunk k of this lane
+      auto before_k = [&](int k) {
+        dfx r = start;
+#pragma unroll
+        for (int j = 1; j < kEmitLane; ++j)
+          if (j == k) r = dfx_add(start, pre[j - 1]);
+        return r;
+      };
+      if (cs < 0 && cross) {
+        const int f = __ffs(cross) - 1;
+        const dfx bk = before_k(kc);
+        cs = __shfl_sync(0xffffffffu, blk * kBlk + lane * kEmitLane + kc, f);
+        before = shfl_dfx(bk, f);
+      }
+      if (nz) {
+        const int l = 31 - __clz(nz);
+        const dfx bk = before_k(kz);
+        last_nz = __shfl_sync(0xffffffffu, blk * kBlk + lane * kEmitLane + kz, l);
+        before_last = shfl_dfx(bk, l);
+      }
+      base = dfx_add(base, shfl_dfx(incl, 31));
+    }
+    if (cs < 0) { cs = last_nz; before = before_last; }
+    if (lane == 0) {
+      s_cs = cs;
+      s_use_res = use_res;
+      s_t = make_float2(t.hi, t.lo);
+      s_before = make_float2(before.hi, before.lo);
     }
   }
   __syncthreads();
-  if (!s_last || wid != 0) return;
-  __threadfence();
-
-  // ---- last CTA of sequence b, warp 0: locate u' * Z ---------------------------
-  const float4* sm = p.smass + (size_t)b * p.nsub;
-  double zr = 0.0, zp = 0.0;
-  for (int k = lane; k < p.nsub; k += 32) {
-    const float4 v = __ldcg(sm + k);
-    zr += (double)v.x + (double)v.y;
-    zp += (double)v.z + (double)v.w;
+  const int cs = s_cs;
+  const bool use_res = s_use_res;
+  const dfx t{s_t.x, s_t.y};
+  if (c.residual) {
+    c.sa = dfx{s_S.x, s_S.y};
+    c.sb = dfx{s_S.z, s_S.w};
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    zr += __shfl_xor_sync(0xffffffffu, zr, o);
-    zp += __shfl_xor_sync(0xffffffffu, zp, o);
-  }
-  const bool use_res = c.residual && zr > 0.0;  // (p - q)_+ vanished: sample p
-  const double t = (double)p.u_sample[b] * (use_res ? zr : zp);
-  auto mass = [&](const float4& v) -> double { return use_res ? (double)v.x + (double)v.y : (double)v.z + (double)v.w; };
-  // level 1: the first sub-chunk whose running mass passes t (else the last non-empty one)
-  double before = 0.0, before_last = 0.0, base = 0.0;
-  int cs = -1, last_nz = 0;
-  for (int r0 = 0; r0 < p.nsub; r0 += 32) {
-    const int k = r0 + lane;
-    const double m = (k < p.nsub) ? mass(__ldcg(sm + k)) : 0.0;
-    double incl = m;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const double excl = incl - m;
-    const unsigned cross = __ballot_sync(0xffffffffu, k < p.nsub && base + incl > t);
-    const unsigned nz = __ballot_sync(0xffffffffu, k < p.nsub && m > 0.0);
-    if (cs < 0 && cross) {
-      const int f = __ffs(cross) - 1;
-      cs = r0 + f;
-      before = base + __shfl_sync(0xffffffffu, excl, f);
-    }
-    if (nz) {
-      const int l = 31 - __clz(nz);
-      last_nz = r0 + l;
-      before_last = base + __shfl_sync(0xffffffffu, excl, l);
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (cs < 0) { cs = last_nz; before = before_last; }  // rounding left t at the very end
-  // level 2: the warp of that sub-chunk (lanes 0..7 hold the 8 warp masses)
-  int wsel;
-  {
-    const double m = (lane < 8) ? mass(__ldcg(p.wmass + ((size_t)b * p.nsub + cs) * 8 + lane)) : 0.0;
-    double incl = m;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const double excl = incl - m;
-    const unsigned cross = __ballot_sync(0xffffffffu, lane < 8 && before + incl > t);
-    const unsigned nz = __ballot_sync(0xffffffffu, lane < 8 && m > 0.0);
-    wsel = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 7);
-    before += __shfl_sync(0xffffffffu, excl, wsel);
-  }
-  // level 3: that warp's 256 entries, 8 consecutive per lane
-  const int e0 = cs * kEmitSub + wsel * 256 + lane * 8;
-  float ya[8], yb[8];
-  ld_run8<T>(p.logits, rbase, e0, p.V, vec, ya);
-  if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, yb);
+  // Every warp forms the weights of its 256 entries of sub-chunk cs (lane:
+  // 8 consecutive entries) while warp 0 finds the warp that holds t (level
+  // 2, from the sub-chunk's 8 warp masses).
+  const int e0 = cs * kEmitSub + wid * 256 + lane * 8;
+  float4 wm = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (wid == 0 && lane < 8) wm = __ldcg(p.wmass + ((size_t)b * p.nsub + cs) * 8 + lane);
   dfx w8[8];
-  dfx run{0.f, 0.f};
-  int last_pos = -1;
+  if (stored) {  // entry e0 + k is [k][32 wid + lane] of sub-chunk cs
+    const float4* ex = p.eexp + ((size_t)b * p.nsub + cs) * kEmitSub + wid * 32 + lane;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    dfx wr, wp;
-    emit_weights(c, ya[k], c.residual ? yb[k] : -INFINITY, s_tab, wr, wp);
-    w8[k] = use_res ? wr : wp;
-    run = dfx_add(run, w8[k]);
-    if (w8[k].hi > 0.f) last_pos = e0 + k;
-  }
-  const double rm = dfx_to_double(run);
-  double incl = rm;
+    for (int k = 0; k < 8; ++k) {
+      const float4 v = __ldcg(ex + k * kAccThreads);
+      const dfx ea{v.x, v.y};
+      w8[k] = use_res ? residual_weight(c, ea, dfx{v.z, v.w}) : ea;
+    }
+  } else {
+    float ya[8], yb[8];
+    ld_run8<T>(p.logits, rbase, e0, p.V, vec, ya);
+    if (c.residual) ld_run8<T>(p.draft_logits, rbase, e0, p.V, vec, yb);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    for (int k = 0; k < 8; ++k) {
+      dfx wr, wp;
+      emit_weights(c, ya[k], c.residual ? yb[k] : -INFINITY, s_tab, wr, wp);
+      w8[k] = use_res ? wr : wp;
+    }
   }
-  const double rel = t - (before + (incl - rm));  // mass still to cross at the start of this lane's run
-  dfx acc{0.f, 0.f};
-  int pick = INT_MAX;
+  if (wid == 0) {
+    const dfx m = use_res ? dfx{wm.x, wm.y} : dfx{wm.z, wm.w};  // zero past lane 7
+    const dfx incl = warp_incl_scan(m, lane);
+    const dfx before{s_before.x, s_before.y};
+    const unsigned cross = __ballot_sync(0xffffffffu, lane < 8 && dfx_gt(dfx_add(before, incl), t));
+    const unsigned nz = __ballot_sync(0xffffffffu, lane < 8 && m.hi > 0.f);
+    const int wsel = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 7);
+    const dfx b2 = dfx_add(before, shfl_dfx(warp_excl_of(incl, lane), wsel));
+    if (lane == 0) {
+      s_wsel = wsel;
+      s_before = make_float2(b2.hi, b2.lo);
+    }
+  }
+  __syncthreads();
+  if (wid == s_wsel) {
+    // Level 3 (warp wsel): the entry where the cumulative mass passes t
+    dfx run{0.f, 0.f};
+    int last_pos = -1;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    acc = dfx_add(acc, w8[k]);
-    if (pick == INT_MAX && w8[k].hi > 0.f && dfx_to_double(acc) > rel) pick = e0 + k;
-  }
-  // lanes are in vocabulary order: the first lane with a crossing holds the token
-  const unsigned has = __ballot_sync(0xffffffffu, pick != INT_MAX);
-  const int v_pick = has ? __shfl_sync(0xffffffffu, pick, __ffs(has) - 1) : INT_MAX;
-  const unsigned anyw = __ballot_sync(0xffffffffu, last_pos >= 0);
-  const int v_last = anyw ? __shfl_sync(0xffffffffu, last_pos, 31 - __clz(anyw)) : -1;
-  if (lane == 0) {
-    int v = v_pick != INT_MAX ? v_pick : v_last;
-    if (v < 0) v = 0;
-    p.tokens[soff + nacc] = v;
-    p.cnt_sample[b] = 0;
+    for (int k = 0; k < 8; ++k) {
+      run = dfx_add(run, w8[k]);
+      if (w8[k].hi > 0.f) last_pos = e0 + k;
+    }
+    const dfx incl = warp_incl_scan(run, lane);
+    // mass still to cross at the start of this lane's run
+    const dfx rel = dfx_add(t, dfx_neg(dfx_add(dfx{s_before.x, s_before.y}, warp_excl_of(incl, lane))));
+    dfx acc{0.f, 0.f};
+    int pick = INT_MAX;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc = dfx_add(acc, w8[k]);
+      if (pick == INT_MAX && w8[k].hi > 0.f && dfx_gt(acc, rel)) pick = e0 + k;
+    }
+    // lanes are in vocabulary order: the first lane with a crossing holds the token
+    const unsigned has = __ballot_sync(0xffffffffu, pick != INT_MAX);
+    const int v_pick = has ? __shfl_sync(0xffffffffu, pick, __ffs(has) - 1) : INT_MAX;
+    const unsigned anyw = __ballot_sync(0xffffffffu, last_pos >= 0);
+    const int v_last = anyw ? __shfl_sync(0xffffffffu, last_pos, 31 - __clz(anyw)) : -1;
+    if (lane == 0) {
+      int v = v_pick != INT_MAX ? v_pick : v_last;
+      if (v < 0) v = 0;
+      p.tokens[p.slot_off[b] + p.n_acc[b]] = v;
+    }
   }
 }
 
@@ -557,6 +776,9 @@ static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaS
   if (accept_stream_supported(p, mode, bf)) {
     e = launch_accept_stream(p, mode, bf, st);
   } else {
+    // every emission record to "none" (-1); the walks write the valid sequences' own
+    if (mode == SSV_ACCEPT_REJECT && cudaMemsetAsync(p.emit, 0xff, sizeof(int32_t) * 2 * (size_t)p.batch, st) != cudaSuccess)
+      return cudaGetLastError();
     switch (mode) {
       case SSV_ACCEPT_ARGMAX:
         e = bf ? launch_reduce_t<SSV_ACCEPT_ARGMAX, __nv_bfloat16>(p, st) : launch_reduce_t<SSV_ACCEPT_ARGMAX, float>(p, st);
@@ -574,16 +796,28 @@ static cudaError_t launch_accept(const AcceptParams& p, int mode, bool bf, cudaS
     }
   }
   if (e != cudaSuccess || mode != SSV_ACCEPT_REJECT) return e;
-  const long long g2 = (long long)p.batch * p.nsub;
-  if (g2 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // emission passes: the normalisers over a grid that is resident at once
+  // (five CTAs per SM beside the row merges still running), its items dealt
+  // round-robin; the masses, one CTA per (sequence, sub-chunk); the token,
+  // one CTA per sequence
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const long long items = (long long)p.batch * p.nsub;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const unsigned g_norm = (unsigned)std::min<long long>(items, 5LL * sms);
   if (bf) {
-    e = launch_pdl(accept_emit_norm_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(accept_sample_kernel<__nv_bfloat16>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+    e = launch_pdl(accept_emit_norm_kernel<__nv_bfloat16>, dim3(g_norm), dim3(kAccThreads), 0, st, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(accept_sample_kernel<__nv_bfloat16>, dim3((unsigned)items), dim3(kAccThreads), 0, st, p);
+    if (e == cudaSuccess)
+      e = launch_pdl(accept_locate_kernel<__nv_bfloat16>, dim3((unsigned)p.batch), dim3(kAccThreads), 0, st, p);
+    return e;
   }
-  e = launch_pdl(accept_emit_norm_kernel<float>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(accept_sample_kernel<float>, dim3((unsigned)g2), dim3(kAccThreads), 0, st, p);
+  e = launch_pdl(accept_emit_norm_kernel<float>, dim3(g_norm), dim3(kAccThreads), 0, st, p);
+  if (e == cudaSuccess) e = launch_pdl(accept_sample_kernel<float>, dim3((unsigned)items), dim3(kAccThreads), 0, st, p);
+  if (e == cudaSuccess) e = launch_pdl(accept_locate_kernel<float>, dim3((unsigned)p.batch), dim3(kAccThreads), 0, st, p);
+  return e;
 }
 
 }  // namespace ssv
@@ -647,7 +881,6 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   p.dev_status = a->dev_status;
   p.early = 0;
   p.cnt_seq = reinterpret_cast<int32_t*>(w + L.cnt_seq);
-  p.cnt_sample = reinterpret_cast<int32_t*>(w + L.cnt_sample);
   p.cnt_row = reinterpret_cast<int32_t*>(w + L.cnt_row);
   p.emit = reinterpret_cast<int32_t*>(w + L.emit);
   p.part = reinterpret_cast<AccPartial*>(w + L.part);
@@ -657,6 +890,7 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   p.enorm = reinterpret_cast<float4*>(w + L.enorm);
   p.smass = reinterpret_cast<float4*>(w + L.smass);
   p.wmass = reinterpret_cast<float4*>(w + L.wmass);
+  p.eexp = L.total > L.eexp ? reinterpret_cast<float4*>(w + L.eexp) : nullptr;
   // double-float constants of the emitted sample: log2(e) / T and 2^(2^i / 256)
   const double c2d = a->T > 0.f ? 1.4426950408889634074 / (double)a->T : 0.0;
   p.c2_hi = (float)c2d;
@@ -682,7 +916,7 @@ extern "C" ssv_status ssv_accept_workspace(const ssv_accept_args* a, size_t* byt
   int nchunks = 0;
   const ssv_status st = accept_check(a, &nchunks);
   if (st != SSV_OK) return st;
-  *bytes = accept_layout(a->batch, a->total_slots, nchunks).total;
+  *bytes = accept_layout(a->batch, a->total_slots, nchunks, a->mode == SSV_ACCEPT_REJECT).total;
   return SSV_OK;
 }
 
@@ -693,7 +927,7 @@ ssv_status accept_validate(const ssv_accept_args* a, void* ws, size_t ws_bytes) 
   const ssv_status st = accept_check(a, &nchunks);
   if (st != SSV_OK) return st;
   if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
-  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
+  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks, a->mode == SSV_ACCEPT_REJECT);
   if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < L.total) return SSV_ERR_WORKSPACE;
   return SSV_OK;
 }
@@ -704,7 +938,7 @@ ssv_status accept_run(const ssv_accept_args* a, void* ws, size_t ws_bytes, cudaS
   if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
   int nchunks = 0;
   accept_check(a, &nchunks);
-  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
+  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks, a->mode == SSV_ACCEPT_REJECT);
   AcceptParams p;
   const int mode = fill_params(a, static_cast<char*>(ws), L, nchunks, &p);
   p.early = early;
@@ -794,13 +1028,16 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   ssv_status st = accept_check(a, &nchunks);
   if (st != SSV_OK) return st;
   if (a->batch == 0 || a->total_slots == 0) return SSV_OK;
-  const AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks);
+  // rejection sampling stores the emitted rows' exponentials where they fit,
+  // else its sampling pass forms them again
+  AccWorkspaceLayout L = accept_layout(a->batch, a->total_slots, nchunks, a->mode == SSV_ACCEPT_REJECT);
+  if (L.total > kNoAllocScratchBytes) L = accept_layout(a->batch, a->total_slots, nchunks, false);
   if (L.total > kNoAllocScratchBytes) return SSV_ERR_WORKSPACE;
   void* scratch = nullptr;
   st = noalloc_scratch_address(&scratch);
   if (st != SSV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The arrival counters (cnt_seq, cnt_sample, cnt_row: the front of the
+  // The arrival counters (cnt_seq, cnt_row: the front of the
   // layout, up to emit) must start at zero.
   if (cudaMemsetAsync(scratch, 0, L.emit, s) != cudaSuccess) return SSV_ERR_CUDA;
   AcceptParams p;

@@ -20,6 +20,7 @@
 #pragma once
 
 #include "ssv_internal.cuh"
+#include "dfloat.cuh"
 #include "noisegen.cuh"
 
 #include <limits.h>
@@ -37,9 +38,8 @@ struct AccPartial {
   int idx;                 // its first index
 };
 
-struct SlotNorm {  // p_v = 2^((l_v - m_a) c2) / s_a, q likewise
+struct __align__(8) SlotNorm {  // row maxima of the logits and the draft logits (p_v = 2^((l_v - m_a) c2) / S_a, q likewise)
   float m_a, m_b;
-  double s_a, s_b;
 };
 
 struct __align__(8) RowResult {
@@ -76,9 +76,8 @@ struct AcceptParams {
   // kernel, whose outputs overlap none of the batch metadata; the metadata
   // may then be read before it completes (programmatic dependent launch).
   int early;
-  // workspace carve-up (the three counter arrays come first and are contiguous)
+  // workspace carve-up (the two counter arrays come first and are contiguous)
   int32_t* cnt_seq;     // [batch]        merged rows of the sequence
-  int32_t* cnt_sample;  // [batch]        emission-row sub-chunks done
   int32_t* cnt_row;     // [total_slots]  chunks of the row done
   int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
   AccPartial* part;     // [total_slots][nchunks]
@@ -90,6 +89,11 @@ struct AcceptParams {
   float4* enorm;        // [batch][nsub]     sums of e_a = 2^((l - m_a) c2) and e_b = 2^((ql - m_b) c2)
   float4* smass;        // [batch][nsub]     residual mass, p mass (each hi, lo)
   float4* wmass;        // [batch][nsub][8]  the same per warp of the sub-chunk's CTA
+  // [batch][nsub][8][256]: e_a and e_b (each hi, lo) of every entry
+  // of the emitted row, written by the normaliser pass for a residual sample
+  // and read back by the sampling pass ([j][t] holds the sub-chunk's entry
+  // 8 t + j); null: the sampling pass forms them again from the logits
+  float4* eexp;
   // c2 = log2(e) / T split into an fp32 head and tail; 2^(2^i / 256),
   // i = 0..7, likewise (host-computed)
   float c2_hi, c2_lo;
@@ -105,15 +109,16 @@ struct AcceptParams {
 constexpr int kEmitSub = 2048;  // vocabulary entries per emission CTA (256 threads x 8)
 
 struct AccWorkspaceLayout {
-  size_t cnt_seq, cnt_sample, cnt_row, emit, part, norm, rowres, enorm, smass, wmass, total;
+  size_t cnt_seq, cnt_row, emit, part, norm, rowres, enorm, smass, wmass, eexp, total;
 };
 
-inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks) {
+// eexp: room for the emitted rows' stored exponentials (rejection sampling);
+// without it L.eexp == L.total and the sampling pass recomputes them.
+inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks, bool eexp) {
   const size_t nsub = (size_t)nchunks * (kAccChunk / kEmitSub);
   AccWorkspaceLayout L;
   size_t o = 0;
   L.cnt_seq = o;    o += sizeof(int32_t) * (size_t)batch;
-  L.cnt_sample = o; o += sizeof(int32_t) * (size_t)batch;
   L.cnt_row = o;    o = align_up(o + sizeof(int32_t) * (size_t)total_slots, 256);
   L.emit = o;       o = align_up(o + sizeof(int32_t) * 2 * (size_t)batch, 256);
   L.part = o;       o = align_up(o + sizeof(AccPartial) * (size_t)total_slots * nchunks, 256);
@@ -122,6 +127,7 @@ inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks)
   L.enorm = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nsub, 256);
   L.smass = o;      o = align_up(o + sizeof(float) * 4 * (size_t)batch * nsub, 256);
   L.wmass = o;      o = align_up(o + sizeof(float) * 4 * 8 * (size_t)batch * nsub, 256);
+  L.eexp = o;       if (eexp) o = align_up(o + sizeof(float) * 4 * (size_t)kEmitSub * batch * nsub, 256);
   L.total = o;
   return L;
 }
@@ -216,10 +222,32 @@ __device__ __forceinline__ bool warp_arrive(int32_t* counter, int add, int targe
   return last != 0;
 }
 
+// Inputs of a rejection test that come with the call (lane 0 holds them):
+// the draft token d, its logit under the target and the draft, u_accept.
+struct RowInputs {
+  int d;
+  float ld, qd, ua;
+};
+
+template <typename T>
+__device__ __forceinline__ RowInputs row_inputs(const AcceptParams& p, int slot, bool tested) {
+  RowInputs in{-1, 0.f, 0.f, 0.f};
+  if (tested && (threadIdx.x & 31) == 0) {
+    in.d = p.draft_tokens[slot];
+    in.ua = p.u_accept[slot];
+    if (in.d >= 0 && in.d < p.V) {
+      in.ld = ld_logit<T>(p.logits, (size_t)slot * p.V + in.d);
+      in.qd = ld_logit<T>(p.draft_logits, (size_t)slot * p.V + in.d);
+    }
+  }
+  return in;
+}
+
 // Merge of verified row `slot` (1-based stage st, draft length g): lanes
 // over chunks.  Writes rowres[slot] and, for rejection sampling, norm[slot].
+// pre: the row's RowInputs when the caller loaded them already, else null.
 template <int MODE, typename T>
-__device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
+__device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g, const RowInputs* pre = nullptr) {
   const int lane = threadIdx.x & 31;
   const AccPartial* pp = p.part + (size_t)slot * p.nchunks;
   const bool tested = st <= g;  // stages past gamma carry no draft token
@@ -236,64 +264,77 @@ __device__ void warp_row_merge(const AcceptParams& p, int slot, int st, int g) {
     if (lane == 0) p.rowres[slot] = rr;
     return;
   }
-  // Rejection sampling: per lane a running (max, sum) over its chunks in
-  // fp64, then a max / rescaled-sum butterfly across the warp.  Lane 0 loads
-  // the draft token's two logits while the chunk records are in flight.
-  // Scale factors 2^((m - M) c2) are fp32 exp2 of an fp64-formed argument
-  // (about 5e-7 relative, the order of the chunk sums' own exp2 rounding):
-  // FP64 is a small fraction of FP32 on this part and a chain of fp64 exp2
-  // calls cost microseconds at the tail of the kernel.
-  int d = -1;
-  double ld = 0.0, qd = 0.0;
-  float ua = 0.f;
-  if (tested && lane == 0) {
-    d = p.draft_tokens[slot];
-    ua = p.u_accept[slot];
-    if (d >= 0 && d < p.V) {
-      ld = ld_logit<T>(p.logits, (size_t)slot * p.V + d);
-      qd = ld_logit<T>(p.draft_logits, (size_t)slot * p.V + d);
+  // Rejection sampling: the row maxima (warp max of the chunk maxima), then
+  // S = sum over chunks of s_c 2^((m_c - M) c2) in double-float arithmetic
+  // (fp32 pairs: fp64 is a narrow pipe on this part, tens of cycles per
+  // dependent operation), each scale factor an fp32 exp2 of an argument
+  // formed from the exact difference m_c - M (about 5e-7 relative, the order
+  // of the chunk sums' own exp2 rounding).  The ratio p(d)/q(d) is then
+  // 2^(((l_d - M_a) - (q_d - M_b)) c2) S_b / S_a in fp32.
+  RowInputs in = pre ? *pre : row_inputs<T>(p, slot, tested);
+  const float c2 = p.c2;
+  constexpr int kHeld = 2;  // chunk records held per lane (up to 64 chunks; beyond that, loaded twice)
+  float cma[kHeld], cmb[kHeld];
+  dfx csa[kHeld], csb[kHeld];
+  float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+  for (int h = 0; h < kHeld; ++h) {
+    const int c = lane + 32 * h;
+    cma[h] = cmb[h] = -INFINITY;
+    csa[h] = csb[h] = dfx{0.f, 0.f};
+    if (c < p.nchunks) {
+      cma[h] = __ldcg(&pp[c].m_a);
+      csa[h] = dfx{__ldcg(&pp[c].sa_hi), __ldcg(&pp[c].sa_lo)};
+      if (tested) {
+        cmb[h] = __ldcg(&pp[c].m_b);
+        csb[h] = dfx{__ldcg(&pp[c].sb_hi), __ldcg(&pp[c].sb_lo)};
+      }
     }
+    ma = fmaxf(ma, cma[h]);
+    mb = fmaxf(mb, cmb[h]);
   }
-  const double c2 = (double)p.c2;
-  double ma = -INFINITY, mb = -INFINITY, sa = 0.0, sb = 0.0;
-  auto scale = [&](double x) -> double { return (double)exp2f((float)(x * c2)); };  // 2^(x c2), x <= 0
-  for (int c = lane; c < p.nchunks; c += 32) {
-    const double cma = __ldcg(&pp[c].m_a);
-    const double csa = (double)__ldcg(&pp[c].sa_hi) + (double)__ldcg(&pp[c].sa_lo);
-    if (cma > ma) { sa = (ma == -INFINITY) ? 0.0 : sa * scale(ma - cma); ma = cma; }
-    if (cma > -INFINITY) sa += (cma == ma) ? csa : csa * scale(cma - ma);
-    if (tested) {
-      const double cmb = __ldcg(&pp[c].m_b);
-      const double csb = (double)__ldcg(&pp[c].sb_hi) + (double)__ldcg(&pp[c].sb_lo);
-      if (cmb > mb) { sb = (mb == -INFINITY) ? 0.0 : sb * scale(mb - cmb); mb = cmb; }
-      if (cmb > -INFINITY) sb += (cmb == mb) ? csb : csb * scale(cmb - mb);
-    }
+  for (int c = lane + 32 * kHeld; c < p.nchunks; c += 32) {
+    ma = fmaxf(ma, __ldcg(&pp[c].m_a));
+    if (tested) mb = fmaxf(mb, __ldcg(&pp[c].m_b));
   }
-  double Ma = ma, Mb = mb;
+  const float Ma = warp_max(ma), Mb = warp_max(mb);
+  // s_c 2^((m_c - M) c2), added into acc
+  auto add_scaled = [&](dfx& acc, float m, dfx sc, float M) {
+    if (m == -INFINITY) return;
+    const dfx dm = dfx_two_sum(m, -M);  // exact m - M <= 0
+    const float f = (m == M) ? 1.f : exp2f(__fmaf_rn(dm.hi, c2, __fmul_rn(dm.lo, c2)));
+    acc = dfx_add(acc, f == 1.f ? sc : dfx_mul(sc, dfx{f, 0.f}));
+  };
+  dfx sa{0.f, 0.f}, sb{0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < kHeld; ++h) {
+    add_scaled(sa, cma[h], csa[h], Ma);
+    if (tested) add_scaled(sb, cmb[h], csb[h], Mb);
+  }
+  for (int c = lane + 32 * kHeld; c < p.nchunks; c += 32) {
+    add_scaled(sa, __ldcg(&pp[c].m_a), dfx{__ldcg(&pp[c].sa_hi), __ldcg(&pp[c].sa_lo)}, Ma);
+    if (tested) add_scaled(sb, __ldcg(&pp[c].m_b), dfx{__ldcg(&pp[c].sb_hi), __ldcg(&pp[c].sb_lo)}, Mb);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    Ma = fmax(Ma, __shfl_xor_sync(0xffffffffu, Ma, o));
-    Mb = fmax(Mb, __shfl_xor_sync(0xffffffffu, Mb, o));
-  }
-  sa = (ma == -INFINITY) ? 0.0 : (ma == Ma ? sa : sa * scale(ma - Ma));
-  sb = (mb == -INFINITY) ? 0.0 : (mb == Mb ? sb : sb * scale(mb - Mb));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    sa += __shfl_xor_sync(0xffffffffu, sa, o);
-    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+    sa = dfx_add(sa, dfx{__shfl_xor_sync(0xffffffffu, sa.hi, o), __shfl_xor_sync(0xffffffffu, sa.lo, o)});
+    sb = dfx_add(sb, dfx{__shfl_xor_sync(0xffffffffu, sb.hi, o), __shfl_xor_sync(0xffffffffu, sb.lo, o)});
   }
   if (lane == 0) {
     SlotNorm nm;
-    nm.m_a = (float)Ma;
-    nm.m_b = (float)Mb;
-    nm.s_a = sa;
-    nm.s_b = sb;
+    nm.m_a = Ma;
+    nm.m_b = Mb;
     p.norm[slot] = nm;
     if (tested) {
-      if (d >= 0 && d < p.V) {
-        // p(d)/q(d) = 2^(((l_d - M_a) - (q_d - M_b)) c2) * S_b / S_a
-        const double ratio = (double)exp2f((float)(((ld - Ma) - (qd - Mb)) * c2)) * (sb / sa);
-        rr.ok = (double)ua < ratio;
+      if (in.d >= 0 && in.d < p.V) {
+        // exponent ((l_d - M_a) - (q_d - M_b)) c2 from exact differences
+        const dfx ea = dfx_two_sum(in.ld, -Ma), eb = dfx_two_sum(in.qd, -Mb);
+        const dfx e = dfx_add(ea, dfx{-eb.hi, -eb.lo});
+        const float r = exp2f(__fmaf_rn(e.hi, c2, __fmul_rn(e.lo, c2)));
+        // S_b / S_a: a quotient of the high parts plus one correction step
+        const float q0 = __fdiv_rn(sb.hi, sa.hi);
+        const float q1 = __fdiv_rn(__fadd_rn(__fmaf_rn(-q0, sa.hi, sb.hi), __fmaf_rn(-q0, sa.lo, sb.lo)), sa.hi);
+        rr.ok = in.ua < __fmul_rn(r, __fadd_rn(q0, q1));
       } else {
         report(p.dev_status, SSV_ERR_INVALID);
       }

@@ -19,7 +19,7 @@
 //                stream as programmatic dependents: accept_finish_kernel (one
 //                CTA per sequence) for the decision modes; for rejection
 //                sampling accept_rowmerge_kernel (a warp per slot, all rows
-//                at once) and accept_walk_kernel (a warp per sequence).
+//                at once; the last row of a sequence walks it).
 // The ring keeps 128 to 192 KB of loads in flight per SM; no CTA-wide
 // barrier is taken once the list is built.  Every mbarrier wait is bounded:
 // on timeout the CTA raises SSV_ERR_TIMEOUT, the producer still waits
@@ -249,6 +249,14 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   // the workspace are read only once the preceding kernel has completed.
   pdl_wait();
   pdl_trigger();
+  if (MODE == SSV_ACCEPT_REJECT && blockIdx.x == 0) {
+    // every emission record to "none"; the walks (after this grid) write the
+    // valid sequences' own, so the emission passes can trust the records
+    for (int b = tid; b < p.batch; b += kStrThreads) {
+      p.emit[2 * b] = -1;
+      p.emit[2 * b + 1] = 0;
+    }
+  }
 
   if (warp == kStrProducerWarp) {
     if (lane != 0) return;
@@ -523,32 +531,43 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const Acc
 }
 
 // Completion under rejection sampling, where a row merge also reads the
-// draft token's two logits and forms the normalisers: every verified row of
-// every sequence at once (one warp per slot), then one warp per sequence walks.
-constexpr int kMergeWarps = 16;
+// draft token's two logits and forms the normalisers in fp64: every verified
+// row of every sequence at once, one warp per slot and few warps per CTA (the
+// fp64 pipe of an SM is narrow, so the merges are spread over the SMs); the
+// last merged row of a sequence (an arrival count) walks it.
+constexpr int kMergeWarps = 4;
 
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kMergeWarps * 32) accept_rowmerge_kernel(const AcceptParams p) {
+  __shared__ WalkSmem walk[kMergeWarps];
+  const int warp = threadIdx.x >> 5;
+  const int slot = blockIdx.x * kMergeWarps + warp;
+  // Before the wait: the call's inputs only (the streaming kernel writes none
+  // of them, and it lets this kernel start only after its own wait) -- the
+  // sequence's validity, the row's stage, its draft token and that token's
+  // two logits.
+  int b = -1, off = 0, B = 0, g = 0, need = 0, st = 0;
+  bool mine = false;
+  RowInputs in{-1, 0.f, 0.f, 0.f};
+  if (slot < p.total_slots) {
+    b = find_seq_by_slot(p.slot_off, p.batch, slot);
+    if (b >= 0 && warp_seq_valid(p, b)) {
+      off = p.slot_off[b];
+      B = p.block[b];
+      g = p.gamma[b];
+      need = min(g + 1, B);
+      st = slot < off + B ? p.tau[slot] : 0;
+      mine = st >= 1 && st <= need;
+      if (mine) in = row_inputs<T>(p, slot, st <= g);
+    }
+  }
   pdl_wait();  // every chunk record of the streaming pass
   pdl_trigger();
-  const int slot = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (slot >= p.total_slots) return;
-  const int b = find_seq_by_slot(p.slot_off, p.batch, slot);
-  if (b < 0 || !warp_seq_valid(p, b)) return;
-  const int off = p.slot_off[b], B = p.block[b], g = p.gamma[b];
-  if (slot >= off + B) return;
-  const int st = p.tau[slot];
-  if (st >= 1 && st <= min(g + 1, B)) warp_row_merge<MODE, T>(p, slot, st, g);
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(32) accept_walk_kernel(const AcceptParams p) {
-  __shared__ WalkSmem walk;
-  pdl_wait();  // every row result
-  pdl_trigger();
-  const int b = blockIdx.x;
-  if (!warp_seq_valid(p, b)) return;
-  warp_seq_walk<MODE>(p, b, p.slot_off[b], p.block[b], p.gamma[b], walk, nullptr);
+  if (!mine) return;
+  warp_row_merge<MODE, T>(p, slot, st, g, &in);
+  if (!warp_arrive(&p.cnt_seq[b], 1, need)) return;
+  warp_seq_walk<MODE>(p, b, off, B, g, walk[warp], nullptr);
+  if ((threadIdx.x & 31) == 0 && need != 1) p.cnt_seq[b] = 0;
 }
 
 int device_sm_count() {
@@ -576,10 +595,8 @@ cudaError_t launch_t(const AcceptParams& p, cudaStream_t st) {
   if (e != cudaSuccess || p.batch == 0) return e;
   if (MODE != SSV_ACCEPT_REJECT)
     return launch_pdl(accept_finish_kernel<MODE, T>, dim3(p.batch), dim3(kFinWarps * 32), 0, st, p);
-  e = launch_pdl(accept_rowmerge_kernel<MODE, T>, dim3((p.total_slots + kMergeWarps - 1) / kMergeWarps),
-                 dim3(kMergeWarps * 32), 0, st, p);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(accept_walk_kernel<MODE>, dim3(p.batch), dim3(32), 0, st, p);
+  return launch_pdl(accept_rowmerge_kernel<MODE, T>, dim3((p.total_slots + kMergeWarps - 1) / kMergeWarps),
+                    dim3(kMergeWarps * 32), 0, st, p);
 }
 
 }  // namespace

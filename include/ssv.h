@@ -250,6 +250,10 @@ SSV_API ssv_status ssv_verify_attn(const ssv_attn_args* a, void* workspace, size
  *          tokens[total_slots]: per sequence, the accepted drafts in stage
  *          order then the emitted token, rest -1.
  * V >= 1; T >= 0 (REJECT needs T > 0); 1 <= block <= 64.
+ * Workspace: ssv_accept_workspace bytes.  Under REJECT it includes
+ *   16 * batch * 8192 * ceil(V / 8192) bytes in which the first emission
+ *   pass keeps the double-float exponentials of each sequence's emitted row
+ *   for the second (about 2.4 MB per sequence at V = 151936).
  * Errors: SSV_ERR_INVALID, SSV_ERR_WORKSPACE, SSV_ERR_NOT_FINITE,
  *         SSV_ERR_CUDA; on device SSV_ERR_BAD_TAU.
  * ---------------------------------------------------------------------- */
@@ -322,7 +326,10 @@ SSV_API ssv_status ssv_verify_step(const ssv_rope_args* rope, const ssv_attn_arg
  *  - Same arguments, semantics and results as ssv_accept.
  *  - Calls whose scratch would exceed 4 MiB (roughly total_slots *
  *    ceil(V / 8192) > 120000 chunk records, e.g. more than ~6000 slots at
- *    V = 151936) return SSV_ERR_WORKSPACE and launch nothing.
+ *    V = 151936) return SSV_ERR_WORKSPACE and launch nothing.  Under REJECT
+ *    the stored exponentials of the emitted rows (see ssv_accept) are kept
+ *    only when they fit too; otherwise the second emission pass forms them
+ *    again from the logits, with identical results.
  *  - Calls nothing that allocates: no cudaMalloc/cudaFree, no allocating
  *    library routine.  It clears its arrival counters with a memset on
  *    `stream` at every call.
