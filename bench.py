@@ -138,8 +138,8 @@ KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh", "ss
                   "commit_kernel": ["commit.cu"],
                   "lmhead_accept_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh", "dfloat.cuh"],
                   "lmhead_gather_kernel": ["lmhead.cu", "tc_ptx.cuh", "accept.cuh", "dfloat.cuh"],
-                  "tree_attn_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh"],
-                  "tree_reduce_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh"]}
+                  "tree_attn_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh", "tc_ptx.cuh"],
+                  "tree_reduce_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh", "tc_ptx.cuh"]}
 
 
 def measured_traffic(op: str, workload: str):

@@ -30,6 +30,7 @@
 #include "ssv_internal.cuh"
 #include "accept.cuh"
 #include "attn.cuh"
+#include "tc_ptx.cuh"
 
 #include <limits.h>
 #include <math.h>
@@ -490,10 +491,9 @@ struct TreeAccParams {
   int32_t* dev_status;
   AccPartial* part;  // [total_out][nchunks]
   int vec;           // rows (logits and noise) allow 16-byte loads of 8-entry runs
-  struct RowConf {
-    double conf;     // log-probability of the decision under softmax(l)
+  struct __align__(8) RowConf {
+    float conf;      // log-probability of the decision under softmax(l)
     int dec;         // the decision token, -1 if none
-    int pad;
   }* rowconf;        // [total_out]
 };
 
@@ -522,10 +522,11 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
   }
   const T* lrow = static_cast<const T*>(p.logits) + (size_t)row * p.V;
   const int c0 = chunk * kAccChunk;
+  const bool unit_t = p.T == 1.0f;  // l / 1 is exact
   float best = -INFINITY, mx = -INFINITY;
   int bi = INT_MAX;
   constexpr int kRuns = kAccChunk / kTrThreads / 8;  // runs of 8 consecutive entries per thread
-  float xs[kRuns * 8];
+  float xs[kRuns * 8];  // entries past V hold -inf
 #pragma unroll
   for (int g = 0; g < kRuns; ++g) {
     const int e0 = c0 + 8 * (g * kTrThreads + (int)threadIdx.x);
@@ -556,29 +557,50 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float x = x8[j];
-      if (e0 + j < p.V) {
-        float sc = x;
-        if (MODE == SSV_ACCEPT_GUMBEL) sc = __fadd_rn(__fdiv_rn(x, p.T), n8[j]);
+      xs[g * 8 + j] = x8[j];
+      if (MODE == SSV_ACCEPT_GUMBEL && e0 + j < p.V) {
+        const float sc = __fadd_rn(unit_t ? x8[j] : __fdiv_rn(x8[j], p.T), n8[j]);
         if (sc > best || bi == INT_MAX) { best = sc; bi = e0 + j; }
       }
-      xs[g * 8 + j] = x;
-      mx = fmaxf(mx, x);
     }
   }
-  // chunk max, then the compensated sum of 2^((x - max) c2)
+  // chunk max (3-input max)
+#pragma unroll
+  for (int k = 0; k < kRuns * 8; k += 2) mx = ptx::max3(mx, xs[k], xs[k + 1]);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  float wm = warp_max(mx);
+  const float wm = warp_max(mx);
+  if (MODE != SSV_ACCEPT_GUMBEL) {
+    // greedy: the score is the logit, so the warp's best is its max; only
+    // lanes holding it look for their first entry equal to it (entries in
+    // increasing order; past V never)
+    if (mx == wm) {
+#pragma unroll
+      for (int k = 0; k < kRuns * 8; ++k) {
+        const int e = c0 + 8 * ((k >> 3) * kTrThreads + (int)threadIdx.x) + (k & 7);
+        if (bi == INT_MAX && xs[k] == wm && e < p.V) bi = e;
+      }
+      best = wm;
+    }
+  }
   if (lane == 0) s_m[wid] = wm;
   __syncthreads();
   float cm = s_m[0];
 #pragma unroll
   for (int w2 = 1; w2 < kTrThreads / 32; ++w2) cm = fmaxf(cm, s_m[w2]);
+  // the sum of 2^((x - max) c2): packed f32x2 FMA and add, two chains per thread
   const float nm = (cm == -INFINITY) ? 0.f : -cm * p.c2;
-  float sh = 0.f, sl = 0.f;
+  using namespace ptx;
+  const uint64_t c22 = pack2(p.c2, p.c2), nm2 = pack2(nm, nm);
+  uint64_t acc2 = pack2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < kRuns * 8; ++k) kahan_add(sh, sl, ex2f(fmaf(xs[k], p.c2, nm)));
-  sl = -sl;
+  for (int k = 0; k < kRuns * 8; k += 2) {
+    float y0, y1;
+    unpack2(ffma2(pack2(xs[k], xs[k + 1]), c22, nm2), y0, y1);
+    acc2 = fadd2(acc2, pack2(ex2f(y0), ex2f(y1)));
+  }
+  float sh, sl = 0.f, s1;
+  unpack2(acc2, sh, s1);
+  two_sum_acc(sh, sl, s1, 0.f);
   warp_sum2(sh, sl);
   warp_argmax(best, bi);
   if (lane == 0) { s_h[wid] = sh; s_l[wid] = sl; s_v[wid] = best; s_i[wid] = bi; }
@@ -597,12 +619,18 @@ __global__ void __launch_bounds__(kTrThreads) tree_reduce_kernel(const TreeAccPa
 }
 
 // Every output row's decision and confidence from its chunk records, one
-// thread per row, all rows at once (the walk then only compares them).
+// warp per row (lanes over chunks), all rows at once (the walk then only
+// compares them).  No fp64 (a narrow pipe on this part): the normaliser
+// S = sum of s_c e^(m_c - M) in double-float, each scale factor an fp32 exp2
+// of an argument formed from the exact difference m_c - M.
+constexpr int kConfWarps = 4;
+
 template <int MODE, typename T>
-__global__ void __launch_bounds__(128) tree_rowconf_kernel(const TreeAccParams p) {
+__global__ void __launch_bounds__(kConfWarps * 32) tree_rowconf_kernel(const TreeAccParams p) {
   pdl_wait();  // the chunk records
   pdl_trigger();
-  const int row = blockIdx.x * 128 + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kConfWarps + (threadIdx.x >> 5);
   if (row >= p.total_out) return;
   const int b = find_tree_seq(p.seqs, p.batch, row, [](const ssv_tree_seq& s) { return s.o_off; });
   if (b < 0) return;
@@ -610,29 +638,35 @@ __global__ void __launch_bounds__(128) tree_rowconf_kernel(const TreeAccParams p
   const int li = row - s.o_off - s.new_len;
   if (s.block < 1 || s.block > kTreeMaxB || li < 0 || li >= (s.n_edges + 1) * s.block) return;
   const AccPartial* pr = p.part + (size_t)row * p.nchunks;
-  float v = -INFINITY;
+  float v = -INFINITY, M = -INFINITY;
   int idx = INT_MAX;
-  double M = -INFINITY;
-  for (int c = 0; c < p.nchunks; ++c) {
+  for (int c = lane; c < p.nchunks; c += 32) {
     argmax_combine(v, idx, __ldcg(&pr[c].val), __ldcg(&pr[c].idx));
-    M = fmax(M, (double)__ldcg(&pr[c].m_a));
+    M = fmaxf(M, __ldcg(&pr[c].m_a));
   }
-  const double c2 = (double)p.c2;
-  double S = 0.0;
-  for (int c = 0; c < p.nchunks; ++c) {
-    const double cmx = __ldcg(&pr[c].m_a);
+  warp_argmax(v, idx);
+  M = warp_max(M);
+  dfx S{0.f, 0.f};
+  for (int c = lane; c < p.nchunks; c += 32) {
+    const float cmx = __ldcg(&pr[c].m_a);
     if (cmx == -INFINITY) continue;
-    const double cs = (double)__ldcg(&pr[c].sa_hi) + (double)__ldcg(&pr[c].sa_lo);
-    S += cs * (double)exp2f((float)((cmx - M) * c2));
+    const dfx cs{__ldcg(&pr[c].sa_hi), __ldcg(&pr[c].sa_lo)};
+    const dfx dm = dfx_two_sum(cmx, -M);  // exact m_c - M <= 0
+    const float f = (cmx == M) ? 1.f : exp2f(__fmaf_rn(dm.hi, p.c2, __fmul_rn(dm.lo, p.c2)));
+    S = dfx_add(S, dfx_mul(cs, dfx{f, 0.f}));
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    S = dfx_add(S, dfx{__shfl_xor_sync(0xffffffffu, S.hi, o), __shfl_xor_sync(0xffffffffu, S.lo, o)});
+  if (lane != 0) return;
   TreeAccParams::RowConf rc;
   rc.dec = -1;
   rc.conf = -INFINITY;
-  rc.pad = 0;
   if (idx != INT_MAX) {
-    const double ld = (MODE == SSV_ACCEPT_GUMBEL) ? (double)Elem<T>::to_f32(static_cast<const T*>(p.logits)[(size_t)row * p.V + idx])
-                                                  : (double)v;
-    rc.conf = (ld - M) - log(S);  // S = sum e^(l - M)
+    const float ld = (MODE == SSV_ACCEPT_GUMBEL) ? Elem<T>::to_f32(static_cast<const T*>(p.logits)[(size_t)row * p.V + idx])
+                                                 : v;
+    // (l_d - M) - ln S, S = sum e^(l - M) >= 1; ln(hi + lo) = ln hi + lo / hi to first order
+    rc.conf = __fsub_rn(__fsub_rn(ld, M), __fadd_rn(logf(S.hi), __fdiv_rn(S.lo, S.hi)));
     rc.dec = idx;
   }
   p.rowconf[row] = rc;
@@ -666,7 +700,7 @@ __global__ void __launch_bounds__(32) tree_walk_kernel(const TreeAccParams p) {
     const unsigned long long und = full & ~s_cm[n];
     if (!und) break;
     // each lane: positions lane and lane + 32
-    double best_c = -INFINITY;
+    float best_c = -INFINITY;
     int best_p = INT_MAX, best_t = -1;
 #pragma unroll
     for (int hpos = 0; hpos < 2; ++hpos) {
@@ -675,12 +709,12 @@ __global__ void __launch_bounds__(32) tree_walk_kernel(const TreeAccParams p) {
       const size_t row = (size_t)s.o_off + s.new_len + (size_t)n * s.block + pp;
       const int dec = __ldcg(&p.rowconf[row].dec);
       if (dec < 0) continue;
-      const double conf = __ldcg(&p.rowconf[row].conf);  // log-probability of the decision under softmax(l)
+      const float conf = __ldcg(&p.rowconf[row].conf);  // log-probability of the decision under softmax(l)
       if (conf > best_c || (conf == best_c && pp < best_p)) { best_c = conf; best_p = pp; best_t = dec; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const double oc = __shfl_xor_sync(0xffffffffu, best_c, o);
+      const float oc = __shfl_xor_sync(0xffffffffu, best_c, o);
       const int op = __shfl_xor_sync(0xffffffffu, best_p, o), ot = __shfl_xor_sync(0xffffffffu, best_t, o);
       if (oc > best_c || (oc == best_c && op < best_p)) { best_c = oc; best_p = op; best_t = ot; }
     }
@@ -926,13 +960,13 @@ extern "C" ssv_status ssv_tree_accept(const ssv_tree_accept_args* a, void* ws, s
     e = cudaGetLastError();
   }
   if (e == cudaSuccess && a->total_out > 0) {
-    const dim3 gr((unsigned)((a->total_out + 127) / 128));
+    const dim3 gr((unsigned)((a->total_out + kConfWarps - 1) / kConfWarps)), bl(kConfWarps * 32);
     if (mode == SSV_ACCEPT_GUMBEL)
-      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, __nv_bfloat16>, gr, dim3(128), 0, s, p)
-             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, float>, gr, dim3(128), 0, s, p);
+      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, __nv_bfloat16>, gr, bl, 0, s, p)
+             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_GUMBEL, float>, gr, bl, 0, s, p);
     else
-      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, __nv_bfloat16>, gr, dim3(128), 0, s, p)
-             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, float>, gr, dim3(128), 0, s, p);
+      e = bf ? launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, __nv_bfloat16>, gr, bl, 0, s, p)
+             : launch_pdl(tree_rowconf_kernel<SSV_ACCEPT_ARGMAX, float>, gr, bl, 0, s, p);
   }
   if (e == cudaSuccess) {
     if (mode == SSV_ACCEPT_GUMBEL)

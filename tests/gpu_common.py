@@ -83,9 +83,11 @@ def gpu_accept(x: W.AcceptInputs, dev_status=None, workspace=None):
 # Rejection test u < p(d)/q(d): the device forms the ratio as
 # 2^(((l_d - M_a) - (q_d - M_b)) c2) S_b / S_a with fp32 c2, an fp32-rounded
 # exponent and fp32 exp2, over chunk sums of ex2.approx weights (about 2^-22
-# each) merged in fp64: the log ratio is within |arg| 2^-22 + 2^-19 of the
-# exact one, below 2.5e-5 for |arg| <= 100.  Decisions closer than 1e-4 (log
-# space) to the threshold would be inside that band; the seeded sets have none.
+# each) merged in double-float arithmetic, then the quotient (one correction
+# step) and the product in fp32 (three more roundings of 2^-24): the log
+# ratio is within |arg| 2^-22 + 2^-19 + 2^-22 of the exact one, below 2.6e-5
+# for |arg| <= 100.  Decisions closer than 1e-4 (log space) to the threshold
+# would be inside that band; the seeded sets have none.
 REJECT_MARGIN = 1e-4
 
 # Emitted sample (residual or bonus): the device computes every weight in
