@@ -96,6 +96,40 @@ def test_repeated_calls_share_workspace():
     assert int(ws[:256].sum()) == 0
 
 
+def test_reject_sequence_rejected_after_an_emitting_call():
+    """Rejection sampling, one workspace for two calls: the first emits a token
+    for every sequence; in the second, sequence 1's stage map is not a
+    permutation.  Its emission record from the first call must not be acted
+    on: its outputs stay untouched, SSV_ERR_BAD_TAU is raised, and the other
+    sequences still match the oracle bit for bit."""
+    from diffusion_speculative_verification_gb300 import io as sio
+    import oracle.accept as oacc
+    x = W.make_accept_inputs("stale", W.MODE_REJECT, 1.0, 9000, [8, 8, 4], [6, 7, 3], seed=103)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+    first = gpu_accept(x, workspace=ws)
+    compare_accept(x, first)
+    ref = oacc.accept_batch(x)
+    assert all(int(r.n_out) > int(r.n_acc) for r in ref["results"]), "every sequence should emit; pick another seed"
+    assert ref["results"][1].emit_kind == "residual", "sequence 1 should sample the residual; pick another seed"
+    d = sio.accept_to_device(x)
+    tau = d["tau"].clone()
+    tau[8:16] = torch.tensor([1, 2, 2, 4, 5, 6, 7, 8], dtype=torch.int32)
+    out = (torch.full((3,), -7, dtype=torch.int32, device="cuda"), torch.full((3,), -7, dtype=torch.int32, device="cuda"),
+           torch.full((20,), -7, dtype=torch.int32, device="cuda"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_acc, n_out, tokens = ssv.accept(d["mode"], d["T"], d["logits"], d["draft_tokens"], tau, d["block"], d["gamma"],
+                                      d["slot_off"], draft_logits=d["draft_logits"], u_accept=d["u_accept"],
+                                      u_sample=d["u_sample"], max_block=d["max_block"], dev_status=st,
+                                      workspace=ws, out=out)
+    n_acc, n_out, tokens = n_acc.cpu().numpy(), n_out.cpu().numpy(), tokens.cpu().numpy()
+    assert ssv.get_status(st) == ssv.SSV_ERR_BAD_TAU
+    assert n_acc[1] == -7 and n_out[1] == -7 and np.all(tokens[8:16] == -7)
+    for b, (off, B) in ((0, (0, 8)), (2, (16, 4))):
+        r = ref["results"][b]
+        assert n_acc[b] == r.n_acc and n_out[b] == r.n_out
+        np.testing.assert_array_equal(tokens[off:off + B], first[2][off:off + B])
+
+
 def _accept_with_logits_offset(x: W.AcceptInputs, elem_offset: int, dev_status=None):
     """Runs ssv_accept with the logits (and draft logits) stored `elem_offset`
     elements into a larger buffer, so that rows are not 16-byte aligned."""
