@@ -182,6 +182,16 @@ def test_many_slots_general_kernel():
     compare_accept(x, gpu_accept(x))
 
 
+def test_reject_more_sequences_than_one_emission_list():
+    """Rejection sampling over 2100 sequences (4200 slots, the general reduce):
+    the emission passes list the emitting sequences 2048 at a time, and the
+    emission records are cleared before the walks; every token bit-exact."""
+    blocks = [2] * 2100
+    gammas = [int(g) for g in np.random.default_rng(22).integers(0, 3, size=len(blocks))]
+    x = W.make_accept_inputs("manyrej", W.MODE_REJECT, 1.0, 256, blocks, gammas, seed=22)
+    compare_accept(x, gpu_accept(x))
+
+
 @pytest.mark.parametrize("V", [4096, 4097])
 def test_bad_noise_row_reports_status(V):
     x = W.make_accept_inputs("badnoise", W.MODE_GUMBEL, 1.0, V, [4, 4], [4, 4], seed=13)
