@@ -142,10 +142,45 @@ KERNEL_SOURCES = {"attn_tc_kernel": ["attn_tc.cu", "tc_ptx.cuh", "attn.cuh", "ss
                   "tree_reduce_kernel": ["tree.cu", "accept.cuh", "dfloat.cuh", "tc_ptx.cuh"]}
 
 
+def strip_comments(src: str) -> str:
+    """C/CUDA source without its comments, whitespace runs collapsed (string
+    and character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def code_digest(kern: str) -> str:
+    """First 16 hex digits of the sha256 of a kernel's source files, comments
+    and whitespace left out: an edit of the comments keeps it, any change of
+    the code alters it."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kern]:
+        with open(os.path.join(ROOT, "diffusion_speculative_verification_gb300", "csrc", name)) as f:
+            h.update(strip_comments(f.read()).encode())
+    return h.hexdigest()[:16]
+
+
 def measured_traffic(op: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json),
-    or None when there is none or the kernel source changed since it was taken."""
-    import hashlib
+    or None when there is none or the kernel's code changed since it was taken."""
     kern = KERNEL_OF_OP.get(op)
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if kern is None or not os.path.exists(path):
@@ -154,11 +189,7 @@ def measured_traffic(op: str, workload: str):
         rec = json.load(f).get(f"{kern}_{workload}")
     if not rec:
         return None
-    h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kern]:
-        with open(os.path.join(ROOT, "diffusion_speculative_verification_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest()[:16] != rec.get("source_sha256_16"):
+    if code_digest(kern) != rec.get("source_sha256_16"):
         return None
     return rec["dram_bytes_per_launch"]
 

@@ -531,10 +531,10 @@ __global__ void __launch_bounds__(kFinWarps * 32) accept_finish_kernel(const Acc
 }
 
 // Completion under rejection sampling, where a row merge also reads the
-// draft token's two logits and forms the normalisers in fp64: every verified
-// row of every sequence at once, one warp per slot and few warps per CTA (the
-// fp64 pipe of an SM is narrow, so the merges are spread over the SMs); the
-// last merged row of a sequence (an arrival count) walks it.
+// draft token's two logits and forms the normalisers (double-float): every
+// verified row of every sequence at once, one warp per slot and few warps per
+// CTA, so the merges are spread over the SMs; the last merged row of a
+// sequence (an arrival count) walks it.
 constexpr int kMergeWarps = 4;
 
 template <int MODE, typename T>

@@ -22,11 +22,12 @@
 //
 // ssv_tree_accept: a reduce kernel over (row, vocabulary chunk) records each
 // chunk's decision (first argmax of l or of fl(fl(l/T) + G)) and its
-// max / compensated sum of 2^((l - max) log2 e); a walk kernel (one warp per
-// sequence) merges, at each node of the walk, the rows of its undecided
-// positions -- decision token and confidence l[dec] - logsumexp(l) in fp64 --
-// takes the most confident position (ties: lowest) and follows the edge with
-// that (position, token) (lowest such edge), or emits the transition.
+// max and sum of 2^((l - max) log2 e); a row kernel (one warp per row) forms
+// every row's decision token and confidence l[dec] - logsumexp(l) (the sum
+// in double-float); a walk kernel (one warp per sequence) takes, at each node
+// of the walk, the most confident undecided position (ties: lowest) and
+// follows the edge with that (position, token) (lowest such edge), or emits
+// the transition.
 #include "ssv_internal.cuh"
 #include "accept.cuh"
 #include "attn.cuh"

@@ -48,3 +48,15 @@ def test_accept_bytes_per_mode():
 def test_rope_bytes():
     a = W.make_attn_inputs("t", [1], [2], [3], 4, 2, 64, W.F32, seed=5)
     assert bench.rope_bytes(a) == 2 * 8 * 6 * 64 * 4
+
+
+def test_code_digest_ignores_comments_only():
+    src = "__global__ void k(float* x) {  // scale\n  /* one */ x[0] = 2.f * x[0];\n  const char* s = \"a // b\";\n}\n"
+    same = "// header comment\n__global__ void k(float* x) {\n    x[0] = 2.f * x[0];   // twice\n  const char* s = \"a // b\";\n}"
+    other = src.replace("2.f", "3.f")
+    lit = src.replace("a // b", "a // c")
+    assert bench.strip_comments(src) == bench.strip_comments(same)
+    assert bench.strip_comments(src) != bench.strip_comments(other)
+    assert bench.strip_comments(src) != bench.strip_comments(lit)
+    for kern in bench.KERNEL_SOURCES:
+        assert len(bench.code_digest(kern)) == 16
