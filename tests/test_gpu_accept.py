@@ -192,6 +192,15 @@ def test_reject_more_sequences_than_one_emission_list():
     compare_accept(x, gpu_accept(x))
 
 
+def test_reject_vocabulary_of_74_chunks():
+    """Rejection sampling at V = 600000: 74 vocabulary chunks (the row merge
+    holds 64 per warp and reads the rest again) and 296 emission sub-chunks
+    (the normaliser and locating scans run in three blocks); a residual and
+    two bonus samples, every token bit-exact."""
+    x = W.make_accept_inputs("bigV", W.MODE_REJECT, 1.0, 600000, [4, 3, 2], [3, 3, 1], seed=33)
+    compare_accept(x, gpu_accept(x))
+
+
 @pytest.mark.parametrize("V", [4096, 4097])
 def test_bad_noise_row_reports_status(V):
     x = W.make_accept_inputs("badnoise", W.MODE_GUMBEL, 1.0, V, [4, 4], [4, 4], seed=13)

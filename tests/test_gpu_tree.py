@@ -111,6 +111,10 @@ ACC = {
     "gumbel_T1": dict(mode=W.MODE_GUMBEL, T=1.0, V=5000, cache=[5] * 4, blocks=[8, 16, 4, 12], edges=[10, 25, 3, 14]),
     "argmax_full_vocab": dict(mode=W.MODE_ARGMAX, T=0.0, V=151936, cache=[5] * 2, blocks=[8, 4], edges=[9, 5]),
     "max_tree": dict(mode=W.MODE_ARGMAX, T=0.0, V=300, cache=[5], blocks=[64], edges=[63]),
+    # T != 1: the score divides by T (IEEE division) before the noise is added
+    "gumbel_T07": dict(mode=W.MODE_GUMBEL, T=0.7, V=5000, cache=[5] * 3, blocks=[8, 12, 4], edges=[10, 20, 3]),
+    # 37 vocabulary chunks: a row's confidence merges more chunks than a warp has lanes
+    "argmax_37_chunks": dict(mode=W.MODE_ARGMAX, T=0.0, V=300000, cache=[5] * 2, blocks=[8, 4], edges=[6, 4]),
 }
 
 
