@@ -880,6 +880,7 @@ static int fill_params(const ssv_accept_args* a, char* w, const AccWorkspaceLayo
   p.tokens = a->tokens;
   p.dev_status = a->dev_status;
   p.early = 0;
+  p.unit_ctr = reinterpret_cast<int32_t*>(w + L.unit_ctr);
   p.cnt_seq = reinterpret_cast<int32_t*>(w + L.cnt_seq);
   p.cnt_row = reinterpret_cast<int32_t*>(w + L.cnt_row);
   p.emit = reinterpret_cast<int32_t*>(w + L.emit);
@@ -1037,7 +1038,7 @@ extern "C" ssv_status ssv_accept_noalloc(const ssv_accept_args* a, void* stream)
   st = noalloc_scratch_address(&scratch);
   if (st != SSV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The arrival counters (cnt_seq, cnt_row: the front of the
+  // The arrival counters (unit_ctr, cnt_seq, cnt_row: the front of the
   // layout, up to emit) must start at zero.
   if (cudaMemsetAsync(scratch, 0, L.emit, s) != cudaSuccess) return SSV_ERR_CUDA;
   AcceptParams p;

@@ -76,7 +76,8 @@ struct AcceptParams {
   // kernel, whose outputs overlap none of the batch metadata; the metadata
   // may then be read before it completes (programmatic dependent launch).
   int early;
-  // workspace carve-up (the two counter arrays come first and are contiguous)
+  // workspace carve-up (the counters come first and are contiguous)
+  int32_t* unit_ctr;    // [2]            streaming pass: next unit, producers done
   int32_t* cnt_seq;     // [batch]        merged rows of the sequence
   int32_t* cnt_row;     // [total_slots]  chunks of the row done
   int32_t* emit;        // [batch][2] : emission slot (or -1), 1 = residual / 0 = p
@@ -109,7 +110,7 @@ struct AcceptParams {
 constexpr int kEmitSub = 2048;  // vocabulary entries per emission CTA (256 threads x 8)
 
 struct AccWorkspaceLayout {
-  size_t cnt_seq, cnt_row, emit, part, norm, rowres, enorm, smass, wmass, eexp, total;
+  size_t unit_ctr, cnt_seq, cnt_row, emit, part, norm, rowres, enorm, smass, wmass, eexp, total;
 };
 
 // eexp: room for the emitted rows' stored exponentials (rejection sampling);
@@ -118,6 +119,7 @@ inline AccWorkspaceLayout accept_layout(int batch, int total_slots, int nchunks,
   const size_t nsub = (size_t)nchunks * (kAccChunk / kEmitSub);
   AccWorkspaceLayout L;
   size_t o = 0;
+  L.unit_ctr = o;   o += sizeof(int32_t) * 2;
   L.cnt_seq = o;    o += sizeof(int32_t) * (size_t)batch;
   L.cnt_row = o;    o = align_up(o + sizeof(int32_t) * (size_t)total_slots, 256);
   L.emit = o;       o = align_up(o + sizeof(int32_t) * 2 * (size_t)batch, 256);

@@ -1,8 +1,9 @@
 // accept_stream: the acceptance reduce as one persistent CTA per SM.
 //
 // Each CTA lists the verified rows of the batch in slot order (the same list
-// in every CTA), then takes a contiguous range of the list's (row, chunk)
-// units; a unit is kAccChunk vocabulary entries of the target logits row
+// in every CTA), then takes the list's (row, chunk) units one at a time from
+// a counter in the workspace (the last CTA to finish returns it to zero); a
+// unit is kAccChunk vocabulary entries of the target logits row
 // plus, where the rule needs one, the same entries of the draft logits
 // (rejection sampling, tested stages) or of the noise row (coupled noise
 // from a table; generated noise needs the logits alone).
@@ -66,6 +67,8 @@ struct StrShared {
   uint64_t rec_full[kStrRecRing];
   uint64_t rec_empty[kStrRecRing];
   AccPartial rec[kStrRecRing][kStrConsumerWarps];
+  int unit_of[kStrMaxStages];          // unit held by each ring stage (-1: no units left)
+  int rec_unit[kStrRecRing];           // unit of each record-ring slot (-1: end)
   int32_t list[kStrMaxRows];           // verified slot | tested << 31
   int32_t off[kStrMaxRows];            // slot_off per sequence
   unsigned char blk[kStrMaxRows];      // block (0 when the sizes are invalid)
@@ -220,15 +223,15 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     __syncthreads();
   }
 
-  // ---- this CTA's contiguous range of (row, chunk) units
-  const long long U = (long long)total * p.nchunks;
-  const long long u0 = U * blockIdx.x / gridDim.x;
-  const int n = (int)(U * (blockIdx.x + 1) / gridDim.x - u0);
+  // ---- the list's (row, chunk) units, U of them: each CTA's producer takes
+  // the next one from a counter in the workspace whenever a ring stage frees,
+  // so CTAs that stream faster take more units (a fixed split left the sweep's
+  // CTAs finishing 30 us apart)
+  const int U = total * p.nchunks;
 
-  // Rows of a unit: the logits chunk and, where the rule needs it, the draft
+  // Rows of unit u: the logits chunk and, where the rule needs it, the draft
   // logits or noise chunk (bytes multiples of 16 by construction).
-  auto unit_rows = [&](int k, const void*& a, uint32_t& bytes_a, const void*& b, uint32_t& bytes_b) {
-    const long long u = u0 + k;
+  auto unit_rows = [&](int u, const void*& a, uint32_t& bytes_a, const void*& b, uint32_t& bytes_b) {
     const int e = sh.list[u / p.nchunks];
     const int slot = e & 0x7fffffff;
     const int c0 = (int)(u % p.nchunks) * kAccChunk;
@@ -261,14 +264,24 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
   if (warp == kStrProducerWarp) {
     if (lane != 0) return;
     int issued = 0;
-    for (int k = 0; k < n; ++k) {
+    int next = atomicAdd(p.unit_ctr, 1);  // one unit taken ahead, so the atomic's round trip overlaps the wait
+    for (int k = 0;; ++k) {
       const int s = k % C::kStages;
       if (k >= C::kStages && !mbar_wait(smem_u32(&sh.empty[s]), ((k / C::kStages) - 1) & 1, &sh.abort, p.wait_budget)) break;
+      const uint32_t fb = smem_u32(&sh.full[s]);
+      const int u = next;
+      if (u >= U) {  // no units left: this stage carries the end mark
+        sh.unit_of[s] = -1;
+        mbar_arrive(fb);
+        issued = k + 1;
+        break;
+      }
+      next = atomicAdd(p.unit_ctr, 1);
+      sh.unit_of[s] = u;
       const void *src_a, *src_b;
       uint32_t bytes_a, bytes_b;
-      unit_rows(k, src_a, bytes_a, src_b, bytes_b);
+      unit_rows(u, src_a, bytes_a, src_b, bytes_b);
       const uint32_t dst = smem_u32(ring + (size_t)s * C::kStage);
-      const uint32_t fb = smem_u32(&sh.full[s]);
       if (blockIdx.x == 0 && k == p.fault_skip) {  // test support: this chunk's copy is left out
         issued = k + 1;
         continue;
@@ -283,18 +296,35 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
       const int k_last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
       drain_wait(smem_u32(&sh.full[s]), (k_last / C::kStages) & 1, p.dev_status, p.wait_budget);
     }
+    // the last producer to finish taking units returns the counter to zero
+    __threadfence();
+    if (atomicAdd(p.unit_ctr + 1, 1) == (int)gridDim.x - 1) {
+      p.unit_ctr[0] = 0;
+      p.unit_ctr[1] = 0;
+    }
     if (sh.abort) report(p.dev_status, SSV_ERR_TIMEOUT);
     return;
   }
 
   if (warp < kStrConsumerWarps) {
     const bool unit_t = p.T == 1.0f;  // l / 1 is exact
-    for (int k = 0; k < n; ++k) {
+    for (int k = 0;; ++k) {
       const int s = k % C::kStages;
       const bool got = mbar_wait(smem_u32(&sh.full[s]), (k / C::kStages) & 1, &sh.abort, p.wait_budget);
       if (!__all_sync(0xffffffffu, got)) break;
-      const long long u = u0 + k;
-      const int chunk = (int)(u % p.nchunks);
+      const int u = sh.unit_of[s];
+      if (u < 0) {  // end mark: passed on to the publisher through the record ring
+        const int rs = k % kStrRecRing;
+        const bool room =
+            k < kStrRecRing || mbar_wait(smem_u32(&sh.rec_empty[rs]), ((k / kStrRecRing) - 1) & 1, &sh.abort, p.wait_budget);
+        if (!__all_sync(0xffffffffu, room)) break;
+        if (lane == 0) {
+          if (warp == 0) sh.rec_unit[rs] = -1;
+          mbar_arrive(smem_u32(&sh.rec_full[rs]));
+        }
+        break;
+      }
+      const int chunk = u % p.nchunks;
       const bool tested = sh.list[u / p.nchunks] < 0;
       const int c0 = chunk * kAccChunk;
       const int nvalid = min(kAccChunk, p.V - c0);
@@ -434,6 +464,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
       if (!__all_sync(0xffffffffu, room)) break;
       if (lane == 0) {
         sh.rec[rs][warp] = r;
+        if (warp == 0) sh.rec_unit[rs] = u;
         mbar_arrive(smem_u32(&sh.rec_full[rs]));
       }
     }
@@ -442,10 +473,12 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
 
   // ---- publisher warp: the unit's record; the rows are merged and the
   // sequences walked by the completion kernels once every record is written.
-  for (int k = 0; k < n; ++k) {
+  for (int k = 0;; ++k) {
     const int rs = k % kStrRecRing;
     const bool got = mbar_wait(smem_u32(&sh.rec_full[rs]), (k / kStrRecRing) & 1, &sh.abort, p.wait_budget);
     if (!__all_sync(0xffffffffu, got)) break;
+    const int u = sh.rec_unit[rs];  // read before the slot is released
+    if (u < 0) break;
     AccPartial x;
     if (lane < kStrConsumerWarps) {
       x = sh.rec[rs][lane];
@@ -469,8 +502,7 @@ __global__ void __launch_bounds__(kStrThreads, 1) accept_stream_kernel(const Acc
     } else {
       warp_argmax(x.val, x.idx);
     }
-    const long long u = u0 + k;
-    const int row = (int)(u / p.nchunks), chunk = (int)(u % p.nchunks);
+    const int row = u / p.nchunks, chunk = u % p.nchunks;
     const int slot = sh.list[row] & 0x7fffffff;
     if (lane == 0) p.part[(size_t)slot * p.nchunks + chunk] = x;
   }
