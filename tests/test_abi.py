@@ -111,6 +111,20 @@ def test_accept_validation(L):
     assert L.ssv_accept(C.byref(_acc(batch=0, total_slots=0)), None, 0, None) == ssv.SSV_OK
 
 
+def test_accept_workspace_holds_the_emission_exponentials(L):
+    """Under rejection sampling the workspace adds 16 bytes per vocabulary
+    entry (rounded up to 8192-entry chunks) per sequence, as the header
+    states, for the emitted rows' stored exponentials."""
+    for V, batch in ((1000, 2), (151936, 16), (8193, 3)):
+        g, r = C.c_size_t(0), C.c_size_t(0)
+        kw = dict(V=V, batch=batch, total_slots=4 * batch)
+        assert L.ssv_accept_workspace(C.byref(_acc(**kw)), C.byref(g)) == ssv.SSV_OK
+        rej = _acc(mode=ssv.REJECT, T=1.0, draft_logits=16, u_accept=16, u_sample=16, **kw)
+        assert L.ssv_accept_workspace(C.byref(rej), C.byref(r)) == ssv.SSV_OK
+        stored = 16 * batch * 8192 * ((V + 8191) // 8192)
+        assert stored <= r.value - g.value < stored + 256, (V, batch, r.value - g.value)
+
+
 def test_bench_rejects_unknown_config(L):
     buf = C.create_string_buffer(256)
     assert L.ssv_bench(b"nope", 1, buf, 256) == ssv.SSV_ERR_INVALID
